@@ -1,0 +1,144 @@
+"""Plant plausible slips in the oracle (CPU only) and check that the pins in
+test_oracle_pins.py catch every one of them."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+import tests.test_oracle_pins as P
+
+
+def _topk_ties_reversed(logits, k, renorm=True):
+    l = np.asarray(logits).astype(np.float64)
+    T, E = l.shape
+    eidx = np.broadcast_to(np.arange(E)[::-1], (T, E))  # higher index first on ties
+    order = np.lexsort((eidx, -l), axis=-1)
+    idx = order[:, :k].astype(np.int32)
+    sel = np.take_along_axis(l, idx.astype(np.int64), 1)
+    z = np.exp(sel - sel[:, :1])
+    return idx, z / z.sum(1, keepdims=True)
+
+
+def _topk_weight_sign(logits, k, renorm=True):
+    idx, w = ORIG["topk_gate"](logits, k, renorm)
+    l = np.take_along_axis(np.asarray(logits, np.float64), idx.astype(np.int64), 1)
+    z = np.exp(l[:, :1] - l)  # sign slip
+    return idx, z / z.sum(1, keepdims=True)
+
+
+def _cosel_transposed(a, b, E):
+    return ORIG["coselection"](a, b, E).T
+
+
+def _predict_transposed(self, layer):
+    p, c, n = ORIG["predict"](self, layer)
+    if c is None:
+        return p, c, n
+    return p, c, c @ p
+
+
+def _predict_no_row_norm(self, layer):
+    p, c, n = ORIG["predict"](self, layer)
+    if c is None:
+        return p, c, n
+    Cb = self.window_cosel(layer).astype(np.float64)
+    c2 = Cb / max(Cb.sum(), 1)
+    return p, c2, p @ c2
+
+
+def _replicate_ge(load, total, thresh_num=6, thresh_den=5, max_copies=-1):
+    E = len(load)
+    copies = []
+    for ld in load:
+        c = math.ceil(ld * E / total) - 1 if ld * E * thresh_den >= thresh_num * total else 0
+        copies.append(min(c, max_copies) if max_copies >= 0 else c)
+    return _tables(copies)
+
+
+def _replicate_floor(load, total, thresh_num=6, thresh_den=5, max_copies=-1):
+    E = len(load)
+    copies = []
+    for ld in load:
+        c = (ld * E) // total - 1 if ld * E * thresh_den > thresh_num * total else 0
+        copies.append(min(c, max_copies) if max_copies >= 0 else c)
+    return _tables(copies)
+
+
+def _tables(copies):
+    E = len(copies)
+    rb = np.concatenate([[0], np.cumsum(np.array(copies) + 1)]).astype(np.int32)
+    ge = [e for e, c in enumerate(copies) for _ in range(c + 1)]
+    ge += [-1] * (2 * E - len(ge))
+    return np.array(copies, np.int32), rb, np.array(ge, np.int32)
+
+
+def _dispatch_block_split(idx, E, rep_base=None):
+    idx = np.asarray(idx)
+    A = idx.size
+    if rep_base is None:
+        rep_base = np.arange(E + 1)
+    flat = idx.reshape(-1)
+    groups = []
+    for e in range(E):
+        fs = [f for f in range(A) if flat[f] == e]
+        n_e = int(rep_base[e + 1] - rep_base[e])
+        sz = [len(fs) // n_e + (1 if q < len(fs) % n_e else 0) for q in range(n_e)]
+        p = 0
+        for q in range(n_e):
+            groups.append(fs[p:p + sz[q]])
+            p += sz[q]
+    off = [0]
+    for g in groups:
+        off.append(off[-1] + len(g))
+    off += [A] * (2 * E + 1 - len(off))
+    perm = np.array([f for g in groups for f in g], np.int32)
+    inv = np.empty(A, np.int32)
+    inv[perm] = np.arange(A)
+    return np.array(off, np.int32), perm, inv
+
+
+def _gelu_tanh(z):
+    return 0.5 * z * (1 + np.tanh(math.sqrt(2 / math.pi) * (z + 0.044715 * z ** 3)))
+
+
+def _ffn_drop_up(x_rows, experts, w1, w3, w2, act):
+    return ORIG["expert_ffn_rows"](x_rows, experts, w1, w1 if w3 is not None else None, w2, act)
+
+
+def _combine_rank_swap(y, inv_perm, w):
+    return ORIG["combine"](y, inv_perm, np.asarray(w)[:, ::-1])
+
+
+ORIG = {
+    "topk_gate": O.topk_gate,
+    "coselection": O.coselection,
+    "predict": O.WindowStats.predict,
+    "expert_ffn_rows": O.expert_ffn_rows,
+    "combine": O.combine,
+}
+
+MUTANTS = [
+    ("topk_gate", _topk_ties_reversed, [P.test_topk_brute_force_with_many_ties]),
+    ("topk_gate", _topk_weight_sign, [P.test_topk_hand_cases]),
+    ("coselection", _cosel_transposed, [P.test_coselection_hand_case]),
+    ("WindowStats.predict", _predict_transposed, [P.test_window_hand_case_ring_overwrite]),
+    ("WindowStats.predict", _predict_no_row_norm, [P.test_window_stationary_stream_closed_form]),
+    ("replicate", _replicate_ge, [P.test_replicate_hand_tables]),
+    ("replicate", _replicate_floor, [P.test_replicate_hand_tables]),
+    ("dispatch", _dispatch_block_split, [P.test_dispatch_hand_case]),
+    ("_gelu", _gelu_tanh, [P.test_ffn_closed_form_values]),
+    ("expert_ffn_rows", _ffn_drop_up, [lambda: P.test_ffn_matches_naive_triple_loop("swiglu")]),
+    ("combine", _combine_rank_swap, [P.test_combine_hand_case]),
+]
+
+
+@pytest.mark.parametrize("name,mutant,pins", MUTANTS, ids=[m[1].__name__ for m in MUTANTS])
+def test_pins_catch_planted_slip(monkeypatch, name, mutant, pins):
+    if name.startswith("WindowStats."):
+        monkeypatch.setattr(O.WindowStats, name.split(".")[1], mutant)
+    else:
+        monkeypatch.setattr(O, name, mutant)
+    for pin in pins:
+        with pytest.raises(AssertionError):
+            pin()
