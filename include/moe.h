@@ -1,0 +1,258 @@
+/*
+ * moe.h -- C ABI of the B300 MoE routing-and-expert step (libmoe.so).
+ *
+ * One MoE layer, on one GPU, as seven stream-ordered calls:
+ *
+ *   moe_route         top-k gate over router logits
+ *   moe_stats_update  per-expert histogram + layer j-1 -> j co-selection counts,
+ *                     kept over a sliding window
+ *   moe_predict       window popularity p_seq, conditional probability,
+ *                     predicted next-layer popularity
+ *   moe_replicate     replica counts for hot experts
+ *   moe_dispatch      stable permutation of assignments by expert / replica,
+ *                     and the permuted copy of the token rows
+ *   moe_expert_ffn    grouped expert FFN (GeLU or SwiGLU) on tcgen05 tensor cores
+ *   moe_combine       gate-weighted sum of each token's k expert outputs
+ *
+ * Conventions
+ *   T tokens, E experts, k experts per token, A = T*k assignments (assignment
+ *   f = t*k + r is token t's r-th choice), H hidden size, F expert FFN width.
+ *   Matrices are row-major and contiguous.  bf16 tensors are passed as
+ *   uint16_t bit patterns.  Every pointer is a DEVICE pointer unless the
+ *   argument says "host".  `stream` is a cudaStream_t (NULL = legacy stream).
+ *
+ * Ownership and ordering
+ *   The caller owns every tensor and stream.  The library allocates device
+ *   memory only in moe_stats_create (the window state) and frees it in
+ *   moe_stats_destroy; scratch for moe_dispatch / moe_expert_ffn is passed in
+ *   by the caller (size from moe_workspace_bytes).  Every call only enqueues
+ *   work on `stream` and returns; none synchronises except moe_check,
+ *   moe_stats_export and moe_stats_import.  Calls that share a moe_stats
+ *   handle or a workspace must be ordered on one stream.
+ *
+ * Errors
+ *   Every call returns a moe_status.  Arguments are validated on the host
+ *   before anything is enqueued: MOE_ERR_INVALID for null required pointers,
+ *   out-of-range sizes (T < 0, E < 1 or E > 256, k < 1 or k > min(E, 8),
+ *   H/F not multiples of the stated granule, A = T*k >= 2^31) and misaligned
+ *   pointers; MOE_ERR_WORKSPACE for a workspace smaller than
+ *   moe_workspace_bytes; MOE_ERR_CUDA when a launch fails (message from
+ *   moe_last_error).  Kernels that meet invalid device data (an expert id
+ *   outside [0, E), inconsistent group offsets) or a bounded wait that ran
+ *   out skip the offending work and set a device error word; moe_check
+ *   reports it (MOE_ERR_DEVICE / MOE_ERR_TIMEOUT) and clears it.  No C++
+ *   exception crosses this ABI.  T = 0 is a valid empty batch.
+ *
+ * Source of each operation: the pages that define the method are reviews of
+ * PopFetcher (ATC'25), MoE-GPS, EPS-MoE, MoE-MPMC and "Prediction Is All MoE
+ * Needs"; each entry below names the passage it follows.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID = 1,      /* bad argument (host-side check)                 */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run            */
+    MOE_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed           */
+    MOE_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out (moe_check) */
+    MOE_ERR_WORKSPACE = 5,    /* workspace too small                            */
+    MOE_ERR_DEVICE = 6        /* invalid device data met by a kernel (moe_check) */
+} moe_status;
+
+typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
+
+typedef enum { MOE_OP_DISPATCH = 1, MOE_OP_EXPERT_FFN = 2 } moe_op;
+
+/* Opaque window state: device ring buffers of per-layer histograms and
+ * per-layer-pair co-selection counts, plus running window sums. */
+typedef struct moe_stats moe_stats;
+
+/* ---------------------------------------------------------------------------
+ * moe_stats_create / moe_stats_destroy
+ * PopFetcher review, core method (Routing Information Collector): token
+ * allocation statistics are kept over a sliding window of s iterations
+ * (s = 10 in the paper).
+ *   st      (host) receives the handle
+ *   L       MoE layers (1..1024);  E experts (1..256);  window s (1..1024)
+ *   stream  used to zero the state (the call returns after the zeroing is
+ *           enqueued; the handle is usable by later calls on any stream
+ *           ordered after it)
+ * Device memory: L*s*E*4 + L*E*8 + (L-1)*(s*E*E*4 + E*E*8) bytes + O(E*E).
+ * ------------------------------------------------------------------------- */
+moe_status moe_stats_create(moe_stats** st, int L, int E, int window, void* stream);
+moe_status moe_stats_destroy(moe_stats* st);
+
+/* ---------------------------------------------------------------------------
+ * moe_route -- top-k gate.
+ * PopFetcher review (naive top-k gate) and EPS-MoE review, experiments (top-2
+ * Mixtral, top-4 DBRX, top-6 DeepSeekV2; softmax-renormalised gate weights).
+ *   logits  [T,E] fp32, finite (not checked per element); 16-byte aligned
+ *   idx     [T,k] int32 out: chosen experts by logit descending; equal logits
+ *           (including -0.0 vs +0.0) -> lower expert index first
+ *   w       [T,k] fp32 out: renorm=1: softmax over the k chosen logits;
+ *           renorm=0: full softmax over all E logits, at the chosen experts
+ * ------------------------------------------------------------------------- */
+moe_status moe_route(const float* logits, int T, int E, int k, int renorm,
+                     int32_t* idx, float* w, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_stats_update -- token allocation statistics of one layer.
+ * PopFetcher review, observation 1 (per-expert token counts) and observation
+ * 2 / Fig. 6 (layer-to-layer selection counts behind Pr(E^{h,j+1}|E^{i,j})).
+ *   iter       iteration number (>= 0); the update goes to ring slot iter % s
+ *              and replaces what that slot held for this layer
+ *   layer      j in [0, L)
+ *   idx_layer  [T,k] int32: layer j's routing (from moe_route)
+ *   idx_prev   [T,k] int32: layer j-1's routing of the same tokens; required
+ *              for j > 0 (co-selection counts C_{j-1}[e,e'] = number of
+ *              tokens with e among their layer j-1 choices and e' among
+ *              their layer j choices; all k*k pairs count), NULL for j = 0
+ *   hist_out   [E] int32 out (nullable): this update's histogram h_j
+ * Expert ids outside [0,E) are skipped and flagged (moe_check).
+ * ------------------------------------------------------------------------- */
+moe_status moe_stats_update(moe_stats* st, int64_t iter, int layer,
+                            const int32_t* idx_layer, const int32_t* idx_prev,
+                            int T, int k, int32_t* hist_out, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_predict -- window popularity and next-layer prediction.
+ * PopFetcher review, core method: Eq. (1) sequence popularity p_seq over the
+ * window; Eq. (2)(3) p(E^{j+1}) = sum_e p_seq^j(e) * Pr(e'|e).  MoE-GPS blog
+ * section 2.1: p_i = n_i / N with a sliding-window average.
+ *   layer   j; predicts layer j+1
+ *   p_seq   [E] fp32 out: H_j[e] / sum H_j (window sums; 1/E while empty)
+ *   cond    [E,E] fp32 out (nullable): Cbar_j[e,e'] / sum_e'' Cbar_j[e,e'']
+ *           (1/E for a row with no counts)
+ *   p_next  [E] fp32 out (nullable): sum_e p_seq[e] * cond[e,e']
+ * Computed in fp64.  For j = L-1, cond and p_next must be NULL.
+ * ------------------------------------------------------------------------- */
+moe_status moe_predict(moe_stats* st, int layer, float* p_seq, float* cond,
+                       float* p_next, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_replicate -- replica counts for hot experts.
+ * MoE-GPS blog section 2.1 (duplicate_experts): target = total / E; an
+ * expert whose load exceeds (thresh_num/thresh_den) * target (6/5 = 1.2)
+ * gets ceil(load / target) - 1 extra copies.  MoE-MPMC summary, contribution
+ * 3: a capacity bound caps the copies (max_copies; -1 = none).
+ *   load          [E] int32 (device), e.g. hist_out of moe_stats_update;
+ *                 must be >= 0 and sum to <= total
+ *   total         (host) A = T*k
+ *   copies        [E] int32 out
+ *   rep_base      [E+1] int32 out: exclusive scan of copies+1; rep_base[E]
+ *                 = number of groups G (<= 2E-1 when loads sum to <= total)
+ *   group_expert  [2E] int32 out: expert of group g; -1 for g >= G
+ * Exact integer arithmetic.  Loads that break the precondition set the
+ * device error word and produce the no-replication table.
+ * ------------------------------------------------------------------------- */
+moe_status moe_replicate(const int32_t* load, int E, int64_t total, int thresh_num,
+                         int thresh_den, int max_copies, int32_t* copies,
+                         int32_t* rep_base, int32_t* group_expert, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_dispatch -- stable permutation by expert, then replica.
+ * PopFetcher review, problem statement (token dispatch before the expert
+ * FFN); MoE-MPMC summary (tokens of one expert spread over its physical
+ * replicas).  Expert e's assignments are taken in ascending f; the m-th goes
+ * to replica q = m mod n_e (n_e = rep_base[e+1]-rep_base[e]) at position
+ * floor(m / n_e) of group g = rep_base[e] + q.
+ *   x              [T,H] bf16; may be NULL together with xp (permutation only)
+ *   idx            [T,k] int32 routing
+ *   rep_base       [E+1] int32 from moe_replicate, or NULL (one group per expert)
+ *   group_offsets  [2E+1] int32 out: row offset of each group in xp;
+ *                  entries past the last group equal A
+ *   perm           [A] int32 out: slot -> assignment f
+ *   inv_perm       [A] int32 out: assignment f -> slot
+ *   xp             [A,H] bf16 out: xp[slot] = x[perm[slot] / k] (bit copy)
+ *   workspace      ws_bytes >= moe_workspace_bytes(MOE_OP_DISPATCH, T, k, E, H, 0),
+ *                  16-byte aligned
+ * H must be a multiple of 8; x and xp 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int H, int E,
+                        const int32_t* rep_base, int32_t* group_offsets, int32_t* perm,
+                        int32_t* inv_perm, uint16_t* xp, void* workspace, size_t ws_bytes,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_expert_ffn -- grouped expert FFN over the dispatched rows.
+ * PopFetcher review (MoE-GPT experts: GeLU MLP with F = alpha*H); EPS-MoE
+ * review, "MoE architecture analysis" (gate, up, down GEMMs) and
+ * "GroupGemm vs DenseGemm" (all experts in one grouped kernel, and a
+ * separate path for small per-expert batches).
+ *   xp             [A,H] bf16 dispatched rows
+ *   group_offsets  [G+1] int32, G = 2E when group_expert is given, else E
+ *   group_expert   [G] int32 expert of each group (-1 / empty groups
+ *                  allowed) or NULL (group g = expert g)
+ *   rep_base       [E+1] int32 or NULL: groups of expert e are
+ *                  rep_base[e]..rep_base[e+1]-1; used to pick the kernel
+ *                  path by the expert's total rows, so every replica of an
+ *                  expert takes the same path
+ *   w1, w3         [E,H,F] bf16 (w1 = gate / first projection, w3 = up
+ *                  projection, NULL for GeLU);  w2 [E,F,H] bf16
+ *   act            MOE_ACT_GELU: y = gelu(x w1) w2 (exact erf)
+ *                  MOE_ACT_SWIGLU: y = (silu(x w1) * (x w3)) w2
+ *   small_group_threshold  experts with fewer rows use the small-batch path
+ *                  (0 = never)
+ *   y              [A,H] bf16 out (fp32 accumulation, bf16 intermediate)
+ *   workspace      ws_bytes >= moe_workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F)
+ *                  with T*k = A; 1024-byte aligned
+ * H and F must be multiples of 64; all matrices 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets,
+                          const int32_t* group_expert, const int32_t* rep_base, int E, int A,
+                          const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
+                          int H, int F, moe_act act, int small_group_threshold, uint16_t* y,
+                          void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_combine -- gate-weighted sum of each token's expert outputs.
+ * EPS-MoE review, compute/communication overlap (LocalReduce of expert
+ * outputs); PopFetcher review (result collect).
+ *   out[t] = sum_{r<k} w[t,r] * y[inv_perm[t*k+r]], accumulated in fp32 in
+ *   rank order r = 0..k-1, rounded once to bf16.
+ *   y [A,H] bf16, inv_perm [A] int32, w [T,k] fp32, out [T,H] bf16.
+ * H must be a multiple of 8; y and out 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+moe_status moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* w, int T,
+                       int k, int H, uint16_t* out, void* stream);
+
+/* Workspace bytes for op (MOE_OP_DISPATCH or MOE_OP_EXPERT_FFN); 0 for bad sizes. */
+size_t moe_workspace_bytes(int op, int T, int k, int E, int H, int F);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device: MOE_ERR_TIMEOUT if a bounded wait ran out, MOE_ERR_DEVICE if
+ * a kernel met invalid data, MOE_ERR_CUDA on an asynchronous CUDA error. */
+moe_status moe_check(void* stream);
+
+/* Raw device error word of the current device (bit 0: invalid data, bit 1:
+ * timeout), without clearing it; synchronises the device. */
+moe_status moe_error_word(uint32_t* word_out /* host */);
+
+const char* moe_status_string(moe_status s);
+
+/* Text of the last MOE_ERR_CUDA / MOE_ERR_INVALID raised by this thread. */
+const char* moe_last_error(void);
+
+/* Checkpoint / resume of the window state: moe_stats_bytes gives the size;
+ * export copies ring buffers and window sums into host memory (synchronous,
+ * after all work queued on the legacy stream), import restores them. */
+size_t moe_stats_bytes(const moe_stats* st);
+moe_status moe_stats_export(const moe_stats* st, void* host_buf, size_t bytes);
+moe_status moe_stats_import(moe_stats* st, const void* host_buf, size_t bytes);
+
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

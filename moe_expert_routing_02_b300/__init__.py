@@ -1,0 +1,329 @@
+"""Python binding of libmoe, the B300 MoE routing-and-expert step.
+
+Argument marshalling only: every function here checks tensor placement and
+dtype, passes raw device pointers and the current CUDA stream to the C ABI
+(include/moe.h) and returns the output tensors.  All arithmetic runs in the
+library's CUDA kernels; there is no CPU fallback, and using any function
+without the built library raises.
+
+Functions carry the C names: moe_route, moe_stats_update, moe_predict,
+moe_replicate, moe_dispatch, moe_expert_ffn, moe_combine (plus MoEStats, the
+owner of the sliding-window state, and moe_check).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = [
+    "MoEError", "lib", "library_path", "MoEStats", "moe_route", "moe_stats_update", "moe_predict",
+    "moe_replicate", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_check", "moe_error_word",
+    "workspace_bytes", "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_ACT_GELU", "MOE_ACT_SWIGLU",
+    "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_WORKSPACE, MOE_ERR_DEVICE = range(7)
+MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
+MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN = 1, 2
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes)
+_SIGS = {
+    "moe_stats_create": (_I, [ctypes.POINTER(_P), _I, _I, _I, _P]),
+    "moe_stats_destroy": (_I, [_P]),
+    "moe_route": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_stats_update": (_I, [_P, _I64, _I, _P, _P, _I, _I, _P, _P]),
+    "moe_predict": (_I, [_P, _I, _P, _P, _P, _P]),
+    "moe_replicate": (_I, [_P, _I, _I64, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_ffn": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "moe_check": (_I, [_P]),
+    "moe_error_word": (_I, [ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_last_error": (ctypes.c_char_p, []),
+    "moe_stats_bytes": (_SZ, [_P]),
+    "moe_stats_export": (_I, [_P, _P, _SZ]),
+    "moe_stats_import": (_I, [_P, _P, _SZ]),
+    "moe_version": (ctypes.c_char_p, []),
+}
+EXPORTED_SYMBOLS = tuple(_SIGS)
+
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def lib():
+    """The loaded libmoe (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"libmoe.so is not built ({library_path}); run "
+                               "`python -m moe_expert_routing_02_b300._build`")
+        L = ctypes.CDLL(library_path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        L = lib()
+        raise MoEError(status, f"{what}: {L.moe_status_string(status).decode()}: {L.moe_last_error().decode()}")
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _dev(t, dtype, name, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+    return t
+
+
+def workspace_bytes(op: int, T: int, k: int, E: int, H: int = 64, F: int = 64) -> int:
+    return int(lib().moe_workspace_bytes(op, T, k, E, H, F))
+
+
+# ----------------------------------------------------------------------------
+def moe_route(logits, k: int, renorm: bool = True, idx=None, w=None, stream=None):
+    """Top-k gate: returns (idx [T,k] int32, w [T,k] float32)."""
+    torch = _torch()
+    _dev(logits, torch.float32, "logits", 2)
+    T, E = logits.shape
+    if idx is None:
+        idx = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if w is None:
+        w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _dev(idx, torch.int32, "idx")
+    _dev(w, torch.float32, "w")
+    _check(lib().moe_route(_ptr(logits), T, E, k, int(bool(renorm)), _ptr(idx), _ptr(w), _stream(stream)),
+           "moe_route")
+    return idx, w
+
+
+class MoEStats:
+    """Owner of the device-side sliding-window statistics (moe_stats_*)."""
+
+    def __init__(self, L: int, E: int, window: int = 10, stream=None):
+        self.L, self.E, self.window = L, E, window
+        h = ctypes.c_void_p()
+        _check(lib().moe_stats_create(ctypes.byref(h), L, E, window, _stream(stream)), "moe_stats_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().moe_stats_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def export_state(self) -> bytes:
+        n = int(lib().moe_stats_bytes(self._h))
+        buf = ctypes.create_string_buffer(n)
+        _check(lib().moe_stats_export(self._h, buf, n), "moe_stats_export")
+        return buf.raw
+
+    def import_state(self, data: bytes):
+        buf = ctypes.create_string_buffer(bytes(data), len(data))
+        _check(lib().moe_stats_import(self._h, buf, len(data)), "moe_stats_import")
+
+    def state_arrays(self):
+        """Exported state decoded as NumPy arrays (ring_h, hsum, ring_c, csum)."""
+        import numpy as np
+        raw = self.export_state()
+        hdr = 32
+        L, E, s = self.L, self.E, self.window
+        off = hdr
+        def take(dtype, n):
+            nonlocal off
+            a = np.frombuffer(raw, dtype=dtype, count=n, offset=off)
+            off += a.nbytes
+            return a
+        hsum = take(np.uint64, L * E).reshape(L, E)
+        csum = take(np.uint64, (L - 1) * E * E).reshape(L - 1, E, E)
+        ring_h = take(np.uint32, L * s * E).reshape(L, s, E)
+        ring_c = take(np.uint32, (L - 1) * s * E * E).reshape(L - 1, s, E, E)
+        return ring_h, hsum, ring_c, csum
+
+
+def moe_stats_update(stats: MoEStats, it: int, layer: int, idx_layer, idx_prev=None, hist_out=None, stream=None):
+    """Record one layer's routing; returns hist_out ([E] int32) if given, else None."""
+    torch = _torch()
+    _dev(idx_layer, torch.int32, "idx_layer", 2)
+    T, k = idx_layer.shape
+    if idx_prev is not None:
+        _dev(idx_prev, torch.int32, "idx_prev", 2)
+        if tuple(idx_prev.shape) != (T, k):
+            raise ValueError("idx_prev must match idx_layer's shape")
+    if hist_out is not None:
+        _dev(hist_out, torch.int32, "hist_out")
+    _check(lib().moe_stats_update(stats.handle, int(it), int(layer), _ptr(idx_layer), _ptr(idx_prev), T, k,
+                                  _ptr(hist_out), _stream(stream)), "moe_stats_update")
+    return hist_out
+
+
+def moe_predict(stats: MoEStats, layer: int, want_cond: bool = True, want_next: Optional[bool] = None,
+                device=None, stream=None):
+    """(p_seq [E], cond [E,E] or None, p_next [E] or None), float32."""
+    torch = _torch()
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    E = stats.E
+    last = layer == stats.L - 1
+    if want_next is None:
+        want_next = not last
+    p_seq = torch.empty(E, dtype=torch.float32, device=device)
+    cond = torch.empty((E, E), dtype=torch.float32, device=device) if (want_cond and not last) else None
+    p_next = torch.empty(E, dtype=torch.float32, device=device) if (want_next and not last) else None
+    _check(lib().moe_predict(stats.handle, int(layer), _ptr(p_seq), _ptr(cond), _ptr(p_next), _stream(stream)),
+           "moe_predict")
+    return p_seq, cond, p_next
+
+
+def moe_replicate(load, total: int, thresh=(6, 5), max_copies: int = -1, out=None, stream=None):
+    """(copies [E], rep_base [E+1], group_expert [2E]) int32."""
+    torch = _torch()
+    _dev(load, torch.int32, "load", 1)
+    E = load.shape[0]
+    if out is None:
+        out = (torch.empty(E, dtype=torch.int32, device=load.device),
+               torch.empty(E + 1, dtype=torch.int32, device=load.device),
+               torch.empty(2 * E, dtype=torch.int32, device=load.device))
+    copies, rep_base, group_expert = out
+    _check(lib().moe_replicate(_ptr(load), E, int(total), int(thresh[0]), int(thresh[1]), int(max_copies),
+                               _ptr(copies), _ptr(rep_base), _ptr(group_expert), _stream(stream)), "moe_replicate")
+    return copies, rep_base, group_expert
+
+
+def moe_dispatch(x, idx, E: int, rep_base=None, out=None, workspace=None, stream=None):
+    """(group_offsets [2E+1], perm [A], inv_perm [A], xp [A,H] or None).
+
+    x may be None for the permutation only."""
+    torch = _torch()
+    _dev(idx, torch.int32, "idx", 2)
+    T, k = idx.shape
+    A = T * k
+    dev = idx.device
+    H = 8
+    if x is not None:
+        _dev(x, torch.bfloat16, "x", 2)
+        H = x.shape[1]
+        if x.shape[0] != T:
+            raise ValueError("x and idx disagree on T")
+    if rep_base is not None:
+        _dev(rep_base, torch.int32, "rep_base", 1)
+    if out is None:
+        out = (torch.empty(2 * E + 1, dtype=torch.int32, device=dev),
+               torch.empty(A, dtype=torch.int32, device=dev),
+               torch.empty(A, dtype=torch.int32, device=dev),
+               None if x is None else torch.empty((A, H), dtype=torch.bfloat16, device=dev))
+    go, perm, inv, xp = out
+    need = workspace_bytes(MOE_OP_DISPATCH, T, k, E)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check(lib().moe_dispatch(_ptr(x), _ptr(idx), T, k, H, E, _ptr(rep_base), _ptr(go), _ptr(perm), _ptr(inv),
+                              _ptr(xp), _ptr(workspace), workspace.numel(), _stream(stream)), "moe_dispatch")
+    return go, perm, inv, xp
+
+
+def moe_expert_ffn(xp, group_offsets, group_expert, rep_base, w1, w3, w2, act: str = "gelu",
+                   small_group_threshold: int = 64, y=None, workspace=None, stream=None):
+    """Grouped expert FFN: returns y [A, H] bf16."""
+    torch = _torch()
+    _dev(xp, torch.bfloat16, "xp", 2)
+    _dev(w1, torch.bfloat16, "w1", 3)
+    _dev(w2, torch.bfloat16, "w2", 3)
+    if w3 is not None:
+        _dev(w3, torch.bfloat16, "w3", 3)
+    _dev(group_offsets, torch.int32, "group_offsets", 1)
+    if group_expert is not None:
+        _dev(group_expert, torch.int32, "group_expert", 1)
+    if rep_base is not None:
+        _dev(rep_base, torch.int32, "rep_base", 1)
+    A, H = xp.shape
+    E, H1, F = w1.shape
+    if H1 != H or tuple(w2.shape) != (E, F, H):
+        raise ValueError("weight shapes must be w1/w3 [E,H,F], w2 [E,F,H]")
+    act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
+    if y is None:
+        y = torch.empty((A, H), dtype=torch.bfloat16, device=xp.device)
+    _dev(y, torch.bfloat16, "y", 2)
+    need = int(lib().moe_workspace_bytes(MOE_OP_EXPERT_FFN, A, 1, E, H, F))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=xp.device)
+    _check(lib().moe_expert_ffn(_ptr(xp), _ptr(group_offsets), _ptr(group_expert), _ptr(rep_base), E, A,
+                                _ptr(w1), _ptr(w3), _ptr(w2), H, F, act_id, int(small_group_threshold), _ptr(y),
+                                _ptr(workspace), workspace.numel(), _stream(stream)), "moe_expert_ffn")
+    return y
+
+
+def moe_combine(y, inv_perm, w, out=None, stream=None):
+    """out [T, H] bf16 = sum_r w[t,r] * y[inv_perm[t*k+r]]."""
+    torch = _torch()
+    _dev(y, torch.bfloat16, "y", 2)
+    _dev(inv_perm, torch.int32, "inv_perm", 1)
+    _dev(w, torch.float32, "w", 2)
+    T, k = w.shape
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
+    _dev(out, torch.bfloat16, "out", 2)
+    _check(lib().moe_combine(_ptr(y), _ptr(inv_perm), _ptr(w), T, k, H, _ptr(out), _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_check(stream=None):
+    """Synchronise the stream and raise if a kernel flagged an error."""
+    _check(lib().moe_check(_stream(stream)), "moe_check")
+
+
+def moe_error_word() -> int:
+    w = ctypes.c_uint32(0)
+    _check(lib().moe_error_word(ctypes.byref(w)), "moe_error_word")
+    return int(w.value)

@@ -1,0 +1,97 @@
+// K7: gate-weighted combine of each token's k expert outputs.
+//
+// EPS-MoE review, compute/communication overlap: the LocalReduce of expert
+// outputs is a memory-bound step; PopFetcher review: result collect.
+//   out[t] = sum_{r<k} w[t,r] * y[inv_perm[t*k+r]]
+// One warp per token row; each lane owns 16-byte chunks (8 bf16) and, for
+// each chunk, issues the k gathered row loads before accumulating them in
+// fp32 in rank order r = 0..k-1, rounding once to bf16.  Bound by HBM
+// bandwidth: A*H*2 bytes read, T*H*2 written, plus the small index/weight reads.
+#pragma once
+#include "common.cuh"
+
+namespace combine {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+template <int K>
+__device__ __forceinline__ void combine_row(const uint16_t* __restrict__ y, const long long* slot, const float* wr,
+                                            int H, uint16_t* __restrict__ dst, int lane) {
+  const int chunks = H / 8;
+  for (int c = lane; c < chunks; c += 32) {
+    uint4 v[K];
+#pragma unroll
+    for (int r = 0; r < K; ++r) v[r] = ld_nc_v4(y + slot[r] * H + (size_t)c * 8);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int r = 0; r < K; ++r) {
+      const uint32_t u[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(wr[r], bf16lo(u[i]), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wr[r], bf16hi(u[i]), acc[2 * i + 1]);
+      }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    st_v4(dst + (size_t)c * 8, o);
+  }
+}
+
+template <int K>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __restrict__ y,
+                                                           const int32_t* __restrict__ inv_perm,
+                                                           const float* __restrict__ w, long long T, int H,
+                                                           long long A, uint16_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * kWarps;
+  for (long long t = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5; t < T; t += warps) {
+    long long slot[K];
+    float wr[K];
+    bool ok = true;
+#pragma unroll
+    for (int r = 0; r < K; ++r) {
+      const int32_t s = inv_perm[t * K + r];
+      ok &= (unsigned long long)s < (unsigned long long)A;
+      slot[r] = ok ? s : 0;
+      wr[r] = w[t * K + r];
+    }
+    if (!ok) {  // hole left by invalid routing (flagged upstream)
+      if (lane == 0) moe_flag_error(MOE_DEVERR_DATA);
+      continue;
+    }
+    combine_row<K>(y, slot, wr, H, out + t * H, lane);
+  }
+}
+
+static cudaError_t launch(const uint16_t* y, const int32_t* inv_perm, const float* w, long long T, int k, int H,
+                          uint16_t* out, int num_sms, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  long long blocks = (T + kWarps - 1) / kWarps;
+  const long long cap = (long long)num_sms * 16;
+  if (blocks > cap) blocks = cap;
+  const long long A = T * k;
+  switch (k) {
+#define MOE_COMBINE_CASE(KK) \
+  case KK: combine_kernel<KK><<<(unsigned)blocks, kThreads, 0, st>>>(y, inv_perm, w, T, H, A, out); break;
+    MOE_COMBINE_CASE(1)
+    MOE_COMBINE_CASE(2)
+    MOE_COMBINE_CASE(3)
+    MOE_COMBINE_CASE(4)
+    MOE_COMBINE_CASE(5)
+    MOE_COMBINE_CASE(6)
+    MOE_COMBINE_CASE(7)
+    MOE_COMBINE_CASE(8)
+#undef MOE_COMBINE_CASE
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace combine

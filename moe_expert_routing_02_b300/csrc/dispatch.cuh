@@ -1,0 +1,233 @@
+// K5: stable dispatch by expert, then replica (round-robin), and the
+//     permuted copy of the token rows.
+//
+// PopFetcher (ATC'25) review, problem statement: tokens are dispatched to
+// their experts before the expert FFN and collected afterwards.  MoE-MPMC
+// summary (physical replication): tokens needing the same expert are spread
+// over its distinct physical replicas.
+//
+// Assignment f = t*k + r.  Expert e's assignments, in ascending f, get ranks
+// m = 0, 1, ...; rank m goes to replica q = m mod n_e at position
+// floor(m / n_e) of group g = rep_base[e] + q.  Group sizes follow in closed
+// form: floor(h_e / n_e) + [q < h_e mod n_e], so
+//   slot(e, m) = base_e + q * floor(h_e/n_e) + min(q, h_e mod n_e) + floor(m/n_e)
+// with base_e the exclusive scan of the expert totals h_e.
+//
+// Four launches, all deterministic (no slot depends on atomic order):
+//   count   : per tile of 1024 assignments, per-expert counts (warp-aggregated
+//             shared atomics) -> workspace
+//   scan    : one block; per expert an exclusive scan over tiles (-> each
+//             tile's starting rank), expert totals, group offsets
+//   scatter : per tile, the stable in-tile rank of every assignment
+//             (__match_any_sync rank inside the warp + earlier warps' counts +
+//             earlier rounds' counts) -> slot -> perm / inv_perm
+//   gather  : one warp per slot row, 128-bit loads/stores: xp[slot] = x[perm[slot]/k]
+#pragma once
+#include "common.cuh"
+
+namespace dispatch {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTile = 1024;
+constexpr int kRounds = kTile / kThreads;
+
+// Workspace: counts[ntiles][E] int32, then info[4][E] int32 (base, n, h, unused).
+__host__ __device__ inline long long num_tiles(long long A) { return (A + kTile - 1) / kTile; }
+__host__ inline size_t workspace_bytes(long long A, int E) {
+  const long long nt = num_tiles(A) > 0 ? num_tiles(A) : 1;
+  return (size_t)(nt * E + 4LL * E) * sizeof(int32_t);
+}
+
+__global__ void __launch_bounds__(kThreads) count_kernel(const int32_t* __restrict__ idx, long long A, int E,
+                                                         int32_t* __restrict__ counts) {
+  extern __shared__ int32_t sh_cnt[];
+  for (int i = threadIdx.x; i < E; i += kThreads) sh_cnt[i] = 0;
+  __syncthreads();
+  const long long f0 = (long long)blockIdx.x * kTile;
+  bool bad = false;
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const long long f = f0 + r * kThreads + threadIdx.x;
+    int e = -1;
+    if (f < A) {
+      e = idx[f];
+      if ((unsigned)e >= (unsigned)E) {
+        bad = true;
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&sh_cnt[e], __popc(peers));
+  }
+  if (bad) moe_flag_error(MOE_DEVERR_DATA);
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += kThreads) counts[(size_t)blockIdx.x * E + i] = sh_cnt[i];
+}
+
+__global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ counts, long long ntiles, int E,
+                                                        long long A, const int32_t* __restrict__ rep_base,
+                                                        int32_t* __restrict__ info,
+                                                        int32_t* __restrict__ group_offsets) {
+  __shared__ int32_t warp_tot[kWarps];
+  __shared__ int bad_sh;
+  const int e = threadIdx.x, lane = e & 31, wid = e >> 5;
+  if (e == 0) bad_sh = 0;
+  __syncthreads();
+  int h = 0, n = 1, rb = e;
+  if (e < E) {
+    for (long long b = 0; b < ntiles; ++b) {
+      const int c = counts[b * E + e];
+      counts[b * E + e] = h;
+      h += c;
+    }
+    if (rep_base) {
+      rb = rep_base[e];
+      n = rep_base[e + 1] - rb;
+      if (n < 1 || rb < 0 || (e == 0 && rb != 0) || rep_base[e + 1] > 2 * E) bad_sh = 1;
+    }
+  }
+  __syncthreads();
+  const bool use_rep = rep_base != nullptr && !bad_sh;
+  if (!use_rep) {
+    // invalid replica table: flag it and lay out one group per expert
+    if (rep_base != nullptr && e == 0) moe_flag_error(MOE_DEVERR_DATA);
+    n = 1;
+    rb = e;
+  }
+  // exclusive scan of h over experts
+  int incl = (e < E) ? h : 0;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < wid; ++w) before += warp_tot[w];
+  const int base = before + incl - ((e < E) ? h : 0);
+  if (e < E) {
+    info[e] = base;
+    info[E + e] = n;
+    info[2 * E + e] = h;
+    const int qs = h / n, qr = h % n;
+    for (int q = 0; q < n; ++q) group_offsets[rb + q] = base + q * qs + (q < qr ? q : qr);
+  }
+  // entries past the last group equal A
+  const int ngroups = use_rep ? rep_base[E] : E;
+  for (int g = ngroups + e; g <= 2 * E; g += kThreads) group_offsets[g] = (int32_t)A;
+}
+
+__global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __restrict__ idx, long long A, int E,
+                                                           const int32_t* __restrict__ tile_base,
+                                                           const int32_t* __restrict__ info,
+                                                           int32_t* __restrict__ perm,
+                                                           int32_t* __restrict__ inv_perm) {
+  extern __shared__ int32_t sm[];
+  int32_t* warp_cnt = sm;            // [kWarps][E]
+  int32_t* run = sm + kWarps * E;    // [E]
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  for (int i = tid; i < kWarps * E; i += kThreads) warp_cnt[i] = 0;
+  for (int i = tid; i < E; i += kThreads) run[i] = tile_base[(size_t)blockIdx.x * E + i];
+  __syncthreads();
+  const long long f0 = (long long)blockIdx.x * kTile;
+  for (int r = 0; r < kRounds; ++r) {
+    const long long f = f0 + r * kThreads + tid;
+    int e = -1;
+    if (f < A) {
+      e = idx[f];
+      if ((unsigned)e >= (unsigned)E) e = -1;  // flagged by count_kernel
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) warp_cnt[wid * E + e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int m = run[e] + __popc(peers & lanemask_lt());
+      for (int w = 0; w < wid; ++w) m += warp_cnt[w * E + e];
+      const int base = info[e], n = info[E + e], h = info[2 * E + e];
+      const int q = m % n, pos = m / n, qs = h / n, qr = h % n;
+      const int slot = base + q * qs + (q < qr ? q : qr) + pos;
+      if ((unsigned long long)slot < (unsigned long long)A) {
+        perm[slot] = (int32_t)f;
+        inv_perm[f] = slot;
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < E; i += kThreads) {
+      int s = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        s += warp_cnt[w * E + i];
+        warp_cnt[w * E + i] = 0;
+      }
+      run[i] += s;
+    }
+    __syncthreads();
+  }
+}
+
+// xp[slot, :] = x[perm[slot] / k, :], one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(kThreads) gather_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ perm, long long A, int k,
+                                                          int H, uint16_t* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * kWarps;
+  const int chunks = H / 8;
+  for (long long row = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5; row < A; row += warps) {
+    const int32_t p = perm[row];
+    if ((unsigned long long)p >= (unsigned long long)A) continue;  // hole left by invalid routing
+    const long long t = p / k;
+    const uint16_t* src = x + t * H;
+    uint16_t* dst = xp + row * H;
+    int c = lane;
+    for (; c + 96 < chunks; c += 128) {
+      const uint4 v0 = ld_nc_v4(src + (size_t)c * 8);
+      const uint4 v1 = ld_nc_v4(src + (size_t)(c + 32) * 8);
+      const uint4 v2 = ld_nc_v4(src + (size_t)(c + 64) * 8);
+      const uint4 v3 = ld_nc_v4(src + (size_t)(c + 96) * 8);
+      st_v4(dst + (size_t)c * 8, v0);
+      st_v4(dst + (size_t)(c + 32) * 8, v1);
+      st_v4(dst + (size_t)(c + 64) * 8, v2);
+      st_v4(dst + (size_t)(c + 96) * 8, v3);
+    }
+    for (; c < chunks; c += 32) st_v4(dst + (size_t)c * 8, ld_nc_v4(src + (size_t)c * 8));
+  }
+}
+
+struct Args {
+  const uint16_t* x;
+  const int32_t* idx;
+  long long T;
+  int k, H, E;
+  const int32_t* rep_base;
+  int32_t* group_offsets;
+  int32_t* perm;
+  int32_t* inv_perm;
+  uint16_t* xp;
+  void* ws;
+};
+
+static cudaError_t launch(const Args& a, int num_sms, cudaStream_t st) {
+  const long long A = a.T * a.k;
+  const int E = a.E;
+  if (A == 0) {
+    // empty batch: every offset is 0
+    return cudaMemsetAsync(a.group_offsets, 0, sizeof(int32_t) * (2 * E + 1), st);
+  }
+  const long long nt = num_tiles(A);
+  int32_t* counts = reinterpret_cast<int32_t*>(a.ws);
+  int32_t* info = counts + nt * E;
+  count_kernel<<<(unsigned)nt, kThreads, sizeof(int32_t) * E, st>>>(a.idx, A, E, counts);
+  scan_kernel<<<1, kThreads, 0, st>>>(counts, nt, E, A, a.rep_base, info, a.group_offsets);
+  scatter_kernel<<<(unsigned)nt, kThreads, sizeof(int32_t) * (kWarps + 1) * E, st>>>(a.idx, A, E, counts, info,
+                                                                                      a.perm, a.inv_perm);
+  if (a.x != nullptr) {
+    long long blocks = (A + kWarps - 1) / kWarps;
+    const long long cap = (long long)num_sms * 16;
+    if (blocks > cap) blocks = cap;
+    gather_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(a.x, a.perm, A, a.k, a.H, a.xp);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dispatch

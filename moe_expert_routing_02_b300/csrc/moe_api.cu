@@ -1,0 +1,475 @@
+// libmoe: C ABI of the B300 MoE routing-and-expert step.
+//
+// This file is the only translation unit of the library: it includes every
+// kernel, validates arguments on the host, and enqueues the launches.  The
+// declarations and their contracts are in include/moe.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+#include <string>
+
+#include "../../include/moe.h"
+#include "combine.cuh"
+#include "common.cuh"
+#include "dispatch.cuh"
+#include "ffn.cuh"
+#include "replicate.cuh"
+#include "route.cuh"
+#include "stats.cuh"
+
+#define MOE_VERSION_STRING "moe-b300 0.1 (sm_103a)"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+moe_status fail(moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+moe_status cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return MOE_OK;
+  return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool init = false;
+  int num_sms = 0;
+  bool ffn_attr[3] = {false, false, false};
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+moe_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device id %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_status(e, "cudaDeviceGetAttribute");
+    d.init = true;
+  }
+  *out = &d;
+  return MOE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+moe_status get_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return MOE_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return MOE_OK;
+}
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// box of box_inner x box_outer, 128-byte swizzle, zero fill out of bounds.
+moe_status encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                     uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MOE_OK;
+}
+
+size_t ffn_workspace_bytes(long long A, int F) {
+  // bf16 intermediate [A, F], 1024-byte aligned
+  const size_t inter = (size_t)A * (size_t)F * 2;
+  return ((inter + 1023) / 1024) * 1024 + 1024;
+}
+
+}  // namespace
+
+struct moe_stats {
+  int L, E, s, device;
+  void* block;                       // one allocation for everything below
+  size_t block_bytes;
+  uint32_t* ring_h;                  // [L][s][E]
+  unsigned long long* hsum;          // [L][E]
+  uint32_t* ring_c;                  // [L-1][s][E][E]
+  unsigned long long* csum;          // [L-1][E][E]
+  uint32_t* acc;                     // [E + E*E] (zero between calls)
+  uint32_t* ticket;                  // [1]
+  size_t state_bytes;                // exported bytes (rings + sums), without header
+};
+
+namespace {
+constexpr uint32_t kStatsMagic = 0x53454F4Du;  // "MOES"
+struct StatsHeader {
+  uint32_t magic, version;
+  int32_t L, E, s, pad;
+  uint64_t bytes;
+};
+}  // namespace
+
+extern "C" {
+
+const char* moe_version(void) { return MOE_VERSION_STRING; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_DEVICE: return "invalid device data";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+size_t moe_workspace_bytes(int op, int T, int k, int E, int H, int F) {
+  if (T < 0 || k < 1 || k > 8 || E < 1 || E > 256) return 0;
+  const long long A = (long long)T * k;
+  if (op == MOE_OP_DISPATCH) return dispatch::workspace_bytes(A, E);
+  if (op == MOE_OP_EXPERT_FFN) {
+    if (F < 64 || F % 64 || H < 64 || H % 64) return 0;
+    return ffn_workspace_bytes(A, F);
+  }
+  return 0;
+}
+
+// ------------------------------------------------------------------ stats
+moe_status moe_stats_create(moe_stats** out, int L, int E, int window, void* stream) {
+  if (!out) return fail(MOE_ERR_INVALID, "moe_stats_create: null handle pointer");
+  *out = nullptr;
+  if (L < 1 || L > 1024 || E < 1 || E > 256 || window < 1 || window > 1024)
+    return fail(MOE_ERR_INVALID, "moe_stats_create: need 1<=L<=1024, 1<=E<=256, 1<=window<=1024");
+  moe_stats* st = new (std::nothrow) moe_stats();
+  if (!st) return fail(MOE_ERR_CUDA, "moe_stats_create: host allocation failed");
+  st->L = L;
+  st->E = E;
+  st->s = window;
+  cudaGetDevice(&st->device);
+  const size_t nh = (size_t)L * window * E;
+  const size_t nhs = (size_t)L * E;
+  const size_t nc = (size_t)(L - 1) * window * E * E;
+  const size_t ncs = (size_t)(L - 1) * E * E;
+  const size_t nacc = (size_t)E + (size_t)E * E;
+  // layout: 8-byte sums first, then 4-byte arrays
+  const size_t bytes = (nhs + ncs) * 8 + (nh + nc + nacc + 1) * 4;
+  cudaError_t e = cudaMalloc(&st->block, bytes);
+  if (e != cudaSuccess) {
+    delete st;
+    return cuda_status(e, "moe_stats_create: cudaMalloc");
+  }
+  st->block_bytes = bytes;
+  char* p = static_cast<char*>(st->block);
+  st->hsum = reinterpret_cast<unsigned long long*>(p);
+  p += nhs * 8;
+  st->csum = reinterpret_cast<unsigned long long*>(p);
+  p += ncs * 8;
+  st->ring_h = reinterpret_cast<uint32_t*>(p);
+  p += nh * 4;
+  st->ring_c = reinterpret_cast<uint32_t*>(p);
+  p += nc * 4;
+  st->acc = reinterpret_cast<uint32_t*>(p);
+  p += nacc * 4;
+  st->ticket = reinterpret_cast<uint32_t*>(p);
+  st->state_bytes = (nhs + ncs) * 8 + (nh + nc) * 4;
+  e = cudaMemsetAsync(st->block, 0, bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaFree(st->block);
+    delete st;
+    return cuda_status(e, "moe_stats_create: cudaMemsetAsync");
+  }
+  *out = st;
+  return MOE_OK;
+}
+
+moe_status moe_stats_destroy(moe_stats* st) {
+  if (!st) return MOE_OK;
+  cudaError_t e = cudaFree(st->block);
+  delete st;
+  return cuda_status(e, "moe_stats_destroy: cudaFree");
+}
+
+size_t moe_stats_bytes(const moe_stats* st) { return st ? sizeof(StatsHeader) + st->state_bytes : 0; }
+
+moe_status moe_stats_export(const moe_stats* st, void* host_buf, size_t bytes) {
+  if (!st || !host_buf) return fail(MOE_ERR_INVALID, "moe_stats_export: null argument");
+  if (bytes < moe_stats_bytes(st)) return fail(MOE_ERR_INVALID, "moe_stats_export: buffer too small");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_status(e, "moe_stats_export: sync");
+  StatsHeader h{kStatsMagic, 1u, st->L, st->E, st->s, 0, (uint64_t)st->state_bytes};
+  memcpy(host_buf, &h, sizeof(h));
+  e = cudaMemcpy(static_cast<char*>(host_buf) + sizeof(h), st->block, st->state_bytes, cudaMemcpyDeviceToHost);
+  return cuda_status(e, "moe_stats_export: cudaMemcpy");
+}
+
+moe_status moe_stats_import(moe_stats* st, const void* host_buf, size_t bytes) {
+  if (!st || !host_buf) return fail(MOE_ERR_INVALID, "moe_stats_import: null argument");
+  if (bytes < moe_stats_bytes(st)) return fail(MOE_ERR_INVALID, "moe_stats_import: buffer too small");
+  StatsHeader h;
+  memcpy(&h, host_buf, sizeof(h));
+  if (h.magic != kStatsMagic || h.version != 1u || h.L != st->L || h.E != st->E || h.s != st->s ||
+      h.bytes != st->state_bytes)
+    return fail(MOE_ERR_INVALID, "moe_stats_import: buffer does not match this handle (L, E, window)");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_status(e, "moe_stats_import: sync");
+  e = cudaMemcpy(st->block, static_cast<const char*>(host_buf) + sizeof(h), st->state_bytes, cudaMemcpyHostToDevice);
+  return cuda_status(e, "moe_stats_import: cudaMemcpy");
+}
+
+// ------------------------------------------------------------------ route
+moe_status moe_route(const float* logits, int T, int E, int k, int renorm, int32_t* idx, float* w, void* stream) {
+  if (T < 0 || E < 1 || E > 256 || k < 1 || k > 8 || k > E)
+    return fail(MOE_ERR_INVALID, "moe_route: need T>=0, 1<=E<=256, 1<=k<=min(E,8)");
+  if ((long long)T * k >= (1LL << 31)) return fail(MOE_ERR_INVALID, "moe_route: T*k too large");
+  if (T == 0) return MOE_OK;
+  if (!logits || !idx || !w) return fail(MOE_ERR_INVALID, "moe_route: null pointer");
+  if (!aligned(logits, 16) || !aligned(idx, 4) || !aligned(w, 4))
+    return fail(MOE_ERR_INVALID, "moe_route: logits must be 16-byte aligned, idx/w 4-byte aligned");
+  return cuda_status(route::launch(logits, T, E, k, renorm ? 1 : 0, idx, w, static_cast<cudaStream_t>(stream)),
+                     "moe_route launch");
+}
+
+// ------------------------------------------------------------------ stats update / predict
+moe_status moe_stats_update(moe_stats* st, int64_t iter, int layer, const int32_t* idx_layer,
+                            const int32_t* idx_prev, int T, int k, int32_t* hist_out, void* stream) {
+  if (!st) return fail(MOE_ERR_INVALID, "moe_stats_update: null handle");
+  if (iter < 0 || layer < 0 || layer >= st->L || T < 0 || k < 1 || k > 8 || k > st->E)
+    return fail(MOE_ERR_INVALID, "moe_stats_update: bad iter/layer/T/k");
+  if ((long long)T * k >= (1LL << 31)) return fail(MOE_ERR_INVALID, "moe_stats_update: T*k too large");
+  if (T > 0 && !idx_layer) return fail(MOE_ERR_INVALID, "moe_stats_update: null idx_layer");
+  if (layer > 0 && T > 0 && !idx_prev) return fail(MOE_ERR_INVALID, "moe_stats_update: layer > 0 needs idx_prev");
+  if (layer == 0 && idx_prev) return fail(MOE_ERR_INVALID, "moe_stats_update: idx_prev must be NULL for layer 0");
+  DeviceInfo* d = nullptr;
+  moe_status ms = device_info(&d);
+  if (ms != MOE_OK) return ms;
+  const int E = st->E, s = st->s;
+  const int slot = (int)(iter % s);
+  stats::UpdateArgs a;
+  a.idx_cur = idx_layer;
+  a.idx_prev = layer > 0 ? idx_prev : nullptr;
+  a.has_prev = layer > 0 ? 1 : 0;
+  a.T = T;
+  a.k = k;
+  a.E = E;
+  a.acc_h = st->acc;
+  a.acc_c = st->acc + E;
+  a.ticket = st->ticket;
+  a.ring_h = st->ring_h + ((size_t)layer * s + slot) * E;
+  a.hsum = st->hsum + (size_t)layer * E;
+  a.ring_c = layer > 0 ? st->ring_c + ((size_t)(layer - 1) * s + slot) * E * E : nullptr;
+  a.csum = layer > 0 ? st->csum + (size_t)(layer - 1) * E * E : nullptr;
+  a.hist_out = hist_out;
+  return cuda_status(stats::launch_update(a, d->num_sms, static_cast<cudaStream_t>(stream)),
+                     "moe_stats_update launch");
+}
+
+moe_status moe_predict(moe_stats* st, int layer, float* p_seq, float* cond, float* p_next, void* stream) {
+  if (!st) return fail(MOE_ERR_INVALID, "moe_predict: null handle");
+  if (layer < 0 || layer >= st->L) return fail(MOE_ERR_INVALID, "moe_predict: layer out of range");
+  if (!p_seq) return fail(MOE_ERR_INVALID, "moe_predict: null p_seq");
+  if (layer == st->L - 1 && (cond || p_next))
+    return fail(MOE_ERR_INVALID, "moe_predict: the last layer has no next layer (cond/p_next must be NULL)");
+  const int E = st->E;
+  const unsigned long long* csum = (layer < st->L - 1) ? st->csum + (size_t)layer * E * E : nullptr;
+  stats::predict_kernel<<<1, stats::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      st->hsum + (size_t)layer * E, csum, E, p_seq, cond, p_next);
+  return cuda_status(cudaGetLastError(), "moe_predict launch");
+}
+
+// ------------------------------------------------------------------ replicate
+moe_status moe_replicate(const int32_t* load, int E, int64_t total, int thresh_num, int thresh_den, int max_copies,
+                         int32_t* copies, int32_t* rep_base, int32_t* group_expert, void* stream) {
+  if (E < 1 || E > 256 || total < 0 || total >= (1LL << 31))
+    return fail(MOE_ERR_INVALID, "moe_replicate: need 1<=E<=256, 0<=total<2^31");
+  if (thresh_num < 1 || thresh_den < 1 || thresh_num > 1024 || thresh_den > 1024)
+    return fail(MOE_ERR_INVALID, "moe_replicate: threshold num/den must be in [1, 1024]");
+  if (max_copies < -1) return fail(MOE_ERR_INVALID, "moe_replicate: max_copies must be >= -1");
+  if (!load || !copies || !rep_base || !group_expert) return fail(MOE_ERR_INVALID, "moe_replicate: null pointer");
+  return cuda_status(replicate::launch(load, E, total, thresh_num, thresh_den, max_copies, copies, rep_base,
+                                       group_expert, static_cast<cudaStream_t>(stream)),
+                     "moe_replicate launch");
+}
+
+// ------------------------------------------------------------------ dispatch
+moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int H, int E, const int32_t* rep_base,
+                        int32_t* group_offsets, int32_t* perm, int32_t* inv_perm, uint16_t* xp, void* workspace,
+                        size_t ws_bytes, void* stream) {
+  if (T < 0 || E < 1 || E > 256 || k < 1 || k > 8 || k > E || H < 8 || H % 8)
+    return fail(MOE_ERR_INVALID, "moe_dispatch: need T>=0, 1<=E<=256, 1<=k<=min(E,8), H a positive multiple of 8");
+  if ((long long)T * k >= (1LL << 31)) return fail(MOE_ERR_INVALID, "moe_dispatch: T*k too large");
+  if (!group_offsets) return fail(MOE_ERR_INVALID, "moe_dispatch: null group_offsets");
+  if ((x == nullptr) != (xp == nullptr)) return fail(MOE_ERR_INVALID, "moe_dispatch: x and xp must both be set or both NULL");
+  if (T > 0 && (!idx || !perm || !inv_perm || !workspace)) return fail(MOE_ERR_INVALID, "moe_dispatch: null pointer");
+  if (x && (!aligned(x, 16) || !aligned(xp, 16))) return fail(MOE_ERR_INVALID, "moe_dispatch: x/xp must be 16-byte aligned");
+  if (workspace && !aligned(workspace, 16)) return fail(MOE_ERR_INVALID, "moe_dispatch: workspace must be 16-byte aligned");
+  if (T > 0 && ws_bytes < dispatch::workspace_bytes((long long)T * k, E))
+    return fail(MOE_ERR_WORKSPACE, "moe_dispatch: workspace needs %zu bytes", dispatch::workspace_bytes((long long)T * k, E));
+  DeviceInfo* d = nullptr;
+  moe_status ms = device_info(&d);
+  if (ms != MOE_OK) return ms;
+  dispatch::Args a{x, idx, (long long)T, k, H, E, rep_base, group_offsets, perm, inv_perm, xp, workspace};
+  return cuda_status(dispatch::launch(a, d->num_sms, static_cast<cudaStream_t>(stream)), "moe_dispatch launch");
+}
+
+// ------------------------------------------------------------------ expert FFN
+moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, const int32_t* group_expert,
+                          const int32_t* rep_base, int E, int A, const uint16_t* w1, const uint16_t* w3,
+                          const uint16_t* w2, int H, int F, moe_act act, int small_group_threshold, uint16_t* y,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  (void)rep_base;
+  (void)small_group_threshold;
+  if (E < 1 || E > 256 || A < 0) return fail(MOE_ERR_INVALID, "moe_expert_ffn: need 1<=E<=256, A>=0");
+  if (H < 64 || H % 64 || F < 64 || F % 64) return fail(MOE_ERR_INVALID, "moe_expert_ffn: H and F must be positive multiples of 64");
+  if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) return fail(MOE_ERR_INVALID, "moe_expert_ffn: unknown activation");
+  if (small_group_threshold < 0) return fail(MOE_ERR_INVALID, "moe_expert_ffn: small_group_threshold must be >= 0");
+  if ((long long)E * H >= (1LL << 31) || (long long)E * F >= (1LL << 31))
+    return fail(MOE_ERR_INVALID, "moe_expert_ffn: weights too large");
+  if (A == 0) return MOE_OK;
+  if (!xp || !group_offsets || !w1 || !w2 || !y || !workspace) return fail(MOE_ERR_INVALID, "moe_expert_ffn: null pointer");
+  if (act == MOE_ACT_SWIGLU && !w3) return fail(MOE_ERR_INVALID, "moe_expert_ffn: SwiGLU needs w3");
+  if (!aligned(xp, 16) || !aligned(w1, 16) || !aligned(w2, 16) || !aligned(y, 16) || (w3 && !aligned(w3, 16)))
+    return fail(MOE_ERR_INVALID, "moe_expert_ffn: matrices must be 16-byte aligned");
+  if (!aligned(workspace, 1024)) return fail(MOE_ERR_INVALID, "moe_expert_ffn: workspace must be 1024-byte aligned");
+  if (ws_bytes < ffn_workspace_bytes(A, F))
+    return fail(MOE_ERR_WORKSPACE, "moe_expert_ffn: workspace needs %zu bytes", ffn_workspace_bytes(A, F));
+  const int G = group_expert ? 2 * E : E;
+  const long long tiles_bound = ((long long)(A + ffn::BM - 1) / ffn::BM + G) *
+                                (long long)((act == MOE_ACT_SWIGLU ? (F + 127) / 128 : (F + 255) / 256) +
+                                            (H + 255) / 256);
+  if (tiles_bound >= (1LL << 31)) return fail(MOE_ERR_INVALID, "moe_expert_ffn: problem too large");
+
+  DeviceInfo* d = nullptr;
+  moe_status ms = device_info(&d);
+  if (ms != MOE_OK) return ms;
+  ms = get_encoder();
+  if (ms != MOE_OK) return ms;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint16_t* inter = static_cast<uint16_t*>(workspace);
+
+  CUtensorMap mA1, mW1, mW3, mA2, mW2;
+  if ((ms = encode_2d(&mA1, xp, H, A, 64, ffn::BM)) != MOE_OK) return ms;
+  if ((ms = encode_2d(&mW1, w1, F, (uint64_t)E * H, 64, 64)) != MOE_OK) return ms;
+  if (act == MOE_ACT_SWIGLU) {
+    if ((ms = encode_2d(&mW3, w3, F, (uint64_t)E * H, 64, 64)) != MOE_OK) return ms;
+  } else {
+    mW3 = mW1;
+  }
+  if ((ms = encode_2d(&mA2, inter, F, A, 64, ffn::BM)) != MOE_OK) return ms;
+  if ((ms = encode_2d(&mW2, w2, H, (uint64_t)E * F, 64, 64)) != MOE_OK) return ms;
+
+  const int epi1 = act == MOE_ACT_SWIGLU ? ffn::kSwiglu : ffn::kGelu;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < 3; ++i) {
+      if (d->ffn_attr[i]) continue;
+      const void* fn = i == 0 ? (const void*)ffn::gemm_kernel<ffn::kGelu>
+                     : i == 1 ? (const void*)ffn::gemm_kernel<ffn::kSwiglu>
+                              : (const void*)ffn::gemm_kernel<ffn::kStore>;
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ffn::kSmemBytes);
+      if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: cudaFuncSetAttribute");
+      d->ffn_attr[i] = true;
+    }
+  }
+  ffn::Params p1;
+  p1.group_offsets = group_offsets;
+  p1.group_expert = group_expert;
+  p1.G = G;
+  p1.E = E;
+  p1.A_rows = A;
+  p1.K = H;
+  p1.N_out = F;
+  p1.n_tiles = act == MOE_ACT_SWIGLU ? (F + 127) / 128 : (F + 255) / 256;
+  p1.out = inter;
+  p1.flags = 0;
+  ffn::Params p2 = p1;
+  p2.K = F;
+  p2.N_out = H;
+  p2.n_tiles = (H + 255) / 256;
+  p2.out = y;
+
+  const long long mt_bound = (long long)(A + ffn::BM - 1) / ffn::BM + G;
+  auto grid_for = [&](const ffn::Params& p) {
+    long long g = mt_bound * p.n_tiles;
+    if (g > d->num_sms) g = d->num_sms;
+    return (unsigned)(g < 1 ? 1 : g);
+  };
+  if (epi1 == ffn::kSwiglu)
+    ffn::gemm_kernel<ffn::kSwiglu><<<grid_for(p1), ffn::THREADS, ffn::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
+  else
+    ffn::gemm_kernel<ffn::kGelu><<<grid_for(p1), ffn::THREADS, ffn::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM1 launch");
+  ffn::gemm_kernel<ffn::kStore><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
+  return cuda_status(cudaGetLastError(), "moe_expert_ffn: GEMM2 launch");
+}
+
+// ------------------------------------------------------------------ combine
+moe_status moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* w, int T, int k, int H, uint16_t* out,
+                       void* stream) {
+  if (T < 0 || k < 1 || k > 8 || H < 8 || H % 8)
+    return fail(MOE_ERR_INVALID, "moe_combine: need T>=0, 1<=k<=8, H a positive multiple of 8");
+  if ((long long)T * k >= (1LL << 31)) return fail(MOE_ERR_INVALID, "moe_combine: T*k too large");
+  if (T == 0) return MOE_OK;
+  if (!y || !inv_perm || !w || !out) return fail(MOE_ERR_INVALID, "moe_combine: null pointer");
+  if (!aligned(y, 16) || !aligned(out, 16)) return fail(MOE_ERR_INVALID, "moe_combine: y/out must be 16-byte aligned");
+  DeviceInfo* d = nullptr;
+  moe_status ms = device_info(&d);
+  if (ms != MOE_OK) return ms;
+  return cuda_status(combine::launch(y, inv_perm, w, T, k, H, out, d->num_sms, static_cast<cudaStream_t>(stream)),
+                     "moe_combine launch");
+}
+
+// ------------------------------------------------------------------ errors
+moe_status moe_error_word(uint32_t* word_out) {
+  if (!word_out) return fail(MOE_ERR_INVALID, "moe_error_word: null pointer");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_status(e, "moe_error_word: sync");
+  e = cudaMemcpyFromSymbol(word_out, g_moe_dev_error, sizeof(uint32_t));
+  return cuda_status(e, "moe_error_word: read");
+}
+
+moe_status moe_check(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e, "moe_check: stream sync");
+  uint32_t word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_moe_dev_error, sizeof(uint32_t));
+  if (e != cudaSuccess) return cuda_status(e, "moe_check: read error word");
+  if (word) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_moe_dev_error, &zero, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_status(e, "moe_check: clear error word");
+    if (word & MOE_DEVERR_TIMEOUT) return fail(MOE_ERR_TIMEOUT, "a bounded device wait ran out (word 0x%x)", word);
+    return fail(MOE_ERR_DEVICE, "a kernel met invalid device data (word 0x%x)", word);
+  }
+  e = cudaGetLastError();
+  return cuda_status(e, "moe_check");
+}
+
+}  // extern "C"

@@ -1,0 +1,194 @@
+// K2: per-expert histogram and layer j-1 -> j co-selection counts, written to
+//     the window ring and folded into running window sums.
+// K3: window popularity, conditional probability and next-layer prediction.
+//
+// PopFetcher (ATC'25) review: observation 1 (token allocation per expert),
+// observation 2 / Fig. 6 (inter-layer conditional probability), core method
+// (Routing Information Collector with a sliding window of s iterations;
+// Eq. (1) sequence popularity, Eq. (2)(3) next-layer popularity).  MoE-GPS
+// blog, section 2.1: p_i = n_i / N averaged over a sliding window.
+//
+// K2 is one launch: blocks count into shared memory with warp-aggregated
+// atomics (__match_any_sync: one atomic per distinct bin per warp), flush the
+// non-zero bins to a global accumulator, and the last block to finish (ticket
+// counter after a fence) moves the accumulator into ring slot iter % s,
+// updates the window sums by (new - old) and zeroes the accumulator for the
+// next call.  Counts are integers, so the result does not depend on the
+// order in which atomics land.
+#pragma once
+#include "common.cuh"
+
+namespace stats {
+
+constexpr int kThreads = 256;
+constexpr int kSmemCoselMaxE = 64;  // E*E counters in shared memory up to E = 64
+
+struct UpdateArgs {
+  const int32_t* idx_cur;   // [T,k]
+  const int32_t* idx_prev;  // [T,k] (read only when has_prev and T > 0)
+  int has_prev;             // layer > 0: co-selection counts are kept
+  int T, k, E;
+  uint32_t* acc_h;          // [E]   zero between calls
+  uint32_t* acc_c;          // [E*E] zero between calls
+  uint32_t* ticket;         // zero between calls
+  uint32_t* ring_h;         // slot of layer j   [E]
+  unsigned long long* hsum; // window sum layer j [E]
+  uint32_t* ring_c;         // slot of pair j-1  [E*E] or null
+  unsigned long long* csum; // window sum pair j-1 [E*E] or null
+  int32_t* hist_out;        // [E] or null
+};
+
+__device__ __forceinline__ void agg_add(uint32_t* base, int bin, bool ok) {
+  // Lanes holding the same bin add once, by their lowest lane.
+  const int key = ok ? bin : -1;
+  const unsigned peers = __match_any_sync(0xffffffffu, key);
+  const int leader = __ffs(peers) - 1;
+  if (ok && (int)(threadIdx.x & 31) == leader) atomicAdd(base + bin, (uint32_t)__popc(peers));
+}
+
+__global__ void __launch_bounds__(kThreads) update_kernel(UpdateArgs a) {
+  extern __shared__ uint32_t sh[];
+  const int E = a.E, k = a.k;
+  const bool cos = a.has_prev != 0;
+  const bool cos_smem = cos && E <= kSmemCoselMaxE;
+  uint32_t* sh_h = sh;
+  uint32_t* sh_c = sh + E;
+  const int nsh = E + (cos_smem ? E * E : 0);
+  for (int i = threadIdx.x; i < nsh; i += kThreads) sh[i] = 0;
+  __syncthreads();
+
+  const long long stride = (long long)gridDim.x * kThreads;
+  for (long long base = (long long)blockIdx.x * kThreads; base < a.T; base += stride) {
+    const long long t = base + threadIdx.x;
+    const bool live = t < a.T;
+    int cur[8], prv[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      cur[r] = -1;
+      prv[r] = -1;
+      if (r < k && live) {
+        cur[r] = a.idx_cur[t * k + r];
+        if (cos) prv[r] = a.idx_prev[t * k + r];
+      }
+    }
+    bool bad = false;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (r < k) {
+        const bool okc = live && (unsigned)cur[r] < (unsigned)E;
+        bad |= live && !okc;
+        agg_add(sh_h, cur[r], okc);
+      }
+    }
+    if (cos) {
+#pragma unroll
+      for (int r1 = 0; r1 < 8; ++r1) {
+        if (r1 < k) {
+          const bool okp = live && (unsigned)prv[r1] < (unsigned)E;
+          bad |= live && !okp;
+#pragma unroll
+          for (int r2 = 0; r2 < 8; ++r2) {
+            if (r2 < k) {
+              const bool ok = okp && (unsigned)cur[r2] < (unsigned)E;
+              const int bin = ok ? prv[r1] * E + cur[r2] : 0;
+              if (cos_smem)
+                agg_add(sh_c, bin, ok);
+              else
+                agg_add(a.acc_c, bin, ok);
+            }
+          }
+        }
+      }
+    }
+    if (bad) moe_flag_error(MOE_DEVERR_DATA);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += kThreads)
+    if (sh_h[i]) atomicAdd(a.acc_h + i, sh_h[i]);
+  if (cos_smem)
+    for (int i = threadIdx.x; i < E * E; i += kThreads)
+      if (sh_c[i]) atomicAdd(a.acc_c + i, sh_c[i]);
+
+  // last block folds the totals into the window
+  __shared__ bool is_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < E; i += kThreads) {
+    const uint32_t nw = atomicExch(a.acc_h + i, 0u);
+    const uint32_t old = a.ring_h[i];
+    a.ring_h[i] = nw;
+    a.hsum[i] = a.hsum[i] + nw - old;
+    if (a.hist_out) a.hist_out[i] = (int32_t)nw;
+  }
+  if (cos) {
+    for (int i = threadIdx.x; i < E * E; i += kThreads) {
+      const uint32_t nw = atomicExch(a.acc_c + i, 0u);
+      const uint32_t old = a.ring_c[i];
+      a.ring_c[i] = nw;
+      a.csum[i] = a.csum[i] + nw - old;
+    }
+  }
+  if (threadIdx.x == 0) *a.ticket = 0;
+}
+
+static cudaError_t launch_update(const UpdateArgs& a, int num_sms, cudaStream_t st) {
+  const bool cos_smem = a.has_prev != 0 && a.E <= kSmemCoselMaxE;
+  const size_t smem = sizeof(uint32_t) * (a.E + (cos_smem ? a.E * a.E : 0));
+  long long blocks = ((long long)a.T + kThreads - 1) / kThreads;
+  if (blocks > 2LL * num_sms) blocks = 2LL * num_sms;
+  if (blocks < 1) blocks = 1;
+  update_kernel<<<(int)blocks, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- K3
+// One block.  fp64 throughout; integers converted exactly.
+__global__ void __launch_bounds__(kThreads) predict_kernel(const unsigned long long* __restrict__ hsum,
+                                                           const unsigned long long* __restrict__ csum, int E,
+                                                           float* __restrict__ p_seq, float* __restrict__ cond,
+                                                           float* __restrict__ p_next) {
+  __shared__ double ps[256];
+  __shared__ double rows[256];
+  __shared__ unsigned long long tot_sh;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    unsigned long long tot = 0;
+    for (int e = 0; e < E; ++e) tot += hsum[e];
+    tot_sh = tot;
+  }
+  if (csum && tid < E) {
+    unsigned long long r = 0;
+    for (int e2 = 0; e2 < E; ++e2) r += csum[(size_t)tid * E + e2];
+    rows[tid] = (double)r;
+  }
+  __syncthreads();
+  const unsigned long long tot = tot_sh;
+  if (tid < E) {
+    const double p = tot > 0 ? (double)hsum[tid] / (double)tot : 1.0 / (double)E;
+    ps[tid] = p;
+    p_seq[tid] = (float)p;
+  }
+  __syncthreads();
+  if (!csum) return;
+  if (cond) {
+    for (int i = tid; i < E * E; i += kThreads) {
+      const int e = i / E;
+      const double c = rows[e] > 0 ? (double)csum[i] / rows[e] : 1.0 / (double)E;
+      cond[i] = (float)c;
+    }
+  }
+  if (p_next && tid < E) {
+    double acc = 0.0;
+    for (int e = 0; e < E; ++e) {
+      const double c = rows[e] > 0 ? (double)csum[(size_t)e * E + tid] / rows[e] : 1.0 / (double)E;
+      acc = fma(ps[e], c, acc);
+    }
+    p_next[tid] = (float)acc;
+  }
+}
+
+}  // namespace stats
