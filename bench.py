@@ -1,0 +1,455 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE routing-and-expert step on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+
+Metric: routed tokens/s per MoE layer (T / layer time) on the 12-layer
+MoE-GPT-like routing stream (T=16384 tokens per iteration, E=16 experts,
+top-2, H=1024, F=2048 GeLU experts, bf16 weights/activations, fp32
+accumulate, window s=10).  One step = one iteration of the whole hot path
+over all 12 layers: route, window-statistics update, next-layer prediction,
+replica counts, dispatch, grouped expert FFN, combine (every stage a libmoe
+kernel, launched through the C ABI on one stream).  value = T * L * steps *
+n_gpus / (max over ranks of the timed region).
+
+Inputs are synthetic (seeded Zipf-biased logits with inter-layer correlation,
+N(0,1) activations, N(0,0.02) weights; no dataset or checkpoint exists here)
+and already resident in HBM; every step touches ~1.5 GB of expert weights
+plus ~0.9 GB of activations, far above the 126 MB L2, so no L2 flush is
+needed.  `e2e` repeats the measurement through the same public calls with the
+per-step inputs (X, logits) copied from pinned host memory and the layer
+outputs copied back inside the timed region.
+
+--impl reference times the CPU oracle (NumPy float64, the repository's
+correctness reference) on a bounded sample of the same workload; under
+torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "routed tokens/sec per MoE layer (1xB300) and % of HBM / bf16 tensor roofline"
+UNIT = "tokens/s"
+STAGES = ["route", "stats", "predict", "replicate", "dispatch", "ffn", "combine"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="moe_gpt_stream")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (tokens of one layer)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers (small profiling captures; not a bench line)")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------
+# process group (one rank per GPU; replicas only: ranks share no data)
+# ----------------------------------------------------------------------------
+def dist_init():
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    """Max of a host float over ranks (the timing aggregate; no data exchange)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank: float, world: int, elapsed_max_s: float) -> float:
+    return units_per_rank * world / elapsed_max_s
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            gid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            gid = str(device_index)
+        self.gid = gid
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gid}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                rows.append((float(p[0]), float(p[1]), float(p[2]) if p[2] not in ("[N/A]", "N/A") else 0.0,
+                             p[3], p[4], p[5], p[6], p[7]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        load = [r for r in rows if r[2] > 200.0] or rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in load:
+            for nm, v in zip(names, r[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+# ----------------------------------------------------------------------------
+# workload
+# ----------------------------------------------------------------------------
+def algorithmic_work(c):
+    """Per-layer algorithmic bytes (HBM stages) and flops (FFN), as the method
+    must move them (not what the kernels happen to move)."""
+    T, E, k, H, F, A = c.T, c.E, c.k, c.H, c.F, c.A
+    ngemm = 3 if c.act == "swiglu" else 2
+    return {
+        "route": {"bytes": T * E * 4 + A * 8},
+        "stats": {"bytes": 2 * A * 4 + (E + E * E) * 4 * 2 + (E + E * E) * 8 * 2},
+        "predict": {"bytes": E * E * 8 + E * 8 + E * E * 4 + E * 8},
+        "replicate": {"bytes": E * 16},
+        "dispatch": {"bytes": A * 4 + T * H * 2 + A * H * 2 + 2 * A * 4},
+        "ffn": {"flops": 2 * ngemm * A * H * F,
+                "bytes": ngemm * E * H * F * 2 + A * H * 2 * 2 + (ngemm - 1) * A * F * 2 * 2},
+        "combine": {"bytes": A * H * 2 + A * 8 + T * H * 2},
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def ffn_traffic_per_launch():
+    """DRAM bytes per FFN call from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "ffn_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line:
+            a, b = line.split(":", 1)
+            kv[a.strip()] = b.strip()
+    src = os.path.join(ROOT, "moe_expert_routing_02_b300", "csrc", "ffn.cuh")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if kv.get("ffn_source_sha256_16") != h:
+        return None
+    try:
+        return float(kv["dram_bytes_per_ffn_call_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    from moe_expert_routing_02_b300 import _build
+    _build.build()
+    import moe_expert_routing_02_b300 as M
+    from moe_expert_routing_02_b300 import workloads as W
+    from moe_expert_routing_02_b300.layer import MoELayerStep
+
+    torch.cuda.set_device(local)
+    c = W.config_by_name(args.config)
+    if args.layers:
+        import dataclasses
+        c = dataclasses.replace(c, L=min(args.layers, c.L))
+    dev = torch.device("cuda", local)
+    POOL = 2  # distinct iterations of logits cycled through the steps
+    logits = [[torch.from_numpy(l).to(dev) for l in W.make_layer_logits(c, it)] for it in range(POOL)]
+    xs = [W.make_x(c, 0, j, device=dev) for j in range(c.L)]
+    weights = [W.make_weights(c, j, device=dev) for j in range(c.L)]
+    outs = [torch.empty((c.T, c.H), dtype=torch.bfloat16, device=dev) for _ in range(c.L)]
+    stats = M.MoEStats(c.L, c.E, c.window)
+    step = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, stats=stats, replicate=True, device=dev)
+
+    def run_step(it, ev=None):
+        for j in range(c.L):
+            step.run(it, j, logits[it % POOL][j], xs[j], weights[j], outs[j],
+                     events=None if ev is None else ev[j])
+
+    for it in range(args.warmup):
+        run_step(it)
+    torch.cuda.synchronize()
+    M.moe_check()
+
+    K = args.steps
+    stage_ev = [[{s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for s in STAGES} for _ in range(c.L)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0.record()
+    for s in range(K):
+        run_step(args.warmup + s, stage_ev[s])
+    t1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    M.moe_check()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    elapsed_max = max_over_ranks(elapsed)
+    units = c.T * c.L * K
+    value = whole_job_value(units, world, elapsed_max)
+
+    # per-stage mean duration per layer call
+    work = algorithmic_work(c)
+    peaks = load_peaks()
+    stage_ms = {}
+    for sname in STAGES:
+        ts = [stage_ev[s][j][sname][0].elapsed_time(stage_ev[s][j][sname][1]) for s in range(K) for j in range(c.L)
+              if not (sname == "predict" and j == c.L - 1)]
+        if ts:
+            stage_ms[sname] = sum(ts) / len(ts)
+    stages = {}
+    for sname in STAGES:
+        if sname not in stage_ms:
+            continue
+        t = stage_ms[sname] / 1e3
+        d = {"us_per_layer": round(stage_ms[sname] * 1e3, 2)}
+        if "flops" in work[sname]:
+            d["tflops"] = round(work[sname]["flops"] / t / 1e12, 1)
+            d["frac_bf16_sustained"] = round(work[sname]["flops"] / t / 1e12 / peaks["bf16_tflops_sustained"], 3)
+        d["gbs"] = round(work[sname]["bytes"] / t / 1e9, 1)
+        d["frac_hbm"] = round(work[sname]["bytes"] / t / 1e9 / peaks["hbm_gbs"], 3)
+        stages[sname] = d
+    ffn_t = stage_ms["ffn"] / 1e3
+    achieved = work["ffn"]["flops"] / ffn_t / 1e12
+    roofline = {"bound": "tensor", "kernel": "moe_expert_ffn (GEMM1+GEMM2 launches)", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                "peak_source": f"bf16_tflops_sustained of {peaks['source']} peaks (kernel timed inside a long step)",
+                "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": ffn_traffic_per_launch(),
+                "algorithmic_flops_per_call": work["ffn"]["flops"],
+                "algorithmic_bytes_per_call": work["ffn"]["bytes"]}
+
+    launches = K * sum(step.launches(j, c.L) for j in range(c.L))
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_max / K * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": c.name, "T": c.T, "L": c.L, "E": c.E, "k": c.k, "H": c.H, "F": c.F, "act": c.act,
+                   "window": c.window, "replication": "on (layer's own histogram)",
+                   "parallelism": f"replicas x{world} (no data exchange)",
+                   "l2": "no flush: each step streams ~1.5 GB of weights + activations, >> 126 MB L2"},
+        "roofline": roofline, "stages": stages, "gpu_launches": launches, "clocks": clk,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, c, step, logits, weights, dev, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = run_cpu_baseline(c, args.cpu_tokens or c.T)
+    return result
+
+
+def run_e2e(args, c, step, logits, weights, dev, world):
+    """Same metric through the same calls, per-step inputs from pinned host
+    memory and the per-layer outputs back to pinned host memory, all inside
+    the timed region (one stream, copies and kernels serialised)."""
+    import torch
+    h_logits = [[l.cpu().pin_memory() for l in it] for it in logits]
+    h_x = [torch.empty((c.T, c.H), dtype=torch.bfloat16).pin_memory() for _ in range(c.L)]
+    for j in range(c.L):
+        h_x[j].copy_(torch.randn((c.T, c.H), dtype=torch.float32).to(torch.bfloat16))
+    h_out = [torch.empty((c.T, c.H), dtype=torch.bfloat16).pin_memory() for _ in range(c.L)]
+    d_logits = torch.empty((c.T, c.E), dtype=torch.float32, device=dev)
+    d_x = torch.empty((c.T, c.H), dtype=torch.bfloat16, device=dev)
+    d_out = torch.empty((c.T, c.H), dtype=torch.bfloat16, device=dev)
+
+    def run_step(it):
+        for j in range(c.L):
+            d_logits.copy_(h_logits[it % len(h_logits)][j], non_blocking=True)
+            d_x.copy_(h_x[j], non_blocking=True)
+            step.run(it, j, d_logits, d_x, weights[j], d_out)
+            h_out[j].copy_(d_out, non_blocking=True)
+
+    base = 10_000
+    for it in range(args.warmup):
+        run_step(base + it)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        run_step(base + args.warmup + s)
+    torch.cuda.synchronize()
+    el = max_over_ranks(time.perf_counter() - t0)
+    h2d = c.L * (c.T * c.E * 4 + c.T * c.H * 2)
+    d2h = c.L * c.T * c.H * 2
+    return {"value": round(whole_job_value(c.T * c.L * args.steps, world, el), 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(el / args.steps * 1e3, 3)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (the baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+def oracle_layer_sample(c, T_s, it=0, seed_layer=0, cache={}):
+    """One layer of the workload for the first T_s tokens, every stage in the
+    oracle: top-k, histogram + window update + prediction, replica counts,
+    dispatch, expert FFN of every assignment, combine.  Returns seconds."""
+    import numpy as np
+    from moe_expert_routing_02_b300 import workloads as W
+    from oracle import moe_oracle as O
+    key = (c.name, T_s)
+    if key not in cache:
+        lg = W.make_layer_logits(c, it, T=T_s, layers=min(2, c.L))
+        x = W.bf16_bits(W.make_x(c, it, seed_layer, T=T_s))
+        w1, w3, w2 = (None if t is None else W.bf16_bits(t) for t in W.make_weights(c, seed_layer))
+        cache.clear()
+        cache[key] = (lg, x, w1, w3, w2)
+    lg, x, w1, w3, w2 = cache[key]
+    t0 = time.perf_counter()
+    st = O.WindowStats(len(lg), c.E, c.window)
+    prev = None
+    for j, l in enumerate(lg):  # layer j-1's routing feeds layer j's co-selection counts
+        idx, w = O.topk_gate(l, c.k)
+        st.update(it, j, idx, prev)
+        prev = idx
+    h = O.histogram(idx, c.E)
+    st.predict(0)
+    rep = O.replicate(h, idx.size)
+    go, perm, inv = O.dispatch(idx, c.E, rep[1])
+    xp = O.gather_rows(x, perm, c.k)
+    y = O.expert_ffn(xp, go, rep[2], w1, w3, w2, c.act)
+    O.combine(y, inv, w)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_cpu_baseline(c, T_s, reps=3):
+    # warm once (input generation, imports), then time `reps` layer samples
+    oracle_layer_sample(c, T_s)
+    t = sum(oracle_layer_sample(c, T_s) for _ in range(reps))
+    return {"value": round(reps * T_s / t, 1), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{reps} x one layer of {c.name} with {T_s} of {c.T} tokens (all k={c.k} assignments "
+                      f"through route, stats+predict over 2 layers' routing, replicate, dispatch, fp64 FFN, "
+                      f"combine), {t:.2f} s total; NumPy BLAS threads on {cpu_cores()} host cores"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from moe_expert_routing_02_b300 import workloads as W
+    c = W.config_by_name(args.config)
+    T_s = args.cpu_tokens or 4096
+    for _ in range(max(args.warmup, 1)):
+        oracle_layer_sample(c, T_s)
+    ts = [oracle_layer_sample(c, T_s) for _ in range(args.steps)]
+    total = sum(ts)
+    value = T_s * args.steps / total
+    return {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": c.name, "T": c.T, "L": c.L, "E": c.E, "k": c.k, "H": c.H, "F": c.F,
+                       "act": c.act, "sample_tokens_per_step": T_s},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"each step: one layer of {c.name} for {T_s} tokens, every stage in the "
+                                       f"float64 NumPy oracle"},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+    rank, world, local = dist_init()
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    try:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -203,7 +203,7 @@ moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int
  *                  (0 = never)
  *   y              [A,H] bf16 out (fp32 accumulation, bf16 intermediate)
  *   workspace      ws_bytes >= moe_workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F)
- *                  with T*k = A; 1024-byte aligned
+ *                  with T*k = A; 16-byte aligned
  * H and F must be multiples of 64; all matrices 16-byte aligned.
  * ------------------------------------------------------------------------- */
 moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets,

@@ -210,17 +210,27 @@ def moe_stats_update(stats: MoEStats, it: int, layer: int, idx_layer, idx_prev=N
 
 
 def moe_predict(stats: MoEStats, layer: int, want_cond: bool = True, want_next: Optional[bool] = None,
-                device=None, stream=None):
-    """(p_seq [E], cond [E,E] or None, p_next [E] or None), float32."""
+                device=None, out=None, stream=None):
+    """(p_seq [E], cond [E,E] or None, p_next [E] or None), float32.
+
+    `out` = (p_seq, cond or None, p_next or None) preallocated outputs."""
     torch = _torch()
-    device = device or torch.device("cuda", torch.cuda.current_device())
     E = stats.E
     last = layer == stats.L - 1
-    if want_next is None:
-        want_next = not last
-    p_seq = torch.empty(E, dtype=torch.float32, device=device)
-    cond = torch.empty((E, E), dtype=torch.float32, device=device) if (want_cond and not last) else None
-    p_next = torch.empty(E, dtype=torch.float32, device=device) if (want_next and not last) else None
+    if out is None:
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        if want_next is None:
+            want_next = not last
+        p_seq = torch.empty(E, dtype=torch.float32, device=device)
+        cond = torch.empty((E, E), dtype=torch.float32, device=device) if (want_cond and not last) else None
+        p_next = torch.empty(E, dtype=torch.float32, device=device) if (want_next and not last) else None
+    else:
+        p_seq, cond, p_next = out
+        _dev(p_seq, torch.float32, "p_seq")
+        if cond is not None:
+            _dev(cond, torch.float32, "cond")
+        if p_next is not None:
+            _dev(p_next, torch.float32, "p_next")
     _check(lib().moe_predict(stats.handle, int(layer), _ptr(p_seq), _ptr(cond), _ptr(p_next), _stream(stream)),
            "moe_predict")
     return p_seq, cond, p_next

@@ -356,7 +356,7 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
   if (act == MOE_ACT_SWIGLU && !w3) return fail(MOE_ERR_INVALID, "moe_expert_ffn: SwiGLU needs w3");
   if (!aligned(xp, 16) || !aligned(w1, 16) || !aligned(w2, 16) || !aligned(y, 16) || (w3 && !aligned(w3, 16)))
     return fail(MOE_ERR_INVALID, "moe_expert_ffn: matrices must be 16-byte aligned");
-  if (!aligned(workspace, 1024)) return fail(MOE_ERR_INVALID, "moe_expert_ffn: workspace must be 1024-byte aligned");
+  if (!aligned(workspace, 16)) return fail(MOE_ERR_INVALID, "moe_expert_ffn: workspace must be 16-byte aligned");
   if (ws_bytes < ffn_workspace_bytes(A, F))
     return fail(MOE_ERR_WORKSPACE, "moe_expert_ffn: workspace needs %zu bytes", ffn_workspace_bytes(A, F));
   const int G = group_expert ? 2 * E : E;

@@ -1,0 +1,110 @@
+"""One MoE layer step over the seven C-ABI calls, with preallocated buffers.
+
+route -> stats update -> predict (next layer) -> replicate -> dispatch ->
+grouped expert FFN -> combine, all enqueued on the current CUDA stream with
+no host synchronisation.  This is orchestration only; every step is a libmoe
+kernel.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MoEStats, moe_combine, moe_dispatch, moe_expert_ffn,
+               moe_predict, moe_replicate, moe_route, moe_stats_update, workspace_bytes)
+
+__all__ = ["MoELayerStep"]
+
+
+class MoELayerStep:
+    """Buffers for layers of one shape (T, E, k, H, F, act); call `run` per layer.
+
+    replicate=True feeds the replica table of the layer's own histogram into
+    dispatch and the FFN (hot experts split into replica groups; the output is
+    unchanged).  stats (MoEStats) is shared by all layers of a model."""
+
+    def __init__(self, T: int, E: int, k: int, H: int, F: int, act: str, stats: Optional[MoEStats] = None,
+                 replicate: bool = True, thresh=(6, 5), max_copies: int = -1, renorm: bool = True,
+                 small_group_threshold: int = 64, device="cuda"):
+        self.T, self.E, self.k, self.H, self.F, self.act = T, E, k, H, F, act
+        self.A = T * k
+        self.stats = stats
+        self.replicate = replicate
+        self.thresh, self.max_copies, self.renorm = thresh, max_copies, renorm
+        self.small = small_group_threshold
+        d = torch.device(device)
+        i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
+        A = self.A
+        self.idx = [torch.empty((T, k), dtype=i32, device=d) for _ in range(2)]  # ping-pong: prev layer kept
+        self.w = torch.empty((T, k), dtype=f32, device=d)
+        self.hist = torch.empty(E, dtype=i32, device=d)
+        self.p_seq = torch.empty(E, dtype=f32, device=d)
+        self.cond = torch.empty((E, E), dtype=f32, device=d)
+        self.p_next = torch.empty(E, dtype=f32, device=d)
+        self.copies = torch.empty(E, dtype=i32, device=d)
+        self.rep_base = torch.empty(E + 1, dtype=i32, device=d)
+        self.group_expert = torch.empty(2 * E, dtype=i32, device=d)
+        self.go = torch.empty(2 * E + 1, dtype=i32, device=d)
+        self.perm = torch.empty(A, dtype=i32, device=d)
+        self.inv = torch.empty(A, dtype=i32, device=d)
+        self.xp = torch.empty((A, H), dtype=bf, device=d)
+        self.y = torch.empty((A, H), dtype=bf, device=d)
+        self.ws_dispatch = torch.empty(max(workspace_bytes(MOE_OP_DISPATCH, T, k, E), 16), dtype=torch.uint8, device=d)
+        self.ws_ffn = torch.empty(max(workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F), 1024), dtype=torch.uint8,
+                                  device=d)
+        self._cur = 0
+        # launches per call of run(): route, stats, [predict], replicate, dispatch x4, ffn x2, combine
+        self.kernels_per_layer = {"route": 1, "stats": 1, "predict": 1, "replicate": 1, "dispatch": 4, "ffn": 2,
+                                  "combine": 1}
+
+    def run(self, it: int, layer: int, logits, x, weights, out, events=None, predict: bool = True):
+        """Enqueue one layer.  weights = (w1, w3 or None, w2).  `events`, if
+        given, is a dict stage -> (start, end) torch.cuda.Event recorded
+        around each stage on the current stream."""
+        def mark(stage, i):
+            if events is not None and stage in events:
+                events[stage][i].record()
+
+        prev = self.idx[self._cur ^ 1] if layer > 0 else None
+        idx = self.idx[self._cur]
+        mark("route", 0)
+        moe_route(logits, self.k, self.renorm, idx=idx, w=self.w)
+        mark("route", 1)
+        if self.stats is not None:
+            mark("stats", 0)
+            moe_stats_update(self.stats, it, layer, idx, prev, hist_out=self.hist)
+            mark("stats", 1)
+            if predict and layer < self.stats.L - 1:
+                mark("predict", 0)
+                moe_predict(self.stats, layer, out=(self.p_seq, self.cond, self.p_next))
+                mark("predict", 1)
+        rb = ge = None
+        if self.replicate:
+            mark("replicate", 0)
+            moe_replicate(self.hist, self.A, self.thresh, self.max_copies,
+                          out=(self.copies, self.rep_base, self.group_expert))
+            mark("replicate", 1)
+            rb, ge = self.rep_base, self.group_expert
+        mark("dispatch", 0)
+        moe_dispatch(x, idx, self.E, rb, out=(self.go, self.perm, self.inv, self.xp), workspace=self.ws_dispatch)
+        mark("dispatch", 1)
+        w1, w3, w2 = weights
+        mark("ffn", 0)
+        moe_expert_ffn(self.xp, self.go, ge, rb, w1, w3, w2, self.act, self.small, y=self.y, workspace=self.ws_ffn)
+        mark("ffn", 1)
+        mark("combine", 0)
+        moe_combine(self.y, self.inv, self.w, out=out)
+        mark("combine", 1)
+        self._cur ^= 1
+        return out
+
+    def launches(self, layer: int, L: int) -> int:
+        n = 1 + 1 + 4 + 2 + 1
+        if self.stats is not None:
+            n += 1
+            if layer < L - 1:
+                n += 1
+        if self.replicate:
+            n += 1
+        return n

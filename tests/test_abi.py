@@ -103,8 +103,8 @@ def test_dispatch_ffn_combine_reject_bad_arguments(L):
     assert f(*a) == inv                                   # unknown activation
     a = list(args); a[11] = M.MOE_ACT_SWIGLU
     assert f(*a) == inv                                   # SwiGLU without w3
-    a = list(args); a[14] = P(0x10400 + 256)
-    assert f(*a) == inv                                   # workspace not 1 KB aligned
+    a = list(args); a[14] = P(0x10400 + 8)
+    assert f(*a) == inv                                   # workspace not 16-byte aligned
     a = list(args); a[15] = 1000
     assert f(*a) == M.MOE_ERR_WORKSPACE
     a = list(args); a[12] = -1
