@@ -224,6 +224,36 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets,
 moe_status moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* w, int T,
                        int k, int H, uint16_t* out, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * moe_dispatch_noalloc -- moe_dispatch without a caller-provided workspace.
+ * The paper has no counterpart to this call.  It is for callers that cannot
+ * allocate device memory at dispatch time: a host framework that owns all
+ * device memory and forbids plug-ins from allocating, code enqueueing work
+ * while a stream is being captured, or a latency-critical thread that must
+ * not call cudaMalloc (it can synchronise the device).  The caller still
+ * passes the inputs and outputs exactly as for moe_dispatch (same meaning,
+ * layout and results); the scratch is a file-scope device array of
+ * MOE_DISPATCH_NOALLOC_SCRATCH_BYTES (1 MiB) that every GPU loading the
+ * library holds until the process exits.
+ *   Limit   T*k assignments over E experts must need at most 1 MiB of
+ *           scratch (moe_workspace_bytes(MOE_OP_DISPATCH, ...) <= 1 MiB:
+ *           about 16.7M assignments at E = 16, 1.04M at E = 256); larger
+ *           requests return MOE_ERR_WORKSPACE and enqueue nothing.
+ *   Set-up  the first call on a device (with that device current) looks up
+ *           the array's device address once; make that first call before
+ *           any stream capture.
+ *   Sharing every call on a device uses the same array, which keeps the last
+ *           call's contents (each call writes every word it reads, so nothing
+ *           needs clearing).  Calls whose work overlaps on the GPU (different
+ *           streams, or different host threads) race on the array: order
+ *           them on one stream.
+ * Calls no cudaMalloc / cudaFree and no allocating library routine.
+ * ------------------------------------------------------------------------- */
+#define MOE_DISPATCH_NOALLOC_SCRATCH_BYTES (1u << 20)
+moe_status moe_dispatch_noalloc(const uint16_t* x, const int32_t* idx, int T, int k, int H, int E,
+                                const int32_t* rep_base, int32_t* group_offsets, int32_t* perm,
+                                int32_t* inv_perm, uint16_t* xp, void* stream);
+
 /* Workspace bytes for op (MOE_OP_DISPATCH or MOE_OP_EXPERT_FFN); 0 for bad sizes. */
 size_t moe_workspace_bytes(int op, int T, int k, int E, int H, int F);
 

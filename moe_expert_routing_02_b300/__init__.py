@@ -18,7 +18,7 @@ from typing import Optional
 
 __all__ = [
     "MoEError", "lib", "library_path", "MoEStats", "moe_route", "moe_stats_update", "moe_predict",
-    "moe_replicate", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_check", "moe_error_word",
+    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_check", "moe_error_word",
     "workspace_bytes", "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_ACT_GELU", "MOE_ACT_SWIGLU",
     "EXPORTED_SYMBOLS",
 ]
@@ -44,6 +44,7 @@ _SIGS = {
     "moe_predict": (_I, [_P, _I, _P, _P, _P, _P]),
     "moe_replicate": (_I, [_P, _I, _I64, _I, _I, _I, _P, _P, _P, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_dispatch_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
@@ -279,6 +280,32 @@ def moe_dispatch(x, idx, E: int, rep_base=None, out=None, workspace=None, stream
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     _check(lib().moe_dispatch(_ptr(x), _ptr(idx), T, k, H, E, _ptr(rep_base), _ptr(go), _ptr(perm), _ptr(inv),
                               _ptr(xp), _ptr(workspace), workspace.numel(), _stream(stream)), "moe_dispatch")
+    return go, perm, inv, xp
+
+
+def moe_dispatch_noalloc(x, idx, E: int, rep_base=None, out=None, stream=None):
+    """moe_dispatch with the library's static per-device scratch instead of a
+    workspace (for callers that cannot allocate).  `out` = (group_offsets,
+    perm, inv_perm, xp or None), allocated here when not given."""
+    torch = _torch()
+    _dev(idx, torch.int32, "idx", 2)
+    T, k = idx.shape
+    A = T * k
+    dev = idx.device
+    H = 8
+    if x is not None:
+        _dev(x, torch.bfloat16, "x", 2)
+        H = x.shape[1]
+    if rep_base is not None:
+        _dev(rep_base, torch.int32, "rep_base", 1)
+    if out is None:
+        out = (torch.empty(2 * E + 1, dtype=torch.int32, device=dev),
+               torch.empty(A, dtype=torch.int32, device=dev),
+               torch.empty(A, dtype=torch.int32, device=dev),
+               None if x is None else torch.empty((A, H), dtype=torch.bfloat16, device=dev))
+    go, perm, inv, xp = out
+    _check(lib().moe_dispatch_noalloc(_ptr(x), _ptr(idx), T, k, H, E, _ptr(rep_base), _ptr(go), _ptr(perm),
+                                      _ptr(inv), _ptr(xp), _stream(stream)), "moe_dispatch_noalloc")
     return go, perm, inv, xp
 
 

@@ -473,3 +473,7 @@ moe_status moe_check(void* stream) {
 }
 
 }  // extern "C"
+
+// moe_dispatch_noalloc lives in its own file and is compiled into this
+// translation unit.
+#include "dispatch_noalloc.cu"
