@@ -254,6 +254,23 @@ moe_status moe_dispatch_noalloc(const uint16_t* x, const int32_t* idx, int T, in
                                 const int32_t* rep_base, int32_t* group_offsets, int32_t* perm,
                                 int32_t* inv_perm, uint16_t* xp, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Library options (process-wide, host side; no device work).
+ *   MOE_OPT_FFN_KERNEL  which grouped-GEMM kernel moe_expert_ffn launches:
+ *     MOE_FFN_KERNEL_AUTO   (default) the CTA-pair kernel (tcgen05
+ *                           cta_group::2, 256-row tiles over two SMs) when the
+ *                           experts average >= 256 rows (A >= 256*E), else the
+ *                           single-CTA kernel (128-row tiles).  The choice
+ *                           depends only on (A, E).
+ *     MOE_FFN_KERNEL_SINGLE / MOE_FFN_KERNEL_PAIR  force one kernel.
+ * Unknown options or values return MOE_ERR_INVALID.  Not thread-safe against
+ * concurrent moe_expert_ffn calls.
+ * ------------------------------------------------------------------------- */
+typedef enum { MOE_OPT_FFN_KERNEL = 1 } moe_option;
+typedef enum { MOE_FFN_KERNEL_AUTO = 0, MOE_FFN_KERNEL_SINGLE = 1, MOE_FFN_KERNEL_PAIR = 2 } moe_ffn_kernel;
+moe_status moe_set_option(int option, int value);
+moe_status moe_get_option(int option, int* value /* host */);
+
 /* Workspace bytes for op (MOE_OP_DISPATCH or MOE_OP_EXPERT_FFN); 0 for bad sizes. */
 size_t moe_workspace_bytes(int op, int T, int k, int E, int H, int F);
 

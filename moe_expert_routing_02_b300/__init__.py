@@ -20,7 +20,8 @@ __all__ = [
     "MoEError", "lib", "library_path", "MoEStats", "moe_route", "moe_stats_update", "moe_predict",
     "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_check", "moe_error_word",
     "workspace_bytes", "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_ACT_GELU", "MOE_ACT_SWIGLU",
-    "EXPORTED_SYMBOLS",
+    "EXPORTED_SYMBOLS", "moe_set_option", "moe_get_option", "MOE_OPT_FFN_KERNEL", "MOE_FFN_KERNEL_AUTO",
+    "MOE_FFN_KERNEL_SINGLE", "MOE_FFN_KERNEL_PAIR",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -29,6 +30,8 @@ library_path = os.path.join(_HERE, "libmoe.so")
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_WORKSPACE, MOE_ERR_DEVICE = range(7)
 MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
 MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN = 1, 2
+MOE_OPT_FFN_KERNEL = 1
+MOE_FFN_KERNEL_AUTO, MOE_FFN_KERNEL_SINGLE, MOE_FFN_KERNEL_PAIR = 0, 1, 2
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -56,6 +59,8 @@ _SIGS = {
     "moe_stats_export": (_I, [_P, _P, _SZ]),
     "moe_stats_import": (_I, [_P, _P, _SZ]),
     "moe_version": (ctypes.c_char_p, []),
+    "moe_set_option": (_I, [_I, _I]),
+    "moe_get_option": (_I, [_I, ctypes.POINTER(_I)]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -353,6 +358,16 @@ def moe_combine(y, inv_perm, w, out=None, stream=None):
     _dev(out, torch.bfloat16, "out", 2)
     _check(lib().moe_combine(_ptr(y), _ptr(inv_perm), _ptr(w), T, k, H, _ptr(out), _stream(stream)), "moe_combine")
     return out
+
+
+def moe_set_option(option: int, value: int):
+    _check(lib().moe_set_option(int(option), int(value)), "moe_set_option")
+
+
+def moe_get_option(option: int) -> int:
+    v = ctypes.c_int(0)
+    _check(lib().moe_get_option(int(option), ctypes.byref(v)), "moe_get_option")
+    return int(v.value)
 
 
 def moe_check(stream=None):

@@ -31,6 +31,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTile = 1024;
 constexpr int kRounds = kTile / kThreads;
+constexpr int kScanChunk = 8192;  // int32 counts staged per pass of the scan
 
 // Workspace: counts[ntiles][E] int32, then info[4][E] int32 (base, n, h, unused).
 __host__ __device__ inline long long num_tiles(long long A) { return (A + kTile - 1) / kTile; }
@@ -74,13 +75,28 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(int32_t* __restrict__ co
   const int e = threadIdx.x, lane = e & 31, wid = e >> 5;
   if (e == 0) bad_sh = 0;
   __syncthreads();
+  // per-expert exclusive scan over tiles, staged through shared memory in
+  // chunks (coalesced loads; the serial walk runs on shared memory)
+  __shared__ int32_t chunk[kScanChunk];
   int h = 0, n = 1, rb = e;
-  if (e < E) {
-    for (long long b = 0; b < ntiles; ++b) {
-      const int c = counts[b * E + e];
-      counts[b * E + e] = h;
-      h += c;
+  const long long per = kScanChunk / E;  // tiles per chunk
+  for (long long b0 = 0; b0 < ntiles; b0 += per) {
+    const long long nb = (ntiles - b0 < per) ? (ntiles - b0) : per;
+    const long long cnt = nb * E;
+    for (long long i = e; i < cnt; i += kThreads) chunk[i] = counts[b0 * E + i];
+    __syncthreads();
+    if (e < E) {
+      for (long long b = 0; b < nb; ++b) {
+        const int c = chunk[b * E + e];
+        chunk[b * E + e] = h;
+        h += c;
+      }
     }
+    __syncthreads();
+    for (long long i = e; i < cnt; i += kThreads) counts[b0 * E + i] = chunk[i];
+    __syncthreads();
+  }
+  if (e < E) {
     if (rep_base) {
       rb = rep_base[e];
       n = rep_base[e + 1] - rb;

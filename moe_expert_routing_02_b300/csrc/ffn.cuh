@@ -15,7 +15,7 @@
 // (group, n-tile, m-tile) itself, m fastest so that CTAs running at the same
 // time share the expert's weight tile in L2.  CTA c takes tiles c, c+grid, ...
 //
-// Per CTA (one per SM, 320 threads):
+// Per CTA (one per SM, 576 threads):
 //   warp 0      TMA producer: A tile 128x64 (K-major) and B tile 64x256
 //               (weights as stored, N contiguous = MN-major), 128-byte
 //               swizzle, into a 4-stage ring guarded by full/empty mbarriers.
@@ -24,10 +24,13 @@
 //               TMEM) and tcgen05.commit frees each smem stage; two TMEM
 //               accumulators (2 x 256 columns) let the epilogue of one tile
 //               overlap the main loop of the next.
-//   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//               lanes 32*(w%4).., half the columns each), activation in
-//               fp32, bf16 rounding, row-masked stores (rows past the
+//   warps 2..17 epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4).., a quarter of the columns each), activation
+//               in fp32, bf16 rounding, row-masked stores (rows past the
 //               group's end belong to another group and are not written).
+//               Four warps per SM sub-partition keep the issue slots busy:
+//               GeLU's epilogue costs about as many instructions per tile as
+//               the main loop has cycles when H = 1024.
 // For SwiGLU the B tile holds 128 columns of W1 then the same 128 columns of
 // W3, so one N=256 MMA yields gate and up side by side in TMEM.
 //
@@ -37,6 +40,7 @@
 // the copies it issued, the MMA thread for its MMAs, and TMEM is freed before
 // the CTA exits.
 #pragma once
+#include <cstddef>
 #include "common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -44,14 +48,26 @@ namespace ffn {
 
 using namespace sm100;
 
+#ifndef MOE_FFN_BN
+#define MOE_FFN_BN 256
+#endif
+#ifndef MOE_FFN_STAGES
+#define MOE_FFN_STAGES 4
+#endif
+#ifndef MOE_FFN_EPI_WARPS
+#define MOE_FFN_EPI_WARPS 16
+#endif
 constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BN = MOE_FFN_BN;          // MMA N: 256 (or 128)
 constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int STAGES = MOE_FFN_STAGES;
 constexpr int A_BYTES = BM * BK * 2;      // 16 KB
 constexpr int B_BOX_BYTES = 64 * BK * 2;  // 8 KB: 64 columns x 64 k-rows
 constexpr int B_BYTES = BN * BK * 2;      // 32 KB
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = MOE_FFN_EPI_WARPS;
+constexpr int B_BOXES = BN / 64;       // 64-column TMA boxes per B stage
+static_assert(BN % 128 == 0 && BN <= 256, "BN must be 128 or 256");
+constexpr int EPI_SLICES = EPI_WARPS / 4;  // column slices per TMEM lane quarter
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr int MAX_G = 512;
 constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -88,9 +104,12 @@ struct Smem {
   int32_t tstart[MAX_G + 1];
   int32_t mt[MAX_G];
   int32_t ex[MAX_G];
+  alignas(128) uint8_t stg[EPI_WARPS][1024];  // per-warp output staging (store_rows32; 16-byte accesses)
 };
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory beyond the 227 KB per-block opt-in limit");
+static_assert(offsetof(Smem, stg) % 128 == 0 && offsetof(Smem, b) % 1024 == 0, "staging / stage buffers misaligned");
 
 // Wait for the phase of `bar` with parity `parity`.  Returns false when another
 // role of this CTA aborted (unless ignore_abort) or after the time budget, in
@@ -135,7 +154,30 @@ __device__ __forceinline__ Tile decode(const Smem& s, int G, int tile) {
   return t;
 }
 
-__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26 (Hastings' rational approximation): for x >= 0,
+//   erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2),
+//   t = 1 / (1 + p x),  |error| <= 1.5e-7,
+// extended to x < 0 by oddness.  In fp32 with the fast reciprocal and
+// exponential the error stays near 3e-7, far below the bf16 rounding of the
+// output (2^-9 relative).  Two MUFU operations and ten FMA-pipe operations.
+__device__ __forceinline__ float erf_as7126(float x) {
+  const float ax = fabsf(x);
+  const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
+  float q = fmaf(1.061405429f, t, -1.453152027f);
+  q = fmaf(q, t, 1.421413741f);
+  q = fmaf(q, t, -0.284496736f);
+  q = fmaf(q, t, 0.254829592f);
+  q *= t;
+  const float r = fmaf(-q, __expf(-ax * ax), 1.0f);
+  return copysignf(r, x);
+}
+
+// Exact-erf GeLU: z * Phi(z) = z/2 * (1 + erf(z / sqrt 2)).
+__device__ __forceinline__ float gelu_erf(float z) {
+  const float h = 0.5f * z;
+  return fmaf(h, erf_as7126(z * 0.70710678118654752f), h);
+}
 
 __device__ __forceinline__ void store32(uint16_t* dst, const float (&v)[32]) {
 #pragma unroll
@@ -147,6 +189,42 @@ __device__ __forceinline__ void store32(uint16_t* dst, const float (&v)[32]) {
     o.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
     st_v4(dst + 8 * q, o);
   }
+}
+
+// Write a warp's 32 rows x 32 bf16 columns (lane i holds row i, packed in
+// pk) through 1 KB of shared memory, 16 rows at a time, so that each global
+// store instruction covers 8 whole 64-byte row segments instead of 32 rows x
+// 16 bytes.  In the buffer, 16-byte chunk j of row r sits at slot
+// (j + r/2) mod 4 of the row: conflict-free for both the row-wise writes and
+// the chunk-wise reads.  Rows >= rows_valid (another group's rows) are not
+// written.
+__device__ __forceinline__ void store_rows32(uint8_t* stg, uint16_t* out, size_t ld, int rows_valid,
+                                             const uint32_t (&pk)[16], int lane) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    __syncwarp();
+    if ((lane >> 4) == h) {
+      const int r = lane & 15;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(stg + r * 64 + (((j + (r >> 1)) & 3) << 4)) =
+            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int idx = pass * 32 + lane;
+      const int r = idx >> 2, c = idx & 3;
+      const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 64 + (((c + (r >> 1)) & 3) << 4));
+      const int row = h * 16 + r;
+      if (row < rows_valid) st_v4(out + (size_t)row * ld + c * 8, v);
+    }
+  }
+}
+
+__device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
 }
 
 template <int EPI>
@@ -242,15 +320,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
           tma_load_2d(s.a[stage], &tmA, &s.full[stage], kb * BK, arow);
           if (EPI == kSwiglu) {
+            // first half of the B tile: W1 (gate) columns, second half: the same W3 (up) columns
             const int n0 = t.nt * (BN / 2);
-            tma_load_2d(s.b[stage] + 0 * B_BOX_BYTES, &tmB0, &s.full[stage], n0, brow + kb * BK);
-            tma_load_2d(s.b[stage] + 1 * B_BOX_BYTES, &tmB0, &s.full[stage], n0 + 64, brow + kb * BK);
-            tma_load_2d(s.b[stage] + 2 * B_BOX_BYTES, &tmB1, &s.full[stage], n0, brow + kb * BK);
-            tma_load_2d(s.b[stage] + 3 * B_BOX_BYTES, &tmB1, &s.full[stage], n0 + 64, brow + kb * BK);
+#pragma unroll
+            for (int c = 0; c < B_BOXES / 2; ++c) {
+              tma_load_2d(s.b[stage] + c * B_BOX_BYTES, &tmB0, &s.full[stage], n0 + 64 * c, brow + kb * BK);
+              tma_load_2d(s.b[stage] + (c + B_BOXES / 2) * B_BOX_BYTES, &tmB1, &s.full[stage], n0 + 64 * c,
+                          brow + kb * BK);
+            }
           } else {
             const int n0 = t.nt * BN;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < B_BOXES; ++c)
               tma_load_2d(s.b[stage] + c * B_BOX_BYTES, &tmB0, &s.full[stage], n0 + 64 * c, brow + kb * BK);
           }
           ++issued;
@@ -272,6 +353,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, true);
+      // descriptors of stage 0; stages are contiguous, so stage s adds
+      // s * (stage bytes >> 4) to the start-address field
+      const uint64_t adesc0 = smem_desc_sw128(smem_u32(s.a[0]), 16, 1024);
+      const uint64_t bdesc0 = smem_desc_sw128(smem_u32(s.b[0]), B_BOX_BYTES, 1024);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true, withheld = false, any_mma = false;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
@@ -284,16 +369,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(s.a[stage]);
-          const uint32_t b0 = smem_u32(s.b[stage]);
+          // A: K-major, 128-byte rows, 8-row groups 1024 B apart; a K step of 16 is
+          //    32 B, i.e. +2 in the descriptor's start-address field (16-B units).
+          // B: MN-major, 64-column boxes 8 KB apart (LBO), 8 k-rows 1024 B apart
+          //    (SBO); a K step of 16 rows is 2048 B, i.e. +128 in that field.
+          const uint64_t ad = adesc0 + (uint64_t)(stage * (A_BYTES >> 4));
+          const uint64_t bd = bdesc0 + (uint64_t)(stage * (B_BYTES >> 4));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; K step = 32 B.
-            // B: MN-major, 64-column boxes 8 KB apart (LBO), 8 k-rows 1024 B apart (SBO);
-            //    K step of 16 rows = 2048 B.
-            mma_bf16(d, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 2048, B_BOX_BYTES, 1024),
-                     idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 128), idesc, (kb | kk) != 0 ? 1u : 0u);
           mma_commit(&s.empty[stage]);
           any_mma = true;
           if (++stage == STAGES) {
@@ -318,53 +402,59 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
+    const int slice = (warp - 2) >> 2;         // column slice 0..EPI_SLICES-1
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode(s, G, tile);
       // every lane waits; the vote keeps the warp converged for tcgen05.ld
       if (!__all_sync(0xffffffffu, wait_phase(&s.tfull[acc], acc_phase, &s.abort_flag))) break;
       tc_fence_after();
-      const int r = quarter * 32 + lane;
-      const bool row_ok = r < t.rows;
-      uint16_t* orow = p.out + (size_t)(t.row0 + (row_ok ? r : 0)) * p.N_out;
+      // this warp's 32 rows: tile rows quarter*32 .. +31, of which wrows are the group's
+      const int wrows = t.rows - quarter * 32;
+      uint16_t* wbase = p.out + (size_t)(t.row0 + quarter * 32) * p.N_out;
       const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
       if (EPI == kSwiglu) {
+        constexpr int W = (BN / 2) / EPI_SLICES;   // output columns per warp
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = half * 64 + cc * 32;
+        for (int cc = 0; cc < W; cc += 32) {
+          const int c = slice * W + cc;
           uint32_t gr[32], ur[32];
           __syncwarp();
           tmem_ld32(tb + c, gr);
           tmem_ld32(tb + BN / 2 + c, ur);
           const int col = t.nt * (BN / 2) + c;
-          if (row_ok && col < p.N_out) {
+          if (col < p.N_out) {
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float g = __uint_as_float(gr[i]);
-              v[i] = g / (1.0f + __expf(-g)) * __uint_as_float(ur[i]);
+              v[i] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(ur[i]);
             }
-            store32(orow + col, v);
+            uint32_t pk[16];
+            pack32(v, pk);
+            store_rows32(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pk, lane);
           }
         }
       } else {
+        constexpr int W = BN / EPI_SLICES;
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          const int c = half * (BN / 2) + cc * 32;
+        for (int cc = 0; cc < W; cc += 32) {
+          const int c = slice * W + cc;
           uint32_t raw[32];
           __syncwarp();
           tmem_ld32(tb + c, raw);
           const int col = t.nt * BN + c;
-          if (row_ok && col < p.N_out) {
+          if (col < p.N_out) {
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float z = __uint_as_float(raw[i]);
               v[i] = (EPI == kGelu) ? gelu_erf(z) : z;
             }
-            store32(orow + col, v);
+            uint32_t pk[16];
+            pack32(v, pk);
+            store_rows32(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pk, lane);
           }
         }
       }

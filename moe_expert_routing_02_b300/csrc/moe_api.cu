@@ -18,6 +18,7 @@
 #include "common.cuh"
 #include "dispatch.cuh"
 #include "ffn.cuh"
+#include "ffn_pair.cuh"
 #include "replicate.cuh"
 #include "route.cuh"
 #include "stats.cuh"
@@ -52,7 +53,12 @@ struct DeviceInfo {
   bool init = false;
   int num_sms = 0;
   bool ffn_attr[3] = {false, false, false};
+  bool pair_attr[3] = {false, false, false};
+  int pair_clusters[3] = {0, 0, 0};  // max co-resident CTA pairs per pair-kernel instance
 };
+
+// Library options (moe_set_option).
+int g_opt_ffn_kernel = MOE_FFN_KERNEL_AUTO;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
@@ -361,8 +367,7 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
     return fail(MOE_ERR_WORKSPACE, "moe_expert_ffn: workspace needs %zu bytes", ffn_workspace_bytes(A, F));
   const int G = group_expert ? 2 * E : E;
   const long long tiles_bound = ((long long)(A + ffn::BM - 1) / ffn::BM + G) *
-                                (long long)((act == MOE_ACT_SWIGLU ? (F + 127) / 128 : (F + 255) / 256) +
-                                            (H + 255) / 256);
+                                (long long)((F + 63) / 64 + (H + 63) / 64);
   if (tiles_bound >= (1LL << 31)) return fail(MOE_ERR_INVALID, "moe_expert_ffn: problem too large");
 
   DeviceInfo* d = nullptr;
@@ -385,6 +390,75 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
   if ((ms = encode_2d(&mW2, w2, H, (uint64_t)E * F, 64, 64)) != MOE_OK) return ms;
 
   const int epi1 = act == MOE_ACT_SWIGLU ? ffn::kSwiglu : ffn::kGelu;
+  // Kernel choice: the CTA-pair kernel works in 256-row pair tiles, so it is
+  // used when the experts average at least 256 rows; the choice depends on
+  // (A, E) only, so a call with and without replica groups takes the same path.
+  bool use_pair = (long long)A >= 256LL * E;
+  if (g_opt_ffn_kernel == MOE_FFN_KERNEL_SINGLE) use_pair = false;
+  if (g_opt_ffn_kernel == MOE_FFN_KERNEL_PAIR) use_pair = true;
+
+  ffn::Params p1;
+  p1.group_offsets = group_offsets;
+  p1.group_expert = group_expert;
+  p1.G = G;
+  p1.E = E;
+  p1.A_rows = A;
+  p1.K = H;
+  p1.N_out = F;
+  p1.out = inter;
+  p1.flags = 0;
+  ffn::Params p2 = p1;
+  p2.K = F;
+  p2.N_out = H;
+  p2.out = y;
+
+  if (use_pair) {
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      for (int i = 0; i < 3; ++i) {
+        if (d->pair_attr[i]) continue;
+        const void* fn = i == 0 ? (const void*)ffn2::gemm_pair_kernel<ffn::kGelu>
+                       : i == 1 ? (const void*)ffn2::gemm_pair_kernel<ffn::kSwiglu>
+                                : (const void*)ffn2::gemm_pair_kernel<ffn::kStore>;
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ffn2::kSmemBytes);
+        if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: cudaFuncSetAttribute (pair)");
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (d->num_sms / 2), 1, 1);
+        cfg.blockDim = dim3(ffn2::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = ffn2::kSmemBytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+        if (e != cudaSuccess || n < 1) return cuda_status(e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
+                                                          "moe_expert_ffn: cudaOccupancyMaxActiveClusters");
+        d->pair_clusters[i] = n;
+        d->pair_attr[i] = true;
+      }
+    }
+    p1.n_tiles = act == MOE_ACT_SWIGLU ? (F + ffn2::BN / 2 - 1) / (ffn2::BN / 2) : (F + ffn2::BN - 1) / ffn2::BN;
+    p2.n_tiles = (H + ffn2::BN - 1) / ffn2::BN;
+    const long long pt_bound = (long long)(A + ffn2::BMP - 1) / ffn2::BMP + G;
+    auto grid_for = [&](const ffn::Params& p, int inst) {
+      long long pairs = pt_bound * p.n_tiles;
+      if (pairs > d->pair_clusters[inst]) pairs = d->pair_clusters[inst];
+      return (unsigned)(2 * (pairs < 1 ? 1 : pairs));
+    };
+    if (epi1 == ffn::kSwiglu)
+      ffn2::gemm_pair_kernel<ffn::kSwiglu><<<grid_for(p1, 1), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
+    else
+      ffn2::gemm_pair_kernel<ffn::kGelu><<<grid_for(p1, 0), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM1 (pair) launch");
+    ffn2::gemm_pair_kernel<ffn::kStore><<<grid_for(p2, 2), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
+    return cuda_status(cudaGetLastError(), "moe_expert_ffn: GEMM2 (pair) launch");
+  }
+
   {
     std::lock_guard<std::mutex> lk(g_mu);
     for (int i = 0; i < 3; ++i) {
@@ -397,23 +471,8 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
       d->ffn_attr[i] = true;
     }
   }
-  ffn::Params p1;
-  p1.group_offsets = group_offsets;
-  p1.group_expert = group_expert;
-  p1.G = G;
-  p1.E = E;
-  p1.A_rows = A;
-  p1.K = H;
-  p1.N_out = F;
-  p1.n_tiles = act == MOE_ACT_SWIGLU ? (F + 127) / 128 : (F + 255) / 256;
-  p1.out = inter;
-  p1.flags = 0;
-  ffn::Params p2 = p1;
-  p2.K = F;
-  p2.N_out = H;
-  p2.n_tiles = (H + 255) / 256;
-  p2.out = y;
-
+  p1.n_tiles = act == MOE_ACT_SWIGLU ? (F + ffn::BN / 2 - 1) / (ffn::BN / 2) : (F + ffn::BN - 1) / ffn::BN;
+  p2.n_tiles = (H + ffn::BN - 1) / ffn::BN;
   const long long mt_bound = (long long)(A + ffn::BM - 1) / ffn::BM + G;
   auto grid_for = [&](const ffn::Params& p) {
     long long g = mt_bound * p.n_tiles;
@@ -428,6 +487,26 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
   if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM1 launch");
   ffn::gemm_kernel<ffn::kStore><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
   return cuda_status(cudaGetLastError(), "moe_expert_ffn: GEMM2 launch");
+}
+
+// ------------------------------------------------------------------ options
+moe_status moe_set_option(int option, int value) {
+  if (option == MOE_OPT_FFN_KERNEL) {
+    if (value < MOE_FFN_KERNEL_AUTO || value > MOE_FFN_KERNEL_PAIR)
+      return fail(MOE_ERR_INVALID, "moe_set_option: unknown FFN kernel %d", value);
+    g_opt_ffn_kernel = value;
+    return MOE_OK;
+  }
+  return fail(MOE_ERR_INVALID, "moe_set_option: unknown option %d", option);
+}
+
+moe_status moe_get_option(int option, int* value) {
+  if (!value) return fail(MOE_ERR_INVALID, "moe_get_option: null value");
+  if (option == MOE_OPT_FFN_KERNEL) {
+    *value = g_opt_ffn_kernel;
+    return MOE_OK;
+  }
+  return fail(MOE_ERR_INVALID, "moe_get_option: unknown option %d", option);
 }
 
 // ------------------------------------------------------------------ combine

@@ -138,54 +138,70 @@ __global__ void __launch_bounds__(kThreads) update_kernel(UpdateArgs a) {
 static cudaError_t launch_update(const UpdateArgs& a, int num_sms, cudaStream_t st) {
   const bool cos_smem = a.has_prev != 0 && a.E <= kSmemCoselMaxE;
   const size_t smem = sizeof(uint32_t) * (a.E + (cos_smem ? a.E * a.E : 0));
-  long long blocks = ((long long)a.T + kThreads - 1) / kThreads;
-  if (blocks > 2LL * num_sms) blocks = 2LL * num_sms;
+  long long blocks = ((long long)a.T + 4 * kThreads - 1) / (4 * kThreads);
+  if (blocks > num_sms) blocks = num_sms;
   if (blocks < 1) blocks = 1;
   update_kernel<<<(int)blocks, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- K3
-// One block.  fp64 throughout; integers converted exactly.
+// One block, fp64 throughout (window sums are integers, converted exactly).
+// Every read is a cooperative, coalesced load into shared memory first; the
+// row sums of Cbar are one warp per row.  Pr(e'|e) = Cbar[e,e'] / row[e] is
+// formed as Cbar * (1 / row) -- within one fp64 ulp of the division, far below
+// the fp32 output rounding.
+constexpr int kPredictSmemE = 64;  // Cbar staged in shared memory up to E = 64
+
 __global__ void __launch_bounds__(kThreads) predict_kernel(const unsigned long long* __restrict__ hsum,
                                                            const unsigned long long* __restrict__ csum, int E,
                                                            float* __restrict__ p_seq, float* __restrict__ cond,
                                                            float* __restrict__ p_next) {
   __shared__ double ps[256];
-  __shared__ double rows[256];
-  __shared__ unsigned long long tot_sh;
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    unsigned long long tot = 0;
-    for (int e = 0; e < E; ++e) tot += hsum[e];
-    tot_sh = tot;
-  }
-  if (csum && tid < E) {
-    unsigned long long r = 0;
-    for (int e2 = 0; e2 < E; ++e2) r += csum[(size_t)tid * E + e2];
-    rows[tid] = (double)r;
-  }
+  __shared__ double rinv[256];   // 1 / row sum, or 0 for an empty row
+  __shared__ unsigned long long wsum[kThreads / 32];
+  __shared__ unsigned long long cs[kPredictSmemE * kPredictSmemE];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const bool stage = csum != nullptr && E <= kPredictSmemE;
+  unsigned long long h = tid < E ? hsum[tid] : 0ull;
+  if (stage)
+    for (int i = tid; i < E * E; i += kThreads) cs[i] = csum[i];
+  unsigned long long tot = h;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+  if (lane == 0) wsum[wid] = tot;
   __syncthreads();
-  const unsigned long long tot = tot_sh;
+  tot = 0;
+  for (int w = 0; w < kThreads / 32; ++w) tot += wsum[w];
   if (tid < E) {
-    const double p = tot > 0 ? (double)hsum[tid] / (double)tot : 1.0 / (double)E;
+    const double p = tot > 0 ? (double)h / (double)tot : 1.0 / (double)E;
     ps[tid] = p;
     p_seq[tid] = (float)p;
   }
-  __syncthreads();
   if (!csum) return;
+  // row sums: one warp per row
+  for (int e = wid; e < E; e += kThreads / 32) {
+    unsigned long long r = 0;
+    for (int e2 = lane; e2 < E; e2 += 32) r += stage ? cs[e * E + e2] : csum[(size_t)e * E + e2];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+    if (lane == 0) rinv[e] = r > 0 ? 1.0 / (double)r : 0.0;
+  }
+  __syncthreads();
+  const double uni = 1.0 / (double)E;
   if (cond) {
     for (int i = tid; i < E * E; i += kThreads) {
-      const int e = i / E;
-      const double c = rows[e] > 0 ? (double)csum[i] / rows[e] : 1.0 / (double)E;
-      cond[i] = (float)c;
+      const double ri = rinv[i / E];
+      const unsigned long long cv = stage ? cs[i] : csum[i];
+      cond[i] = (float)(ri > 0 ? (double)cv * ri : uni);
     }
   }
   if (p_next && tid < E) {
     double acc = 0.0;
     for (int e = 0; e < E; ++e) {
-      const double c = rows[e] > 0 ? (double)csum[(size_t)e * E + tid] / rows[e] : 1.0 / (double)E;
-      acc = fma(ps[e], c, acc);
+      const double ri = rinv[e];
+      const unsigned long long cv = stage ? cs[e * E + tid] : csum[(size_t)e * E + tid];
+      acc = fma(ps[e], ri > 0 ? (double)cv * ri : uni, acc);
     }
     p_next[tid] = (float)acc;
   }

@@ -108,3 +108,57 @@ class MoELayerStep:
         if self.replicate:
             n += 1
         return n
+
+
+class HostPipeline:
+    """Run layers whose inputs and outputs live in (pinned) host memory.
+
+    Three streams overlap the work: the copy of layer j+1's logits and X to
+    the device, the seven calls of layer j, and the copy of layer j-1's output
+    back to the host.  Device staging buffers are double-buffered; events order
+    each buffer's reuse.  Host tensors should be pinned for the copies to run
+    asynchronously."""
+
+    def __init__(self, step: MoELayerStep, device="cuda"):
+        self.step = step
+        d = torch.device(device)
+        T, E, H = step.T, step.E, step.H
+        self.d_logits = [torch.empty((T, E), dtype=torch.float32, device=d) for _ in range(2)]
+        self.d_x = [torch.empty((T, H), dtype=torch.bfloat16, device=d) for _ in range(2)]
+        self.d_out = [torch.empty((T, H), dtype=torch.bfloat16, device=d) for _ in range(2)]
+        self.h2d = torch.cuda.Stream(device=d)
+        self.d2h = torch.cuda.Stream(device=d)
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.in_free = [torch.cuda.Event() for _ in range(2)]
+        self.out_ready = [torch.cuda.Event() for _ in range(2)]
+        self.out_free = [torch.cuda.Event() for _ in range(2)]
+        self._fresh = [True, True]
+
+    def run(self, it: int, h_logits, h_x, weights, h_out, layers=None):
+        """h_logits[j] [T,E] f32, h_x[j] [T,H] bf16, h_out[j] [T,H] bf16 host
+        tensors; weights[j] = (w1, w3, w2) on the device.  Enqueues every layer
+        and returns; synchronise the current stream (or the device) before
+        reading h_out."""
+        comp = torch.cuda.current_stream()
+        L = len(h_x) if layers is None else layers
+        for j in range(L):
+            b = j & 1
+            with torch.cuda.stream(self.h2d):
+                if not self._fresh[b]:
+                    self.h2d.wait_event(self.in_free[b])
+                self.d_logits[b].copy_(h_logits[j], non_blocking=True)
+                self.d_x[b].copy_(h_x[j], non_blocking=True)
+                self.in_ready[b].record(self.h2d)
+            comp.wait_event(self.in_ready[b])
+            if not self._fresh[b]:
+                comp.wait_event(self.out_free[b])
+            self.step.run(it, j, self.d_logits[b], self.d_x[b], weights[j], self.d_out[b])
+            self.in_free[b].record(comp)
+            self.out_ready[b].record(comp)
+            with torch.cuda.stream(self.d2h):
+                self.d2h.wait_event(self.out_ready[b])
+                h_out[j].copy_(self.d_out[b], non_blocking=True)
+                self.out_free[b].record(self.d2h)
+            self._fresh[b] = False
+        # the caller's stream covers the last copies back
+        comp.wait_stream(self.d2h)

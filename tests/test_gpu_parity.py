@@ -47,6 +47,17 @@ def ok_check():
     M.moe_check()
 
 
+KERNELS = {"auto": 0, "single": 1, "pair": 2}
+
+
+@pytest.fixture
+def ffn_kernel(request):
+    """Force the grouped-GEMM kernel for one test, then restore the default."""
+    M.moe_set_option(M.MOE_OPT_FFN_KERNEL, KERNELS[request.param])
+    yield request.param
+    M.moe_set_option(M.MOE_OPT_FFN_KERNEL, M.MOE_FFN_KERNEL_AUTO)
+
+
 # ----------------------------------------------------------------------------
 # K1 route
 # ----------------------------------------------------------------------------
@@ -307,23 +318,28 @@ def _ffn_check(c, sample=256, rep=False, seed=0):
     return err, (go, perm, inv, xp, y, idx, x, (w1, w3, w2), rb, ge)
 
 
-def test_ffn_tiny_full():
+@pytest.mark.parametrize("ffn_kernel", ["single", "pair"], indirect=True)
+def test_ffn_tiny_full(ffn_kernel):
     err, _ = _ffn_check(W.config_by_name("tiny"), sample=None)
     assert err < 1e-2
 
 
-@pytest.mark.parametrize("name", ["moe_gpt_stream", "mixtral_layer", "deepseekv2_layer", "dbrx_replicated_layer"])
-def test_ffn_full_size_sampled(name):
+@pytest.mark.parametrize("name,ffn_kernel", [("moe_gpt_stream", "auto"), ("mixtral_layer", "auto"),
+                                              ("deepseekv2_layer", "auto"), ("dbrx_replicated_layer", "auto"),
+                                              ("moe_gpt_stream", "single"), ("deepseekv2_layer", "pair")],
+                         indirect=["ffn_kernel"])
+def test_ffn_full_size_sampled(name, ffn_kernel):
     c = W.config_by_name(name)
     _ffn_check(c, sample=256, rep=c.replicate)
     torch.cuda.empty_cache()
 
 
-def test_ffn_ragged_groups_and_partial_tiles():
+@pytest.mark.parametrize("ffn_kernel", ["single", "pair"], indirect=True)
+def test_ffn_ragged_groups_and_partial_tiles(ffn_kernel):
     """Groups of 0, 1, 127, 128, 129 rows; F and H not multiples of the 256 tile."""
     import dataclasses
-    c = dataclasses.replace(W.config_by_name("tiny"), name="ragged", E=6, k=1, H=192, F=320, act="swiglu")
-    sizes = [0, 1, 127, 128, 129, 300]
+    c = dataclasses.replace(W.config_by_name("tiny"), name="ragged", E=10, k=1, H=192, F=320, act="swiglu")
+    sizes = [0, 1, 127, 128, 129, 300, 255, 256, 257, 513]
     idx = np.concatenate([np.full(n, e, np.int32) for e, n in enumerate(sizes)])
     np.random.default_rng(0).shuffle(idx)
     idx = idx.reshape(-1, 1)
@@ -341,6 +357,59 @@ def test_ffn_ragged_groups_and_partial_tiles():
         lo, hi = host(go)[g], host(go)[g + 1]
         if hi > lo:
             assert rel_fro(got[lo:hi], ref[lo:hi]) <= FFN_TOL
+
+
+def _rne_bf16(v):
+    u = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + ((u >> 16) & 1) + 0x7FFF) >> 16).astype(np.uint16)
+
+
+def _act_bound(v, x):
+    """Half a bf16 ulp of the result (8 significant bits), plus the fp32
+    activation's own error: 1e-6 relative, and 3e-7 |x| + 1e-7 absolute.  The
+    absolute part covers the erf approximation (|error| <= 1.5e-7, scaled by
+    x/2) and the cancellation in 1 + erf for very negative x, where every fp32
+    erf has large relative but tiny absolute error."""
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    half_ulp = np.where(a > 0, 2.0 ** (e - 8), 0.0)
+    return half_ulp + 1e-6 * a + 3e-7 * np.abs(x) + 1e-7
+
+
+@pytest.mark.parametrize("ffn_kernel", ["single", "pair"], indirect=True)
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_ffn_activation_accuracy_identity_weights(act, ffn_kernel):
+    """With identity projections each output is bf16(act(x)) exactly as the
+    epilogue computes it: GeLU(x) = x Phi(x) (exact-erf form) or silu(x) * x.
+    The GPU value must be the fp64 activation rounded to bf16, up to half an
+    ulp plus the error budget of the fp32 activation (see _act_bound).  A tanh
+    GeLU (error up to ~1e-3 |x|), a dropped factor or a wrong sign fails."""
+    from scipy.special import erf
+    E, H, F, T = 2, 64, 128, 512
+    eye = torch.eye(H, dtype=torch.float32, device="cuda")
+    w1 = torch.zeros((E, H, F), device="cuda")
+    w1[:, :, :H] = eye
+    w1[:, :, H:] = eye
+    w2 = torch.zeros((E, F, H), device="cuda")
+    w2[:, :H, :] = eye
+    w1, w2 = w1.to(torch.bfloat16), w2.to(torch.bfloat16)
+    w3 = w1.clone() if act == "swiglu" else None
+    x = torch.linspace(-9.0, 9.0, T * H, device="cuda").reshape(T, H).to(torch.bfloat16)
+    idx = torch.arange(T, device="cuda", dtype=torch.int32).remainder(E).reshape(T, 1)
+    go, perm, inv, xp = M.moe_dispatch(x, idx, E)
+    y = M.moe_expert_ffn(xp, go, None, None, w1, w3, w2, act)
+    ok_check()
+    xv = O.bf16_to_f64(W.bf16_bits(xp))
+    ref = 0.5 * xv * (1.0 + erf(xv / np.sqrt(2.0))) if act == "gelu" else xv / (1.0 + np.exp(-xv)) * xv
+    got = O.bf16_to_f64(W.bf16_bits(y))
+    err = np.abs(got - ref)
+    bound = _act_bound(ref, xv)
+    assert np.all(err <= bound), float((err - bound).max())
+    # away from the cancellation tail almost every output is the correctly
+    # rounded value
+    core = np.abs(xv) <= 2.0
+    exact = np.mean(got[core] == O.bf16_to_f64(_rne_bf16(ref[core])))
+    assert exact > 0.99, exact
 
 
 # ----------------------------------------------------------------------------
@@ -361,7 +430,8 @@ def test_combine_matches_oracle_on_gpu_y():
     ok_check()
 
 
-def test_replication_output_bit_identical():
+@pytest.mark.parametrize("ffn_kernel", ["auto", "single"], indirect=True)
+def test_replication_output_bit_identical(ffn_kernel):
     c = W.config_by_name("dbrx_replicated_layer")
     lg = W.make_layer_logits(c, 0, layers=1)[0]
     x = W.make_x(c, 0, 0, device="cuda")
