@@ -263,10 +263,16 @@ moe_status moe_dispatch_noalloc(const uint16_t* x, const int32_t* idx, int T, in
  *                           single-CTA kernel (128-row tiles).  The choice
  *                           depends only on (A, E).
  *     MOE_FFN_KERNEL_SINGLE / MOE_FFN_KERNEL_PAIR  force one kernel.
+ *   MOE_OPT_FFN_TIMEOUT_SELFTEST  value 1 arms a one-shot self-test of the
+ *     bounded waits: in the next moe_expert_ffn call, the first GEMM's CTA
+ *     (pair) 0 never signals its first accumulator, so its epilogue's wait
+ *     runs out after ~2 s; the kernel then releases its resources and
+ *     returns, and moe_check reports MOE_ERR_TIMEOUT (that call's output is
+ *     incomplete).  The option resets itself after that call.
  * Unknown options or values return MOE_ERR_INVALID.  Not thread-safe against
  * concurrent moe_expert_ffn calls.
  * ------------------------------------------------------------------------- */
-typedef enum { MOE_OPT_FFN_KERNEL = 1 } moe_option;
+typedef enum { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_FFN_TIMEOUT_SELFTEST = 2 } moe_option;
 typedef enum { MOE_FFN_KERNEL_AUTO = 0, MOE_FFN_KERNEL_SINGLE = 1, MOE_FFN_KERNEL_PAIR = 2 } moe_ffn_kernel;
 moe_status moe_set_option(int option, int value);
 moe_status moe_get_option(int option, int* value /* host */);

@@ -59,6 +59,7 @@ struct DeviceInfo {
 
 // Library options (moe_set_option).
 int g_opt_ffn_kernel = MOE_FFN_KERNEL_AUTO;
+int g_opt_ffn_selftest = 0;  // one-shot: next GEMM1 withholds an accumulator signal
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
@@ -406,8 +407,10 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
   p1.K = H;
   p1.N_out = F;
   p1.out = inter;
-  p1.flags = 0;
+  p1.flags = g_opt_ffn_selftest ? 1 : 0;
+  g_opt_ffn_selftest = 0;
   ffn::Params p2 = p1;
+  p2.flags = 0;
   p2.K = F;
   p2.N_out = H;
   p2.out = y;
@@ -497,6 +500,11 @@ moe_status moe_set_option(int option, int value) {
     g_opt_ffn_kernel = value;
     return MOE_OK;
   }
+  if (option == MOE_OPT_FFN_TIMEOUT_SELFTEST) {
+    if (value != 0 && value != 1) return fail(MOE_ERR_INVALID, "moe_set_option: self-test value must be 0 or 1");
+    g_opt_ffn_selftest = value;
+    return MOE_OK;
+  }
   return fail(MOE_ERR_INVALID, "moe_set_option: unknown option %d", option);
 }
 
@@ -504,6 +512,10 @@ moe_status moe_get_option(int option, int* value) {
   if (!value) return fail(MOE_ERR_INVALID, "moe_get_option: null value");
   if (option == MOE_OPT_FFN_KERNEL) {
     *value = g_opt_ffn_kernel;
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_FFN_TIMEOUT_SELFTEST) {
+    *value = g_opt_ffn_selftest;
     return MOE_OK;
   }
   return fail(MOE_ERR_INVALID, "moe_get_option: unknown option %d", option);

@@ -133,6 +133,11 @@ def test_stats_and_replicate_reject_bad_arguments(L):
     assert L.moe_stats_bytes(NULL) == 0
     assert L.moe_stats_export(NULL, FAKE, 10) == inv
     assert L.moe_error_word(None) == inv
+    assert L.moe_set_option(99, 0) == inv
+    assert L.moe_set_option(M.MOE_OPT_FFN_KERNEL, 7) == inv
+    assert L.moe_set_option(M.MOE_OPT_FFN_TIMEOUT_SELFTEST, 2) == inv
+    v = ctypes.c_int(-1)
+    assert L.moe_get_option(M.MOE_OPT_FFN_KERNEL, ctypes.byref(v)) == M.MOE_OK and v.value == 0
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

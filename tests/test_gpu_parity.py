@@ -463,3 +463,33 @@ def test_tiny_layer_end_to_end():
         ok_check()
         ref = O.moe_layer(lg, W.bf16_bits(x), c.k, W.bf16_bits(w1), None, W.bf16_bits(w2), c.act)
         assert rel_fro(O.bf16_to_f64(W.bf16_bits(out)), ref["out"]) <= FFN_TOL
+
+
+# ----------------------------------------------------------------------------
+# bounded waits: a wait that runs out is reported, and the context survives
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("ffn_kernel", ["single", "pair"], indirect=True)
+def test_ffn_bounded_wait_timeout_is_reported_and_context_survives(ffn_kernel):
+    """A one-shot self-test makes CTA (pair) 0 of GEMM1 withhold one
+    accumulator-ready signal (a flag nothing else sets): its epilogue's wait
+    runs out after ~2 s, the kernel releases TMEM and returns, moe_check
+    reports MOE_ERR_TIMEOUT, and the next call on the same context is correct."""
+    import time
+    c = W.config_by_name("tiny")
+    lg = W.make_layer_logits(c, 0, layers=1)[0]
+    idx, _ = O.topk_gate(lg, c.k)
+    x = W.make_x(c, 0, 0, device="cuda")
+    w1, w3, w2 = _weights(c)
+    go, perm, inv, xp = M.moe_dispatch(x, dev(idx), c.E)
+    M.moe_set_option(M.MOE_OPT_FFN_TIMEOUT_SELFTEST, 1)
+    t0 = time.time()
+    M.moe_expert_ffn(xp, go, None, None, w1, w3, w2, c.act)
+    with pytest.raises(M.MoEError) as ei:
+        M.moe_check()
+    assert ei.value.status == M.MOE_ERR_TIMEOUT
+    assert time.time() - t0 < 60
+    assert M.moe_get_option(M.MOE_OPT_FFN_TIMEOUT_SELFTEST) == 0   # one-shot
+    y = M.moe_expert_ffn(xp, go, None, None, w1, w3, w2, c.act)
+    ok_check()
+    ref = O.expert_ffn(W.bf16_bits(xp), host(go)[:c.E + 1], None, W.bf16_bits(w1), None, W.bf16_bits(w2), c.act)
+    assert rel_fro(O.bf16_to_f64(W.bf16_bits(y)), ref) <= FFN_TOL
