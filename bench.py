@@ -57,6 +57,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (tokens of one layer)")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers (small profiling captures; not a bench line)")
+    ap.add_argument("--T", type=int, default=0, help="override tokens (small profiling captures; not a bench line)")
+    ap.add_argument("--E", type=int, default=0, help="override experts (small profiling captures; not a bench line)")
     return ap.parse_args(argv)
 
 
@@ -163,11 +165,15 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # workload
 # ----------------------------------------------------------------------------
-def algorithmic_work(c):
+def algorithmic_work(c, used_experts=None):
     """Per-layer algorithmic bytes (HBM stages) and flops (FFN), as the method
-    must move them (not what the kernels happen to move)."""
+    must move them (not what the kernels happen to move).  The FFN must read
+    the weights of every expert that received a token (used_experts, counted
+    from a layer's histogram; all E when unknown) once, its input rows once and write its output
+    rows once (plus the bf16 intermediate written and read back)."""
     T, E, k, H, F, A = c.T, c.E, c.k, c.H, c.F, c.A
     ngemm = 3 if c.act == "swiglu" else 2
+    Eu = E if used_experts is None else used_experts
     return {
         "route": {"bytes": T * E * 4 + A * 8},
         "stats": {"bytes": 2 * A * 4 + (E + E * E) * 4 * 2 + (E + E * E) * 8 * 2},
@@ -175,7 +181,7 @@ def algorithmic_work(c):
         "replicate": {"bytes": E * 16},
         "dispatch": {"bytes": A * 4 + T * H * 2 + A * H * 2 + 2 * A * 4},
         "ffn": {"flops": 2 * ngemm * A * H * F,
-                "bytes": ngemm * E * H * F * 2 + A * H * 2 * 2 + (ngemm - 1) * A * F * 2 * 2},
+                "bytes": int(ngemm * Eu * H * F * 2 + A * H * 2 * 2 + (ngemm - 1) * A * F * 2 * 2)},
         "combine": {"bytes": A * H * 2 + A * 8 + T * H * 2},
     }
 
@@ -223,9 +229,10 @@ def run_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     c = W.config_by_name(args.config)
-    if args.layers:
+    if args.layers or args.T or args.E:
         import dataclasses
-        c = dataclasses.replace(c, L=min(args.layers, c.L))
+        c = dataclasses.replace(c, L=min(args.layers, c.L) if args.layers else c.L, T=args.T or c.T,
+                                E=args.E or c.E)
     dev = torch.device("cuda", local)
     POOL = 2  # distinct iterations of logits cycled through the steps
     logits = [[torch.from_numpy(l).to(dev) for l in W.make_layer_logits(c, it)] for it in range(POOL)]
@@ -332,7 +339,9 @@ def run_ours(args, rank, world, local):
         stage_ms = stage_means(stage_ev)
         ffn_ms = stage_ms["ffn"]
     stage_note = None
-    work = algorithmic_work(c)
+    # experts that received tokens, from the last layer call's histogram (libmoe's own count)
+    used = float((step.hist > 0).sum().item())
+    work = algorithmic_work(c, used_experts=used)
     peaks = load_peaks()
     stages = {}
     for sname in STAGES:
@@ -347,16 +356,24 @@ def run_ours(args, rank, world, local):
         d["frac_hbm"] = round(work[sname]["bytes"] / t / 1e9 / peaks["hbm_gbs"], 3)
         stages[sname] = d
     ffn_t = ffn_ms / 1e3
-    achieved = work["ffn"]["flops"] / ffn_t / 1e12
-    roofline = {"bound": "tensor", "kernel": "moe_expert_ffn (GEMM1+GEMM2 launches)", "achieved": round(achieved, 1),
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
-                "peak_source": f"bf16_tflops_sustained of {peaks['source']} peaks (kernel timed inside a long step)",
-                "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": ffn_traffic_per_launch(),
-                "algorithmic_flops_per_call": work["ffn"]["flops"],
-                "algorithmic_bytes_per_call": work["ffn"]["bytes"]}
-
+    fl, by = work["ffn"]["flops"], work["ffn"]["bytes"]
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)   # flop/B
+    if fl / by >= ridge:
+        achieved = fl / ffn_t / 1e12
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops_sustained"],
+                    "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                    "peak_source": f"bf16_tflops_sustained of {peaks['source']} peaks (kernel timed inside a long step)",
+                    "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4)}
+    else:
+        achieved = by / ffn_t / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "peak_source": f"hbm_gbs of {peaks['source']} peaks",
+                    "tflops": round(fl / ffn_t / 1e12, 1)}
+    roofline.update({"kernel": "moe_expert_ffn (GEMM1+GEMM2 launches)", "traffic": ffn_traffic_per_launch(),
+                     "algorithmic_flops_per_call": fl, "algorithmic_bytes_per_call": by,
+                     "arithmetic_intensity": round(fl / by, 1), "ridge_flop_per_byte": round(ridge, 1),
+                     "experts_with_tokens": used})
     launches = K * sum(step.launches(j, c.L) for j in range(c.L))
     if stage_note:
         roofline["note"] = stage_note

@@ -191,16 +191,20 @@ moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int
  *   group_offsets  [G+1] int32, G = 2E when group_expert is given, else E
  *   group_expert   [G] int32 expert of each group (-1 / empty groups
  *                  allowed) or NULL (group g = expert g)
- *   rep_base       [E+1] int32 or NULL: groups of expert e are
- *                  rep_base[e]..rep_base[e+1]-1; used to pick the kernel
- *                  path by the expert's total rows, so every replica of an
- *                  expert takes the same path
+ *   rep_base       [E+1] int32 or NULL; not needed by the kernels: adjacent
+ *                  groups with the same expert (the layout moe_dispatch
+ *                  writes) are treated as that expert's rows, tiled as one
+ *                  range, and the kernel path is chosen from their total, so
+ *                  every replica of an expert takes the same path and the
+ *                  output does not depend on the replica split
  *   w1, w3         [E,H,F] bf16 (w1 = gate / first projection, w3 = up
  *                  projection, NULL for GeLU);  w2 [E,F,H] bf16
  *   act            MOE_ACT_GELU: y = gelu(x w1) w2 (exact erf)
  *                  MOE_ACT_SWIGLU: y = (silu(x w1) * (x w3)) w2
- *   small_group_threshold  experts with fewer rows use the small-batch path
- *                  (0 = never)
+ *   small_group_threshold  experts with fewer rows use the small-batch kernel
+ *                  (0 = never): Y^T = W^T X^T with the expert's rows as the
+ *                  MMA N dimension (EPS-MoE review: DenseGemm below the
+ *                  GroupGemm crossover); the others use the grouped kernel
  *   y              [A,H] bf16 out (fp32 accumulation, bf16 intermediate)
  *   workspace      ws_bytes >= moe_workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F)
  *                  with T*k = A; 16-byte aligned

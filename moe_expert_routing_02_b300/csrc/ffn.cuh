@@ -11,9 +11,12 @@
 //          inter[A, F] = silu(xp . W1[e]) * (xp . W3[e])  (SwiGLU)
 //   GEMM2: y[A, H]     = inter[A, F] . W2[e]
 // Rows are grouped by expert (or replica group); group sizes live only on the
-// device, so every CTA reads the group offsets and enumerates the tiles
-// (group, n-tile, m-tile) itself, m fastest so that CTAs running at the same
-// time share the expert's weight tile in L2.  CTA c takes tiles c, c+grid, ...
+// device, so every CTA reads the group offsets, folds adjacent groups of the
+// same expert into one row range ("unit", build_units) and enumerates the
+// tiles (unit, n-tile, m-tile) itself, m fastest so that CTAs running at the
+// same time share the expert's weight tile in L2.  CTA c takes tiles c,
+// c+grid, ...  Experts below the small-batch threshold are left to
+// ffn_small.cuh.
 //
 // Per CTA (one per SM, 576 threads):
 //   warp 0      TMA producer: A tile 128x64 (K-major) and B tile 64x256
@@ -40,6 +43,7 @@
 // the copies it issued, the MMA thread for its MMAs, and TMEM is freed before
 // the CTA exits.
 #pragma once
+#include <climits>
 #include <cstddef>
 #include "common.cuh"
 #include "sm100_ptx.cuh"
@@ -87,7 +91,10 @@ struct Params {
   int n_tiles;       // N tiles per group
   uint16_t* out;     // [A_rows, N_out] bf16
   int flags;         // bit 0: CTA 0 withholds its first accumulator signal (timeout self-test)
+  const int32_t* rep_base;  // [E+1] or null: groups of expert e are rep_base[e]..rep_base[e+1]-1
+  int small_threshold;      // experts with fewer rows take the small-batch kernel (0 = none)
 };
+
 
 struct Smem {
   uint8_t a[STAGES][A_BYTES];
@@ -100,10 +107,12 @@ struct Smem {
   uint32_t tmem_base;
   uint32_t abort_flag;
   int32_t total_tiles;
-  int32_t goff[MAX_G + 1];
+  int32_t u_count;
+  int32_t goff[MAX_G + 1];   // staged group offsets
+  int32_t us[MAX_G + 1];     // unit first rows (build_units)
   int32_t tstart[MAX_G + 1];
   int32_t mt[MAX_G];
-  int32_t ex[MAX_G];
+  int32_t ex[MAX_G];         // unit experts
   alignas(128) uint8_t stg[EPI_WARPS][1024];  // per-warp output staging (store_rows32; 16-byte accesses)
 };
 
@@ -132,24 +141,117 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint3
   return false;
 }
 
+// Group table -> "units": maximal runs of consecutive groups that serve the
+// same expert.  The replica groups of an expert are adjacent in the dispatched
+// layout and alias that expert's weights, so a unit is tiled as one row range:
+// every row's result is the same as when its replica group is tiled alone
+// (same weights, same K order), without a partial tile per replica.  A unit's
+// rows are the expert's total rows, so the kernel path chosen from them is
+// the same for all replicas of an expert.
+//   us[u] first row of unit u, us[U] = end of the last unit; ue[u] its expert
+//   (-1: no valid expert; such a unit gets no tiles).  Offsets are clamped to
+//   [0, A_rows]; decreasing or out-of-range offsets and unknown experts are
+//   flagged as invalid data.  Call from all NT threads; returns U.
+template <int NT>
+__device__ int build_units(const Params& p, int32_t* goff, int32_t* us, int32_t* ue, int32_t* u_count) {
+  const int G = p.G;
+  const int lane = threadIdx.x & 31;
+  for (int g = threadIdx.x; g <= G; g += NT) {
+    long long v = p.group_offsets[g];
+    if (v < 0 || v > p.A_rows) {
+      moe_flag_error(MOE_DEVERR_DATA);
+      v = v < 0 ? 0 : p.A_rows;
+    }
+    goff[g] = (int32_t)v;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int carry = 0, prev_e = INT_MIN;
+    for (int c0 = 0; c0 < G; c0 += 32) {
+      const int g = c0 + lane;
+      int e = INT_MIN;
+      if (g < G) e = p.group_expert ? p.group_expert[g] : g;
+      int pe = __shfl_up_sync(0xffffffffu, e, 1);
+      if (lane == 0) pe = prev_e;
+      const bool start = g < G && (g == 0 || e != pe);
+      const unsigned starts = __ballot_sync(0xffffffffu, start);
+      const int u = carry + __popc(starts & ((1u << lane) - 1u));
+      if (start) {
+        us[u] = goff[g];
+        ue[u] = e;
+      }
+      if (g < G && goff[g + 1] < goff[g]) moe_flag_error(MOE_DEVERR_DATA);
+      carry += __popc(starts);
+      prev_e = __shfl_sync(0xffffffffu, e, 31);
+    }
+    if (lane == 0) {
+      us[carry] = goff[G];
+      *u_count = carry;
+    }
+  }
+  __syncthreads();
+  const int U = *u_count;
+  for (int u = threadIdx.x; u < U; u += NT) {
+    const int rows = us[u + 1] - us[u];
+    if (rows > 0 && (ue[u] < 0 || ue[u] >= p.E)) {
+      moe_flag_error(MOE_DEVERR_DATA);
+      ue[u] = -1;
+    }
+  }
+  __syncthreads();
+  return U;
+}
+
+// Tiles of each unit and their prefix (warp 0): tiles_u = ceil(rows_u / tile_rows)
+// * n_tiles for units the caller's filter keeps (keep(rows) -> bool), else 0.
+template <int NT, typename Keep>
+__device__ void unit_tile_prefix(const Params& p, int U, const int32_t* us, const int32_t* ue, int32_t* mt,
+                                 int32_t* tstart, int32_t* total, int tile_rows, Keep keep) {
+  const int lane = threadIdx.x & 31;
+  for (int u = threadIdx.x; u < U; u += NT) {
+    const int rows = us[u + 1] - us[u];
+    mt[u] = (rows > 0 && ue[u] >= 0 && keep(rows)) ? (rows + tile_rows - 1) / tile_rows : 0;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int carry = 0;
+    for (int c0 = 0; c0 < U; c0 += 32) {
+      const int u = c0 + lane;
+      const int v = u < U ? mt[u] * p.n_tiles : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int w = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += w;
+      }
+      if (u < U) tstart[u] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      tstart[U] = carry;
+      *total = carry;
+    }
+  }
+}
+
 struct Tile {
   int g, nt, rows;
   long long row0;
 };
 
-__device__ __forceinline__ Tile decode(const Smem& s, int G, int tile) {
-  int lo = 0, hi = G;  // tstart[lo] <= tile < tstart[hi]
+__device__ __forceinline__ Tile decode(const Smem& s, int U, int tile) {
+  int lo = 0, hi = U;  // tstart[lo] <= tile < tstart[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (s.tstart[mid] <= tile) lo = mid; else hi = mid;
   }
   Tile t;
-  t.g = lo;
+  t.g = lo;  // unit
   const int local = tile - s.tstart[lo];
   const int m = s.mt[lo];
   t.nt = local / m;
-  t.row0 = (long long)s.goff[lo] + (long long)(local % m) * BM;
-  const long long left = (long long)s.goff[lo + 1] - t.row0;
+  t.row0 = (long long)s.us[lo] + (long long)(local % m) * BM;
+  const long long left = (long long)s.us[lo + 1] - t.row0;
   t.rows = left < BM ? (int)left : BM;
   return t;
 }
@@ -236,8 +338,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   Smem& s = *reinterpret_cast<Smem*>(base);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int G = p.G;
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&s.full[i], 1);
@@ -260,42 +360,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
   }
 
-  // ---- group table: validate offsets, m-tiles per group, tile prefix
-  for (int g = threadIdx.x; g <= G; g += THREADS) s.goff[g] = p.group_offsets[g];
-  __syncthreads();
-  for (int g = threadIdx.x; g < G; g += THREADS) {
-    const long long lo = s.goff[g], hi = s.goff[g + 1];
-    long long rows = hi - lo;
-    const int e = p.group_expert ? p.group_expert[g] : g;
-    bool bad = lo < 0 || hi < lo || hi > p.A_rows;
-    if (!bad && rows > 0 && (e < 0 || e >= p.E)) bad = true;
-    if (bad) {
-      moe_flag_error(MOE_DEVERR_DATA);
-      rows = 0;
-    }
-    s.mt[g] = (int)((rows + BM - 1) / BM);
-    s.ex[g] = e;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int carry = 0;
-    for (int c0 = 0; c0 < G; c0 += 32) {
-      const int g = c0 + lane;
-      const int v = g < G ? s.mt[g] * p.n_tiles : 0;
-      int incl = v;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += u;
-      }
-      if (g < G) s.tstart[g] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-      s.tstart[G] = carry;
-      s.total_tiles = carry;
-    }
-  }
+  // ---- units (an expert's adjacent groups), their tiles and prefix; experts
+  // below the small-batch threshold are left to the small-batch kernel
+  const int U = build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
+  unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.mt, s.tstart, &s.total_tiles, BM,
+                            [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; });
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -309,7 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode(s, G, tile);
+        const Tile t = decode(s, U, tile);
         const int brow = s.ex[t.g] * p.K;
         const int arow = (int)t.row0;
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -406,7 +475,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int slice = (warp - 2) >> 2;         // column slice 0..EPI_SLICES-1
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode(s, G, tile);
+      const Tile t = decode(s, U, tile);
       // every lane waits; the vote keeps the warp converged for tcgen05.ld
       if (!__all_sync(0xffffffffu, wait_phase(&s.tfull[acc], acc_phase, &s.abort_flag))) break;
       tc_fence_after();

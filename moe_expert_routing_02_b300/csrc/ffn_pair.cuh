@@ -67,10 +67,12 @@ struct Smem {
   uint32_t tmem_base;
   uint32_t abort_flag;
   int32_t total_tiles;
-  int32_t goff[MAX_G + 1];
+  int32_t u_count;
+  int32_t goff[MAX_G + 1];   // staged group offsets
+  int32_t us[MAX_G + 1];     // unit first rows (ffn::build_units)
   int32_t tstart[MAX_G + 1];
   int32_t mt[MAX_G];
-  int32_t ex[MAX_G];
+  int32_t ex[MAX_G];         // unit experts
   alignas(128) uint8_t stg[EPI_WARPS][1024];  // per-warp output staging (store_rows32; 16-byte accesses)
 };
 
@@ -105,8 +107,8 @@ struct Tile {
   long long row0;  // first row of the pair tile
 };
 
-__device__ __forceinline__ Tile decode(const Smem& s, int G, int tile) {
-  int lo = 0, hi = G;  // tstart[lo] <= tile < tstart[hi]
+__device__ __forceinline__ Tile decode(const Smem& s, int U, int tile) {
+  int lo = 0, hi = U;  // tstart[lo] <= tile < tstart[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (s.tstart[mid] <= tile) lo = mid; else hi = mid;
@@ -116,7 +118,7 @@ __device__ __forceinline__ Tile decode(const Smem& s, int G, int tile) {
   const int local = tile - s.tstart[lo];
   const int m = s.mt[lo];
   t.nt = local / m;
-  t.row0 = (long long)s.goff[lo] + (long long)(local % m) * BMP;
+  t.row0 = (long long)s.us[lo] + (long long)(local % m) * BMP;
   return t;
 }
 
@@ -133,7 +135,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
-  const int G = p.G;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -157,42 +158,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tmem_relinquish_pair();
   }
 
-  // ---- group table (identical in both CTAs of the pair)
-  for (int g = threadIdx.x; g <= G; g += THREADS) s.goff[g] = p.group_offsets[g];
-  __syncthreads();
-  for (int g = threadIdx.x; g < G; g += THREADS) {
-    const long long lo = s.goff[g], hi = s.goff[g + 1];
-    long long rows = hi - lo;
-    const int e = p.group_expert ? p.group_expert[g] : g;
-    bool bad = lo < 0 || hi < lo || hi > p.A_rows;
-    if (!bad && rows > 0 && (e < 0 || e >= p.E)) bad = true;
-    if (bad) {
-      if (leader) moe_flag_error(MOE_DEVERR_DATA);
-      rows = 0;
-    }
-    s.mt[g] = (int)((rows + BMP - 1) / BMP);
-    s.ex[g] = e;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int carry = 0;
-    for (int c0 = 0; c0 < G; c0 += 32) {
-      const int g = c0 + lane;
-      const int v = g < G ? s.mt[g] * p.n_tiles : 0;
-      int incl = v;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += u;
-      }
-      if (g < G) s.tstart[g] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-      s.tstart[G] = carry;
-      s.total_tiles = carry;
-    }
-  }
+  // ---- units and their tiles (identical in both CTAs of the pair); experts
+  // below the small-batch threshold are left to the small-batch kernel
+  const int U = ffn::build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
+  ffn::unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.mt, s.tstart, &s.total_tiles, BMP,
+                                 [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; });
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the peer's barriers are initialised before any remote arrive
@@ -209,7 +179,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const CUtensorMap* mB = (EPI == kSwiglu && !leader) ? &tmB1 : &tmB0;
       const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);  // leader's barriers
       for (int tile = pair; tile < total && ok; tile += npairs) {
-        const Tile t = decode(s, G, tile);
+        const Tile t = decode(s, U, tile);
         const int brow = s.ex[t.g] * p.K;
         const int arow = (int)(t.row0 + BM * rank);
         const int n0 = (EPI == kSwiglu) ? t.nt * (BN / 2) : t.nt * BN + (int)rank * (BN / 2);
@@ -295,11 +265,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&s.tempty[0]), 0);
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = pair; tile < total; tile += npairs) {
-      const Tile t = decode(s, G, tile);
+      const Tile t = decode(s, U, tile);
       if (!__all_sync(0xffffffffu, wait_phase<true>(&s.tfull[acc], acc_phase, &s.abort_flag))) break;
       tc_fence_after();
       const long long myrow0 = t.row0 + BM * rank;
-      const long long left = (long long)s.goff[t.g + 1] - myrow0;
+      const long long left = (long long)s.us[t.g + 1] - myrow0;
       const int rows = left <= 0 ? 0 : (left < BM ? (int)left : BM);
       const int wrows = rows - quarter * 32;  // rows of this warp's 32 that belong to the group
       uint16_t* wbase = p.out + (size_t)(myrow0 + quarter * 32) * p.N_out;

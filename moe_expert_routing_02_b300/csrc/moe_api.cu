@@ -19,6 +19,7 @@
 #include "dispatch.cuh"
 #include "ffn.cuh"
 #include "ffn_pair.cuh"
+#include "ffn_small.cuh"
 #include "replicate.cuh"
 #include "route.cuh"
 #include "stats.cuh"
@@ -54,6 +55,7 @@ struct DeviceInfo {
   int num_sms = 0;
   bool ffn_attr[3] = {false, false, false};
   bool pair_attr[3] = {false, false, false};
+  bool small_attr[3] = {false, false, false};
   int pair_clusters[3] = {0, 0, 0};  // max co-resident CTA pairs per pair-kernel instance
 };
 
@@ -350,8 +352,6 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
                           const int32_t* rep_base, int E, int A, const uint16_t* w1, const uint16_t* w3,
                           const uint16_t* w2, int H, int F, moe_act act, int small_group_threshold, uint16_t* y,
                           void* workspace, size_t ws_bytes, void* stream) {
-  (void)rep_base;
-  (void)small_group_threshold;
   if (E < 1 || E > 256 || A < 0) return fail(MOE_ERR_INVALID, "moe_expert_ffn: need 1<=E<=256, A>=0");
   if (H < 64 || H % 64 || F < 64 || F % 64) return fail(MOE_ERR_INVALID, "moe_expert_ffn: H and F must be positive multiples of 64");
   if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) return fail(MOE_ERR_INVALID, "moe_expert_ffn: unknown activation");
@@ -409,11 +409,60 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
   p1.out = inter;
   p1.flags = g_opt_ffn_selftest ? 1 : 0;
   g_opt_ffn_selftest = 0;
+  p1.rep_base = rep_base;
+  p1.small_threshold = small_group_threshold;
   ffn::Params p2 = p1;
   p2.flags = 0;
   p2.K = F;
   p2.N_out = H;
   p2.out = y;
+
+  // small-batch kernels (experts with fewer than small_group_threshold rows)
+  CUtensorMap mS1, mS2;
+  ffn::Params ps1 = p1, ps2 = p2;
+  ps1.flags = 0;
+  ps1.n_tiles = (F + ffn_small::BMF - 1) / ffn_small::BMF;
+  ps2.n_tiles = (H + ffn_small::BMF - 1) / ffn_small::BMF;
+  const bool small_path = small_group_threshold > 0;
+  if (small_path) {
+    if ((ms = encode_2d(&mS1, xp, H, A, 64, ffn_small::BT)) != MOE_OK) return ms;
+    if ((ms = encode_2d(&mS2, inter, F, A, 64, ffn_small::BT)) != MOE_OK) return ms;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < 3; ++i) {
+      if (d->small_attr[i]) continue;
+      const void* fn = i == 0 ? (const void*)ffn_small::small_kernel<ffn::kGelu>
+                     : i == 1 ? (const void*)ffn_small::small_kernel<ffn::kSwiglu>
+                              : (const void*)ffn_small::small_kernel<ffn::kStore>;
+      const int bytes = i == 0 ? (int)ffn_small::smem_bytes<ffn::kGelu>()
+                      : i == 1 ? (int)ffn_small::smem_bytes<ffn::kSwiglu>()
+                               : (int)ffn_small::smem_bytes<ffn::kStore>();
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: cudaFuncSetAttribute (small)");
+      d->small_attr[i] = true;
+    }
+  }
+  const long long small_bound = (long long)G + (long long)A / ffn_small::BT + 1;
+  auto small_grid = [&](const ffn::Params& p) {
+    long long g = small_bound * p.n_tiles;
+    if (g > d->num_sms) g = d->num_sms;
+    return (unsigned)(g < 1 ? 1 : g);
+  };
+  auto launch_small1 = [&]() -> cudaError_t {
+    if (!small_path) return cudaSuccess;
+    if (epi1 == ffn::kSwiglu)
+      ffn_small::small_kernel<ffn::kSwiglu><<<small_grid(ps1), ffn_small::THREADS,
+                                              ffn_small::smem_bytes<ffn::kSwiglu>(), st>>>(mS1, mW1, mW3, ps1);
+    else
+      ffn_small::small_kernel<ffn::kGelu><<<small_grid(ps1), ffn_small::THREADS, ffn_small::smem_bytes<ffn::kGelu>(),
+                                            st>>>(mS1, mW1, mW3, ps1);
+    return cudaGetLastError();
+  };
+  auto launch_small2 = [&]() -> cudaError_t {
+    if (!small_path) return cudaSuccess;
+    ffn_small::small_kernel<ffn::kStore><<<small_grid(ps2), ffn_small::THREADS, ffn_small::smem_bytes<ffn::kStore>(),
+                                           st>>>(mS2, mW2, mW2, ps2);
+    return cudaGetLastError();
+  };
 
   if (use_pair) {
     {
@@ -458,8 +507,10 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
       ffn2::gemm_pair_kernel<ffn::kGelu><<<grid_for(p1, 0), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM1 (pair) launch");
+    if ((e = launch_small1()) != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM1 (small) launch");
     ffn2::gemm_pair_kernel<ffn::kStore><<<grid_for(p2, 2), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
-    return cuda_status(cudaGetLastError(), "moe_expert_ffn: GEMM2 (pair) launch");
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM2 (pair) launch");
+    return cuda_status(launch_small2(), "moe_expert_ffn: GEMM2 (small) launch");
   }
 
   {
@@ -488,8 +539,10 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
     ffn::gemm_kernel<ffn::kGelu><<<grid_for(p1), ffn::THREADS, ffn::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM1 launch");
+  if ((e = launch_small1()) != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM1 (small) launch");
   ffn::gemm_kernel<ffn::kStore><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
-  return cuda_status(cudaGetLastError(), "moe_expert_ffn: GEMM2 launch");
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM2 launch");
+  return cuda_status(launch_small2(), "moe_expert_ffn: GEMM2 (small) launch");
 }
 
 // ------------------------------------------------------------------ options

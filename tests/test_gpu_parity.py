@@ -359,6 +359,57 @@ def test_ffn_ragged_groups_and_partial_tiles(ffn_kernel):
             assert rel_fro(got[lo:hi], ref[lo:hi]) <= FFN_TOL
 
 
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("thresh", [0, 64, 1 << 30])
+@pytest.mark.parametrize("ffn_kernel", ["single", "pair"], indirect=True)
+def test_ffn_small_batch_path_thresholds(thresh, act, ffn_kernel):
+    """Experts below small_group_threshold rows take the swap-AB small-batch
+    kernel, the rest the grouped kernel: threshold 0 = grouped only, 64 = the
+    default split, 2^30 = everything small (groups above 64 rows are then
+    split into 64-token chunks).  Every group is checked against the oracle."""
+    import dataclasses
+    sizes = [0, 1, 15, 16, 17, 63, 64, 65, 127, 200, 300]
+    c = dataclasses.replace(W.config_by_name("tiny"), name="small-path", E=len(sizes), k=1, H=192, F=320, act=act)
+    idx = np.concatenate([np.full(n, e, np.int32) for e, n in enumerate(sizes)])
+    np.random.default_rng(1).shuffle(idx)
+    idx = idx.reshape(-1, 1)
+    x = W.make_x(c, 0, 0, device="cuda", T=idx.shape[0])
+    w1, w3, w2 = _weights(c)
+    go, perm, inv, xp = M.moe_dispatch(x, dev(idx), c.E)
+    y = M.moe_expert_ffn(xp, go, None, None, w1, w3, w2, act, small_group_threshold=thresh)
+    ok_check()
+    ref = O.expert_ffn(W.bf16_bits(xp), host(go)[:c.E + 1], None, W.bf16_bits(w1),
+                       None if w3 is None else W.bf16_bits(w3), W.bf16_bits(w2), act)
+    got = O.bf16_to_f64(W.bf16_bits(y))
+    gof = host(go)
+    for g in range(c.E):
+        lo, hi = gof[g], gof[g + 1]
+        if hi > lo:
+            assert rel_fro(got[lo:hi], ref[lo:hi]) <= FFN_TOL, (g, sizes[g])
+
+
+def test_replication_bit_identical_with_small_experts():
+    """The tiny workload has both hot experts (replicated) and experts below 64
+    rows (small-batch kernel): outputs with and without replication match
+    bit for bit."""
+    c = W.config_by_name("tiny")
+    lg = W.make_layer_logits(c, 0, layers=1)[0]
+    x = W.make_x(c, 0, 0, device="cuda")
+    w1, w3, w2 = _weights(c)
+    idx, w = M.moe_route(dev(lg), c.k)
+    h = torch.bincount(idx.reshape(-1).long(), minlength=c.E).to(torch.int32)
+    copies, rb, ge = M.moe_replicate(h, idx.numel())
+    hh = host(h)
+    assert int(host(rb)[-1]) > c.E and (hh < 64).any() and (hh > 0).any()
+    outs = []
+    for use_rep in (False, True):
+        go, perm, inv, xp = M.moe_dispatch(x, idx, c.E, rb if use_rep else None)
+        y = M.moe_expert_ffn(xp, go, ge if use_rep else None, rb if use_rep else None, w1, w3, w2, c.act)
+        outs.append(M.moe_combine(y, inv, w))
+    ok_check()
+    assert torch.equal(outs[0], outs[1])
+
+
 def _rne_bf16(v):
     u = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
     return ((u + ((u >> 16) & 1) + 0x7FFF) >> 16).astype(np.uint16)
