@@ -53,6 +53,8 @@ def parse_args(argv=None):
     ap.add_argument("--config", default="moe_gpt_stream")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch every call from Python instead of graph replay")
+    ap.add_argument("--unfused", action="store_true",
+                    help="make the five separate front calls instead of moe_layer_front")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (tokens of one layer)")
     ap.add_argument("--layers", type=int, default=0,
@@ -174,7 +176,7 @@ def algorithmic_work(c, used_experts=None):
     T, E, k, H, F, A = c.T, c.E, c.k, c.H, c.F, c.A
     ngemm = 3 if c.act == "swiglu" else 2
     Eu = E if used_experts is None else used_experts
-    return {
+    work = {
         "route": {"bytes": T * E * 4 + A * 8},
         "stats": {"bytes": 2 * A * 4 + (E + E * E) * 4 * 2 + (E + E * E) * 8 * 2},
         "predict": {"bytes": E * E * 8 + E * 8 + E * E * 4 + E * 8},
@@ -184,6 +186,9 @@ def algorithmic_work(c, used_experts=None):
                 "bytes": int(ngemm * Eu * H * F * 2 + A * H * 2 * 2 + (ngemm - 1) * A * F * 2 * 2)},
         "combine": {"bytes": A * H * 2 + A * 8 + T * H * 2},
     }
+    # the fused front does the work of the five calls it replaces
+    work["front"] = {"bytes": sum(work[s]["bytes"] for s in ("route", "stats", "predict", "replicate", "dispatch"))}
+    return work
 
 
 def load_peaks():
@@ -240,14 +245,17 @@ def run_ours(args, rank, world, local):
     weights = [W.make_weights(c, j, device=dev) for j in range(c.L)]
     outs = [torch.empty((c.T, c.H), dtype=torch.bfloat16, device=dev) for _ in range(c.L)]
     stats = M.MoEStats(c.L, c.E, c.window)
-    step = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, stats=stats, replicate=True, device=dev)
+    step = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, stats=stats, replicate=True, fused=not args.unfused,
+                        device=dev)
+    stage_names = ["front", "ffn", "combine"] if step.fused else STAGES
 
     def run_step(it, ev=None):
         for j in range(c.L):
             step.run(it, j, logits[it % POOL][j], xs[j], weights[j], outs[j],
                      events=None if ev is None else ev[j])
 
-    def new_events(names=STAGES):
+    def new_events(names=None):
+        names = stage_names if names is None else names
         # external=True: inside a captured graph the records become event nodes
         # whose timestamps are readable after a replay
         return [{s: (torch.cuda.Event(enable_timing=True, external=True),
@@ -315,7 +323,8 @@ def run_ours(args, rank, world, local):
     units = c.T * c.L * K
     value = whole_job_value(units, world, elapsed_max)
 
-    def stage_means(sets, names=STAGES):
+    def stage_means(sets, names=None):
+        names = stage_names if names is None else names
         out = {}
         for sname in names:
             ts = [ev[j][sname][0].elapsed_time(ev[j][sname][1]) for ev in sets for j in range(c.L)
@@ -329,7 +338,7 @@ def run_ours(args, rank, world, local):
         replayed = sorted({(args.warmup + s_i) % n_graphs for s_i in range(K)})
         ffn_ms = stage_means([graph_ev[q] for q in replayed], ["ffn"])["ffn"]
         # stage breakdown: instrumented graphs replayed once per slot afterwards
-        graphs_all, ev_all = capture(STAGES)
+        graphs_all, ev_all = capture(stage_names)
         for q in range(n_graphs):
             graphs_all[q].replay()
         torch.cuda.synchronize()
@@ -344,7 +353,7 @@ def run_ours(args, rank, world, local):
     work = algorithmic_work(c, used_experts=used)
     peaks = load_peaks()
     stages = {}
-    for sname in STAGES:
+    for sname in stage_names:
         if sname not in stage_ms:
             continue
         t = stage_ms[sname] / 1e3
@@ -386,6 +395,7 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world} (no data exchange)",
                    "l2": "no flush: each step streams ~1.5 GB of weights + activations, >> 126 MB L2",
                    "launch": "eager" if args.eager else f"CUDA graph per step ({c.window} graphs, one per window slot)",
+                   "front": "separate calls" if args.unfused else "moe_layer_front (2 launches)",
                    "stage_timing": "CUDA events around each stage, every layer of every timed step" if args.eager
                    else "FFN: events captured around it in the timed graphs (last replay of each); other stages: "
                         "a second set of graphs with events around every stage, replayed once per slot after the "

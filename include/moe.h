@@ -69,7 +69,7 @@ typedef enum {
 
 typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
 
-typedef enum { MOE_OP_DISPATCH = 1, MOE_OP_EXPERT_FFN = 2 } moe_op;
+typedef enum { MOE_OP_DISPATCH = 1, MOE_OP_EXPERT_FFN = 2, MOE_OP_LAYER_FRONT = 3 } moe_op;
 
 /* Opaque window state: device ring buffers of per-layer histograms and
  * per-layer-pair co-selection counts, plus running window sums. */
@@ -180,6 +180,33 @@ moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int
                         const int32_t* rep_base, int32_t* group_offsets, int32_t* perm,
                         int32_t* inv_perm, uint16_t* xp, void* workspace, size_t ws_bytes,
                         void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_layer_front -- route, statistics, prediction, replicas and dispatch of one
+ * layer in two launches.
+ * The same results, bit for bit, as
+ *   moe_route(logits) -> moe_stats_update(st, iter, layer, idx, idx_prev) ->
+ *   moe_predict(st, layer) [when p_seq != NULL] -> moe_replicate(hist, T*k)
+ *   [when replicate != 0] -> moe_dispatch(x, idx, rep_base or NULL)
+ * (passages as for those calls), with the arguments of those calls:
+ *   logits [T,E] f32, x [T,H] bf16 (NULL with xp = NULL: permutation only),
+ *   renorm, st / iter / layer / idx_prev (NULL for layer 0), replicate and its
+ *   thresh_num / thresh_den / max_copies, and the outputs idx, w, hist_out
+ *   (nullable), p_seq / cond / p_next (nullable; cond and p_next NULL for the
+ *   last layer), copies / rep_base / group_expert (required when replicating),
+ *   group_offsets [2E+1], perm, inv_perm, xp.
+ *   workspace  ws_bytes >= moe_workspace_bytes(MOE_OP_LAYER_FRONT, T, k, E, H, 0),
+ *              16-byte aligned
+ * The first launch routes tiles of tokens and counts them; its last block
+ * folds the window, predicts, replicates and lays out the groups; the second
+ * scatters the permutation and copies the rows.  E must equal the handle's E.
+ * ------------------------------------------------------------------------- */
+moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E, int k, int H, int renorm,
+                           moe_stats* st, int64_t iter, int layer, const int32_t* idx_prev, int replicate,
+                           int thresh_num, int thresh_den, int max_copies, int32_t* idx, float* w,
+                           int32_t* hist_out, float* p_seq, float* cond, float* p_next, int32_t* copies,
+                           int32_t* rep_base, int32_t* group_expert, int32_t* group_offsets, int32_t* perm,
+                           int32_t* inv_perm, uint16_t* xp, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * moe_expert_ffn -- grouped expert FFN over the dispatched rows.

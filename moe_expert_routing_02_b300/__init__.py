@@ -18,7 +18,7 @@ from typing import Optional
 
 __all__ = [
     "MoEError", "lib", "library_path", "MoEStats", "moe_route", "moe_stats_update", "moe_predict",
-    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_check", "moe_error_word",
+    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_layer_front", "moe_expert_ffn", "moe_combine", "moe_check", "moe_error_word",
     "workspace_bytes", "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_ACT_GELU", "MOE_ACT_SWIGLU",
     "EXPORTED_SYMBOLS", "moe_set_option", "moe_get_option", "MOE_OPT_FFN_KERNEL", "MOE_FFN_KERNEL_AUTO",
     "MOE_FFN_KERNEL_SINGLE", "MOE_FFN_KERNEL_PAIR", "MOE_OPT_FFN_TIMEOUT_SELFTEST",
@@ -29,7 +29,7 @@ library_path = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_WORKSPACE, MOE_ERR_DEVICE = range(7)
 MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
-MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN = 1, 2
+MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT = 1, 2, 3
 MOE_OPT_FFN_KERNEL, MOE_OPT_FFN_TIMEOUT_SELFTEST = 1, 2
 MOE_FFN_KERNEL_AUTO, MOE_FFN_KERNEL_SINGLE, MOE_FFN_KERNEL_PAIR = 0, 1, 2
 
@@ -60,6 +60,8 @@ _SIGS = {
     "moe_stats_import": (_I, [_P, _P, _SZ]),
     "moe_version": (ctypes.c_char_p, []),
     "moe_set_option": (_I, [_I, _I]),
+    "moe_layer_front": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _I64, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                             _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_get_option": (_I, [_I, ctypes.POINTER(_I)]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -312,6 +314,57 @@ def moe_dispatch_noalloc(x, idx, E: int, rep_base=None, out=None, stream=None):
     _check(lib().moe_dispatch_noalloc(_ptr(x), _ptr(idx), T, k, H, E, _ptr(rep_base), _ptr(go), _ptr(perm),
                                       _ptr(inv), _ptr(xp), _stream(stream)), "moe_dispatch_noalloc")
     return go, perm, inv, xp
+
+
+def moe_layer_front(logits, x, stats: "MoEStats", it: int, layer: int, k: int, idx_prev=None, renorm: bool = True,
+                    predict: bool = True, replicate: bool = True, thresh=(6, 5), max_copies: int = -1, out=None,
+                    workspace=None, stream=None):
+    """Route + stats update + predict + replicate + dispatch of one layer in two
+    launches (results identical to the separate calls).  Returns a dict of the
+    outputs: idx, w, hist, p_seq, cond, p_next, copies, rep_base, group_expert,
+    group_offsets, perm, inv_perm, xp (absent ones None).  `out` may hold
+    preallocated tensors under those names."""
+    torch = _torch()
+    _dev(logits, torch.float32, "logits", 2)
+    T, E = logits.shape
+    dev = logits.device
+    H = 8
+    if x is not None:
+        _dev(x, torch.bfloat16, "x", 2)
+        H = x.shape[1]
+    if idx_prev is not None:
+        _dev(idx_prev, torch.int32, "idx_prev", 2)
+    last = layer == stats.L - 1
+    o = dict(out or {})
+    i32, f32 = torch.int32, torch.float32
+    def need(name, shape, dtype, cond=True):
+        if cond and o.get(name) is None:
+            o[name] = torch.empty(shape, dtype=dtype, device=dev)
+        return o.get(name) if cond else None
+    idx = need("idx", (T, k), i32)
+    w = need("w", (T, k), f32)
+    hist = need("hist", (E,), i32)
+    p_seq = need("p_seq", (E,), f32, predict)
+    cond = need("cond", (E, E), f32, predict and not last)
+    p_next = need("p_next", (E,), f32, predict and not last)
+    copies = need("copies", (E,), i32, replicate)
+    rep_base = need("rep_base", (E + 1,), i32, replicate)
+    group_expert = need("group_expert", (2 * E,), i32, replicate)
+    go = need("group_offsets", (2 * E + 1,), i32)
+    perm = need("perm", (T * k,), i32)
+    inv = need("inv_perm", (T * k,), i32)
+    xp = need("xp", (T * k, H), torch.bfloat16, x is not None)
+    if workspace is None:
+        workspace = torch.empty(max(workspace_bytes(MOE_OP_LAYER_FRONT, T, k, E), 16), dtype=torch.uint8, device=dev)
+    _check(lib().moe_layer_front(_ptr(logits), _ptr(x), T, E, k, H, int(bool(renorm)), stats.handle, int(it),
+                                 int(layer), _ptr(idx_prev), int(bool(replicate)), int(thresh[0]), int(thresh[1]),
+                                 int(max_copies), _ptr(idx), _ptr(w), _ptr(hist), _ptr(p_seq), _ptr(cond),
+                                 _ptr(p_next), _ptr(copies), _ptr(rep_base), _ptr(group_expert), _ptr(go),
+                                 _ptr(perm), _ptr(inv), _ptr(xp), _ptr(workspace), workspace.numel(),
+                                 _stream(stream)), "moe_layer_front")
+    return {"idx": idx, "w": w, "hist": hist, "p_seq": p_seq, "cond": cond, "p_next": p_next, "copies": copies,
+            "rep_base": rep_base, "group_expert": group_expert, "group_offsets": go, "perm": perm,
+            "inv_perm": inv, "xp": xp}
 
 
 def moe_expert_ffn(xp, group_offsets, group_expert, rep_base, w1, w3, w2, act: str = "gelu",

@@ -338,6 +338,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   Smem& s = *reinterpret_cast<Smem*>(base);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // ---- units (an expert's adjacent groups), their tiles and prefix; experts
+  // below the small-batch threshold are left to the small-batch kernel
+  const int U = build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
+  unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.mt, s.tstart, &s.total_tiles, BM,
+                            [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; });
+  __syncthreads();
+  if (s.total_tiles == 0) return;  // no tiles: exit before any barrier or TMEM set-up
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&s.full[i], 1);
@@ -360,11 +367,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
   }
 
-  // ---- units (an expert's adjacent groups), their tiles and prefix; experts
-  // below the small-batch threshold are left to the small-batch kernel
-  const int U = build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
-  unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.mt, s.tstart, &s.total_tiles, BM,
-                            [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; });
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

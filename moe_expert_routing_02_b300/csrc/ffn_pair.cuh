@@ -136,6 +136,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
 
+  // ---- units and their tiles (identical in both CTAs of the pair); experts
+  // below the small-batch threshold are left to the small-batch kernel
+  const int U = ffn::build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
+  ffn::unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.mt, s.tstart, &s.total_tiles, BMP,
+                                 [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; });
+  __syncthreads();
+  if (s.total_tiles == 0) return;  // no tiles: exit before any barrier or TMEM set-up
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&s.full[i], 1);
@@ -158,11 +165,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tmem_relinquish_pair();
   }
 
-  // ---- units and their tiles (identical in both CTAs of the pair); experts
-  // below the small-batch threshold are left to the small-batch kernel
-  const int U = ffn::build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
-  ffn::unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.mt, s.tstart, &s.total_tiles, BMP,
-                                 [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; });
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the peer's barriers are initialised before any remote arrive

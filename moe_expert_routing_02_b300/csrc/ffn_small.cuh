@@ -125,6 +125,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // ---- units (an expert's adjacent groups) with fewer than small_threshold
+  // rows, in 64-token chunks
+  const int U = ffn::build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
+  ffn::unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.nchunk, s.tstart, &s.total_tiles, BT,
+                                 [&](int rows) { return rows < p.small_threshold; });
+  __syncthreads();
+  if (s.total_tiles == 0) return;  // no tiles: exit before any barrier or TMEM set-up
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(&s.full[i], 1);
@@ -147,11 +154,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
   }
 
-  // ---- units (an expert's adjacent groups) with fewer than small_threshold
-  // rows, in 64-token chunks
-  const int U = ffn::build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
-  ffn::unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.nchunk, s.tstart, &s.total_tiles, BT,
-                                 [&](int rows) { return rows < p.small_threshold; });
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

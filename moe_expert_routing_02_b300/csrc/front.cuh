@@ -1,0 +1,378 @@
+// Fused front of the layer: top-k gate, token statistics and window, next-layer
+// prediction, replica counts and the dispatch, in two launches.
+//
+// Same results as moe_route -> moe_stats_update -> moe_predict ->
+// moe_replicate -> moe_dispatch (PopFetcher review: gate, Routing Information
+// Collector with Eq. (1)-(3); MoE-GPS blog section 2.1 duplicate_experts;
+// MoE-MPMC summary, replica dispatch), with five fewer launches:
+//
+//   F1 (route_count_kernel), one block per TT_BLOCK tokens:
+//      top-k of each token (route::topk_token), idx / w written; per tile of
+//      TT tokens the expert counts (shared atomics -> counts[tile][E]); the
+//      co-selection pairs with the previous layer's routing (shared atomics,
+//      flushed to the window state's accumulator).  The last block to finish
+//      (ticket after a fence) then, alone:
+//        - scans the tile counts per expert (tile starting ranks, histogram),
+//        - folds histogram and co-selection counts into the window ring and
+//          sums (as stats::update_kernel does),
+//        - predicts the next layer (stats::predict_block),
+//        - computes replica counts (replicate::replicate_block),
+//        - lays out the groups (closed form of the round-robin split).
+//   F2 (scatter_copy_kernel), one block per tile: stable in-tile ranks ->
+//      slots -> perm / inv_perm, then the rows of the tile's assignments are
+//      copied to their slots with 16-byte vectors.
+// Counts are integers, so nothing depends on the order of atomics.
+#pragma once
+#include "common.cuh"
+#include "dispatch.cuh"
+#include "replicate.cuh"
+#include "route.cuh"
+#include "stats.cuh"
+
+namespace front {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kSmemCoselMaxE = 64;
+
+// Tokens per dispatch tile, from T alone (so workspace sizes need no device):
+// the smallest power of two in [16, 128] giving at most 512 tiles.
+__host__ __device__ inline int tile_tokens(long long T) {
+  int tt = 16;
+  while (tt < 128 && (T + tt - 1) / tt > 512) tt <<= 1;
+  return tt;
+}
+__host__ inline long long num_tiles(long long T) { return (T + tile_tokens(T) - 1) / tile_tokens(T); }
+__host__ inline size_t workspace_bytes(long long T, int E) {
+  const long long nt = num_tiles(T) > 0 ? num_tiles(T) : 1;
+  return (size_t)(nt * E + 4LL * E) * sizeof(int32_t);
+}
+
+struct Args {
+  // route
+  const float* logits;
+  int T, E, k, renorm;
+  int32_t* idx;
+  float* w;
+  // window update (pointers into the stats handle for this layer / pair)
+  int has_prev;
+  const int32_t* idx_prev;
+  uint32_t* acc_c;
+  uint32_t* ticket;
+  uint32_t* ring_h;
+  unsigned long long* hsum;
+  uint32_t* ring_c;
+  unsigned long long* csum;
+  int32_t* hist_out;
+  // prediction (p_seq == null: skipped); pred_csum null for the last layer
+  const unsigned long long* pred_csum;
+  float* p_seq;
+  float* cond;
+  float* p_next;
+  // replication
+  int replicate, num, den, max_copies;
+  int32_t* copies;
+  int32_t* rep_base;
+  int32_t* group_expert;
+  // dispatch
+  int TT;            // tokens per tile
+  int tiles_per_block;
+  long long ntiles;
+  int32_t* counts;   // [ntiles][E]: tile counts, then tile starting ranks
+  int32_t* info;     // [4][E]: expert base, replicas, rows, -
+  int32_t* group_offsets;
+};
+
+template <int G, bool VEC>
+__global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
+  extern __shared__ uint32_t dsm[];  // cnt[tiles_per_block][E], then cosel[E*E] (small E)
+  constexpr int TPW = 32 / G;
+  const int E = a.E, k = a.k;
+  const bool cos = a.has_prev != 0;
+  const bool cos_smem = cos && E <= kSmemCoselMaxE;
+  const int tpb = a.tiles_per_block;
+  uint32_t* cnt = dsm;
+  uint32_t* cs = dsm + tpb * E;
+  const int nsh = tpb * E + (cos_smem ? E * E : 0);
+  for (int i = threadIdx.x; i < nsh; i += kThreads) dsm[i] = 0;
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gl = lane % G;
+  const long long tb0 = (long long)blockIdx.x * tpb * a.TT;  // first token of the block
+  long long tb1 = tb0 + (long long)tpb * a.TT;
+  if (tb1 > a.T) tb1 = a.T;
+  bool bad = false;
+  for (long long t0 = tb0 + (long long)warp * TPW; t0 < tb1; t0 += (long long)kWarps * TPW) {
+    const long long t = t0 + lane / G;
+    const bool live = t < tb1;
+    float sel_v[8], denom;
+    int sel_i[8];
+    route::topk_token<G, VEC>(a.logits + (size_t)(live ? t : 0) * E, live, E, k, a.renorm, sel_v, sel_i, &denom);
+    if (live) {
+      route::write_token<G>(t, k, sel_v, sel_i, denom, a.idx, a.w);
+      if (gl == 0) {
+        uint32_t* c = cnt + (int)((t - tb0) / a.TT) * E;
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r < k) atomicAdd(c + sel_i[r], 1u);
+        if (cos) {
+#pragma unroll
+          for (int r1 = 0; r1 < 8; ++r1) {
+            if (r1 < k) {
+              const int pe = a.idx_prev[t * k + r1];
+              if ((unsigned)pe >= (unsigned)E) {
+                bad = true;
+                continue;
+              }
+#pragma unroll
+              for (int r2 = 0; r2 < 8; ++r2) {
+                if (r2 < k) {
+                  const int bin = pe * E + sel_i[r2];
+                  if (cos_smem)
+                    atomicAdd(cs + bin, 1u);
+                  else
+                    atomicAdd(a.acc_c + bin, 1u);
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  if (bad) moe_flag_error(MOE_DEVERR_DATA);
+  __syncthreads();
+  // tile counts (each tile row written in full by its block)
+  const long long tile0 = (long long)blockIdx.x * tpb;
+  for (int i = threadIdx.x; i < tpb * E; i += kThreads) {
+    const long long tile = tile0 + i / E;
+    if (tile < a.ntiles) a.counts[tile * E + (i % E)] = (int32_t)cnt[i];
+  }
+  if (cos_smem)
+    for (int i = threadIdx.x; i < E * E; i += kThreads)
+      if (cs[i]) atomicAdd(a.acc_c + i, cs[i]);
+
+  // ---- the last block plans the layer
+  __shared__ bool is_last;
+  __shared__ int32_t hist_s[256];
+  __shared__ int32_t wtot[kWarps];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  const int e = threadIdx.x;
+  // per-expert exclusive scan over tiles: tile starting ranks and the histogram
+  int h = 0;
+  if (e < E) {
+    long long b = 0;
+    for (; b + 8 <= a.ntiles; b += 8) {
+      int c[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) c[u] = a.counts[(b + u) * E + e];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        a.counts[(b + u) * E + e] = h;
+        h += c[u];
+      }
+    }
+    for (; b < a.ntiles; ++b) {
+      const int c = a.counts[b * E + e];
+      a.counts[b * E + e] = h;
+      h += c;
+    }
+    hist_s[e] = h;
+    // window: histogram slot and sums
+    const uint32_t old = a.ring_h[e];
+    a.ring_h[e] = (uint32_t)h;
+    a.hsum[e] = a.hsum[e] + (uint32_t)h - old;
+    if (a.hist_out) a.hist_out[e] = h;
+  }
+  if (cos) {
+    for (int i = threadIdx.x; i < E * E; i += kThreads) {
+      const uint32_t nw = atomicExch(a.acc_c + i, 0u);
+      const uint32_t old = a.ring_c[i];
+      a.ring_c[i] = nw;
+      a.csum[i] = a.csum[i] + nw - old;
+    }
+  }
+  __syncthreads();
+  if (a.p_seq) stats::predict_block(a.hsum, a.pred_csum, E, a.p_seq, a.cond, a.p_next);
+  __syncthreads();
+  const long long A = (long long)a.T * k;
+  if (a.replicate)
+    replicate::replicate_block(hist_s, E, A, a.num, a.den, a.max_copies, a.copies, a.rep_base, a.group_expert);
+  __syncthreads();
+  // group layout: expert bases (exclusive scan of the histogram), replicas,
+  // group offsets in the closed form of the round-robin split
+  const int lane2 = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = e < E ? hist_s[e] : 0;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane2 >= off) incl += v;
+  }
+  if (lane2 == 31) wtot[wid] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int ww = 0; ww < wid; ++ww) before += wtot[ww];
+  const int ngroups = a.replicate ? a.rep_base[E] : E;
+  if (e < E) {
+    const int hh = hist_s[e];
+    const int base = before + incl - hh;
+    int n = 1, rb = e;
+    if (a.replicate) {
+      rb = a.rep_base[e];
+      n = a.rep_base[e + 1] - rb;
+    }
+    a.info[e] = base;
+    a.info[E + e] = n;
+    a.info[2 * E + e] = hh;
+    const int qs = hh / n, qr = hh % n;
+    for (int q = 0; q < n; ++q) a.group_offsets[rb + q] = base + q * qs + (q < qr ? q : qr);
+  }
+  for (int g = ngroups + threadIdx.x; g <= 2 * E; g += kThreads) a.group_offsets[g] = (int32_t)A;
+  if (threadIdx.x == 0) *a.ticket = 0;
+}
+
+// One block per tile: stable ranks of the tile's assignments (in f order),
+// slots, perm / inv_perm, then the row copy xp[slot] = x[f / k].
+__global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const int32_t* __restrict__ idx, long long T, int k,
+                                                                int E, int TT, const int32_t* __restrict__ tile_base,
+                                                                const int32_t* __restrict__ info,
+                                                                int32_t* __restrict__ perm,
+                                                                int32_t* __restrict__ inv_perm,
+                                                                const uint16_t* __restrict__ x, int H,
+                                                                uint16_t* __restrict__ xp) {
+  extern __shared__ int32_t sm[];
+  int32_t* warp_cnt = sm;                 // [kWarps][E]
+  int32_t* run = sm + kWarps * E;         // [E]
+  int32_t* slot_s = run + E;              // [TT*k]
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const long long A = T * k;
+  const long long f0 = (long long)blockIdx.x * TT * k;
+  long long f1 = f0 + (long long)TT * k;
+  if (f1 > A) f1 = A;
+  const int nA = (int)(f1 - f0);
+  for (int i = tid; i < kWarps * E; i += kThreads) warp_cnt[i] = 0;
+  for (int i = tid; i < E; i += kThreads) run[i] = tile_base[(size_t)blockIdx.x * E + i];
+  __syncthreads();
+  for (int r0 = 0; r0 < nA; r0 += kThreads) {
+    const int i = r0 + tid;
+    int e = -1;
+    if (i < nA) {
+      e = idx[f0 + i];
+      if ((unsigned)e >= (unsigned)E) e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) warp_cnt[wid * E + e] = __popc(peers);
+    __syncthreads();
+    int slot = -1;
+    if (e >= 0) {
+      int m = run[e] + __popc(peers & lanemask_lt());
+      for (int w = 0; w < wid; ++w) m += warp_cnt[w * E + e];
+      const int base = info[e], n = info[E + e], h = info[2 * E + e];
+      const int q = m % n, pos = m / n, qs = h / n, qr = h % n;
+      slot = base + q * qs + (q < qr ? q : qr) + pos;
+      if ((unsigned long long)slot < (unsigned long long)A) {
+        perm[slot] = (int32_t)(f0 + i);
+        inv_perm[f0 + i] = slot;
+      } else {
+        slot = -1;
+      }
+    }
+    if (i < nA) slot_s[i] = slot;
+    __syncthreads();
+    for (int j = tid; j < E; j += kThreads) {
+      int s2 = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        s2 += warp_cnt[w * E + j];
+        warp_cnt[w * E + j] = 0;
+      }
+      run[j] += s2;
+    }
+    __syncthreads();
+  }
+  if (x == nullptr) return;
+  // rows: one warp per assignment, 16-byte chunks
+  const int chunks = H / 8;
+  for (int i = wid; i < nA; i += kWarps) {
+    const int slot = slot_s[i];
+    if (slot < 0) continue;
+    const uint16_t* src = x + ((f0 + i) / k) * H;
+    uint16_t* dst = xp + (size_t)slot * H;
+    int c = lane;
+    for (; c + 96 < chunks; c += 128) {
+      const uint4 v0 = ld_nc_v4(src + (size_t)c * 8);
+      const uint4 v1 = ld_nc_v4(src + (size_t)(c + 32) * 8);
+      const uint4 v2 = ld_nc_v4(src + (size_t)(c + 64) * 8);
+      const uint4 v3 = ld_nc_v4(src + (size_t)(c + 96) * 8);
+      st_v4(dst + (size_t)c * 8, v0);
+      st_v4(dst + (size_t)(c + 32) * 8, v1);
+      st_v4(dst + (size_t)(c + 64) * 8, v2);
+      st_v4(dst + (size_t)(c + 96) * 8, v3);
+    }
+    for (; c < chunks; c += 32) st_v4(dst + (size_t)c * 8, ld_nc_v4(src + (size_t)c * 8));
+  }
+}
+
+// Dynamic shared memory of route_count_kernel stays below 17 KB (tile counts
+// plus, for E <= 64, the E*E co-selection bins); with the block-level static
+// arrays of the plan phase it passes 48 KB, so the limit is raised once per
+// device and kernel instance.
+constexpr int kRouteDynSmemMax = 20 * 1024;
+
+template <typename K>
+static cudaError_t ensure_smem_attr(K kernel, bool* done_per_device) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done_per_device[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteDynSmemMax);
+  if (e == cudaSuccess) done_per_device[dev] = true;
+  return e;
+}
+
+template <int G>
+static cudaError_t launch_route_g(const Args& a, bool vec, cudaStream_t st) {
+  static bool done_vec[64] = {}, done_scalar[64] = {};
+  const int tokens_per_pass = kWarps * (32 / G);
+  Args b = a;
+  b.tiles_per_block = tokens_per_pass >= a.TT ? tokens_per_pass / a.TT : 1;
+  const long long tokens_per_block = (long long)b.tiles_per_block * a.TT;
+  const long long blocks = (a.T + tokens_per_block - 1) / tokens_per_block;
+  const bool cos_smem = a.has_prev && a.E <= kSmemCoselMaxE;
+  const size_t smem = sizeof(uint32_t) * ((size_t)b.tiles_per_block * a.E + (cos_smem ? (size_t)a.E * a.E : 0));
+  if (smem > (size_t)kRouteDynSmemMax) return cudaErrorInvalidValue;
+  if (vec) {
+    cudaError_t e = ensure_smem_attr(route_count_kernel<G, true>, done_vec);
+    if (e != cudaSuccess) return e;
+    route_count_kernel<G, true><<<(unsigned)blocks, kThreads, smem, st>>>(b);
+  } else {
+    cudaError_t e = ensure_smem_attr(route_count_kernel<G, false>, done_scalar);
+    if (e != cudaSuccess) return e;
+    route_count_kernel<G, false><<<(unsigned)blocks, kThreads, smem, st>>>(b);
+  }
+  return cudaGetLastError();
+}
+
+static cudaError_t launch(const Args& a, const uint16_t* x, int H, uint16_t* xp, int32_t* perm, int32_t* inv_perm,
+                          cudaStream_t st) {
+  const bool vec = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.logits) & 15) == 0);
+  cudaError_t e;
+  if (a.E <= 8) e = launch_route_g<1>(a, vec, st);
+  else if (a.E <= 16) e = launch_route_g<2>(a, vec, st);
+  else if (a.E <= 32) e = launch_route_g<4>(a, vec, st);
+  else if (a.E <= 64) e = launch_route_g<8>(a, vec, st);
+  else if (a.E <= 128) e = launch_route_g<16>(a, vec, st);
+  else e = launch_route_g<32>(a, vec, st);
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(int32_t) * ((size_t)(kWarps + 1) * a.E + (size_t)a.TT * a.k);
+  scatter_copy_kernel<<<(unsigned)a.ntiles, kThreads, smem, st>>>(a.idx, a.T, a.k, a.E, a.TT, a.counts, a.info, perm,
+                                                                  inv_perm, x, H, xp);
+  return cudaGetLastError();
+}
+
+}  // namespace front

@@ -17,6 +17,7 @@
 #include "combine.cuh"
 #include "common.cuh"
 #include "dispatch.cuh"
+#include "front.cuh"
 #include "ffn.cuh"
 #include "ffn_pair.cuh"
 #include "ffn_small.cuh"
@@ -163,6 +164,7 @@ size_t moe_workspace_bytes(int op, int T, int k, int E, int H, int F) {
   if (T < 0 || k < 1 || k > 8 || E < 1 || E > 256) return 0;
   const long long A = (long long)T * k;
   if (op == MOE_OP_DISPATCH) return dispatch::workspace_bytes(A, E);
+  if (op == MOE_OP_LAYER_FRONT) return front::workspace_bytes(T, E);
   if (op == MOE_OP_EXPERT_FFN) {
     if (F < 64 || F % 64 || H < 64 || H % 64) return 0;
     return ffn_workspace_bytes(A, F);
@@ -345,6 +347,90 @@ moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int
   if (ms != MOE_OK) return ms;
   dispatch::Args a{x, idx, (long long)T, k, H, E, rep_base, group_offsets, perm, inv_perm, xp, workspace};
   return cuda_status(dispatch::launch(a, d->num_sms, static_cast<cudaStream_t>(stream)), "moe_dispatch launch");
+}
+
+// ------------------------------------------------------------------ fused front
+moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E, int k, int H, int renorm,
+                           moe_stats* st, int64_t iter, int layer, const int32_t* idx_prev, int replicate,
+                           int thresh_num, int thresh_den, int max_copies, int32_t* idx, float* w,
+                           int32_t* hist_out, float* p_seq, float* cond, float* p_next, int32_t* copies,
+                           int32_t* rep_base, int32_t* group_expert, int32_t* group_offsets, int32_t* perm,
+                           int32_t* inv_perm, uint16_t* xp, void* workspace, size_t ws_bytes, void* stream) {
+  if (!st) return fail(MOE_ERR_INVALID, "moe_layer_front: null stats handle");
+  if (E != st->E) return fail(MOE_ERR_INVALID, "moe_layer_front: E differs from the stats handle's");
+  if (T < 0 || k < 1 || k > 8 || k > E || H < 8 || H % 8)
+    return fail(MOE_ERR_INVALID, "moe_layer_front: need T>=0, 1<=k<=min(E,8), H a positive multiple of 8");
+  if ((long long)T * k >= (1LL << 31)) return fail(MOE_ERR_INVALID, "moe_layer_front: T*k too large");
+  if (iter < 0 || layer < 0 || layer >= st->L) return fail(MOE_ERR_INVALID, "moe_layer_front: bad iter/layer");
+  if (layer > 0 && T > 0 && !idx_prev) return fail(MOE_ERR_INVALID, "moe_layer_front: layer > 0 needs idx_prev");
+  if (layer == 0 && idx_prev) return fail(MOE_ERR_INVALID, "moe_layer_front: idx_prev must be NULL for layer 0");
+  if (layer == st->L - 1 && (cond || p_next))
+    return fail(MOE_ERR_INVALID, "moe_layer_front: the last layer has no next layer (cond/p_next must be NULL)");
+  if (!p_seq && (cond || p_next)) return fail(MOE_ERR_INVALID, "moe_layer_front: cond/p_next need p_seq");
+  if (replicate && (!copies || !rep_base || !group_expert))
+    return fail(MOE_ERR_INVALID, "moe_layer_front: replication needs copies, rep_base, group_expert");
+  if (replicate && (thresh_num < 1 || thresh_den < 1 || thresh_num > 1024 || thresh_den > 1024 || max_copies < -1))
+    return fail(MOE_ERR_INVALID, "moe_layer_front: bad replication threshold or cap");
+  if (!group_offsets) return fail(MOE_ERR_INVALID, "moe_layer_front: null group_offsets");
+  if ((x == nullptr) != (xp == nullptr))
+    return fail(MOE_ERR_INVALID, "moe_layer_front: x and xp must both be set or both NULL");
+  if (T == 0) {
+    // empty batch: the separate calls handle it (window slot cleared, empty layout)
+    moe_status r = moe_stats_update(st, iter, layer, nullptr, nullptr, 0, k, hist_out, stream);
+    if (r != MOE_OK) return r;
+    if (p_seq && (r = moe_predict(st, layer, p_seq, cond, p_next, stream)) != MOE_OK) return r;
+    if (replicate) {
+      if (!hist_out) return fail(MOE_ERR_INVALID, "moe_layer_front: an empty batch with replication needs hist_out");
+      if ((r = moe_replicate(hist_out, E, 0, thresh_num, thresh_den, max_copies, copies, rep_base, group_expert,
+                             stream)) != MOE_OK)
+        return r;
+    }
+    return moe_dispatch(nullptr, nullptr, 0, k, H, E, nullptr, group_offsets, nullptr, nullptr, nullptr, nullptr, 0,
+                        stream);
+  }
+  if (!logits || !idx || !w || !perm || !inv_perm || !workspace)
+    return fail(MOE_ERR_INVALID, "moe_layer_front: null pointer");
+  if (!aligned(logits, 16) || !aligned(workspace, 16) || (x && (!aligned(x, 16) || !aligned(xp, 16))))
+    return fail(MOE_ERR_INVALID, "moe_layer_front: logits, workspace, x and xp must be 16-byte aligned");
+  if (ws_bytes < front::workspace_bytes(T, E))
+    return fail(MOE_ERR_WORKSPACE, "moe_layer_front: workspace needs %zu bytes", front::workspace_bytes(T, E));
+  const int s = st->s;
+  const int slot = (int)(iter % s);
+  front::Args a{};
+  a.logits = logits;
+  a.T = T;
+  a.E = E;
+  a.k = k;
+  a.renorm = renorm ? 1 : 0;
+  a.idx = idx;
+  a.w = w;
+  a.has_prev = layer > 0 ? 1 : 0;
+  a.idx_prev = idx_prev;
+  a.acc_c = st->acc + E;
+  a.ticket = st->ticket;
+  a.ring_h = st->ring_h + ((size_t)layer * s + slot) * E;
+  a.hsum = st->hsum + (size_t)layer * E;
+  a.ring_c = layer > 0 ? st->ring_c + ((size_t)(layer - 1) * s + slot) * E * E : nullptr;
+  a.csum = layer > 0 ? st->csum + (size_t)(layer - 1) * E * E : nullptr;
+  a.hist_out = hist_out;
+  a.pred_csum = (layer < st->L - 1) ? st->csum + (size_t)layer * E * E : nullptr;
+  a.p_seq = p_seq;
+  a.cond = cond;
+  a.p_next = p_next;
+  a.replicate = replicate ? 1 : 0;
+  a.num = thresh_num;
+  a.den = thresh_den;
+  a.max_copies = max_copies;
+  a.copies = copies;
+  a.rep_base = rep_base;
+  a.group_expert = group_expert;
+  a.TT = front::tile_tokens(T);
+  a.ntiles = front::num_tiles(T);
+  a.counts = static_cast<int32_t*>(workspace);
+  a.info = a.counts + a.ntiles * E;
+  a.group_offsets = group_offsets;
+  return cuda_status(front::launch(a, x, H, xp, perm, inv_perm, static_cast<cudaStream_t>(stream)),
+                     "moe_layer_front launch");
 }
 
 // ------------------------------------------------------------------ expert FFN

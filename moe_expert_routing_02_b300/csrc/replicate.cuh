@@ -16,11 +16,11 @@ namespace replicate {
 
 constexpr int kThreads = 256;
 
-__global__ void __launch_bounds__(kThreads) replicate_kernel(const int32_t* __restrict__ load, int E,
-                                                             long long total, int num, int den, int max_copies,
-                                                             int32_t* __restrict__ copies_out,
-                                                             int32_t* __restrict__ rep_base,
-                                                             int32_t* __restrict__ group_expert) {
+// Block-level body (blockDim.x == kThreads, E <= kThreads).
+__device__ __forceinline__ void replicate_block(const int32_t* __restrict__ load, int E, long long total, int num,
+                                                int den, int max_copies, int32_t* __restrict__ copies_out,
+                                                int32_t* __restrict__ rep_base,
+                                                int32_t* __restrict__ group_expert) {
   __shared__ int warp_sum[kThreads / 32];
   __shared__ long long load_sum[kThreads / 32];
   __shared__ int bad_sh;
@@ -77,6 +77,14 @@ __global__ void __launch_bounds__(kThreads) replicate_kernel(const int32_t* __re
   }
   if (e == 0) rep_base[E] = all;
   for (int g = all + e; g < 2 * E; g += kThreads) group_expert[g] = -1;
+}
+
+__global__ void __launch_bounds__(kThreads) replicate_kernel(const int32_t* __restrict__ load, int E,
+                                                             long long total, int num, int den, int max_copies,
+                                                             int32_t* __restrict__ copies_out,
+                                                             int32_t* __restrict__ rep_base,
+                                                             int32_t* __restrict__ group_expert) {
+  replicate_block(load, E, total, num, den, max_copies, copies_out, rep_base, group_expert);
 }
 
 static cudaError_t launch(const int32_t* load, int E, long long total, int num, int den, int max_copies,

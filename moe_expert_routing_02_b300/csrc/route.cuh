@@ -21,18 +21,15 @@ __device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
   return a > b || (a == b && ia < ib);
 }
 
+// Top-k of one token's logits by its group of G lanes (all G lanes call it,
+// `live` false for a lane group past the last token).  On return every lane
+// of the group holds the k winners (sel_i, rank order) and their logits
+// (sel_v); *denom is the softmax denominator of the chosen weighting, so
+// w_r = expf(sel_v[r] - sel_v[0]) / *denom.
 template <int G, bool VEC>
-__global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                        int renorm, int32_t* __restrict__ idx,
-                                                        float* __restrict__ wout) {
-  constexpr int TPW = 32 / G;  // tokens per warp
-  const int lane = threadIdx.x & 31;
-  const int sub = lane / G;
-  const int gl = lane % G;
-  const long long warp_id = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
-  const long long t = warp_id * TPW + sub;
-  const bool live = t < T;
-
+__device__ __forceinline__ void topk_token(const float* __restrict__ row, bool live, int E, int k, int renorm,
+                                           float (&sel_v)[8], int (&sel_i)[8], float* denom_out) {
+  const int gl = (threadIdx.x & 31) % G;
   float v[8];
   int id[8];
 #pragma unroll
@@ -41,7 +38,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
     id[s] = 0x7fffffff;
   }
   if (live) {
-    const float* row = logits + (size_t)t * E;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int chunk = gl + c * G;
@@ -66,10 +62,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
   }
 
   unsigned chosen = 0;
-  float sel_v[8];
-  int sel_i[8];
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
+    sel_v[r] = -INFINITY;
+    sel_i[r] = 0;
     if (r < k) {
       float bv = -INFINITY;
       int bi = 0x7fffffff;
@@ -97,8 +93,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
     }
   }
 
-  // gate weights
-  float denom = 0.f, ref = sel_v[0];
+  // gate-weight denominator
+  float denom = 0.f;
+  const float ref = sel_v[0];
   if (renorm) {
 #pragma unroll
     for (int r = 0; r < 8; ++r)
@@ -110,15 +107,36 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
 #pragma unroll
     for (int off = G / 2; off >= 1; off >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, off);
   }
-  if (live) {
+  *denom_out = denom;
+}
+
+// Lane gl of the token's group writes ranks r with r % G == gl.
+template <int G>
+__device__ __forceinline__ void write_token(long long t, int k, const float (&sel_v)[8], const int (&sel_i)[8],
+                                            float denom, int32_t* __restrict__ idx, float* __restrict__ wout) {
+  const int gl = (threadIdx.x & 31) % G;
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      if (r < k && (r % G) == gl) {
-        idx[(size_t)t * k + r] = sel_i[r];
-        wout[(size_t)t * k + r] = expf(sel_v[r] - ref) / denom;
-      }
+  for (int r = 0; r < 8; ++r) {
+    if (r < k && (r % G) == gl) {
+      idx[(size_t)t * k + r] = sel_i[r];
+      wout[(size_t)t * k + r] = expf(sel_v[r] - sel_v[0]) / denom;
     }
   }
+}
+
+template <int G, bool VEC>
+__global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                        int renorm, int32_t* __restrict__ idx,
+                                                        float* __restrict__ wout) {
+  constexpr int TPW = 32 / G;  // tokens per warp
+  const int lane = threadIdx.x & 31;
+  const long long warp_id = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const long long t = warp_id * TPW + lane / G;
+  const bool live = t < T;
+  float sel_v[8], denom;
+  int sel_i[8];
+  topk_token<G, VEC>(logits + (size_t)(live ? t : 0) * E, live, E, k, renorm, sel_v, sel_i, &denom);
+  if (live) write_token<G>(t, k, sel_v, sel_i, denom, idx, wout);
 }
 
 template <int G>

@@ -153,10 +153,12 @@ static cudaError_t launch_update(const UpdateArgs& a, int num_sms, cudaStream_t 
 // the fp32 output rounding.
 constexpr int kPredictSmemE = 64;  // Cbar staged in shared memory up to E = 64
 
-__global__ void __launch_bounds__(kThreads) predict_kernel(const unsigned long long* __restrict__ hsum,
-                                                           const unsigned long long* __restrict__ csum, int E,
-                                                           float* __restrict__ p_seq, float* __restrict__ cond,
-                                                           float* __restrict__ p_next) {
+// Block-level body (blockDim.x == kThreads).  Callable from any kernel whose
+// block reaches it with all threads.
+__device__ __forceinline__ void predict_block(const unsigned long long* __restrict__ hsum,
+                                              const unsigned long long* __restrict__ csum, int E,
+                                              float* __restrict__ p_seq, float* __restrict__ cond,
+                                              float* __restrict__ p_next) {
   __shared__ double ps[256];
   __shared__ double rinv[256];   // 1 / row sum, or 0 for an empty row
   __shared__ unsigned long long wsum[kThreads / 32];
@@ -205,6 +207,13 @@ __global__ void __launch_bounds__(kThreads) predict_kernel(const unsigned long l
     }
     p_next[tid] = (float)acc;
   }
+}
+
+__global__ void __launch_bounds__(kThreads) predict_kernel(const unsigned long long* __restrict__ hsum,
+                                                           const unsigned long long* __restrict__ csum, int E,
+                                                           float* __restrict__ p_seq, float* __restrict__ cond,
+                                                           float* __restrict__ p_next) {
+  predict_block(hsum, csum, E, p_seq, cond, p_next);
 }
 
 }  // namespace stats

@@ -11,8 +11,9 @@ from typing import Optional
 
 import torch
 
-from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MoEStats, moe_combine, moe_dispatch, moe_expert_ffn,
-               moe_predict, moe_replicate, moe_route, moe_stats_update, workspace_bytes)
+from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT, MoEStats, moe_combine, moe_dispatch,
+               moe_expert_ffn, moe_layer_front, moe_predict, moe_replicate, moe_route, moe_stats_update,
+               workspace_bytes)
 
 __all__ = ["MoELayerStep"]
 
@@ -22,17 +23,21 @@ class MoELayerStep:
 
     replicate=True feeds the replica table of the layer's own histogram into
     dispatch and the FFN (hot experts split into replica groups; the output is
-    unchanged).  stats (MoEStats) is shared by all layers of a model."""
+    unchanged).  stats (MoEStats) is shared by all layers of a model.
+    fused=True (needs stats) runs route, statistics, prediction, replicas and
+    dispatch as moe_layer_front (two launches); fused=False makes the five
+    separate calls.  Both give identical results."""
 
     def __init__(self, T: int, E: int, k: int, H: int, F: int, act: str, stats: Optional[MoEStats] = None,
                  replicate: bool = True, thresh=(6, 5), max_copies: int = -1, renorm: bool = True,
-                 small_group_threshold: int = 64, device="cuda"):
+                 small_group_threshold: int = 64, fused: bool = True, device="cuda"):
         self.T, self.E, self.k, self.H, self.F, self.act = T, E, k, H, F, act
         self.A = T * k
         self.stats = stats
         self.replicate = replicate
         self.thresh, self.max_copies, self.renorm = thresh, max_copies, renorm
         self.small = small_group_threshold
+        self.fused = fused and stats is not None
         d = torch.device(device)
         i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
         A = self.A
@@ -50,7 +55,9 @@ class MoELayerStep:
         self.inv = torch.empty(A, dtype=i32, device=d)
         self.xp = torch.empty((A, H), dtype=bf, device=d)
         self.y = torch.empty((A, H), dtype=bf, device=d)
-        self.ws_dispatch = torch.empty(max(workspace_bytes(MOE_OP_DISPATCH, T, k, E), 16), dtype=torch.uint8, device=d)
+        self.ws_dispatch = torch.empty(max(workspace_bytes(MOE_OP_DISPATCH, T, k, E),
+                                           workspace_bytes(MOE_OP_LAYER_FRONT, T, k, E), 16),
+                                       dtype=torch.uint8, device=d)
         self.ws_ffn = torch.empty(max(workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F), 1024), dtype=torch.uint8,
                                   device=d)
         self._cur = 0
@@ -68,6 +75,19 @@ class MoELayerStep:
 
         prev = self.idx[self._cur ^ 1] if layer > 0 else None
         idx = self.idx[self._cur]
+        if self.fused:
+            last = layer == self.stats.L - 1
+            mark("front", 0)
+            out_front = {"idx": idx, "w": self.w, "hist": self.hist, "p_seq": self.p_seq,
+                         "cond": None if last else self.cond, "p_next": None if last else self.p_next,
+                         "copies": self.copies, "rep_base": self.rep_base, "group_expert": self.group_expert,
+                         "group_offsets": self.go, "perm": self.perm, "inv_perm": self.inv, "xp": self.xp}
+            moe_layer_front(logits, x, self.stats, it, layer, self.k, idx_prev=prev, renorm=self.renorm,
+                            predict=predict, replicate=self.replicate, thresh=self.thresh,
+                            max_copies=self.max_copies, out=out_front, workspace=self.ws_dispatch)
+            mark("front", 1)
+            rb, ge = (self.rep_base, self.group_expert) if self.replicate else (None, None)
+            return self._expert_and_combine(weights, rb, ge, out, mark)
         mark("route", 0)
         moe_route(logits, self.k, self.renorm, idx=idx, w=self.w)
         mark("route", 1)
@@ -89,6 +109,9 @@ class MoELayerStep:
         mark("dispatch", 0)
         moe_dispatch(x, idx, self.E, rb, out=(self.go, self.perm, self.inv, self.xp), workspace=self.ws_dispatch)
         mark("dispatch", 1)
+        return self._expert_and_combine(weights, rb, ge, out, mark)
+
+    def _expert_and_combine(self, weights, rb, ge, out, mark):
         w1, w3, w2 = weights
         mark("ffn", 0)
         moe_expert_ffn(self.xp, self.go, ge, rb, w1, w3, w2, self.act, self.small, y=self.y, workspace=self.ws_ffn)
@@ -100,7 +123,10 @@ class MoELayerStep:
         return out
 
     def launches(self, layer: int, L: int) -> int:
-        n = 1 + 1 + 4 + 2 + 1
+        ffn = 2 + (2 if self.small > 0 else 0)
+        if self.fused:
+            return 2 + ffn + 1
+        n = 1 + 4 + ffn + 1
         if self.stats is not None:
             n += 1
             if layer < L - 1:
