@@ -53,6 +53,8 @@ def parse_args(argv=None):
     ap.add_argument("--config", default="moe_gpt_stream")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch every call from Python instead of graph replay")
+    ap.add_argument("--gather", action="store_true",
+                    help="gather the rows in the FFN's loads (moe_expert_ffn_gather) instead of copying them")
     ap.add_argument("--unfused", action="store_true",
                     help="make the five separate front calls instead of moe_layer_front")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -167,12 +169,14 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # workload
 # ----------------------------------------------------------------------------
-def algorithmic_work(c, used_experts=None):
+def algorithmic_work(c, used_experts=None, gather=False):
     """Per-layer algorithmic bytes (HBM stages) and flops (FFN), as the method
     must move them (not what the kernels happen to move).  The FFN must read
     the weights of every expert that received a token (used_experts, counted
     from a layer's histogram; all E when unknown) once, its input rows once and write its output
-    rows once (plus the bf16 intermediate written and read back)."""
+    rows once (plus the bf16 intermediate written and read back).  With the
+    gathered FFN input (gather=True) dispatch moves no rows and the FFN reads
+    the T token rows instead of the A dispatched ones."""
     T, E, k, H, F, A = c.T, c.E, c.k, c.H, c.F, c.A
     ngemm = 3 if c.act == "swiglu" else 2
     Eu = E if used_experts is None else used_experts
@@ -181,9 +185,10 @@ def algorithmic_work(c, used_experts=None):
         "stats": {"bytes": 2 * A * 4 + (E + E * E) * 4 * 2 + (E + E * E) * 8 * 2},
         "predict": {"bytes": E * E * 8 + E * 8 + E * E * 4 + E * 8},
         "replicate": {"bytes": E * 16},
-        "dispatch": {"bytes": A * 4 + T * H * 2 + A * H * 2 + 2 * A * 4},
+        "dispatch": {"bytes": A * 4 + 2 * A * 4 + (0 if gather else T * H * 2 + A * H * 2)},
         "ffn": {"flops": 2 * ngemm * A * H * F,
-                "bytes": int(ngemm * Eu * H * F * 2 + A * H * 2 * 2 + (ngemm - 1) * A * F * 2 * 2)},
+                "bytes": int(ngemm * Eu * H * F * 2 + (T if gather else A) * H * 2 + A * H * 2
+                             + (ngemm - 1) * A * F * 2 * 2)},
         "combine": {"bytes": A * H * 2 + A * 8 + T * H * 2},
     }
     # the fused front does the work of the five calls it replaces
@@ -246,7 +251,7 @@ def run_ours(args, rank, world, local):
     outs = [torch.empty((c.T, c.H), dtype=torch.bfloat16, device=dev) for _ in range(c.L)]
     stats = M.MoEStats(c.L, c.E, c.window)
     step = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, stats=stats, replicate=True, fused=not args.unfused,
-                        device=dev)
+                        gather=args.gather, device=dev)
     stage_names = ["front", "ffn", "combine"] if step.fused else STAGES
 
     def run_step(it, ev=None):
@@ -350,7 +355,7 @@ def run_ours(args, rank, world, local):
     stage_note = None
     # experts that received tokens, from the last layer call's histogram (libmoe's own count)
     used = float((step.hist > 0).sum().item())
-    work = algorithmic_work(c, used_experts=used)
+    work = algorithmic_work(c, used_experts=used, gather=step.gather)
     peaks = load_peaks()
     stages = {}
     for sname in stage_names:
@@ -396,6 +401,8 @@ def run_ours(args, rank, world, local):
                    "l2": "no flush: each step streams ~1.5 GB of weights + activations, >> 126 MB L2",
                    "launch": "eager" if args.eager else f"CUDA graph per step ({c.window} graphs, one per window slot)",
                    "front": "separate calls" if args.unfused else "moe_layer_front (2 launches)",
+                   "ffn_input": "gathered from x in GEMM1's loads (tile::gather4)" if step.gather
+                                else "rows copied into dispatch order",
                    "stage_timing": "CUDA events around each stage, every layer of every timed step" if args.eager
                    else "FFN: events captured around it in the timed graphs (last replay of each); other stages: "
                         "a second set of graphs with events around every stage, replayed once per slot after the "

@@ -14,6 +14,10 @@
  *   moe_expert_ffn    grouped expert FFN (GeLU or SwiGLU) on tcgen05 tensor cores
  *   moe_combine       gate-weighted sum of each token's k expert outputs
  *
+ * and two fused forms of the same work: moe_layer_front (route through
+ * dispatch in two launches) and moe_expert_ffn_gather (the FFN reading the
+ * token rows in place, so that dispatch writes only the permutation).
+ *
  * Conventions
  *   T tokens, E experts, k experts per token, A = T*k assignments (assignment
  *   f = t*k + r is token t's r-th choice), H hidden size, F expert FFN width.
@@ -242,6 +246,29 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets,
                           const uint16_t* w1, const uint16_t* w3, const uint16_t* w2,
                           int H, int F, moe_act act, int small_group_threshold, uint16_t* y,
                           void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_expert_ffn_gather -- the same grouped expert FFN, reading the token
+ * rows in place: the dispatch copy is folded into the first GEMM's operand
+ * loads (EPS-MoE review, expert pipeline: the dispatched rows are only an
+ * input of the expert GEMMs), so moe_dispatch / moe_layer_front can be run
+ * with x = xp = NULL (permutation only).
+ *   x              [T,H] bf16 token rows (not permuted)
+ *   perm           [T*k] int32 slot -> assignment f (moe_dispatch's perm);
+ *                  dispatched row i is x[perm[i] / k].  A value outside
+ *                  [0, T*k) sets the device error word (MOE_ERR_DEVICE from
+ *                  moe_check) and row 0 is read in its place.
+ *   the other arguments as in moe_expert_ffn, with A = T*k.
+ * y is bit-identical to moe_expert_ffn on the copied rows.  T = 0 is a valid
+ * empty batch; the workspace is moe_workspace_bytes(MOE_OP_EXPERT_FFN, T, k,
+ * E, H, F) bytes.
+ * ------------------------------------------------------------------------- */
+moe_status moe_expert_ffn_gather(const uint16_t* x, int T, const int32_t* perm, int k,
+                                 const int32_t* group_offsets, const int32_t* group_expert,
+                                 const int32_t* rep_base, int E, const uint16_t* w1,
+                                 const uint16_t* w3, const uint16_t* w2, int H, int F, moe_act act,
+                                 int small_group_threshold, uint16_t* y, void* workspace,
+                                 size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * moe_combine -- gate-weighted sum of each token's expert outputs.

@@ -18,7 +18,7 @@ from typing import Optional
 
 __all__ = [
     "MoEError", "lib", "library_path", "MoEStats", "moe_route", "moe_stats_update", "moe_predict",
-    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_layer_front", "moe_expert_ffn", "moe_combine", "moe_check", "moe_error_word",
+    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_layer_front", "moe_expert_ffn", "moe_expert_ffn_gather", "moe_combine", "moe_check", "moe_error_word",
     "workspace_bytes", "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_ACT_GELU", "MOE_ACT_SWIGLU",
     "EXPORTED_SYMBOLS", "moe_set_option", "moe_get_option", "MOE_OPT_FFN_KERNEL", "MOE_FFN_KERNEL_AUTO",
     "MOE_FFN_KERNEL_SINGLE", "MOE_FFN_KERNEL_PAIR", "MOE_OPT_FFN_TIMEOUT_SELFTEST",
@@ -49,6 +49,7 @@ _SIGS = {
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_expert_ffn_gather": (_I, [_P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_check": (_I, [_P]),
@@ -395,6 +396,43 @@ def moe_expert_ffn(xp, group_offsets, group_expert, rep_base, w1, w3, w2, act: s
     _check(lib().moe_expert_ffn(_ptr(xp), _ptr(group_offsets), _ptr(group_expert), _ptr(rep_base), E, A,
                                 _ptr(w1), _ptr(w3), _ptr(w2), H, F, act_id, int(small_group_threshold), _ptr(y),
                                 _ptr(workspace), workspace.numel(), _stream(stream)), "moe_expert_ffn")
+    return y
+
+
+def moe_expert_ffn_gather(x, perm, k: int, group_offsets, group_expert, rep_base, w1, w3, w2, act: str = "gelu",
+                          small_group_threshold: int = 64, y=None, workspace=None, stream=None):
+    """Grouped expert FFN reading the token rows in place: dispatched row i is
+    x[perm[i] // k].  Returns y [T*k, H] bf16, bit-identical to
+    moe_expert_ffn on the copied rows."""
+    torch = _torch()
+    _dev(x, torch.bfloat16, "x", 2)
+    _dev(perm, torch.int32, "perm", 1)
+    _dev(w1, torch.bfloat16, "w1", 3)
+    _dev(w2, torch.bfloat16, "w2", 3)
+    if w3 is not None:
+        _dev(w3, torch.bfloat16, "w3", 3)
+    _dev(group_offsets, torch.int32, "group_offsets", 1)
+    if group_expert is not None:
+        _dev(group_expert, torch.int32, "group_expert", 1)
+    if rep_base is not None:
+        _dev(rep_base, torch.int32, "rep_base", 1)
+    T, H = x.shape
+    E, H1, F = w1.shape
+    if H1 != H or tuple(w2.shape) != (E, F, H):
+        raise ValueError("weight shapes must be w1/w3 [E,H,F], w2 [E,F,H]")
+    if perm.numel() != T * k:
+        raise ValueError("perm must hold T*k entries")
+    act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
+    if y is None:
+        y = torch.empty((T * k, H), dtype=torch.bfloat16, device=x.device)
+    _dev(y, torch.bfloat16, "y", 2)
+    need = int(lib().moe_workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=x.device)
+    _check(lib().moe_expert_ffn_gather(_ptr(x), T, _ptr(perm), int(k), _ptr(group_offsets), _ptr(group_expert),
+                                       _ptr(rep_base), E, _ptr(w1), _ptr(w3), _ptr(w2), H, F, act_id,
+                                       int(small_group_threshold), _ptr(y), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)), "moe_expert_ffn_gather")
     return y
 
 

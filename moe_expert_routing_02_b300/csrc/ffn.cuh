@@ -71,6 +71,7 @@ constexpr int B_BYTES = BN * BK * 2;      // 32 KB
 constexpr int EPI_WARPS = MOE_FFN_EPI_WARPS;
 constexpr int B_BOXES = BN / 64;       // 64-column TMA boxes per B stage
 static_assert(BN % 128 == 0 && BN <= 256, "BN must be 128 or 256");
+static_assert(BM == 4 * 32 && BK * 2 == 128, "a gathered A tile is 32 lanes x 4 rows of 128 bytes");
 constexpr int EPI_SLICES = EPI_WARPS / 4;  // column slices per TMEM lane quarter
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr int MAX_G = 512;
@@ -93,6 +94,12 @@ struct Params {
   int flags;         // bit 0: CTA 0 withholds its first accumulator signal (timeout self-test)
   const int32_t* rep_base;  // [E+1] or null: groups of expert e are rep_base[e]..rep_base[e+1]-1
   int small_threshold;      // experts with fewer rows take the small-batch kernel (0 = none)
+  // Gathered A operand (GEMM1 only): row i of A is row a_src[i] / a_src_div
+  // of the tensor behind tmA (a token of x, a_src = the dispatch permutation,
+  // a_src_div = k); null = A is stored in row order.
+  const int32_t* a_src;
+  int a_src_div;
+  int a_src_rows;  // rows of that tensor (T)
 };
 
 
@@ -263,6 +270,28 @@ __device__ __forceinline__ Tile decode(const Smem& s, int U, int tile) {
 // extended to x < 0 by oddness.  In fp32 with the fast reciprocal and
 // exponential the error stays near 3e-7, far below the bf16 rounding of the
 // output (2^-9 relative).  Two MUFU operations and ten FMA-pipe operations.
+// Source rows of A rows row0 + 4*q .. row0 + 4*q + 3 (gathered A operand).
+// Rows past the operand's end read row 0: they fill the ragged tail of the
+// last tile, whose results are never stored.  A source outside [0, rows)
+// is invalid device data: flagged, and row 0 is read instead.
+__device__ __forceinline__ int4 gather_src4(const Params& p, long long row0, int q) {
+  int r[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const long long row = row0 + 4 * q + j;
+    int src = 0;
+    if (row < p.A_rows) {
+      src = __ldg(p.a_src + row) / p.a_src_div;
+      if ((unsigned)src >= (unsigned)p.a_src_rows) {
+        moe_flag_error(MOE_DEVERR_DATA);
+        src = 0;
+      }
+    }
+    r[j] = src;
+  }
+  return make_int4(r[0], r[1], r[2], r[3]);
+}
+
 __device__ __forceinline__ float erf_as7126(float x) {
   const float ax = fabsf(x);
   const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
@@ -376,20 +405,26 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, issued = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode(s, U, tile);
-        const int brow = s.ex[t.g] * p.K;
-        const int arow = (int)t.row0;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_phase(&s.empty[stage], phase ^ 1, &s.abort_flag)) {
-            ok = false;
-            break;
-          }
+    // lane 0 waits, arms the stage and loads B (and A when stored in row
+    // order); a gathered A is copied by all 32 lanes, four rows each
+    const bool gather = p.a_src != nullptr;
+    uint32_t stage = 0, phase = 0, issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const Tile t = decode(s, U, tile);
+      const int brow = s.ex[t.g] * p.K;
+      const int arow = (int)t.row0;
+      const int4 src = gather ? gather_src4(p, t.row0, lane) : make_int4(0, 0, 0, 0);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        bool w = true;
+        if (lane == 0) w = wait_phase(&s.empty[stage], phase ^ 1, &s.abort_flag);
+        if (!__shfl_sync(0xffffffffu, (int)w, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
           mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
-          tma_load_2d(s.a[stage], &tmA, &s.full[stage], kb * BK, arow);
+          if (!gather) tma_load_2d(s.a[stage], &tmA, &s.full[stage], kb * BK, arow);
           if (EPI == kSwiglu) {
             // first half of the B tile: W1 (gate) columns, second half: the same W3 (up) columns
             const int n0 = t.nt * (BN / 2);
@@ -405,14 +440,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int c = 0; c < B_BOXES; ++c)
               tma_load_2d(s.b[stage] + c * B_BOX_BYTES, &tmB0, &s.full[stage], n0 + 64 * c, brow + kb * BK);
           }
-          ++issued;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+        }
+        __syncwarp();
+        if (gather) tma_gather4(s.a[stage] + lane * 512, &tmA, &s.full[stage], kb * BK, src);
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
         }
       }
-      // every stage's latest copy must have landed before the CTA may exit
+    }
+    // every stage's latest copy must have landed before the CTA may exit
+    if (lane == 0) {
       for (uint32_t st = 0; st < (uint32_t)STAGES; ++st) {
         if (issued > st) {
           const uint32_t last = issued - 1 - ((issued - 1 - st) % STAGES);

@@ -55,6 +55,7 @@ constexpr int EPI_SLICES = EPI_WARPS / 4;
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr int MAX_G = 512;
 constexpr uint32_t TMEM_COLS = 2 * BN;
+static_assert(BM == 4 * 32 && BK * 2 == 128, "a gathered A tile is 32 lanes x 4 rows of 128 bytes");
 
 struct Smem {
   uint8_t a[STAGES][A_BYTES];
@@ -175,41 +176,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, issued = 0;
-      bool ok = true;
-      const CUtensorMap* mB = (EPI == kSwiglu && !leader) ? &tmB1 : &tmB0;
-      const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);  // leader's barriers
-      for (int tile = pair; tile < total && ok; tile += npairs) {
-        const Tile t = decode(s, U, tile);
-        const int brow = s.ex[t.g] * p.K;
-        const int arow = (int)(t.row0 + BM * rank);
-        const int n0 = (EPI == kSwiglu) ? t.nt * (BN / 2) : t.nt * BN + (int)rank * (BN / 2);
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_phase<true>(&s.empty[stage], phase ^ 1, &s.abort_flag)) {
-            ok = false;
-            break;
-          }
+    // lane 0 waits, arms (leader) and loads B (and A when stored in row
+    // order); a gathered A is copied by all 32 lanes, four rows each
+    const bool gather = p.a_src != nullptr;
+    uint32_t stage = 0, phase = 0, issued = 0;
+    bool ok = true;
+    const CUtensorMap* mB = (EPI == kSwiglu && !leader) ? &tmB1 : &tmB0;
+    const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);  // leader's barriers
+    for (int tile = pair; tile < total && ok; tile += npairs) {
+      const Tile t = decode(s, U, tile);
+      const int brow = s.ex[t.g] * p.K;
+      const int arow = (int)(t.row0 + BM * rank);
+      const int n0 = (EPI == kSwiglu) ? t.nt * (BN / 2) : t.nt * BN + (int)rank * (BN / 2);
+      const int4 src = gather ? ffn::gather_src4(p, t.row0 + BM * rank, lane) : make_int4(0, 0, 0, 0);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        bool w = true;
+        if (lane == 0) w = wait_phase<true>(&s.empty[stage], phase ^ 1, &s.abort_flag);
+        if (!__shfl_sync(0xffffffffu, (int)w, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = full0 + stage * (uint32_t)sizeof(uint64_t);
+        if (lane == 0) {
           if (leader) mbar_arrive_expect_tx(&s.full[stage], 2 * (A_BYTES + B_HALF_BYTES));
-          const uint32_t fb = full0 + stage * (uint32_t)sizeof(uint64_t);
-          tma_load_2d_pair(s.a[stage], &tmA, fb, kb * BK, arow);
+          if (!gather) tma_load_2d_pair(s.a[stage], &tmA, fb, kb * BK, arow);
           tma_load_2d_pair(s.b[stage], mB, fb, n0, brow + kb * BK);
           tma_load_2d_pair(s.b[stage] + B_BOX_BYTES, mB, fb, n0 + 64, brow + kb * BK);
-          ++issued;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+        }
+        __syncwarp();
+        if (gather) tma_gather4_pair(s.a[stage] + lane * 512, &tmA, fb, kb * BK, src);
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
         }
       }
-      // normal path: the pair's MMAs released every stage this CTA filled, so
-      // its copies landed and no commit arrival is still travelling here
-      if (ok) {
-        for (uint32_t st = 0; st < (uint32_t)STAGES; ++st) {
-          if (issued > st) {
-            const uint32_t last = issued - 1 - ((issued - 1 - st) % STAGES);
-            wait_phase<true>(&s.empty[st], (last / STAGES) & 1u, &s.abort_flag);
-          }
+    }
+    // normal path: the pair's MMAs released every stage this CTA filled, so
+    // its copies landed and no commit arrival is still travelling here
+    if (ok && lane == 0) {
+      for (uint32_t st = 0; st < (uint32_t)STAGES; ++st) {
+        if (issued > st) {
+          const uint32_t last = issued - 1 - ((issued - 1 - st) % STAGES);
+          wait_phase<true>(&s.empty[st], (last / STAGES) & 1u, &s.abort_flag);
         }
       }
     }

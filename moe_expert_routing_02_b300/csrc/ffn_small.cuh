@@ -42,6 +42,7 @@ constexpr int X_BYTES = BT * BK * 2;      // 8 KB: 64 token rows x 64 k
 constexpr int EPI_WARPS = 4;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int MAX_G = 512;
+static_assert(BT % 4 == 0 && BT / 4 <= 32 && BK * 2 == 128, "a gathered X tile is BT/4 lanes x 4 rows of 128 bytes");
 
 template <int EPI>
 struct Cfg {
@@ -163,19 +164,25 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, issued = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode(s, U, tile);
-        const int wrow = s.ex[t.g] * p.K;
-        const int f0 = t.ft * BMF;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_phase(&s.empty[stage], phase ^ 1, &s.abort_flag)) {
-            ok = false;
-            break;
-          }
-          uint8_t* st = s.stage[stage];
+    // lane 0 waits, arms the stage and loads the weights (and X when stored
+    // in row order); a gathered X is copied by lanes 0..15, four rows each
+    const bool gather = p.a_src != nullptr;
+    uint32_t stage = 0, phase = 0, issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const Tile t = decode(s, U, tile);
+      const int wrow = s.ex[t.g] * p.K;
+      const int f0 = t.ft * BMF;
+      const int4 src = (gather && lane < BT / 4) ? ffn::gather_src4(p, t.row0, lane) : make_int4(0, 0, 0, 0);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        bool w = true;
+        if (lane == 0) w = wait_phase(&s.empty[stage], phase ^ 1, &s.abort_flag);
+        if (!__shfl_sync(0xffffffffu, (int)w, 0)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = s.stage[stage];
+        if (lane == 0) {
           mbar_arrive_expect_tx(&s.full[stage], C::STAGE);
 #pragma unroll
           for (int op = 0; op < C::NW; ++op) {
@@ -183,14 +190,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(st + op * W_BYTES, m, &s.full[stage], f0, wrow + kb * BK);
             tma_load_2d(st + op * W_BYTES + W_BOX_BYTES, m, &s.full[stage], f0 + 64, wrow + kb * BK);
           }
-          tma_load_2d(st + C::NW * W_BYTES, &tmX, &s.full[stage], kb * BK, (int)t.row0);
-          ++issued;
-          if (++stage == (uint32_t)C::STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+          if (!gather) tma_load_2d(st + C::NW * W_BYTES, &tmX, &s.full[stage], kb * BK, (int)t.row0);
+        }
+        __syncwarp();
+        if (gather && lane < BT / 4) tma_gather4(st + C::NW * W_BYTES + lane * 512, &tmX, &s.full[stage], kb * BK, src);
+        ++issued;
+        if (++stage == (uint32_t)C::STAGES) {
+          stage = 0;
+          phase ^= 1;
         }
       }
+    }
+    if (lane == 0) {
       for (uint32_t st = 0; st < (uint32_t)C::STAGES; ++st) {
         if (issued > st) {
           const uint32_t last = issued - 1 - ((issued - 1 - st) % C::STAGES);

@@ -6,21 +6,27 @@
 // Collector with Eq. (1)-(3); MoE-GPS blog section 2.1 duplicate_experts;
 // MoE-MPMC summary, replica dispatch), with five fewer launches:
 //
-//   F1 (route_count_kernel), one block per TT_BLOCK tokens:
-//      top-k of each token (route::topk_token), idx / w written; per tile of
-//      TT tokens the expert counts (shared atomics -> counts[tile][E]); the
-//      co-selection pairs with the previous layer's routing (shared atomics,
-//      flushed to the window state's accumulator).  The last block to finish
-//      (ticket after a fence) then, alone:
-//        - scans the tile counts per expert (tile starting ranks, histogram),
+//   F1 (route_count_kernel), one block per tiles_per_block tiles of TT tokens:
+//      top-k of each token (route::topk_token), idx / w written; per tile the
+//      expert counts (shared atomics), written as the tile's exclusive prefix
+//      within the block, and the block's totals (blk_tot, and added to the
+//      histogram accumulator); the co-selection pairs with the previous
+//      layer's routing (shared atomics, flushed to the window state's
+//      accumulator).  The last block to finish (ticket after a fence) then,
+//      alone:
+//        - takes the histogram from the accumulator,
 //        - folds histogram and co-selection counts into the window ring and
 //          sums (as stats::update_kernel does),
 //        - predicts the next layer (stats::predict_block),
 //        - computes replica counts (replicate::replicate_block),
 //        - lays out the groups (closed form of the round-robin split).
-//   F2 (scatter_copy_kernel), one block per tile: stable in-tile ranks ->
-//      slots -> perm / inv_perm, then the rows of the tile's assignments are
-//      copied to their slots with 16-byte vectors.
+//   F2 (scatter_copy_kernel), one block per tile: the tile's starting rank
+//      per expert (totals of the route blocks before its own, plus its
+//      prefix within its block), stable in-tile ranks -> slots -> perm /
+//      inv_perm, then the rows of the tile's assignments are copied to their
+//      slots with 16-byte vectors.
+// The plan (last block) thus reads O(E) and O(E^2) values only; the
+// per-tile prefix over the route blocks is spread over the F2 blocks.
 // Counts are integers, so nothing depends on the order of atomics.
 #pragma once
 #include "common.cuh"
@@ -43,9 +49,13 @@ __host__ __device__ inline int tile_tokens(long long T) {
   return tt;
 }
 __host__ inline long long num_tiles(long long T) { return (T + tile_tokens(T) - 1) / tile_tokens(T); }
+// Route blocks: at most kMaxRouteBlocks (the F2 prologue reads the totals
+// of the blocks before its own), and at least one pass of every warp.
+constexpr int kMaxRouteBlocks = 128;
+// Workspace: tile prefixes [ntiles][E], block totals [<= ntiles][E], info [4][E].
 __host__ inline size_t workspace_bytes(long long T, int E) {
   const long long nt = num_tiles(T) > 0 ? num_tiles(T) : 1;
-  return (size_t)(nt * E + 4LL * E) * sizeof(int32_t);
+  return (size_t)(2 * nt * E + 4LL * E) * sizeof(int32_t);
 }
 
 struct Args {
@@ -57,7 +67,8 @@ struct Args {
   // window update (pointers into the stats handle for this layer / pair)
   int has_prev;
   const int32_t* idx_prev;
-  uint32_t* acc_c;
+  uint32_t* acc_h;   // [E] histogram accumulator (zero between calls)
+  uint32_t* acc_c;   // [E*E] co-selection accumulator (zero between calls)
   uint32_t* ticket;
   uint32_t* ring_h;
   unsigned long long* hsum;
@@ -78,7 +89,8 @@ struct Args {
   int TT;            // tokens per tile
   int tiles_per_block;
   long long ntiles;
-  int32_t* counts;   // [ntiles][E]: tile counts, then tile starting ranks
+  int32_t* counts;   // [ntiles][E]: tile's exclusive prefix within its route block
+  int32_t* blk_tot;  // [route blocks][E]: block totals
   int32_t* info;     // [4][E]: expert base, replicas, rows, -
   int32_t* group_offsets;
 };
@@ -105,6 +117,10 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
   for (long long t0 = tb0 + (long long)warp * TPW; t0 < tb1; t0 += (long long)kWarps * TPW) {
     const long long t = t0 + lane / G;
     const bool live = t < tb1;
+    // the previous layer's choices of the token, loaded ahead of the top-k
+    int pe[8];
+#pragma unroll
+    for (int r1 = 0; r1 < 8; ++r1) pe[r1] = (cos && live && gl == 0 && r1 < k) ? a.idx_prev[t * k + r1] : 0;
     float sel_v[8], denom;
     int sel_i[8];
     route::topk_token<G, VEC>(a.logits + (size_t)(live ? t : 0) * E, live, E, k, a.renorm, sel_v, sel_i, &denom);
@@ -119,15 +135,14 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
 #pragma unroll
           for (int r1 = 0; r1 < 8; ++r1) {
             if (r1 < k) {
-              const int pe = a.idx_prev[t * k + r1];
-              if ((unsigned)pe >= (unsigned)E) {
+              if ((unsigned)pe[r1] >= (unsigned)E) {
                 bad = true;
                 continue;
               }
 #pragma unroll
               for (int r2 = 0; r2 < 8; ++r2) {
                 if (r2 < k) {
-                  const int bin = pe * E + sel_i[r2];
+                  const int bin = pe[r1] * E + sel_i[r2];
                   if (cos_smem)
                     atomicAdd(cs + bin, 1u);
                   else
@@ -142,11 +157,17 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
   }
   if (bad) moe_flag_error(MOE_DEVERR_DATA);
   __syncthreads();
-  // tile counts (each tile row written in full by its block)
+  // per expert: tile prefixes within the block, block total, histogram
   const long long tile0 = (long long)blockIdx.x * tpb;
-  for (int i = threadIdx.x; i < tpb * E; i += kThreads) {
-    const long long tile = tile0 + i / E;
-    if (tile < a.ntiles) a.counts[tile * E + (i % E)] = (int32_t)cnt[i];
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    uint32_t run = 0;
+    for (int i = 0; i < tpb; ++i) {
+      const long long tile = tile0 + i;
+      if (tile < a.ntiles) a.counts[tile * E + e] = (int32_t)run;
+      run += cnt[i * E + e];
+    }
+    a.blk_tot[(size_t)blockIdx.x * E + e] = (int32_t)run;
+    if (run) atomicAdd(a.acc_h + e, run);
   }
   if (cos_smem)
     for (int i = threadIdx.x; i < E * E; i += kThreads)
@@ -163,25 +184,8 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
   if (!is_last) return;
   __threadfence();
   const int e = threadIdx.x;
-  // per-expert exclusive scan over tiles: tile starting ranks and the histogram
-  int h = 0;
   if (e < E) {
-    long long b = 0;
-    for (; b + 8 <= a.ntiles; b += 8) {
-      int c[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) c[u] = a.counts[(b + u) * E + e];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        a.counts[(b + u) * E + e] = h;
-        h += c[u];
-      }
-    }
-    for (; b < a.ntiles; ++b) {
-      const int c = a.counts[b * E + e];
-      a.counts[b * E + e] = h;
-      h += c;
-    }
+    const int h = (int)atomicExch(a.acc_h + e, 0u);
     hist_s[e] = h;
     // window: histogram slot and sums
     const uint32_t old = a.ring_h[e];
@@ -236,10 +240,13 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
   if (threadIdx.x == 0) *a.ticket = 0;
 }
 
-// One block per tile: stable ranks of the tile's assignments (in f order),
-// slots, perm / inv_perm, then the row copy xp[slot] = x[f / k].
+// One block per tile: the tile's starting ranks, stable ranks of its
+// assignments (in f order), slots, perm / inv_perm, then the row copy
+// xp[slot] = x[f / k].
 __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const int32_t* __restrict__ idx, long long T, int k,
-                                                                int E, int TT, const int32_t* __restrict__ tile_base,
+                                                                int E, int TT, int tpb,
+                                                                const int32_t* __restrict__ tile_pre,
+                                                                const int32_t* __restrict__ blk_tot,
                                                                 const int32_t* __restrict__ info,
                                                                 int32_t* __restrict__ perm,
                                                                 int32_t* __restrict__ inv_perm,
@@ -256,7 +263,18 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const int32_t* _
   if (f1 > A) f1 = A;
   const int nA = (int)(f1 - f0);
   for (int i = tid; i < kWarps * E; i += kThreads) warp_cnt[i] = 0;
-  for (int i = tid; i < E; i += kThreads) run[i] = tile_base[(size_t)blockIdx.x * E + i];
+  for (int i = tid; i < E; i += kThreads) run[i] = tile_pre[(size_t)blockIdx.x * E + i];
+  __syncthreads();
+  // starting rank of the tile: add the totals of the route blocks before its own
+  const int nprev = (int)(blockIdx.x / tpb) * E;
+  for (int i0 = tid; i0 < nprev; i0 += 8 * kThreads) {
+    int v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = i0 + u * kThreads < nprev ? blk_tot[i0 + u * kThreads] : 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (v[u]) atomicAdd(&run[(i0 + u * kThreads) % E], v[u]);
+  }
   __syncthreads();
   for (int r0 = 0; r0 < nA; r0 += kThreads) {
     const int i = r0 + tid;
@@ -295,25 +313,34 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const int32_t* _
     __syncthreads();
   }
   if (x == nullptr) return;
-  // rows: one warp per assignment, 16-byte chunks
+  // rows: one warp per two assignments (8 loads of 16 bytes in flight per
+  // lane), 16-byte chunks
   const int chunks = H / 8;
-  for (int i = wid; i < nA; i += kWarps) {
-    const int slot = slot_s[i];
-    if (slot < 0) continue;
-    const uint16_t* src = x + ((f0 + i) / k) * H;
-    uint16_t* dst = xp + (size_t)slot * H;
-    int c = lane;
-    for (; c + 96 < chunks; c += 128) {
-      const uint4 v0 = ld_nc_v4(src + (size_t)c * 8);
-      const uint4 v1 = ld_nc_v4(src + (size_t)(c + 32) * 8);
-      const uint4 v2 = ld_nc_v4(src + (size_t)(c + 64) * 8);
-      const uint4 v3 = ld_nc_v4(src + (size_t)(c + 96) * 8);
-      st_v4(dst + (size_t)c * 8, v0);
-      st_v4(dst + (size_t)(c + 32) * 8, v1);
-      st_v4(dst + (size_t)(c + 64) * 8, v2);
-      st_v4(dst + (size_t)(c + 96) * 8, v3);
+  for (int i = 2 * wid; i < nA; i += 2 * kWarps) {
+    const int s0 = slot_s[i], s1 = i + 1 < nA ? slot_s[i + 1] : -1;
+    const uint16_t* src0 = x + ((f0 + i) / k) * H;
+    const uint16_t* src1 = x + ((f0 + i + 1) / k) * H;
+    uint16_t* dst0 = xp + (size_t)(s0 < 0 ? 0 : s0) * H;
+    uint16_t* dst1 = xp + (size_t)(s1 < 0 ? 0 : s1) * H;
+    for (int c = lane; c < chunks; c += 128) {
+      uint4 v0[4], v1[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int cu = c + 32 * u;
+        if (cu < chunks) {
+          if (s0 >= 0) v0[u] = ld_nc_v4(src0 + (size_t)cu * 8);
+          if (s1 >= 0) v1[u] = ld_nc_v4(src1 + (size_t)cu * 8);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int cu = c + 32 * u;
+        if (cu < chunks) {
+          if (s0 >= 0) st_v4(dst0 + (size_t)cu * 8, v0[u]);
+          if (s1 >= 0) st_v4(dst1 + (size_t)cu * 8, v1[u]);
+        }
+      }
     }
-    for (; c < chunks; c += 32) st_v4(dst + (size_t)c * 8, ld_nc_v4(src + (size_t)c * 8));
   }
 }
 
@@ -335,31 +362,43 @@ static cudaError_t ensure_smem_attr(K kernel, bool* done_per_device) {
   return e;
 }
 
+// Tiles per route block: every warp gets at least one pass of tokens, and
+// there are at most kMaxRouteBlocks blocks.
+__host__ inline int route_tiles_per_block(long long T, int E) {
+  const int G = E <= 8 ? 1 : E <= 16 ? 2 : E <= 32 ? 4 : E <= 64 ? 8 : E <= 128 ? 16 : 32;
+  const int TT = tile_tokens(T);
+  const int tokens_per_pass = kWarps * (32 / G);
+  int tpb = tokens_per_pass >= TT ? tokens_per_pass / TT : 1;
+  const long long nt = num_tiles(T);
+  const long long need = (nt + kMaxRouteBlocks - 1) / kMaxRouteBlocks;
+  if (need > tpb) tpb = (int)need;
+  return tpb;
+}
+
 template <int G>
 static cudaError_t launch_route_g(const Args& a, bool vec, cudaStream_t st) {
   static bool done_vec[64] = {}, done_scalar[64] = {};
-  const int tokens_per_pass = kWarps * (32 / G);
-  Args b = a;
-  b.tiles_per_block = tokens_per_pass >= a.TT ? tokens_per_pass / a.TT : 1;
-  const long long tokens_per_block = (long long)b.tiles_per_block * a.TT;
+  const long long tokens_per_block = (long long)a.tiles_per_block * a.TT;
   const long long blocks = (a.T + tokens_per_block - 1) / tokens_per_block;
   const bool cos_smem = a.has_prev && a.E <= kSmemCoselMaxE;
-  const size_t smem = sizeof(uint32_t) * ((size_t)b.tiles_per_block * a.E + (cos_smem ? (size_t)a.E * a.E : 0));
+  const size_t smem = sizeof(uint32_t) * ((size_t)a.tiles_per_block * a.E + (cos_smem ? (size_t)a.E * a.E : 0));
   if (smem > (size_t)kRouteDynSmemMax) return cudaErrorInvalidValue;
   if (vec) {
     cudaError_t e = ensure_smem_attr(route_count_kernel<G, true>, done_vec);
     if (e != cudaSuccess) return e;
-    route_count_kernel<G, true><<<(unsigned)blocks, kThreads, smem, st>>>(b);
+    route_count_kernel<G, true><<<(unsigned)blocks, kThreads, smem, st>>>(a);
   } else {
     cudaError_t e = ensure_smem_attr(route_count_kernel<G, false>, done_scalar);
     if (e != cudaSuccess) return e;
-    route_count_kernel<G, false><<<(unsigned)blocks, kThreads, smem, st>>>(b);
+    route_count_kernel<G, false><<<(unsigned)blocks, kThreads, smem, st>>>(a);
   }
   return cudaGetLastError();
 }
 
-static cudaError_t launch(const Args& a, const uint16_t* x, int H, uint16_t* xp, int32_t* perm, int32_t* inv_perm,
+static cudaError_t launch(const Args& a0, const uint16_t* x, int H, uint16_t* xp, int32_t* perm, int32_t* inv_perm,
                           cudaStream_t st) {
+  Args a = a0;
+  a.tiles_per_block = route_tiles_per_block(a.T, a.E);
   const bool vec = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.logits) & 15) == 0);
   cudaError_t e;
   if (a.E <= 8) e = launch_route_g<1>(a, vec, st);
@@ -370,8 +409,9 @@ static cudaError_t launch(const Args& a, const uint16_t* x, int H, uint16_t* xp,
   else e = launch_route_g<32>(a, vec, st);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(int32_t) * ((size_t)(kWarps + 1) * a.E + (size_t)a.TT * a.k);
-  scatter_copy_kernel<<<(unsigned)a.ntiles, kThreads, smem, st>>>(a.idx, a.T, a.k, a.E, a.TT, a.counts, a.info, perm,
-                                                                  inv_perm, x, H, xp);
+  scatter_copy_kernel<<<(unsigned)a.ntiles, kThreads, smem, st>>>(a.idx, a.T, a.k, a.E, a.TT, a.tiles_per_block,
+                                                                  a.counts, a.blk_tot, a.info, perm, inv_perm, x, H,
+                                                                  xp);
   return cudaGetLastError();
 }
 

@@ -47,6 +47,11 @@ moe_status cuda_status(cudaError_t e, const char* where) {
   return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }
 
+moe_status cuda_at(const char* who, cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return MOE_OK;
+  return fail(MOE_ERR_CUDA, "%s: %s: %s", who, where, cudaGetErrorString(e));
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 constexpr int kMaxDevices = 64;
@@ -290,6 +295,7 @@ moe_status moe_stats_update(moe_stats* st, int64_t iter, int layer, const int32_
   a.k = k;
   a.E = E;
   a.acc_h = st->acc;
+  a.acc_h = st->acc;
   a.acc_c = st->acc + E;
   a.ticket = st->ticket;
   a.ring_h = st->ring_h + ((size_t)layer * s + slot) * E;
@@ -406,6 +412,7 @@ moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E,
   a.w = w;
   a.has_prev = layer > 0 ? 1 : 0;
   a.idx_prev = idx_prev;
+  a.acc_h = st->acc;
   a.acc_c = st->acc + E;
   a.ticket = st->ticket;
   a.ring_h = st->ring_h + ((size_t)layer * s + slot) * E;
@@ -427,35 +434,43 @@ moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E,
   a.TT = front::tile_tokens(T);
   a.ntiles = front::num_tiles(T);
   a.counts = static_cast<int32_t*>(workspace);
-  a.info = a.counts + a.ntiles * E;
+  a.blk_tot = a.counts + a.ntiles * E;
+  a.info = a.blk_tot + a.ntiles * E;
   a.group_offsets = group_offsets;
   return cuda_status(front::launch(a, x, H, xp, perm, inv_perm, static_cast<cudaStream_t>(stream)),
                      "moe_layer_front launch");
 }
 
 // ------------------------------------------------------------------ expert FFN
-moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, const int32_t* group_expert,
-                          const int32_t* rep_base, int E, int A, const uint16_t* w1, const uint16_t* w3,
-                          const uint16_t* w2, int H, int F, moe_act act, int small_group_threshold, uint16_t* y,
-                          void* workspace, size_t ws_bytes, void* stream) {
-  if (E < 1 || E > 256 || A < 0) return fail(MOE_ERR_INVALID, "moe_expert_ffn: need 1<=E<=256, A>=0");
-  if (H < 64 || H % 64 || F < 64 || F % 64) return fail(MOE_ERR_INVALID, "moe_expert_ffn: H and F must be positive multiples of 64");
-  if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) return fail(MOE_ERR_INVALID, "moe_expert_ffn: unknown activation");
-  if (small_group_threshold < 0) return fail(MOE_ERR_INVALID, "moe_expert_ffn: small_group_threshold must be >= 0");
+namespace {
+
+// Both FFN entry points.  a_src == null: A (GEMM1's input rows) is `a`
+// itself, [A, H] in dispatched order.  Otherwise `a` is x [T, H] and row i
+// of A is x[a_src[i] / k], gathered by GEMM1's loads.
+moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, int k, int T,
+                      const int32_t* group_offsets, const int32_t* group_expert, const int32_t* rep_base, int E, int A,
+                      const uint16_t* w1, const uint16_t* w3, const uint16_t* w2, int H, int F, moe_act act,
+                      int small_group_threshold, uint16_t* y, void* workspace, size_t ws_bytes, void* stream) {
+  const uint16_t* xp = a;
+  const bool gather = a_src != nullptr;
+  if (E < 1 || E > 256 || A < 0) return fail(MOE_ERR_INVALID, "%s: need 1<=E<=256, A>=0", who);
+  if (H < 64 || H % 64 || F < 64 || F % 64) return fail(MOE_ERR_INVALID, "%s: H and F must be positive multiples of 64", who);
+  if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) return fail(MOE_ERR_INVALID, "%s: unknown activation", who);
+  if (small_group_threshold < 0) return fail(MOE_ERR_INVALID, "%s: small_group_threshold must be >= 0", who);
   if ((long long)E * H >= (1LL << 31) || (long long)E * F >= (1LL << 31))
-    return fail(MOE_ERR_INVALID, "moe_expert_ffn: weights too large");
+    return fail(MOE_ERR_INVALID, "%s: weights too large", who);
   if (A == 0) return MOE_OK;
-  if (!xp || !group_offsets || !w1 || !w2 || !y || !workspace) return fail(MOE_ERR_INVALID, "moe_expert_ffn: null pointer");
-  if (act == MOE_ACT_SWIGLU && !w3) return fail(MOE_ERR_INVALID, "moe_expert_ffn: SwiGLU needs w3");
+  if (!xp || !group_offsets || !w1 || !w2 || !y || !workspace) return fail(MOE_ERR_INVALID, "%s: null pointer", who);
+  if (act == MOE_ACT_SWIGLU && !w3) return fail(MOE_ERR_INVALID, "%s: SwiGLU needs w3", who);
   if (!aligned(xp, 16) || !aligned(w1, 16) || !aligned(w2, 16) || !aligned(y, 16) || (w3 && !aligned(w3, 16)))
-    return fail(MOE_ERR_INVALID, "moe_expert_ffn: matrices must be 16-byte aligned");
-  if (!aligned(workspace, 16)) return fail(MOE_ERR_INVALID, "moe_expert_ffn: workspace must be 16-byte aligned");
+    return fail(MOE_ERR_INVALID, "%s: matrices must be 16-byte aligned", who);
+  if (!aligned(workspace, 16)) return fail(MOE_ERR_INVALID, "%s: workspace must be 16-byte aligned", who);
   if (ws_bytes < ffn_workspace_bytes(A, F))
-    return fail(MOE_ERR_WORKSPACE, "moe_expert_ffn: workspace needs %zu bytes", ffn_workspace_bytes(A, F));
+    return fail(MOE_ERR_WORKSPACE, "%s: workspace needs %zu bytes", who, ffn_workspace_bytes(A, F));
   const int G = group_expert ? 2 * E : E;
   const long long tiles_bound = ((long long)(A + ffn::BM - 1) / ffn::BM + G) *
                                 (long long)((F + 63) / 64 + (H + 63) / 64);
-  if (tiles_bound >= (1LL << 31)) return fail(MOE_ERR_INVALID, "moe_expert_ffn: problem too large");
+  if (tiles_bound >= (1LL << 31)) return fail(MOE_ERR_INVALID, "%s: problem too large", who);
 
   DeviceInfo* d = nullptr;
   moe_status ms = device_info(&d);
@@ -466,7 +481,8 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
   uint16_t* inter = static_cast<uint16_t*>(workspace);
 
   CUtensorMap mA1, mW1, mW3, mA2, mW2;
-  if ((ms = encode_2d(&mA1, xp, H, A, 64, ffn::BM)) != MOE_OK) return ms;
+  // gathered rows: a one-row box, four rows per copy (tile::gather4)
+  if ((ms = gather ? encode_2d(&mA1, xp, H, T, 64, 1) : encode_2d(&mA1, xp, H, A, 64, ffn::BM)) != MOE_OK) return ms;
   if ((ms = encode_2d(&mW1, w1, F, (uint64_t)E * H, 64, 64)) != MOE_OK) return ms;
   if (act == MOE_ACT_SWIGLU) {
     if ((ms = encode_2d(&mW3, w3, F, (uint64_t)E * H, 64, 64)) != MOE_OK) return ms;
@@ -497,8 +513,14 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
   g_opt_ffn_selftest = 0;
   p1.rep_base = rep_base;
   p1.small_threshold = small_group_threshold;
+  p1.a_src = a_src;
+  p1.a_src_div = gather ? k : 1;
+  p1.a_src_rows = gather ? T : 0;
   ffn::Params p2 = p1;
   p2.flags = 0;
+  p2.a_src = nullptr;
+  p2.a_src_div = 1;
+  p2.a_src_rows = 0;
   p2.K = F;
   p2.N_out = H;
   p2.out = y;
@@ -511,7 +533,10 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
   ps2.n_tiles = (H + ffn_small::BMF - 1) / ffn_small::BMF;
   const bool small_path = small_group_threshold > 0;
   if (small_path) {
-    if ((ms = encode_2d(&mS1, xp, H, A, 64, ffn_small::BT)) != MOE_OK) return ms;
+    if (gather)
+      mS1 = mA1;
+    else if ((ms = encode_2d(&mS1, xp, H, A, 64, ffn_small::BT)) != MOE_OK)
+      return ms;
     if ((ms = encode_2d(&mS2, inter, F, A, 64, ffn_small::BT)) != MOE_OK) return ms;
     std::lock_guard<std::mutex> lk(g_mu);
     for (int i = 0; i < 3; ++i) {
@@ -523,7 +548,7 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
                       : i == 1 ? (int)ffn_small::smem_bytes<ffn::kSwiglu>()
                                : (int)ffn_small::smem_bytes<ffn::kStore>();
       cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-      if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: cudaFuncSetAttribute (small)");
+      if (e != cudaSuccess) return cuda_at(who, e, "cudaFuncSetAttribute (small)");
       d->small_attr[i] = true;
     }
   }
@@ -559,7 +584,7 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
                        : i == 1 ? (const void*)ffn2::gemm_pair_kernel<ffn::kSwiglu>
                                 : (const void*)ffn2::gemm_pair_kernel<ffn::kStore>;
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ffn2::kSmemBytes);
-        if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: cudaFuncSetAttribute (pair)");
+        if (e != cudaSuccess) return cuda_at(who, e, "cudaFuncSetAttribute (pair)");
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (d->num_sms / 2), 1, 1);
         cfg.blockDim = dim3(ffn2::THREADS, 1, 1);
@@ -573,8 +598,8 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
         cfg.numAttrs = 1;
         int n = 0;
         e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
-        if (e != cudaSuccess || n < 1) return cuda_status(e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
-                                                          "moe_expert_ffn: cudaOccupancyMaxActiveClusters");
+        if (e != cudaSuccess || n < 1) return cuda_at(who, e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
+                                                          "cudaOccupancyMaxActiveClusters");
         d->pair_clusters[i] = n;
         d->pair_attr[i] = true;
       }
@@ -592,11 +617,11 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
     else
       ffn2::gemm_pair_kernel<ffn::kGelu><<<grid_for(p1, 0), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM1 (pair) launch");
-    if ((e = launch_small1()) != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM1 (small) launch");
+    if (e != cudaSuccess) return cuda_at(who, e, "GEMM1 (pair) launch");
+    if ((e = launch_small1()) != cudaSuccess) return cuda_at(who, e, "GEMM1 (small) launch");
     ffn2::gemm_pair_kernel<ffn::kStore><<<grid_for(p2, 2), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM2 (pair) launch");
-    return cuda_status(launch_small2(), "moe_expert_ffn: GEMM2 (small) launch");
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_at(who, e, "GEMM2 (pair) launch");
+    return cuda_at(who, launch_small2(), "GEMM2 (small) launch");
   }
 
   {
@@ -607,7 +632,7 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
                      : i == 1 ? (const void*)ffn::gemm_kernel<ffn::kSwiglu>
                               : (const void*)ffn::gemm_kernel<ffn::kStore>;
       cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ffn::kSmemBytes);
-      if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: cudaFuncSetAttribute");
+      if (e != cudaSuccess) return cuda_at(who, e, "cudaFuncSetAttribute");
       d->ffn_attr[i] = true;
     }
   }
@@ -624,11 +649,33 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
   else
     ffn::gemm_kernel<ffn::kGelu><<<grid_for(p1), ffn::THREADS, ffn::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM1 launch");
-  if ((e = launch_small1()) != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM1 (small) launch");
+  if (e != cudaSuccess) return cuda_at(who, e, "GEMM1 launch");
+  if ((e = launch_small1()) != cudaSuccess) return cuda_at(who, e, "GEMM1 (small) launch");
   ffn::gemm_kernel<ffn::kStore><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e, "moe_expert_ffn: GEMM2 launch");
-  return cuda_status(launch_small2(), "moe_expert_ffn: GEMM2 (small) launch");
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_at(who, e, "GEMM2 launch");
+  return cuda_at(who, launch_small2(), "GEMM2 (small) launch");
+}
+
+}  // namespace
+
+moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, const int32_t* group_expert,
+                          const int32_t* rep_base, int E, int A, const uint16_t* w1, const uint16_t* w3,
+                          const uint16_t* w2, int H, int F, moe_act act, int small_group_threshold, uint16_t* y,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  return expert_ffn("moe_expert_ffn", xp, nullptr, 1, 0, group_offsets, group_expert, rep_base, E, A, w1, w3, w2,
+                    H, F, act, small_group_threshold, y, workspace, ws_bytes, stream);
+}
+
+moe_status moe_expert_ffn_gather(const uint16_t* x, int T, const int32_t* perm, int k, const int32_t* group_offsets,
+                                 const int32_t* group_expert, const int32_t* rep_base, int E, const uint16_t* w1,
+                                 const uint16_t* w3, const uint16_t* w2, int H, int F, moe_act act,
+                                 int small_group_threshold, uint16_t* y, void* workspace, size_t ws_bytes,
+                                 void* stream) {
+  if (T < 0 || k < 1 || k > 8 || k > E) return fail(MOE_ERR_INVALID, "moe_expert_ffn_gather: need T>=0, 1<=k<=min(E,8)");
+  if ((long long)T * k >= (1LL << 31)) return fail(MOE_ERR_INVALID, "moe_expert_ffn_gather: T*k too large");
+  if (T > 0 && (!x || !perm)) return fail(MOE_ERR_INVALID, "moe_expert_ffn_gather: null pointer");
+  return expert_ffn("moe_expert_ffn_gather", x, T > 0 ? perm : nullptr, k, T, group_offsets, group_expert, rep_base,
+                    E, T * k, w1, w3, w2, H, F, act, small_group_threshold, y, workspace, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------ options

@@ -161,6 +161,7 @@ __device__ __forceinline__ void predict_block(const unsigned long long* __restri
                                               float* __restrict__ p_next) {
   __shared__ double ps[256];
   __shared__ double rinv[256];   // 1 / row sum, or 0 for an empty row
+  __shared__ unsigned long long rsum[256];
   __shared__ unsigned long long wsum[kThreads / 32];
   __shared__ unsigned long long cs[kPredictSmemE * kPredictSmemE];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -173,22 +174,30 @@ __device__ __forceinline__ void predict_block(const unsigned long long* __restri
   for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
   if (lane == 0) wsum[wid] = tot;
   __syncthreads();
+  // row sums of Cbar: one warp per row
+  if (csum) {
+    for (int e = wid; e < E; e += kThreads / 32) {
+      unsigned long long r = 0;
+      for (int e2 = lane; e2 < E; e2 += 32) r += stage ? cs[e * E + e2] : csum[(size_t)e * E + e2];
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+      if (lane == 0) rsum[e] = r;
+    }
+  }
   tot = 0;
   for (int w = 0; w < kThreads / 32; ++w) tot += wsum[w];
+  __syncthreads();
+  // the two divisions of each expert run side by side in its thread
   if (tid < E) {
     const double p = tot > 0 ? (double)h / (double)tot : 1.0 / (double)E;
     ps[tid] = p;
     p_seq[tid] = (float)p;
+    if (csum) {
+      const unsigned long long r = rsum[tid];
+      rinv[tid] = r > 0 ? 1.0 / (double)r : 0.0;
+    }
   }
   if (!csum) return;
-  // row sums: one warp per row
-  for (int e = wid; e < E; e += kThreads / 32) {
-    unsigned long long r = 0;
-    for (int e2 = lane; e2 < E; e2 += 32) r += stage ? cs[e * E + e2] : csum[(size_t)e * E + e2];
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
-    if (lane == 0) rinv[e] = r > 0 ? 1.0 / (double)r : 0.0;
-  }
   __syncthreads();
   const double uni = 1.0 / (double)E;
   if (cond) {
@@ -198,14 +207,34 @@ __device__ __forceinline__ void predict_block(const unsigned long long* __restri
       cond[i] = (float)(ri > 0 ? (double)cv * ri : uni);
     }
   }
-  if (p_next && tid < E) {
-    double acc = 0.0;
-    for (int e = 0; e < E; ++e) {
-      const double ri = rinv[e];
-      const unsigned long long cv = stage ? cs[e * E + tid] : csum[(size_t)e * E + tid];
-      acc = fma(ps[e], ri > 0 ? (double)cv * ri : uni, acc);
+  if (p_next) {
+    // p_next[e'] = sum_e p_seq[e] * Pr(e'|e).  Thread t works on column
+    // e' = t / P and rows e = q, q + P, ... (q = t % P, P a power of two with
+    // P * E <= 256), two interleaved accumulators; the P partial sums of a
+    // column sit in P adjacent lanes and are added by a butterfly, so the
+    // order of the additions is fixed (the result is deterministic)
+    int P = 1;
+    while (P * 2 * E <= kThreads && P < 32) P *= 2;
+    const int col = tid / P, q = tid % P;
+    double a0 = 0.0, a1 = 0.0;
+    if (col < E) {
+      int e = q;
+      for (; e + P < E; e += 2 * P) {
+        const double r0 = rinv[e], r1 = rinv[e + P];
+        const unsigned long long c0 = stage ? cs[e * E + col] : csum[(size_t)e * E + col];
+        const unsigned long long c1 = stage ? cs[(e + P) * E + col] : csum[(size_t)(e + P) * E + col];
+        a0 = fma(ps[e], r0 > 0 ? (double)c0 * r0 : uni, a0);
+        a1 = fma(ps[e + P], r1 > 0 ? (double)c1 * r1 : uni, a1);
+      }
+      if (e < E) {
+        const double r0 = rinv[e];
+        const unsigned long long c0 = stage ? cs[e * E + col] : csum[(size_t)e * E + col];
+        a0 = fma(ps[e], r0 > 0 ? (double)c0 * r0 : uni, a0);
+      }
     }
-    p_next[tid] = (float)acc;
+    double acc = a0 + a1;
+    for (int off = 1; off < P; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (col < E && q == 0) p_next[col] = (float)acc;
   }
 }
 

@@ -12,8 +12,8 @@ from typing import Optional
 import torch
 
 from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT, MoEStats, moe_combine, moe_dispatch,
-               moe_expert_ffn, moe_layer_front, moe_predict, moe_replicate, moe_route, moe_stats_update,
-               workspace_bytes)
+               moe_expert_ffn, moe_expert_ffn_gather, moe_layer_front, moe_predict, moe_replicate, moe_route,
+               moe_stats_update, workspace_bytes)
 
 __all__ = ["MoELayerStep"]
 
@@ -26,11 +26,14 @@ class MoELayerStep:
     unchanged).  stats (MoEStats) is shared by all layers of a model.
     fused=True (needs stats) runs route, statistics, prediction, replicas and
     dispatch as moe_layer_front (two launches); fused=False makes the five
-    separate calls.  Both give identical results."""
+    separate calls.  gather=True leaves the token rows in place: dispatch
+    writes only the permutation and the FFN's first GEMM reads the rows of x
+    through it (moe_expert_ffn_gather); gather=False copies the rows into
+    dispatch order first.  All four combinations give identical results."""
 
     def __init__(self, T: int, E: int, k: int, H: int, F: int, act: str, stats: Optional[MoEStats] = None,
                  replicate: bool = True, thresh=(6, 5), max_copies: int = -1, renorm: bool = True,
-                 small_group_threshold: int = 64, fused: bool = True, device="cuda"):
+                 small_group_threshold: int = 64, fused: bool = True, gather: bool = False, device="cuda"):
         self.T, self.E, self.k, self.H, self.F, self.act = T, E, k, H, F, act
         self.A = T * k
         self.stats = stats
@@ -38,6 +41,7 @@ class MoELayerStep:
         self.thresh, self.max_copies, self.renorm = thresh, max_copies, renorm
         self.small = small_group_threshold
         self.fused = fused and stats is not None
+        self.gather = gather
         d = torch.device(device)
         i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
         A = self.A
@@ -53,7 +57,7 @@ class MoELayerStep:
         self.go = torch.empty(2 * E + 1, dtype=i32, device=d)
         self.perm = torch.empty(A, dtype=i32, device=d)
         self.inv = torch.empty(A, dtype=i32, device=d)
-        self.xp = torch.empty((A, H), dtype=bf, device=d)
+        self.xp = None if gather else torch.empty((A, H), dtype=bf, device=d)
         self.y = torch.empty((A, H), dtype=bf, device=d)
         self.ws_dispatch = torch.empty(max(workspace_bytes(MOE_OP_DISPATCH, T, k, E),
                                            workspace_bytes(MOE_OP_LAYER_FRONT, T, k, E), 16),
@@ -61,9 +65,6 @@ class MoELayerStep:
         self.ws_ffn = torch.empty(max(workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F), 1024), dtype=torch.uint8,
                                   device=d)
         self._cur = 0
-        # launches per call of run(): route, stats, [predict], replicate, dispatch x4, ffn x2, combine
-        self.kernels_per_layer = {"route": 1, "stats": 1, "predict": 1, "replicate": 1, "dispatch": 4, "ffn": 2,
-                                  "combine": 1}
 
     def run(self, it: int, layer: int, logits, x, weights, out, events=None, predict: bool = True):
         """Enqueue one layer.  weights = (w1, w3 or None, w2).  `events`, if
@@ -82,12 +83,12 @@ class MoELayerStep:
                          "cond": None if last else self.cond, "p_next": None if last else self.p_next,
                          "copies": self.copies, "rep_base": self.rep_base, "group_expert": self.group_expert,
                          "group_offsets": self.go, "perm": self.perm, "inv_perm": self.inv, "xp": self.xp}
-            moe_layer_front(logits, x, self.stats, it, layer, self.k, idx_prev=prev, renorm=self.renorm,
-                            predict=predict, replicate=self.replicate, thresh=self.thresh,
+            moe_layer_front(logits, None if self.gather else x, self.stats, it, layer, self.k, idx_prev=prev,
+                            renorm=self.renorm, predict=predict, replicate=self.replicate, thresh=self.thresh,
                             max_copies=self.max_copies, out=out_front, workspace=self.ws_dispatch)
             mark("front", 1)
             rb, ge = (self.rep_base, self.group_expert) if self.replicate else (None, None)
-            return self._expert_and_combine(weights, rb, ge, out, mark)
+            return self._expert_and_combine(x, weights, rb, ge, out, mark)
         mark("route", 0)
         moe_route(logits, self.k, self.renorm, idx=idx, w=self.w)
         mark("route", 1)
@@ -107,14 +108,20 @@ class MoELayerStep:
             mark("replicate", 1)
             rb, ge = self.rep_base, self.group_expert
         mark("dispatch", 0)
-        moe_dispatch(x, idx, self.E, rb, out=(self.go, self.perm, self.inv, self.xp), workspace=self.ws_dispatch)
+        moe_dispatch(None if self.gather else x, idx, self.E, rb, out=(self.go, self.perm, self.inv, self.xp),
+                     workspace=self.ws_dispatch)
         mark("dispatch", 1)
-        return self._expert_and_combine(weights, rb, ge, out, mark)
+        return self._expert_and_combine(x, weights, rb, ge, out, mark)
 
-    def _expert_and_combine(self, weights, rb, ge, out, mark):
+    def _expert_and_combine(self, x, weights, rb, ge, out, mark):
         w1, w3, w2 = weights
         mark("ffn", 0)
-        moe_expert_ffn(self.xp, self.go, ge, rb, w1, w3, w2, self.act, self.small, y=self.y, workspace=self.ws_ffn)
+        if self.gather:
+            moe_expert_ffn_gather(x, self.perm, self.k, self.go, ge, rb, w1, w3, w2, self.act, self.small, y=self.y,
+                                  workspace=self.ws_ffn)
+        else:
+            moe_expert_ffn(self.xp, self.go, ge, rb, w1, w3, w2, self.act, self.small, y=self.y,
+                           workspace=self.ws_ffn)
         mark("ffn", 1)
         mark("combine", 0)
         moe_combine(self.y, self.inv, self.w, out=out)
@@ -126,7 +133,7 @@ class MoELayerStep:
         ffn = 2 + (2 if self.small > 0 else 0)
         if self.fused:
             return 2 + ffn + 1
-        n = 1 + 4 + ffn + 1
+        n = 1 + (3 if self.gather else 4) + ffn + 1
         if self.stats is not None:
             n += 1
             if layer < L - 1:
