@@ -63,6 +63,11 @@ struct DeviceInfo {
   bool pair_attr[3] = {false, false, false};
   bool small_attr[3] = {false, false, false};
   int pair_clusters[3] = {0, 0, 0};  // max co-resident CTA pairs per pair-kernel instance
+  // The FFN's small-batch kernels run as a second chain on this stream, forked
+  // from and joined back to the caller's stream (created once, kept for the
+  // life of the process).
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
 };
 
 // Library options (moe_set_option).
@@ -70,6 +75,7 @@ int g_opt_ffn_kernel = MOE_FFN_KERNEL_AUTO;
 int g_opt_ffn_selftest = 0;  // one-shot: next GEMM1 withholds an accumulator signal
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
+std::mutex g_side_mu;  // one fork/join sequence at a time per process
 
 moe_status device_info(DeviceInfo** out) {
   int dev = 0;
@@ -81,6 +87,10 @@ moe_status device_info(DeviceInfo** out) {
   if (!d.init) {
     e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_status(e, "cudaDeviceGetAttribute");
+    e = cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.fork_ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.join_ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_status(e, "device set-up (FFN side stream)");
     d.init = true;
   }
   *out = &d;
@@ -558,21 +568,43 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
     if (g > d->num_sms) g = d->num_sms;
     return (unsigned)(g < 1 ? 1 : g);
   };
-  auto launch_small1 = [&]() -> cudaError_t {
-    if (!small_path) return cudaSuccess;
+  // The small-batch kernels touch other rows of inter and y than the grouped
+  // kernels (experts below the threshold), so they form a second chain,
+  // small1 -> small2, on the device's side stream: forked from `st` before
+  // GEMM1 and joined back after GEMM2 (the whole sequence is enqueued under
+  // one lock, so concurrent callers cannot interleave their forks and joins).
+  auto launch_small_chain = [&](cudaStream_t ss) -> cudaError_t {
     if (epi1 == ffn::kSwiglu)
       ffn_small::small_kernel<ffn::kSwiglu><<<small_grid(ps1), ffn_small::THREADS,
-                                              ffn_small::smem_bytes<ffn::kSwiglu>(), st>>>(mS1, mW1, mW3, ps1);
+                                              ffn_small::smem_bytes<ffn::kSwiglu>(), ss>>>(mS1, mW1, mW3, ps1);
     else
       ffn_small::small_kernel<ffn::kGelu><<<small_grid(ps1), ffn_small::THREADS, ffn_small::smem_bytes<ffn::kGelu>(),
-                                            st>>>(mS1, mW1, mW3, ps1);
+                                            ss>>>(mS1, mW1, mW3, ps1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ffn_small::small_kernel<ffn::kStore><<<small_grid(ps2), ffn_small::THREADS, ffn_small::smem_bytes<ffn::kStore>(),
+                                           ss>>>(mS2, mW2, mW2, ps2);
     return cudaGetLastError();
   };
-  auto launch_small2 = [&]() -> cudaError_t {
+  std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
+  // forks the side chain off `st`, right before the first grouped kernel
+  auto fork = [&]() -> cudaError_t {
     if (!small_path) return cudaSuccess;
-    ffn_small::small_kernel<ffn::kStore><<<small_grid(ps2), ffn_small::THREADS, ffn_small::smem_bytes<ffn::kStore>(),
-                                           st>>>(mS2, mW2, mW2, ps2);
-    return cudaGetLastError();
+    side_lock.lock();
+    cudaError_t e = cudaEventRecord(d->fork_ev, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->side, d->fork_ev, 0);
+    if (e != cudaSuccess) side_lock.unlock();
+    return e;
+  };
+  // joins the side chain back into `st` (after the grouped kernels are enqueued)
+  auto finish = [&](cudaError_t e_main, const char* what) -> moe_status {
+    if (!small_path) return cuda_at(who, e_main, what);
+    cudaError_t e = launch_small_chain(d->side);
+    cudaError_t j = cudaEventRecord(d->join_ev, d->side);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(st, d->join_ev, 0);
+    if (e_main != cudaSuccess) return cuda_at(who, e_main, what);
+    if (e != cudaSuccess) return cuda_at(who, e, "small-batch kernels launch");
+    return cuda_at(who, j, "join of the small-batch chain");
   };
 
   if (use_pair) {
@@ -612,16 +644,15 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
       if (pairs > d->pair_clusters[inst]) pairs = d->pair_clusters[inst];
       return (unsigned)(2 * (pairs < 1 ? 1 : pairs));
     };
+    if (cudaError_t fe = fork(); fe != cudaSuccess) return cuda_at(who, fe, "fork of the small-batch chain");
     if (epi1 == ffn::kSwiglu)
       ffn2::gemm_pair_kernel<ffn::kSwiglu><<<grid_for(p1, 1), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
     else
       ffn2::gemm_pair_kernel<ffn::kGelu><<<grid_for(p1, 0), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_at(who, e, "GEMM1 (pair) launch");
-    if ((e = launch_small1()) != cudaSuccess) return cuda_at(who, e, "GEMM1 (small) launch");
+    if (e != cudaSuccess) return finish(e, "GEMM1 (pair) launch");
     ffn2::gemm_pair_kernel<ffn::kStore><<<grid_for(p2, 2), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_at(who, e, "GEMM2 (pair) launch");
-    return cuda_at(who, launch_small2(), "GEMM2 (small) launch");
+    return finish(cudaGetLastError(), "GEMM2 (pair) launch");
   }
 
   {
@@ -644,16 +675,15 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
     if (g > d->num_sms) g = d->num_sms;
     return (unsigned)(g < 1 ? 1 : g);
   };
+  if (cudaError_t fe = fork(); fe != cudaSuccess) return cuda_at(who, fe, "fork of the small-batch chain");
   if (epi1 == ffn::kSwiglu)
     ffn::gemm_kernel<ffn::kSwiglu><<<grid_for(p1), ffn::THREADS, ffn::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
   else
     ffn::gemm_kernel<ffn::kGelu><<<grid_for(p1), ffn::THREADS, ffn::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_at(who, e, "GEMM1 launch");
-  if ((e = launch_small1()) != cudaSuccess) return cuda_at(who, e, "GEMM1 (small) launch");
+  if (e != cudaSuccess) return finish(e, "GEMM1 launch");
   ffn::gemm_kernel<ffn::kStore><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_at(who, e, "GEMM2 launch");
-  return cuda_at(who, launch_small2(), "GEMM2 (small) launch");
+  return finish(cudaGetLastError(), "GEMM2 launch");
 }
 
 }  // namespace
