@@ -206,6 +206,17 @@ def load_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
+FFN_SOURCES = ("ffn.cuh", "ffn_pair.cuh", "ffn_small.cuh", "sm100_ptx.cuh")
+
+
+def ffn_source_hash():
+    """First 16 hex digits of the SHA-256 of the FFN kernel sources."""
+    h = hashlib.sha256()
+    for name in FFN_SOURCES:
+        h.update(open(os.path.join(ROOT, "moe_expert_routing_02_b300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def ffn_traffic_per_launch():
     """DRAM bytes per FFN call from the committed ncu summary, if it was taken
     on the current kernel source (else None)."""
@@ -217,8 +228,7 @@ def ffn_traffic_per_launch():
         if ":" in line:
             a, b = line.split(":", 1)
             kv[a.strip()] = b.strip()
-    src = os.path.join(ROOT, "moe_expert_routing_02_b300", "csrc", "ffn.cuh")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = ffn_source_hash()
     if kv.get("ffn_source_sha256_16") != h:
         return None
     try:

@@ -32,7 +32,12 @@
  *   by the caller (size from moe_workspace_bytes).  Every call only enqueues
  *   work on `stream` and returns; none synchronises except moe_check,
  *   moe_stats_export and moe_stats_import.  Calls that share a moe_stats
- *   handle or a workspace must be ordered on one stream.
+ *   handle or a workspace must be ordered on one stream.  The expert FFN
+ *   runs its small-batch kernels on a library-owned stream per device
+ *   (created with two events at the first call on that device, kept for the
+ *   life of the process), forked from `stream` and joined back to it within
+ *   the call, so callers see ordinary stream order; FFN calls on different
+ *   streams share that side stream.
  *
  * Errors
  *   Every call returns a moe_status.  Arguments are validated on the host
