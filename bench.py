@@ -63,6 +63,10 @@ def parse_args(argv=None):
                     help="run only the first N layers (small profiling captures; not a bench line)")
     ap.add_argument("--T", type=int, default=0, help="override tokens (small profiling captures; not a bench line)")
     ap.add_argument("--E", type=int, default=0, help="override experts (small profiling captures; not a bench line)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time each stage alone over T = 2^14 .. 2^20 (one JSON line per T; not the bench line)")
+    ap.add_argument("--sweep-min-log2", type=int, default=14)
+    ap.add_argument("--sweep-max-log2", type=int, default=20)
     return ap.parse_args(argv)
 
 
@@ -537,8 +541,94 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_sweep(args):
+    """Every stage of the path timed alone over T = 2^14 .. 2^20 tokens with the
+    moe_gpt_stream workload's distributions (E=16, top-2, H=1024, Zipf bias,
+    correlated second layer).  Each stage: 5 warm-up calls, then 20 calls,
+    each preceded by a write of 2x the L2 size (L2 flushed) and timed alone with
+    CUDA events; median, p10 and p90.  Fraction of HBM = algorithmic bytes /
+    median time / the measured copy bandwidth."""
+    import dataclasses
+    import torch
+    import moe_expert_routing_02_b300 as M
+    from moe_expert_routing_02_b300 import workloads as W
+    M.lib()
+    base = W.config_by_name(args.config)
+    peaks = load_peaks()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(2 * 126 * 2 ** 20, dtype=torch.uint8, device=dev)
+    for lg2 in range(args.sweep_min_log2, args.sweep_max_log2 + 1):
+        T = 2 ** lg2
+        c = dataclasses.replace(base, T=T, L=2)
+        E, k, H, A = c.E, c.k, c.H, T * c.k
+        lgs = [torch.from_numpy(l).to(dev) for l in W.make_layer_logits(c, 0, layers=2)]
+        x = W.make_x(c, 0, 1, device=dev)
+        st = M.MoEStats(2, E, c.window)
+        i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
+        idx0, w0 = M.moe_route(lgs[0], k)
+        idx1 = torch.empty((T, k), dtype=i32, device=dev)
+        w1 = torch.empty((T, k), dtype=f32, device=dev)
+        hist = torch.empty(E, dtype=i32, device=dev)
+        pred = (torch.empty(E, dtype=f32, device=dev), torch.empty((E, E), dtype=f32, device=dev),
+                torch.empty(E, dtype=f32, device=dev))
+        rep = (torch.empty(E, dtype=i32, device=dev), torch.empty(E + 1, dtype=i32, device=dev),
+               torch.empty(2 * E, dtype=i32, device=dev))
+        disp = (torch.empty(2 * E + 1, dtype=i32, device=dev), torch.empty(A, dtype=i32, device=dev),
+                torch.empty(A, dtype=i32, device=dev), torch.empty((A, H), dtype=bf, device=dev))
+        ws = torch.empty(max(M.workspace_bytes(M.MOE_OP_DISPATCH, T, k, E),
+                             M.workspace_bytes(M.MOE_OP_LAYER_FRONT, T, k, E), 16), dtype=torch.uint8, device=dev)
+        y = torch.zeros((A, H), dtype=bf, device=dev)
+        out = torch.empty((T, H), dtype=bf, device=dev)
+        M.moe_route(lgs[1], k, idx=idx1, w=w1)
+        M.moe_stats_update(st, 0, 1, idx1, idx0, hist_out=hist)
+        M.moe_replicate(hist, A, out=rep)
+        front_out = {"idx": idx1, "w": w1, "hist": hist, "p_seq": pred[0], "cond": None, "p_next": None,
+                     "copies": rep[0], "rep_base": rep[1], "group_expert": rep[2], "group_offsets": disp[0],
+                     "perm": disp[1], "inv_perm": disp[2], "xp": disp[3]}
+        stages = {
+            "route": (lambda: M.moe_route(lgs[1], k, idx=idx1, w=w1), T * E * 4 + A * 8),
+            "stats": (lambda: M.moe_stats_update(st, 0, 1, idx1, idx0, hist_out=hist),
+                      2 * A * 4 + (E + E * E) * 4 * 2 + (E + E * E) * 8 * 2),
+            "predict": (lambda: M.moe_predict(st, 0, out=pred), E * E * 8 + E * 8 + E * E * 4 + E * 8),
+            "replicate": (lambda: M.moe_replicate(hist, A, out=rep), E * 16),
+            "dispatch": (lambda: M.moe_dispatch(x, idx1, E, rep[1], out=disp, workspace=ws),
+                         A * 4 + T * H * 2 + A * H * 2 + 2 * A * 4),
+            "front": (lambda: M.moe_layer_front(lgs[1], x, st, 0, 1, k, idx_prev=idx0, out=front_out, workspace=ws),
+                      T * E * 4 + A * 8 + 2 * A * 4 + A * 4 + T * H * 2 + A * H * 2 + 2 * A * 4),
+            "combine": (lambda: M.moe_combine(y, disp[2], w1, out=out), A * H * 2 + A * 8 + T * H * 2),
+        }
+        res = {}
+        for name, (fn, nbytes) in stages.items():
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(20):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            M.moe_check()
+            ts.sort()
+            med = ts[len(ts) // 2]
+            gbs = nbytes / (med * 1e-6) / 1e9
+            res[name] = {"us_median": round(med, 2), "us_p10": round(ts[2], 2), "us_p90": round(ts[17], 2),
+                         "bytes": int(nbytes), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)}
+        print(json.dumps({"sweep": f"{c.name} distributions, each stage alone, L2 flushed before every call",
+                          "T": T, "E": E, "k": k, "H": H, "hbm_peak_gbs": peaks["hbm_gbs"],
+                          "peak_source": peaks["source"], "stages": res}), flush=True)
+        del lgs, x, st, idx0, w0, idx1, w1, disp, ws, y, out, front_out, stages
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))

@@ -8,13 +8,14 @@
 // Eq. (1) sequence popularity, Eq. (2)(3) next-layer popularity).  MoE-GPS
 // blog, section 2.1: p_i = n_i / N averaged over a sliding window.
 //
-// K2 is one launch: blocks count into shared memory with warp-aggregated
-// atomics (__match_any_sync: one atomic per distinct bin per warp), flush the
-// non-zero bins to a global accumulator, and the last block to finish (ticket
-// counter after a fence) moves the accumulator into ring slot iter % s,
-// updates the window sums by (new - old) and zeroes the accumulator for the
-// next call.  Counts are integers, so the result does not depend on the
-// order in which atomics land.
+// K2 is one launch: blocks walk the tokens grid-stride, each thread with the
+// choices of kTokensAhead tokens loaded before it counts them, and count into
+// shared memory with plain atomics (E bins, and the E*E co-selection bins
+// when E <= 64); blocks flush the non-zero bins to a global accumulator, and
+// the last block to finish (ticket counter after a fence) moves the
+// accumulator into ring slot iter % s, updates the window sums by
+// (new - old) and zeroes the accumulator for the next call.  Counts are
+// integers, so the result does not depend on the order in which atomics land.
 #pragma once
 #include "common.cuh"
 
@@ -38,13 +39,7 @@ struct UpdateArgs {
   int32_t* hist_out;        // [E] or null
 };
 
-__device__ __forceinline__ void agg_add(uint32_t* base, int bin, bool ok) {
-  // Lanes holding the same bin add once, by their lowest lane.
-  const int key = ok ? bin : -1;
-  const unsigned peers = __match_any_sync(0xffffffffu, key);
-  const int leader = __ffs(peers) - 1;
-  if (ok && (int)(threadIdx.x & 31) == leader) atomicAdd(base + bin, (uint32_t)__popc(peers));
-}
+constexpr int kTokensAhead = 4;
 
 __global__ void __launch_bounds__(kThreads) update_kernel(UpdateArgs a) {
   extern __shared__ uint32_t sh[];
@@ -53,55 +48,62 @@ __global__ void __launch_bounds__(kThreads) update_kernel(UpdateArgs a) {
   const bool cos_smem = cos && E <= kSmemCoselMaxE;
   uint32_t* sh_h = sh;
   uint32_t* sh_c = sh + E;
+  uint32_t* cbase = cos_smem ? sh_c : a.acc_c;
   const int nsh = E + (cos_smem ? E * E : 0);
   for (int i = threadIdx.x; i < nsh; i += kThreads) sh[i] = 0;
   __syncthreads();
 
-  const long long stride = (long long)gridDim.x * kThreads;
-  for (long long base = (long long)blockIdx.x * kThreads; base < a.T; base += stride) {
-    const long long t = base + threadIdx.x;
-    const bool live = t < a.T;
-    int cur[8], prv[8];
+  constexpr int U = kTokensAhead;
+  const long long stride = (long long)gridDim.x * kThreads * U;
+  bool bad = false;
+  for (long long base = (long long)blockIdx.x * kThreads * U + threadIdx.x; base < a.T; base += stride) {
+    // tokens base, base + kThreads, ... (coalesced across the block)
+    int cur[U][8], prv[U][8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      cur[r] = -1;
-      prv[r] = -1;
-      if (r < k && live) {
-        cur[r] = a.idx_cur[t * k + r];
-        if (cos) prv[r] = a.idx_prev[t * k + r];
+    for (int u = 0; u < U; ++u) {
+      const long long t = base + (long long)u * kThreads;
+      const bool live = t < a.T;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        cur[u][r] = -1;
+        prv[u][r] = -1;
+        if (r < k && live) {
+          cur[u][r] = a.idx_cur[t * k + r];
+          if (cos) prv[u][r] = a.idx_prev[t * k + r];
+        }
       }
     }
-    bool bad = false;
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      if (r < k) {
-        const bool okc = live && (unsigned)cur[r] < (unsigned)E;
-        bad |= live && !okc;
-        agg_add(sh_h, cur[r], okc);
+    for (int u = 0; u < U; ++u) {
+      const bool live = base + (long long)u * kThreads < a.T;
+      if (!live) continue;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r < k) {
+          if ((unsigned)cur[u][r] < (unsigned)E)
+            atomicAdd(sh_h + cur[u][r], 1u);
+          else
+            bad = true;
+        }
       }
-    }
-    if (cos) {
+      if (cos) {
 #pragma unroll
-      for (int r1 = 0; r1 < 8; ++r1) {
-        if (r1 < k) {
-          const bool okp = live && (unsigned)prv[r1] < (unsigned)E;
-          bad |= live && !okp;
-#pragma unroll
-          for (int r2 = 0; r2 < 8; ++r2) {
-            if (r2 < k) {
-              const bool ok = okp && (unsigned)cur[r2] < (unsigned)E;
-              const int bin = ok ? prv[r1] * E + cur[r2] : 0;
-              if (cos_smem)
-                agg_add(sh_c, bin, ok);
-              else
-                agg_add(a.acc_c, bin, ok);
+        for (int r1 = 0; r1 < 8; ++r1) {
+          if (r1 < k) {
+            const int p = prv[u][r1];
+            if ((unsigned)p >= (unsigned)E) {
+              bad = true;
+              continue;
             }
+#pragma unroll
+            for (int r2 = 0; r2 < 8; ++r2)
+              if (r2 < k && (unsigned)cur[u][r2] < (unsigned)E) atomicAdd(cbase + p * E + cur[u][r2], 1u);
           }
         }
       }
     }
-    if (bad) moe_flag_error(MOE_DEVERR_DATA);
   }
+  if (bad) moe_flag_error(MOE_DEVERR_DATA);
   __syncthreads();
   for (int i = threadIdx.x; i < E; i += kThreads)
     if (sh_h[i]) atomicAdd(a.acc_h + i, sh_h[i]);
@@ -138,8 +140,8 @@ __global__ void __launch_bounds__(kThreads) update_kernel(UpdateArgs a) {
 static cudaError_t launch_update(const UpdateArgs& a, int num_sms, cudaStream_t st) {
   const bool cos_smem = a.has_prev != 0 && a.E <= kSmemCoselMaxE;
   const size_t smem = sizeof(uint32_t) * (a.E + (cos_smem ? a.E * a.E : 0));
-  long long blocks = ((long long)a.T + 4 * kThreads - 1) / (4 * kThreads);
-  if (blocks > num_sms) blocks = num_sms;
+  long long blocks = ((long long)a.T + kTokensAhead * kThreads - 1) / (kTokensAhead * kThreads);
+  if (blocks > 2LL * num_sms) blocks = 2LL * num_sms;  // each block flushes up to E + E*E bins
   if (blocks < 1) blocks = 1;
   update_kernel<<<(int)blocks, kThreads, smem, st>>>(a);
   return cudaGetLastError();
