@@ -7,6 +7,7 @@ import pytest
 
 from oracle import moe_oracle as O
 import tests.test_oracle_pins as P
+import tests.test_oracle_prediction as PP
 
 
 def _topk_ties_reversed(logits, k, renorm=True):
@@ -110,12 +111,63 @@ def _combine_rank_swap(y, inv_perm, w):
     return ORIG["combine"](y, inv_perm, np.asarray(w)[:, ::-1])
 
 
+def _decay_age_off_by_one(self, layer, it, lam):
+    return ORIG["predict_decay"](self, layer, it + 1, lam)
+
+
+def _decay_cosel_same_age(self, layer, it, lam):
+    # co-selection ages counted from `it` instead of it - 1
+    E, s = self.E, self.s
+    p, _, _ = ORIG["predict_decay"](self, layer, it, lam)
+    if layer >= self.L - 1:
+        return p, None, None
+    Cb = sum((lam ** a if a else 1.0) * self.C[layer, (it - a) % s].astype(np.float64) for a in range(s))
+    rows = Cb.sum(axis=1, keepdims=True)
+    c = np.where(rows > 0, Cb / np.where(rows > 0, rows, 1), 1.0 / E)
+    return p, c, p @ c
+
+
+def _apportion_ties_high_first(p32, total):
+    p32 = np.asarray(p32, np.float32)
+    q = [max(float(v), 0.0) * total for v in p32]
+    f = [math.floor(v) for v in q]
+    left = total - sum(f)
+    order = sorted(range(len(q)), key=lambda e: (-(q[e] - f[e]), -e))
+    for e in order[:max(left, 0)]:
+        f[e] += 1
+    return np.array(f, np.int64)
+
+
+def _apportion_plain_round(p32, total):
+    return np.array([int(round(float(v) * total)) for v in np.asarray(p32, np.float32)], np.int64)
+
+
+def _cap_coldest_first(copies, load, budget):
+    copies = [int(c) for c in copies]
+    if budget < 0:
+        return np.array(copies, np.int32)
+    left, out = int(budget), [0] * len(copies)
+    for e in sorted(range(len(copies)), key=lambda e: (int(load[e]), e)):
+        out[e] = min(copies[e], left)
+        left -= out[e]
+    return np.array(out, np.int32)
+
+
+def _overlap_bottom(p_pred, load_actual, m=5):
+    p_pred = np.asarray(p_pred, np.float64)
+    load_actual = np.asarray(load_actual)
+    pred = sorted(range(p_pred.size), key=lambda e: (p_pred[e], e))[:m]
+    act = sorted(range(load_actual.size), key=lambda e: (-load_actual[e], e))[:m]
+    return len(set(pred) & set(act)) / m
+
+
 ORIG = {
     "topk_gate": O.topk_gate,
     "coselection": O.coselection,
     "predict": O.WindowStats.predict,
     "expert_ffn_rows": O.expert_ffn_rows,
     "combine": O.combine,
+    "predict_decay": O.WindowStats.predict_decay,
 }
 
 MUTANTS = [
@@ -130,6 +182,12 @@ MUTANTS = [
     ("_gelu", _gelu_tanh, [P.test_ffn_closed_form_values]),
     ("expert_ffn_rows", _ffn_drop_up, [lambda: P.test_ffn_matches_naive_triple_loop("swiglu")]),
     ("combine", _combine_rank_swap, [P.test_combine_hand_case]),
+    ("WindowStats.predict_decay", _decay_age_off_by_one, [PP.test_decay_hand_cases]),
+    ("WindowStats.predict_decay", _decay_cosel_same_age, [PP.test_decay_hand_cases]),
+    ("apportion", _apportion_ties_high_first, [PP.test_apportion_hand_cases]),
+    ("apportion", _apportion_plain_round, [PP.test_apportion_hand_cases]),
+    ("cap_copies", _cap_coldest_first, [PP.test_budget_hand_cases]),
+    ("top_overlap", _overlap_bottom, [PP.test_quality_hand_cases]),
 ]
 
 
