@@ -147,6 +147,25 @@ moe_status moe_predict(moe_stats* st, int layer, float* p_seq, float* cond,
                        float* p_next, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_predict_decay -- next-layer prediction from a decay-weighted window.
+ * MoE-GPS blog section 2.1: the sliding-window estimate p_i = n_i / N carries
+ * a decay factor against distribution drift (no formula printed).  Reading:
+ * with the causal order of the calls (layer j recorded at iteration `iter`,
+ * then predicted, then layer j+1 recorded), ring slot (iter - a) mod s of the
+ * histogram and slot (iter - 1 - a) mod s of the co-selection counts weigh
+ * lambda^a (a = 0 .. s-1, lambda^0 = 1); p_seq, cond and p_next are then
+ * formed as in moe_predict.  lambda = 1 gives moe_predict's results bit for
+ * bit; lambda = 0 uses the newest iteration only.
+ *   iter    >= 0, the iteration of the newest histogram of layer j
+ *   lambda  in [0, 1]
+ *   p_seq, cond, p_next as in moe_predict (cond/p_next NULL for the last
+ *           layer).  Computed in fp64 in one block; uses the handle's own
+ *           scratch, so calls on one handle must be ordered on one stream.
+ * ------------------------------------------------------------------------- */
+moe_status moe_predict_decay(moe_stats* st, int layer, int64_t iter, double lambda,
+                             float* p_seq, float* cond, float* p_next, void* stream);
+
+/* ---------------------------------------------------------------------------
  * moe_replicate -- replica counts for hot experts.
  * MoE-GPS blog section 2.1 (duplicate_experts): target = total / E; an
  * expert whose load exceeds (thresh_num/thresh_den) * target (6/5 = 1.2)
@@ -165,6 +184,31 @@ moe_status moe_predict(moe_stats* st, int layer, float* p_seq, float* cond,
 moe_status moe_replicate(const int32_t* load, int E, int64_t total, int thresh_num,
                          int thresh_den, int max_copies, int32_t* copies,
                          int32_t* rep_base, int32_t* group_expert, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_replicate_predicted -- replica table from a predicted popularity
+ * (prediction-driven replication: replicas placed before the layer runs).
+ * MoE-GPS blog section 2.1 (duplicate_experts rule on the predicted token
+ * distribution); MoE-MPMC summary, contribution 3 (replica counts bounded by
+ * a predefined memory budget).
+ *   p_next     [E] fp32 predicted shares (moe_predict's p_next of the layer
+ *              before); a negative share counts as 0, a NaN share also sets
+ *              the device error word
+ *   total      A = T*k assignments the prediction is for, 1 <= total < 2^29
+ *   load_out   [E] int32 out: the largest-remainder apportionment of total
+ *              by the shares (sums to total; quotas computed exactly from
+ *              the fp32 values; ties: lower expert first)
+ *   thresh_num/thresh_den, max_copies: the replica rule of moe_replicate on
+ *              load_out
+ *   budget     bound on the total number of extra copies (-1 = none); the
+ *              hottest experts (by load_out, lower expert first on ties)
+ *              keep their copies first
+ *   copies [E], rep_base [E+1], group_expert [2E]: as moe_replicate
+ * ------------------------------------------------------------------------- */
+moe_status moe_replicate_predicted(const float* p_next, int E, int64_t total, int thresh_num,
+                                   int thresh_den, int max_copies, int budget, int32_t* load_out,
+                                   int32_t* copies, int32_t* rep_base, int32_t* group_expert,
+                                   void* stream);
 
 /* ---------------------------------------------------------------------------
  * moe_dispatch -- stable permutation by expert, then replica.

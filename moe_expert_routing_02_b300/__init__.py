@@ -18,7 +18,7 @@ from typing import Optional
 
 __all__ = [
     "MoEError", "lib", "library_path", "MoEStats", "moe_route", "moe_stats_update", "moe_predict",
-    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_layer_front", "moe_expert_ffn", "moe_expert_ffn_gather", "moe_combine", "moe_check", "moe_error_word",
+    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_layer_front", "moe_expert_ffn", "moe_expert_ffn_gather", "moe_combine", "moe_predict_decay", "moe_replicate_predicted", "moe_check", "moe_error_word",
     "workspace_bytes", "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_ACT_GELU", "MOE_ACT_SWIGLU",
     "EXPORTED_SYMBOLS", "moe_set_option", "moe_get_option", "MOE_OPT_FFN_KERNEL", "MOE_FFN_KERNEL_AUTO",
     "MOE_FFN_KERNEL_SINGLE", "MOE_FFN_KERNEL_PAIR", "MOE_OPT_FFN_TIMEOUT_SELFTEST",
@@ -49,6 +49,8 @@ _SIGS = {
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_predict_decay": (_I, [_P, _I, ctypes.c_int64, ctypes.c_double, _P, _P, _P, _P]),
+    "moe_replicate_predicted": (_I, [_P, _I, ctypes.c_int64, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_expert_ffn_gather": (_I, [_P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
@@ -243,6 +245,47 @@ def moe_predict(stats: MoEStats, layer: int, want_cond: bool = True, want_next: 
     _check(lib().moe_predict(stats.handle, int(layer), _ptr(p_seq), _ptr(cond), _ptr(p_next), _stream(stream)),
            "moe_predict")
     return p_seq, cond, p_next
+
+
+def moe_predict_decay(stats: "MoEStats", layer: int, it: int, lam: float, want_cond: bool = True,
+                      want_next: Optional[bool] = None, out=None, stream=None):
+    """(p_seq [E], cond [E,E] or None, p_next [E] or None) from the
+    decay-weighted window (weights lam**age; lam = 1 is moe_predict)."""
+    torch = _torch()
+    E = stats.E
+    last = layer == stats.L - 1
+    if want_next is None:
+        want_next = not last
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if out is None:
+        p_seq = torch.empty(E, dtype=torch.float32, device=dev)
+        cond = torch.empty((E, E), dtype=torch.float32, device=dev) if (want_cond and not last) else None
+        p_next = torch.empty(E, dtype=torch.float32, device=dev) if (want_next and not last) else None
+    else:
+        p_seq, cond, p_next = out
+    _check(lib().moe_predict_decay(stats.handle, int(layer), int(it), float(lam), _ptr(p_seq), _ptr(cond),
+                                   _ptr(p_next), _stream(stream)), "moe_predict_decay")
+    return p_seq, cond, p_next
+
+
+def moe_replicate_predicted(p_next, total: int, thresh=(6, 5), max_copies: int = -1, budget: int = -1, out=None,
+                            stream=None):
+    """(load [E], copies [E], rep_base [E+1], group_expert [2E]) int32 from a
+    predicted popularity: largest-remainder loads of `total`, the replica rule,
+    the copy budget (-1 = none)."""
+    torch = _torch()
+    _dev(p_next, torch.float32, "p_next", 1)
+    E = p_next.numel()
+    if out is None:
+        out = (torch.empty(E, dtype=torch.int32, device=p_next.device),
+               torch.empty(E, dtype=torch.int32, device=p_next.device),
+               torch.empty(E + 1, dtype=torch.int32, device=p_next.device),
+               torch.empty(2 * E, dtype=torch.int32, device=p_next.device))
+    load, copies, rb, ge = out
+    _check(lib().moe_replicate_predicted(_ptr(p_next), E, int(total), int(thresh[0]), int(thresh[1]),
+                                         int(max_copies), int(budget), _ptr(load), _ptr(copies), _ptr(rb), _ptr(ge),
+                                         _stream(stream)), "moe_replicate_predicted")
+    return load, copies, rb, ge
 
 
 def moe_replicate(load, total: int, thresh=(6, 5), max_copies: int = -1, out=None, stream=None):

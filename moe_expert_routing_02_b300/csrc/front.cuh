@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
     }
   }
   __syncthreads();
-  if (a.p_seq) stats::predict_block(a.hsum, a.pred_csum, E, a.p_seq, a.cond, a.p_next);
+  if (a.p_seq) stats::predict_block<unsigned long long>(a.hsum, a.pred_csum, E, a.p_seq, a.cond, a.p_next);
   __syncthreads();
   const long long A = (long long)a.T * k;
   if (a.replicate)

@@ -144,6 +144,7 @@ struct moe_stats {
   unsigned long long* csum;          // [L-1][E][E]
   uint32_t* acc;                     // [E + E*E] (zero between calls)
   uint32_t* ticket;                  // [1]
+  double* dscratch;                  // [E + E*E] decay-weighted sums (moe_predict_decay), not exported
   size_t state_bytes;                // exported bytes (rings + sums), without header
 };
 
@@ -204,8 +205,9 @@ moe_status moe_stats_create(moe_stats** out, int L, int E, int window, void* str
   const size_t nc = (size_t)(L - 1) * window * E * E;
   const size_t ncs = (size_t)(L - 1) * E * E;
   const size_t nacc = (size_t)E + (size_t)E * E;
-  // layout: 8-byte sums first, then 4-byte arrays
-  const size_t bytes = (nhs + ncs) * 8 + (nh + nc + nacc + 1) * 4;
+  // layout: 8-byte sums first, then 4-byte arrays, then the fp64 scratch
+  const size_t four = ((nh + nc + nacc + 1) * 4 + 7) / 8 * 8;
+  const size_t bytes = (nhs + ncs) * 8 + four + nacc * 8;
   cudaError_t e = cudaMalloc(&st->block, bytes);
   if (e != cudaSuccess) {
     delete st;
@@ -224,6 +226,7 @@ moe_status moe_stats_create(moe_stats** out, int L, int E, int window, void* str
   st->acc = reinterpret_cast<uint32_t*>(p);
   p += nacc * 4;
   st->ticket = reinterpret_cast<uint32_t*>(p);
+  st->dscratch = reinterpret_cast<double*>(static_cast<char*>(st->block) + (nhs + ncs) * 8 + four);
   st->state_bytes = (nhs + ncs) * 8 + (nh + nc) * 4;
   e = cudaMemsetAsync(st->block, 0, bytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
@@ -330,6 +333,23 @@ moe_status moe_predict(moe_stats* st, int layer, float* p_seq, float* cond, floa
   return cuda_status(cudaGetLastError(), "moe_predict launch");
 }
 
+moe_status moe_predict_decay(moe_stats* st, int layer, int64_t iter, double lambda, float* p_seq, float* cond,
+                             float* p_next, void* stream) {
+  if (!st) return fail(MOE_ERR_INVALID, "moe_predict_decay: null handle");
+  if (layer < 0 || layer >= st->L) return fail(MOE_ERR_INVALID, "moe_predict_decay: layer out of range");
+  if (iter < 0) return fail(MOE_ERR_INVALID, "moe_predict_decay: iter must be >= 0");
+  if (!(lambda >= 0.0 && lambda <= 1.0)) return fail(MOE_ERR_INVALID, "moe_predict_decay: lambda must lie in [0, 1]");
+  if (!p_seq) return fail(MOE_ERR_INVALID, "moe_predict_decay: null p_seq");
+  if (layer == st->L - 1 && (cond || p_next))
+    return fail(MOE_ERR_INVALID, "moe_predict_decay: the last layer has no next layer (cond/p_next must be NULL)");
+  const int E = st->E, s = st->s;
+  const uint32_t* rh = st->ring_h + (size_t)layer * s * E;
+  const uint32_t* rc = (layer < st->L - 1) ? st->ring_c + (size_t)layer * s * E * E : nullptr;
+  stats::predict_decay_kernel<<<1, stats::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      rh, rc, E, s, (long long)iter, lambda, st->dscratch, p_seq, cond, p_next);
+  return cuda_status(cudaGetLastError(), "moe_predict_decay launch");
+}
+
 // ------------------------------------------------------------------ replicate
 moe_status moe_replicate(const int32_t* load, int E, int64_t total, int thresh_num, int thresh_den, int max_copies,
                          int32_t* copies, int32_t* rep_base, int32_t* group_expert, void* stream) {
@@ -342,6 +362,24 @@ moe_status moe_replicate(const int32_t* load, int E, int64_t total, int thresh_n
   return cuda_status(replicate::launch(load, E, total, thresh_num, thresh_den, max_copies, copies, rep_base,
                                        group_expert, static_cast<cudaStream_t>(stream)),
                      "moe_replicate launch");
+}
+
+moe_status moe_replicate_predicted(const float* p_next, int E, int64_t total, int thresh_num, int thresh_den,
+                                   int max_copies, int budget, int32_t* load_out, int32_t* copies, int32_t* rep_base,
+                                   int32_t* group_expert, void* stream) {
+  if (E < 1 || E > 256) return fail(MOE_ERR_INVALID, "moe_replicate_predicted: need 1<=E<=256");
+  if (total < 1 || total >= (1LL << 29))
+    return fail(MOE_ERR_INVALID, "moe_replicate_predicted: need 1 <= total < 2^29 (exact quotas)");
+  if (thresh_num < 1 || thresh_den < 1 || thresh_num > 1024 || thresh_den > 1024)
+    return fail(MOE_ERR_INVALID, "moe_replicate_predicted: threshold num/den must be in [1, 1024]");
+  if (max_copies < -1 || budget < -1)
+    return fail(MOE_ERR_INVALID, "moe_replicate_predicted: max_copies and budget must be >= -1");
+  if (!p_next || !load_out || !copies || !rep_base || !group_expert)
+    return fail(MOE_ERR_INVALID, "moe_replicate_predicted: null pointer");
+  return cuda_status(replicate::launch_predicted(p_next, E, total, thresh_num, thresh_den, max_copies, budget,
+                                                 load_out, copies, rep_base, group_expert,
+                                                 static_cast<cudaStream_t>(stream)),
+                     "moe_replicate_predicted launch");
 }
 
 // ------------------------------------------------------------------ dispatch

@@ -156,22 +156,24 @@ static cudaError_t launch_update(const UpdateArgs& a, int num_sms, cudaStream_t 
 constexpr int kPredictSmemE = 64;  // Cbar staged in shared memory up to E = 64
 
 // Block-level body (blockDim.x == kThreads).  Callable from any kernel whose
-// block reaches it with all threads.
-__device__ __forceinline__ void predict_block(const unsigned long long* __restrict__ hsum,
-                                              const unsigned long long* __restrict__ csum, int E,
+// block reaches it with all threads.  S is the type of the window sums:
+// unsigned long long (plain window) or double (decay-weighted window; integer
+// sums are exact in double, so both give the same result for equal sums).
+template <typename S>
+__device__ __forceinline__ void predict_block(const S* __restrict__ hsum, const S* __restrict__ csum, int E,
                                               float* __restrict__ p_seq, float* __restrict__ cond,
                                               float* __restrict__ p_next) {
   __shared__ double ps[256];
   __shared__ double rinv[256];   // 1 / row sum, or 0 for an empty row
-  __shared__ unsigned long long rsum[256];
-  __shared__ unsigned long long wsum[kThreads / 32];
-  __shared__ unsigned long long cs[kPredictSmemE * kPredictSmemE];
+  __shared__ S rsum[256];
+  __shared__ S wsum[kThreads / 32];
+  __shared__ S cs[kPredictSmemE * kPredictSmemE];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const bool stage = csum != nullptr && E <= kPredictSmemE;
-  unsigned long long h = tid < E ? hsum[tid] : 0ull;
+  S h = tid < E ? hsum[tid] : S(0);
   if (stage)
     for (int i = tid; i < E * E; i += kThreads) cs[i] = csum[i];
-  unsigned long long tot = h;
+  S tot = h;
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
   if (lane == 0) wsum[wid] = tot;
@@ -179,7 +181,7 @@ __device__ __forceinline__ void predict_block(const unsigned long long* __restri
   // row sums of Cbar: one warp per row
   if (csum) {
     for (int e = wid; e < E; e += kThreads / 32) {
-      unsigned long long r = 0;
+      S r = 0;
       for (int e2 = lane; e2 < E; e2 += 32) r += stage ? cs[e * E + e2] : csum[(size_t)e * E + e2];
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
@@ -195,7 +197,7 @@ __device__ __forceinline__ void predict_block(const unsigned long long* __restri
     ps[tid] = p;
     p_seq[tid] = (float)p;
     if (csum) {
-      const unsigned long long r = rsum[tid];
+      const S r = rsum[tid];
       rinv[tid] = r > 0 ? 1.0 / (double)r : 0.0;
     }
   }
@@ -205,7 +207,7 @@ __device__ __forceinline__ void predict_block(const unsigned long long* __restri
   if (cond) {
     for (int i = tid; i < E * E; i += kThreads) {
       const double ri = rinv[i / E];
-      const unsigned long long cv = stage ? cs[i] : csum[i];
+      const S cv = stage ? cs[i] : csum[i];
       cond[i] = (float)(ri > 0 ? (double)cv * ri : uni);
     }
   }
@@ -223,14 +225,14 @@ __device__ __forceinline__ void predict_block(const unsigned long long* __restri
       int e = q;
       for (; e + P < E; e += 2 * P) {
         const double r0 = rinv[e], r1 = rinv[e + P];
-        const unsigned long long c0 = stage ? cs[e * E + col] : csum[(size_t)e * E + col];
-        const unsigned long long c1 = stage ? cs[(e + P) * E + col] : csum[(size_t)(e + P) * E + col];
+        const S c0 = stage ? cs[e * E + col] : csum[(size_t)e * E + col];
+        const S c1 = stage ? cs[(e + P) * E + col] : csum[(size_t)(e + P) * E + col];
         a0 = fma(ps[e], r0 > 0 ? (double)c0 * r0 : uni, a0);
         a1 = fma(ps[e + P], r1 > 0 ? (double)c1 * r1 : uni, a1);
       }
       if (e < E) {
         const double r0 = rinv[e];
-        const unsigned long long c0 = stage ? cs[e * E + col] : csum[(size_t)e * E + col];
+        const S c0 = stage ? cs[e * E + col] : csum[(size_t)e * E + col];
         a0 = fma(ps[e], r0 > 0 ? (double)c0 * r0 : uni, a0);
       }
     }
@@ -244,7 +246,52 @@ __global__ void __launch_bounds__(kThreads) predict_kernel(const unsigned long l
                                                            const unsigned long long* __restrict__ csum, int E,
                                                            float* __restrict__ p_seq, float* __restrict__ cond,
                                                            float* __restrict__ p_next) {
-  predict_block(hsum, csum, E, p_seq, cond, p_next);
+  predict_block<unsigned long long>(hsum, csum, E, p_seq, cond, p_next);
+}
+
+// Decay-weighted window (MoE-GPS blog section 2.1: sliding-window average
+// with a decay factor against drift).  Under the causal order (layer j
+// recorded at iteration `iter`, then predicted, then layer j+1 recorded),
+// ring slot (iter - a) mod s of h_j and slot (iter - 1 - a) mod s of C_j
+// weigh lam^a, a = 0 .. s-1 (weights lam^a by repeated multiplication in
+// fp64, lam^0 = 1).  The weighted sums go to `scratch` ([E + E*E] doubles),
+// then the block predicts from them as from the plain window sums.
+__global__ void __launch_bounds__(kThreads) predict_decay_kernel(const uint32_t* __restrict__ ring_h,
+                                                                 const uint32_t* __restrict__ ring_c, int E, int s,
+                                                                 long long iter, double lam,
+                                                                 double* __restrict__ scratch,
+                                                                 float* __restrict__ p_seq,
+                                                                 float* __restrict__ cond,
+                                                                 float* __restrict__ p_next) {
+  __shared__ double w[1024];
+  for (int a = threadIdx.x; a < s; a += kThreads) {
+    double v = 1.0;
+    for (int q = 0; q < a; ++q) v *= lam;
+    w[a] = v;
+  }
+  __syncthreads();
+  double* H = scratch;
+  double* C = scratch + E;
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    double acc = 0.0;
+    for (int a = 0; a < s; ++a) {
+      const long long slot = ((iter - a) % s + s) % s;
+      acc += w[a] * (double)ring_h[(size_t)slot * E + e];
+    }
+    H[e] = acc;
+  }
+  if (ring_c) {
+    for (int i = threadIdx.x; i < E * E; i += kThreads) {
+      double acc = 0.0;
+      for (int a = 0; a < s; ++a) {
+        const long long slot = ((iter - 1 - a) % s + s) % s;
+        acc += w[a] * (double)ring_c[(size_t)slot * E * E + i];
+      }
+      C[i] = acc;
+    }
+  }
+  __syncthreads();  // the block's global writes are visible to the block after the barrier
+  predict_block<double>(H, ring_c ? C : nullptr, E, p_seq, cond, p_next);
 }
 
 }  // namespace stats
