@@ -250,13 +250,21 @@ moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int
  *   group_offsets [2E+1], perm, inv_perm, xp.
  *   workspace  ws_bytes >= moe_workspace_bytes(MOE_OP_LAYER_FRONT, T, k, E, H, 0),
  *              16-byte aligned
+ * Replication before routing (prediction-driven): rep_share [E] fp32 (for
+ * instance the p_next of the previous layer's prediction) makes the replica
+ * table that of moe_replicate_predicted(rep_share, T*k, ..., budget) instead
+ * of moe_replicate(hist, T*k) (T*k < 2^29); NULL keeps the layer's own
+ * histogram.  budget bounds the total copies in both cases (-1 = none;
+ * hottest experts first).  The tokens are still dispatched by their actual
+ * choices, split over the replica groups of their expert.
  * The first launch routes tiles of tokens and counts them; its last block
  * folds the window, predicts, replicates and lays out the groups; the second
  * scatters the permutation and copies the rows.  E must equal the handle's E.
  * ------------------------------------------------------------------------- */
 moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E, int k, int H, int renorm,
                            moe_stats* st, int64_t iter, int layer, const int32_t* idx_prev, int replicate,
-                           int thresh_num, int thresh_den, int max_copies, int32_t* idx, float* w,
+                           int thresh_num, int thresh_den, int max_copies, const float* rep_share, int budget,
+                           int32_t* idx, float* w,
                            int32_t* hist_out, float* p_seq, float* cond, float* p_next, int32_t* copies,
                            int32_t* rep_base, int32_t* group_expert, int32_t* group_offsets, int32_t* perm,
                            int32_t* inv_perm, uint16_t* xp, void* workspace, size_t ws_bytes, void* stream);

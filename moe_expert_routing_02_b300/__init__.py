@@ -63,8 +63,8 @@ _SIGS = {
     "moe_stats_import": (_I, [_P, _P, _SZ]),
     "moe_version": (ctypes.c_char_p, []),
     "moe_set_option": (_I, [_I, _I]),
-    "moe_layer_front": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _I64, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
-                             _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_layer_front": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _I64, _I, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P,
+                             _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_get_option": (_I, [_I, ctypes.POINTER(_I)]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -361,13 +361,15 @@ def moe_dispatch_noalloc(x, idx, E: int, rep_base=None, out=None, stream=None):
 
 
 def moe_layer_front(logits, x, stats: "MoEStats", it: int, layer: int, k: int, idx_prev=None, renorm: bool = True,
-                    predict: bool = True, replicate: bool = True, thresh=(6, 5), max_copies: int = -1, out=None,
-                    workspace=None, stream=None):
+                    predict: bool = True, replicate: bool = True, thresh=(6, 5), max_copies: int = -1,
+                    rep_share=None, budget: int = -1, out=None, workspace=None, stream=None):
     """Route + stats update + predict + replicate + dispatch of one layer in two
     launches (results identical to the separate calls).  Returns a dict of the
     outputs: idx, w, hist, p_seq, cond, p_next, copies, rep_base, group_expert,
     group_offsets, perm, inv_perm, xp (absent ones None).  `out` may hold
-    preallocated tensors under those names."""
+    preallocated tensors under those names.  rep_share ([E] float32, e.g. the
+    previous layer's p_next) takes the replica table from that prediction
+    instead of the layer's own histogram; budget bounds the total copies."""
     torch = _torch()
     _dev(logits, torch.float32, "logits", 2)
     T, E = logits.shape
@@ -400,9 +402,12 @@ def moe_layer_front(logits, x, stats: "MoEStats", it: int, layer: int, k: int, i
     xp = need("xp", (T * k, H), torch.bfloat16, x is not None)
     if workspace is None:
         workspace = torch.empty(max(workspace_bytes(MOE_OP_LAYER_FRONT, T, k, E), 16), dtype=torch.uint8, device=dev)
+    if rep_share is not None:
+        _dev(rep_share, torch.float32, "rep_share", 1)
     _check(lib().moe_layer_front(_ptr(logits), _ptr(x), T, E, k, H, int(bool(renorm)), stats.handle, int(it),
                                  int(layer), _ptr(idx_prev), int(bool(replicate)), int(thresh[0]), int(thresh[1]),
-                                 int(max_copies), _ptr(idx), _ptr(w), _ptr(hist), _ptr(p_seq), _ptr(cond),
+                                 int(max_copies), _ptr(rep_share), int(budget), _ptr(idx), _ptr(w), _ptr(hist),
+                                 _ptr(p_seq), _ptr(cond),
                                  _ptr(p_next), _ptr(copies), _ptr(rep_base), _ptr(group_expert), _ptr(go),
                                  _ptr(perm), _ptr(inv), _ptr(xp), _ptr(workspace), workspace.numel(),
                                  _stream(stream)), "moe_layer_front")

@@ -18,7 +18,9 @@
 //        - folds histogram and co-selection counts into the window ring and
 //          sums (as stats::update_kernel does),
 //        - predicts the next layer (stats::predict_block),
-//        - computes replica counts (replicate::replicate_block),
+//        - computes replica counts (replicate::replicate_block) from the
+//          histogram, or from the apportionment of a predicted popularity
+//          (replicate::apportion_block) when one is given,
 //        - lays out the groups (closed form of the round-robin split).
 //   F2 (scatter_copy_kernel), one block per tile: the tile's starting rank
 //      per expert (totals of the route blocks before its own, plus its
@@ -81,7 +83,8 @@ struct Args {
   float* cond;
   float* p_next;
   // replication
-  int replicate, num, den, max_copies;
+  int replicate, num, den, max_copies, budget;
+  const float* rep_share;  // [E] shares for the replica decision, or null (own histogram)
   int32_t* copies;
   int32_t* rep_base;
   int32_t* group_expert;
@@ -91,7 +94,7 @@ struct Args {
   long long ntiles;
   int32_t* counts;   // [ntiles][E]: tile's exclusive prefix within its route block
   int32_t* blk_tot;  // [route blocks][E]: block totals
-  int32_t* info;     // [4][E]: expert base, replicas, rows, -
+  int32_t* info;     // [4][E]: expert base, replicas, rows, loads from rep_share
   int32_t* group_offsets;
 };
 
@@ -205,8 +208,16 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
   if (a.p_seq) stats::predict_block<unsigned long long>(a.hsum, a.pred_csum, E, a.p_seq, a.cond, a.p_next);
   __syncthreads();
   const long long A = (long long)a.T * k;
-  if (a.replicate)
-    replicate::replicate_block(hist_s, E, A, a.num, a.den, a.max_copies, a.copies, a.rep_base, a.group_expert);
+  if (a.replicate) {
+    const int32_t* ld = hist_s;
+    if (a.rep_share) {  // replicas from a prediction: loads apportioned by the shares
+      replicate::apportion_block(a.rep_share, E, A, a.info + 3 * E);
+      __syncthreads();
+      ld = a.info + 3 * E;
+    }
+    replicate::replicate_block(ld, E, A, a.num, a.den, a.max_copies, a.copies, a.rep_base, a.group_expert,
+                               a.budget);
+  }
   __syncthreads();
   // group layout: expert bases (exclusive scan of the histogram), replicas,
   // group offsets in the closed form of the round-robin split

@@ -406,7 +406,8 @@ moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int
 // ------------------------------------------------------------------ fused front
 moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E, int k, int H, int renorm,
                            moe_stats* st, int64_t iter, int layer, const int32_t* idx_prev, int replicate,
-                           int thresh_num, int thresh_den, int max_copies, int32_t* idx, float* w,
+                           int thresh_num, int thresh_den, int max_copies, const float* rep_share, int budget,
+                           int32_t* idx, float* w,
                            int32_t* hist_out, float* p_seq, float* cond, float* p_next, int32_t* copies,
                            int32_t* rep_base, int32_t* group_expert, int32_t* group_offsets, int32_t* perm,
                            int32_t* inv_perm, uint16_t* xp, void* workspace, size_t ws_bytes, void* stream) {
@@ -423,8 +424,11 @@ moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E,
   if (!p_seq && (cond || p_next)) return fail(MOE_ERR_INVALID, "moe_layer_front: cond/p_next need p_seq");
   if (replicate && (!copies || !rep_base || !group_expert))
     return fail(MOE_ERR_INVALID, "moe_layer_front: replication needs copies, rep_base, group_expert");
-  if (replicate && (thresh_num < 1 || thresh_den < 1 || thresh_num > 1024 || thresh_den > 1024 || max_copies < -1))
-    return fail(MOE_ERR_INVALID, "moe_layer_front: bad replication threshold or cap");
+  if (replicate && (thresh_num < 1 || thresh_den < 1 || thresh_num > 1024 || thresh_den > 1024 || max_copies < -1 ||
+                    budget < -1))
+    return fail(MOE_ERR_INVALID, "moe_layer_front: bad replication threshold, cap or budget");
+  if (replicate && rep_share && (long long)T * k >= (1LL << 29))
+    return fail(MOE_ERR_INVALID, "moe_layer_front: replication from shares needs T*k < 2^29");
   if (!group_offsets) return fail(MOE_ERR_INVALID, "moe_layer_front: null group_offsets");
   if ((x == nullptr) != (xp == nullptr))
     return fail(MOE_ERR_INVALID, "moe_layer_front: x and xp must both be set or both NULL");
@@ -473,6 +477,8 @@ moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E,
   a.cond = cond;
   a.p_next = p_next;
   a.replicate = replicate ? 1 : 0;
+  a.rep_share = replicate ? rep_share : nullptr;
+  a.budget = budget;
   a.num = thresh_num;
   a.den = thresh_den;
   a.max_copies = max_copies;

@@ -12,8 +12,8 @@ from typing import Optional
 import torch
 
 from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT, MoEStats, moe_combine, moe_dispatch,
-               moe_expert_ffn, moe_expert_ffn_gather, moe_layer_front, moe_predict, moe_replicate, moe_route,
-               moe_stats_update, workspace_bytes)
+               moe_expert_ffn, moe_expert_ffn_gather, moe_layer_front, moe_predict, moe_replicate,
+               moe_replicate_predicted, moe_route, moe_stats_update, workspace_bytes)
 
 __all__ = ["MoELayerStep"]
 
@@ -29,11 +29,17 @@ class MoELayerStep:
     separate calls.  gather=True leaves the token rows in place: dispatch
     writes only the permutation and the FFN's first GEMM reads the rows of x
     through it (moe_expert_ffn_gather); gather=False copies the rows into
-    dispatch order first.  All four combinations give identical results."""
+    dispatch order first.  replicate_from="prediction" takes layer j's replica
+    table from the prediction made at layer j-1 (its p_next) instead of layer
+    j's own histogram -- replicas decided before routing -- with `budget`
+    bounding the total copies (-1 = none); layer 0 uses its histogram.  The
+    output is the same in every combination (replicas alias their expert's
+    weights)."""
 
     def __init__(self, T: int, E: int, k: int, H: int, F: int, act: str, stats: Optional[MoEStats] = None,
                  replicate: bool = True, thresh=(6, 5), max_copies: int = -1, renorm: bool = True,
-                 small_group_threshold: int = 64, fused: bool = True, gather: bool = False, device="cuda"):
+                 small_group_threshold: int = 64, fused: bool = True, gather: bool = False,
+                 replicate_from: str = "histogram", budget: int = -1, device="cuda"):
         self.T, self.E, self.k, self.H, self.F, self.act = T, E, k, H, F, act
         self.A = T * k
         self.stats = stats
@@ -41,6 +47,12 @@ class MoELayerStep:
         self.thresh, self.max_copies, self.renorm = thresh, max_copies, renorm
         self.small = small_group_threshold
         self.fused = fused and stats is not None
+        if replicate_from not in ("histogram", "prediction"):
+            raise ValueError("replicate_from must be 'histogram' or 'prediction'")
+        self.replicate_from = replicate_from
+        self.budget = budget
+        if budget >= 0 and not self.fused:
+            raise ValueError("a copies budget needs the fused front (fused=True with stats)")
         self.gather = gather
         d = torch.device(device)
         i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
@@ -50,8 +62,10 @@ class MoELayerStep:
         self.hist = torch.empty(E, dtype=i32, device=d)
         self.p_seq = torch.empty(E, dtype=f32, device=d)
         self.cond = torch.empty((E, E), dtype=f32, device=d)
-        self.p_next = torch.empty(E, dtype=f32, device=d)
+        self.pn = [torch.empty(E, dtype=f32, device=d) for _ in range(2)]  # ping-pong with idx
+        self.p_next = self.pn[0]
         self.copies = torch.empty(E, dtype=i32, device=d)
+        self.pred_load = torch.empty(E, dtype=i32, device=d)
         self.rep_base = torch.empty(E + 1, dtype=i32, device=d)
         self.group_expert = torch.empty(2 * E, dtype=i32, device=d)
         self.go = torch.empty(2 * E + 1, dtype=i32, device=d)
@@ -76,6 +90,9 @@ class MoELayerStep:
 
         prev = self.idx[self._cur ^ 1] if layer > 0 else None
         idx = self.idx[self._cur]
+        self.p_next = self.pn[self._cur]
+        # the prediction for this layer, made at the layer before (when there was one)
+        share = self.pn[self._cur ^ 1] if (self.replicate_from == "prediction" and layer > 0 and predict) else None
         if self.fused:
             last = layer == self.stats.L - 1
             mark("front", 0)
@@ -85,7 +102,8 @@ class MoELayerStep:
                          "group_offsets": self.go, "perm": self.perm, "inv_perm": self.inv, "xp": self.xp}
             moe_layer_front(logits, None if self.gather else x, self.stats, it, layer, self.k, idx_prev=prev,
                             renorm=self.renorm, predict=predict, replicate=self.replicate, thresh=self.thresh,
-                            max_copies=self.max_copies, out=out_front, workspace=self.ws_dispatch)
+                            max_copies=self.max_copies, rep_share=share, budget=self.budget, out=out_front,
+                            workspace=self.ws_dispatch)
             mark("front", 1)
             rb, ge = (self.rep_base, self.group_expert) if self.replicate else (None, None)
             return self._expert_and_combine(x, weights, rb, ge, out, mark)
@@ -103,8 +121,12 @@ class MoELayerStep:
         rb = ge = None
         if self.replicate:
             mark("replicate", 0)
-            moe_replicate(self.hist, self.A, self.thresh, self.max_copies,
-                          out=(self.copies, self.rep_base, self.group_expert))
+            if share is not None:
+                moe_replicate_predicted(share, self.A, self.thresh, self.max_copies, self.budget,
+                                        out=(self.pred_load, self.copies, self.rep_base, self.group_expert))
+            else:
+                moe_replicate(self.hist, self.A, self.thresh, self.max_copies,
+                              out=(self.copies, self.rep_base, self.group_expert))
             mark("replicate", 1)
             rb, ge = self.rep_base, self.group_expert
         mark("dispatch", 0)

@@ -90,3 +90,47 @@ def test_front_edges_and_oracle():
     out = M.moe_layer_front(torch.empty((0, 8), device="cuda"), None, st, 0, 0, 2)
     M.moe_check()
     assert out["group_offsets"].cpu().tolist() == [0] * 17
+
+
+@pytest.mark.parametrize("budget", [-1, 0, 2])
+def test_front_replicates_from_a_prediction(budget):
+    """rep_share: the front's replica table equals moe_replicate_predicted on
+    the same shares (and, with budget, the oracle's capped table); the rest of
+    the front is unchanged."""
+    c = W.config_by_name("moe_gpt_stream")
+    T, L = 4096, 3
+    st_a = M.MoEStats(L, c.E, c.window)
+    st_b = M.MoEStats(L, c.E, c.window)
+    lgs = W.make_layer_logits(c, 0, T=T, layers=L)
+    x = W.make_x(c, 0, 0, device="cuda", T=T)
+    prev_a = prev_b = None
+    share = None
+    for j in range(L):
+        lg = torch.from_numpy(lgs[j]).cuda()
+        a = M.moe_layer_front(lg, x, st_a, 0, j, c.k, idx_prev=prev_a, predict=True, replicate=True,
+                              rep_share=share, budget=budget)
+        b = _separate(lg, x, st_b, 0, j, c.k, prev_b, True, False)
+        if share is not None:
+            load, copies, rb, ge = M.moe_replicate_predicted(share, T * c.k, budget=budget)
+            p32 = share.cpu().numpy()
+            ol, oc, orb, oge = O.replicate_predicted(p32, T * c.k, budget=budget)
+            assert copies.cpu().numpy().tolist() == oc.tolist()
+        else:
+            copies, rb, ge = M.moe_replicate(b["hist"], T * c.k)
+            if budget >= 0:
+                oc = O.cap_copies(copies.cpu().numpy(), b["hist"].cpu().numpy(), budget)
+                copies = torch.from_numpy(oc).cuda()
+                rb = torch.from_numpy(np.concatenate([[0], np.cumsum(oc.astype(np.int64) + 1)]).astype(np.int32)).cuda()
+                ge_np = np.full(2 * c.E, -1, np.int32)
+                ge_np[:int(rb[-1])] = np.repeat(np.arange(c.E), oc + 1)
+                ge = torch.from_numpy(ge_np).cuda()
+        assert torch.equal(a["copies"], copies) and torch.equal(a["rep_base"], rb) and torch.equal(a["group_expert"], ge)
+        go, perm, inv, xp = M.moe_dispatch(x, b["idx"], c.E, rb)
+        for key, ref in (("idx", b["idx"]), ("w", b["w"]), ("hist", b["hist"]), ("p_seq", b["p_seq"]),
+                         ("group_offsets", go), ("perm", perm), ("inv_perm", inv), ("xp", xp)):
+            assert torch.equal(a[key], ref), (j, key)
+        if j < L - 1:
+            assert torch.equal(a["p_next"], b["p_next"])
+            share = a["p_next"].clone()
+        prev_a, prev_b = a["idx"], b["idx"]
+    M.moe_check()

@@ -181,3 +181,29 @@ def test_layer_step_gather_and_copy_identical(name):
     for key, res in outs.items():
         for a, b in zip(res, base):
             assert torch.equal(a, b), key
+
+
+def test_layer_step_prediction_driven_replication_same_output():
+    """Replicas from the previous layer's prediction (with and without a copies
+    budget, fused and separate calls) leave the layer output unchanged."""
+    c = W.config_by_name("moe_gpt_stream")
+    L = 3
+    weights = [W.make_weights(c, j, device="cuda") for j in range(L)]
+    outs = {}
+    for key, kw in {"hist": dict(), "pred": dict(replicate_from="prediction"),
+                    "pred_budget": dict(replicate_from="prediction", budget=1),
+                    "pred_unfused": dict(replicate_from="prediction", fused=False)}.items():
+        st = M.MoEStats(L, c.E, c.window)
+        step = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, stats=st, replicate=True, **kw)
+        res = []
+        for it in range(2):
+            lgs = W.make_layer_logits(c, it, layers=L)
+            for j in range(L):
+                out = torch.empty((c.T, c.H), dtype=torch.bfloat16, device="cuda")
+                step.run(it, j, dev(lgs[j]), W.make_x(c, it, j, device="cuda"), weights[j], out)
+                res.append(out)
+        M.moe_check()
+        outs[key] = res
+    for key, res in outs.items():
+        for a, b in zip(res, outs["hist"]):
+            assert torch.equal(a, b), key
