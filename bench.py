@@ -57,6 +57,8 @@ def parse_args(argv=None):
                     help="gather the rows in the FFN's loads (moe_expert_ffn_gather) instead of copying them")
     ap.add_argument("--unfused", action="store_true",
                     help="make the five separate front calls instead of moe_layer_front")
+    ap.add_argument("--ffn-kernel", choices=["auto", "single", "pair", "fused"], default="auto",
+                    help="grouped-GEMM kernel of the expert FFN (default: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (tokens of one layer)")
     ap.add_argument("--layers", type=int, default=0,
@@ -271,6 +273,9 @@ def run_ours(args, rank, world, local):
     step = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, stats=stats, replicate=True, fused=not args.unfused,
                         gather=args.gather, device=dev)
     stage_names = ["front", "ffn", "combine"] if step.fused else STAGES
+    M.moe_set_option(M.MOE_OPT_FFN_KERNEL, {"auto": M.MOE_FFN_KERNEL_AUTO, "single": M.MOE_FFN_KERNEL_SINGLE,
+                                            "pair": M.MOE_FFN_KERNEL_PAIR,
+                                            "fused": M.MOE_FFN_KERNEL_FUSED}[args.ffn_kernel])
 
     def run_step(it, ev=None):
         for j in range(c.L):
@@ -419,6 +424,7 @@ def run_ours(args, rank, world, local):
                    "l2": "no flush: each step streams ~1.5 GB of weights + activations, >> 126 MB L2",
                    "launch": "eager" if args.eager else f"CUDA graph per step ({c.window} graphs, one per window slot)",
                    "front": "separate calls" if args.unfused else "moe_layer_front (2 launches)",
+                   "ffn_kernel": args.ffn_kernel,
                    "ffn_input": "gathered from x in GEMM1's loads (tile::gather4)" if step.gather
                                 else "rows copied into dispatch order",
                    "stage_timing": "CUDA events around each stage, every layer of every timed step" if args.eager

@@ -295,7 +295,9 @@ moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E,
  *                  GroupGemm crossover); the others use the grouped kernel
  *   y              [A,H] bf16 out (fp32 accumulation, bf16 intermediate)
  *   workspace      ws_bytes >= moe_workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F)
- *                  with T*k = A; 16-byte aligned
+ *                  with T*k = A; 16-byte aligned (the bf16 intermediate
+ *                  [A,F], then one counter per 256-row block for the fused
+ *                  kernel, zeroed by the call)
  * H and F must be multiples of 64; all matrices 16-byte aligned.
  * ------------------------------------------------------------------------- */
 moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets,
@@ -372,12 +374,20 @@ moe_status moe_dispatch_noalloc(const uint16_t* x, const int32_t* idx, int T, in
 /* ---------------------------------------------------------------------------
  * Library options (process-wide, host side; no device work).
  *   MOE_OPT_FFN_KERNEL  which grouped-GEMM kernel moe_expert_ffn launches:
- *     MOE_FFN_KERNEL_AUTO   (default) the CTA-pair kernel (tcgen05
- *                           cta_group::2, 256-row tiles over two SMs) when the
- *                           experts average >= 256 rows (A >= 256*E), else the
- *                           single-CTA kernel (128-row tiles).  The choice
- *                           depends only on (A, E).
- *     MOE_FFN_KERNEL_SINGLE / MOE_FFN_KERNEL_PAIR  force one kernel.
+ *     MOE_FFN_KERNEL_AUTO   (default) when the experts average >= 256 rows
+ *                           (A >= 256*E): a CTA-pair kernel (tcgen05
+ *                           cta_group::2, 256-row tiles over two SMs) -- the
+ *                           fused one (both GEMMs in one launch, tiles
+ *                           interleaved block by block) when one expert's
+ *                           weights take at most 16 MB, else the two-launch
+ *                           one (moe_expert_ffn_gather always uses the
+ *                           two-launch one); otherwise the single-CTA kernel
+ *                           (128-row tiles).  The choice depends only on
+ *                           (A, E, H, F, act).
+ *     MOE_FFN_KERNEL_SINGLE / MOE_FFN_KERNEL_PAIR / MOE_FFN_KERNEL_FUSED
+ *                           force one kernel (PAIR: two launches).
+ * All kernels give bit-identical outputs except SINGLE vs the pair kernels
+ * (different tiles; the same math, within the FFN tolerance).
  *   MOE_OPT_FFN_TIMEOUT_SELFTEST  value 1 arms a one-shot self-test of the
  *     bounded waits: in the next moe_expert_ffn call, the first GEMM's CTA
  *     (pair) 0 never signals its first accumulator, so its epilogue's wait
@@ -388,7 +398,12 @@ moe_status moe_dispatch_noalloc(const uint16_t* x, const int32_t* idx, int T, in
  * concurrent moe_expert_ffn calls.
  * ------------------------------------------------------------------------- */
 typedef enum { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_FFN_TIMEOUT_SELFTEST = 2 } moe_option;
-typedef enum { MOE_FFN_KERNEL_AUTO = 0, MOE_FFN_KERNEL_SINGLE = 1, MOE_FFN_KERNEL_PAIR = 2 } moe_ffn_kernel;
+typedef enum {
+    MOE_FFN_KERNEL_AUTO = 0,
+    MOE_FFN_KERNEL_SINGLE = 1,
+    MOE_FFN_KERNEL_PAIR = 2,
+    MOE_FFN_KERNEL_FUSED = 3
+} moe_ffn_kernel;
 moe_status moe_set_option(int option, int value);
 moe_status moe_get_option(int option, int* value /* host */);
 

@@ -263,13 +263,6 @@ __device__ __forceinline__ Tile decode(const Smem& s, int U, int tile) {
   return t;
 }
 
-// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
-// 7.1.26 (Hastings' rational approximation): for x >= 0,
-//   erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2),
-//   t = 1 / (1 + p x),  |error| <= 1.5e-7,
-// extended to x < 0 by oddness.  In fp32 with the fast reciprocal and
-// exponential the error stays near 3e-7, far below the bf16 rounding of the
-// output (2^-9 relative).  Two MUFU operations and ten FMA-pipe operations.
 // Source rows of A rows row0 + 4*q .. row0 + 4*q + 3 (gathered A operand).
 // Rows past the operand's end read row 0: they fill the ragged tail of the
 // last tile, whose results are never stored.  A source outside [0, rows)
@@ -292,6 +285,13 @@ __device__ __forceinline__ int4 gather_src4(const Params& p, long long row0, int
   return make_int4(r[0], r[1], r[2], r[3]);
 }
 
+// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26 (Hastings' rational approximation): for x >= 0,
+//   erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2),
+//   t = 1 / (1 + p x),  |error| <= 1.5e-7,
+// extended to x < 0 by oddness.  In fp32 with the fast reciprocal and
+// exponential the error stays near 3e-7, far below the bf16 rounding of the
+// output (2^-9 relative).  Two MUFU operations and ten FMA-pipe operations.
 __device__ __forceinline__ float erf_as7126(float x) {
   const float ax = fabsf(x);
   const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));

@@ -20,6 +20,7 @@
 #include "front.cuh"
 #include "ffn.cuh"
 #include "ffn_pair.cuh"
+#include "ffn_fused.cuh"
 #include "ffn_small.cuh"
 #include "replicate.cuh"
 #include "route.cuh"
@@ -63,6 +64,8 @@ struct DeviceInfo {
   bool pair_attr[3] = {false, false, false};
   bool small_attr[3] = {false, false, false};
   int pair_clusters[3] = {0, 0, 0};  // max co-resident CTA pairs per pair-kernel instance
+  bool fused_attr[2] = {false, false};
+  int fused_clusters[2] = {0, 0};    // max co-resident CTA pairs of the fused kernel (GeLU, SwiGLU)
   // The FFN's small-batch kernels run as a second chain on this stream, forked
   // from and joined back to the caller's stream (created once, kept for the
   // life of the process).
@@ -126,10 +129,18 @@ moe_status encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t o
   return MOE_OK;
 }
 
-size_t ffn_workspace_bytes(long long A, int F) {
+// Upper bound on the 256-row blocks of the fused FFN kernel: each unit (at
+// most 2E of them) adds at most one partial block.
+long long ffn_blocks_bound(long long A, int E) { return (A + 255) / 256 + 2LL * E + 1; }
+
+size_t ffn_inter_bytes(long long A, int F) {
   // bf16 intermediate [A, F], 1024-byte aligned
-  const size_t inter = (size_t)A * (size_t)F * 2;
-  return ((inter + 1023) / 1024) * 1024 + 1024;
+  return (((size_t)A * (size_t)F * 2 + 1023) / 1024) * 1024;
+}
+
+size_t ffn_workspace_bytes(long long A, int F, int E) {
+  // intermediate, then the fused kernel's per-block counters
+  return ffn_inter_bytes(A, F) + (size_t)ffn_blocks_bound(A, E) * 4 + 1024;
 }
 
 }  // namespace
@@ -183,7 +194,7 @@ size_t moe_workspace_bytes(int op, int T, int k, int E, int H, int F) {
   if (op == MOE_OP_LAYER_FRONT) return front::workspace_bytes(T, E);
   if (op == MOE_OP_EXPERT_FFN) {
     if (F < 64 || F % 64 || H < 64 || H % 64) return 0;
-    return ffn_workspace_bytes(A, F);
+    return ffn_workspace_bytes(A, F, E);
   }
   return 0;
 }
@@ -519,8 +530,8 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   if (!aligned(xp, 16) || !aligned(w1, 16) || !aligned(w2, 16) || !aligned(y, 16) || (w3 && !aligned(w3, 16)))
     return fail(MOE_ERR_INVALID, "%s: matrices must be 16-byte aligned", who);
   if (!aligned(workspace, 16)) return fail(MOE_ERR_INVALID, "%s: workspace must be 16-byte aligned", who);
-  if (ws_bytes < ffn_workspace_bytes(A, F))
-    return fail(MOE_ERR_WORKSPACE, "%s: workspace needs %zu bytes", who, ffn_workspace_bytes(A, F));
+  if (ws_bytes < ffn_workspace_bytes(A, F, E))
+    return fail(MOE_ERR_WORKSPACE, "%s: workspace needs %zu bytes", who, ffn_workspace_bytes(A, F, E));
   const int G = group_expert ? 2 * E : E;
   const long long tiles_bound = ((long long)(A + ffn::BM - 1) / ffn::BM + G) *
                                 (long long)((F + 63) / 64 + (H + 63) / 64);
@@ -552,7 +563,18 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   // (A, E) only, so a call with and without replica groups takes the same path.
   bool use_pair = (long long)A >= 256LL * E;
   if (g_opt_ffn_kernel == MOE_FFN_KERNEL_SINGLE) use_pair = false;
-  if (g_opt_ffn_kernel == MOE_FFN_KERNEL_PAIR) use_pair = true;
+  if (g_opt_ffn_kernel == MOE_FFN_KERNEL_PAIR || g_opt_ffn_kernel == MOE_FFN_KERNEL_FUSED) use_pair = true;
+  // The fused kernel (both GEMMs in one launch) orders its tiles block by
+  // block, so every 256-row block reads all of its expert's weight columns:
+  // that pays while an expert's weights stay in L2 (measured: +6% at 8 MB per
+  // expert) and loses when they do not (-12..-15% at 235-400 MB per expert,
+  // re-read from DRAM per block), where the two-launch kernel's m-fastest
+  // order reuses each weight slice across blocks.  AUTO therefore takes it for
+  // experts of at most 16 MB of weights; never with gathered rows.
+  const long long expert_weight_bytes = (long long)(act == MOE_ACT_SWIGLU ? 3 : 2) * H * F * 2;
+  const bool use_fused = use_pair && !gather &&
+                         (g_opt_ffn_kernel == MOE_FFN_KERNEL_FUSED ||
+                          (g_opt_ffn_kernel == MOE_FFN_KERNEL_AUTO && expert_weight_bytes <= (16LL << 20)));
 
   ffn::Params p1;
   p1.group_offsets = group_offsets;
@@ -650,6 +672,59 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
     if (e != cudaSuccess) return cuda_at(who, e, "small-batch kernels launch");
     return cuda_at(who, j, "join of the small-batch chain");
   };
+
+  if (use_fused) {
+    const int fi = epi1 == ffn::kSwiglu ? 1 : 0;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (!d->fused_attr[fi]) {
+        const void* fn = fi ? (const void*)ffn3::ffn_fused_kernel<ffn::kSwiglu>
+                            : (const void*)ffn3::ffn_fused_kernel<ffn::kGelu>;
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ffn2::kSmemBytes);
+        if (e != cudaSuccess) return cuda_at(who, e, "cudaFuncSetAttribute (fused)");
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (d->num_sms / 2), 1, 1);
+        cfg.blockDim = dim3(ffn2::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = ffn2::kSmemBytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+        if (e != cudaSuccess || n < 1)
+          return cuda_at(who, e != cudaSuccess ? e : cudaErrorInvalidConfiguration,
+                         "cudaOccupancyMaxActiveClusters (fused)");
+        d->fused_clusters[fi] = n;
+        d->fused_attr[fi] = true;
+      }
+    }
+    ffn3::FusedParams fp;
+    fp.p1 = p1;
+    fp.p2 = p2;
+    fp.p1.n_tiles = act == MOE_ACT_SWIGLU ? (F + ffn2::BN / 2 - 1) / (ffn2::BN / 2) : (F + ffn2::BN - 1) / ffn2::BN;
+    fp.p2.n_tiles = (H + ffn2::BN - 1) / ffn2::BN;
+    const long long blocks = ffn_blocks_bound(A, E);
+    fp.done = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + ffn_inter_bytes(A, F));
+    const int npairs_max = d->fused_clusters[fi];
+    const int per_block = fp.p1.n_tiles + fp.p2.n_tiles;
+    fp.lag = (2 * npairs_max + per_block - 1) / per_block + 1;  // about two rounds of tiles
+    long long pairs = blocks * per_block;
+    if (pairs > npairs_max) pairs = npairs_max;
+    cudaError_t e = cudaMemsetAsync(fp.done, 0, (size_t)blocks * 4, st);
+    if (e != cudaSuccess) return cuda_at(who, e, "cudaMemsetAsync (block counters)");
+    if (cudaError_t fe = fork(); fe != cudaSuccess) return cuda_at(who, fe, "fork of the small-batch chain");
+    if (fi)
+      ffn3::ffn_fused_kernel<ffn::kSwiglu><<<(unsigned)(2 * pairs), ffn2::THREADS, ffn2::kSmemBytes, st>>>(
+          mA1, mW1, mW3, mA2, mW2, fp);
+    else
+      ffn3::ffn_fused_kernel<ffn::kGelu><<<(unsigned)(2 * pairs), ffn2::THREADS, ffn2::kSmemBytes, st>>>(
+          mA1, mW1, mW3, mA2, mW2, fp);
+    return finish(cudaGetLastError(), "fused FFN launch");
+  }
 
   if (use_pair) {
     {
@@ -755,7 +830,7 @@ moe_status moe_expert_ffn_gather(const uint16_t* x, int T, const int32_t* perm, 
 // ------------------------------------------------------------------ options
 moe_status moe_set_option(int option, int value) {
   if (option == MOE_OPT_FFN_KERNEL) {
-    if (value < MOE_FFN_KERNEL_AUTO || value > MOE_FFN_KERNEL_PAIR)
+    if (value < MOE_FFN_KERNEL_AUTO || value > MOE_FFN_KERNEL_FUSED)
       return fail(MOE_ERR_INVALID, "moe_set_option: unknown FFN kernel %d", value);
     g_opt_ffn_kernel = value;
     return MOE_OK;

@@ -60,8 +60,9 @@ def test_status_strings(L):
 def test_workspace_bytes(L):
     # dispatch: one int32 counter per (tile of 1024 assignments, expert) + 4E
     assert L.moe_workspace_bytes(M.MOE_OP_DISPATCH, 16384, 2, 16, 1024, 0) == (32 * 16 + 64) * 4
-    # ffn: bf16 intermediate [A, F] rounded up to 1 KB, plus 1 KB
-    assert L.moe_workspace_bytes(M.MOE_OP_EXPERT_FFN, 256, 2, 8, 64, 128) == 512 * 128 * 2 + 1024
+    # ffn: bf16 intermediate [A, F] rounded up to 1 KB, one uint32 counter per
+    # 256-row block of the fused kernel (A/256 rounded up, + 2E + 1), plus 1 KB
+    assert L.moe_workspace_bytes(M.MOE_OP_EXPERT_FFN, 256, 2, 8, 64, 128) == 512 * 128 * 2 + (2 + 16 + 1) * 4 + 1024
     assert L.moe_workspace_bytes(M.MOE_OP_EXPERT_FFN, 256, 2, 8, 64, 100) == 0   # F not a multiple of 64
     assert L.moe_workspace_bytes(99, 1, 1, 1, 64, 64) == 0
     assert L.moe_workspace_bytes(M.MOE_OP_DISPATCH, 16, 9, 16, 64, 64) == 0       # k > 8
