@@ -216,7 +216,7 @@ def load_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
-FFN_SOURCES = ("ffn.cuh", "ffn_pair.cuh", "ffn_small.cuh", "sm100_ptx.cuh")
+FFN_SOURCES = ("ffn.cuh", "ffn_pair.cuh", "ffn_fused.cuh", "ffn_small.cuh", "sm100_ptx.cuh")
 
 
 def ffn_source_hash():
@@ -407,7 +407,11 @@ def run_ours(args, rank, world, local):
                     "frac": round(achieved / peaks["hbm_gbs"], 4),
                     "peak_source": f"hbm_gbs of {peaks['source']} peaks",
                     "tflops": round(fl / ffn_t / 1e12, 1)}
-    roofline.update({"kernel": "moe_expert_ffn (GEMM1+GEMM2 launches)", "traffic": ffn_traffic_per_launch(),
+    n_ffn = M.moe_ffn_launches(c.A, c.E, c.H, c.F, c.act, 64, step.gather)
+    ffn_desc = ("moe_expert_ffn: fused GEMM1+GEMM2 launch" if n_ffn in (1, 3) else
+                "moe_expert_ffn: GEMM1 and GEMM2 launches") + (" (+2 small-batch launches on the side stream)"
+                                                               if n_ffn >= 3 else "")
+    roofline.update({"kernel": ffn_desc, "traffic": ffn_traffic_per_launch(),
                      "algorithmic_flops_per_call": fl, "algorithmic_bytes_per_call": by,
                      "arithmetic_intensity": round(fl / by, 1), "ridge_flop_per_byte": round(ridge, 1),
                      "experts_with_tokens": used})

@@ -407,6 +407,12 @@ typedef enum {
 moe_status moe_set_option(int option, int value);
 moe_status moe_get_option(int option, int* value /* host */);
 
+/* Kernel launches one moe_expert_ffn (gather = 0) or moe_expert_ffn_gather
+ * (gather = 1) call makes under the current options: 1 (fused) or 2 grouped
+ * launches, plus 2 small-batch launches when small_group_threshold > 0.
+ * 0 for bad sizes.  Host only. */
+int moe_ffn_launches(int A, int E, int H, int F, int act, int small_group_threshold, int gather);
+
 /* Workspace bytes for op (MOE_OP_DISPATCH or MOE_OP_EXPERT_FFN); 0 for bad sizes. */
 size_t moe_workspace_bytes(int op, int T, int k, int E, int H, int F);
 

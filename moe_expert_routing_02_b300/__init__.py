@@ -18,7 +18,7 @@ from typing import Optional
 
 __all__ = [
     "MoEError", "lib", "library_path", "MoEStats", "moe_route", "moe_stats_update", "moe_predict",
-    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_layer_front", "moe_expert_ffn", "moe_expert_ffn_gather", "moe_combine", "moe_predict_decay", "moe_replicate_predicted", "moe_check", "moe_error_word",
+    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_layer_front", "moe_expert_ffn", "moe_expert_ffn_gather", "moe_combine", "moe_predict_decay", "moe_replicate_predicted", "moe_ffn_launches", "moe_check", "moe_error_word",
     "workspace_bytes", "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_ACT_GELU", "MOE_ACT_SWIGLU",
     "EXPORTED_SYMBOLS", "moe_set_option", "moe_get_option", "MOE_OPT_FFN_KERNEL", "MOE_FFN_KERNEL_AUTO",
     "MOE_FFN_KERNEL_SINGLE", "MOE_FFN_KERNEL_PAIR", "MOE_FFN_KERNEL_FUSED", "MOE_OPT_FFN_TIMEOUT_SELFTEST",
@@ -49,6 +49,7 @@ _SIGS = {
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_ffn_launches": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_predict_decay": (_I, [_P, _I, ctypes.c_int64, ctypes.c_double, _P, _P, _P, _P]),
     "moe_replicate_predicted": (_I, [_P, _I, ctypes.c_int64, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_expert_ffn_gather": (_I, [_P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
@@ -482,6 +483,14 @@ def moe_expert_ffn_gather(x, perm, k: int, group_offsets, group_expert, rep_base
                                        int(small_group_threshold), _ptr(y), _ptr(workspace), workspace.numel(),
                                        _stream(stream)), "moe_expert_ffn_gather")
     return y
+
+
+def moe_ffn_launches(A: int, E: int, H: int, F: int, act: str = "gelu", small_group_threshold: int = 64,
+                     gather: bool = False) -> int:
+    """Kernel launches of one FFN call under the current options."""
+    act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
+    return int(lib().moe_ffn_launches(int(A), int(E), int(H), int(F), act_id, int(small_group_threshold),
+                                      int(bool(gather))))
 
 
 def moe_combine(y, inv_perm, w, out=None, stream=None):

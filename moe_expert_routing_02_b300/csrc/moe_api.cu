@@ -509,6 +509,24 @@ moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E,
 // ------------------------------------------------------------------ expert FFN
 namespace {
 
+// Kernel choice of the expert FFN (see moe_set_option): the CTA-pair kernels
+// when the experts average >= 256 rows; among them the fused one (both GEMMs
+// in one launch, tiles block by block) for experts of at most 16 MB of
+// weights -- it re-reads larger experts' weights from DRAM per 256-row block
+// (measured: +6% at 8 MB per expert, -12..-15% at 235-400 MB), where the
+// two-launch kernel's order reuses each weight slice across blocks -- and
+// never with gathered rows.  Depends only on the sizes and the options.
+void ffn_choice(long long A, int E, int H, int F, int act, bool gather, bool* use_pair, bool* use_fused) {
+  bool pair = A >= 256LL * E;
+  if (g_opt_ffn_kernel == MOE_FFN_KERNEL_SINGLE) pair = false;
+  if (g_opt_ffn_kernel == MOE_FFN_KERNEL_PAIR || g_opt_ffn_kernel == MOE_FFN_KERNEL_FUSED) pair = true;
+  const long long expert_weight_bytes = (long long)(act == MOE_ACT_SWIGLU ? 3 : 2) * H * F * 2;
+  *use_pair = pair;
+  *use_fused = pair && !gather &&
+               (g_opt_ffn_kernel == MOE_FFN_KERNEL_FUSED ||
+                (g_opt_ffn_kernel == MOE_FFN_KERNEL_AUTO && expert_weight_bytes <= (16LL << 20)));
+}
+
 // Both FFN entry points.  a_src == null: A (GEMM1's input rows) is `a`
 // itself, [A, H] in dispatched order.  Otherwise `a` is x [T, H] and row i
 // of A is x[a_src[i] / k], gathered by GEMM1's loads.
@@ -561,20 +579,8 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   // Kernel choice: the CTA-pair kernel works in 256-row pair tiles, so it is
   // used when the experts average at least 256 rows; the choice depends on
   // (A, E) only, so a call with and without replica groups takes the same path.
-  bool use_pair = (long long)A >= 256LL * E;
-  if (g_opt_ffn_kernel == MOE_FFN_KERNEL_SINGLE) use_pair = false;
-  if (g_opt_ffn_kernel == MOE_FFN_KERNEL_PAIR || g_opt_ffn_kernel == MOE_FFN_KERNEL_FUSED) use_pair = true;
-  // The fused kernel (both GEMMs in one launch) orders its tiles block by
-  // block, so every 256-row block reads all of its expert's weight columns:
-  // that pays while an expert's weights stay in L2 (measured: +6% at 8 MB per
-  // expert) and loses when they do not (-12..-15% at 235-400 MB per expert,
-  // re-read from DRAM per block), where the two-launch kernel's m-fastest
-  // order reuses each weight slice across blocks.  AUTO therefore takes it for
-  // experts of at most 16 MB of weights; never with gathered rows.
-  const long long expert_weight_bytes = (long long)(act == MOE_ACT_SWIGLU ? 3 : 2) * H * F * 2;
-  const bool use_fused = use_pair && !gather &&
-                         (g_opt_ffn_kernel == MOE_FFN_KERNEL_FUSED ||
-                          (g_opt_ffn_kernel == MOE_FFN_KERNEL_AUTO && expert_weight_bytes <= (16LL << 20)));
+  bool use_pair = false, use_fused = false;
+  ffn_choice(A, E, H, F, act, gather, &use_pair, &use_fused);
 
   ffn::Params p1;
   p1.group_offsets = group_offsets;
@@ -825,6 +831,13 @@ moe_status moe_expert_ffn_gather(const uint16_t* x, int T, const int32_t* perm, 
   if (T > 0 && (!x || !perm)) return fail(MOE_ERR_INVALID, "moe_expert_ffn_gather: null pointer");
   return expert_ffn("moe_expert_ffn_gather", x, T > 0 ? perm : nullptr, k, T, group_offsets, group_expert, rep_base,
                     E, T * k, w1, w3, w2, H, F, act, small_group_threshold, y, workspace, ws_bytes, stream);
+}
+
+int moe_ffn_launches(int A, int E, int H, int F, int act, int small_group_threshold, int gather) {
+  if (A <= 0 || E < 1 || E > 256 || H < 64 || F < 64) return 0;
+  bool use_pair = false, use_fused = false;
+  ffn_choice(A, E, H, F, act, gather != 0, &use_pair, &use_fused);
+  return (use_fused ? 1 : 2) + (small_group_threshold > 0 ? 2 : 0);
 }
 
 // ------------------------------------------------------------------ options

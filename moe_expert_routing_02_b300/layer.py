@@ -12,7 +12,7 @@ from typing import Optional
 import torch
 
 from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT, MoEStats, moe_combine, moe_dispatch,
-               moe_expert_ffn, moe_expert_ffn_gather, moe_layer_front, moe_predict, moe_replicate,
+               moe_expert_ffn, moe_expert_ffn_gather, moe_ffn_launches, moe_layer_front, moe_predict, moe_replicate,
                moe_replicate_predicted, moe_route, moe_stats_update, workspace_bytes)
 
 __all__ = ["MoELayerStep"]
@@ -152,7 +152,7 @@ class MoELayerStep:
         return out
 
     def launches(self, layer: int, L: int) -> int:
-        ffn = 2 + (2 if self.small > 0 else 0)
+        ffn = moe_ffn_launches(self.A, self.E, self.H, self.F, self.act, self.small, self.gather)
         if self.fused:
             return 2 + ffn + 1
         n = 1 + (3 if self.gather else 4) + ffn + 1
