@@ -57,6 +57,10 @@ def parse_args(argv=None):
                     help="gather the rows in the FFN's loads (moe_expert_ffn_gather) instead of copying them")
     ap.add_argument("--unfused", action="store_true",
                     help="make the five separate front calls instead of moe_layer_front")
+    ap.add_argument("--physical-replicas", action="store_true",
+                    help="copy each replica's weights into its own slot (moe_replicate_weights) before the FFN")
+    ap.add_argument("--replicate-from", choices=["histogram", "prediction"], default="histogram",
+                    help="replica table from the layer's own histogram or from the previous layer's prediction")
     ap.add_argument("--ffn-kernel", choices=["auto", "single", "pair", "fused"], default="auto",
                     help="grouped-GEMM kernel of the expert FFN (default: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -271,7 +275,10 @@ def run_ours(args, rank, world, local):
     outs = [torch.empty((c.T, c.H), dtype=torch.bfloat16, device=dev) for _ in range(c.L)]
     stats = M.MoEStats(c.L, c.E, c.window)
     step = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, stats=stats, replicate=True, fused=not args.unfused,
-                        gather=args.gather, device=dev)
+                        gather=args.gather, replicate_from=args.replicate_from,
+                        physical_replicas=args.physical_replicas, device=dev)
+    if args.physical_replicas:
+        weights = [MoELayerStep.replica_buffers(w) for w in weights]
     stage_names = ["front", "ffn", "combine"] if step.fused else STAGES
     M.moe_set_option(M.MOE_OPT_FFN_KERNEL, {"auto": M.MOE_FFN_KERNEL_AUTO, "single": M.MOE_FFN_KERNEL_SINGLE,
                                             "pair": M.MOE_FFN_KERNEL_PAIR,
@@ -423,12 +430,14 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": round(elapsed_max / K * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": c.name, "T": c.T, "L": c.L, "E": c.E, "k": c.k, "H": c.H, "F": c.F, "act": c.act,
-                   "window": c.window, "replication": "on (layer's own histogram)",
+                   "window": c.window, "replication": "on",
                    "parallelism": f"replicas x{world} (no data exchange)",
                    "l2": "no flush: each step streams ~1.5 GB of weights + activations, >> 126 MB L2",
                    "launch": "eager" if args.eager else f"CUDA graph per step ({c.window} graphs, one per window slot)",
                    "front": "separate calls" if args.unfused else "moe_layer_front (2 launches)",
                    "ffn_kernel": args.ffn_kernel,
+                   "replicas": ("physical copies (moe_replicate_weights)" if args.physical_replicas
+                                else "aliasing their expert's weights") + f", table from {args.replicate_from}",
                    "ffn_input": "gathered from x in GEMM1's loads (tile::gather4)" if step.gather
                                 else "rows copied into dispatch order",
                    "stage_timing": "CUDA events around each stage, every layer of every timed step" if args.eager

@@ -330,6 +330,44 @@ moe_status moe_expert_ffn_gather(const uint16_t* x, int T, const int32_t* perm, 
                                  size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_replicate_weights -- physical replica copies of hot experts' weights.
+ * MoE-MPMC summary, contribution 2 (predicted experts physically replicated
+ * on the GPU); PopFetcher review (expert copies moved on a separate stream).
+ * The replica table stays on the device, so a kernel makes the copies.
+ *   rep_base   [E+1] int32 device: moe_replicate's table (groups of expert e
+ *              are rep_base[e] .. rep_base[e+1]-1)
+ *   w_all      [2E-1, rows, cols] bf16: slots 0..E-1 hold the experts'
+ *              weights (the caller's); the call writes the extra replicas to
+ *              slots E.., expert e's q-th extra copy (q >= 1) to slot
+ *              E + (rep_base[e] - e) + q - 1.  NULL: only group_slot.
+ *              rows*cols a multiple of 8, 16-byte aligned.
+ *   group_slot [2E] int32 device out (nullable): weight slot of every group
+ *              (the expert's own slot for its first group, a copy's slot
+ *              for the others, -1 past the last group)
+ * Call once per weight matrix (w1, w3, w2: rows x cols = H x F or F x H).
+ * ------------------------------------------------------------------------- */
+moe_status moe_replicate_weights(const int32_t* rep_base, int E, uint16_t* w_all, int rows, int cols,
+                                 int32_t* group_slot, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_expert_ffn_slots -- the grouped expert FFN with each group reading
+ * its own weight slot (physical replicas, moe_replicate_weights).
+ *   group_slot  [G] int32: weight slot of group g (-1 / empty groups
+ *               allowed); G <= 512
+ *   n_slots     weight slots in w1/w3/w2 ([n_slots,H,F] / [n_slots,F,H]),
+ *               <= 512
+ *   the other arguments as moe_expert_ffn; workspace as for moe_expert_ffn
+ *   with G groups (moe_workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F)
+ *   covers G = 2E).
+ * The output equals moe_expert_ffn's with the logical table when the slots
+ * hold copies of the same weights (each row's arithmetic is the same).
+ * ------------------------------------------------------------------------- */
+moe_status moe_expert_ffn_slots(const uint16_t* xp, const int32_t* group_offsets, const int32_t* group_slot,
+                                int G, int n_slots, int A, const uint16_t* w1, const uint16_t* w3,
+                                const uint16_t* w2, int H, int F, moe_act act, int small_group_threshold,
+                                uint16_t* y, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * moe_combine -- gate-weighted sum of each token's expert outputs.
  * EPS-MoE review, compute/communication overlap (LocalReduce of expert
  * outputs); PopFetcher review (result collect).

@@ -18,7 +18,7 @@ from typing import Optional
 
 __all__ = [
     "MoEError", "lib", "library_path", "MoEStats", "moe_route", "moe_stats_update", "moe_predict",
-    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_layer_front", "moe_expert_ffn", "moe_expert_ffn_gather", "moe_combine", "moe_predict_decay", "moe_replicate_predicted", "moe_ffn_launches", "moe_check", "moe_error_word",
+    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_layer_front", "moe_expert_ffn", "moe_expert_ffn_gather", "moe_combine", "moe_predict_decay", "moe_replicate_predicted", "moe_ffn_launches", "moe_replicate_weights", "moe_expert_ffn_slots", "moe_check", "moe_error_word",
     "workspace_bytes", "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_ACT_GELU", "MOE_ACT_SWIGLU",
     "EXPORTED_SYMBOLS", "moe_set_option", "moe_get_option", "MOE_OPT_FFN_KERNEL", "MOE_FFN_KERNEL_AUTO",
     "MOE_FFN_KERNEL_SINGLE", "MOE_FFN_KERNEL_PAIR", "MOE_FFN_KERNEL_FUSED", "MOE_OPT_FFN_TIMEOUT_SELFTEST",
@@ -49,6 +49,8 @@ _SIGS = {
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_replicate_weights": (_I, [_P, _I, _P, _I, _I, _P, _P]),
+    "moe_expert_ffn_slots": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_ffn_launches": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_predict_decay": (_I, [_P, _I, ctypes.c_int64, ctypes.c_double, _P, _P, _P, _P]),
     "moe_replicate_predicted": (_I, [_P, _I, ctypes.c_int64, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
@@ -482,6 +484,49 @@ def moe_expert_ffn_gather(x, perm, k: int, group_offsets, group_expert, rep_base
                                        _ptr(rep_base), E, _ptr(w1), _ptr(w3), _ptr(w2), H, F, act_id,
                                        int(small_group_threshold), _ptr(y), _ptr(workspace), workspace.numel(),
                                        _stream(stream)), "moe_expert_ffn_gather")
+    return y
+
+
+def moe_replicate_weights(rep_base, w_all=None, group_slot=None, stream=None):
+    """Fill the replica slots of w_all [2E-1, rows, cols] (slots 0..E-1 = the
+    experts) from the device table rep_base [E+1]; returns group_slot [2E]."""
+    torch = _torch()
+    _dev(rep_base, torch.int32, "rep_base", 1)
+    E = rep_base.numel() - 1
+    rows = cols = 0
+    if w_all is not None:
+        _dev(w_all, torch.bfloat16, "w_all", 3)
+        if w_all.shape[0] != 2 * E - 1:
+            raise ValueError("w_all must hold 2E-1 slots")
+        rows, cols = int(w_all.shape[1]), int(w_all.shape[2])
+    if group_slot is None:
+        group_slot = torch.empty(2 * E, dtype=torch.int32, device=rep_base.device)
+    _check(lib().moe_replicate_weights(_ptr(rep_base), E, _ptr(w_all), rows, cols, _ptr(group_slot),
+                                       _stream(stream)), "moe_replicate_weights")
+    return group_slot
+
+
+def moe_expert_ffn_slots(xp, group_offsets, group_slot, w1, w3, w2, act: str = "gelu",
+                         small_group_threshold: int = 64, y=None, workspace=None, stream=None):
+    """Grouped expert FFN where group g reads weight slot group_slot[g]."""
+    torch = _torch()
+    _dev(xp, torch.bfloat16, "xp", 2)
+    _dev(group_offsets, torch.int32, "group_offsets", 1)
+    _dev(group_slot, torch.int32, "group_slot", 1)
+    A, H = xp.shape
+    S, H1, F = w1.shape
+    if H1 != H or tuple(w2.shape) != (S, F, H):
+        raise ValueError("weight shapes must be w1/w3 [S,H,F], w2 [S,F,H]")
+    G = group_slot.numel()
+    act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
+    if y is None:
+        y = torch.empty((A, H), dtype=torch.bfloat16, device=xp.device)
+    need = int(lib().moe_workspace_bytes(MOE_OP_EXPERT_FFN, A, 1, max((G + 1) // 2, 1), H, F))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=xp.device)
+    _check(lib().moe_expert_ffn_slots(_ptr(xp), _ptr(group_offsets), _ptr(group_slot), G, S, A, _ptr(w1), _ptr(w3),
+                                      _ptr(w2), H, F, act_id, int(small_group_threshold), _ptr(y), _ptr(workspace),
+                                      workspace.numel(), _stream(stream)), "moe_expert_ffn_slots")
     return y
 
 

@@ -22,6 +22,7 @@
 #include "ffn_pair.cuh"
 #include "ffn_fused.cuh"
 #include "ffn_small.cuh"
+#include "replica_copy.cuh"
 #include "replicate.cuh"
 #include "route.cuh"
 #include "stats.cuh"
@@ -131,16 +132,17 @@ moe_status encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t o
 
 // Upper bound on the 256-row blocks of the fused FFN kernel: each unit (at
 // most 2E of them) adds at most one partial block.
-long long ffn_blocks_bound(long long A, int E) { return (A + 255) / 256 + 2LL * E + 1; }
+long long ffn_blocks_bound(long long A, int G) { return (A + 255) / 256 + (long long)G + 1; }
 
 size_t ffn_inter_bytes(long long A, int F) {
   // bf16 intermediate [A, F], 1024-byte aligned
   return (((size_t)A * (size_t)F * 2 + 1023) / 1024) * 1024;
 }
 
-size_t ffn_workspace_bytes(long long A, int F, int E) {
+// G: group count of the call (2E for moe_expert_ffn's workspace size)
+size_t ffn_workspace_bytes(long long A, int F, int G) {
   // intermediate, then the fused kernel's per-block counters
-  return ffn_inter_bytes(A, F) + (size_t)ffn_blocks_bound(A, E) * 4 + 1024;
+  return ffn_inter_bytes(A, F) + (size_t)ffn_blocks_bound(A, G) * 4 + 1024;
 }
 
 }  // namespace
@@ -194,7 +196,7 @@ size_t moe_workspace_bytes(int op, int T, int k, int E, int H, int F) {
   if (op == MOE_OP_LAYER_FRONT) return front::workspace_bytes(T, E);
   if (op == MOE_OP_EXPERT_FFN) {
     if (F < 64 || F % 64 || H < 64 || H % 64) return 0;
-    return ffn_workspace_bytes(A, F, E);
+    return ffn_workspace_bytes(A, F, 2 * E);
   }
   return 0;
 }
@@ -531,12 +533,14 @@ void ffn_choice(long long A, int E, int H, int F, int act, bool gather, bool* us
 // itself, [A, H] in dispatched order.  Otherwise `a` is x [T, H] and row i
 // of A is x[a_src[i] / k], gathered by GEMM1's loads.
 moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, int k, int T,
-                      const int32_t* group_offsets, const int32_t* group_expert, const int32_t* rep_base, int E, int A,
+                      const int32_t* group_offsets, const int32_t* group_expert, int G, const int32_t* rep_base, int E,
+                      int A,
                       const uint16_t* w1, const uint16_t* w3, const uint16_t* w2, int H, int F, moe_act act,
                       int small_group_threshold, uint16_t* y, void* workspace, size_t ws_bytes, void* stream) {
   const uint16_t* xp = a;
   const bool gather = a_src != nullptr;
-  if (E < 1 || E > 256 || A < 0) return fail(MOE_ERR_INVALID, "%s: need 1<=E<=256, A>=0", who);
+  if (E < 1 || E > ffn::MAX_G || A < 0) return fail(MOE_ERR_INVALID, "%s: need 1<=E<=%d, A>=0", who, ffn::MAX_G);
+  if (G < 1 || G > ffn::MAX_G) return fail(MOE_ERR_INVALID, "%s: need 1 <= groups <= %d", who, ffn::MAX_G);
   if (H < 64 || H % 64 || F < 64 || F % 64) return fail(MOE_ERR_INVALID, "%s: H and F must be positive multiples of 64", who);
   if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) return fail(MOE_ERR_INVALID, "%s: unknown activation", who);
   if (small_group_threshold < 0) return fail(MOE_ERR_INVALID, "%s: small_group_threshold must be >= 0", who);
@@ -548,9 +552,8 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   if (!aligned(xp, 16) || !aligned(w1, 16) || !aligned(w2, 16) || !aligned(y, 16) || (w3 && !aligned(w3, 16)))
     return fail(MOE_ERR_INVALID, "%s: matrices must be 16-byte aligned", who);
   if (!aligned(workspace, 16)) return fail(MOE_ERR_INVALID, "%s: workspace must be 16-byte aligned", who);
-  if (ws_bytes < ffn_workspace_bytes(A, F, E))
-    return fail(MOE_ERR_WORKSPACE, "%s: workspace needs %zu bytes", who, ffn_workspace_bytes(A, F, E));
-  const int G = group_expert ? 2 * E : E;
+  if (ws_bytes < ffn_workspace_bytes(A, F, G))
+    return fail(MOE_ERR_WORKSPACE, "%s: workspace needs %zu bytes", who, ffn_workspace_bytes(A, F, G));
   const long long tiles_bound = ((long long)(A + ffn::BM - 1) / ffn::BM + G) *
                                 (long long)((F + 63) / 64 + (H + 63) / 64);
   if (tiles_bound >= (1LL << 31)) return fail(MOE_ERR_INVALID, "%s: problem too large", who);
@@ -713,7 +716,7 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
     fp.p2 = p2;
     fp.p1.n_tiles = act == MOE_ACT_SWIGLU ? (F + ffn2::BN / 2 - 1) / (ffn2::BN / 2) : (F + ffn2::BN - 1) / ffn2::BN;
     fp.p2.n_tiles = (H + ffn2::BN - 1) / ffn2::BN;
-    const long long blocks = ffn_blocks_bound(A, E);
+    const long long blocks = ffn_blocks_bound(A, G);
     fp.done = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + ffn_inter_bytes(A, F));
     const int npairs_max = d->fused_clusters[fi];
     const int per_block = fp.p1.n_tiles + fp.p2.n_tiles;
@@ -817,8 +820,9 @@ moe_status moe_expert_ffn(const uint16_t* xp, const int32_t* group_offsets, cons
                           const int32_t* rep_base, int E, int A, const uint16_t* w1, const uint16_t* w3,
                           const uint16_t* w2, int H, int F, moe_act act, int small_group_threshold, uint16_t* y,
                           void* workspace, size_t ws_bytes, void* stream) {
-  return expert_ffn("moe_expert_ffn", xp, nullptr, 1, 0, group_offsets, group_expert, rep_base, E, A, w1, w3, w2,
-                    H, F, act, small_group_threshold, y, workspace, ws_bytes, stream);
+  if (E < 1 || E > 256) return fail(MOE_ERR_INVALID, "moe_expert_ffn: need 1<=E<=256");
+  return expert_ffn("moe_expert_ffn", xp, nullptr, 1, 0, group_offsets, group_expert, group_expert ? 2 * E : E,
+                    rep_base, E, A, w1, w3, w2, H, F, act, small_group_threshold, y, workspace, ws_bytes, stream);
 }
 
 moe_status moe_expert_ffn_gather(const uint16_t* x, int T, const int32_t* perm, int k, const int32_t* group_offsets,
@@ -829,12 +833,37 @@ moe_status moe_expert_ffn_gather(const uint16_t* x, int T, const int32_t* perm, 
   if (T < 0 || k < 1 || k > 8 || k > E) return fail(MOE_ERR_INVALID, "moe_expert_ffn_gather: need T>=0, 1<=k<=min(E,8)");
   if ((long long)T * k >= (1LL << 31)) return fail(MOE_ERR_INVALID, "moe_expert_ffn_gather: T*k too large");
   if (T > 0 && (!x || !perm)) return fail(MOE_ERR_INVALID, "moe_expert_ffn_gather: null pointer");
-  return expert_ffn("moe_expert_ffn_gather", x, T > 0 ? perm : nullptr, k, T, group_offsets, group_expert, rep_base,
-                    E, T * k, w1, w3, w2, H, F, act, small_group_threshold, y, workspace, ws_bytes, stream);
+  if (E < 1 || E > 256) return fail(MOE_ERR_INVALID, "moe_expert_ffn_gather: need 1<=E<=256");
+  return expert_ffn("moe_expert_ffn_gather", x, T > 0 ? perm : nullptr, k, T, group_offsets, group_expert,
+                    group_expert ? 2 * E : E, rep_base, E, T * k, w1, w3, w2, H, F, act, small_group_threshold, y,
+                    workspace, ws_bytes, stream);
+}
+
+moe_status moe_expert_ffn_slots(const uint16_t* xp, const int32_t* group_offsets, const int32_t* group_slot, int G,
+                                int n_slots, int A, const uint16_t* w1, const uint16_t* w3, const uint16_t* w2, int H,
+                                int F, moe_act act, int small_group_threshold, uint16_t* y, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  if (!group_slot) return fail(MOE_ERR_INVALID, "moe_expert_ffn_slots: null group_slot");
+  return expert_ffn("moe_expert_ffn_slots", xp, nullptr, 1, 0, group_offsets, group_slot, G, nullptr, n_slots, A, w1,
+                    w3, w2, H, F, act, small_group_threshold, y, workspace, ws_bytes, stream);
+}
+
+moe_status moe_replicate_weights(const int32_t* rep_base, int E, uint16_t* w_all, int rows, int cols,
+                                 int32_t* group_slot, void* stream) {
+  if (E < 1 || E > 256) return fail(MOE_ERR_INVALID, "moe_replicate_weights: need 1<=E<=256");
+  if (!rep_base) return fail(MOE_ERR_INVALID, "moe_replicate_weights: null rep_base");
+  if (w_all && (rows < 1 || cols < 1 || ((long long)rows * cols) % 8 != 0 || !aligned(w_all, 16)))
+    return fail(MOE_ERR_INVALID, "moe_replicate_weights: rows*cols must be a positive multiple of 8, w_all 16-byte aligned");
+  DeviceInfo* d = nullptr;
+  moe_status ms = device_info(&d);
+  if (ms != MOE_OK) return ms;
+  return cuda_status(replica_copy::launch(rep_base, E, w_all, (long long)rows * cols, group_slot, d->num_sms,
+                                          static_cast<cudaStream_t>(stream)),
+                     "moe_replicate_weights launch");
 }
 
 int moe_ffn_launches(int A, int E, int H, int F, int act, int small_group_threshold, int gather) {
-  if (A <= 0 || E < 1 || E > 256 || H < 64 || F < 64) return 0;
+  if (A <= 0 || E < 1 || E > ffn::MAX_G || H < 64 || F < 64) return 0;
   bool use_pair = false, use_fused = false;
   ffn_choice(A, E, H, F, act, gather != 0, &use_pair, &use_fused);
   return (use_fused ? 1 : 2) + (small_group_threshold > 0 ? 2 : 0);

@@ -13,7 +13,8 @@ import torch
 
 from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT, MoEStats, moe_combine, moe_dispatch,
                moe_expert_ffn, moe_expert_ffn_gather, moe_ffn_launches, moe_layer_front, moe_predict, moe_replicate,
-               moe_replicate_predicted, moe_route, moe_stats_update, workspace_bytes)
+               moe_replicate_predicted, moe_replicate_weights, moe_expert_ffn_slots, moe_route, moe_stats_update,
+               workspace_bytes)
 
 __all__ = ["MoELayerStep"]
 
@@ -32,14 +33,17 @@ class MoELayerStep:
     dispatch order first.  replicate_from="prediction" takes layer j's replica
     table from the prediction made at layer j-1 (its p_next) instead of layer
     j's own histogram -- replicas decided before routing -- with `budget`
-    bounding the total copies (-1 = none); layer 0 uses its histogram.  The
-    output is the same in every combination (replicas alias their expert's
-    weights)."""
+    bounding the total copies (-1 = none); layer 0 uses its histogram.
+    physical_replicas=True copies each replica's weights into its own slot
+    (moe_replicate_weights) and runs the FFN over the slots; `weights` must
+    then be the buffers of replica_buffers().  The output is the same in
+    every combination."""
 
     def __init__(self, T: int, E: int, k: int, H: int, F: int, act: str, stats: Optional[MoEStats] = None,
                  replicate: bool = True, thresh=(6, 5), max_copies: int = -1, renorm: bool = True,
                  small_group_threshold: int = 64, fused: bool = True, gather: bool = False,
-                 replicate_from: str = "histogram", budget: int = -1, device="cuda"):
+                 replicate_from: str = "histogram", budget: int = -1, physical_replicas: bool = False,
+                 device="cuda"):
         self.T, self.E, self.k, self.H, self.F, self.act = T, E, k, H, F, act
         self.A = T * k
         self.stats = stats
@@ -51,6 +55,7 @@ class MoELayerStep:
             raise ValueError("replicate_from must be 'histogram' or 'prediction'")
         self.replicate_from = replicate_from
         self.budget = budget
+        self.physical = physical_replicas and replicate
         if budget >= 0 and not self.fused:
             raise ValueError("a copies budget needs the fused front (fused=True with stats)")
         self.gather = gather
@@ -66,6 +71,7 @@ class MoELayerStep:
         self.p_next = self.pn[0]
         self.copies = torch.empty(E, dtype=i32, device=d)
         self.pred_load = torch.empty(E, dtype=i32, device=d)
+        self.gslot = torch.empty(2 * E, dtype=i32, device=d)
         self.rep_base = torch.empty(E + 1, dtype=i32, device=d)
         self.group_expert = torch.empty(2 * E, dtype=i32, device=d)
         self.go = torch.empty(2 * E + 1, dtype=i32, device=d)
@@ -135,10 +141,34 @@ class MoELayerStep:
         mark("dispatch", 1)
         return self._expert_and_combine(x, weights, rb, ge, out, mark)
 
+    @staticmethod
+    def replica_buffers(weights):
+        """(w1, w3, w2) [E, ...] -> buffers of 2E-1 slots with the experts in
+        slots 0..E-1, for physical_replicas=True."""
+        out = []
+        for w in weights:
+            if w is None:
+                out.append(None)
+                continue
+            E = w.shape[0]
+            b = torch.empty((2 * E - 1,) + tuple(w.shape[1:]), dtype=w.dtype, device=w.device)
+            b[:E].copy_(w)
+            out.append(b)
+        return tuple(out)
+
     def _expert_and_combine(self, x, weights, rb, ge, out, mark):
         w1, w3, w2 = weights
         mark("ffn", 0)
-        if self.gather:
+        if self.physical:
+            if w1.shape[0] != 2 * self.E - 1:
+                raise ValueError("physical_replicas needs the 2E-1 slot buffers of replica_buffers()")
+            moe_replicate_weights(self.rep_base, w1, group_slot=self.gslot)
+            moe_replicate_weights(self.rep_base, w2, group_slot=self.gslot)
+            if w3 is not None:
+                moe_replicate_weights(self.rep_base, w3, group_slot=self.gslot)
+            moe_expert_ffn_slots(self.xp, self.go, self.gslot, w1, w3, w2, self.act, self.small, y=self.y,
+                                 workspace=self.ws_ffn)
+        elif self.gather:
             moe_expert_ffn_gather(x, self.perm, self.k, self.go, ge, rb, w1, w3, w2, self.act, self.small, y=self.y,
                                   workspace=self.ws_ffn)
         else:
@@ -152,7 +182,11 @@ class MoELayerStep:
         return out
 
     def launches(self, layer: int, L: int) -> int:
-        ffn = moe_ffn_launches(self.A, self.E, self.H, self.F, self.act, self.small, self.gather)
+        if self.physical:   # slot map + copy kernel per weight matrix, FFN over 2E-1 slots
+            ffn = (moe_ffn_launches(self.A, 2 * self.E - 1, self.H, self.F, self.act, self.small, False)
+                   + 2 * (3 if self.act == "swiglu" else 2))
+        else:
+            ffn = moe_ffn_launches(self.A, self.E, self.H, self.F, self.act, self.small, self.gather)
         if self.fused:
             return 2 + ffn + 1
         n = 1 + (3 if self.gather else 4) + ffn + 1
