@@ -57,6 +57,8 @@ def parse_args(argv=None):
                     help="gather the rows in the FFN's loads (moe_expert_ffn_gather) instead of copying them")
     ap.add_argument("--unfused", action="store_true",
                     help="make the five separate front calls instead of moe_layer_front")
+    ap.add_argument("--chunks", type=int, default=1,
+                    help="EPS-MoE pipeline: dispatch/FFN/combine over this many token chunks on two streams")
     ap.add_argument("--physical-replicas", action="store_true",
                     help="copy each replica's weights into its own slot (moe_replicate_weights) before the FFN")
     ap.add_argument("--replicate-from", choices=["histogram", "prediction"], default="histogram",
@@ -279,6 +281,11 @@ def run_ours(args, rank, world, local):
                         physical_replicas=args.physical_replicas, device=dev)
     if args.physical_replicas:
         weights = [MoELayerStep.replica_buffers(w) for w in weights]
+    if args.chunks > 1:
+        from moe_expert_routing_02_b300.layer import ChunkedLayerStep
+        step = ChunkedLayerStep(c.T, c.E, c.k, c.H, c.F, c.act, stats, chunks=args.chunks, device=dev)
+        step.fused, step.gather = True, False
+        stage_names = ["ffn"]
     stage_names = ["front", "ffn", "combine"] if step.fused else STAGES
     M.moe_set_option(M.MOE_OPT_FFN_KERNEL, {"auto": M.MOE_FFN_KERNEL_AUTO, "single": M.MOE_FFN_KERNEL_SINGLE,
                                             "pair": M.MOE_FFN_KERNEL_PAIR,
@@ -372,13 +379,16 @@ def run_ours(args, rank, world, local):
         # FFN time from the timed region (last replay of each slot graph)
         replayed = sorted({(args.warmup + s_i) % n_graphs for s_i in range(K)})
         ffn_ms = stage_means([graph_ev[q] for q in replayed], ["ffn"])["ffn"]
-        # stage breakdown: instrumented graphs replayed once per slot afterwards
-        graphs_all, ev_all = capture(stage_names)
-        for q in range(n_graphs):
-            graphs_all[q].replay()
-        torch.cuda.synchronize()
-        stage_ms = stage_means(ev_all)
-        del graphs_all
+        if args.chunks > 1:
+            stage_ms = {"ffn": ffn_ms}   # the chunked step times its whole chunked part as one stage
+        else:
+            # stage breakdown: instrumented graphs replayed once per slot afterwards
+            graphs_all, ev_all = capture(stage_names)
+            for q in range(n_graphs):
+                graphs_all[q].replay()
+            torch.cuda.synchronize()
+            stage_ms = stage_means(ev_all)
+            del graphs_all
     else:
         stage_ms = stage_means(stage_ev)
         ffn_ms = stage_ms["ffn"]
@@ -436,6 +446,7 @@ def run_ours(args, rank, world, local):
                    "launch": "eager" if args.eager else f"CUDA graph per step ({c.window} graphs, one per window slot)",
                    "front": "separate calls" if args.unfused else "moe_layer_front (2 launches)",
                    "ffn_kernel": args.ffn_kernel,
+                   "chunks": args.chunks,
                    "replicas": ("physical copies (moe_replicate_weights)" if args.physical_replicas
                                 else "aliasing their expert's weights") + f", table from {args.replicate_from}",
                    "ffn_input": "gathered from x in GEMM1's loads (tile::gather4)" if step.gather

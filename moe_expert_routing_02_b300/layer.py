@@ -16,7 +16,7 @@ from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT, MoEStats,
                moe_replicate_predicted, moe_replicate_weights, moe_expert_ffn_slots, moe_route, moe_stats_update,
                workspace_bytes)
 
-__all__ = ["MoELayerStep"]
+__all__ = ["MoELayerStep", "ChunkedLayerStep", "HostPipeline"]
 
 
 class MoELayerStep:
@@ -197,6 +197,116 @@ class MoELayerStep:
         if self.replicate:
             n += 1
         return n
+
+
+class ChunkedLayerStep:
+    """EPS-MoE's single-GPU expert pipeline (EPS-MoE review, pipeline of
+    dispatch, expert computation and combine over PN chunks of the tokens).
+
+    The front (route, statistics, prediction, replica table) runs once for
+    the whole layer, so the window statistics are those of the unchunked
+    layer; then each of `chunks` token chunks is dispatched, run through the
+    expert FFN and combined on one of two streams, so that a chunk's
+    dispatch can overlap the previous chunk's FFN where the GPU has room.
+    The output equals MoELayerStep's bit for bit (each row's FFN and each
+    token's combine are the same arithmetic; replica groups alias their
+    expert's weights)."""
+
+    def __init__(self, T: int, E: int, k: int, H: int, F: int, act: str, stats: MoEStats, chunks: int = 2,
+                 replicate: bool = True, thresh=(6, 5), max_copies: int = -1, renorm: bool = True,
+                 small_group_threshold: int = 64, device="cuda"):
+        if chunks < 1 or T % chunks:
+            raise ValueError("chunks must divide T")
+        self.T, self.E, self.k, self.H, self.F, self.act = T, E, k, H, F, act
+        self.stats, self.chunks = stats, chunks
+        self.replicate, self.thresh, self.max_copies, self.renorm = replicate, thresh, max_copies, renorm
+        self.small = small_group_threshold
+        d = torch.device(device)
+        i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
+        A = T * k
+        Tc = T // chunks
+        Ac = Tc * k
+        self.Tc = Tc
+        self.idx = [torch.empty((T, k), dtype=i32, device=d) for _ in range(2)]
+        self.w = torch.empty((T, k), dtype=f32, device=d)
+        self.hist = torch.empty(E, dtype=i32, device=d)
+        self.p_seq = torch.empty(E, dtype=f32, device=d)
+        self.cond = torch.empty((E, E), dtype=f32, device=d)
+        self.p_next = torch.empty(E, dtype=f32, device=d)
+        self.copies = torch.empty(E, dtype=i32, device=d)
+        self.rep_base = torch.empty(E + 1, dtype=i32, device=d)
+        self.group_expert = torch.empty(2 * E, dtype=i32, device=d)
+        self.go_full = torch.empty(2 * E + 1, dtype=i32, device=d)
+        self.perm_full = torch.empty(A, dtype=i32, device=d)
+        self.inv_full = torch.empty(A, dtype=i32, device=d)
+        self.ws_front = torch.empty(max(workspace_bytes(MOE_OP_LAYER_FRONT, T, k, E), 16), dtype=torch.uint8,
+                                    device=d)
+        # per stream: chunk buffers
+        self.streams = [torch.cuda.Stream(device=d) for _ in range(2)]
+        self.buf = []
+        for _ in range(2):
+            self.buf.append({
+                "go": torch.empty(2 * E + 1, dtype=i32, device=d),
+                "perm": torch.empty(Ac, dtype=i32, device=d),
+                "inv": torch.empty(Ac, dtype=i32, device=d),
+                "xp": torch.empty((Ac, H), dtype=bf, device=d),
+                "y": torch.empty((Ac, H), dtype=bf, device=d),
+                "ws_d": torch.empty(max(workspace_bytes(MOE_OP_DISPATCH, Tc, k, E), 16), dtype=torch.uint8, device=d),
+                "ws_f": torch.empty(max(workspace_bytes(MOE_OP_EXPERT_FFN, Tc, k, E, H, F), 1024),
+                                    dtype=torch.uint8, device=d),
+                "free": torch.cuda.Event(),
+            })
+        self.front_done = torch.cuda.Event()
+        self._fresh = [True, True]
+        self._cur = 0
+
+    def run(self, it: int, layer: int, logits, x, weights, out, events=None, predict: bool = True):
+        main = torch.cuda.current_stream()
+        prev = self.idx[self._cur ^ 1] if layer > 0 else None
+        idx = self.idx[self._cur]
+        last = layer == self.stats.L - 1
+        fo = {"idx": idx, "w": self.w, "hist": self.hist, "p_seq": self.p_seq,
+              "cond": None if last else self.cond, "p_next": None if last else self.p_next,
+              "copies": self.copies, "rep_base": self.rep_base, "group_expert": self.group_expert,
+              "group_offsets": self.go_full, "perm": self.perm_full, "inv_perm": self.inv_full, "xp": None}
+        moe_layer_front(logits, None, self.stats, it, layer, self.k, idx_prev=prev, renorm=self.renorm,
+                        predict=predict, replicate=self.replicate, thresh=self.thresh, max_copies=self.max_copies,
+                        out=fo, workspace=self.ws_front)
+        self.front_done.record(main)
+        if events is not None and "ffn" in events:   # the chunked part: dispatch, FFN and combine of all chunks
+            events["ffn"][0].record(main)
+        rb, ge = (self.rep_base, self.group_expert) if self.replicate else (None, None)
+        w1, w3, w2 = weights
+        Tc = self.Tc
+        # the previous run's chunks were joined into the main stream before the
+        # front, so a buffer only waits for an earlier chunk of this run
+        self._fresh = [True, True]
+        for c in range(self.chunks):
+            j = c & 1
+            s, b = self.streams[j], self.buf[j]
+            s.wait_event(self.front_done)
+            if not self._fresh[j]:
+                s.wait_event(b["free"])
+            with torch.cuda.stream(s):
+                rows = slice(c * Tc, (c + 1) * Tc)
+                moe_dispatch(x[rows], idx[rows], self.E, rb, out=(b["go"], b["perm"], b["inv"], b["xp"]),
+                             workspace=b["ws_d"])
+                moe_expert_ffn(b["xp"], b["go"], ge, rb, w1, w3, w2, self.act, self.small, y=b["y"],
+                               workspace=b["ws_f"])
+                moe_combine(b["y"], b["inv"], self.w[rows], out=out[rows])
+                b["free"].record(s)
+            self._fresh[j] = False
+        for j in range(2):
+            if not self._fresh[j]:
+                main.wait_event(self.buf[j]["free"])
+        if events is not None and "ffn" in events:
+            events["ffn"][1].record(main)
+        self._cur ^= 1
+        return out
+
+    def launches(self, layer: int, L: int) -> int:
+        ffn = moe_ffn_launches(self.Tc * self.k, self.E, self.H, self.F, self.act, self.small, False)
+        return 2 + self.chunks * (4 + ffn + 1)
 
 
 class HostPipeline:

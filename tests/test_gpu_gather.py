@@ -207,3 +207,31 @@ def test_layer_step_prediction_driven_replication_same_output():
     for key, res in outs.items():
         for a, b in zip(res, outs["hist"]):
             assert torch.equal(a, b), key
+
+
+@pytest.mark.parametrize("chunks", [2, 4])
+def test_chunked_pipeline_same_output(chunks):
+    """EPS-MoE pipeline over token chunks on two streams: bit-identical to the
+    one-shot layer step, statistics included."""
+    from moe_expert_routing_02_b300.layer import ChunkedLayerStep
+    c = W.config_by_name("moe_gpt_stream")
+    L = 2
+    weights = [W.make_weights(c, j, device="cuda") for j in range(L)]
+    st_a = M.MoEStats(L, c.E, c.window)
+    st_b = M.MoEStats(L, c.E, c.window)
+    a = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, stats=st_a, replicate=True)
+    b = ChunkedLayerStep(c.T, c.E, c.k, c.H, c.F, c.act, st_b, chunks=chunks)
+    for it in (60, 61):
+        lgs = W.make_layer_logits(c, it, layers=L)
+        for j in range(L):
+            x = W.make_x(c, it, j, device="cuda")
+            oa = torch.empty((c.T, c.H), dtype=torch.bfloat16, device="cuda")
+            ob = torch.empty((c.T, c.H), dtype=torch.bfloat16, device="cuda")
+            a.run(it, j, dev(lgs[j]), x, weights[j], oa)
+            b.run(it, j, dev(lgs[j]), x, weights[j], ob)
+            torch.cuda.synchronize()
+            assert torch.equal(oa, ob), (it, j)
+            assert torch.equal(a.hist, b.hist) and torch.equal(a.rep_base, b.rep_base)
+    M.moe_check()
+    sa, sb = st_a.export_state(), st_b.export_state()
+    assert sa == sb
