@@ -28,6 +28,11 @@ in float64 (integers exact), written from the pages:
     budget), PopFetcher review (top-5 next-layer prediction accuracy, s = 10),
     "Prediction Is All MoE Needs" (mean error of the predicted expert-load
     proportion).
+  * backward of the routed FFN (PopFetcher trains the MoE models it routes:
+    its prefetched expert copies send their gradients back to the primary
+    expert for the reduction) -- the gradients of the expert FFN, the
+    combine and the gate weights, with every replica's rows reducing into
+    its expert's one gradient.
   * stable dispatch by expert / replica and the gate-weighted combine --
     PopFetcher review, problem statement (token dispatch + result collect);
     EPS-MoE review, compute/communication overlap (LocalReduce); MoE-MPMC
@@ -483,6 +488,123 @@ def expert_ffn(xp: np.ndarray, group_offsets: np.ndarray, group_expert: Optional
     ge = np.arange(len(go)) if group_expert is None else np.asarray(group_expert)
     experts = np.asarray(ge)[g]
     return expert_ffn_rows(np.asarray(xp)[slots], experts, w1, w3, w2, act)
+
+
+# ----------------------------------------------------------------------------
+# Backward of the routed FFN
+# ----------------------------------------------------------------------------
+def _gelu_grad(z):
+    # d/dz [z Phi(z)] = Phi(z) + z phi(z)
+    return 0.5 * (1.0 + _erf(z / math.sqrt(2.0))) + z * np.exp(-0.5 * z * z) / math.sqrt(2.0 * math.pi)
+
+
+def _silu_grad(z):
+    s = 1.0 / (1.0 + np.exp(-z))
+    return s * (1.0 + z * (1.0 - s))
+
+
+def expert_ffn_backward_f64(x, experts, w1, w3, w2, act: str, dy):
+    """Gradients of expert_ffn_rows, all in float64 (x [n,H], w1/w3 [E,H,F],
+    w2 [E,F,H] and dy [n,H] float64).  Per row of expert e:
+      GeLU  : z = x W1, a = gelu(z), y = a W2
+              dA = dy W2^T, dz = dA * gelu'(z),
+              dW2 += a^T dy, dW1 += x^T dz, dx = dz W1^T
+      SwiGLU: g = x W1, u = x W3, a = silu(g) * u, y = a W2
+              dA = dy W2^T, dg = dA * u * silu'(g), du = dA * silu(g),
+              dW2 += a^T dy, dW1 += x^T dg, dW3 += x^T du,
+              dx = dg W1^T + du W3^T
+    Every row adds into its expert's gradients, so the rows of an expert's
+    replica groups reduce into the expert's one gradient.
+    Returns dx [n,H], dw1 [E,H,F], dw3 [E,H,F] or None, dw2 [E,F,H]."""
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    experts = np.asarray(experts).astype(np.int64)
+    w1 = np.asarray(w1, dtype=np.float64)
+    w2 = np.asarray(w2, dtype=np.float64)
+    w3 = None if w3 is None else np.asarray(w3, dtype=np.float64)
+    dx = np.zeros_like(x)
+    dw1 = np.zeros_like(w1)
+    dw2 = np.zeros_like(w2)
+    dw3 = None if w3 is None else np.zeros_like(w3)
+    for e in np.unique(experts):
+        rows = np.nonzero(experts == e)[0]
+        xe, dye = x[rows], dy[rows]
+        dA = dye @ w2[e].T
+        if act == "gelu":
+            z = xe @ w1[e]
+            a = _gelu(z)
+            dz = dA * _gelu_grad(z)
+            dw1[e] += xe.T @ dz
+            dx[rows] = dz @ w1[e].T
+        elif act == "swiglu":
+            g = xe @ w1[e]
+            u = xe @ w3[e]
+            a = _silu(g) * u
+            dg = dA * u * _silu_grad(g)
+            du = dA * _silu(g)
+            dw1[e] += xe.T @ dg
+            dw3[e] += xe.T @ du
+            dx[rows] = dg @ w1[e].T + du @ w3[e].T
+        else:
+            raise ValueError(act)
+        dw2[e] += a.T @ dye
+    return dx, dw1, dw3, dw2
+
+
+def combine_backward(dout, y, inv_perm, w):
+    """Gradients of combine: out[t] = sum_r w[t,r] Y[slot(t,r)].
+    dY[slot(t,r)] = w[t,r] dout[t];  dw[t,r] = <dout[t], Y[slot(t,r)]>.
+    float64 in and out (y may be bf16 bits)."""
+    dout = np.asarray(dout, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    T, k = w.shape
+    yy = bf16_to_f64(y) if np.asarray(y).dtype == np.uint16 else np.asarray(y, dtype=np.float64)
+    inv = np.asarray(inv_perm).astype(np.int64)
+    dY = np.zeros_like(yy)
+    dw = np.zeros((T, k), dtype=np.float64)
+    for r in range(k):
+        slots = inv[np.arange(T) * k + r]
+        dY[slots] = w[:, r:r + 1] * dout
+        dw[:, r] = np.sum(dout * yy[slots], axis=1)
+    return dY, dw
+
+
+def scatter_sum(dxp, inv_perm, T: int, k: int):
+    """Token gradients from the dispatched rows: dx[t] = sum_r dxp[slot(t,r)]
+    (the backward of the row copy xp[slot] = x[t])."""
+    d = np.asarray(dxp, dtype=np.float64)
+    inv = np.asarray(inv_perm).astype(np.int64)
+    dx = np.zeros((T, d.shape[1]), dtype=np.float64)
+    for r in range(k):
+        dx += d[inv[np.arange(T) * k + r]]
+    return dx
+
+
+def router_backward(logits, idx, dw, renorm: bool = True):
+    """Gradient of the gate weights with respect to the router logits, the
+    choice of experts held fixed (it is piecewise constant).
+      renorm: w_r = softmax over the k chosen logits ->
+              dlogit[e_r] = w_r (dw_r - sum_s w_s dw_s), 0 elsewhere;
+      full  : w_r = p[e_r], p = softmax over all E ->
+              dlogit[j] = p_j (g_j - sum_r dw_r p[e_r]), g_j = dw_r if j = e_r else 0."""
+    l = np.asarray(logits, dtype=np.float64)
+    idx = np.asarray(idx).astype(np.int64)
+    dw = np.asarray(dw, dtype=np.float64)
+    T, E = l.shape
+    out = np.zeros((T, E), dtype=np.float64)
+    for t in range(T):
+        sel = l[t, idx[t]]
+        if renorm:
+            z = np.exp(sel - sel.max())
+            w = z / z.sum()
+            out[t, idx[t]] = w * (dw[t] - np.dot(w, dw[t]))
+        else:
+            z = np.exp(l[t] - l[t].max())
+            p = z / z.sum()
+            g = np.zeros(E)
+            g[idx[t]] = dw[t]
+            out[t] = p * (g - np.dot(dw[t], p[idx[t]]))
+    return out
 
 
 # ----------------------------------------------------------------------------

@@ -8,6 +8,7 @@ import pytest
 from oracle import moe_oracle as O
 import tests.test_oracle_pins as P
 import tests.test_oracle_prediction as PP
+import tests.test_oracle_backward as PB
 
 
 def _topk_ties_reversed(logits, k, renorm=True):
@@ -161,6 +162,37 @@ def _overlap_bottom(p_pred, load_actual, m=5):
     return len(set(pred) & set(act)) / m
 
 
+def _gelu_grad_cdf_only(z):
+    return 0.5 * (1.0 + O._erf(z / math.sqrt(2.0)))
+
+
+def _silu_grad_sign(z):
+    s = 1.0 / (1.0 + np.exp(-z))
+    return s * (1.0 + z * s)
+
+
+def _combine_bwd_unweighted(dout, y, inv_perm, w):
+    _, dw = ORIG["combine_backward"](dout, y, inv_perm, w)
+    dY, _ = ORIG["combine_backward"](dout, y, inv_perm, np.ones_like(np.asarray(w, np.float64)))
+    return dY, dw
+
+
+def _scatter_sum_perm(dxp, inv_perm, T, k):
+    perm = np.argsort(np.asarray(inv_perm))
+    return ORIG["scatter_sum"](dxp, perm, T, k)
+
+
+def _router_bwd_no_centering(logits, idx, dw, renorm=True):
+    l = np.asarray(logits, np.float64)
+    idx = np.asarray(idx).astype(np.int64)
+    out = np.zeros_like(l)
+    for t in range(l.shape[0]):
+        z = np.exp(l[t, idx[t]] - l[t, idx[t]].max())
+        w = z / z.sum()
+        out[t, idx[t]] = w * np.asarray(dw, np.float64)[t]
+    return out
+
+
 ORIG = {
     "topk_gate": O.topk_gate,
     "coselection": O.coselection,
@@ -168,6 +200,8 @@ ORIG = {
     "expert_ffn_rows": O.expert_ffn_rows,
     "combine": O.combine,
     "predict_decay": O.WindowStats.predict_decay,
+    "combine_backward": O.combine_backward,
+    "scatter_sum": O.scatter_sum,
 }
 
 MUTANTS = [
@@ -188,6 +222,11 @@ MUTANTS = [
     ("apportion", _apportion_plain_round, [PP.test_apportion_hand_cases]),
     ("cap_copies", _cap_coldest_first, [PP.test_budget_hand_cases]),
     ("top_overlap", _overlap_bottom, [PP.test_quality_hand_cases]),
+    ("_gelu_grad", _gelu_grad_cdf_only, [lambda: PB.test_ffn_backward_matches_finite_differences("gelu")]),
+    ("_silu_grad", _silu_grad_sign, [lambda: PB.test_ffn_backward_matches_finite_differences("swiglu")]),
+    ("combine_backward", _combine_bwd_unweighted, [PB.test_combine_backward_matches_finite_differences]),
+    ("scatter_sum", _scatter_sum_perm, [PB.test_scatter_sum_is_the_adjoint_of_the_row_copy]),
+    ("router_backward", _router_bwd_no_centering, [lambda: PB.test_router_backward_matches_finite_differences(True)]),
 ]
 
 
