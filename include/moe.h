@@ -368,6 +368,71 @@ moe_status moe_expert_ffn_slots(const uint16_t* xp, const int32_t* group_offsets
                                 uint16_t* y, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_ffn_backward -- backward of the routed expert layer: combine, expert
+ * FFN and dispatch copy.
+ * PopFetcher (ATC'25) review: the system trains MoE models; in the backward
+ * pass the gradients of an expert's replicas are reduced into the primary
+ * expert (core method; design trade-offs).  Here every row routed to expert e,
+ * in whichever of its replica groups, adds into the one gradient dW[e].
+ *
+ * Forward being differentiated (moe_dispatch -> moe_expert_ffn -> moe_combine):
+ *   xp[i] = x[t(i)],  Y = FFN_e(xp),  out[t] = sum_r w[t,r] Y[inv_perm[t k + r]].
+ * Given dout = dL/dout:
+ *   dY[i] = w[t,r] dout[t];  dw[t,r] = <dout[t], Y[inv_perm[t k + r]]>;
+ *   GeLU:   z = xp W1, a = gelu(z), dA = dY W2^T, dz = dA gelu'(z),
+ *           dW2[e] = a^T dY, dW1[e] = xp^T dz, dxp = dz W1^T;
+ *   SwiGLU: g = xp W1, u = xp W3, a = silu(g) u, dg = dA u silu'(g),
+ *           du = dA silu(g), dW1 = xp^T dg, dW3 = xp^T du,
+ *           dxp = dg W1^T + du W3^T;
+ *   dx[t] = sum_r dxp[inv_perm[t k + r]].
+ * Arithmetic: bf16 operands, fp32 accumulation; dY, dA, a, dz (dg, du) and
+ * dxp are rounded to bf16 between the GEMMs (as the forward rounds its
+ * intermediate); the weight gradients and dw are fp32.
+ *
+ *   x, dout      bf16 [T, H]: the layer input and the output's gradient
+ *   w            f32 [T, k] gate weights (moe_route)
+ *   y            bf16 [A, H] the forward FFN output in dispatched order, or
+ *                NULL: then dw is not computed (dw may be NULL)
+ *   perm, inv_perm, group_offsets, group_expert, E: from moe_dispatch (or
+ *                moe_layer_front) of the same routing; group_expert NULL =
+ *                group g is expert g (E groups), else 2E groups.  The groups of
+ *                one expert must be adjacent (as the dispatch writes them).
+ *   w1, w3, w2   expert weights as in moe_expert_ffn (w3 NULL for GeLU)
+ *   dx           bf16 [T, H] out
+ *   dw           f32 [T, k] out (when y is given)
+ *   dw1, dw3, dw2  f32 [E, H, F], [E, H, F] (SwiGLU; else NULL), [E, F, H] out:
+ *                every expert's gradient is written (0 for experts without rows)
+ *   workspace    ws_bytes >= moe_ffn_backward_workspace_bytes(T, k, E, H, F),
+ *                256-byte aligned; holds the padded intermediates (each
+ *                expert's rows start at a multiple of 64, zero-padded).
+ * Seven launches on `stream`.  Errors: MOE_ERR_INVALID (sizes as moe_expert_ffn,
+ * null or misaligned pointers, y without dw), MOE_ERR_WORKSPACE; invalid device
+ * data (offsets, permutation, an expert's groups not adjacent) sets the
+ * device error word.
+ * ------------------------------------------------------------------------- */
+size_t moe_ffn_backward_workspace_bytes(int T, int k, int E, int H, int F);
+moe_status moe_ffn_backward(const uint16_t* x, const uint16_t* dout, const float* w, const uint16_t* y,
+                            const int32_t* perm, const int32_t* inv_perm, int T, int k,
+                            const int32_t* group_offsets, const int32_t* group_expert, int E,
+                            const uint16_t* w1, const uint16_t* w3, const uint16_t* w2, int H, int F,
+                            moe_act act, uint16_t* dx, float* dw, float* dw1, float* dw3, float* dw2,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_route_backward -- gradient of the gate weights with respect to the
+ * router logits, the chosen experts held fixed (the top-k choice is piecewise
+ * constant).  PopFetcher and EPS-MoE reviews: softmax gate over the chosen
+ * experts (renorm = 1) or over all E (renorm = 0), as moe_route.
+ *   renorm = 1: dlogits[t, e_r] = w_r (dw_r - sum_s w_s dw_s), 0 elsewhere
+ *   renorm = 0: dlogits[t, j] = p_j (g_j - sum_r dw_r p[e_r]),
+ *               p = softmax(logits[t]), g_j = dw_r if j = e_r else 0
+ *   logits f32 [T, E]; idx i32 [T, k] (moe_route); dw f32 [T, k];
+ *   dlogits f32 [T, E] out.  fp32 arithmetic.  One launch.
+ * ------------------------------------------------------------------------- */
+moe_status moe_route_backward(const float* logits, const int32_t* idx, const float* dw, int T, int E, int k,
+                              int renorm, float* dlogits, void* stream);
+
+/* ---------------------------------------------------------------------------
  * moe_combine -- gate-weighted sum of each token's expert outputs.
  * EPS-MoE review, compute/communication overlap (LocalReduce of expert
  * outputs); PopFetcher review (result collect).

@@ -69,6 +69,10 @@ _SIGS = {
     "moe_layer_front": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _I64, _I, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P,
                              _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_get_option": (_I, [_I, ctypes.POINTER(_I)]),
+    "moe_ffn_backward_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_ffn_backward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P,
+                              _P, _SZ, _P]),
+    "moe_route_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -536,6 +540,75 @@ def moe_ffn_launches(A: int, E: int, H: int, F: int, act: str = "gelu", small_gr
     act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
     return int(lib().moe_ffn_launches(int(A), int(E), int(H), int(F), act_id, int(small_group_threshold),
                                       int(bool(gather))))
+
+
+def moe_ffn_backward(x, dout, w, y, perm, inv_perm, group_offsets, group_expert, w1, w3, w2, act: str = "gelu",
+                     workspace=None, stream=None, out=None):
+    """Backward of dispatch -> expert FFN -> combine for one routing.
+    x, dout bf16 [T, H]; w f32 [T, k]; y bf16 [T*k, H] (the forward FFN
+    output, or None: no dw); perm, inv_perm, group_offsets, group_expert as
+    written by the dispatch.  Returns (dx bf16 [T, H], dw f32 [T, k] or None,
+    dw1 f32 [E, H, F], dw3 f32 [E, H, F] or None, dw2 f32 [E, F, H]).
+    `out` may give those five tensors to write into."""
+    torch = _torch()
+    _dev(x, torch.bfloat16, "x", 2)
+    _dev(dout, torch.bfloat16, "dout", 2)
+    _dev(w, torch.float32, "w", 2)
+    _dev(perm, torch.int32, "perm", 1)
+    _dev(inv_perm, torch.int32, "inv_perm", 1)
+    _dev(group_offsets, torch.int32, "group_offsets", 1)
+    if group_expert is not None:
+        _dev(group_expert, torch.int32, "group_expert", 1)
+    _dev(w1, torch.bfloat16, "w1", 3)
+    _dev(w2, torch.bfloat16, "w2", 3)
+    if w3 is not None:
+        _dev(w3, torch.bfloat16, "w3", 3)
+    if y is not None:
+        _dev(y, torch.bfloat16, "y", 2)
+    T, H = x.shape
+    k = w.shape[1]
+    E, H1, F = w1.shape
+    if H1 != H or tuple(w2.shape) != (E, F, H) or tuple(dout.shape) != (T, H) or w.shape[0] != T:
+        raise ValueError("shapes: x, dout [T,H]; w [T,k]; w1/w3 [E,H,F]; w2 [E,F,H]")
+    act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
+    dev = x.device
+    if out is None:
+        f32 = dict(dtype=torch.float32, device=dev)
+        out = (torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+               torch.empty((T, k), **f32) if y is not None else None,
+               torch.empty((E, H, F), **f32),
+               torch.empty((E, H, F), **f32) if act == "swiglu" else None,
+               torch.empty((E, F, H), **f32))
+    dx, dw, dw1, dw3, dw2 = out
+    need = int(lib().moe_ffn_backward_workspace_bytes(T, k, E, H, F))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=dev)
+    _check(lib().moe_ffn_backward(_ptr(x), _ptr(dout), _ptr(w), _ptr(y), _ptr(perm), _ptr(inv_perm), T, k,
+                                  _ptr(group_offsets), _ptr(group_expert), E, _ptr(w1), _ptr(w3), _ptr(w2), H, F,
+                                  act_id, _ptr(dx), _ptr(dw), _ptr(dw1), _ptr(dw3), _ptr(dw2), _ptr(workspace),
+                                  workspace.numel(), _stream(stream)), "moe_ffn_backward")
+    return dx, dw, dw1, dw3, dw2
+
+
+def moe_ffn_backward_workspace_bytes(T: int, k: int, E: int, H: int, F: int) -> int:
+    return int(lib().moe_ffn_backward_workspace_bytes(int(T), int(k), int(E), int(H), int(F)))
+
+
+def moe_route_backward(logits, idx, dw, renorm: bool = True, out=None, stream=None):
+    """dlogits f32 [T, E]: gradient of the gate weights w.r.t. the logits,
+    the chosen experts held fixed."""
+    torch = _torch()
+    _dev(logits, torch.float32, "logits", 2)
+    _dev(idx, torch.int32, "idx", 2)
+    _dev(dw, torch.float32, "dw", 2)
+    T, E = logits.shape
+    k = idx.shape[1]
+    if out is None:
+        out = torch.empty((T, E), dtype=torch.float32, device=logits.device)
+    _dev(out, torch.float32, "dlogits", 2)
+    _check(lib().moe_route_backward(_ptr(logits), _ptr(idx), _ptr(dw), T, E, k, int(bool(renorm)), _ptr(out),
+                                    _stream(stream)), "moe_route_backward")
+    return out
 
 
 def moe_combine(y, inv_perm, w, out=None, stream=None):

@@ -79,7 +79,16 @@ constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr uint64_t kWaitBudgetNs = 2000000000ull;
 constexpr uint32_t kMaxPolls = 1u << 30;
 
-enum Epi : int { kGelu = 0, kSwiglu = 1, kStore = 2 };
+// kGelu / kSwiglu / kStore: forward GEMM1 and GEMM2 (B = weights as stored,
+// MN-major).  kStoreKM: data gradient, B = the transpose of the weights as
+// stored (K-major rows of the weight tensor), K optionally split between two
+// weight tensors at k_split blocks.  kBwdGelu / kBwdSwiglu: GEMM1 recomputed in
+// the backward pass; the epilogue reads the activation's gradient dA (side)
+// and writes the activation (out) and the pre-activation gradients (out2).
+enum Epi : int { kGelu = 0, kSwiglu = 1, kStore = 2, kStoreKM = 3, kBwdGelu = 4, kBwdSwiglu = 5 };
+
+__host__ __device__ constexpr bool epi_pair_b(int e) { return e == kSwiglu || e == kBwdSwiglu; }
+__host__ __device__ constexpr bool epi_kmajor_b(int e) { return e == kStoreKM; }
 
 struct Params {
   const int32_t* group_offsets;  // [G+1]
@@ -100,6 +109,14 @@ struct Params {
   const int32_t* a_src;
   int a_src_div;
   int a_src_rows;  // rows of that tensor (T)
+  // kStoreKM: k-blocks below k_split read the first weight tensor, the rest
+  // the second (at k-block kb - k_split).
+  int k_split;
+  // kBwdGelu / kBwdSwiglu: side = dA [A_rows, N_out]; out = activation
+  // [A_rows, N_out]; out2 = dz [A_rows, N_out] (GeLU) or [dg | du]
+  // [A_rows, 2 N_out] (SwiGLU).
+  const uint16_t* side;
+  uint16_t* out2;
 };
 
 
@@ -310,6 +327,27 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return fmaf(h, erf_as7126(z * 0.70710678118654752f), h);
 }
 
+// GeLU and its derivative from one exponential:
+//   gelu(z) = z Phi(z),  gelu'(z) = Phi(z) + z phi(z),
+//   Phi(z) = (1 + erf(z / sqrt 2)) / 2,  phi(z) = exp(-z^2 / 2) / sqrt(2 pi),
+// with erf by the same 7.1.26 approximation, whose exp(-x^2) at x = z/sqrt 2
+// is exp(-z^2 / 2).
+__device__ __forceinline__ void gelu_and_grad(float z, float& a, float& da) {
+  const float x = z * 0.70710678118654752f;
+  const float ax = fabsf(x);
+  const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
+  float q = fmaf(1.061405429f, t, -1.453152027f);
+  q = fmaf(q, t, 1.421413741f);
+  q = fmaf(q, t, -0.284496736f);
+  q = fmaf(q, t, 0.254829592f);
+  q *= t;
+  const float ex = __expf(-ax * ax);
+  const float erfv = copysignf(fmaf(-q, ex, 1.0f), x);
+  const float Phi = fmaf(0.5f, erfv, 0.5f);
+  a = z * Phi;
+  da = fmaf(z * 0.39894228040143268f, ex, Phi);
+}
+
 __device__ __forceinline__ void store32(uint16_t* dst, const float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -353,6 +391,37 @@ __device__ __forceinline__ void store_rows32(uint8_t* stg, uint16_t* out, size_t
   }
 }
 
+// The reverse of store_rows32: lane i receives row i's 32 bf16 columns of
+// src (packed pairs in pk), read through 1 KB of shared memory with whole
+// 64-byte row segments per load instruction.  Rows >= rows_valid read as 0.
+__device__ __forceinline__ void load_rows32(uint8_t* stg, const uint16_t* src, size_t ld, int rows_valid,
+                                            uint32_t (&pk)[16], int lane) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    __syncwarp();
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int idx = pass * 32 + lane;
+      const int r = idx >> 2, c = idx & 3;
+      const int row = h * 16 + r;
+      const uint4 v = row < rows_valid ? ld_nc_v4(src + (size_t)row * ld + c * 8) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(stg + r * 64 + (((c + (r >> 1)) & 3) << 4)) = v;
+    }
+    __syncwarp();
+    if ((lane >> 4) == h) {
+      const int r = lane & 15;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 64 + (((j + (r >> 1)) & 3) << 4));
+        pk[4 * j] = v.x;
+        pk[4 * j + 1] = v.y;
+        pk[4 * j + 2] = v.z;
+        pk[4 * j + 3] = v.w;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&pk)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
@@ -388,7 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
-    if (EPI == kSwiglu) tma_prefetch_desc(&tmB1);
+    if (epi_pair_b(EPI) || epi_kmajor_b(EPI)) tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) {
     __syncwarp();  // .sync.aligned: whole warp, converged
@@ -412,7 +481,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const Tile t = decode(s, U, tile);
-      const int brow = s.ex[t.g] * p.K;
+      const int brow = epi_kmajor_b(EPI) ? s.ex[t.g] * p.N_out + t.nt * BN : s.ex[t.g] * p.K;
       const int arow = (int)t.row0;
       const int4 src = gather ? gather_src4(p, t.row0, lane) : make_int4(0, 0, 0, 0);
       for (int kb = 0; kb < kblocks; ++kb) {
@@ -425,7 +494,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(&s.full[stage], A_BYTES + B_BYTES);
           if (!gather) tma_load_2d(s.a[stage], &tmA, &s.full[stage], kb * BK, arow);
-          if (EPI == kSwiglu) {
+          if (epi_kmajor_b(EPI)) {
+            // B = rows n0.. of the expert's [N_out, K] weight block, K-major: one 128 x BN box
+            if (kb < p.k_split)
+              tma_load_2d(s.b[stage], &tmB0, &s.full[stage], kb * BK, brow);
+            else
+              tma_load_2d(s.b[stage], &tmB1, &s.full[stage], (kb - p.k_split) * BK, brow);
+          } else if (epi_pair_b(EPI)) {
             // first half of the B tile: W1 (gate) columns, second half: the same W3 (up) columns
             const int n0 = t.nt * (BN / 2);
 #pragma unroll
@@ -462,11 +537,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, true);
+      constexpr bool kmb = epi_kmajor_b(EPI);
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, !kmb);
+      // B K-major (kStoreKM): BN rows of 128 bytes like the A tile; a K step
+      // of 16 is +2 in the start-address field
+      constexpr uint32_t kBStep = kmb ? 2u : 128u;
       // descriptors of stage 0; stages are contiguous, so stage s adds
       // s * (stage bytes >> 4) to the start-address field
       const uint64_t adesc0 = smem_desc_sw128(smem_u32(s.a[0]), 16, 1024);
-      const uint64_t bdesc0 = smem_desc_sw128(smem_u32(s.b[0]), B_BOX_BYTES, 1024);
+      const uint64_t bdesc0 = smem_desc_sw128(smem_u32(s.b[0]), kmb ? 16u : (uint32_t)B_BOX_BYTES, 1024);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true, withheld = false, any_mma = false;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
@@ -487,7 +566,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t bd = bdesc0 + (uint64_t)(stage * (B_BYTES >> 4));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 128), idesc, (kb | kk) != 0 ? 1u : 0u);
+            mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * kBStep), idesc, (kb | kk) != 0 ? 1u : 0u);
           mma_commit(&s.empty[stage]);
           any_mma = true;
           if (++stage == STAGES) {
@@ -524,7 +603,77 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int wrows = t.rows - quarter * 32;
       uint16_t* wbase = p.out + (size_t)(t.row0 + quarter * 32) * p.N_out;
       const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      if (EPI == kSwiglu) {
+      if (EPI == kBwdSwiglu) {
+        // a = silu(g) u;  dg = dA u silu'(g);  du = dA silu(g);
+        // silu(g) = g s, silu'(g) = s (1 + g (1 - s)), s = 1 / (1 + exp(-g))
+        constexpr int W = (BN / 2) / EPI_SLICES;
+        const size_t ld2 = 2 * (size_t)p.N_out;
+        uint16_t* w2base = p.out2 + (size_t)(t.row0 + quarter * 32) * ld2;
+        const uint16_t* sbase = p.side + (size_t)(t.row0 + quarter * 32) * p.N_out;
+#pragma unroll 1
+        for (int cc = 0; cc < W; cc += 32) {
+          const int c = slice * W + cc;
+          uint32_t gr[32], ur[32];
+          __syncwarp();
+          tmem_ld32(tb + c, gr);
+          tmem_ld32(tb + BN / 2 + c, ur);
+          const int col = t.nt * (BN / 2) + c;
+          if (col < p.N_out) {
+            uint32_t dak[16];
+            load_rows32(s.stg[warp - 2], sbase + col, (size_t)p.N_out, wrows, dak, lane);
+            float va[32], vg[32], vu[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float g = __uint_as_float(gr[i]);
+              const float u = __uint_as_float(ur[i]);
+              const float da = (i & 1) ? bf16hi(dak[i >> 1]) : bf16lo(dak[i >> 1]);
+              const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
+              const float silu = g * sg;
+              va[i] = silu * u;
+              vg[i] = da * u * sg * fmaf(g, 1.0f - sg, 1.0f);
+              vu[i] = da * silu;
+            }
+            uint32_t pk[16];
+            pack32(va, pk);
+            store_rows32(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pk, lane);
+            pack32(vg, pk);
+            store_rows32(s.stg[warp - 2], w2base + col, ld2, wrows, pk, lane);
+            pack32(vu, pk);
+            store_rows32(s.stg[warp - 2], w2base + p.N_out + col, ld2, wrows, pk, lane);
+          }
+        }
+      } else if (EPI == kBwdGelu) {
+        // a = gelu(z);  dz = dA gelu'(z)
+        constexpr int W = BN / EPI_SLICES;
+        uint16_t* w2base = p.out2 + (size_t)(t.row0 + quarter * 32) * p.N_out;
+        const uint16_t* sbase = p.side + (size_t)(t.row0 + quarter * 32) * p.N_out;
+#pragma unroll 1
+        for (int cc = 0; cc < W; cc += 32) {
+          const int c = slice * W + cc;
+          uint32_t raw[32];
+          __syncwarp();
+          tmem_ld32(tb + c, raw);
+          const int col = t.nt * BN + c;
+          if (col < p.N_out) {
+            uint32_t dak[16];
+            load_rows32(s.stg[warp - 2], sbase + col, (size_t)p.N_out, wrows, dak, lane);
+            float va[32], vd[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float da = (i & 1) ? bf16hi(dak[i >> 1]) : bf16lo(dak[i >> 1]);
+              float a, g;
+              gelu_and_grad(__uint_as_float(raw[i]), a, g);
+              va[i] = a;
+              vd[i] = da * g;
+            }
+            uint32_t pk[16];
+            pack32(va, pk);
+            store_rows32(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pk, lane);
+            pack32(vd, pk);
+            store_rows32(s.stg[warp - 2], w2base + col, (size_t)p.N_out, wrows, pk, lane);
+          }
+        }
+      } else if (EPI == kSwiglu) {
         constexpr int W = (BN / 2) / EPI_SLICES;   // output columns per warp
 #pragma unroll 1
         for (int cc = 0; cc < W; cc += 32) {

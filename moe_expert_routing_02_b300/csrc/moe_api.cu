@@ -585,7 +585,7 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   bool use_pair = false, use_fused = false;
   ffn_choice(A, E, H, F, act, gather, &use_pair, &use_fused);
 
-  ffn::Params p1;
+  ffn::Params p1{};
   p1.group_offsets = group_offsets;
   p1.group_expert = group_expert;
   p1.G = G;
@@ -945,3 +945,6 @@ moe_status moe_check(void* stream) {
 // moe_dispatch_noalloc lives in its own file and is compiled into this
 // translation unit.
 #include "dispatch_noalloc.cu"
+
+// The backward of the routed expert layer, likewise.
+#include "ffn_backward.cu"
