@@ -77,6 +77,8 @@ def parse_args(argv=None):
                     help="prediction quality and prediction-driven replication over the workload's iterations "
                          "(one JSON line; not the bench line)")
     ap.add_argument("--quality-iters", type=int, default=200)
+    ap.add_argument("--backward", action="store_true",
+                    help="time the layer's backward (moe_ffn_backward + moe_route_backward) instead; one JSON line")
     ap.add_argument("--sweep-min-log2", type=int, default=14)
     ap.add_argument("--sweep-max-log2", type=int, default=20)
     return ap.parse_args(argv)
@@ -659,6 +661,98 @@ def run_sweep(args):
     return 0
 
 
+def backward_flops(c):
+    """Algorithmic flops of the expert FFN's backward for one layer: the data
+    gradients dA = dY W2^T and dxp = dz W1^T (+ du W3^T), GEMM1 recomputed
+    (one GEMM for GeLU, two for SwiGLU) and the weight gradients (2 or 3),
+    each 2 A H F: 10 A H F for GeLU, 16 A H F for SwiGLU."""
+    return (16 if c.act == "swiglu" else 10) * c.A * c.H * c.F
+
+
+def run_backward(args):
+    """The backward of one routed expert layer at the config's full size:
+    moe_ffn_backward (combine, FFN and dispatch backward, all weight
+    gradients) plus moe_route_backward, after a forward that produced y.
+    W warm-up steps, then K steps timed with CUDA events on the launching
+    stream; the operands (xp, dY, intermediates, fp32 gradients) are far
+    larger than L2.  The forward FFN (moe_expert_ffn) is timed the same way
+    for comparison."""
+    import dataclasses
+    import torch
+    import moe_expert_routing_02_b300 as M
+    from moe_expert_routing_02_b300 import workloads as W
+    M.lib()
+    c = W.config_by_name(args.config)
+    if args.T:
+        c = dataclasses.replace(c, T=args.T)
+    peaks = load_peaks()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    T, E, k, H, F = c.T, c.E, c.k, c.H, c.F
+    lg = torch.from_numpy(W.make_layer_logits(c, 0, layers=1)[0]).to(dev)
+    x = W.make_x(c, 0, 0, device=dev)
+    w1, w3, w2 = W.make_weights(c, 0, device=dev)
+    idx, w = M.moe_route(lg, k)
+    go, perm, inv, xp = M.moe_dispatch(x, idx, E, None)
+    ffn_ws = torch.empty(max(M.workspace_bytes(M.MOE_OP_EXPERT_FFN, T, k, E, H, F), 1024), dtype=torch.uint8,
+                         device=dev)
+    y = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+    fwd = lambda: M.moe_expert_ffn(xp, go, None, None, w1, w3, w2, c.act, y=y, workspace=ffn_ws)
+    fwd()
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    dout = torch.randn((T, H), generator=g, device=dev).to(torch.bfloat16)
+    f32 = dict(dtype=torch.float32, device=dev)
+    outs = (torch.empty((T, H), dtype=torch.bfloat16, device=dev), torch.empty((T, k), **f32),
+            torch.empty((E, H, F), **f32), torch.empty((E, H, F), **f32) if c.act == "swiglu" else None,
+            torch.empty((E, F, H), **f32))
+    ws = torch.empty(M.moe_ffn_backward_workspace_bytes(T, k, E, H, F), dtype=torch.uint8, device=dev)
+    dl = torch.empty((T, E), **f32)
+
+    def bwd():
+        M.moe_ffn_backward(x, dout, w, y, perm, inv, go, None, w1, w3, w2, c.act, workspace=ws, out=outs)
+        M.moe_route_backward(lg, idx, outs[1], out=dl)
+
+    def timed(fn, steps, warmup):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        e1.synchronize()
+        M.moe_check()
+        return e0.elapsed_time(e1) * 1e-3 / steps
+
+    steps, warmup = max(args.steps, 1), max(args.warmup, 3)
+    clk = ClockSampler(0)
+    clk.start()
+    t_bwd = timed(bwd, steps, warmup)
+    clocks = clk.stop()
+    t_fwd = timed(fwd, steps, warmup)
+    fl_b = backward_flops(c)
+    fl_f = (6 if c.act == "swiglu" else 4) * c.A * H * F
+    peak = peaks["bf16_tflops_sustained"]
+    res = {
+        "backward": c.name, "T": T, "E": E, "k": k, "H": H, "F": F, "act": c.act,
+        "steps": steps, "warmup": warmup,
+        "us_per_backward": round(t_bwd * 1e6, 1),
+        "tokens_per_s": round(T / t_bwd, 1),
+        "backward_tflops": round(fl_b / t_bwd / 1e12, 1),
+        "backward_frac_of_sustained_bf16": round(fl_b / t_bwd / 1e12 / peak, 3),
+        "us_forward_ffn": round(t_fwd * 1e6, 1),
+        "forward_ffn_tflops": round(fl_f / t_fwd / 1e12, 1),
+        "backward_over_forward_ffn": round(t_bwd / t_fwd, 2),
+        "gpu_launches_per_backward": 8,
+        "peak": {"bf16_tflops_sustained": peak, "source": peaks["source"]},
+        "clocks": clocks,
+        "data": "synthetic: the config's logits, x and weights; dout ~ N(0,1) bf16",
+    }
+    return res
+
+
 def _top_overlap(p_pred, load, m=5):
     """Share of the m most loaded experts that are among the m most popular
     predicted ones (ties: lower expert first on both sides)."""
@@ -760,6 +854,9 @@ def main(argv=None):
         return run_sweep(args)
     if args.quality:
         print(json.dumps(run_quality(args)), flush=True)
+        return 0
+    if args.backward:
+        print(json.dumps(run_backward(args)), flush=True)
         return 0
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))

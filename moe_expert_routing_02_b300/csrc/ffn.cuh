@@ -422,6 +422,62 @@ __device__ __forceinline__ void load_rows32(uint8_t* stg, const uint16_t* src, s
   }
 }
 
+// Coalesced read of a warp's 32 rows x 16 bf16 columns of src (row stride
+// ld) into registers: two 16-byte loads per lane, each instruction covering
+// 16 whole 32-byte row segments.  Rows >= rows_valid read as 0.
+__device__ __forceinline__ void prefetch_rows16(const uint16_t* src, size_t ld, int rows_valid, int lane,
+                                                uint4 (&v)[2]) {
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int idx = pass * 32 + lane;
+    const int r = idx >> 1, c = idx & 1;
+    v[pass] = r < rows_valid ? ld_nc_v4(src + (size_t)r * ld + c * 8) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// prefetch_rows16's registers -> lane i holds row i's 16 columns (8 packed
+// pairs), through the staging buffer in store_rows16's slot layout.
+__device__ __forceinline__ void transpose_rows16(uint8_t* stg, const uint4 (&v)[2], int lane, uint32_t (&dv)[8]) {
+  __syncwarp();
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int idx = pass * 32 + lane;
+    const int r = idx >> 1, c = idx & 1;
+    *reinterpret_cast<uint4*>(stg + r * 32 + (((c + (r >> 2)) & 1) << 4)) = v[pass];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint4 q = *reinterpret_cast<const uint4*>(stg + lane * 32 + (((j + (lane >> 2)) & 1) << 4));
+    dv[4 * j] = q.x;
+    dv[4 * j + 1] = q.y;
+    dv[4 * j + 2] = q.z;
+    dv[4 * j + 3] = q.w;
+  }
+}
+
+// store_rows32 for 16 columns: lane i holds row i's 16 bf16 columns (8
+// packed pairs); through 1 KB of staging, each row's two 16-byte chunks at
+// slots (j + r/4) mod 2, so that the writes (8 lanes per phase, rows r and
+// r+4 in different slots) and the reads (4 whole 32-byte rows per phase) are
+// free of bank conflicts.  Rows >= rows_valid are not written.
+__device__ __forceinline__ void store_rows16(uint8_t* stg, uint16_t* out, size_t ld, int rows_valid,
+                                             const uint32_t (&pk)[8], int lane) {
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+    *reinterpret_cast<uint4*>(stg + lane * 32 + (((j + (lane >> 2)) & 1) << 4)) =
+        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int idx = pass * 32 + lane;
+    const int r = idx >> 1, c = idx & 1;
+    const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 32 + (((c + (r >> 2)) & 1) << 4));
+    if (r < rows_valid) st_v4(out + (size_t)r * ld + c * 8, v);
+  }
+}
+
 __device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&pk)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
@@ -596,6 +652,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode(s, U, tile);
+      // backward epilogues: this lane's row of dA for the warp's first 16
+      // columns, loaded before the accumulator wait (the next pieces are
+      // loaded one piece ahead)
+      constexpr bool kBwd = EPI == kBwdGelu || EPI == kBwdSwiglu;
+      constexpr int kBwdW = EPI == kBwdSwiglu ? (BN / 2) / EPI_SLICES : BN / EPI_SLICES;
+      const int bcol0 = EPI == kBwdSwiglu ? t.nt * (BN / 2) + slice * kBwdW : t.nt * BN + slice * kBwdW;
+      const int brows = t.rows - quarter * 32;
+      const uint16_t* bsrc = kBwd ? p.side + (size_t)(t.row0 + quarter * 32) * p.N_out : nullptr;
+      uint4 pre[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+      if (kBwd && bcol0 < p.N_out) prefetch_rows16(bsrc + bcol0, (size_t)p.N_out, brows, lane, pre);
       // every lane waits; the vote keeps the warp converged for tcgen05.ld
       if (!__all_sync(0xffffffffu, wait_phase(&s.tfull[acc], acc_phase, &s.abort_flag))) break;
       tc_fence_after();
@@ -603,74 +669,61 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int wrows = t.rows - quarter * 32;
       uint16_t* wbase = p.out + (size_t)(t.row0 + quarter * 32) * p.N_out;
       const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      if (EPI == kBwdSwiglu) {
-        // a = silu(g) u;  dg = dA u silu'(g);  du = dA silu(g);
-        // silu(g) = g s, silu'(g) = s (1 + g (1 - s)), s = 1 / (1 + exp(-g))
-        constexpr int W = (BN / 2) / EPI_SLICES;
-        const size_t ld2 = 2 * (size_t)p.N_out;
+      if (EPI == kBwdSwiglu || EPI == kBwdGelu) {
+        // 16-column pieces.  GeLU: a = gelu(z), dz = dA gelu'(z).  SwiGLU:
+        // a = silu(g) u, dg = dA u silu'(g), du = dA silu(g), with
+        // silu(g) = g s, silu'(g) = s (1 + g (1 - s)), s = 1 / (1 + exp(-g)).
+        constexpr int NP = kBwdW / 16;
+        const size_t ld2 = (EPI == kBwdSwiglu ? 2 : 1) * (size_t)p.N_out;
         uint16_t* w2base = p.out2 + (size_t)(t.row0 + quarter * 32) * ld2;
-        const uint16_t* sbase = p.side + (size_t)(t.row0 + quarter * 32) * p.N_out;
-#pragma unroll 1
-        for (int cc = 0; cc < W; cc += 32) {
-          const int c = slice * W + cc;
-          uint32_t gr[32], ur[32];
-          __syncwarp();
-          tmem_ld32(tb + c, gr);
-          tmem_ld32(tb + BN / 2 + c, ur);
-          const int col = t.nt * (BN / 2) + c;
-          if (col < p.N_out) {
-            uint32_t dak[16];
-            load_rows32(s.stg[warp - 2], sbase + col, (size_t)p.N_out, wrows, dak, lane);
-            float va[32], vg[32], vu[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float g = __uint_as_float(gr[i]);
-              const float u = __uint_as_float(ur[i]);
-              const float da = (i & 1) ? bf16hi(dak[i >> 1]) : bf16lo(dak[i >> 1]);
-              const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
-              const float silu = g * sg;
-              va[i] = silu * u;
-              vg[i] = da * u * sg * fmaf(g, 1.0f - sg, 1.0f);
-              vu[i] = da * silu;
-            }
-            uint32_t pk[16];
-            pack32(va, pk);
-            store_rows32(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pk, lane);
-            pack32(vg, pk);
-            store_rows32(s.stg[warp - 2], w2base + col, ld2, wrows, pk, lane);
-            pack32(vu, pk);
-            store_rows32(s.stg[warp - 2], w2base + p.N_out + col, ld2, wrows, pk, lane);
-          }
-        }
-      } else if (EPI == kBwdGelu) {
-        // a = gelu(z);  dz = dA gelu'(z)
-        constexpr int W = BN / EPI_SLICES;
-        uint16_t* w2base = p.out2 + (size_t)(t.row0 + quarter * 32) * p.N_out;
-        const uint16_t* sbase = p.side + (size_t)(t.row0 + quarter * 32) * p.N_out;
-#pragma unroll 1
-        for (int cc = 0; cc < W; cc += 32) {
-          const int c = slice * W + cc;
-          uint32_t raw[32];
+        for (int pc = 0; pc < NP; ++pc) {
+          const int col = bcol0 + pc * 16;
+          if (col >= p.N_out) break;  // warp-uniform; later pieces lie further right
+          uint32_t dv[8];
+          transpose_rows16(s.stg[warp - 2], pre, lane, dv);
+          if (pc + 1 < NP && col + 16 < p.N_out) prefetch_rows16(bsrc + col + 16, (size_t)p.N_out, brows, lane, pre);
+          const int c = slice * kBwdW + pc * 16;  // TMEM column
           __syncwarp();
-          tmem_ld32(tb + c, raw);
-          const int col = t.nt * BN + c;
-          if (col < p.N_out) {
-            uint32_t dak[16];
-            load_rows32(s.stg[warp - 2], sbase + col, (size_t)p.N_out, wrows, dak, lane);
-            float va[32], vd[32];
+          if (EPI == kBwdGelu) {
+            uint32_t raw[16];
+            tmem_ld16(tb + c, raw);
+            uint32_t pa[8], pd[8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float da = (i & 1) ? bf16hi(dak[i >> 1]) : bf16lo(dak[i >> 1]);
-              float a, g;
-              gelu_and_grad(__uint_as_float(raw[i]), a, g);
-              va[i] = a;
-              vd[i] = da * g;
+            for (int i = 0; i < 8; ++i) {
+              float a0, g0, a1, g1;
+              gelu_and_grad(__uint_as_float(raw[2 * i]), a0, g0);
+              gelu_and_grad(__uint_as_float(raw[2 * i + 1]), a1, g1);
+              pa[i] = pack_bf16x2(a0, a1);
+              pd[i] = pack_bf16x2(bf16lo(dv[i]) * g0, bf16hi(dv[i]) * g1);
             }
-            uint32_t pk[16];
-            pack32(va, pk);
-            store_rows32(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pk, lane);
-            pack32(vd, pk);
-            store_rows32(s.stg[warp - 2], w2base + col, (size_t)p.N_out, wrows, pk, lane);
+            store_rows16(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pa, lane);
+            store_rows16(s.stg[warp - 2], w2base + col, ld2, wrows, pd, lane);
+          } else {
+            uint32_t gr[16], ur[16];
+            tmem_ld16x2(tb + c, tb + BN / 2 + c, gr, ur);
+            uint32_t pa[8], pg[8], pu[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float va[2], vg[2], vu[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const float g = __uint_as_float(gr[2 * i + h]);
+                const float u = __uint_as_float(ur[2 * i + h]);
+                const float da = h ? bf16hi(dv[i]) : bf16lo(dv[i]);
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
+                const float silu = g * sg;
+                va[h] = silu * u;
+                vg[h] = da * u * sg * fmaf(g, 1.0f - sg, 1.0f);
+                vu[h] = da * silu;
+              }
+              pa[i] = pack_bf16x2(va[0], va[1]);
+              pg[i] = pack_bf16x2(vg[0], vg[1]);
+              pu[i] = pack_bf16x2(vu[0], vu[1]);
+            }
+            store_rows16(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pa, lane);
+            store_rows16(s.stg[warp - 2], w2base + col, ld2, wrows, pg, lane);
+            store_rows16(s.stg[warp - 2], w2base + p.N_out + col, ld2, wrows, pu, lane);
           }
         }
       } else if (EPI == kSwiglu) {
