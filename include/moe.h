@@ -385,9 +385,10 @@ moe_status moe_expert_ffn_slots(const uint16_t* xp, const int32_t* group_offsets
  *           du = dA silu(g), dW1 = xp^T dg, dW3 = xp^T du,
  *           dxp = dg W1^T + du W3^T;
  *   dx[t] = sum_r dxp[inv_perm[t k + r]].
- * Arithmetic: bf16 operands, fp32 accumulation; dY, dA, a, dz (dg, du) and
- * dxp are rounded to bf16 between the GEMMs (as the forward rounds its
- * intermediate); the weight gradients and dw are fp32.
+ * Arithmetic: bf16 operands, fp32 accumulation; dY, a, the derivative
+ * factors (gelu'(z); u silu'(g) and silu(g)), dz (dg, du) and dxp are rounded
+ * to bf16 between the GEMMs (as the forward rounds its intermediate); dA
+ * stays fp32 in the accumulator; the weight gradients and dw are fp32.
  *
  *   x, dout      bf16 [T, H]: the layer input and the output's gradient
  *   w            f32 [T, k] gate weights (moe_route)

@@ -83,12 +83,17 @@ constexpr uint32_t kMaxPolls = 1u << 30;
 // MN-major).  kStoreKM: data gradient, B = the transpose of the weights as
 // stored (K-major rows of the weight tensor), K optionally split between two
 // weight tensors at k_split blocks.  kBwdGelu / kBwdSwiglu: GEMM1 recomputed in
-// the backward pass; the epilogue reads the activation's gradient dA (side)
-// and writes the activation (out) and the pre-activation gradients (out2).
-enum Epi : int { kGelu = 0, kSwiglu = 1, kStore = 2, kStoreKM = 3, kBwdGelu = 4, kBwdSwiglu = 5 };
+// the backward pass; the epilogue writes the activation (out) and the factors
+// that turn dA into the pre-activation gradients (out2): gelu'(z), or
+// [u silu'(g) | silu(g)] for SwiGLU.  kStoreKMMul: dA = dY W2^T (K-major B);
+// the epilogue multiplies dA by those factors in place (out), giving dz;
+// kStoreKMMul2 likewise with the SwiGLU pair of factors, giving [dg | du].
+enum Epi : int {
+  kGelu = 0, kSwiglu = 1, kStore = 2, kStoreKM = 3, kBwdGelu = 4, kBwdSwiglu = 5, kStoreKMMul = 6, kStoreKMMul2 = 7
+};
 
 __host__ __device__ constexpr bool epi_pair_b(int e) { return e == kSwiglu || e == kBwdSwiglu; }
-__host__ __device__ constexpr bool epi_kmajor_b(int e) { return e == kStoreKM; }
+__host__ __device__ constexpr bool epi_kmajor_b(int e) { return e == kStoreKM || e == kStoreKMMul || e == kStoreKMMul2; }
 
 struct Params {
   const int32_t* group_offsets;  // [G+1]
@@ -112,10 +117,10 @@ struct Params {
   // kStoreKM: k-blocks below k_split read the first weight tensor, the rest
   // the second (at k-block kb - k_split).
   int k_split;
-  // kBwdGelu / kBwdSwiglu: side = dA [A_rows, N_out]; out = activation
-  // [A_rows, N_out]; out2 = dz [A_rows, N_out] (GeLU) or [dg | du]
-  // [A_rows, 2 N_out] (SwiGLU).
-  const uint16_t* side;
+  // kBwdGelu / kBwdSwiglu: out = activation [A_rows, N_out]; out2 = the
+  // factors, [A_rows, N_out] (GeLU) or [A_rows, 2 N_out] (SwiGLU).
+  // kStoreKMMul / kStoreKMMul2: out = those factors, overwritten with the
+  // products.
   uint16_t* out2;
 };
 
@@ -128,6 +133,7 @@ struct Smem {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t fbar[EPI_WARPS][2];  // kStoreKMMul: per-warp factor buffers
   uint32_t tmem_base;
   uint32_t abort_flag;
   int32_t total_tiles;
@@ -348,6 +354,43 @@ __device__ __forceinline__ void gelu_and_grad(float z, float& a, float& da) {
   da = fmaf(z * 0.39894228040143268f, ex, Phi);
 }
 
+// gelu_and_grad on a pair (z0, z1), on packed fp32 pairs where the two
+// halves share an instruction; the same operations in the same order as the
+// scalar form, so each half's results are bit-identical to it.  The erf
+// polynomial is evaluated with negated coefficients (each step exactly the
+// negation of the scalar step), which gives 1 - q e as one fused step.
+__device__ __forceinline__ void gelu_and_grad2(f32x2 z, f32x2& a, f32x2& da) {
+  const f32x2 x = f2_mul(z, f2_splat(0.70710678118654752f));
+  float x0, x1;
+  f2_unpack(x, x0, x1);
+  const f32x2 ax = f2_pack(fabsf(x0), fabsf(x1));
+  float d0, d1;
+  f2_unpack(f2_fma(f2_splat(0.3275911f), ax, f2_splat(1.0f)), d0, d1);
+  const f32x2 t = f2_pack(__fdividef(1.0f, d0), __fdividef(1.0f, d1));
+  f32x2 nq = f2_fma(f2_splat(-1.061405429f), t, f2_splat(1.453152027f));
+  nq = f2_fma(nq, t, f2_splat(-1.421413741f));
+  nq = f2_fma(nq, t, f2_splat(0.284496736f));
+  nq = f2_fma(nq, t, f2_splat(-0.254829592f));
+  nq = f2_mul(nq, t);
+  float s0, s1;
+  f2_unpack(f2_mul(ax, ax), s0, s1);
+  const f32x2 ex = f2_pack(__expf(-s0), __expf(-s1));
+  float r0, r1;
+  f2_unpack(f2_fma(nq, ex, f2_splat(1.0f)), r0, r1);
+  const f32x2 Phi = f2_fma(f2_splat(0.5f), f2_pack(copysignf(r0, x0), copysignf(r1, x1)), f2_splat(0.5f));
+  a = f2_mul(z, Phi);
+  da = f2_fma(f2_mul(z, f2_splat(0.39894228040143268f)), ex, Phi);
+}
+
+// bf16 pair (packed as in pack_bf16x2) -> fp32 pair
+__device__ __forceinline__ f32x2 bf16x2_to_f2(uint32_t v) { return f2_pack(bf16lo(v), bf16hi(v)); }
+
+__device__ __forceinline__ uint32_t f2_to_bf16x2(f32x2 v) {
+  float lo, hi;
+  f2_unpack(v, lo, hi);
+  return pack_bf16x2(lo, hi);
+}
+
 __device__ __forceinline__ void store32(uint16_t* dst, const float (&v)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -504,6 +547,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
+    for (int w = 0; w < EPI_WARPS; ++w) {
+      mbar_init(&s.fbar[w][0], 1);
+      mbar_init(&s.fbar[w][1], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
       mbar_init(&s.tempty[i], EPI_WARPS);
@@ -527,6 +574,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = s.tmem_base;
   const int total = s.total_tiles;
   const int kblocks = p.K / BK;
+  // kStoreKMMul keeps the last stage's B buffer for its epilogue's factor
+  // tiles (16 warps x two 1 KB buffers) and runs the operand ring on the rest
+  constexpr int NST = EPI == kStoreKMMul ? STAGES - 1 : STAGES;
+  static_assert(EPI_WARPS * 2 * 1024 <= B_BYTES, "factor buffers exceed one B stage");
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -575,7 +626,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (gather) tma_gather4(s.a[stage] + lane * 512, &tmA, &s.full[stage], kb * BK, src);
         ++issued;
-        if (++stage == STAGES) {
+        if (++stage == NST) {
           stage = 0;
           phase ^= 1;
         }
@@ -583,10 +634,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     // every stage's latest copy must have landed before the CTA may exit
     if (lane == 0) {
-      for (uint32_t st = 0; st < (uint32_t)STAGES; ++st) {
+      for (uint32_t st = 0; st < (uint32_t)NST; ++st) {
         if (issued > st) {
-          const uint32_t last = issued - 1 - ((issued - 1 - st) % STAGES);
-          wait_phase(&s.full[st], (last / STAGES) & 1u, &s.abort_flag, true);
+          const uint32_t last = issued - 1 - ((issued - 1 - st) % NST);
+          wait_phase(&s.full[st], (last / NST) & 1u, &s.abort_flag, true);
         }
       }
     }
@@ -625,7 +676,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * kBStep), idesc, (kb | kk) != 0 ? 1u : 0u);
           mma_commit(&s.empty[stage]);
           any_mma = true;
-          if (++stage == STAGES) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1;
           }
@@ -650,18 +701,48 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
     const int slice = (warp - 2) >> 2;         // column slice 0..EPI_SLICES-1
     uint32_t acc = 0, acc_phase = 0;
+    // kStoreKMMul: this warp's two factor buffers, their next phases and
+    // whether a copy into them is outstanding
+    uint8_t* fbuf = s.b[STAGES - 1] + (warp - 2) * 2048;
+    uint32_t fph[2] = {0u, 0u};
+    bool fpend[2] = {false, false};
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode(s, U, tile);
-      // backward epilogues: this lane's row of dA for the warp's first 16
-      // columns, loaded before the accumulator wait (the next pieces are
-      // loaded one piece ahead)
-      constexpr bool kBwd = EPI == kBwdGelu || EPI == kBwdSwiglu;
-      constexpr int kBwdW = EPI == kBwdSwiglu ? (BN / 2) / EPI_SLICES : BN / EPI_SLICES;
-      const int bcol0 = EPI == kBwdSwiglu ? t.nt * (BN / 2) + slice * kBwdW : t.nt * BN + slice * kBwdW;
-      const int brows = t.rows - quarter * 32;
-      const uint16_t* bsrc = kBwd ? p.side + (size_t)(t.row0 + quarter * 32) * p.N_out : nullptr;
-      uint4 pre[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-      if (kBwd && bcol0 < p.N_out) prefetch_rows16(bsrc + bcol0, (size_t)p.N_out, brows, lane, pre);
+      // Multiply epilogues: the factor rows of the warp's 64 columns are
+      // requested before the accumulator wait.  kStoreKMMul: two 32x16 TMA
+      // boxes into the warp's factor buffers (pieces 2, 3 follow as 0, 1 are
+      // read); kStoreKMMul2 (SwiGLU, two factors): plain loads, the first
+      // factor's whole slice ahead and the second one piece ahead.
+      constexpr bool kMul = EPI == kStoreKMMul || EPI == kStoreKMMul2;
+      constexpr bool kPair = EPI == kStoreKMMul2;
+      constexpr int kMulW = BN / EPI_SLICES;
+      constexpr int kMulNP = kMulW / 16;
+      const int mcol0 = t.nt * BN + slice * kMulW;
+      const size_t mld = (kPair ? 2 : 1) * (size_t)p.N_out;
+      const int mrow = (int)t.row0 + quarter * 32;
+      uint16_t* mbase = kMul ? p.out + (size_t)mrow * mld : nullptr;
+      uint4 pre[kPair ? kMulNP : 1][2];
+      uint4 preu[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+      if (EPI == kStoreKMMul) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          if (mcol0 + 16 * q < p.N_out) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&s.fbar[warp - 2][q], 1024);
+              tma_load_2d(fbuf + q * 1024, &tmB1, &s.fbar[warp - 2][q], mcol0 + 16 * q, mrow);
+            }
+            fpend[q] = true;
+          }
+        }
+      } else if (kPair) {
+#pragma unroll
+        for (int pc = 0; pc < kMulNP; ++pc) {
+          pre[pc][0] = pre[pc][1] = make_uint4(0, 0, 0, 0);
+          if (mcol0 + 16 * pc < p.N_out)
+            prefetch_rows16(mbase + mcol0 + 16 * pc, mld, t.rows - quarter * 32, lane, pre[pc]);
+        }
+        if (mcol0 < p.N_out) prefetch_rows16(mbase + p.N_out + mcol0, mld, t.rows - quarter * 32, lane, preu);
+      }
       // every lane waits; the vote keeps the warp converged for tcgen05.ld
       if (!__all_sync(0xffffffffu, wait_phase(&s.tfull[acc], acc_phase, &s.abort_flag))) break;
       tc_fence_after();
@@ -669,21 +750,75 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int wrows = t.rows - quarter * 32;
       uint16_t* wbase = p.out + (size_t)(t.row0 + quarter * 32) * p.N_out;
       const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      if (EPI == kBwdSwiglu || EPI == kBwdGelu) {
-        // 16-column pieces.  GeLU: a = gelu(z), dz = dA gelu'(z).  SwiGLU:
-        // a = silu(g) u, dg = dA u silu'(g), du = dA silu(g), with
-        // silu(g) = g s, silu'(g) = s (1 + g (1 - s)), s = 1 / (1 + exp(-g)).
-        constexpr int NP = kBwdW / 16;
-        const size_t ld2 = (EPI == kBwdSwiglu ? 2 : 1) * (size_t)p.N_out;
-        uint16_t* w2base = p.out2 + (size_t)(t.row0 + quarter * 32) * ld2;
+      if (kMul) {
+        // dz = dA * gelu'(z), or dg = dA * u silu'(g) and du = dA * silu(g),
+        // over the factors in place; 16-column pieces
+        constexpr int NP = kMulNP;
+        bool ok = true;
 #pragma unroll
         for (int pc = 0; pc < NP; ++pc) {
-          const int col = bcol0 + pc * 16;
+          const int col = mcol0 + pc * 16;
           if (col >= p.N_out) break;  // warp-uniform; later pieces lie further right
-          uint32_t dv[8];
-          transpose_rows16(s.stg[warp - 2], pre, lane, dv);
-          if (pc + 1 < NP && col + 16 < p.N_out) prefetch_rows16(bsrc + col + 16, (size_t)p.N_out, brows, lane, pre);
-          const int c = slice * kBwdW + pc * 16;  // TMEM column
+          uint32_t fv[8], fu[8];
+          if (EPI == kStoreKMMul) {
+            const int b = pc & 1;
+            if (!__all_sync(0xffffffffu, wait_phase(&s.fbar[warp - 2][b], fph[b], &s.abort_flag))) {
+              ok = false;
+              break;
+            }
+            fph[b] ^= 1u;
+            fpend[b] = false;
+            const uint4 q0 = *reinterpret_cast<const uint4*>(fbuf + b * 1024 + lane * 32);
+            const uint4 q1 = *reinterpret_cast<const uint4*>(fbuf + b * 1024 + lane * 32 + 16);
+            fv[0] = q0.x; fv[1] = q0.y; fv[2] = q0.z; fv[3] = q0.w;
+            fv[4] = q1.x; fv[5] = q1.y; fv[6] = q1.z; fv[7] = q1.w;
+            __syncwarp();
+            if (pc + 2 < NP && col + 32 < p.N_out) {
+              if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // reads above, then the copy
+                mbar_arrive_expect_tx(&s.fbar[warp - 2][b], 1024);
+                tma_load_2d(fbuf + b * 1024, &tmB1, &s.fbar[warp - 2][b], col + 32, mrow);
+              }
+              fpend[b] = true;
+            }
+          } else {
+            transpose_rows16(s.stg[warp - 2], pre[kPair ? pc : 0], lane, fv);
+            transpose_rows16(s.stg[warp - 2], preu, lane, fu);
+            if (pc + 1 < NP && col + 16 < p.N_out)
+              prefetch_rows16(mbase + p.N_out + col + 16, mld, wrows, lane, preu);
+          }
+          __syncwarp();
+          uint32_t raw[16];
+          tmem_ld16(tb + slice * kMulW + pc * 16, raw);
+          uint32_t o[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            o[i] = f2_to_bf16x2(f2_mul(f2_pack(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),
+                                       bf16x2_to_f2(fv[i])));
+          store_rows16(s.stg[warp - 2], mbase + col, mld, wrows, o, lane);
+          if (kPair) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o[i] = f2_to_bf16x2(f2_mul(f2_pack(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),
+                                         bf16x2_to_f2(fu[i])));
+            store_rows16(s.stg[warp - 2], mbase + p.N_out + col, mld, wrows, o, lane);
+          }
+        }
+        if (!ok) break;
+      } else if (EPI == kBwdSwiglu || EPI == kBwdGelu) {
+        // 16-column pieces.  GeLU: a = gelu(z), factor gelu'(z).  SwiGLU:
+        // a = silu(g) u, factors u silu'(g) and silu(g), with silu(g) = g s,
+        // silu'(g) = s (1 + g (1 - s)), s = 1 / (1 + exp(-g)).
+        constexpr int W = EPI == kBwdSwiglu ? (BN / 2) / EPI_SLICES : BN / EPI_SLICES;
+        constexpr int NP = W / 16;
+        const int col0 = EPI == kBwdSwiglu ? t.nt * (BN / 2) + slice * W : t.nt * BN + slice * W;
+        const size_t ld2 = (EPI == kBwdSwiglu ? 2 : 1) * (size_t)p.N_out;
+        uint16_t* w2base = p.out2 + (size_t)(t.row0 + quarter * 32) * ld2;
+#pragma unroll 1
+        for (int pc = 0; pc < NP; ++pc) {
+          const int col = col0 + pc * 16;
+          if (col >= p.N_out) break;  // warp-uniform
+          const int c = slice * W + pc * 16;  // TMEM column
           __syncwarp();
           if (EPI == kBwdGelu) {
             uint32_t raw[16];
@@ -691,11 +826,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t pa[8], pd[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              float a0, g0, a1, g1;
-              gelu_and_grad(__uint_as_float(raw[2 * i]), a0, g0);
-              gelu_and_grad(__uint_as_float(raw[2 * i + 1]), a1, g1);
-              pa[i] = pack_bf16x2(a0, a1);
-              pd[i] = pack_bf16x2(bf16lo(dv[i]) * g0, bf16hi(dv[i]) * g1);
+              f32x2 a, g;
+              gelu_and_grad2(f2_pack(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])), a, g);
+              pa[i] = f2_to_bf16x2(a);
+              pd[i] = f2_to_bf16x2(g);
             }
             store_rows16(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pa, lane);
             store_rows16(s.stg[warp - 2], w2base + col, ld2, wrows, pd, lane);
@@ -705,21 +839,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t pa[8], pg[8], pu[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              float va[2], vg[2], vu[2];
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const float g = __uint_as_float(gr[2 * i + h]);
-                const float u = __uint_as_float(ur[2 * i + h]);
-                const float da = h ? bf16hi(dv[i]) : bf16lo(dv[i]);
-                const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
-                const float silu = g * sg;
-                va[h] = silu * u;
-                vg[h] = da * u * sg * fmaf(g, 1.0f - sg, 1.0f);
-                vu[h] = da * silu;
-              }
-              pa[i] = pack_bf16x2(va[0], va[1]);
-              pg[i] = pack_bf16x2(vg[0], vg[1]);
-              pu[i] = pack_bf16x2(vu[0], vu[1]);
+              const float g0 = __uint_as_float(gr[2 * i]), g1 = __uint_as_float(gr[2 * i + 1]);
+              const f32x2 g = f2_pack(g0, g1);
+              const f32x2 u = f2_pack(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1]));
+              float e0, e1;
+              f2_unpack(f2_add(f2_pack(__expf(-g0), __expf(-g1)), f2_splat(1.0f)), e0, e1);
+              const f32x2 sg = f2_pack(__fdividef(1.0f, e0), __fdividef(1.0f, e1));
+              const f32x2 silu = f2_mul(g, sg);
+              const f32x2 oms = f2_add(f2_splat(1.0f), f2_mul(sg, f2_splat(-1.0f)));
+              pa[i] = f2_to_bf16x2(f2_mul(silu, u));
+              pg[i] = f2_to_bf16x2(f2_mul(f2_mul(u, sg), f2_fma(g, oms, f2_splat(1.0f))));
+              pu[i] = f2_to_bf16x2(silu);
             }
             store_rows16(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pa, lane);
             store_rows16(s.stg[warp - 2], w2base + col, ld2, wrows, pg, lane);
@@ -777,6 +907,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         acc = 0;
         acc_phase ^= 1;
       }
+    }
+    // factor copies still in flight (a role aborted) land before the exit
+    if (EPI == kStoreKMMul && lane == 0) {
+      for (int b = 0; b < 2; ++b)
+        if (fpend[b]) wait_phase(&s.fbar[warp - 2][b], fph[b], &s.abort_flag, true);
     }
   }
 

@@ -10,9 +10,11 @@
 // Steps (one stream, seven launches):
 //   1 layout   padded row space of the expert units (bwd::layout_kernel)
 //   2 gather   xp = x rows, dY = w * dout rows in that space, dw = <dout, y>
-//   3 dgrad    dA = dY W2^T                       (ffn::gemm_kernel<kStoreKM>)
-//   4 recompute GEMM1 with the backward epilogue:   (ffn::gemm_kernel<kBwd*>)
-//              GeLU: a = gelu(z), dz = dA gelu'(z);  SwiGLU: a, dg, du
+//   3 recompute GEMM1 with the backward epilogue:   (ffn::gemm_kernel<kBwd*>)
+//              GeLU: a = gelu(z) and the factor gelu'(z);
+//              SwiGLU: a = silu(g) u and the factors u silu'(g), silu(g)
+//   4 dgrad    dA = dY W2^T, multiplied by the factors in the epilogue:
+//              dz (GeLU) or [dg | du] (SwiGLU)  (ffn::gemm_kernel<kStoreKMMul>)
 //   5 dgrad    dxp = dz W1^T  (SwiGLU: [dg du] [W1; W3]^T, K = 2F)
 //   6 wgrad    dW2 = a^T dY, dW1 = xp^T dz (SwiGLU: dg), dW3 = xp^T du
 //   7 scatter  dx[t] = sum_r dxp[row of (t, r)]
@@ -29,7 +31,7 @@ namespace {
 // activation); offsets in bytes, each a multiple of 256.
 struct BwdWs {
   long long P;  // rows of the padded row space (bound)
-  size_t pgoff, pue, ustart, pbeg, pcnt, prow, xp, dy, dA, act, dz, dxp, total;
+  size_t pgoff, pue, ustart, pbeg, pcnt, prow, xp, dy, act, dz, dxp, total;
 };
 
 BwdWs bwd_ws(long long A, int E, int H, int F) {
@@ -50,7 +52,6 @@ BwdWs bwd_ws(long long A, int E, int H, int F) {
   w.prow = take((size_t)(A > 0 ? A : 1) * 4);
   w.xp = take((size_t)w.P * H * 2);
   w.dy = take((size_t)w.P * H * 2);
-  w.dA = take((size_t)w.P * F * 2);
   w.act = take((size_t)w.P * F * 2);
   w.dz = take((size_t)w.P * 2 * F * 2);
   w.dxp = take((size_t)w.P * H * 2);
@@ -58,14 +59,16 @@ BwdWs bwd_ws(long long A, int E, int H, int F) {
   return w;
 }
 
-bool g_bwd_attr[kMaxDevices][4] = {};
+bool g_bwd_attr[kMaxDevices][6] = {};
 
 moe_status bwd_attrs(int dev) {
   std::lock_guard<std::mutex> lk(g_mu);
-  const void* fns[4] = {(const void*)ffn::gemm_kernel<ffn::kStoreKM>, (const void*)ffn::gemm_kernel<ffn::kBwdGelu>,
-                        (const void*)ffn::gemm_kernel<ffn::kBwdSwiglu>, (const void*)ffn_wg::wgrad_kernel};
-  const int bytes[4] = {(int)ffn::kSmemBytes, (int)ffn::kSmemBytes, (int)ffn::kSmemBytes, (int)ffn_wg::kSmemBytes};
-  for (int i = 0; i < 4; ++i) {
+  const void* fns[6] = {(const void*)ffn::gemm_kernel<ffn::kStoreKM>,    (const void*)ffn::gemm_kernel<ffn::kBwdGelu>,
+                        (const void*)ffn::gemm_kernel<ffn::kBwdSwiglu>,  (const void*)ffn_wg::wgrad_kernel,
+                        (const void*)ffn::gemm_kernel<ffn::kStoreKMMul>, (const void*)ffn::gemm_kernel<ffn::kStoreKMMul2>};
+  const int bytes[6] = {(int)ffn::kSmemBytes, (int)ffn::kSmemBytes, (int)ffn::kSmemBytes, (int)ffn_wg::kSmemBytes,
+                        (int)ffn::kSmemBytes, (int)ffn::kSmemBytes};
+  for (int i = 0; i < 6; ++i) {
     if (g_bwd_attr[dev][i]) continue;
     cudaError_t e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, bytes[i]);
     if (e != cudaSuccess) return cuda_at("moe_ffn_backward", e, "cudaFuncSetAttribute");
@@ -126,7 +129,6 @@ moe_status moe_ffn_backward(const uint16_t* x, const uint16_t* dout, const float
   int32_t* prow = reinterpret_cast<int32_t*>(ws + L.prow);
   uint16_t* xp = reinterpret_cast<uint16_t*>(ws + L.xp);
   uint16_t* dy = reinterpret_cast<uint16_t*>(ws + L.dy);
-  uint16_t* dA = reinterpret_cast<uint16_t*>(ws + L.dA);
   uint16_t* av = reinterpret_cast<uint16_t*>(ws + L.act);
   uint16_t* dz = reinterpret_cast<uint16_t*>(ws + L.dz);
   uint16_t* dxp = reinterpret_cast<uint16_t*>(ws + L.dxp);
@@ -180,27 +182,33 @@ moe_status moe_ffn_backward(const uint16_t* x, const uint16_t* dout, const float
     if (g > d->num_sms) g = d->num_sms;
     return (unsigned)(g < 1 ? 1 : g);
   };
-  ffn::Params p3 = pb;  // dA = dY W2^T: K = H, N = F
-  p3.K = H;
-  p3.N_out = F;
-  p3.n_tiles = (F + ffn::BN - 1) / ffn::BN;
-  p3.k_split = H / ffn::BK;
-  p3.out = dA;
-  ffn::gemm_kernel<ffn::kStoreKM><<<grid_for(p3), ffn::THREADS, ffn::kSmemBytes, st>>>(mDy, mW2k, mW2k, p3);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_at(who, e, "dgrad (dA) launch");
-
-  ffn::Params p4 = pb;  // GEMM1 recomputed, backward epilogue
+  ffn::Params p4 = pb;  // GEMM1 recomputed: activation and derivative factors
   p4.K = H;
   p4.N_out = F;
   p4.n_tiles = swiglu ? (F + ffn::BN / 2 - 1) / (ffn::BN / 2) : (F + ffn::BN - 1) / ffn::BN;
   p4.out = av;
-  p4.side = dA;
   p4.out2 = dz;
   if (swiglu)
     ffn::gemm_kernel<ffn::kBwdSwiglu><<<grid_for(p4), ffn::THREADS, ffn::kSmemBytes, st>>>(mXp, mW1, mW3, p4);
   else
     ffn::gemm_kernel<ffn::kBwdGelu><<<grid_for(p4), ffn::THREADS, ffn::kSmemBytes, st>>>(mXp, mW1, mW3, p4);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_at(who, e, "recompute launch");
+
+  ffn::Params p3 = pb;  // dA = dY W2^T (K = H, N = F) times the factors, in place
+  p3.K = H;
+  p3.N_out = F;
+  p3.n_tiles = (F + ffn::BN - 1) / ffn::BN;
+  p3.k_split = H / ffn::BK;
+  p3.out = dz;
+  if (swiglu) {
+    ffn::gemm_kernel<ffn::kStoreKMMul2><<<grid_for(p3), ffn::THREADS, ffn::kSmemBytes, st>>>(mDy, mW2k, mW2k, p3);
+  } else {
+    // the factor tiles come through TMA: 16-column x 32-row boxes of dz
+    CUtensorMap mF;
+    if ((ms = encode_2d(&mF, dz, F, P, 16, 32, false)) != MOE_OK) return ms;
+    ffn::gemm_kernel<ffn::kStoreKMMul><<<grid_for(p3), ffn::THREADS, ffn::kSmemBytes, st>>>(mDy, mW2k, mF, p3);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_at(who, e, "dgrad (dA) launch");
 
   ffn::Params p5 = pb;  // dxp = dz W1^T (+ du W3^T): K = F or 2F, N = H
   p5.K = KZ;

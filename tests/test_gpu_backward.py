@@ -2,9 +2,9 @@
 moe_route_backward) against the oracle's float64 gradients on the same seeded
 bf16 inputs and the same routing.
 
-Tolerances: the GPU rounds dY, dA, the activation, dz (dg, du) and dxp to
-bf16 between its GEMMs (2^-9 relative each, as the forward rounds its
-intermediate), so dx and the weight gradients are held to the forward FFN's
+Tolerances: the GPU rounds dY, the activation, the derivative factors, dz
+(dg, du) and dxp to bf16 between its GEMMs (2^-9 relative each, as the
+forward rounds its intermediate), so dx and the weight gradients are held to the forward FFN's
 2e-2 relative Frobenius error.  dw is an fp32 dot product of bf16 values
 (exact products): |error| <= 1e-5 * sum |terms|.  The gate's gradient is fp32
 softmax arithmetic: 1e-5 relative to the largest |dw|."""
