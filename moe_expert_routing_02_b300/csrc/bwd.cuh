@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(256)
         src[r] = pr;
       }
     }
+#pragma unroll 2
     for (int c = lane; c < H8; c += 32) {
       float acc[8];
 #pragma unroll
@@ -271,7 +272,9 @@ __global__ void __launch_bounds__(256)
 }
 
 // Gradient of the gate weights with respect to the router logits, the chosen
-// experts held fixed.  One warp per token, fp32.
+// experts held fixed.  One thread per token (the work per token is a few
+// dependent loads and k..E exponentials, so a warp per token leaves most
+// lanes idle and the grid latency-bound), fp32.
 //   renorm: w_r = softmax over the chosen logits;
 //           dl[e_r] = w_r (dw_r - sum_s w_s dw_s), 0 for the other experts
 //   full:   w_r = p[e_r], p = softmax over all E logits;
@@ -279,62 +282,61 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     route_bwd_kernel(const float* logits, const int32_t* idx, const float* dwt, int T, int E, int k, int renorm,
                      float* dl) {
-  const int lane = threadIdx.x & 31;
-  for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
-       t += (long long)gridDim.x * (blockDim.x >> 5)) {
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < T; t += (long long)gridDim.x * blockDim.x) {
     const float* l = logits + t * E;
     float* o = dl + t * E;
-    int e_r = 0;
-    float d_r = 0.f;
-    if (lane < k) {
-      e_r = idx[t * k + lane];
-      if (e_r < 0 || e_r >= E) {
-        moe_flag_error(MOE_DEVERR_DATA);
-        e_r = 0;
+    int e[8];
+    float d[8], lr[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      e[r] = 0;
+      d[r] = 0.f;
+      if (r < k) {
+        e[r] = idx[t * k + r];
+        if (e[r] < 0 || e[r] >= E) {
+          moe_flag_error(MOE_DEVERR_DATA);
+          e[r] = 0;
+        }
+        d[r] = dwt[t * k + r];
       }
-      d_r = dwt[t * k + lane];
     }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) lr[r] = r < k ? l[e[r]] : -INFINITY;
     if (renorm) {
-      const float lr = lane < k ? l[e_r] : -INFINITY;
-      float m = lr;
+      float m = lr[0];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      const float z = lane < k ? expf(lr - m) : 0.f;
-      float sum = z;
+      for (int r = 1; r < 8; ++r) m = fmaxf(m, lr[r]);
+      float z[8], sum = 0.f;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      const float w_r = z / sum;
-      float c = w_r * d_r;
+      for (int r = 0; r < 8; ++r) {
+        z[r] = r < k ? expf(lr[r] - m) : 0.f;
+        sum += z[r];
+      }
+      float c = 0.f;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-      for (int j = lane; j < E; j += 32) o[j] = 0.f;
-      __syncwarp();
-      if (lane < k) o[e_r] = w_r * (d_r - c);
+      for (int r = 0; r < 8; ++r) {
+        z[r] /= sum;  // w_r
+        c = fmaf(z[r], d[r], c);
+      }
+      for (int j = 0; j < E; ++j) o[j] = 0.f;
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < k) o[e[r]] = z[r] * (d[r] - c);
     } else {
       float m = -INFINITY;
-      for (int j = lane; j < E; j += 32) m = fmaxf(m, l[j]);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      for (int j = 0; j < E; ++j) m = fmaxf(m, l[j]);
       float sum = 0.f;
-      for (int j = lane; j < E; j += 32) sum += expf(l[j] - m);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      for (int j = 0; j < E; ++j) sum += expf(l[j] - m);
       const float inv = 1.0f / sum;
-      float c = lane < k ? d_r * expf(l[e_r] - m) * inv : 0.f;
+      float c = 0.f;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-      int er_all[8];
-      float dr_all[8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {  // every lane shuffles, before the lane-dependent loop
-        er_all[r] = __shfl_sync(0xffffffffu, e_r, r);
-        dr_all[r] = __shfl_sync(0xffffffffu, d_r, r);
-      }
-      for (int j = lane; j < E; j += 32) {
+      for (int r = 0; r < 8; ++r)
+        if (r < k) c = fmaf(d[r], expf(lr[r] - m) * inv, c);
+      for (int j = 0; j < E; ++j) {
         float g = 0.f;
 #pragma unroll
         for (int r = 0; r < 8; ++r)
-          if (r < k && er_all[r] == j) g = dr_all[r];
+          if (r < k && e[r] == j) g = d[r];
         o[j] = expf(l[j] - m) * inv * (g - c);
       }
     }

@@ -266,7 +266,7 @@ moe_status moe_route_backward(const float* logits, const int32_t* idx, const flo
   DeviceInfo* d = nullptr;
   moe_status ms = device_info(&d);
   if (ms != MOE_OK) return ms;
-  long long blocks = ((long long)T + 7) / 8;
+  long long blocks = ((long long)T + 255) / 256;
   if (blocks > 16LL * d->num_sms) blocks = 16LL * d->num_sms;
   bwd::route_bwd_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(logits, idx, dw, T, E, k,
                                                                                          renorm ? 1 : 0, dlogits);

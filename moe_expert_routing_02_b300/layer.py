@@ -12,11 +12,23 @@ from typing import Optional
 import torch
 
 from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT, MoEStats, moe_combine, moe_dispatch,
-               moe_expert_ffn, moe_expert_ffn_gather, moe_ffn_launches, moe_layer_front, moe_predict, moe_replicate,
-               moe_replicate_predicted, moe_replicate_weights, moe_expert_ffn_slots, moe_route, moe_stats_update,
+               moe_expert_ffn, moe_expert_ffn_gather, moe_ffn_backward, moe_ffn_backward_workspace_bytes,
+               moe_ffn_launches, moe_layer_front, moe_predict, moe_replicate, moe_replicate_predicted,
+               moe_replicate_weights, moe_expert_ffn_slots, moe_route, moe_route_backward, moe_stats_update,
                workspace_bytes)
 
-__all__ = ["MoELayerStep", "ChunkedLayerStep", "HostPipeline"]
+__all__ = ["MoELayerStep", "MoESaved", "ChunkedLayerStep", "HostPipeline"]
+
+
+class MoESaved:
+    """What the backward of one layer keeps from its forward: the routing
+    (idx, w), the dispatch (group offsets, the replica groups' experts or
+    None, perm, inv_perm) and the FFN output y in dispatched order."""
+
+    __slots__ = ("idx", "w", "go", "ge", "perm", "inv", "y")
+
+    def __init__(self, idx, w, go, ge, perm, inv, y):
+        self.idx, self.w, self.go, self.ge, self.perm, self.inv, self.y = idx, w, go, ge, perm, inv, y
 
 
 class MoELayerStep:
@@ -84,12 +96,19 @@ class MoELayerStep:
                                        dtype=torch.uint8, device=d)
         self.ws_ffn = torch.empty(max(workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F), 1024), dtype=torch.uint8,
                                   device=d)
+        self.ws_bwd = None   # allocated by the first backward
+        self.saved = None    # the last run(save=True)
+        self._save = False
         self._cur = 0
 
-    def run(self, it: int, layer: int, logits, x, weights, out, events=None, predict: bool = True):
+    def run(self, it: int, layer: int, logits, x, weights, out, events=None, predict: bool = True,
+            save: bool = False):
         """Enqueue one layer.  weights = (w1, w3 or None, w2).  `events`, if
         given, is a dict stage -> (start, end) torch.cuda.Event recorded
-        around each stage on the current stream."""
+        around each stage on the current stream.  save=True copies what the
+        layer's backward needs into a MoESaved (self.saved), since the step's
+        buffers are reused by the next layer."""
+        self._save = save
         def mark(stage, i):
             if events is not None and stage in events:
                 events[stage][i].record()
@@ -178,8 +197,28 @@ class MoELayerStep:
         mark("combine", 0)
         moe_combine(self.y, self.inv, self.w, out=out)
         mark("combine", 1)
+        if self._save:
+            self.saved = MoESaved(self.idx[self._cur].clone(), self.w.clone(), self.go.clone(),
+                                  None if ge is None else ge.clone(), self.perm.clone(), self.inv.clone(),
+                                  self.y.clone())
         self._cur ^= 1
         return out
+
+    def backward(self, saved: MoESaved, logits, x, weights, dout, grads=None, dlogits=None):
+        """Backward of one layer run with save=True: dout = dL/d(out) [T, H]
+        bf16.  Returns (dx [T, H] bf16, dlogits [T, E] f32, (dW1, dW3 or None,
+        dW2) f32).  Every row of an expert adds into that expert's gradient,
+        whichever replica group served it.  weights = the experts' (w1, w3,
+        w2) [E, ...] (with physical replicas, their first E slots).  `grads`
+        may give (dx, dw, dW1, dW3, dW2) buffers to write into."""
+        w1, w3, w2 = (None if w is None else w[:self.E] for w in weights)
+        if self.ws_bwd is None:
+            n = moe_ffn_backward_workspace_bytes(self.T, self.k, self.E, self.H, self.F)
+            self.ws_bwd = torch.empty(n, dtype=torch.uint8, device=dout.device)
+        dx, dw, dw1, dw3, dw2 = moe_ffn_backward(x, dout, saved.w, saved.y, saved.perm, saved.inv, saved.go, saved.ge,
+                                                 w1, w3, w2, self.act, workspace=self.ws_bwd, out=grads)
+        dl = moe_route_backward(logits, saved.idx, dw, self.renorm, out=dlogits)
+        return dx, dl, (dw1, dw3, dw2)
 
     def launches(self, layer: int, L: int) -> int:
         if self.physical:   # slot map + copy kernel per weight matrix, FFN over 2E-1 slots

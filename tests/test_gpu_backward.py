@@ -242,3 +242,42 @@ def test_backward_rejects_bad_arguments():
         M.moe_ffn_backward(c["x"], c["dout"], dev(c["w"]), c["y"], dev(c["perm"]), dev(c["inv"]), dev(c["go"]),
                            None, c["w1"], None, c["w2"], "swiglu")
     assert M.moe_ffn_backward_workspace_bytes(64, 2, 4, 60, 64) == 0
+
+
+@pytest.mark.parametrize("replicate,physical", [(True, False), (False, False), (True, True)])
+def test_layer_step_backward(replicate, physical):
+    """MoELayerStep.run(save=True) for every layer of a stream, then the
+    layers' backward in reverse order, each against the oracle's gradients of
+    that layer's own routing."""
+    from moe_expert_routing_02_b300.layer import MoELayerStep
+    c = W.config_by_name("tiny")
+    st = M.MoEStats(c.L, c.E, c.window)
+    step = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, st, replicate=replicate, physical_replicas=physical)
+    lgs = [torch.from_numpy(l).cuda() for l in W.make_layer_logits(c, 0)]
+    xs = [W.make_x(c, 0, j, device="cuda") for j in range(c.L)]
+    ws = [W.make_weights(c, j, device="cuda") for j in range(c.L)]
+    if physical:
+        ws = [MoELayerStep.replica_buffers(w) for w in ws]
+    saved = []
+    for j in range(c.L):
+        out = torch.empty((c.T, c.H), dtype=torch.bfloat16, device="cuda")
+        step.run(0, j, lgs[j], xs[j], ws[j], out, save=True)
+        saved.append(step.saved)
+    M.moe_check()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    for j in reversed(range(c.L)):
+        dout = torch.randn((c.T, c.H), generator=g, device="cuda").to(torch.bfloat16)
+        dx, dl, (dw1, _, dw2) = step.backward(saved[j], lgs[j], xs[j], ws[j], dout)
+        M.moe_check()
+        sv = saved[j]
+        cs = dict(T=c.T, E=c.E, k=c.k, H=c.H, F=c.F, act=c.act, w=host(sv.w), go=host(sv.go), perm=host(sv.perm),
+                  inv=host(sv.inv), ge=None if sv.ge is None else host(sv.ge), x=xs[j], dout=dout, y=sv.y,
+                  w1=ws[j][0][:c.E], w3=None, w2=ws[j][2][:c.E])
+        rdx, rdw, rdw1, _, rdw2 = _oracle(cs)
+        assert rel_fro(O.bf16_to_f64(W.bf16_bits(dx)), rdx) <= GRAD_TOL, j
+        assert rel_fro(host(dw1), rdw1) <= GRAD_TOL and rel_fro(host(dw2), rdw2) <= GRAD_TOL, j
+        oi, _ = O.topk_gate(host(lgs[j]), c.k)
+        assert np.array_equal(host(sv.idx), oi)
+        rdl = O.router_backward(host(lgs[j]), oi, rdw)
+        assert np.max(np.abs(host(dl) - rdl)) <= 1e-4 * max(1.0, float(np.max(np.abs(rdw)))), j
