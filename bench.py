@@ -65,6 +65,7 @@ def parse_args(argv=None):
                     help="replica table from the layer's own histogram or from the previous layer's prediction")
     ap.add_argument("--ffn-kernel", choices=["auto", "single", "pair", "fused"], default="auto",
                     help="grouped-GEMM kernel of the expert FFN (default: the library's choice)")
+    ap.add_argument("--no-pdl", action="store_true", help="ordinary launches instead of programmatic dependent launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (tokens of one layer)")
     ap.add_argument("--layers", type=int, default=0,
@@ -292,6 +293,7 @@ def run_ours(args, rank, world, local):
     M.moe_set_option(M.MOE_OPT_FFN_KERNEL, {"auto": M.MOE_FFN_KERNEL_AUTO, "single": M.MOE_FFN_KERNEL_SINGLE,
                                             "pair": M.MOE_FFN_KERNEL_PAIR,
                                             "fused": M.MOE_FFN_KERNEL_FUSED}[args.ffn_kernel])
+    M.moe_set_option(M.MOE_OPT_PDL, 0 if args.no_pdl else 1)
 
     def run_step(it, ev=None):
         for j in range(c.L):
@@ -448,6 +450,7 @@ def run_ours(args, rank, world, local):
                    "launch": "eager" if args.eager else f"CUDA graph per step ({c.window} graphs, one per window slot)",
                    "front": "separate calls" if args.unfused else "moe_layer_front (2 launches)",
                    "ffn_kernel": args.ffn_kernel,
+                   "pdl": not args.no_pdl,
                    "chunks": args.chunks,
                    "replicas": ("physical copies (moe_replicate_weights)" if args.physical_replicas
                                 else "aliasing their expert's weights") + f", table from {args.replicate_from}",

@@ -498,10 +498,17 @@ moe_status moe_dispatch_noalloc(const uint16_t* x, const int32_t* idx, int T, in
  *     runs out after ~2 s; the kernel then releases its resources and
  *     returns, and moe_check reports MOE_ERR_TIMEOUT (that call's output is
  *     incomplete).  The option resets itself after that call.
+ *   MOE_OPT_PDL  1 (default): the route/plan, scatter/copy, grouped FFN and
+ *     combine kernels are launched as programmatic dependents of the
+ *     previous kernel in their stream (CUDA programmatic dependent launch):
+ *     the hardware may start one once every block of the kernel before it
+ *     has exited, and each waits for that kernel's completion (griddepcontrol
+ *     .wait) before touching memory; no kernel releases its dependents early.
+ *     0: ordinary launches.  Results are identical either way.
  * Unknown options or values return MOE_ERR_INVALID.  Not thread-safe against
  * concurrent moe_expert_ffn calls.
  * ------------------------------------------------------------------------- */
-typedef enum { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_FFN_TIMEOUT_SELFTEST = 2 } moe_option;
+typedef enum { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_FFN_TIMEOUT_SELFTEST = 2, MOE_OPT_PDL = 3 } moe_option;
 typedef enum {
     MOE_FFN_KERNEL_AUTO = 0,
     MOE_FFN_KERNEL_SINGLE = 1,

@@ -21,7 +21,7 @@ __all__ = [
     "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_layer_front", "moe_expert_ffn", "moe_expert_ffn_gather", "moe_combine", "moe_predict_decay", "moe_replicate_predicted", "moe_ffn_launches", "moe_replicate_weights", "moe_expert_ffn_slots", "moe_check", "moe_error_word",
     "workspace_bytes", "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_ACT_GELU", "MOE_ACT_SWIGLU",
     "EXPORTED_SYMBOLS", "moe_set_option", "moe_get_option", "MOE_OPT_FFN_KERNEL", "MOE_FFN_KERNEL_AUTO",
-    "MOE_FFN_KERNEL_SINGLE", "MOE_FFN_KERNEL_PAIR", "MOE_FFN_KERNEL_FUSED", "MOE_OPT_FFN_TIMEOUT_SELFTEST",
+    "MOE_FFN_KERNEL_SINGLE", "MOE_FFN_KERNEL_PAIR", "MOE_FFN_KERNEL_FUSED", "MOE_OPT_FFN_TIMEOUT_SELFTEST", "MOE_OPT_PDL",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +30,7 @@ library_path = os.path.join(_HERE, "libmoe.so")
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_WORKSPACE, MOE_ERR_DEVICE = range(7)
 MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
 MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT = 1, 2, 3
-MOE_OPT_FFN_KERNEL, MOE_OPT_FFN_TIMEOUT_SELFTEST = 1, 2
+MOE_OPT_FFN_KERNEL, MOE_OPT_FFN_TIMEOUT_SELFTEST, MOE_OPT_PDL = 1, 2, 3
 MOE_FFN_KERNEL_AUTO, MOE_FFN_KERNEL_SINGLE, MOE_FFN_KERNEL_PAIR, MOE_FFN_KERNEL_FUSED = 0, 1, 2, 3
 
 _P = ctypes.c_void_p

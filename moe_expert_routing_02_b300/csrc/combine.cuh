@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __res
                                                            long long A, uint16_t* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * kWarps;
+  pdl_wait();
   for (long long t = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5; t < T; t += warps) {
     long long slot[K];
     float wr[K];
@@ -79,7 +80,8 @@ static cudaError_t launch(const uint16_t* y, const int32_t* inv_perm, const floa
   const long long A = T * k;
   switch (k) {
 #define MOE_COMBINE_CASE(KK) \
-  case KK: combine_kernel<KK><<<(unsigned)blocks, kThreads, 0, st>>>(y, inv_perm, w, T, H, A, out); break;
+  case KK: return launch_pdl(combine_kernel<KK>, dim3((unsigned)blocks), dim3(kThreads), 0, st, y, inv_perm, w, T, \
+                             H, A, out);
     MOE_COMBINE_CASE(1)
     MOE_COMBINE_CASE(2)
     MOE_COMBINE_CASE(3)

@@ -16,6 +16,35 @@ __device__ unsigned int g_moe_dev_error = 0;
 
 __device__ __forceinline__ void moe_flag_error(unsigned int bits) { atomicOr(&g_moe_dev_error, bits); }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may be
+// started by the hardware once every block of the stream's previous kernel
+// has exited, before that kernel's completion is processed; it calls
+// pdl_wait() before its first access to memory that earlier work writes or
+// reads, which waits for that completion and its memory operations.  Without
+// a programmatic predecessor pdl_wait() returns at once.  No kernel here
+// releases its dependents early (measured: blocks of the next kernel parked
+// beside the running one cost more than the launch latency they hide), so a
+// dependent never shares the GPU with its predecessor's blocks.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+inline int g_moe_pdl = 1;  // host option (moe_set_option(MOE_OPT_PDL, ...))
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = g_moe_pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

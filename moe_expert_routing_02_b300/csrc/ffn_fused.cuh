@@ -150,6 +150,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     ffn_fused_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmW1,
                      const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmA2,
                      const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ FusedParams fp) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Smem& s = *reinterpret_cast<Smem*>(base);

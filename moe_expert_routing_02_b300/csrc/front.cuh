@@ -100,6 +100,7 @@ struct Args {
 
 template <int G, bool VEC>
 __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
+  pdl_wait();
   extern __shared__ uint32_t dsm[];  // cnt[tiles_per_block][E], then cosel[E*E] (small E)
   constexpr int TPW = 32 / G;
   const int E = a.E, k = a.k;
@@ -263,6 +264,7 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const int32_t* _
                                                                 int32_t* __restrict__ inv_perm,
                                                                 const uint16_t* __restrict__ x, int H,
                                                                 uint16_t* __restrict__ xp) {
+  pdl_wait();
   extern __shared__ int32_t sm[];
   int32_t* warp_cnt = sm;                 // [kWarps][E]
   int32_t* run = sm + kWarps * E;         // [E]
@@ -397,11 +399,13 @@ static cudaError_t launch_route_g(const Args& a, bool vec, cudaStream_t st) {
   if (vec) {
     cudaError_t e = ensure_smem_attr(route_count_kernel<G, true>, done_vec);
     if (e != cudaSuccess) return e;
-    route_count_kernel<G, true><<<(unsigned)blocks, kThreads, smem, st>>>(a);
+    e = launch_pdl(route_count_kernel<G, true>, dim3((unsigned)blocks), dim3(kThreads), smem, st, a);
+    if (e != cudaSuccess) return e;
   } else {
     cudaError_t e = ensure_smem_attr(route_count_kernel<G, false>, done_scalar);
     if (e != cudaSuccess) return e;
-    route_count_kernel<G, false><<<(unsigned)blocks, kThreads, smem, st>>>(a);
+    e = launch_pdl(route_count_kernel<G, false>, dim3((unsigned)blocks), dim3(kThreads), smem, st, a);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
@@ -420,10 +424,8 @@ static cudaError_t launch(const Args& a0, const uint16_t* x, int H, uint16_t* xp
   else e = launch_route_g<32>(a, vec, st);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(int32_t) * ((size_t)(kWarps + 1) * a.E + (size_t)a.TT * a.k);
-  scatter_copy_kernel<<<(unsigned)a.ntiles, kThreads, smem, st>>>(a.idx, a.T, a.k, a.E, a.TT, a.tiles_per_block,
-                                                                  a.counts, a.blk_tot, a.info, perm, inv_perm, x, H,
-                                                                  xp);
-  return cudaGetLastError();
+  return launch_pdl(scatter_copy_kernel, dim3((unsigned)a.ntiles), dim3(kThreads), smem, st, a.idx, a.T, a.k, a.E,
+                    a.TT, a.tiles_per_block, a.counts, a.blk_tot, a.info, perm, inv_perm, x, H, xp);
 }
 
 }  // namespace front

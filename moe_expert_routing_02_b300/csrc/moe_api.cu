@@ -728,13 +728,10 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
     cudaError_t e = cudaMemsetAsync(fp.done, 0, (size_t)blocks * 4, st);
     if (e != cudaSuccess) return cuda_at(who, e, "cudaMemsetAsync (block counters)");
     if (cudaError_t fe = fork(); fe != cudaSuccess) return cuda_at(who, fe, "fork of the small-batch chain");
-    if (fi)
-      ffn3::ffn_fused_kernel<ffn::kSwiglu><<<(unsigned)(2 * pairs), ffn2::THREADS, ffn2::kSmemBytes, st>>>(
-          mA1, mW1, mW3, mA2, mW2, fp);
-    else
-      ffn3::ffn_fused_kernel<ffn::kGelu><<<(unsigned)(2 * pairs), ffn2::THREADS, ffn2::kSmemBytes, st>>>(
-          mA1, mW1, mW3, mA2, mW2, fp);
-    return finish(cudaGetLastError(), "fused FFN launch");
+    cudaError_t le = launch_pdl(fi ? ffn3::ffn_fused_kernel<ffn::kSwiglu> : ffn3::ffn_fused_kernel<ffn::kGelu>,
+                                dim3((unsigned)(2 * pairs)), dim3(ffn2::THREADS), ffn2::kSmemBytes, st, mA1, mW1, mW3,
+                                mA2, mW2, fp);
+    return finish(le, "fused FFN launch");
   }
 
   if (use_pair) {
@@ -775,14 +772,14 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
       return (unsigned)(2 * (pairs < 1 ? 1 : pairs));
     };
     if (cudaError_t fe = fork(); fe != cudaSuccess) return cuda_at(who, fe, "fork of the small-batch chain");
-    if (epi1 == ffn::kSwiglu)
-      ffn2::gemm_pair_kernel<ffn::kSwiglu><<<grid_for(p1, 1), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
-    else
-      ffn2::gemm_pair_kernel<ffn::kGelu><<<grid_for(p1, 0), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(epi1 == ffn::kSwiglu ? ffn2::gemm_pair_kernel<ffn::kSwiglu>
+                                                    : ffn2::gemm_pair_kernel<ffn::kGelu>,
+                               dim3(grid_for(p1, epi1 == ffn::kSwiglu ? 1 : 0)), dim3(ffn2::THREADS),
+                               ffn2::kSmemBytes, st, mA1, mW1, mW3, p1);
     if (e != cudaSuccess) return finish(e, "GEMM1 (pair) launch");
-    ffn2::gemm_pair_kernel<ffn::kStore><<<grid_for(p2, 2), ffn2::THREADS, ffn2::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
-    return finish(cudaGetLastError(), "GEMM2 (pair) launch");
+    e = launch_pdl(ffn2::gemm_pair_kernel<ffn::kStore>, dim3(grid_for(p2, 2)), dim3(ffn2::THREADS), ffn2::kSmemBytes,
+                   st, mA2, mW2, mW2, p2);
+    return finish(e, "GEMM2 (pair) launch");
   }
 
   {
@@ -879,6 +876,11 @@ moe_status moe_set_option(int option, int value) {
     g_opt_ffn_kernel = value;
     return MOE_OK;
   }
+  if (option == MOE_OPT_PDL) {
+    if (value != 0 && value != 1) return fail(MOE_ERR_INVALID, "moe_set_option: PDL value must be 0 or 1");
+    g_moe_pdl = value;
+    return MOE_OK;
+  }
   if (option == MOE_OPT_FFN_TIMEOUT_SELFTEST) {
     if (value != 0 && value != 1) return fail(MOE_ERR_INVALID, "moe_set_option: self-test value must be 0 or 1");
     g_opt_ffn_selftest = value;
@@ -891,6 +893,10 @@ moe_status moe_get_option(int option, int* value) {
   if (!value) return fail(MOE_ERR_INVALID, "moe_get_option: null value");
   if (option == MOE_OPT_FFN_KERNEL) {
     *value = g_opt_ffn_kernel;
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_PDL) {
+    *value = g_moe_pdl;
     return MOE_OK;
   }
   if (option == MOE_OPT_FFN_TIMEOUT_SELFTEST) {
