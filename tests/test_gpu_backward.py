@@ -281,3 +281,13 @@ def test_layer_step_backward(replicate, physical):
         assert np.array_equal(host(sv.idx), oi)
         rdl = O.router_backward(host(lgs[j]), oi, rdw)
         assert np.max(np.abs(host(dl) - rdl)) <= 1e-4 * max(1.0, float(np.max(np.abs(rdw)))), j
+
+
+@pytest.mark.parametrize("T,E,k,H,F,act", [
+    (100, 256, 8, 64, 64, "gelu"),      # the largest E and k, most experts with a few rows or none
+    (77, 1, 1, 128, 64, "swiglu"),      # one expert: every row in one unit
+    (1, 4, 2, 64, 128, "gelu"),         # one token
+    (513, 3, 3, 64, 192, "swiglu"),     # k = E: every token chooses every expert
+])
+def test_edge_shapes(T, E, k, H, F, act):
+    _check(_case(T, E, k, H, F, act, seed=T + E))
