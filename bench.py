@@ -738,6 +738,14 @@ def run_backward(args):
     fl_b = backward_flops(c)
     fl_f = (6 if c.act == "swiglu" else 4) * c.A * H * F
     peak = peaks["bf16_tflops_sustained"]
+    # bytes the backward must move at least: the weights read by the GEMM1
+    # recompute, the dA and the dxp GEMMs (W1, W3 twice; W2 once), the fp32
+    # weight gradients written, and its inputs and outputs (x, dout, y, dx)
+    n1 = 2 if c.act == "swiglu" else 1
+    by_b = (2 * n1 + 1) * E * H * F * 2 + (n1 + 1) * E * H * F * 4 + 3 * T * H * 2 + c.A * H * 2
+    t_tensor = fl_b / (peak * 1e12)
+    t_hbm = by_b / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tensor >= t_hbm else "hbm"
     res = {
         "backward": c.name, "T": T, "E": E, "k": k, "H": H, "F": F, "act": c.act,
         "steps": steps, "warmup": warmup,
@@ -745,6 +753,10 @@ def run_backward(args):
         "tokens_per_s": round(T / t_bwd, 1),
         "backward_tflops": round(fl_b / t_bwd / 1e12, 1),
         "backward_frac_of_sustained_bf16": round(fl_b / t_bwd / 1e12 / peak, 3),
+        "roofline": {"bound": bound, "flops": fl_b, "bytes": by_b,
+                     "time_lower_bound_us": round(max(t_tensor, t_hbm) * 1e6, 1),
+                     "frac": round(max(t_tensor, t_hbm) / t_bwd, 3),
+                     "peaks": "sustained bf16 and measured copy rate of MEASURED_PEAKS.json"},
         "us_forward_ffn": round(t_fwd * 1e6, 1),
         "forward_ffn_tflops": round(fl_f / t_fwd / 1e12, 1),
         "backward_over_forward_ffn": round(t_bwd / t_fwd, 2),
