@@ -32,6 +32,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -132,7 +133,8 @@ class ClockSampler:
 
     def __init__(self, device_index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        out_dir = os.environ.get("MOE_BENCH_OUT_DIR", tempfile.gettempdir())
+        self.path = os.path.join(out_dir, f"moe_bench_clocks_rank{device_index}.csv")
         try:
             import torch
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)

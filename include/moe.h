@@ -69,7 +69,7 @@ extern "C" {
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID = 1,      /* bad argument (host-side check)                 */
-    MOE_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run            */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid request the library does not support      */
     MOE_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed           */
     MOE_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out (moe_check) */
     MOE_ERR_WORKSPACE = 5,    /* workspace too small                            */
