@@ -10,6 +10,12 @@
 //   GEMM1: inter[A, F] = act(xp[A, H] . W1[e])            (GeLU)
 //          inter[A, F] = silu(xp . W1[e]) * (xp . W3[e])  (SwiGLU)
 //   GEMM2: y[A, H]     = inter[A, F] . W2[e]
+// The same kernel serves the backward pass (ffn_backward.cu): dgrad GEMMs
+// with the weights as a K-major B operand (kStoreKM), GEMM1 recomputed with
+// an epilogue that writes the activation and its derivative factors
+// (kBwdGelu, kBwdSwiglu), and dA = dY W2^T multiplied by those factors in its
+// epilogue (kStoreKMMul, kStoreKMMul2); see the Epi modes below.
+//
 // Rows are grouped by expert (or replica group); group sizes live only on the
 // device, so every CTA reads the group offsets, folds adjacent groups of the
 // same expert into one row range ("unit", build_units) and enumerates the
@@ -115,7 +121,9 @@ struct Params {
   int a_src_div;
   int a_src_rows;  // rows of that tensor (T)
   // kStoreKM: k-blocks below k_split read the first weight tensor, the rest
-  // the second (at k-block kb - k_split).
+  // the second (at k-block kb - k_split).  kStoreKMMul / kStoreKMMul2: K/BK
+  // (kStoreKMMul passes the factor tensor, 16-column x 32-row boxes, as the
+  // second tensor map).
   int k_split;
   // kBwdGelu / kBwdSwiglu: out = activation [A_rows, N_out]; out2 = the
   // factors, [A_rows, N_out] (GeLU) or [A_rows, 2 N_out] (SwiGLU).
