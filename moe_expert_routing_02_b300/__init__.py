@@ -71,7 +71,7 @@ _SIGS = {
     "moe_get_option": (_I, [_I, ctypes.POINTER(_I)]),
     "moe_ffn_backward_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_ffn_backward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P,
-                              _P, _SZ, _P]),
+                              _I, _P, _SZ, _P]),
     "moe_route_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -542,14 +542,18 @@ def moe_ffn_launches(A: int, E: int, H: int, F: int, act: str = "gelu", small_gr
                                       int(bool(gather))))
 
 
+MOE_BWD_ACCUMULATE_WGRAD = 1
+
+
 def moe_ffn_backward(x, dout, w, y, perm, inv_perm, group_offsets, group_expert, w1, w3, w2, act: str = "gelu",
-                     workspace=None, stream=None, out=None):
+                     workspace=None, stream=None, out=None, accumulate: bool = False):
     """Backward of dispatch -> expert FFN -> combine for one routing.
     x, dout bf16 [T, H]; w f32 [T, k]; y bf16 [T*k, H] (the forward FFN
     output, or None: no dw); perm, inv_perm, group_offsets, group_expert as
     written by the dispatch.  Returns (dx bf16 [T, H], dw f32 [T, k] or None,
     dw1 f32 [E, H, F], dw3 f32 [E, H, F] or None, dw2 f32 [E, F, H]).
-    `out` may give those five tensors to write into."""
+    `out` may give those five tensors to write into; accumulate=True adds
+    this batch's weight gradients to what out's dw1, dw3, dw2 hold."""
     torch = _torch()
     _dev(x, torch.bfloat16, "x", 2)
     _dev(dout, torch.bfloat16, "dout", 2)
@@ -572,6 +576,8 @@ def moe_ffn_backward(x, dout, w, y, perm, inv_perm, group_offsets, group_expert,
         raise ValueError("shapes: x, dout [T,H]; w [T,k]; w1/w3 [E,H,F]; w2 [E,F,H]")
     act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
     dev = x.device
+    if accumulate and out is None:
+        raise ValueError("accumulate=True needs `out`: the gradients to add to")
     if out is None:
         f32 = dict(dtype=torch.float32, device=dev)
         out = (torch.empty((T, H), dtype=torch.bfloat16, device=dev),
@@ -585,7 +591,8 @@ def moe_ffn_backward(x, dout, w, y, perm, inv_perm, group_offsets, group_expert,
         workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=dev)
     _check(lib().moe_ffn_backward(_ptr(x), _ptr(dout), _ptr(w), _ptr(y), _ptr(perm), _ptr(inv_perm), T, k,
                                   _ptr(group_offsets), _ptr(group_expert), E, _ptr(w1), _ptr(w3), _ptr(w2), H, F,
-                                  act_id, _ptr(dx), _ptr(dw), _ptr(dw1), _ptr(dw3), _ptr(dw2), _ptr(workspace),
+                                  act_id, _ptr(dx), _ptr(dw), _ptr(dw1), _ptr(dw3), _ptr(dw2),
+                                  MOE_BWD_ACCUMULATE_WGRAD if accumulate else 0, _ptr(workspace),
                                   workspace.numel(), _stream(stream)), "moe_ffn_backward")
     return dx, dw, dw1, dw3, dw2
 

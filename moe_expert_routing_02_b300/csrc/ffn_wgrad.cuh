@@ -6,7 +6,7 @@
 // there.  On one GPU that reduction is the sum over every row routed to the
 // expert, whichever replica group served the row:
 //
-//   dW[e] = L_e^T R_e    [M_out, N_out], fp32,
+//   dW[e] = L_e^T R_e    [M_out, N_out], fp32   (or dW[e] += ..., accumulate),
 //
 // where L_e [rows_e, M_out] and R_e [rows_e, N_out] are expert e's rows of two
 // row-major bf16 activation tensors (the reduction runs over rows).  The rows
@@ -67,6 +67,7 @@ struct WParams {
   int jobs;
   int tiles_per_expert;  // sum over jobs of m_tiles * n_tiles
   long long rows;        // rows of the operand tensors
+  int accumulate;        // 1: dW += result (gradient accumulation), 0: dW = result
   Job job[MAX_JOBS];
 };
 
@@ -111,9 +112,10 @@ __device__ __forceinline__ WTile wdecode(const WParams& p, int tile) {
 // Through 1 KB of shared memory, 8 rows at a time: chunk j (16 bytes) of row
 // r sits at slot (j + r) mod 8, so the writes (8 lanes, one row each) and the
 // reads (8 lanes per row, one 128-byte row segment per 8 lanes) are free of
-// bank conflicts.
+// bank conflicts.  accumulate: each 16-byte chunk is added to what the output
+// holds (read with the same coalesced pattern) instead of replacing it.
 __device__ __forceinline__ void store_rows32_f32(uint8_t* stg, float* out, size_t ld, int rows_valid,
-                                                 const uint32_t (&v)[32], int lane) {
+                                                 const uint32_t (&v)[32], int lane, bool accumulate) {
 #pragma unroll
   for (int h = 0; h < 4; ++h) {
     __syncwarp();
@@ -129,9 +131,17 @@ __device__ __forceinline__ void store_rows32_f32(uint8_t* stg, float* out, size_
     for (int pass = 0; pass < 2; ++pass) {
       const int idx = pass * 32 + lane;
       const int r = idx >> 3, c = idx & 7;
-      const uint4 q = *reinterpret_cast<const uint4*>(stg + r * 128 + (((c + r) & 7) << 4));
+      uint4 q = *reinterpret_cast<const uint4*>(stg + r * 128 + (((c + r) & 7) << 4));
       const int row = h * 8 + r;
-      if (row < rows_valid) st_v4(out + (size_t)row * ld + c * 4, q);
+      if (row < rows_valid) {
+        float* dst = out + (size_t)row * ld + c * 4;
+        if (accumulate) {
+          const float4 o = *reinterpret_cast<const float4*>(dst);
+          q = make_uint4(__float_as_uint(o.x + __uint_as_float(q.x)), __float_as_uint(o.y + __uint_as_float(q.y)),
+                         __float_as_uint(o.z + __uint_as_float(q.z)), __float_as_uint(o.w + __uint_as_float(q.w)));
+        }
+        st_v4(dst, q);
+      }
     }
   }
 }
@@ -300,7 +310,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           __syncwarp();
           tmem_ld32(tb + c, raw);
         }
-        if (col < J.N_out && wrows > 0) store_rows32_f32(s.stg[warp - 2], obase + col, (size_t)J.N_out, wrows, raw, lane);
+        if (col < J.N_out && wrows > 0)
+          store_rows32_f32(s.stg[warp - 2], obase + col, (size_t)J.N_out, wrows, raw, lane, p.accumulate != 0);
       }
       tc_fence_before();
       __syncwarp();

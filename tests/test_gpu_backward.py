@@ -291,3 +291,59 @@ def test_layer_step_backward(replicate, physical):
 ])
 def test_edge_shapes(T, E, k, H, F, act):
     _check(_case(T, E, k, H, F, act, seed=T + E))
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_accumulate_adds_to_the_weight_gradients(act):
+    """MOE_BWD_ACCUMULATE_WGRAD: a second call adds its weight gradients to the
+    first's (the wgrad is deterministic, so the sum is exactly twice one
+    call's); dx and dw are written, not added."""
+    c = _case(300, 6, 2, 128, 192, act, seed=21, alpha=1.3, empty=(2,))
+    one = _gpu(c)
+    M.moe_check()
+    out = tuple(None if t is None else t.clone() for t in one)
+    got = M.moe_ffn_backward(c["x"], c["dout"], dev(c["w"]), c["y"], dev(c["perm"]), dev(c["inv"]), dev(c["go"]),
+                             None, c["w1"], c["w3"], c["w2"], act, out=out, accumulate=True)
+    M.moe_check()
+    assert torch.equal(got[0], one[0]) and torch.equal(got[1], one[1])
+    for a, b in zip(got[2:], one[2:]):
+        if b is not None:
+            assert torch.equal(a, 2 * b)
+    with pytest.raises(ValueError):
+        M.moe_ffn_backward(c["x"], c["dout"], dev(c["w"]), c["y"], dev(c["perm"]), dev(c["inv"]), dev(c["go"]),
+                           None, c["w1"], c["w3"], c["w2"], act, accumulate=True)
+
+
+def test_backward_in_a_cuda_graph():
+    """The backward (eight launches, no host synchronisation) captured in a
+    CUDA graph and replayed gives the eager results bit for bit."""
+    c = _case(2048, 16, 2, 1024, 2048, "gelu", seed=22, alpha=1.2)
+    eager = _gpu(c)
+    lg = dev(c["logits"])
+    idx = dev(c["idx"].astype(np.int32))
+    dl_eager = M.moe_route_backward(lg, idx, eager[1])
+    M.moe_check()
+    T, k, E, H, F = c["T"], c["k"], c["E"], c["H"], c["F"]
+    ws = torch.empty(M.moe_ffn_backward_workspace_bytes(T, k, E, H, F), dtype=torch.uint8, device="cuda")
+    f32 = dict(dtype=torch.float32, device="cuda")
+    out = (torch.empty((T, H), dtype=torch.bfloat16, device="cuda"), torch.empty((T, k), **f32),
+           torch.empty((E, H, F), **f32), None, torch.empty((E, F, H), **f32))
+    dl = torch.empty((T, E), **f32)
+    args = [dev(a) for a in (c["w"], c["perm"], c["inv"], c["go"])]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            M.moe_ffn_backward(c["x"], c["dout"], args[0], c["y"], args[1], args[2], args[3], None, c["w1"], None,
+                               c["w2"], "gelu", workspace=ws, out=out)
+            M.moe_route_backward(lg, idx, out[1], out=dl)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    M.moe_check()
+    for a, b in zip(out, eager):
+        if b is not None:
+            assert torch.equal(a, b)
+    assert torch.equal(dl, dl_eager)
