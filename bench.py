@@ -67,6 +67,8 @@ def parse_args(argv=None):
     ap.add_argument("--ffn-kernel", choices=["auto", "single", "pair", "fused"], default="auto",
                     help="grouped-GEMM kernel of the expert FFN (default: the library's choice)")
     ap.add_argument("--no-pdl", action="store_true", help="ordinary launches instead of programmatic dependent launch")
+    ap.add_argument("--small-threshold", type=int, default=64,
+                    help="experts with fewer rows take the small-batch FFN kernel (0: none, no side-stream launches)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (tokens of one layer)")
     ap.add_argument("--layers", type=int, default=0,
@@ -283,7 +285,8 @@ def run_ours(args, rank, world, local):
     stats = M.MoEStats(c.L, c.E, c.window)
     step = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, stats=stats, replicate=True, fused=not args.unfused,
                         gather=args.gather, replicate_from=args.replicate_from,
-                        physical_replicas=args.physical_replicas, device=dev)
+                        physical_replicas=args.physical_replicas, small_group_threshold=args.small_threshold,
+                        device=dev)
     if args.physical_replicas:
         weights = [MoELayerStep.replica_buffers(w) for w in weights]
     if args.chunks > 1:
@@ -453,6 +456,7 @@ def run_ours(args, rank, world, local):
                    "front": "separate calls" if args.unfused else "moe_layer_front (2 launches)",
                    "ffn_kernel": args.ffn_kernel,
                    "pdl": not args.no_pdl,
+                   "small_group_threshold": args.small_threshold,
                    "chunks": args.chunks,
                    "replicas": ("physical copies (moe_replicate_weights)" if args.physical_replicas
                                 else "aliasing their expert's weights") + f", table from {args.replicate_from}",
