@@ -245,7 +245,6 @@ __global__ void __launch_bounds__(256)
         src[r] = pr;
       }
     }
-#pragma unroll 2
     for (int c = lane; c < H8; c += 32) {
       float acc[8];
 #pragma unroll

@@ -141,7 +141,7 @@ struct Smem {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
-  uint64_t fbar[EPI_WARPS][2];  // kStoreKMMul: per-warp factor buffers
+  uint64_t fbar[EPI_WARPS][3];  // kStoreKMMul: per-warp factor buffers
   uint32_t tmem_base;
   uint32_t abort_flag;
   int32_t total_tiles;
@@ -556,8 +556,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&s.empty[i], 1);
     }
     for (int w = 0; w < EPI_WARPS; ++w) {
-      mbar_init(&s.fbar[w][0], 1);
-      mbar_init(&s.fbar[w][1], 1);
+      for (int b = 0; b < 3; ++b) mbar_init(&s.fbar[w][b], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
@@ -582,10 +581,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = s.tmem_base;
   const int total = s.total_tiles;
   const int kblocks = p.K / BK;
-  // kStoreKMMul keeps the last stage's B buffer for its epilogue's factor
-  // tiles (16 warps x two 1 KB buffers) and runs the operand ring on the rest
+  // kStoreKMMul keeps the last stage's buffers for its epilogue's factor
+  // tiles (16 warps x three 1 KB buffers: two in the B buffer, one in the A
+  // buffer) and runs the operand ring on the rest
   constexpr int NST = EPI == kStoreKMMul ? STAGES - 1 : STAGES;
-  static_assert(EPI_WARPS * 2 * 1024 <= B_BYTES, "factor buffers exceed one B stage");
+  static_assert(EPI_WARPS * 2 * 1024 <= B_BYTES && EPI_WARPS * 1024 <= A_BYTES, "factor buffers exceed a stage");
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -711,9 +711,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc = 0, acc_phase = 0;
     // kStoreKMMul: this warp's two factor buffers, their next phases and
     // whether a copy into them is outstanding
-    uint8_t* fbuf = s.b[STAGES - 1] + (warp - 2) * 2048;
-    uint32_t fph[2] = {0u, 0u};
-    bool fpend[2] = {false, false};
+    uint8_t* fb3[3] = {s.b[STAGES - 1] + (warp - 2) * 2048, s.b[STAGES - 1] + (warp - 2) * 2048 + 1024,
+                       s.a[STAGES - 1] + (warp - 2) * 1024};
+    uint32_t fph[3] = {0u, 0u, 0u};
+    bool fpend[3] = {false, false, false};
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode(s, U, tile);
       // Multiply epilogues: the factor rows of the warp's 64 columns are
@@ -732,12 +733,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint4 pre[kPair ? kMulNP : 1][2];
       uint4 preu[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
       if (EPI == kStoreKMMul) {
+        // pieces 0, 1, 2 into buffers 0, 1, 2; piece 3 follows into buffer 0
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          if (mcol0 + 16 * q < p.N_out) {
+        if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // last tile's reads first
+        for (int q = 0; q < 3; ++q) {
+          if (q < kMulNP && mcol0 + 16 * q < p.N_out) {
             if (lane == 0) {
               mbar_arrive_expect_tx(&s.fbar[warp - 2][q], 1024);
-              tma_load_2d(fbuf + q * 1024, &tmB1, &s.fbar[warp - 2][q], mcol0 + 16 * q, mrow);
+              tma_load_2d(fb3[q], &tmB1, &s.fbar[warp - 2][q], mcol0 + 16 * q, mrow);
             }
             fpend[q] = true;
           }
@@ -758,43 +761,64 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int wrows = t.rows - quarter * 32;
       uint16_t* wbase = p.out + (size_t)(t.row0 + quarter * 32) * p.N_out;
       const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      if (kMul) {
-        // dz = dA * gelu'(z), or dg = dA * u silu'(g) and du = dA * silu(g),
-        // over the factors in place; 16-column pieces
+      if (EPI == kStoreKMMul) {
+        // dz = dA * gelu'(z) over the factors in place; 16-column pieces,
+        // factor pieces from the TMA buffers, the next piece's TMEM load
+        // issued before this piece's stores
         constexpr int NP = kMulNP;
         bool ok = true;
+        uint32_t raw[16];
+        __syncwarp();
+        if (mcol0 < p.N_out) {
+          tmem_ld16_issue(tb + slice * kMulW, raw);
+          tmem_wait16(raw);
+        }
 #pragma unroll
         for (int pc = 0; pc < NP; ++pc) {
           const int col = mcol0 + pc * 16;
           if (col >= p.N_out) break;  // warp-uniform; later pieces lie further right
-          uint32_t fv[8], fu[8];
-          if (EPI == kStoreKMMul) {
-            const int b = pc & 1;
-            if (!__all_sync(0xffffffffu, wait_phase(&s.fbar[warp - 2][b], fph[b], &s.abort_flag))) {
-              ok = false;
-              break;
-            }
-            fph[b] ^= 1u;
-            fpend[b] = false;
-            const uint4 q0 = *reinterpret_cast<const uint4*>(fbuf + b * 1024 + lane * 32);
-            const uint4 q1 = *reinterpret_cast<const uint4*>(fbuf + b * 1024 + lane * 32 + 16);
-            fv[0] = q0.x; fv[1] = q0.y; fv[2] = q0.z; fv[3] = q0.w;
-            fv[4] = q1.x; fv[5] = q1.y; fv[6] = q1.z; fv[7] = q1.w;
-            __syncwarp();
-            if (pc + 2 < NP && col + 32 < p.N_out) {
-              if (lane == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // reads above, then the copy
-                mbar_arrive_expect_tx(&s.fbar[warp - 2][b], 1024);
-                tma_load_2d(fbuf + b * 1024, &tmB1, &s.fbar[warp - 2][b], col + 32, mrow);
-              }
-              fpend[b] = true;
-            }
-          } else {
-            transpose_rows16(s.stg[warp - 2], pre[kPair ? pc : 0], lane, fv);
-            transpose_rows16(s.stg[warp - 2], preu, lane, fu);
-            if (pc + 1 < NP && col + 16 < p.N_out)
-              prefetch_rows16(mbase + p.N_out + col + 16, mld, wrows, lane, preu);
+          const int b = pc % 3;
+          if (!__all_sync(0xffffffffu, wait_phase(&s.fbar[warp - 2][b], fph[b], &s.abort_flag))) {
+            ok = false;
+            break;
           }
+          fph[b] ^= 1u;
+          fpend[b] = false;
+          const uint4 q0 = *reinterpret_cast<const uint4*>(fb3[b] + lane * 32);
+          const uint4 q1 = *reinterpret_cast<const uint4*>(fb3[b] + lane * 32 + 16);
+          const uint32_t fv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          __syncwarp();
+          if (pc + 3 < NP && col + 48 < p.N_out) {
+            if (lane == 0) {
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // reads above, then the copy
+              mbar_arrive_expect_tx(&s.fbar[warp - 2][b], 1024);
+              tma_load_2d(fb3[b], &tmB1, &s.fbar[warp - 2][b], col + 48, mrow);
+            }
+            fpend[b] = true;
+          }
+          uint32_t o[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            o[i] = f2_to_bf16x2(f2_mul(f2_pack(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),
+                                       bf16x2_to_f2(fv[i])));
+          const bool next = pc + 1 < NP && col + 16 < p.N_out;  // warp-uniform
+          if (next) tmem_ld16_issue(tb + slice * kMulW + (pc + 1) * 16, raw);
+          store_rows16(s.stg[warp - 2], mbase + col, mld, wrows, o, lane);
+          if (next) tmem_wait16(raw);
+        }
+        if (!ok) break;
+      } else if (kPair) {
+        // dg = dA * u silu'(g), du = dA * silu(g) over the factors in place
+        constexpr int NP = kMulNP;
+#pragma unroll
+        for (int pc = 0; pc < NP; ++pc) {
+          const int col = mcol0 + pc * 16;
+          if (col >= p.N_out) break;  // warp-uniform
+          uint32_t fv[8], fu[8];
+          transpose_rows16(s.stg[warp - 2], pre[pc], lane, fv);
+          transpose_rows16(s.stg[warp - 2], preu, lane, fu);
+          if (pc + 1 < NP && col + 16 < p.N_out)
+            prefetch_rows16(mbase + p.N_out + col + 16, mld, wrows, lane, preu);
           __syncwarp();
           uint32_t raw[16];
           tmem_ld16(tb + slice * kMulW + pc * 16, raw);
@@ -804,23 +828,53 @@ __global__ void __launch_bounds__(THREADS, 1)
             o[i] = f2_to_bf16x2(f2_mul(f2_pack(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),
                                        bf16x2_to_f2(fv[i])));
           store_rows16(s.stg[warp - 2], mbase + col, mld, wrows, o, lane);
-          if (kPair) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[i] = f2_to_bf16x2(f2_mul(f2_pack(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),
-                                         bf16x2_to_f2(fu[i])));
-            store_rows16(s.stg[warp - 2], mbase + p.N_out + col, mld, wrows, o, lane);
-          }
+          for (int i = 0; i < 8; ++i)
+            o[i] = f2_to_bf16x2(f2_mul(f2_pack(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])),
+                                       bf16x2_to_f2(fu[i])));
+          store_rows16(s.stg[warp - 2], mbase + p.N_out + col, mld, wrows, o, lane);
         }
-        if (!ok) break;
-      } else if (EPI == kBwdSwiglu || EPI == kBwdGelu) {
-        // 16-column pieces.  GeLU: a = gelu(z), factor gelu'(z).  SwiGLU:
-        // a = silu(g) u, factors u silu'(g) and silu(g), with silu(g) = g s,
-        // silu'(g) = s (1 + g (1 - s)), s = 1 / (1 + exp(-g)).
-        constexpr int W = EPI == kBwdSwiglu ? (BN / 2) / EPI_SLICES : BN / EPI_SLICES;
+      } else if (EPI == kBwdGelu) {
+        // 16-column pieces: a = gelu(z) and the factor gelu'(z).  The next
+        // piece's TMEM load is issued once this piece's values are packed, so
+        // that it completes under this piece's stores.
+        constexpr int W = BN / EPI_SLICES;
         constexpr int NP = W / 16;
-        const int col0 = EPI == kBwdSwiglu ? t.nt * (BN / 2) + slice * W : t.nt * BN + slice * W;
-        const size_t ld2 = (EPI == kBwdSwiglu ? 2 : 1) * (size_t)p.N_out;
+        const int col0 = t.nt * BN + slice * W;
+        uint16_t* w2base = p.out2 + (size_t)(t.row0 + quarter * 32) * p.N_out;
+        uint32_t raw[16];
+        __syncwarp();
+        if (col0 < p.N_out) {
+          tmem_ld16_issue(tb + slice * W, raw);
+          tmem_wait16(raw);
+        }
+#pragma unroll 1
+        for (int pc = 0; pc < NP; ++pc) {
+          const int col = col0 + pc * 16;
+          if (col >= p.N_out) break;  // warp-uniform; later pieces lie further right
+          uint32_t pa[8], pd[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            f32x2 a, g;
+            gelu_and_grad2(f2_pack(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])), a, g);
+            pa[i] = f2_to_bf16x2(a);
+            pd[i] = f2_to_bf16x2(g);
+          }
+          const bool next = pc + 1 < NP && col + 16 < p.N_out;  // warp-uniform
+          __syncwarp();
+          if (next) tmem_ld16_issue(tb + slice * W + (pc + 1) * 16, raw);
+          store_rows16(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pa, lane);
+          store_rows16(s.stg[warp - 2], w2base + col, (size_t)p.N_out, wrows, pd, lane);
+          if (next) tmem_wait16(raw);
+        }
+      } else if (EPI == kBwdSwiglu) {
+        // 16-column pieces: a = silu(g) u and the factors u silu'(g) and
+        // silu(g), with silu(g) = g s, silu'(g) = s (1 + g (1 - s)),
+        // s = 1 / (1 + exp(-g)).
+        constexpr int W = (BN / 2) / EPI_SLICES;
+        constexpr int NP = W / 16;
+        const int col0 = t.nt * (BN / 2) + slice * W;
+        const size_t ld2 = 2 * (size_t)p.N_out;
         uint16_t* w2base = p.out2 + (size_t)(t.row0 + quarter * 32) * ld2;
 #pragma unroll 1
         for (int pc = 0; pc < NP; ++pc) {
@@ -828,41 +882,26 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (col >= p.N_out) break;  // warp-uniform
           const int c = slice * W + pc * 16;  // TMEM column
           __syncwarp();
-          if (EPI == kBwdGelu) {
-            uint32_t raw[16];
-            tmem_ld16(tb + c, raw);
-            uint32_t pa[8], pd[8];
+          uint32_t gr[16], ur[16];
+          tmem_ld16x2(tb + c, tb + BN / 2 + c, gr, ur);
+          uint32_t pa[8], pg[8], pu[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              f32x2 a, g;
-              gelu_and_grad2(f2_pack(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1])), a, g);
-              pa[i] = f2_to_bf16x2(a);
-              pd[i] = f2_to_bf16x2(g);
-            }
-            store_rows16(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pa, lane);
-            store_rows16(s.stg[warp - 2], w2base + col, ld2, wrows, pd, lane);
-          } else {
-            uint32_t gr[16], ur[16];
-            tmem_ld16x2(tb + c, tb + BN / 2 + c, gr, ur);
-            uint32_t pa[8], pg[8], pu[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float g0 = __uint_as_float(gr[2 * i]), g1 = __uint_as_float(gr[2 * i + 1]);
-              const f32x2 g = f2_pack(g0, g1);
-              const f32x2 u = f2_pack(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1]));
-              float e0, e1;
-              f2_unpack(f2_add(f2_pack(__expf(-g0), __expf(-g1)), f2_splat(1.0f)), e0, e1);
-              const f32x2 sg = f2_pack(__fdividef(1.0f, e0), __fdividef(1.0f, e1));
-              const f32x2 silu = f2_mul(g, sg);
-              const f32x2 oms = f2_add(f2_splat(1.0f), f2_mul(sg, f2_splat(-1.0f)));
-              pa[i] = f2_to_bf16x2(f2_mul(silu, u));
-              pg[i] = f2_to_bf16x2(f2_mul(f2_mul(u, sg), f2_fma(g, oms, f2_splat(1.0f))));
-              pu[i] = f2_to_bf16x2(silu);
-            }
-            store_rows16(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pa, lane);
-            store_rows16(s.stg[warp - 2], w2base + col, ld2, wrows, pg, lane);
-            store_rows16(s.stg[warp - 2], w2base + p.N_out + col, ld2, wrows, pu, lane);
+          for (int i = 0; i < 8; ++i) {
+            const float g0 = __uint_as_float(gr[2 * i]), g1 = __uint_as_float(gr[2 * i + 1]);
+            const f32x2 g = f2_pack(g0, g1);
+            const f32x2 u = f2_pack(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1]));
+            float e0, e1;
+            f2_unpack(f2_add(f2_pack(__expf(-g0), __expf(-g1)), f2_splat(1.0f)), e0, e1);
+            const f32x2 sg = f2_pack(__fdividef(1.0f, e0), __fdividef(1.0f, e1));
+            const f32x2 silu = f2_mul(g, sg);
+            const f32x2 oms = f2_add(f2_splat(1.0f), f2_mul(sg, f2_splat(-1.0f)));
+            pa[i] = f2_to_bf16x2(f2_mul(silu, u));
+            pg[i] = f2_to_bf16x2(f2_mul(f2_mul(u, sg), f2_fma(g, oms, f2_splat(1.0f))));
+            pu[i] = f2_to_bf16x2(silu);
           }
+          store_rows16(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pa, lane);
+          store_rows16(s.stg[warp - 2], w2base + col, ld2, wrows, pg, lane);
+          store_rows16(s.stg[warp - 2], w2base + p.N_out + col, ld2, wrows, pu, lane);
         }
       } else if (EPI == kSwiglu) {
         constexpr int W = (BN / 2) / EPI_SLICES;   // output columns per warp
@@ -918,7 +957,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     // factor copies still in flight (a role aborted) land before the exit
     if (EPI == kStoreKMMul && lane == 0) {
-      for (int b = 0; b < 2; ++b)
+      for (int b = 0; b < 3; ++b)
         if (fpend[b]) wait_phase(&s.fbar[warp - 2][b], fph[b], &s.abort_flag, true);
     }
   }
