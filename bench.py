@@ -81,6 +81,7 @@ def parse_args(argv=None):
                     help="prediction quality and prediction-driven replication over the workload's iterations "
                          "(one JSON line; not the bench line)")
     ap.add_argument("--quality-iters", type=int, default=200)
+    ap.add_argument("--wgrad-bf16", action="store_true", help="--backward: weight gradients written in bf16")
     ap.add_argument("--backward", action="store_true",
                     help="time the layer's backward (moe_ffn_backward + moe_route_backward) instead; one JSON line")
     ap.add_argument("--sweep-min-log2", type=int, default=14)
@@ -712,14 +713,17 @@ def run_backward(args):
     g.manual_seed(1234)
     dout = torch.randn((T, H), generator=g, device=dev).to(torch.bfloat16)
     f32 = dict(dtype=torch.float32, device=dev)
+    gdt = torch.bfloat16 if args.wgrad_bf16 else torch.float32
     outs = (torch.empty((T, H), dtype=torch.bfloat16, device=dev), torch.empty((T, k), **f32),
-            torch.empty((E, H, F), **f32), torch.empty((E, H, F), **f32) if c.act == "swiglu" else None,
-            torch.empty((E, F, H), **f32))
+            torch.empty((E, H, F), dtype=gdt, device=dev),
+            torch.empty((E, H, F), dtype=gdt, device=dev) if c.act == "swiglu" else None,
+            torch.empty((E, F, H), dtype=gdt, device=dev))
     ws = torch.empty(M.moe_ffn_backward_workspace_bytes(T, k, E, H, F), dtype=torch.uint8, device=dev)
     dl = torch.empty((T, E), **f32)
 
     def bwd():
-        M.moe_ffn_backward(x, dout, w, y, perm, inv, go, None, w1, w3, w2, c.act, workspace=ws, out=outs)
+        M.moe_ffn_backward(x, dout, w, y, perm, inv, go, None, w1, w3, w2, c.act, workspace=ws, out=outs,
+                           wgrad_bf16=args.wgrad_bf16)
         M.moe_route_backward(lg, idx, outs[1], out=dl)
 
     def timed(fn, steps, warmup):
@@ -748,7 +752,8 @@ def run_backward(args):
     # recompute, the dA and the dxp GEMMs (W1, W3 twice; W2 once), the fp32
     # weight gradients written, and its inputs and outputs (x, dout, y, dx)
     n1 = 2 if c.act == "swiglu" else 1
-    by_b = (2 * n1 + 1) * E * H * F * 2 + (n1 + 1) * E * H * F * 4 + 3 * T * H * 2 + c.A * H * 2
+    gbytes = 2 if args.wgrad_bf16 else 4
+    by_b = (2 * n1 + 1) * E * H * F * 2 + (n1 + 1) * E * H * F * gbytes + 3 * T * H * 2 + c.A * H * 2
     t_tensor = fl_b / (peak * 1e12)
     t_hbm = by_b / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if t_tensor >= t_hbm else "hbm"
@@ -767,6 +772,7 @@ def run_backward(args):
         "forward_ffn_tflops": round(fl_f / t_fwd / 1e12, 1),
         "backward_over_forward_ffn": round(t_bwd / t_fwd, 2),
         "gpu_launches_per_backward": 8,
+        "weight_gradients": "bf16" if args.wgrad_bf16 else "fp32",
         "peak": {"bf16_tflops_sustained": peak, "source": peaks["source"]},
         "clocks": clocks,
         "data": "synthetic: the config's logits, x and weights; dout ~ N(0,1) bf16",

@@ -401,12 +401,15 @@ moe_status moe_expert_ffn_slots(const uint16_t* xp, const int32_t* group_offsets
  *   w1, w3, w2   expert weights as in moe_expert_ffn (w3 NULL for GeLU)
  *   dx           bf16 [T, H] out
  *   dw           f32 [T, k] out (when y is given)
- *   dw1, dw3, dw2  f32 [E, H, F], [E, H, F] (SwiGLU; else NULL), [E, F, H] out:
- *                every expert's gradient is written (0 for experts without rows),
- *                or added to what they hold with MOE_BWD_ACCUMULATE_WGRAD
- *   flags        0 or MOE_BWD_ACCUMULATE_WGRAD (dW += this batch's gradient:
- *                gradient accumulation over micro-batches; dx and dw are
- *                always written)
+ *   dw1, dw3, dw2  [E, H, F], [E, H, F] (SwiGLU; else NULL), [E, F, H] out, f32
+ *                (bf16 bit patterns with MOE_BWD_WGRAD_BF16): every expert's
+ *                gradient is written (0 for experts without rows), or added to
+ *                what they hold with MOE_BWD_ACCUMULATE_WGRAD
+ *   flags        0 or a combination of MOE_BWD_ACCUMULATE_WGRAD (dW += this
+ *                batch's gradient: gradient accumulation over micro-batches)
+ *                and MOE_BWD_WGRAD_BF16 (the fp32 results rounded once to bf16:
+ *                half the bytes written; not with accumulation); dx and dw are
+ *                always written
  *   workspace    ws_bytes >= moe_ffn_backward_workspace_bytes(T, k, E, H, F),
  *                256-byte aligned; holds the padded intermediates (each
  *                expert's rows start at a multiple of 64, zero-padded).
@@ -416,12 +419,13 @@ moe_status moe_expert_ffn_slots(const uint16_t* xp, const int32_t* group_offsets
  * device error word.
  * ------------------------------------------------------------------------- */
 #define MOE_BWD_ACCUMULATE_WGRAD 1
+#define MOE_BWD_WGRAD_BF16 2
 size_t moe_ffn_backward_workspace_bytes(int T, int k, int E, int H, int F);
 moe_status moe_ffn_backward(const uint16_t* x, const uint16_t* dout, const float* w, const uint16_t* y,
                             const int32_t* perm, const int32_t* inv_perm, int T, int k,
                             const int32_t* group_offsets, const int32_t* group_expert, int E,
                             const uint16_t* w1, const uint16_t* w3, const uint16_t* w2, int H, int F,
-                            moe_act act, uint16_t* dx, float* dw, float* dw1, float* dw3, float* dw2,
+                            moe_act act, uint16_t* dx, float* dw, void* dw1, void* dw3, void* dw2,
                             int flags, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------

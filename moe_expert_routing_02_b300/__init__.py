@@ -543,17 +543,19 @@ def moe_ffn_launches(A: int, E: int, H: int, F: int, act: str = "gelu", small_gr
 
 
 MOE_BWD_ACCUMULATE_WGRAD = 1
+MOE_BWD_WGRAD_BF16 = 2
 
 
 def moe_ffn_backward(x, dout, w, y, perm, inv_perm, group_offsets, group_expert, w1, w3, w2, act: str = "gelu",
-                     workspace=None, stream=None, out=None, accumulate: bool = False):
+                     workspace=None, stream=None, out=None, accumulate: bool = False, wgrad_bf16: bool = False):
     """Backward of dispatch -> expert FFN -> combine for one routing.
     x, dout bf16 [T, H]; w f32 [T, k]; y bf16 [T*k, H] (the forward FFN
     output, or None: no dw); perm, inv_perm, group_offsets, group_expert as
     written by the dispatch.  Returns (dx bf16 [T, H], dw f32 [T, k] or None,
     dw1 f32 [E, H, F], dw3 f32 [E, H, F] or None, dw2 f32 [E, F, H]).
     `out` may give those five tensors to write into; accumulate=True adds
-    this batch's weight gradients to what out's dw1, dw3, dw2 hold."""
+    this batch's weight gradients to what out's dw1, dw3, dw2 hold;
+    wgrad_bf16=True returns the weight gradients rounded once to bf16."""
     torch = _torch()
     _dev(x, torch.bfloat16, "x", 2)
     _dev(dout, torch.bfloat16, "dout", 2)
@@ -578,21 +580,28 @@ def moe_ffn_backward(x, dout, w, y, perm, inv_perm, group_offsets, group_expert,
     dev = x.device
     if accumulate and out is None:
         raise ValueError("accumulate=True needs `out`: the gradients to add to")
+    if accumulate and wgrad_bf16:
+        raise ValueError("bf16 weight gradients cannot be accumulated")
+    gdt = torch.bfloat16 if wgrad_bf16 else torch.float32
     if out is None:
         f32 = dict(dtype=torch.float32, device=dev)
         out = (torch.empty((T, H), dtype=torch.bfloat16, device=dev),
                torch.empty((T, k), **f32) if y is not None else None,
-               torch.empty((E, H, F), **f32),
-               torch.empty((E, H, F), **f32) if act == "swiglu" else None,
-               torch.empty((E, F, H), **f32))
+               torch.empty((E, H, F), dtype=gdt, device=dev),
+               torch.empty((E, H, F), dtype=gdt, device=dev) if act == "swiglu" else None,
+               torch.empty((E, F, H), dtype=gdt, device=dev))
     dx, dw, dw1, dw3, dw2 = out
+    for nm, t in (("dw1", dw1), ("dw3", dw3), ("dw2", dw2)):
+        if t is not None:
+            _dev(t, gdt, nm, 3)
     need = int(lib().moe_ffn_backward_workspace_bytes(T, k, E, H, F))
     if workspace is None:
         workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=dev)
     _check(lib().moe_ffn_backward(_ptr(x), _ptr(dout), _ptr(w), _ptr(y), _ptr(perm), _ptr(inv_perm), T, k,
                                   _ptr(group_offsets), _ptr(group_expert), E, _ptr(w1), _ptr(w3), _ptr(w2), H, F,
                                   act_id, _ptr(dx), _ptr(dw), _ptr(dw1), _ptr(dw3), _ptr(dw2),
-                                  MOE_BWD_ACCUMULATE_WGRAD if accumulate else 0, _ptr(workspace),
+                                  (MOE_BWD_ACCUMULATE_WGRAD if accumulate else 0)
+                                  | (MOE_BWD_WGRAD_BF16 if wgrad_bf16 else 0), _ptr(workspace),
                                   workspace.numel(), _stream(stream)), "moe_ffn_backward")
     return dx, dw, dw1, dw3, dw2
 

@@ -89,14 +89,17 @@ size_t moe_ffn_backward_workspace_bytes(int T, int k, int E, int H, int F) {
 moe_status moe_ffn_backward(const uint16_t* x, const uint16_t* dout, const float* w, const uint16_t* y,
                             const int32_t* perm, const int32_t* inv_perm, int T, int k, const int32_t* group_offsets,
                             const int32_t* group_expert, int E, const uint16_t* w1, const uint16_t* w3,
-                            const uint16_t* w2, int H, int F, moe_act act, uint16_t* dx, float* dw, float* dw1,
-                            float* dw3, float* dw2, int flags, void* workspace, size_t ws_bytes, void* stream) {
+                            const uint16_t* w2, int H, int F, moe_act act, uint16_t* dx, float* dw, void* dw1,
+                            void* dw3, void* dw2, int flags, void* workspace, size_t ws_bytes, void* stream) {
   const char* who = "moe_ffn_backward";
   if (T < 0 || k < 1 || k > 8 || E < 1 || E > 256 || k > E)
     return fail(MOE_ERR_INVALID, "%s: need T>=0, 1<=k<=min(E,8), 1<=E<=256", who);
   if (H < 64 || H % 64 || F < 64 || F % 64) return fail(MOE_ERR_INVALID, "%s: H and F must be positive multiples of 64", who);
   if (act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) return fail(MOE_ERR_INVALID, "%s: unknown activation", who);
-  if (flags & ~MOE_BWD_ACCUMULATE_WGRAD) return fail(MOE_ERR_INVALID, "%s: unknown flags 0x%x", who, flags);
+  if (flags & ~(MOE_BWD_ACCUMULATE_WGRAD | MOE_BWD_WGRAD_BF16))
+    return fail(MOE_ERR_INVALID, "%s: unknown flags 0x%x", who, flags);
+  if ((flags & MOE_BWD_ACCUMULATE_WGRAD) && (flags & MOE_BWD_WGRAD_BF16))
+    return fail(MOE_ERR_INVALID, "%s: bf16 weight gradients cannot be accumulated", who);
   const long long A = (long long)T * k;
   const BwdWs L = bwd_ws(A, E, H, F);
   if (L.P * 2 * F >= (1LL << 40) || L.P >= (1LL << 31) - 256 || (long long)E * H >= (1LL << 31) ||
@@ -228,7 +231,8 @@ moe_status moe_ffn_backward(const uint16_t* x, const uint16_t* dout, const float
   wp.rows = P;
   wp.jobs = swiglu ? 3 : 2;
   wp.accumulate = (flags & MOE_BWD_ACCUMULATE_WGRAD) ? 1 : 0;
-  auto job = [&](ffn_wg::Job& j, float* out, int M, int N, int b_col0) {
+  wp.out_bf16 = (flags & MOE_BWD_WGRAD_BF16) ? 1 : 0;
+  auto job = [&](ffn_wg::Job& j, void* out, int M, int N, int b_col0) {
     j.out = out;
     j.M_out = M;
     j.N_out = N;

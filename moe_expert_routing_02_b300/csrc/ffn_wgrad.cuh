@@ -6,7 +6,8 @@
 // there.  On one GPU that reduction is the sum over every row routed to the
 // expert, whichever replica group served the row:
 //
-//   dW[e] = L_e^T R_e    [M_out, N_out], fp32   (or dW[e] += ..., accumulate),
+//   dW[e] = L_e^T R_e    [M_out, N_out], fp32 (or dW[e] += ..., accumulate;
+//                         or rounded once to bf16),
 //
 // where L_e [rows_e, M_out] and R_e [rows_e, N_out] are expert e's rows of two
 // row-major bf16 activation tensors (the reduction runs over rows).  The rows
@@ -49,7 +50,7 @@ constexpr int MAX_JOBS = 3;
 constexpr int MAX_E = 256;
 
 struct Job {
-  float* out;         // [E, M_out, N_out] fp32
+  void* out;          // [E, M_out, N_out] fp32, or bf16 with out_bf16
   int M_out, N_out;   // multiples of 64
   int m_tiles, n_tiles;
   int a_col0, b_col0;  // first column of the job's L and R in their tensors
@@ -68,6 +69,7 @@ struct WParams {
   int tiles_per_expert;  // sum over jobs of m_tiles * n_tiles
   long long rows;        // rows of the operand tensors
   int accumulate;        // 1: dW += result (gradient accumulation), 0: dW = result
+  int out_bf16;          // 1: results rounded once to bf16 (no accumulation)
   Job job[MAX_JOBS];
 };
 
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int row0 = t.mt * BM + quarter * 32;
       const int wrows = J.M_out - row0;
-      float* obase = J.out + ((size_t)t.e * J.M_out + row0) * J.N_out;
+      const size_t ooff = ((size_t)t.e * J.M_out + row0) * J.N_out;
       const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
       constexpr int W = BN / EPI_SLICES;
 #pragma unroll 1
@@ -310,8 +312,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           __syncwarp();
           tmem_ld32(tb + c, raw);
         }
-        if (col < J.N_out && wrows > 0)
-          store_rows32_f32(s.stg[warp - 2], obase + col, (size_t)J.N_out, wrows, raw, lane, p.accumulate != 0);
+        if (col < J.N_out && wrows > 0) {
+          if (p.out_bf16) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(raw[2 * i]), __uint_as_float(raw[2 * i + 1]));
+            ffn::store_rows32(s.stg[warp - 2], static_cast<uint16_t*>(J.out) + ooff + col, (size_t)J.N_out, wrows, pk,
+                              lane);
+          } else {
+            store_rows32_f32(s.stg[warp - 2], static_cast<float*>(J.out) + ooff + col, (size_t)J.N_out, wrows, raw,
+                             lane, p.accumulate != 0);
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();

@@ -204,7 +204,8 @@ class MoELayerStep:
         self._cur ^= 1
         return out
 
-    def backward(self, saved: MoESaved, logits, x, weights, dout, grads=None, dlogits=None, accumulate: bool = False):
+    def backward(self, saved: MoESaved, logits, x, weights, dout, grads=None, dlogits=None, accumulate: bool = False,
+                 wgrad_bf16: bool = False):
         """Backward of one layer run with save=True: dout = dL/d(out) [T, H]
         bf16.  Returns (dx [T, H] bf16, dlogits [T, E] f32, (dW1, dW3 or None,
         dW2) f32).  Every row of an expert adds into that expert's gradient,
@@ -212,14 +213,15 @@ class MoELayerStep:
         w2) [E, ...] (with physical replicas, their first E slots).  `grads`
         may give (dx, dw, dW1, dW3, dW2) buffers to write into; with
         accumulate=True the weight gradients are added to what grads hold
-        (gradient accumulation over micro-batches)."""
+        (gradient accumulation over micro-batches); wgrad_bf16=True returns
+        them rounded once to bf16."""
         w1, w3, w2 = (None if w is None else w[:self.E] for w in weights)
         if self.ws_bwd is None:
             n = moe_ffn_backward_workspace_bytes(self.T, self.k, self.E, self.H, self.F)
             self.ws_bwd = torch.empty(n, dtype=torch.uint8, device=dout.device)
         dx, dw, dw1, dw3, dw2 = moe_ffn_backward(x, dout, saved.w, saved.y, saved.perm, saved.inv, saved.go, saved.ge,
                                                  w1, w3, w2, self.act, workspace=self.ws_bwd, out=grads,
-                                                 accumulate=accumulate)
+                                                 accumulate=accumulate, wgrad_bf16=wgrad_bf16)
         dl = moe_route_backward(logits, saved.idx, dw, self.renorm, out=dlogits)
         return dx, dl, (dw1, dw3, dw2)
 

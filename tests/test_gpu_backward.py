@@ -347,3 +347,22 @@ def test_backward_in_a_cuda_graph():
         if b is not None:
             assert torch.equal(a, b)
     assert torch.equal(dl, dl_eager)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_bf16_weight_gradients_are_the_fp32_ones_rounded(act):
+    """MOE_BWD_WGRAD_BF16: every weight-gradient entry is the fp32 result
+    rounded once to bf16 (round to nearest even), bit for bit; accumulation
+    with bf16 output is refused."""
+    c = _case(300, 6, 2, 128, 192, act, seed=23, alpha=1.3, empty=(4,))
+    f = _gpu(c)
+    b = M.moe_ffn_backward(c["x"], c["dout"], dev(c["w"]), c["y"], dev(c["perm"]), dev(c["inv"]), dev(c["go"]),
+                           None, c["w1"], c["w3"], c["w2"], act, wgrad_bf16=True)
+    M.moe_check()
+    assert torch.equal(b[0], f[0]) and torch.equal(b[1], f[1])
+    for gb, gf in zip(b[2:], f[2:]):
+        if gf is not None:
+            assert gb.dtype == torch.bfloat16 and torch.equal(gb, gf.to(torch.bfloat16))
+    with pytest.raises(ValueError):
+        M.moe_ffn_backward(c["x"], c["dout"], dev(c["w"]), c["y"], dev(c["perm"]), dev(c["inv"]), dev(c["go"]),
+                           None, c["w1"], c["w3"], c["w2"], act, out=b, accumulate=True, wgrad_bf16=True)
