@@ -556,13 +556,26 @@ def cpu_cores():
 
 
 def run_cpu_baseline(c, T_s, reps=3):
-    # warm once (input generation, imports), then time `reps` layer samples
+    # warm once (input generation, imports), then time `reps` layer samples;
+    # then one sample of a quarter of the tokens with the BLAS pool held to
+    # one thread (the single-core rate)
     oracle_layer_sample(c, T_s)
     t = sum(oracle_layer_sample(c, T_s) for _ in range(reps))
-    return {"value": round(reps * T_s / t, 1), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{reps} x one layer of {c.name} with {T_s} of {c.T} tokens (all k={c.k} assignments "
-                      f"through route, stats+predict over 2 layers' routing, replicate, dispatch, fp64 FFN, "
-                      f"combine), {t:.2f} s total; NumPy BLAS threads on {cpu_cores()} host cores"}
+    res = {"value": round(reps * T_s / t, 1), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+           "sample": f"{reps} x one layer of {c.name} with {T_s} of {c.T} tokens (all k={c.k} assignments "
+                     f"through route, stats+predict over 2 layers' routing, replicate, dispatch, fp64 FFN, "
+                     f"combine), {t:.2f} s total; NumPy BLAS threads on {cpu_cores()} host cores"}
+    try:
+        from threadpoolctl import threadpool_limits
+        T_1 = max(T_s // 4, 1)
+        with threadpool_limits(limits=1):
+            oracle_layer_sample(c, T_1)
+            t1 = oracle_layer_sample(c, T_1)
+        res["single_core_value"] = round(T_1 / t1, 1)
+        res["single_core_sample"] = f"one layer of {c.name} with {T_1} tokens, BLAS held to 1 thread, {t1:.2f} s"
+    except ImportError:
+        res["single_core_value"] = None
+    return res
 
 
 def run_reference(args, rank, world):
