@@ -67,6 +67,8 @@ def parse_args(argv=None):
     ap.add_argument("--ffn-kernel", choices=["auto", "single", "pair", "fused"], default="auto",
                     help="grouped-GEMM kernel of the expert FFN (default: the library's choice)")
     ap.add_argument("--no-pdl", action="store_true", help="ordinary launches instead of programmatic dependent launch")
+    ap.add_argument("--fuse-combine", action="store_true",
+                    help="the combine in the FFN's second GEMM epilogue (moe_expert_ffn_combine)")
     ap.add_argument("--small-threshold", type=int, default=64,
                     help="experts with fewer rows take the small-batch FFN kernel (0: none, no side-stream launches)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -287,7 +289,7 @@ def run_ours(args, rank, world, local):
     step = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, stats=stats, replicate=True, fused=not args.unfused,
                         gather=args.gather, replicate_from=args.replicate_from,
                         physical_replicas=args.physical_replicas, small_group_threshold=args.small_threshold,
-                        device=dev)
+                        fuse_combine=args.fuse_combine, device=dev)
     if args.physical_replicas:
         weights = [MoELayerStep.replica_buffers(w) for w in weights]
     if args.chunks > 1:
@@ -458,6 +460,7 @@ def run_ours(args, rank, world, local):
                    "ffn_kernel": args.ffn_kernel,
                    "pdl": not args.no_pdl,
                    "small_group_threshold": args.small_threshold,
+                   "combine": "in the FFN's second GEMM epilogue" if args.fuse_combine else "separate kernel",
                    "chunks": args.chunks,
                    "replicas": ("physical copies (moe_replicate_weights)" if args.physical_replicas
                                 else "aliasing their expert's weights") + f", table from {args.replicate_from}",

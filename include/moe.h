@@ -78,7 +78,7 @@ typedef enum {
 
 typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
 
-typedef enum { MOE_OP_DISPATCH = 1, MOE_OP_EXPERT_FFN = 2, MOE_OP_LAYER_FRONT = 3 } moe_op;
+typedef enum { MOE_OP_DISPATCH = 1, MOE_OP_EXPERT_FFN = 2, MOE_OP_LAYER_FRONT = 3, MOE_OP_EXPERT_FFN_COMBINE = 4 } moe_op;
 
 /* Opaque window state: device ring buffers of per-layer histograms and
  * per-layer-pair co-selection counts, plus running window sums. */
@@ -368,6 +368,32 @@ moe_status moe_expert_ffn_slots(const uint16_t* xp, const int32_t* group_offsets
                                 uint16_t* y, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_expert_ffn_combine -- moe_expert_ffn and moe_combine in one call, the
+ * combine done in the second GEMM's epilogue.
+ * EPS-MoE review (expert pipelining: fusing the LocalReduce of expert outputs
+ * into the expert computation).  Each dispatched row's GEMM2 result, times its
+ * gate weight w[perm[i]], is added with fp32 reductions into row perm[i] / k of
+ * an fp32 [T, H] accumulator in the workspace (zeroed by the call); a last
+ * pass rounds it once to bf16 into out.  Y is never stored.
+ *   Arguments as moe_expert_ffn (xp, group_offsets, group_expert, rep_base,
+ *   E, weights, H, F, act, small_group_threshold) and moe_combine (perm from
+ *   the same dispatch, w [T,k] f32, T, k); out bf16 [T,H].
+ *   workspace  >= moe_workspace_bytes(MOE_OP_EXPERT_FFN_COMBINE, T, k, E, H, F),
+ *              256-byte aligned.
+ * Arithmetic: fp32 sums of w * (fp32 GEMM2 result) -- Y is not rounded to
+ * bf16 first, so out can differ from moe_expert_ffn + moe_combine by about
+ * one bf16 rounding; for k <= 2 every sum is two additions onto zero and the
+ * result does not depend on their order (bit-reproducible); for k > 2 the
+ * order of the reductions, and so the last bits, may vary between runs.
+ * Uses the two-launch grouped kernels (not the fused one).
+ * ------------------------------------------------------------------------- */
+moe_status moe_expert_ffn_combine(const uint16_t* xp, const int32_t* group_offsets, const int32_t* group_expert,
+                                  const int32_t* rep_base, int E, const int32_t* perm, const float* w, int T, int k,
+                                  const uint16_t* w1, const uint16_t* w3, const uint16_t* w2, int H, int F,
+                                  moe_act act, int small_group_threshold, uint16_t* out, void* workspace,
+                                  size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * moe_ffn_backward -- backward of the routed expert layer: combine, expert
  * FFN and dispatch copy.
  * PopFetcher (ATC'25) review: the system trains MoE models; in the backward
@@ -533,7 +559,8 @@ moe_status moe_get_option(int option, int* value /* host */);
  * 0 for bad sizes.  Host only. */
 int moe_ffn_launches(int A, int E, int H, int F, int act, int small_group_threshold, int gather);
 
-/* Workspace bytes for op (MOE_OP_DISPATCH or MOE_OP_EXPERT_FFN); 0 for bad sizes. */
+/* Workspace bytes for op (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT or
+ * MOE_OP_EXPERT_FFN_COMBINE); 0 for bad sizes. */
 size_t moe_workspace_bytes(int op, int T, int k, int E, int H, int F);
 
 /* Synchronises `stream`, then reads and clears the device error word of the

@@ -29,7 +29,7 @@ library_path = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_WORKSPACE, MOE_ERR_DEVICE = range(7)
 MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
-MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT = 1, 2, 3
+MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT, MOE_OP_EXPERT_FFN_COMBINE = 1, 2, 3, 4
 MOE_OPT_FFN_KERNEL, MOE_OPT_FFN_TIMEOUT_SELFTEST, MOE_OPT_PDL = 1, 2, 3
 MOE_FFN_KERNEL_AUTO, MOE_FFN_KERNEL_SINGLE, MOE_FFN_KERNEL_PAIR, MOE_FFN_KERNEL_FUSED = 0, 1, 2, 3
 
@@ -70,6 +70,8 @@ _SIGS = {
                              _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_get_option": (_I, [_I, ctypes.POINTER(_I)]),
     "moe_ffn_backward_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_expert_ffn_combine": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ,
+                                    _P]),
     "moe_ffn_backward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P,
                               _I, _P, _SZ, _P]),
     "moe_route_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
@@ -532,6 +534,42 @@ def moe_expert_ffn_slots(xp, group_offsets, group_slot, w1, w3, w2, act: str = "
                                       _ptr(w2), H, F, act_id, int(small_group_threshold), _ptr(y), _ptr(workspace),
                                       workspace.numel(), _stream(stream)), "moe_expert_ffn_slots")
     return y
+
+
+def moe_expert_ffn_combine(xp, group_offsets, group_expert, rep_base, perm, w, w1, w3, w2, act: str = "gelu",
+                           small_group_threshold: int = 64, out=None, workspace=None, stream=None):
+    """moe_expert_ffn then moe_combine in one call, the combine in the second
+    GEMM's epilogue: returns out [T, H] bf16."""
+    torch = _torch()
+    _dev(xp, torch.bfloat16, "xp", 2)
+    _dev(group_offsets, torch.int32, "group_offsets", 1)
+    _dev(perm, torch.int32, "perm", 1)
+    _dev(w, torch.float32, "w", 2)
+    _dev(w1, torch.bfloat16, "w1", 3)
+    _dev(w2, torch.bfloat16, "w2", 3)
+    if w3 is not None:
+        _dev(w3, torch.bfloat16, "w3", 3)
+    if group_expert is not None:
+        _dev(group_expert, torch.int32, "group_expert", 1)
+    if rep_base is not None:
+        _dev(rep_base, torch.int32, "rep_base", 1)
+    A, H = xp.shape
+    T, k = w.shape
+    E, H1, F = w1.shape
+    if H1 != H or tuple(w2.shape) != (E, F, H) or A != T * k:
+        raise ValueError("shapes: xp [T*k,H], w [T,k], w1/w3 [E,H,F], w2 [E,F,H]")
+    act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=xp.device)
+    _dev(out, torch.bfloat16, "out", 2)
+    need = int(lib().moe_workspace_bytes(MOE_OP_EXPERT_FFN_COMBINE, T, k, E, H, F))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=xp.device)
+    _check(lib().moe_expert_ffn_combine(_ptr(xp), _ptr(group_offsets), _ptr(group_expert), _ptr(rep_base), E,
+                                        _ptr(perm), _ptr(w), T, k, _ptr(w1), _ptr(w3), _ptr(w2), H, F, act_id,
+                                        int(small_group_threshold), _ptr(out), _ptr(workspace), workspace.numel(),
+                                        _stream(stream)), "moe_expert_ffn_combine")
+    return out
 
 
 def moe_ffn_launches(A: int, E: int, H: int, F: int, act: str = "gelu", small_group_threshold: int = 64,

@@ -96,4 +96,25 @@ static cudaError_t launch(const uint16_t* y, const int32_t* inv_perm, const floa
   return cudaGetLastError();
 }
 
+// The combine fused into the FFN's second GEMM leaves its sums in an fp32
+// [T, H] accumulator; this rounds them once to bf16 (8 values per thread).
+__global__ void __launch_bounds__(kThreads) finalize_kernel(const float* __restrict__ acc, long long n8,
+                                                           uint16_t* __restrict__ out) {
+  pdl_wait();
+  for (long long i = (long long)blockIdx.x * kThreads + threadIdx.x; i < n8; i += (long long)gridDim.x * kThreads) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    reinterpret_cast<uint4*>(out)[i] =
+        make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  }
+}
+
+static cudaError_t launch_finalize(const float* acc, long long T, int H, uint16_t* out, int num_sms, cudaStream_t st) {
+  const long long n8 = T * H / 8;
+  if (n8 == 0) return cudaSuccess;
+  long long blocks = (n8 + kThreads - 1) / kThreads;
+  if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
+  return launch_pdl(finalize_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, st, acc, n8, out);
+}
+
 }  // namespace combine

@@ -94,8 +94,12 @@ constexpr uint32_t kMaxPolls = 1u << 30;
 // [u silu'(g) | silu(g)] for SwiGLU.  kStoreKMMul: dA = dY W2^T (K-major B);
 // the epilogue multiplies dA by those factors in place (out), giving dz;
 // kStoreKMMul2 likewise with the SwiGLU pair of factors, giving [dg | du].
+// kCombine: GEMM2 with the combine in its epilogue: row i's result, times
+// its gate weight w[perm[i]], is added (fp32 reductions) into row
+// perm[i] / k of an fp32 [T, N_out] accumulator instead of being stored.
 enum Epi : int {
-  kGelu = 0, kSwiglu = 1, kStore = 2, kStoreKM = 3, kBwdGelu = 4, kBwdSwiglu = 5, kStoreKMMul = 6, kStoreKMMul2 = 7
+  kGelu = 0, kSwiglu = 1, kStore = 2, kStoreKM = 3, kBwdGelu = 4, kBwdSwiglu = 5, kStoreKMMul = 6, kStoreKMMul2 = 7,
+  kCombine = 8
 };
 
 __host__ __device__ constexpr bool epi_pair_b(int e) { return e == kSwiglu || e == kBwdSwiglu; }
@@ -130,7 +134,39 @@ struct Params {
   // kStoreKMMul / kStoreKMMul2: out = those factors, overwritten with the
   // products.
   uint16_t* out2;
+  // kCombine: the dispatch permutation, the gate weights [T*k], k and the
+  // fp32 accumulator [T, N_out] (zero before the call)
+  const int32_t* comb_perm;
+  const float* comb_w;
+  int comb_k;
+  float* comb_acc;
 };
+
+// acc[t, c .. c+31] += wt * v[0 .. 31] with vector fp32 reductions (8 per
+// row segment).  For k = 2 every accumulator element receives exactly two
+// additions onto zero, so the result does not depend on their order.
+__device__ __forceinline__ void red_add32(float* dst, const float (&v)[32], float wt) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * j),
+                 "f"(wt * v[4 * j]), "f"(wt * v[4 * j + 1]), "f"(wt * v[4 * j + 2]), "f"(wt * v[4 * j + 3])
+                 : "memory");
+}
+
+// Token row and gate weight of dispatched row `row` (kCombine); a row
+// outside [0, rows) or an invalid permutation entry gives wt = 0 and
+// acc_row = null (flagged).
+__device__ __forceinline__ float* comb_target(const Params& p, long long row, long long rows_valid_end, float& wt) {
+  wt = 0.f;
+  if (row >= rows_valid_end) return nullptr;
+  const int f = __ldg(p.comb_perm + row);
+  if (f < 0 || (long long)f >= p.A_rows) {
+    moe_flag_error(MOE_DEVERR_DATA);
+    return nullptr;
+  }
+  wt = __ldg(p.comb_w + f);
+  return p.comb_acc + (size_t)(f / p.comb_k) * p.N_out;
+}
 
 
 struct Smem {
@@ -902,6 +938,24 @@ __global__ void __launch_bounds__(THREADS, 1)
           store_rows16(s.stg[warp - 2], wbase + col, (size_t)p.N_out, wrows, pa, lane);
           store_rows16(s.stg[warp - 2], w2base + col, ld2, wrows, pg, lane);
           store_rows16(s.stg[warp - 2], w2base + p.N_out + col, ld2, wrows, pu, lane);
+        }
+      } else if (EPI == kCombine) {
+        constexpr int W = BN / EPI_SLICES;
+        float wt;
+        float* arow = comb_target(p, t.row0 + quarter * 32 + lane, t.row0 + t.rows, wt);
+#pragma unroll 1
+        for (int cc = 0; cc < W; cc += 32) {
+          const int c = slice * W + cc;
+          uint32_t raw[32];
+          __syncwarp();
+          tmem_ld32(tb + c, raw);
+          const int col = t.nt * BN + c;
+          if (col < p.N_out && arow) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
+            red_add32(arow + col, v, wt);
+          }
         }
       } else if (EPI == kSwiglu) {
         constexpr int W = (BN / 2) / EPI_SLICES;   // output columns per warp

@@ -286,7 +286,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int wrows = rows - quarter * 32;  // rows of this warp's 32 that belong to the group
       uint16_t* wbase = p.out + (size_t)(myrow0 + quarter * 32) * p.N_out;
       const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      if (EPI == kSwiglu) {
+      if (EPI == ffn::kCombine) {
+        constexpr int W = BN / EPI_SLICES;
+        float wt;
+        float* arow = ffn::comb_target(p, myrow0 + quarter * 32 + lane, myrow0 + rows, wt);
+#pragma unroll 1
+        for (int cc = 0; cc < W; cc += 32) {
+          const int c = slice * W + cc;
+          uint32_t raw[32];
+          __syncwarp();
+          tmem_ld32(tb + c, raw);
+          const int col = t.nt * BN + c;
+          if (col < p.N_out && arow) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
+            ffn::red_add32(arow + col, v, wt);
+          }
+        }
+      } else if (EPI == kSwiglu) {
         constexpr int W = (BN / 2) / EPI_SLICES;
 #pragma unroll 1
         for (int cc = 0; cc < W; cc += 32) {

@@ -293,7 +293,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             v[i] = (EPI == kGelu) ? gelu_erf(z) : z;
           }
         }
-        if (f_ok) {
+        if (EPI == ffn::kCombine) {
+          // each token row: its gate weight times the value, added into the
+          // row's token in the fp32 accumulator (32 consecutive features per warp)
+#pragma unroll 1
+          for (int i = 0; i < 16; ++i) {
+            if (c0 + i >= t.rows) break;
+            float wt;
+            float* arow = ffn::comb_target(p, t.row0 + c0 + i, t.row0 + t.rows, wt);
+            if (arow && f_ok)
+              asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(arow + f), "f"(wt * v[i]) : "memory");
+          }
+        } else if (f_ok) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             if (c0 + i < t.rows) {

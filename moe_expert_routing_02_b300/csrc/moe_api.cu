@@ -61,10 +61,10 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool init = false;
   int num_sms = 0;
-  bool ffn_attr[3] = {false, false, false};
-  bool pair_attr[3] = {false, false, false};
-  bool small_attr[3] = {false, false, false};
-  int pair_clusters[3] = {0, 0, 0};  // max co-resident CTA pairs per pair-kernel instance
+  bool ffn_attr[4] = {false, false, false, false};    // GeLU, SwiGLU, store, combine
+  bool pair_attr[4] = {false, false, false, false};
+  bool small_attr[4] = {false, false, false, false};
+  int pair_clusters[4] = {0, 0, 0, 0};  // max co-resident CTA pairs per pair-kernel instance
   bool fused_attr[2] = {false, false};
   int fused_clusters[2] = {0, 0};    // max co-resident CTA pairs of the fused kernel (GeLU, SwiGLU)
   // The FFN's small-batch kernels run as a second chain on this stream, forked
@@ -199,6 +199,10 @@ size_t moe_workspace_bytes(int op, int T, int k, int E, int H, int F) {
   if (op == MOE_OP_EXPERT_FFN) {
     if (F < 64 || F % 64 || H < 64 || H % 64) return 0;
     return ffn_workspace_bytes(A, F, 2 * E);
+  }
+  if (op == MOE_OP_EXPERT_FFN_COMBINE) {
+    if (F < 64 || F % 64 || H < 64 || H % 64) return 0;
+    return ((ffn_workspace_bytes(A, F, 2 * E) + 255) & ~(size_t)255) + (size_t)T * H * 4;
   }
   return 0;
 }
@@ -531,14 +535,28 @@ void ffn_choice(long long A, int E, int H, int F, int act, bool gather, bool* us
                 (g_opt_ffn_kernel == MOE_FFN_KERNEL_AUTO && expert_weight_bytes <= (16LL << 20)));
 }
 
-// Both FFN entry points.  a_src == null: A (GEMM1's input rows) is `a`
+// The combine fused into GEMM2 (moe_expert_ffn_combine): GEMM2's epilogues
+// add w[perm[i]] * Y[i] into acc [T, H] fp32 (zeroed first), then one pass
+// rounds acc to bf16 into out.
+struct CombineArgs {
+  const int32_t* perm;
+  const float* w;
+  int k;
+  long long T;
+  float* acc;
+  uint16_t* out;
+};
+
+// The FFN entry points.  a_src == null: A (GEMM1's input rows) is `a`
 // itself, [A, H] in dispatched order.  Otherwise `a` is x [T, H] and row i
-// of A is x[a_src[i] / k], gathered by GEMM1's loads.
+// of A is x[a_src[i] / k], gathered by GEMM1's loads.  comb != null: the
+// combine runs in GEMM2's epilogue instead of storing Y (y unused).
 moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, int k, int T,
                       const int32_t* group_offsets, const int32_t* group_expert, int G, const int32_t* rep_base, int E,
                       int A,
                       const uint16_t* w1, const uint16_t* w3, const uint16_t* w2, int H, int F, moe_act act,
-                      int small_group_threshold, uint16_t* y, void* workspace, size_t ws_bytes, void* stream) {
+                      int small_group_threshold, uint16_t* y, void* workspace, size_t ws_bytes, void* stream,
+                      const CombineArgs* comb = nullptr) {
   const uint16_t* xp = a;
   const bool gather = a_src != nullptr;
   if (E < 1 || E > ffn::MAX_G || A < 0) return fail(MOE_ERR_INVALID, "%s: need 1<=E<=%d, A>=0", who, ffn::MAX_G);
@@ -549,9 +567,10 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   if ((long long)E * H >= (1LL << 31) || (long long)E * F >= (1LL << 31))
     return fail(MOE_ERR_INVALID, "%s: weights too large", who);
   if (A == 0) return MOE_OK;
-  if (!xp || !group_offsets || !w1 || !w2 || !y || !workspace) return fail(MOE_ERR_INVALID, "%s: null pointer", who);
+  if (!xp || !group_offsets || !w1 || !w2 || (!y && !comb) || !workspace)
+    return fail(MOE_ERR_INVALID, "%s: null pointer", who);
   if (act == MOE_ACT_SWIGLU && !w3) return fail(MOE_ERR_INVALID, "%s: SwiGLU needs w3", who);
-  if (!aligned(xp, 16) || !aligned(w1, 16) || !aligned(w2, 16) || !aligned(y, 16) || (w3 && !aligned(w3, 16)))
+  if (!aligned(xp, 16) || !aligned(w1, 16) || !aligned(w2, 16) || (y && !aligned(y, 16)) || (w3 && !aligned(w3, 16)))
     return fail(MOE_ERR_INVALID, "%s: matrices must be 16-byte aligned", who);
   if (!aligned(workspace, 16)) return fail(MOE_ERR_INVALID, "%s: workspace must be 16-byte aligned", who);
   if (ws_bytes < ffn_workspace_bytes(A, F, G))
@@ -586,6 +605,7 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   // (A, E) only, so a call with and without replica groups takes the same path.
   bool use_pair = false, use_fused = false;
   ffn_choice(A, E, H, F, act, gather, &use_pair, &use_fused);
+  if (comb) use_fused = false;  // the fused kernel's GEMM2 stores Y
 
   ffn::Params p1{};
   p1.group_offsets = group_offsets;
@@ -611,6 +631,13 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   p2.K = F;
   p2.N_out = H;
   p2.out = y;
+  if (comb) {
+    p2.comb_perm = comb->perm;
+    p2.comb_w = comb->w;
+    p2.comb_k = comb->k;
+    p2.comb_acc = comb->acc;
+  }
+  const int epi2 = comb ? ffn::kCombine : ffn::kStore;
 
   // small-batch kernels (experts with fewer than small_group_threshold rows)
   CUtensorMap mS1, mS2;
@@ -626,14 +653,16 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
       return ms;
     if ((ms = encode_2d(&mS2, inter, F, A, 64, ffn_small::BT)) != MOE_OK) return ms;
     std::lock_guard<std::mutex> lk(g_mu);
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 4; ++i) {
       if (d->small_attr[i]) continue;
       const void* fn = i == 0 ? (const void*)ffn_small::small_kernel<ffn::kGelu>
                      : i == 1 ? (const void*)ffn_small::small_kernel<ffn::kSwiglu>
-                              : (const void*)ffn_small::small_kernel<ffn::kStore>;
+                     : i == 2 ? (const void*)ffn_small::small_kernel<ffn::kStore>
+                              : (const void*)ffn_small::small_kernel<ffn::kCombine>;
       const int bytes = i == 0 ? (int)ffn_small::smem_bytes<ffn::kGelu>()
                       : i == 1 ? (int)ffn_small::smem_bytes<ffn::kSwiglu>()
-                               : (int)ffn_small::smem_bytes<ffn::kStore>();
+                      : i == 2 ? (int)ffn_small::smem_bytes<ffn::kStore>()
+                               : (int)ffn_small::smem_bytes<ffn::kCombine>();
       cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
       if (e != cudaSuccess) return cuda_at(who, e, "cudaFuncSetAttribute (small)");
       d->small_attr[i] = true;
@@ -659,13 +688,22 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
                                             ss>>>(mS1, mW1, mW3, ps1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    ffn_small::small_kernel<ffn::kStore><<<small_grid(ps2), ffn_small::THREADS, ffn_small::smem_bytes<ffn::kStore>(),
-                                           ss>>>(mS2, mW2, mW2, ps2);
+    if (epi2 == ffn::kCombine)
+      ffn_small::small_kernel<ffn::kCombine><<<small_grid(ps2), ffn_small::THREADS,
+                                               ffn_small::smem_bytes<ffn::kCombine>(), ss>>>(mS2, mW2, mW2, ps2);
+    else
+      ffn_small::small_kernel<ffn::kStore><<<small_grid(ps2), ffn_small::THREADS, ffn_small::smem_bytes<ffn::kStore>(),
+                                             ss>>>(mS2, mW2, mW2, ps2);
     return cudaGetLastError();
   };
   std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
   // forks the side chain off `st`, right before the first grouped kernel
+  // (the combine accumulator is zeroed first, before either chain adds to it)
   auto fork = [&]() -> cudaError_t {
+    if (comb) {
+      cudaError_t z = cudaMemsetAsync(comb->acc, 0, (size_t)comb->T * H * sizeof(float), st);
+      if (z != cudaSuccess) return z;
+    }
     if (!small_path) return cudaSuccess;
     side_lock.lock();
     cudaError_t e = cudaEventRecord(d->fork_ev, st);
@@ -675,13 +713,20 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   };
   // joins the side chain back into `st` (after the grouped kernels are enqueued)
   auto finish = [&](cudaError_t e_main, const char* what) -> moe_status {
-    if (!small_path) return cuda_at(who, e_main, what);
-    cudaError_t e = launch_small_chain(d->side);
-    cudaError_t j = cudaEventRecord(d->join_ev, d->side);
-    if (j == cudaSuccess) j = cudaStreamWaitEvent(st, d->join_ev, 0);
-    if (e_main != cudaSuccess) return cuda_at(who, e_main, what);
-    if (e != cudaSuccess) return cuda_at(who, e, "small-batch kernels launch");
-    return cuda_at(who, j, "join of the small-batch chain");
+    moe_status r;
+    if (!small_path) {
+      r = cuda_at(who, e_main, what);
+    } else {
+      cudaError_t e = launch_small_chain(d->side);
+      cudaError_t j = cudaEventRecord(d->join_ev, d->side);
+      if (j == cudaSuccess) j = cudaStreamWaitEvent(st, d->join_ev, 0);
+      if (e_main != cudaSuccess) return cuda_at(who, e_main, what);
+      if (e != cudaSuccess) return cuda_at(who, e, "small-batch kernels launch");
+      r = cuda_at(who, j, "join of the small-batch chain");
+    }
+    if (r != MOE_OK || !comb) return r;
+    return cuda_at(who, combine::launch_finalize(comb->acc, comb->T, H, comb->out, d->num_sms, st),
+                   "combine finalize launch");
   };
 
   if (use_fused) {
@@ -737,11 +782,12 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   if (use_pair) {
     {
       std::lock_guard<std::mutex> lk(g_mu);
-      for (int i = 0; i < 3; ++i) {
+      for (int i = 0; i < 4; ++i) {
         if (d->pair_attr[i]) continue;
         const void* fn = i == 0 ? (const void*)ffn2::gemm_pair_kernel<ffn::kGelu>
                        : i == 1 ? (const void*)ffn2::gemm_pair_kernel<ffn::kSwiglu>
-                                : (const void*)ffn2::gemm_pair_kernel<ffn::kStore>;
+                       : i == 2 ? (const void*)ffn2::gemm_pair_kernel<ffn::kStore>
+                                : (const void*)ffn2::gemm_pair_kernel<ffn::kCombine>;
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ffn2::kSmemBytes);
         if (e != cudaSuccess) return cuda_at(who, e, "cudaFuncSetAttribute (pair)");
         cudaLaunchConfig_t cfg = {};
@@ -777,18 +823,19 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
                                dim3(grid_for(p1, epi1 == ffn::kSwiglu ? 1 : 0)), dim3(ffn2::THREADS),
                                ffn2::kSmemBytes, st, mA1, mW1, mW3, p1);
     if (e != cudaSuccess) return finish(e, "GEMM1 (pair) launch");
-    e = launch_pdl(ffn2::gemm_pair_kernel<ffn::kStore>, dim3(grid_for(p2, 2)), dim3(ffn2::THREADS), ffn2::kSmemBytes,
-                   st, mA2, mW2, mW2, p2);
+    e = launch_pdl(comb ? ffn2::gemm_pair_kernel<ffn::kCombine> : ffn2::gemm_pair_kernel<ffn::kStore>,
+                   dim3(grid_for(p2, comb ? 3 : 2)), dim3(ffn2::THREADS), ffn2::kSmemBytes, st, mA2, mW2, mW2, p2);
     return finish(e, "GEMM2 (pair) launch");
   }
 
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 4; ++i) {
       if (d->ffn_attr[i]) continue;
       const void* fn = i == 0 ? (const void*)ffn::gemm_kernel<ffn::kGelu>
                      : i == 1 ? (const void*)ffn::gemm_kernel<ffn::kSwiglu>
-                              : (const void*)ffn::gemm_kernel<ffn::kStore>;
+                     : i == 2 ? (const void*)ffn::gemm_kernel<ffn::kStore>
+                              : (const void*)ffn::gemm_kernel<ffn::kCombine>;
       cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ffn::kSmemBytes);
       if (e != cudaSuccess) return cuda_at(who, e, "cudaFuncSetAttribute");
       d->ffn_attr[i] = true;
@@ -809,7 +856,10 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
     ffn::gemm_kernel<ffn::kGelu><<<grid_for(p1), ffn::THREADS, ffn::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return finish(e, "GEMM1 launch");
-  ffn::gemm_kernel<ffn::kStore><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
+  if (comb)
+    ffn::gemm_kernel<ffn::kCombine><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
+  else
+    ffn::gemm_kernel<ffn::kStore><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
   return finish(cudaGetLastError(), "GEMM2 launch");
 }
 
@@ -836,6 +886,32 @@ moe_status moe_expert_ffn_gather(const uint16_t* x, int T, const int32_t* perm, 
   return expert_ffn("moe_expert_ffn_gather", x, T > 0 ? perm : nullptr, k, T, group_offsets, group_expert,
                     group_expert ? 2 * E : E, rep_base, E, T * k, w1, w3, w2, H, F, act, small_group_threshold, y,
                     workspace, ws_bytes, stream);
+}
+
+static size_t ffn_combine_acc_offset(long long A, int F, int G) { return (ffn_workspace_bytes(A, F, G) + 255) & ~(size_t)255; }
+
+moe_status moe_expert_ffn_combine(const uint16_t* xp, const int32_t* group_offsets, const int32_t* group_expert,
+                                  const int32_t* rep_base, int E, const int32_t* perm, const float* w, int T, int k,
+                                  const uint16_t* w1, const uint16_t* w3, const uint16_t* w2, int H, int F,
+                                  moe_act act, int small_group_threshold, uint16_t* out, void* workspace,
+                                  size_t ws_bytes, void* stream) {
+  const char* who = "moe_expert_ffn_combine";
+  if (E < 1 || E > 256 || T < 0 || k < 1 || k > 8 || k > E)
+    return fail(MOE_ERR_INVALID, "%s: need 1<=E<=256, T>=0, 1<=k<=min(E,8)", who);
+  if ((long long)T * k >= (1LL << 31)) return fail(MOE_ERR_INVALID, "%s: T*k too large", who);
+  if (H < 64 || H % 64 || F < 64 || F % 64) return fail(MOE_ERR_INVALID, "%s: H and F must be positive multiples of 64", who);
+  if (T == 0) return MOE_OK;
+  if (!perm || !w || !out || !workspace) return fail(MOE_ERR_INVALID, "%s: null pointer", who);
+  if (!aligned(out, 16) || !aligned(workspace, 256))
+    return fail(MOE_ERR_INVALID, "%s: out must be 16-byte aligned, the workspace 256-byte aligned", who);
+  const int G = group_expert ? 2 * E : E;
+  const long long A = (long long)T * k;
+  const size_t off = ffn_combine_acc_offset(A, F, G);
+  if (ws_bytes < off + (size_t)T * H * 4)
+    return fail(MOE_ERR_WORKSPACE, "%s: workspace needs %zu bytes", who, off + (size_t)T * H * 4);
+  CombineArgs cb{perm, w, k, T, reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + off), out};
+  return expert_ffn(who, xp, nullptr, 1, 0, group_offsets, group_expert, G, rep_base, E, (int)A, w1, w3, w2, H, F,
+                    act, small_group_threshold, nullptr, workspace, off, stream, &cb);
 }
 
 moe_status moe_expert_ffn_slots(const uint16_t* xp, const int32_t* group_offsets, const int32_t* group_slot, int G,

@@ -11,8 +11,8 @@ from typing import Optional
 
 import torch
 
-from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT, MoEStats, moe_combine, moe_dispatch,
-               moe_expert_ffn, moe_expert_ffn_gather, moe_ffn_backward, moe_ffn_backward_workspace_bytes,
+from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_EXPERT_FFN_COMBINE, MOE_OP_LAYER_FRONT, MoEStats,
+               moe_combine, moe_dispatch, moe_expert_ffn, moe_expert_ffn_combine, moe_expert_ffn_gather, moe_ffn_backward, moe_ffn_backward_workspace_bytes,
                moe_ffn_launches, moe_layer_front, moe_predict, moe_replicate, moe_replicate_predicted,
                moe_replicate_weights, moe_expert_ffn_slots, moe_route, moe_route_backward, moe_stats_update,
                workspace_bytes)
@@ -49,13 +49,15 @@ class MoELayerStep:
     physical_replicas=True copies each replica's weights into its own slot
     (moe_replicate_weights) and runs the FFN over the slots; `weights` must
     then be the buffers of replica_buffers().  The output is the same in
-    every combination."""
+    every combination.  fuse_combine=True runs the combine in the second
+    GEMM's epilogue (moe_expert_ffn_combine; Y is not stored, so the output
+    differs by about one bf16 rounding and save=True is not available)."""
 
     def __init__(self, T: int, E: int, k: int, H: int, F: int, act: str, stats: Optional[MoEStats] = None,
                  replicate: bool = True, thresh=(6, 5), max_copies: int = -1, renorm: bool = True,
                  small_group_threshold: int = 64, fused: bool = True, gather: bool = False,
                  replicate_from: str = "histogram", budget: int = -1, physical_replicas: bool = False,
-                 device="cuda"):
+                 fuse_combine: bool = False, device="cuda"):
         self.T, self.E, self.k, self.H, self.F, self.act = T, E, k, H, F, act
         self.A = T * k
         self.stats = stats
@@ -71,6 +73,9 @@ class MoELayerStep:
         if budget >= 0 and not self.fused:
             raise ValueError("a copies budget needs the fused front (fused=True with stats)")
         self.gather = gather
+        self.fuse_combine = fuse_combine
+        if fuse_combine and (gather or self.physical):
+            raise ValueError("fuse_combine works with rows copied into dispatch order and aliased replicas")
         d = torch.device(device)
         i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
         A = self.A
@@ -94,8 +99,8 @@ class MoELayerStep:
         self.ws_dispatch = torch.empty(max(workspace_bytes(MOE_OP_DISPATCH, T, k, E),
                                            workspace_bytes(MOE_OP_LAYER_FRONT, T, k, E), 16),
                                        dtype=torch.uint8, device=d)
-        self.ws_ffn = torch.empty(max(workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F), 1024), dtype=torch.uint8,
-                                  device=d)
+        op = MOE_OP_EXPERT_FFN_COMBINE if fuse_combine else MOE_OP_EXPERT_FFN
+        self.ws_ffn = torch.empty(max(workspace_bytes(op, T, k, E, H, F), 1024), dtype=torch.uint8, device=d)
         self.ws_bwd = None   # allocated by the first backward
         self.saved = None    # the last run(save=True)
         self._save = False
@@ -187,6 +192,16 @@ class MoELayerStep:
                 moe_replicate_weights(self.rep_base, w3, group_slot=self.gslot)
             moe_expert_ffn_slots(self.xp, self.go, self.gslot, w1, w3, w2, self.act, self.small, y=self.y,
                                  workspace=self.ws_ffn)
+        elif self.fuse_combine:
+            if self._save:
+                raise ValueError("save=True needs Y, which fuse_combine does not store")
+            moe_expert_ffn_combine(self.xp, self.go, ge, rb, self.perm, self.w, w1, w3, w2, self.act, self.small,
+                                   out=out, workspace=self.ws_ffn)
+            mark("ffn", 1)
+            mark("combine", 0)  # the combine ran inside the FFN
+            mark("combine", 1)
+            self._cur ^= 1
+            return out
         elif self.gather:
             moe_expert_ffn_gather(x, self.perm, self.k, self.go, ge, rb, w1, w3, w2, self.act, self.small, y=self.y,
                                   workspace=self.ws_ffn)
@@ -231,6 +246,10 @@ class MoELayerStep:
                    + 2 * (3 if self.act == "swiglu" else 2))
         else:
             ffn = moe_ffn_launches(self.A, self.E, self.H, self.F, self.act, self.small, self.gather)
+        if self.fuse_combine:  # the two-launch kernels (the fused one stores Y), the finalize pass, no combine
+            ffn = moe_ffn_launches(self.A, self.E, self.H, self.F, self.act, self.small, True) + 1
+            return (2 if self.fused else 1 + 4 + (1 if self.stats is not None else 0)
+                    + (1 if self.stats is not None and layer < L - 1 else 0) + (1 if self.replicate else 0)) + ffn
         if self.fused:
             return 2 + ffn + 1
         n = 1 + (3 if self.gather else 4) + ffn + 1
