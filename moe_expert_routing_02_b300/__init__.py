@@ -7,8 +7,9 @@ library's CUDA kernels; there is no CPU fallback, and using any function
 without the built library raises.
 
 Functions carry the C names: moe_route, moe_stats_update, moe_predict,
-moe_replicate, moe_dispatch, moe_expert_ffn, moe_combine (plus MoEStats, the
-owner of the sliding-window state, and moe_check).
+moe_replicate, moe_dispatch, moe_expert_ffn, moe_combine, their fused forms,
+the replication and backward calls (plus MoEStats, the owner of the
+sliding-window state, and moe_check).
 """
 from __future__ import annotations
 
@@ -17,11 +18,22 @@ import os
 from typing import Optional
 
 __all__ = [
-    "MoEError", "lib", "library_path", "MoEStats", "moe_route", "moe_stats_update", "moe_predict",
-    "moe_replicate", "moe_dispatch", "moe_dispatch_noalloc", "moe_layer_front", "moe_expert_ffn", "moe_expert_ffn_gather", "moe_combine", "moe_predict_decay", "moe_replicate_predicted", "moe_ffn_launches", "moe_replicate_weights", "moe_expert_ffn_slots", "moe_check", "moe_error_word",
-    "workspace_bytes", "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_ACT_GELU", "MOE_ACT_SWIGLU",
-    "EXPORTED_SYMBOLS", "moe_set_option", "moe_get_option", "MOE_OPT_FFN_KERNEL", "MOE_FFN_KERNEL_AUTO",
-    "MOE_FFN_KERNEL_SINGLE", "MOE_FFN_KERNEL_PAIR", "MOE_FFN_KERNEL_FUSED", "MOE_OPT_FFN_TIMEOUT_SELFTEST", "MOE_OPT_PDL",
+    "MoEError", "lib", "library_path", "MoEStats", "moe_check", "moe_error_word", "EXPORTED_SYMBOLS",
+    # the seven calls of the layer step
+    "moe_route", "moe_stats_update", "moe_predict", "moe_replicate", "moe_dispatch", "moe_expert_ffn",
+    "moe_combine",
+    # fused forms
+    "moe_layer_front", "moe_expert_ffn_gather", "moe_expert_ffn_combine", "moe_dispatch_noalloc",
+    # prediction-driven and physical replication
+    "moe_predict_decay", "moe_replicate_predicted", "moe_replicate_weights", "moe_expert_ffn_slots",
+    # backward
+    "moe_ffn_backward", "moe_ffn_backward_workspace_bytes", "moe_route_backward",
+    "MOE_BWD_ACCUMULATE_WGRAD", "MOE_BWD_WGRAD_BF16",
+    # sizes, options, constants
+    "workspace_bytes", "moe_ffn_launches", "moe_set_option", "moe_get_option",
+    "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_OP_LAYER_FRONT", "MOE_OP_EXPERT_FFN_COMBINE",
+    "MOE_ACT_GELU", "MOE_ACT_SWIGLU", "MOE_OPT_FFN_KERNEL", "MOE_FFN_KERNEL_AUTO", "MOE_FFN_KERNEL_SINGLE",
+    "MOE_FFN_KERNEL_PAIR", "MOE_FFN_KERNEL_FUSED", "MOE_OPT_FFN_TIMEOUT_SELFTEST", "MOE_OPT_PDL",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
