@@ -77,6 +77,9 @@ struct Args {
   uint32_t* ring_c;
   unsigned long long* csum;
   int32_t* hist_out;
+  // deferred = 1: the co-selection window fold and the prediction are left
+  // to stats_tail_kernel (launched beside the scatter/copy), not the plan
+  int deferred;
   // prediction (p_seq == null: skipped); pred_csum null for the last layer
   const unsigned long long* pred_csum;
   float* p_seq;
@@ -97,6 +100,25 @@ struct Args {
   int32_t* info;     // [4][E]: expert base, replicas, rows, loads from rep_share
   int32_t* group_offsets;
 };
+
+// The layer's co-selection counts into window ring slot and sums (pair j-1, j).
+__device__ __forceinline__ void fold_cosel(const Args& a) {
+  for (int i = threadIdx.x; i < a.E * a.E; i += kThreads) {
+    const uint32_t nw = atomicExch(a.acc_c + i, 0u);
+    const uint32_t old = a.ring_c[i];
+    a.ring_c[i] = nw;
+    a.csum[i] = a.csum[i] + nw - old;
+  }
+}
+
+// The part of the plan that the dispatch does not wait for: the co-selection
+// window fold and the prediction for the next layer (one block, after the
+// route/plan kernel, beside the scatter/copy).
+__global__ void __launch_bounds__(kThreads) stats_tail_kernel(Args a) {
+  if (a.has_prev) fold_cosel(a);
+  __syncthreads();
+  if (a.p_seq) stats::predict_block<unsigned long long>(a.hsum, a.pred_csum, a.E, a.p_seq, a.cond, a.p_next);
+}
 
 template <int G, bool VEC>
 __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
@@ -197,16 +219,11 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
     a.hsum[e] = a.hsum[e] + (uint32_t)h - old;
     if (a.hist_out) a.hist_out[e] = h;
   }
-  if (cos) {
-    for (int i = threadIdx.x; i < E * E; i += kThreads) {
-      const uint32_t nw = atomicExch(a.acc_c + i, 0u);
-      const uint32_t old = a.ring_c[i];
-      a.ring_c[i] = nw;
-      a.csum[i] = a.csum[i] + nw - old;
-    }
+  if (!a.deferred) {
+    if (cos) fold_cosel(a);
+    __syncthreads();
+    if (a.p_seq) stats::predict_block<unsigned long long>(a.hsum, a.pred_csum, E, a.p_seq, a.cond, a.p_next);
   }
-  __syncthreads();
-  if (a.p_seq) stats::predict_block<unsigned long long>(a.hsum, a.pred_csum, E, a.p_seq, a.cond, a.p_next);
   __syncthreads();
   const long long A = (long long)a.T * k;
   if (a.replicate) {
@@ -410,9 +427,15 @@ static cudaError_t launch_route_g(const Args& a, bool vec, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// side != null: the co-selection fold and the prediction run in
+// stats_tail_kernel on `side`, forked after the route/plan kernel through
+// fork_ev and joined back into `st` after the scatter/copy through join_ev.
 static cudaError_t launch(const Args& a0, const uint16_t* x, int H, uint16_t* xp, int32_t* perm, int32_t* inv_perm,
-                          cudaStream_t st) {
+                          cudaStream_t st, cudaStream_t side = nullptr, cudaEvent_t fork_ev = nullptr,
+                          cudaEvent_t join_ev = nullptr) {
   Args a = a0;
+  const bool tail = side != nullptr && (a.has_prev || a.p_seq != nullptr);
+  a.deferred = tail ? 1 : 0;
   a.tiles_per_block = route_tiles_per_block(a.T, a.E);
   const bool vec = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.logits) & 15) == 0);
   cudaError_t e;
@@ -423,9 +446,21 @@ static cudaError_t launch(const Args& a0, const uint16_t* x, int H, uint16_t* xp
   else if (a.E <= 128) e = launch_route_g<16>(a, vec, st);
   else e = launch_route_g<32>(a, vec, st);
   if (e != cudaSuccess) return e;
+  if (tail) {
+    if ((e = cudaEventRecord(fork_ev, st)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(side, fork_ev, 0)) != cudaSuccess) return e;
+    stats_tail_kernel<<<1, kThreads, 0, side>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   const size_t smem = sizeof(int32_t) * ((size_t)(kWarps + 1) * a.E + (size_t)a.TT * a.k);
-  return launch_pdl(scatter_copy_kernel, dim3((unsigned)a.ntiles), dim3(kThreads), smem, st, a.idx, a.T, a.k, a.E,
-                    a.TT, a.tiles_per_block, a.counts, a.blk_tot, a.info, perm, inv_perm, x, H, xp);
+  e = launch_pdl(scatter_copy_kernel, dim3((unsigned)a.ntiles), dim3(kThreads), smem, st, a.idx, a.T, a.k, a.E,
+                 a.TT, a.tiles_per_block, a.counts, a.blk_tot, a.info, perm, inv_perm, x, H, xp);
+  if (tail) {
+    cudaError_t j = cudaEventRecord(join_ev, side);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(st, join_ev, 0);
+    if (e == cudaSuccess) e = j;
+  }
+  return e;
 }
 
 }  // namespace front
