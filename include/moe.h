@@ -15,7 +15,7 @@
  *   moe_combine       gate-weighted sum of each token's k expert outputs
  *
  * and two fused forms of the same work: moe_layer_front (route through
- * dispatch in two launches) and moe_expert_ffn_gather (the FFN reading the
+ * dispatch in three launches) and moe_expert_ffn_gather (the FFN reading the
  * token rows in place, so that dispatch writes only the permutation).
  *
  * Conventions
@@ -236,7 +236,7 @@ moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int
 
 /* ---------------------------------------------------------------------------
  * moe_layer_front -- route, statistics, prediction, replicas and dispatch of one
- * layer in two launches.
+ * layer in three launches (one of them on the library's side stream).
  * The same results, bit for bit, as
  *   moe_route(logits) -> moe_stats_update(st, iter, layer, idx, idx_prev) ->
  *   moe_predict(st, layer) [when p_seq != NULL] -> moe_replicate(hist, T*k)
@@ -258,8 +258,12 @@ moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int
  * hottest experts first).  The tokens are still dispatched by their actual
  * choices, split over the replica groups of their expert.
  * The first launch routes tiles of tokens and counts them; its last block
- * folds the window, predicts, replicates and lays out the groups; the second
- * scatters the permutation and copies the rows.  E must equal the handle's E.
+ * folds the histogram into the window, replicates and lays out the groups;
+ * the second scatters the permutation and copies the rows.  When there is a
+ * previous layer's choice or a prediction to make, a third launch, one block
+ * on the library's side stream (forked after the first launch, joined back
+ * into `stream` after the second), folds the co-selection counts and
+ * predicts.  E must equal the handle's E.
  * ------------------------------------------------------------------------- */
 moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E, int k, int H, int renorm,
                            moe_stats* st, int64_t iter, int layer, const int32_t* idx_prev, int replicate,

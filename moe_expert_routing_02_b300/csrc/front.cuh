@@ -1,5 +1,5 @@
 // Fused front of the layer: top-k gate, token statistics and window, next-layer
-// prediction, replica counts and the dispatch, in two launches.
+// prediction, replica counts and the dispatch, in three launches.
 //
 // Same results as moe_route -> moe_stats_update -> moe_predict ->
 // moe_replicate -> moe_dispatch (PopFetcher review: gate, Routing Information
@@ -15,9 +15,10 @@
 //      accumulator).  The last block to finish (ticket after a fence) then,
 //      alone:
 //        - takes the histogram from the accumulator,
-//        - folds histogram and co-selection counts into the window ring and
-//          sums (as stats::update_kernel does),
-//        - predicts the next layer (stats::predict_block),
+//        - folds the histogram into the window ring and sums, and, unless
+//          they are deferred to F3, the co-selection counts (as
+//          stats::update_kernel does) and the prediction of the next layer
+//          (stats::predict_block),
 //        - computes replica counts (replicate::replicate_block) from the
 //          histogram, or from the apportionment of a predicted popularity
 //          (replicate::apportion_block) when one is given,
@@ -27,6 +28,9 @@
 //      prefix within its block), stable in-tile ranks -> slots -> perm /
 //      inv_perm, then the rows of the tile's assignments are copied to their
 //      slots with 16-byte vectors.
+//   F3 (stats_tail_kernel), one block on the side stream, forked after F1
+//      and joined after F2: the co-selection fold and the prediction, which
+//      the dispatch does not read, run beside F2 instead of inside the plan.
 // The plan (last block) thus reads O(E) and O(E^2) values only; the
 // per-tile prefix over the route blocks is spread over the F2 blocks.
 // Counts are integers, so nothing depends on the order of atomics.

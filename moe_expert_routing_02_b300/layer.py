@@ -20,6 +20,13 @@ from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_EXPERT_FFN_COMBINE, MO
 __all__ = ["MoELayerStep", "MoESaved", "ChunkedLayerStep", "HostPipeline"]
 
 
+def _front_launches(layer: int, predict: bool) -> int:
+    """Kernels moe_layer_front launches: route/plan and scatter/copy, plus the
+    co-selection fold and prediction on the side stream when there is a
+    previous layer's choice or a prediction to make."""
+    return 2 + (1 if layer > 0 or predict else 0)
+
+
 class MoESaved:
     """What the backward of one layer keeps from its forward: the routing
     (idx, w), the dispatch (group offsets, the replica groups' experts or
@@ -38,7 +45,9 @@ class MoELayerStep:
     dispatch and the FFN (hot experts split into replica groups; the output is
     unchanged).  stats (MoEStats) is shared by all layers of a model.
     fused=True (needs stats) runs route, statistics, prediction, replicas and
-    dispatch as moe_layer_front (two launches); fused=False makes the five
+    dispatch as moe_layer_front (two launches, plus a third on the side stream
+    for the co-selection fold and prediction when layer > 0 or predict=True);
+    fused=False makes the five
     separate calls.  gather=True leaves the token rows in place: dispatch
     writes only the permutation and the FFN's first GEMM reads the rows of x
     through it (moe_expert_ffn_gather); gather=False copies the rows into
@@ -240,7 +249,8 @@ class MoELayerStep:
         dl = moe_route_backward(logits, saved.idx, dw, self.renorm, out=dlogits)
         return dx, dl, (dw1, dw3, dw2)
 
-    def launches(self, layer: int, L: int) -> int:
+    def launches(self, layer: int, L: int, predict: bool = True) -> int:
+        front = _front_launches(layer, predict)
         if self.physical:   # slot map + copy kernel per weight matrix, FFN over 2E-1 slots
             ffn = (moe_ffn_launches(self.A, 2 * self.E - 1, self.H, self.F, self.act, self.small, False)
                    + 2 * (3 if self.act == "swiglu" else 2))
@@ -248,10 +258,10 @@ class MoELayerStep:
             ffn = moe_ffn_launches(self.A, self.E, self.H, self.F, self.act, self.small, self.gather)
         if self.fuse_combine:  # the two-launch kernels (the fused one stores Y), the finalize pass, no combine
             ffn = moe_ffn_launches(self.A, self.E, self.H, self.F, self.act, self.small, True) + 1
-            return (2 if self.fused else 1 + 4 + (1 if self.stats is not None else 0)
+            return (front if self.fused else 1 + 4 + (1 if self.stats is not None else 0)
                     + (1 if self.stats is not None and layer < L - 1 else 0) + (1 if self.replicate else 0)) + ffn
         if self.fused:
-            return 2 + ffn + 1
+            return front + ffn + 1
         n = 1 + (3 if self.gather else 4) + ffn + 1
         if self.stats is not None:
             n += 1
@@ -367,9 +377,9 @@ class ChunkedLayerStep:
         self._cur ^= 1
         return out
 
-    def launches(self, layer: int, L: int) -> int:
+    def launches(self, layer: int, L: int, predict: bool = True) -> int:
         ffn = moe_ffn_launches(self.Tc * self.k, self.E, self.H, self.F, self.act, self.small, False)
-        return 2 + self.chunks * (4 + ffn + 1)
+        return _front_launches(layer, predict) + self.chunks * (4 + ffn + 1)
 
 
 class HostPipeline:
