@@ -61,8 +61,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     os.makedirs(os.path.dirname(STAMP), exist_ok=True)
     tmp = LIB + ".tmp"
-    cmd = [nvcc()] + FLAGS + ["-I", INCLUDE, "-o", tmp, os.path.join(CSRC, "moe_api.cu"), "-lcuda"
-                              if False else "-lcudart_static"]
+    cmd = [nvcc()] + FLAGS + ["-I", INCLUDE, "-o", tmp, os.path.join(CSRC, "moe_api.cu"), "-lcudart_static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     log = r.stdout + r.stderr
     with open(os.path.join(os.path.dirname(STAMP), "libmoe.build.log"), "w") as f:

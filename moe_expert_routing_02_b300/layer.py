@@ -259,13 +259,14 @@ class MoELayerStep:
         if self.fuse_combine:  # the two-launch kernels (the fused one stores Y), the finalize pass, no combine
             ffn = moe_ffn_launches(self.A, self.E, self.H, self.F, self.act, self.small, True) + 1
             return (front if self.fused else 1 + 4 + (1 if self.stats is not None else 0)
-                    + (1 if self.stats is not None and layer < L - 1 else 0) + (1 if self.replicate else 0)) + ffn
+                    + (1 if self.stats is not None and predict and layer < L - 1 else 0)
+                    + (1 if self.replicate else 0)) + ffn
         if self.fused:
             return front + ffn + 1
         n = 1 + (3 if self.gather else 4) + ffn + 1
         if self.stats is not None:
             n += 1
-            if layer < L - 1:
+            if predict and layer < L - 1:
                 n += 1
         if self.replicate:
             n += 1
