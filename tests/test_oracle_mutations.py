@@ -193,6 +193,143 @@ def _router_bwd_no_centering(logits, idx, dw, renorm=True):
     return out
 
 
+def _topk_full_softmax_always(logits, k, renorm=True):
+    return ORIG["topk_gate"](logits, k, False)
+
+
+def _topk_renorm_always(logits, k, renorm=True):
+    return ORIG["topk_gate"](logits, k, True)
+
+
+def _hist_first_choice_only(idx, E):
+    return np.bincount(np.asarray(idx)[:, 0].astype(np.int64), minlength=E).astype(np.int64)
+
+
+def _cosel_same_rank_only(a, b, E):
+    a = np.asarray(a).astype(np.int64)
+    b = np.asarray(b).astype(np.int64)
+    C = np.zeros((E, E), np.int64)
+    for r in range(min(a.shape[1], b.shape[1])):
+        np.add.at(C, (a[:, r], b[:, r]), 1)
+    return C
+
+
+def _update_accumulates(self, it, layer, idx_layer, idx_prev=None):
+    # the ring slot is added to instead of replaced
+    slot = it % self.s
+    h = O.histogram(idx_layer, self.E)
+    self.h[layer, slot] += h
+    if layer > 0:
+        self.C[layer - 1, slot] += O.coselection(idx_prev, idx_layer, self.E)
+    return h
+
+
+def _update_window_one_short(self, it, layer, idx_layer, idx_prev=None):
+    # a ring of s - 1 slots
+    slot = it % max(self.s - 1, 1)
+    h = O.histogram(idx_layer, self.E)
+    self.h[layer, slot] = h
+    if layer > 0:
+        self.C[layer - 1, slot] = O.coselection(idx_prev, idx_layer, self.E)
+    return h
+
+
+def _predict_unseen_rows_zero(self, layer):
+    p, c, n = ORIG["predict"](self, layer)
+    if c is None:
+        return p, c, n
+    rows = self.window_cosel(layer).sum(axis=1)
+    c = c.copy()
+    c[rows == 0] = 0.0
+    return p, c, p @ c
+
+
+def _replicate_no_cap(load, total, thresh_num=6, thresh_den=5, max_copies=-1):
+    return ORIG["replicate"](load, total, thresh_num, thresh_den, -1)
+
+
+def _replicate_no_minus_one(load, total, thresh_num=6, thresh_den=5, max_copies=-1):
+    E = len(load)
+    copies = []
+    for ld in load:
+        c = math.ceil(ld * E / total) if ld * E * thresh_den > thresh_num * total else 0
+        copies.append(min(c, max_copies) if max_copies >= 0 else c)
+    return _tables(copies)
+
+
+def _dispatch_groups_reversed(idx, E, rep_base=None):
+    go, perm, _ = ORIG["dispatch"](idx, E, rep_base)
+    perm = perm.copy()
+    for g in range(len(go) - 1):
+        perm[go[g]:go[g + 1]] = perm[go[g]:go[g + 1]][::-1]
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size, dtype=perm.dtype)
+    return go, perm, inv
+
+
+def _gather_mod_k(x, perm, k):
+    return np.asarray(x)[np.asarray(perm).astype(np.int64) % k]
+
+
+def _bf16_shift15(bits):
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 15).view(np.float32).astype(np.float64)
+
+
+def _silu_negated_gate(z):
+    return z / (1.0 + np.exp(z))
+
+
+def _combine_unweighted(y, inv_perm, w):
+    return ORIG["combine"](y, inv_perm, np.ones_like(np.asarray(w, np.float64)))
+
+
+def _replicate_predicted_no_budget(p32, total, thresh_num=6, thresh_den=5, max_copies=-1, budget=-1):
+    return ORIG["replicate_predicted"](p32, total, thresh_num, thresh_den, max_copies, -1)
+
+
+def _load_error_unnormalised(p_pred, load_actual):
+    return float(np.mean(np.abs(np.asarray(p_pred, np.float64) - np.asarray(load_actual, np.float64))))
+
+
+def _router_bwd_full_no_centering(logits, idx, dw, renorm=True):
+    if renorm:
+        return ORIG["router_backward"](logits, idx, dw, renorm)
+    l = np.asarray(logits, np.float64)
+    idx = np.asarray(idx).astype(np.int64)
+    out = np.zeros_like(l)
+    for t in range(l.shape[0]):
+        z = np.exp(l[t] - l[t].max())
+        p = z / z.sum()
+        g = np.zeros(l.shape[1])
+        g[idx[t]] = np.asarray(dw, np.float64)[t]
+        out[t] = p * g
+    return out
+
+
+def _ffn_bwd_up_from_gate_preact(x, experts, w1, w3, w2, act, dy):
+    # SwiGLU: du taken as dA * g (the gate's pre-activation) instead of dA * silu(g)
+    if act != "swiglu":
+        return ORIG["expert_ffn_backward_f64"](x, experts, w1, w3, w2, act, dy)
+    x, dy = np.asarray(x, np.float64), np.asarray(dy, np.float64)
+    w1, w3, w2 = (np.asarray(w, np.float64) for w in (w1, w3, w2))
+    experts = np.asarray(experts).astype(np.int64)
+    dx, dw1, dw3, dw2 = np.zeros_like(x), np.zeros_like(w1), np.zeros_like(w3), np.zeros_like(w2)
+    for e in np.unique(experts):
+        rows = np.nonzero(experts == e)[0]
+        xe, dye = x[rows], dy[rows]
+        g, u = xe @ w1[e], xe @ w3[e]
+        a = O._silu(g) * u
+        dA = dye @ w2[e].T
+        dg = dA * u * O._silu_grad(g)
+        du = dA * g
+        dw1[e] += xe.T @ dg
+        dw3[e] += xe.T @ du
+        dw2[e] += a.T @ dye
+        dx[rows] = dg @ w1[e].T + du @ w3[e].T
+    return dx, dw1, dw3, dw2
+
+
 ORIG = {
     "topk_gate": O.topk_gate,
     "coselection": O.coselection,
@@ -202,6 +339,11 @@ ORIG = {
     "predict_decay": O.WindowStats.predict_decay,
     "combine_backward": O.combine_backward,
     "scatter_sum": O.scatter_sum,
+    "replicate": O.replicate,
+    "dispatch": O.dispatch,
+    "replicate_predicted": O.replicate_predicted,
+    "router_backward": O.router_backward,
+    "expert_ffn_backward_f64": O.expert_ffn_backward_f64,
 }
 
 MUTANTS = [
@@ -227,6 +369,27 @@ MUTANTS = [
     ("combine_backward", _combine_bwd_unweighted, [PB.test_combine_backward_matches_finite_differences]),
     ("scatter_sum", _scatter_sum_perm, [PB.test_scatter_sum_is_the_adjoint_of_the_row_copy]),
     ("router_backward", _router_bwd_no_centering, [lambda: PB.test_router_backward_matches_finite_differences(True)]),
+    ("topk_gate", _topk_full_softmax_always, [P.test_gate_weights_closed_forms]),
+    ("topk_gate", _topk_renorm_always, [P.test_gate_weights_closed_forms]),
+    ("histogram", _hist_first_choice_only, [P.test_histogram_brute_force_and_sum]),
+    ("coselection", _cosel_same_rank_only, [P.test_coselection_sums_and_brute_force]),
+    ("WindowStats.update", _update_accumulates, [P.test_window_keeps_last_s_iterations]),
+    ("WindowStats.update", _update_window_one_short, [P.test_window_keeps_last_s_iterations]),
+    ("WindowStats.predict", _predict_unseen_rows_zero, [P.test_window_empty_and_unseen_rows]),
+    ("replicate", _replicate_no_cap, [P.test_replicate_hand_tables]),
+    ("replicate", _replicate_no_minus_one, [P.test_replicate_hand_tables, P.test_replicate_bound_and_float_rule]),
+    ("dispatch", _dispatch_groups_reversed, [P.test_dispatch_hand_case, lambda: P.test_dispatch_properties(True)]),
+    ("gather_rows", _gather_mod_k, [P.test_layer_replication_invariance]),
+    ("bf16_to_f64", _bf16_shift15, [P.test_ffn_closed_form_values]),
+    ("_silu", _silu_negated_gate, [P.test_ffn_closed_form_values]),
+    ("combine", _combine_unweighted, [P.test_combine_hand_case]),
+    ("replicate_predicted", _replicate_predicted_no_budget,
+     [PP.test_replicate_predicted_reduces_to_replicate_on_exact_shares]),
+    ("load_proportion_error", _load_error_unnormalised, [PP.test_quality_hand_cases]),
+    ("router_backward", _router_bwd_full_no_centering,
+     [lambda: PB.test_router_backward_matches_finite_differences(False)]),
+    ("expert_ffn_backward_f64", _ffn_bwd_up_from_gate_preact,
+     [lambda: PB.test_ffn_backward_matches_finite_differences("swiglu")]),
 ]
 
 
