@@ -560,7 +560,7 @@ moe_status moe_get_option(int option, int* value /* host */);
 /* Kernel launches one moe_expert_ffn (gather = 0) or moe_expert_ffn_gather
  * (gather = 1) call makes under the current options: 1 (fused) or 2 grouped
  * launches, plus 2 small-batch launches when small_group_threshold > 0.
- * 0 for bad sizes.  Host only. */
+ * 0 for sizes, activations or thresholds the FFN refuses.  Host only. */
 int moe_ffn_launches(int A, int E, int H, int F, int act, int small_group_threshold, int gather);
 
 /* Workspace bytes for op (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT or

@@ -945,7 +945,9 @@ moe_status moe_replicate_weights(const int32_t* rep_base, int E, uint16_t* w_all
 }
 
 int moe_ffn_launches(int A, int E, int H, int F, int act, int small_group_threshold, int gather) {
-  if (A <= 0 || E < 1 || E > ffn::MAX_G || H < 64 || F < 64) return 0;
+  // the sizes moe_expert_ffn accepts; anything it refuses launches nothing
+  if (A <= 0 || E < 1 || E > ffn::MAX_G || H < 64 || H % 64 || F < 64 || F % 64) return 0;
+  if ((act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) || small_group_threshold < 0) return 0;
   bool use_pair = false, use_fused = false;
   ffn_choice(A, E, H, F, act, gather != 0, &use_pair, &use_fused);
   return (use_fused ? 1 : 2) + (small_group_threshold > 0 ? 2 : 0);

@@ -147,3 +147,123 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(M, "library_path", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         M.lib()
+
+
+ALIGN16_NOT_256 = P(0x10010)
+
+
+def test_fused_and_prediction_calls_reject_bad_arguments(L):
+    inv = M.MOE_ERR_INVALID
+    # moe_layer_front: a stats handle is required (its own checks need it)
+    front = [FAKE, FAKE, 16, 8, 2, 64, 1, NULL, 0, 0, NULL, 1, 6, 5, -1, NULL, -1] + [FAKE] * 14 + [1 << 20, NULL]
+    assert L.moe_layer_front(*front) == inv
+    assert b"stats handle" in L.moe_last_error()
+    assert L.moe_predict_decay(NULL, 0, 0, 0.5, FAKE, NULL, NULL, NULL) == inv
+    rp = L.moe_replicate_predicted
+    ok = [FAKE, 16, 1000, 6, 5, -1, -1, FAKE, FAKE, FAKE, FAKE, NULL]
+    for pos, bad in ((1, 0), (1, 257), (2, 0), (2, 1 << 29), (3, 0), (4, 1025), (5, -2), (6, -2), (0, NULL),
+                     (8, NULL)):
+        a = list(ok); a[pos] = bad
+        assert rp(*a) == inv, (pos, bad)
+    nd = L.moe_dispatch_noalloc
+    assert nd(NULL, FAKE, -1, 2, 64, 8, NULL, FAKE, FAKE, FAKE, NULL, NULL) == inv
+    assert nd(NULL, FAKE, 16, 9, 64, 16, NULL, FAKE, FAKE, FAKE, NULL, NULL) == inv
+    assert nd(NULL, FAKE, 1 << 17, 8, 64, 256, NULL, FAKE, FAKE, FAKE, NULL, NULL) == M.MOE_ERR_WORKSPACE
+
+
+def test_ffn_variants_reject_bad_arguments(L):
+    inv = M.MOE_ERR_INVALID
+    gel, swi = M.MOE_ACT_GELU, M.MOE_ACT_SWIGLU
+    # moe_expert_ffn_gather(x, T, perm, k, go, ge, rb, E, w1, w3, w2, H, F, act, small, y, ws, ws_bytes, stream)
+    g = L.moe_expert_ffn_gather
+    ok = [FAKE, 16, FAKE, 2, FAKE, NULL, NULL, 8, FAKE, NULL, FAKE, 64, 128, gel, 64, FAKE, FAKE, 1 << 30, NULL]
+    for pos, bad in ((3, 0), (3, 9), (7, 1), (7, 300), (0, NULL), (2, NULL), (1, -1), (11, 96), (12, 100),
+                     (13, 7), (14, -1), (13, swi), (15, NULL), (16, NULL), (8, MISALIGNED)):
+        a = list(ok); a[pos] = bad
+        assert g(*a) == inv, (pos, bad)
+    a = list(ok); a[1] = 1 << 28; a[3] = 8
+    assert g(*a) == inv                                   # T*k >= 2^31
+    a = list(ok); a[17] = 64
+    assert g(*a) == M.MOE_ERR_WORKSPACE
+    a = list(ok); a[1] = 0
+    assert g(*a) == M.MOE_OK                              # empty batch: nothing enqueued
+    # moe_expert_ffn_combine(xp, go, ge, rb, E, perm, w, T, k, w1, w3, w2, H, F, act, small, out, ws, ws_bytes, st)
+    c = L.moe_expert_ffn_combine
+    ok = [FAKE, FAKE, NULL, NULL, 8, FAKE, FAKE, 16, 2, FAKE, NULL, FAKE, 64, 128, gel, 64, FAKE, FAKE, 1 << 30,
+          NULL]
+    for pos, bad in ((4, 0), (4, 257), (8, 0), (8, 9), (7, -1), (12, 100), (13, 32), (5, NULL), (6, NULL),
+                     (16, NULL), (17, NULL), (16, MISALIGNED), (17, ALIGN16_NOT_256), (0, NULL), (14, 7),
+                     (14, swi)):
+        a = list(ok); a[pos] = bad
+        assert c(*a) == inv, (pos, bad)
+    a = list(ok); a[18] = 256
+    assert c(*a) == M.MOE_ERR_WORKSPACE
+    a = list(ok); a[7] = 0
+    assert c(*a) == M.MOE_OK
+    # moe_expert_ffn_slots(xp, go, group_slot, G, n_slots, A, w1, w3, w2, H, F, act, small, y, ws, ws_bytes, st)
+    s = L.moe_expert_ffn_slots
+    ok = [FAKE, FAKE, FAKE, 9, 15, 32, FAKE, NULL, FAKE, 64, 128, gel, 64, FAKE, FAKE, 1 << 30, NULL]
+    for pos, bad in ((2, NULL), (3, 0), (4, 0), (5, -1), (9, 32), (11, 5), (0, NULL)):
+        a = list(ok); a[pos] = bad
+        assert s(*a) == inv, (pos, bad)
+    a = list(ok); a[5] = 0
+    assert s(*a) == M.MOE_OK
+    # moe_replicate_weights(rep_base, E, w_all, rows, cols, group_slot, stream)
+    r = L.moe_replicate_weights
+    assert r(FAKE, 0, FAKE, 64, 64, NULL, NULL) == inv
+    assert r(NULL, 8, FAKE, 64, 64, NULL, NULL) == inv
+    assert r(FAKE, 8, FAKE, 3, 4, NULL, NULL) == inv       # rows*cols not a multiple of 8
+    assert r(FAKE, 8, FAKE, 0, 64, NULL, NULL) == inv
+    assert r(FAKE, 8, MISALIGNED, 64, 64, NULL, NULL) == inv
+
+
+def test_backward_calls_reject_bad_arguments(L):
+    inv = M.MOE_ERR_INVALID
+    gel, swi = M.MOE_ACT_GELU, M.MOE_ACT_SWIGLU
+    wsb = L.moe_ffn_backward_workspace_bytes
+    assert wsb(16, 2, 8, 96, 128) == 0 and wsb(16, 0, 8, 64, 128) == 0 and wsb(16, 2, 300, 64, 128) == 0
+    assert 0 < wsb(16, 2, 8, 64, 128) < wsb(4096, 2, 8, 64, 128)
+    need = wsb(16, 2, 8, 64, 128)
+    # moe_ffn_backward(x, dout, w, y, perm, inv, T, k, go, ge, E, w1, w3, w2, H, F, act, dx, dw, dw1, dw3, dw2,
+    #                  flags, ws, ws_bytes, stream)
+    b = L.moe_ffn_backward
+    ok = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 2, FAKE, NULL, 8, FAKE, NULL, FAKE, 64, 128, gel, FAKE, FAKE,
+          FAKE, NULL, FAKE, 0, FAKE, 1 << 30, NULL]
+    for pos, bad in ((6, -1), (7, 0), (7, 9), (10, 1), (10, 300), (14, 96), (15, 100), (16, 7), (22, 4),
+                     (22, M.MOE_BWD_ACCUMULATE_WGRAD | M.MOE_BWD_WGRAD_BF16), (8, NULL), (11, NULL), (13, NULL),
+                     (19, NULL), (21, NULL), (23, NULL), (16, swi), (0, NULL), (1, NULL), (2, NULL), (4, NULL),
+                     (5, NULL), (17, NULL), (18, NULL), (0, MISALIGNED), (17, MISALIGNED), (19, MISALIGNED),
+                     (23, ALIGN16_NOT_256)):
+        a = list(ok); a[pos] = bad
+        assert b(*a) == inv, (pos, bad)
+    a = list(ok); a[24] = need - 1
+    assert b(*a) == M.MOE_ERR_WORKSPACE
+    # moe_route_backward(logits, idx, dw, T, E, k, renorm, dlogits, stream)
+    rb = L.moe_route_backward
+    ok = [FAKE, FAKE, FAKE, 16, 8, 2, 1, FAKE, NULL]
+    for pos, bad in ((3, -1), (4, 0), (4, 257), (5, 0), (5, 9), (0, NULL), (1, NULL), (2, NULL), (7, NULL)):
+        a = list(ok); a[pos] = bad
+        assert rb(*a) == inv, (pos, bad)
+    a = list(ok); a[3] = 0
+    assert rb(*a) == M.MOE_OK
+
+
+def test_ffn_launch_count_rule(L):
+    """The FFN's launch count under the default options: the fused kernel
+    (one launch) for CTA-pair-sized batches of experts of at most 16 MB, two
+    GEMM launches otherwise (the gather path, larger experts, small batches),
+    plus the two small-batch launches when the threshold is positive."""
+    n = L.moe_ffn_launches
+    gel, swi = M.MOE_ACT_GELU, M.MOE_ACT_SWIGLU
+    assert n(32768, 16, 1024, 2048, gel, 64, 0) == 3        # 8 MB experts: fused
+    assert n(32768, 16, 1024, 2048, gel, 0, 0) == 1
+    assert n(32768, 16, 1024, 2048, gel, 64, 1) == 4        # gather: two GEMM launches
+    assert n(32768, 16, 1024, 8192, gel, 64, 0) == 4        # 32 MB experts
+    assert n(32768, 16, 1024, 2048, swi, 64, 0) == 3        # 12 MB
+    assert n(32768, 16, 1024, 4096, swi, 64, 0) == 4        # 24 MB
+    assert n(1000, 16, 1024, 2048, gel, 64, 0) == 4         # A < 256 E: single-CTA GEMMs
+    assert n(0, 16, 1024, 2048, gel, 64, 0) == 0
+    assert n(32768, 16, 96, 2048, gel, 64, 0) == 0
+    assert n(32768, 16, 1024, 2000, gel, 64, 0) == 0
+    assert n(32768, 16, 1024, 2048, 7, 64, 0) == 0
+    assert n(32768, 16, 1024, 2048, gel, -1, 0) == 0
