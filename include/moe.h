@@ -33,11 +33,16 @@
  *   work on `stream` and returns; none synchronises except moe_check,
  *   moe_stats_export and moe_stats_import.  Calls that share a moe_stats
  *   handle or a workspace must be ordered on one stream.  The expert FFN
- *   runs its small-batch kernels on a library-owned stream per device
+ *   (its small-batch kernels) and moe_layer_front (its co-selection fold and
+ *   prediction) run part of their work on a library-owned stream per device
  *   (created with two events at the first call on that device, kept for the
  *   life of the process), forked from `stream` and joined back to it within
- *   the call, so callers see ordinary stream order; FFN calls on different
- *   streams share that side stream.
+ *   the call, so callers see ordinary stream order; calls on different
+ *   streams share that side stream (one fork/join at a time).  Under CUDA
+ *   graph capture the side stream joins the capture through the fork event
+ *   and stays part of it until the capture ends, so while one thread captures
+ *   these calls no other thread may enqueue them on the same device; make the
+ *   first call on a device before capturing (it creates the side stream).
  *
  * Errors
  *   Every call returns a moe_status.  Arguments are validated on the host
