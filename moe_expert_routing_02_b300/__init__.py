@@ -151,6 +151,16 @@ def _dev(t, dtype, name, ndim=None):
     return t
 
 
+def _out(t, dtype, name, numel, ndim=None):
+    """A caller-provided output (or an input read by index): a contiguous
+    CUDA tensor of `dtype` with room for at least `numel` elements, since
+    the kernels reach it through a raw pointer."""
+    _dev(t, dtype, name, ndim)
+    if t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements; the call needs {numel}")
+    return t
+
+
 def workspace_bytes(op: int, T: int, k: int, E: int, H: int = 64, F: int = 64) -> int:
     return int(lib().moe_workspace_bytes(op, T, k, E, H, F))
 
@@ -165,8 +175,8 @@ def moe_route(logits, k: int, renorm: bool = True, idx=None, w=None, stream=None
         idx = torch.empty((T, k), dtype=torch.int32, device=logits.device)
     if w is None:
         w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
-    _dev(idx, torch.int32, "idx")
-    _dev(w, torch.float32, "w")
+    _out(idx, torch.int32, "idx", T * k)
+    _out(w, torch.float32, "w", T * k)
     _check(lib().moe_route(_ptr(logits), T, E, k, int(bool(renorm)), _ptr(idx), _ptr(w), _stream(stream)),
            "moe_route")
     return idx, w
@@ -235,7 +245,7 @@ def moe_stats_update(stats: MoEStats, it: int, layer: int, idx_layer, idx_prev=N
         if tuple(idx_prev.shape) != (T, k):
             raise ValueError("idx_prev must match idx_layer's shape")
     if hist_out is not None:
-        _dev(hist_out, torch.int32, "hist_out")
+        _out(hist_out, torch.int32, "hist_out", stats.E)
     _check(lib().moe_stats_update(stats.handle, int(it), int(layer), _ptr(idx_layer), _ptr(idx_prev), T, k,
                                   _ptr(hist_out), _stream(stream)), "moe_stats_update")
     return hist_out
@@ -258,11 +268,11 @@ def moe_predict(stats: MoEStats, layer: int, want_cond: bool = True, want_next: 
         p_next = torch.empty(E, dtype=torch.float32, device=device) if (want_next and not last) else None
     else:
         p_seq, cond, p_next = out
-        _dev(p_seq, torch.float32, "p_seq")
+        _out(p_seq, torch.float32, "p_seq", E)
         if cond is not None:
-            _dev(cond, torch.float32, "cond")
+            _out(cond, torch.float32, "cond", E * E)
         if p_next is not None:
-            _dev(p_next, torch.float32, "p_next")
+            _out(p_next, torch.float32, "p_next", E)
     _check(lib().moe_predict(stats.handle, int(layer), _ptr(p_seq), _ptr(cond), _ptr(p_next), _stream(stream)),
            "moe_predict")
     return p_seq, cond, p_next
@@ -277,13 +287,18 @@ def moe_predict_decay(stats: "MoEStats", layer: int, it: int, lam: float, want_c
     last = layer == stats.L - 1
     if want_next is None:
         want_next = not last
-    dev = torch.device("cuda", torch.cuda.current_device())
     if out is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
         p_seq = torch.empty(E, dtype=torch.float32, device=dev)
         cond = torch.empty((E, E), dtype=torch.float32, device=dev) if (want_cond and not last) else None
         p_next = torch.empty(E, dtype=torch.float32, device=dev) if (want_next and not last) else None
     else:
         p_seq, cond, p_next = out
+        _out(p_seq, torch.float32, "p_seq", E)
+        if cond is not None:
+            _out(cond, torch.float32, "cond", E * E)
+        if p_next is not None:
+            _out(p_next, torch.float32, "p_next", E)
     _check(lib().moe_predict_decay(stats.handle, int(layer), int(it), float(lam), _ptr(p_seq), _ptr(cond),
                                    _ptr(p_next), _stream(stream)), "moe_predict_decay")
     return p_seq, cond, p_next
@@ -303,6 +318,8 @@ def moe_replicate_predicted(p_next, total: int, thresh=(6, 5), max_copies: int =
                torch.empty(E + 1, dtype=torch.int32, device=p_next.device),
                torch.empty(2 * E, dtype=torch.int32, device=p_next.device))
     load, copies, rb, ge = out
+    for nm, t, n in (("load", load, E), ("copies", copies, E), ("rep_base", rb, E + 1), ("group_expert", ge, 2 * E)):
+        _out(t, torch.int32, nm, n)
     _check(lib().moe_replicate_predicted(_ptr(p_next), E, int(total), int(thresh[0]), int(thresh[1]),
                                          int(max_copies), int(budget), _ptr(load), _ptr(copies), _ptr(rb), _ptr(ge),
                                          _stream(stream)), "moe_replicate_predicted")
@@ -319,9 +336,20 @@ def moe_replicate(load, total: int, thresh=(6, 5), max_copies: int = -1, out=Non
                torch.empty(E + 1, dtype=torch.int32, device=load.device),
                torch.empty(2 * E, dtype=torch.int32, device=load.device))
     copies, rep_base, group_expert = out
+    for nm, t, n in (("copies", copies, E), ("rep_base", rep_base, E + 1), ("group_expert", group_expert, 2 * E)):
+        _out(t, torch.int32, nm, n)
     _check(lib().moe_replicate(_ptr(load), E, int(total), int(thresh[0]), int(thresh[1]), int(max_copies),
                                _ptr(copies), _ptr(rep_base), _ptr(group_expert), _stream(stream)), "moe_replicate")
     return copies, rep_base, group_expert
+
+
+def _dispatch_outputs(go, perm, inv, xp, E, A, H):
+    torch = _torch()
+    _out(go, torch.int32, "group_offsets", 2 * E + 1)
+    _out(perm, torch.int32, "perm", A)
+    _out(inv, torch.int32, "inv_perm", A)
+    if xp is not None:
+        _out(xp, torch.bfloat16, "xp", A * H)
 
 
 def moe_dispatch(x, idx, E: int, rep_base=None, out=None, workspace=None, stream=None):
@@ -347,6 +375,7 @@ def moe_dispatch(x, idx, E: int, rep_base=None, out=None, workspace=None, stream
                torch.empty(A, dtype=torch.int32, device=dev),
                None if x is None else torch.empty((A, H), dtype=torch.bfloat16, device=dev))
     go, perm, inv, xp = out
+    _dispatch_outputs(go, perm, inv, xp, E, A, H)
     need = workspace_bytes(MOE_OP_DISPATCH, T, k, E)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
@@ -368,6 +397,8 @@ def moe_dispatch_noalloc(x, idx, E: int, rep_base=None, out=None, stream=None):
     if x is not None:
         _dev(x, torch.bfloat16, "x", 2)
         H = x.shape[1]
+        if x.shape[0] != T:
+            raise ValueError("x and idx disagree on T")
     if rep_base is not None:
         _dev(rep_base, torch.int32, "rep_base", 1)
     if out is None:
@@ -376,6 +407,7 @@ def moe_dispatch_noalloc(x, idx, E: int, rep_base=None, out=None, stream=None):
                torch.empty(A, dtype=torch.int32, device=dev),
                None if x is None else torch.empty((A, H), dtype=torch.bfloat16, device=dev))
     go, perm, inv, xp = out
+    _dispatch_outputs(go, perm, inv, xp, E, A, H)
     _check(lib().moe_dispatch_noalloc(_ptr(x), _ptr(idx), T, k, H, E, _ptr(rep_base), _ptr(go), _ptr(perm),
                                       _ptr(inv), _ptr(xp), _stream(stream)), "moe_dispatch_noalloc")
     return go, perm, inv, xp
@@ -400,15 +432,22 @@ def moe_layer_front(logits, x, stats: "MoEStats", it: int, layer: int, k: int, i
     if x is not None:
         _dev(x, torch.bfloat16, "x", 2)
         H = x.shape[1]
+        if x.shape[0] != T:
+            raise ValueError("x and logits disagree on T")
     if idx_prev is not None:
-        _dev(idx_prev, torch.int32, "idx_prev", 2)
+        _out(idx_prev, torch.int32, "idx_prev", T * k, 2)
     last = layer == stats.L - 1
     o = dict(out or {})
     i32, f32 = torch.int32, torch.float32
     def need(name, shape, dtype, cond=True):
-        if cond and o.get(name) is None:
+        if not cond:
+            return None
+        if o.get(name) is None:
             o[name] = torch.empty(shape, dtype=dtype, device=dev)
-        return o.get(name) if cond else None
+        n = 1
+        for d in shape:
+            n *= d
+        return _out(o[name], dtype, name, n)
     idx = need("idx", (T, k), i32)
     w = need("w", (T, k), f32)
     hist = need("hist", (E,), i32)
@@ -425,7 +464,7 @@ def moe_layer_front(logits, x, stats: "MoEStats", it: int, layer: int, k: int, i
     if workspace is None:
         workspace = torch.empty(max(workspace_bytes(MOE_OP_LAYER_FRONT, T, k, E), 16), dtype=torch.uint8, device=dev)
     if rep_share is not None:
-        _dev(rep_share, torch.float32, "rep_share", 1)
+        _out(rep_share, torch.float32, "rep_share", E, 1)
     _check(lib().moe_layer_front(_ptr(logits), _ptr(x), T, E, k, H, int(bool(renorm)), stats.handle, int(it),
                                  int(layer), _ptr(idx_prev), int(bool(replicate)), int(thresh[0]), int(thresh[1]),
                                  int(max_copies), _ptr(rep_share), int(budget), _ptr(idx), _ptr(w), _ptr(hist),
@@ -454,12 +493,13 @@ def moe_expert_ffn(xp, group_offsets, group_expert, rep_base, w1, w3, w2, act: s
         _dev(rep_base, torch.int32, "rep_base", 1)
     A, H = xp.shape
     E, H1, F = w1.shape
-    if H1 != H or tuple(w2.shape) != (E, F, H):
+    if H1 != H or tuple(w2.shape) != (E, F, H) or (w3 is not None and w3.shape != w1.shape):
         raise ValueError("weight shapes must be w1/w3 [E,H,F], w2 [E,F,H]")
+    _out(group_offsets, torch.int32, "group_offsets", (2 * E if group_expert is not None else E) + 1)
     act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
     if y is None:
         y = torch.empty((A, H), dtype=torch.bfloat16, device=xp.device)
-    _dev(y, torch.bfloat16, "y", 2)
+    _out(y, torch.bfloat16, "y", A * H, 2)
     need = int(lib().moe_workspace_bytes(MOE_OP_EXPERT_FFN, A, 1, E, H, F))
     if workspace is None:
         workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=xp.device)
@@ -488,14 +528,15 @@ def moe_expert_ffn_gather(x, perm, k: int, group_offsets, group_expert, rep_base
         _dev(rep_base, torch.int32, "rep_base", 1)
     T, H = x.shape
     E, H1, F = w1.shape
-    if H1 != H or tuple(w2.shape) != (E, F, H):
+    if H1 != H or tuple(w2.shape) != (E, F, H) or (w3 is not None and w3.shape != w1.shape):
         raise ValueError("weight shapes must be w1/w3 [E,H,F], w2 [E,F,H]")
     if perm.numel() != T * k:
         raise ValueError("perm must hold T*k entries")
+    _out(group_offsets, torch.int32, "group_offsets", (2 * E if group_expert is not None else E) + 1)
     act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
     if y is None:
         y = torch.empty((T * k, H), dtype=torch.bfloat16, device=x.device)
-    _dev(y, torch.bfloat16, "y", 2)
+    _out(y, torch.bfloat16, "y", T * k * H, 2)
     need = int(lib().moe_workspace_bytes(MOE_OP_EXPERT_FFN, T, k, E, H, F))
     if workspace is None:
         workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=x.device)
@@ -520,6 +561,7 @@ def moe_replicate_weights(rep_base, w_all=None, group_slot=None, stream=None):
         rows, cols = int(w_all.shape[1]), int(w_all.shape[2])
     if group_slot is None:
         group_slot = torch.empty(2 * E, dtype=torch.int32, device=rep_base.device)
+    _out(group_slot, torch.int32, "group_slot", 2 * E)
     _check(lib().moe_replicate_weights(_ptr(rep_base), E, _ptr(w_all), rows, cols, _ptr(group_slot),
                                        _stream(stream)), "moe_replicate_weights")
     return group_slot
@@ -533,13 +575,19 @@ def moe_expert_ffn_slots(xp, group_offsets, group_slot, w1, w3, w2, act: str = "
     _dev(group_offsets, torch.int32, "group_offsets", 1)
     _dev(group_slot, torch.int32, "group_slot", 1)
     A, H = xp.shape
+    _dev(w1, torch.bfloat16, "w1", 3)
+    _dev(w2, torch.bfloat16, "w2", 3)
+    if w3 is not None:
+        _dev(w3, torch.bfloat16, "w3", 3)
     S, H1, F = w1.shape
-    if H1 != H or tuple(w2.shape) != (S, F, H):
+    if H1 != H or tuple(w2.shape) != (S, F, H) or (w3 is not None and w3.shape != w1.shape):
         raise ValueError("weight shapes must be w1/w3 [S,H,F], w2 [S,F,H]")
     G = group_slot.numel()
+    _out(group_offsets, torch.int32, "group_offsets", G + 1)
     act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
     if y is None:
         y = torch.empty((A, H), dtype=torch.bfloat16, device=xp.device)
+    _out(y, torch.bfloat16, "y", A * H, 2)
     need = int(lib().moe_workspace_bytes(MOE_OP_EXPERT_FFN, A, 1, max((G + 1) // 2, 1), H, F))
     if workspace is None:
         workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=xp.device)
@@ -569,12 +617,15 @@ def moe_expert_ffn_combine(xp, group_offsets, group_expert, rep_base, perm, w, w
     A, H = xp.shape
     T, k = w.shape
     E, H1, F = w1.shape
-    if H1 != H or tuple(w2.shape) != (E, F, H) or A != T * k:
+    if (H1 != H or tuple(w2.shape) != (E, F, H) or A != T * k
+            or (w3 is not None and w3.shape != w1.shape)):
         raise ValueError("shapes: xp [T*k,H], w [T,k], w1/w3 [E,H,F], w2 [E,F,H]")
+    _out(perm, torch.int32, "perm", A)
+    _out(group_offsets, torch.int32, "group_offsets", (2 * E if group_expert is not None else E) + 1)
     act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=xp.device)
-    _dev(out, torch.bfloat16, "out", 2)
+    _out(out, torch.bfloat16, "out", T * H, 2)
     need = int(lib().moe_workspace_bytes(MOE_OP_EXPERT_FFN_COMBINE, T, k, E, H, F))
     if workspace is None:
         workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=xp.device)
@@ -625,8 +676,15 @@ def moe_ffn_backward(x, dout, w, y, perm, inv_perm, group_offsets, group_expert,
     T, H = x.shape
     k = w.shape[1]
     E, H1, F = w1.shape
-    if H1 != H or tuple(w2.shape) != (E, F, H) or tuple(dout.shape) != (T, H) or w.shape[0] != T:
+    if (H1 != H or tuple(w2.shape) != (E, F, H) or tuple(dout.shape) != (T, H) or w.shape[0] != T
+            or (w3 is not None and w3.shape != w1.shape)):
         raise ValueError("shapes: x, dout [T,H]; w [T,k]; w1/w3 [E,H,F]; w2 [E,F,H]")
+    A = T * k
+    _out(perm, torch.int32, "perm", A)
+    _out(inv_perm, torch.int32, "inv_perm", A)
+    _out(group_offsets, torch.int32, "group_offsets", (2 * E if group_expert is not None else E) + 1)
+    if y is not None:
+        _out(y, torch.bfloat16, "y", A * H)
     act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
     dev = x.device
     if accumulate and out is None:
@@ -642,9 +700,13 @@ def moe_ffn_backward(x, dout, w, y, perm, inv_perm, group_offsets, group_expert,
                torch.empty((E, H, F), dtype=gdt, device=dev) if act == "swiglu" else None,
                torch.empty((E, F, H), dtype=gdt, device=dev))
     dx, dw, dw1, dw3, dw2 = out
+    if dx is not None:
+        _out(dx, torch.bfloat16, "dx", T * H)
+    if dw is not None:
+        _out(dw, torch.float32, "dw", T * k)
     for nm, t in (("dw1", dw1), ("dw3", dw3), ("dw2", dw2)):
         if t is not None:
-            _dev(t, gdt, nm, 3)
+            _out(t, gdt, nm, E * H * F, 3)
     need = int(lib().moe_ffn_backward_workspace_bytes(T, k, E, H, F))
     if workspace is None:
         workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=dev)
@@ -670,9 +732,11 @@ def moe_route_backward(logits, idx, dw, renorm: bool = True, out=None, stream=No
     _dev(dw, torch.float32, "dw", 2)
     T, E = logits.shape
     k = idx.shape[1]
+    if idx.shape[0] != T or tuple(dw.shape) != tuple(idx.shape):
+        raise ValueError("shapes: logits [T,E], idx and dw [T,k]")
     if out is None:
         out = torch.empty((T, E), dtype=torch.float32, device=logits.device)
-    _dev(out, torch.float32, "dlogits", 2)
+    _out(out, torch.float32, "dlogits", T * E, 2)
     _check(lib().moe_route_backward(_ptr(logits), _ptr(idx), _ptr(dw), T, E, k, int(bool(renorm)), _ptr(out),
                                     _stream(stream)), "moe_route_backward")
     return out
@@ -686,9 +750,12 @@ def moe_combine(y, inv_perm, w, out=None, stream=None):
     _dev(w, torch.float32, "w", 2)
     T, k = w.shape
     H = y.shape[1]
+    if y.shape[0] < T * k:
+        raise ValueError("y must hold the T*k dispatched rows")
+    _out(inv_perm, torch.int32, "inv_perm", T * k)
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
-    _dev(out, torch.bfloat16, "out", 2)
+    _out(out, torch.bfloat16, "out", T * H, 2)
     _check(lib().moe_combine(_ptr(y), _ptr(inv_perm), _ptr(w), T, k, H, _ptr(out), _stream(stream)), "moe_combine")
     return out
 
