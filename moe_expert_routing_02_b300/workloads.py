@@ -111,7 +111,12 @@ def make_logits(T: int, E: int, alpha: float, *, seed_key, prev: Optional[np.nda
     if prev is not None and gamma != 0.0:
         top1 = np.argmax(prev, axis=1)
         g[np.arange(T), perm[top1]] += gamma
-    return g.astype(np.float32)
+    out = g.astype(np.float32)
+    # the gate's contract takes finite logits (the kernels do not check each
+    # element), so the generator checks what it hands out
+    if not np.isfinite(out).all():
+        raise ValueError("non-finite logits")
+    return out
 
 
 def make_layer_logits(cfg: MoEConfig, it: int, *, seed: int = 0, T: Optional[int] = None,
