@@ -471,6 +471,7 @@ def run_ours(args, rank, world, local):
                         "a second set of graphs with events around every stage, replayed once per slot after the "
                         "timed region (each event node adds ~1-2 us)"},
         "roofline": roofline, "stages": stages, "gpu_launches": launches, "clocks": clk,
+        "routing": routing_summary(step, c, args.small_threshold),
     }
 
     if not args.no_e2e:
@@ -478,6 +479,31 @@ def run_ours(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = run_cpu_baseline(c, args.cpu_tokens or c.T)
     return result
+
+
+def routing_summary(step, c, small_threshold):
+    """Load balance of the last layer call, from libmoe's own histogram and
+    dispatch layout (read back after the timed region): per-expert load max
+    and standard deviation over the mean, the replica groups, the largest
+    group over the per-expert target A/E, and the experts the small-batch
+    path serves (fewer than `small_threshold` rows, chosen per expert)."""
+    import numpy as np
+    try:
+        hist = step.hist.cpu().numpy().astype(np.float64)
+        go = step.go_full if hasattr(step, "go_full") else step.go
+        go = go.cpu().numpy().astype(np.int64)
+        n_groups = int(step.rep_base[-1].item()) if step.replicate else c.E
+        rows = np.diff(go[:n_groups + 1])
+        mean = hist.mean()
+        return {"of": "last layer call of the last step",
+                "load_max_over_mean": round(float(hist.max() / mean), 3),
+                "load_stddev_over_mean": round(float(hist.std() / mean), 3),
+                "replica_groups": n_groups, "extra_replicas": n_groups - c.E,
+                "largest_group_over_target": round(float(rows.max() / (c.T * c.k / c.E)), 3),
+                "experts_without_tokens": int((hist == 0).sum()),
+                "small_path_experts": int(((hist > 0) & (hist < small_threshold)).sum())}
+    except Exception as e:  # a summary must never cost the measurement line
+        return {"error": f"{type(e).__name__}: {e}"}
 
 
 def run_e2e(args, c, step, logits, weights, dev, world):
