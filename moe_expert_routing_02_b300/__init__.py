@@ -161,6 +161,11 @@ def _out(t, dtype, name, numel, ndim=None):
     return t
 
 
+def _ws_bytes(workspace) -> int:
+    """A workspace is a contiguous uint8 CUDA tensor; its size in bytes."""
+    return _dev(workspace, _torch().uint8, "workspace").numel()
+
+
 def workspace_bytes(op: int, T: int, k: int, E: int, H: int = 64, F: int = 64) -> int:
     return int(lib().moe_workspace_bytes(op, T, k, E, H, F))
 
@@ -380,7 +385,7 @@ def moe_dispatch(x, idx, E: int, rep_base=None, out=None, workspace=None, stream
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     _check(lib().moe_dispatch(_ptr(x), _ptr(idx), T, k, H, E, _ptr(rep_base), _ptr(go), _ptr(perm), _ptr(inv),
-                              _ptr(xp), _ptr(workspace), workspace.numel(), _stream(stream)), "moe_dispatch")
+                              _ptr(xp), _ptr(workspace), _ws_bytes(workspace), _stream(stream)), "moe_dispatch")
     return go, perm, inv, xp
 
 
@@ -470,7 +475,7 @@ def moe_layer_front(logits, x, stats: "MoEStats", it: int, layer: int, k: int, i
                                  int(max_copies), _ptr(rep_share), int(budget), _ptr(idx), _ptr(w), _ptr(hist),
                                  _ptr(p_seq), _ptr(cond),
                                  _ptr(p_next), _ptr(copies), _ptr(rep_base), _ptr(group_expert), _ptr(go),
-                                 _ptr(perm), _ptr(inv), _ptr(xp), _ptr(workspace), workspace.numel(),
+                                 _ptr(perm), _ptr(inv), _ptr(xp), _ptr(workspace), _ws_bytes(workspace),
                                  _stream(stream)), "moe_layer_front")
     return {"idx": idx, "w": w, "hist": hist, "p_seq": p_seq, "cond": cond, "p_next": p_next, "copies": copies,
             "rep_base": rep_base, "group_expert": group_expert, "group_offsets": go, "perm": perm,
@@ -505,7 +510,7 @@ def moe_expert_ffn(xp, group_offsets, group_expert, rep_base, w1, w3, w2, act: s
         workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=xp.device)
     _check(lib().moe_expert_ffn(_ptr(xp), _ptr(group_offsets), _ptr(group_expert), _ptr(rep_base), E, A,
                                 _ptr(w1), _ptr(w3), _ptr(w2), H, F, act_id, int(small_group_threshold), _ptr(y),
-                                _ptr(workspace), workspace.numel(), _stream(stream)), "moe_expert_ffn")
+                                _ptr(workspace), _ws_bytes(workspace), _stream(stream)), "moe_expert_ffn")
     return y
 
 
@@ -542,7 +547,7 @@ def moe_expert_ffn_gather(x, perm, k: int, group_offsets, group_expert, rep_base
         workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=x.device)
     _check(lib().moe_expert_ffn_gather(_ptr(x), T, _ptr(perm), int(k), _ptr(group_offsets), _ptr(group_expert),
                                        _ptr(rep_base), E, _ptr(w1), _ptr(w3), _ptr(w2), H, F, act_id,
-                                       int(small_group_threshold), _ptr(y), _ptr(workspace), workspace.numel(),
+                                       int(small_group_threshold), _ptr(y), _ptr(workspace), _ws_bytes(workspace),
                                        _stream(stream)), "moe_expert_ffn_gather")
     return y
 
@@ -593,7 +598,7 @@ def moe_expert_ffn_slots(xp, group_offsets, group_slot, w1, w3, w2, act: str = "
         workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=xp.device)
     _check(lib().moe_expert_ffn_slots(_ptr(xp), _ptr(group_offsets), _ptr(group_slot), G, S, A, _ptr(w1), _ptr(w3),
                                       _ptr(w2), H, F, act_id, int(small_group_threshold), _ptr(y), _ptr(workspace),
-                                      workspace.numel(), _stream(stream)), "moe_expert_ffn_slots")
+                                      _ws_bytes(workspace), _stream(stream)), "moe_expert_ffn_slots")
     return y
 
 
@@ -631,7 +636,7 @@ def moe_expert_ffn_combine(xp, group_offsets, group_expert, rep_base, perm, w, w
         workspace = torch.empty(max(need, 1024), dtype=torch.uint8, device=xp.device)
     _check(lib().moe_expert_ffn_combine(_ptr(xp), _ptr(group_offsets), _ptr(group_expert), _ptr(rep_base), E,
                                         _ptr(perm), _ptr(w), T, k, _ptr(w1), _ptr(w3), _ptr(w2), H, F, act_id,
-                                        int(small_group_threshold), _ptr(out), _ptr(workspace), workspace.numel(),
+                                        int(small_group_threshold), _ptr(out), _ptr(workspace), _ws_bytes(workspace),
                                         _stream(stream)), "moe_expert_ffn_combine")
     return out
 
@@ -715,7 +720,7 @@ def moe_ffn_backward(x, dout, w, y, perm, inv_perm, group_offsets, group_expert,
                                   act_id, _ptr(dx), _ptr(dw), _ptr(dw1), _ptr(dw3), _ptr(dw2),
                                   (MOE_BWD_ACCUMULATE_WGRAD if accumulate else 0)
                                   | (MOE_BWD_WGRAD_BF16 if wgrad_bf16 else 0), _ptr(workspace),
-                                  workspace.numel(), _stream(stream)), "moe_ffn_backward")
+                                  _ws_bytes(workspace), _stream(stream)), "moe_ffn_backward")
     return dx, dw, dw1, dw3, dw2
 
 
