@@ -90,6 +90,7 @@ def test_exact_and_larger_buffers_pass(rec):
 @pytest.mark.parametrize("case", [
     "route_idx", "route_w", "hist", "cond", "rep_base", "group_expert", "perm", "xp", "ffn_y", "ffn_offsets",
     "combine_out", "combine_y_rows", "dx", "dw1", "dlogits", "front_inv", "front_idx_prev", "slot_map",
+    "workspace_dtype",
 ])
 def test_undersized_buffers_are_refused_before_launch(rec, case):
     idx = _z(T, k, dtype=i32)
@@ -123,6 +124,7 @@ def test_undersized_buffers_are_refused_before_launch(rec, case):
         "front_inv": lambda: M.moe_layer_front(_z(T, E), None, st, 0, 0, k, out={"inv_perm": _z(A - 1, dtype=i32)}),
         "front_idx_prev": lambda: M.moe_layer_front(_z(T, E), None, st, 0, 1, k, idx_prev=_z(T - 1, k, dtype=i32)),
         "slot_map": lambda: M.moe_replicate_weights(_z(E + 1, dtype=i32), None, group_slot=_z(2 * E - 1, dtype=i32)),
+        "workspace_dtype": lambda: M.moe_dispatch(x, idx, E, out=(go, perm, inv, xp), workspace=_z(1 << 16)),
     }[case]
     with pytest.raises(ValueError):
         short()
