@@ -267,3 +267,40 @@ def test_ffn_launch_count_rule(L):
     assert n(32768, 16, 1024, 2000, gel, 64, 0) == 0
     assert n(32768, 16, 1024, 2048, 7, 64, 0) == 0
     assert n(32768, 16, 1024, 2048, gel, -1, 0) == 0
+
+
+def test_header_is_plain_c_and_a_c_program_links_and_calls_the_library(L, tmp_path):
+    """include/moe.h compiles as C99 and C++17, and a C program (no torch,
+    no Python) links libmoe.so and calls host-only entry points."""
+    import shutil
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    for lang, std in (("c", "-std=c99"), ("c++", "-std=c++17")):
+        r = subprocess.run([gcc if lang == "c" else (shutil.which("g++") or gcc), std, "-Wall", "-Wextra",
+                            "-Werror", "-fsyntax-only", "-x", lang, HEADER], capture_output=True, text=True)
+        assert r.returncode == 0, (lang, r.stderr)
+    src = tmp_path / "use_moe.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "moe.h"
+int main(void) {
+  /* host-only calls: no device is touched */
+  size_t ws = moe_workspace_bytes(MOE_OP_DISPATCH, 16384, 2, 16, 1024, 0);
+  moe_status bad = moe_route(NULL, 16, 0, 1, 1, NULL, NULL, NULL);   /* E < 1: refused on the host */
+  printf("%s|%zu|%d|%s|%d\n", strstr(moe_version(), "sm_103a") ? "sm_103a" : "?", ws, (int)bad,
+         moe_status_string(MOE_ERR_INVALID), moe_ffn_launches(32768, 16, 1024, 2048, MOE_ACT_GELU, 64, 0));
+  return 0;
+}
+''')
+    libdir = os.path.dirname(M.library_path)
+    exe = tmp_path / "use_moe"
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe),
+                        f"-L{libdir}", "-l:libmoe.so", f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    ver, ws, bad, msg, n = out.stdout.strip().split("|")
+    assert ver == "sm_103a" and int(ws) == (32 * 16 + 64) * 4
+    assert int(bad) == M.MOE_ERR_INVALID and msg and int(n) == 3
