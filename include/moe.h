@@ -549,8 +549,10 @@ moe_status moe_dispatch_noalloc(const uint16_t* x, const int32_t* idx, int T, in
  *     has exited, and each waits for that kernel's completion (griddepcontrol
  *     .wait) before touching memory; no kernel releases its dependents early.
  *     0: ordinary launches.  Results are identical either way.
- * Unknown options or values return MOE_ERR_INVALID.  Not thread-safe against
- * concurrent moe_expert_ffn calls.
+ * Unknown options or values return MOE_ERR_INVALID.  Options are process-wide
+ * and stored atomically; a call reads each one once when it is made, so a
+ * set from another thread applies to the calls that start after it returns
+ * (a call made at the same time sees the old or the new value).
  * ------------------------------------------------------------------------- */
 typedef enum { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_FFN_TIMEOUT_SELFTEST = 2, MOE_OPT_PDL = 3 } moe_option;
 typedef enum {

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 // Device error word, one per device (this library is built as one translation
 // unit, so every kernel sees the same variable).
 //   bit 0: a kernel met invalid device data (expert id out of range,
@@ -27,7 +29,8 @@ __device__ __forceinline__ void moe_flag_error(unsigned int bits) { atomicOr(&g_
 // dependent never shares the GPU with its predecessor's blocks.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-inline int g_moe_pdl = 1;  // host option (moe_set_option(MOE_OPT_PDL, ...))
+// host option (moe_set_option(MOE_OPT_PDL, ...)); read once per launch
+inline std::atomic<int> g_moe_pdl{1};
 
 template <typename... KArgs, typename... Args>
 static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
@@ -41,7 +44,7 @@ static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = g_moe_pdl ? 1 : 0;
+  cfg.numAttrs = g_moe_pdl.load(std::memory_order_relaxed) ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 

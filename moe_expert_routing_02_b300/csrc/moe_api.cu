@@ -75,8 +75,9 @@ struct DeviceInfo {
 };
 
 // Library options (moe_set_option).
-int g_opt_ffn_kernel = MOE_FFN_KERNEL_AUTO;
-int g_opt_ffn_selftest = 0;  // one-shot: next GEMM1 withholds an accumulator signal
+// Process-wide and atomic: a call reads each option once when it is made.
+std::atomic<int> g_opt_ffn_kernel{MOE_FFN_KERNEL_AUTO};
+std::atomic<int> g_opt_ffn_selftest{0};  // one-shot: next GEMM1 withholds an accumulator signal
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 std::mutex g_side_mu;  // one fork/join sequence at a time per process
@@ -532,14 +533,14 @@ namespace {
 // two-launch kernel's order reuses each weight slice across blocks -- and
 // never with gathered rows.  Depends only on the sizes and the options.
 void ffn_choice(long long A, int E, int H, int F, int act, bool gather, bool* use_pair, bool* use_fused) {
+  const int opt = g_opt_ffn_kernel.load(std::memory_order_relaxed);
   bool pair = A >= 256LL * E;
-  if (g_opt_ffn_kernel == MOE_FFN_KERNEL_SINGLE) pair = false;
-  if (g_opt_ffn_kernel == MOE_FFN_KERNEL_PAIR || g_opt_ffn_kernel == MOE_FFN_KERNEL_FUSED) pair = true;
+  if (opt == MOE_FFN_KERNEL_SINGLE) pair = false;
+  if (opt == MOE_FFN_KERNEL_PAIR || opt == MOE_FFN_KERNEL_FUSED) pair = true;
   const long long expert_weight_bytes = (long long)(act == MOE_ACT_SWIGLU ? 3 : 2) * H * F * 2;
   *use_pair = pair;
   *use_fused = pair && !gather &&
-               (g_opt_ffn_kernel == MOE_FFN_KERNEL_FUSED ||
-                (g_opt_ffn_kernel == MOE_FFN_KERNEL_AUTO && expert_weight_bytes <= (16LL << 20)));
+               (opt == MOE_FFN_KERNEL_FUSED || (opt == MOE_FFN_KERNEL_AUTO && expert_weight_bytes <= (16LL << 20)));
 }
 
 // The combine fused into GEMM2 (moe_expert_ffn_combine): GEMM2's epilogues
@@ -623,8 +624,7 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   p1.K = H;
   p1.N_out = F;
   p1.out = inter;
-  p1.flags = g_opt_ffn_selftest ? 1 : 0;
-  g_opt_ffn_selftest = 0;
+  p1.flags = g_opt_ffn_selftest.exchange(0) ? 1 : 0;
   p1.rep_base = rep_base;
   p1.small_threshold = small_group_threshold;
   p1.a_src = a_src;
@@ -958,17 +958,17 @@ moe_status moe_set_option(int option, int value) {
   if (option == MOE_OPT_FFN_KERNEL) {
     if (value < MOE_FFN_KERNEL_AUTO || value > MOE_FFN_KERNEL_FUSED)
       return fail(MOE_ERR_INVALID, "moe_set_option: unknown FFN kernel %d", value);
-    g_opt_ffn_kernel = value;
+    g_opt_ffn_kernel.store(value);
     return MOE_OK;
   }
   if (option == MOE_OPT_PDL) {
     if (value != 0 && value != 1) return fail(MOE_ERR_INVALID, "moe_set_option: PDL value must be 0 or 1");
-    g_moe_pdl = value;
+    g_moe_pdl.store(value);
     return MOE_OK;
   }
   if (option == MOE_OPT_FFN_TIMEOUT_SELFTEST) {
     if (value != 0 && value != 1) return fail(MOE_ERR_INVALID, "moe_set_option: self-test value must be 0 or 1");
-    g_opt_ffn_selftest = value;
+    g_opt_ffn_selftest.store(value);
     return MOE_OK;
   }
   return fail(MOE_ERR_INVALID, "moe_set_option: unknown option %d", option);
@@ -977,15 +977,15 @@ moe_status moe_set_option(int option, int value) {
 moe_status moe_get_option(int option, int* value) {
   if (!value) return fail(MOE_ERR_INVALID, "moe_get_option: null value");
   if (option == MOE_OPT_FFN_KERNEL) {
-    *value = g_opt_ffn_kernel;
+    *value = g_opt_ffn_kernel.load();
     return MOE_OK;
   }
   if (option == MOE_OPT_PDL) {
-    *value = g_moe_pdl;
+    *value = g_moe_pdl.load();
     return MOE_OK;
   }
   if (option == MOE_OPT_FFN_TIMEOUT_SELFTEST) {
-    *value = g_opt_ffn_selftest;
+    *value = g_opt_ffn_selftest.load();
     return MOE_OK;
   }
   return fail(MOE_ERR_INVALID, "moe_get_option: unknown option %d", option);
