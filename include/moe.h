@@ -246,7 +246,10 @@ moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int
  *   moe_route(logits) -> moe_stats_update(st, iter, layer, idx, idx_prev) ->
  *   moe_predict(st, layer) [when p_seq != NULL] -> moe_replicate(hist, T*k)
  *   [when replicate != 0] -> moe_dispatch(x, idx, rep_base or NULL)
- * (passages as for those calls), with the arguments of those calls:
+ * (passages as for those calls: PopFetcher review, gate and Routing
+ * Information Collector, Eq. (1)-(3); MoE-GPS blog section 2.1,
+ * duplicate_experts; MoE-MPMC summary, replica dispatch), with the
+ * arguments of those calls:
  *   logits [T,E] f32, x [T,H] bf16 (NULL with xp = NULL: permutation only),
  *   renorm, st / iter / layer / idx_prev (NULL for layer 0), replicate and its
  *   thresh_num / thresh_den / max_copies, and the outputs idx, w, hist_out
@@ -361,6 +364,9 @@ moe_status moe_replicate_weights(const int32_t* rep_base, int E, uint16_t* w_all
 /* ---------------------------------------------------------------------------
  * moe_expert_ffn_slots -- the grouped expert FFN with each group reading
  * its own weight slot (physical replicas, moe_replicate_weights).
+ * MoE-MPMC summary, methodology (the tokens of an expert spread over its
+ * distinct physical replicas, each computing with its own copy); the
+ * arithmetic is moe_expert_ffn's (EPS-MoE review: gate, up and down GEMMs).
  *   group_slot  [G] int32: weight slot of group g (-1 / empty groups
  *               allowed); G <= 512
  *   n_slots     weight slots in w1/w3/w2 ([n_slots,H,F] / [n_slots,F,H]),
