@@ -304,3 +304,15 @@ int main(void) {
     ver, ws, bad, msg, n = out.stdout.strip().split("|")
     assert ver == "sm_103a" and int(ws) == (32 * 16 + 64) * 4
     assert int(bad) == M.MOE_ERR_INVALID and msg and int(n) == 3
+
+
+def test_every_entry_point_names_its_passage():
+    """Each declaration block of include/moe.h cites the passage of the pages
+    it follows (a review, blog or summary, by section), or says that the
+    pages have no counterpart / that the call is host-only bookkeeping."""
+    src = open(HEADER).read()
+    marks = ("review", "blog", "summary", "Prediction Is All", "no counterpart", "Host only", "host only")
+    for block in re.split(r"(?=/\* -{10,})", src):
+        decls = re.findall(r"\b(moe_\w+)\s*\(", re.sub(r"/\*.*?\*/", "", block, flags=re.S))
+        if decls:
+            assert any(m in block for m in marks), decls
