@@ -45,10 +45,14 @@ Readings of points the pages leave open are stated where they are used; every
 one is also listed in the repository's design notes.
 
 Parity pins: every function here is pinned by `-m "not gpu"` tests against
-brute force, hand-computed tables or closed forms.  The numerical content of
-Eq. (1)-(3) beyond the "window sums of counts, normalised" reading is the
-one part the pages do not print (parity of that reading is pinned by the
-stationary-stream closed form, not by printed values).
+brute force, hand-computed tables or closed forms.
+
+Parity unpinned (the pages print no formula or value to pin against):
+  * the numerical content of Eq. (1)-(3) beyond the "window sums of counts,
+    normalised" reading -- that reading is pinned by the stationary-stream
+    closed form and brute-force window sums, not by printed values;
+  * the decay weighting of predict_decay beyond its reading (weights
+    lam**age) -- pinned by hand-derived cases of that reading only.
 """
 from __future__ import annotations
 
