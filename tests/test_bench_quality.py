@@ -44,3 +44,32 @@ def test_routing_summary_from_the_layer_buffers():
     assert s["small_path_experts"] == 5          # 60, 40, 30, 20, 12 rows
     # a broken buffer gives an error entry, not an exception
     assert "error" in bench.routing_summary(types.SimpleNamespace(), c, 64)
+
+
+def test_algorithmic_work_matches_the_quoted_figures():
+    """The roofline numerators (per-layer bytes of the HBM stages, flops of
+    the FFN) for the five workloads, against the per-stage figures quoted for
+    them in the build's scope table (route T*E*4 + A*8; dispatch and combine
+    about A*H*2 + T*H*2 plus the index traffic; FFN (2 or 3)*2*A*H*F flops),
+    each within one unit of its last quoted digit (the figures are rounded or
+    truncated)."""
+    from moe_expert_routing_02_b300 import workloads as W
+    # workload: route (bytes, quoted), dispatch = combine (bytes), FFN (flops)
+    quoted = {
+        "tiny": ((12e3, 1e3), (0.1e6, 0.1e6), (0.017e9, 0.001e9)),
+        "moe_gpt_stream": ((1.31e6, 0.01e6), (101e6, 1e6), (0.275e12, 0.001e12)),
+        "mixtral_layer": ((393e3, 1e3), (201e6, 1e6), (5.77e12, 0.01e12)),
+        "deepseekv2_layer": ((2.82e6, 0.01e6), (294e6, 1e6), (1.16e12, 0.01e12)),
+        "dbrx_replicated_layer": ((393e3, 1e3), (252e6, 1e6), (6.49e12, 0.01e12)),
+    }
+    for name, ((r, dr), (d, dd), (f, df)) in quoted.items():
+        w = bench.algorithmic_work(W.config_by_name(name))
+        assert abs(w["route"]["bytes"] - r) <= dr, (name, w["route"])
+        assert abs(w["dispatch"]["bytes"] - d) <= dd, (name, w["dispatch"])
+        assert abs(w["combine"]["bytes"] - d) <= dd, (name, w["combine"])
+        assert abs(w["ffn"]["flops"] - f) <= df, (name, w["ffn"])
+        front = sum(w[s]["bytes"] for s in ("route", "stats", "predict", "replicate", "dispatch"))
+        assert w["front"]["bytes"] == front
+    # the gathered FFN input: dispatch moves no rows, only the index traffic
+    g = bench.algorithmic_work(W.config_by_name("moe_gpt_stream"), gather=True)
+    assert g["dispatch"]["bytes"] == 3 * 32768 * 4
