@@ -584,12 +584,16 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def run_cpu_baseline(c, T_s, reps=3):
-    # warm once (input generation, imports), then time `reps` layer samples;
-    # then one sample of a quarter of the tokens with the BLAS pool held to
-    # one thread (the single-core rate)
+def run_cpu_baseline(c, T_s, min_reps=3, min_seconds=10.0, max_reps=20):
+    # warm once (input generation, imports), then time layer samples until at
+    # least `min_reps` of them and `min_seconds` of CPU work are done; then one
+    # sample of a quarter of the tokens with the BLAS pool held to one thread
+    # (the single-core rate)
     oracle_layer_sample(c, T_s)
-    t = sum(oracle_layer_sample(c, T_s) for _ in range(reps))
+    t, reps = 0.0, 0
+    while reps < max_reps and (reps < min_reps or t < min_seconds):
+        t += oracle_layer_sample(c, T_s)
+        reps += 1
     res = {"value": round(reps * T_s / t, 1), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
            "sample": f"{reps} x one layer of {c.name} with {T_s} of {c.T} tokens (all k={c.k} assignments "
                      f"through route, stats+predict over 2 layers' routing, replicate, dispatch, fp64 FFN, "
