@@ -54,7 +54,9 @@ class MoELayerStep:
     dispatch order first.  replicate_from="prediction" takes layer j's replica
     table from the prediction made at layer j-1 (its p_next) instead of layer
     j's own histogram -- replicas decided before routing -- with `budget`
-    bounding the total copies (-1 = none); layer 0 uses its histogram.
+    bounding the total copies (-1 = none); layer 0 uses its histogram, and
+    every layer must run with predict=True (layer j reads what layer j-1
+    predicted).
     physical_replicas=True copies each replica's weights into its own slot
     (moe_replicate_weights) and runs the FFN over the slots; `weights` must
     then be the buffers of replica_buffers().  The output is the same in
@@ -76,6 +78,8 @@ class MoELayerStep:
         self.fused = fused and stats is not None
         if replicate_from not in ("histogram", "prediction"):
             raise ValueError("replicate_from must be 'histogram' or 'prediction'")
+        if replicate_from == "prediction" and (stats is None or not replicate):
+            raise ValueError("replicate_from='prediction' needs stats (the prediction) and replicate=True")
         self.replicate_from = replicate_from
         self.budget = budget
         self.physical = physical_replicas and replicate

@@ -152,3 +152,12 @@ def test_backward_uses_the_saved_routing(calls):
     bwd = calls[0][1]
     assert bwd[4] == saved.perm.data_ptr() and bwd[5] == saved.inv.data_ptr() and bwd[3] == saved.y.data_ptr()
     assert calls[1][1][1] == saved.idx.data_ptr()
+
+
+def test_prediction_driven_replication_needs_the_prediction():
+    c = _cfg(2)
+    with pytest.raises(ValueError):
+        LY.MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, None, device="cpu", replicate_from="prediction")
+    with pytest.raises(ValueError):
+        LY.MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, _Stats(c.L, c.E), device="cpu", replicate=False,
+                        replicate_from="prediction")
