@@ -43,7 +43,8 @@ class MoELayerStep:
 
     replicate=True feeds the replica table of the layer's own histogram into
     dispatch and the FFN (hot experts split into replica groups; the output is
-    unchanged).  stats (MoEStats) is shared by all layers of a model.
+    unchanged); it needs stats, whose update writes that histogram.  stats
+    (MoEStats) is shared by all layers of a model.
     fused=True (needs stats) runs route, statistics, prediction, replicas and
     dispatch as moe_layer_front (two launches, plus a third on the side stream
     for the co-selection fold and prediction when layer > 0 or predict=True);
@@ -78,6 +79,9 @@ class MoELayerStep:
         self.fused = fused and stats is not None
         if replicate_from not in ("histogram", "prediction"):
             raise ValueError("replicate_from must be 'histogram' or 'prediction'")
+        if replicate and stats is None:
+            raise ValueError("replication reads the layer's histogram, which the statistics update writes: "
+                             "pass stats, or replicate=False")
         if replicate_from == "prediction" and (stats is None or not replicate):
             raise ValueError("replicate_from='prediction' needs stats (the prediction) and replicate=True")
         self.replicate_from = replicate_from

@@ -161,3 +161,14 @@ def test_prediction_driven_replication_needs_the_prediction():
     with pytest.raises(ValueError):
         LY.MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, _Stats(c.L, c.E), device="cpu", replicate=False,
                         replicate_from="prediction")
+    with pytest.raises(ValueError):     # replication without the statistics that write the histogram
+        LY.MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, None, device="cpu")
+    LY.MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, None, device="cpu", replicate=False)
+
+
+def test_layer_without_statistics_makes_route_dispatch_ffn_combine(calls):
+    c = _cfg(2)
+    step = LY.MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, None, device="cpu", replicate=False)
+    _run(c, step)
+    assert [n for n, _ in calls] == ["moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine"] * c.L
+    assert all(a[6] is None for n, a in calls if n == "moe_dispatch")      # no replica table
