@@ -14,9 +14,15 @@
  *   moe_expert_ffn    grouped expert FFN (GeLU or SwiGLU) on tcgen05 tensor cores
  *   moe_combine       gate-weighted sum of each token's k expert outputs
  *
- * and two fused forms of the same work: moe_layer_front (route through
- * dispatch in three launches) and moe_expert_ffn_gather (the FFN reading the
- * token rows in place, so that dispatch writes only the permutation).
+ * Fused forms of the same work: moe_layer_front (route through dispatch in
+ * three launches), moe_expert_ffn_gather (the FFN reading the token rows in
+ * place, so that dispatch writes only the permutation) and
+ * moe_expert_ffn_combine (the combine in the second GEMM's epilogue).
+ * Widened calls: moe_predict_decay and moe_replicate_predicted (replicas from
+ * a prediction, with a copies budget), moe_replicate_weights and
+ * moe_expert_ffn_slots (physical replica copies), moe_ffn_backward and
+ * moe_route_backward (the layer's backward), and moe_dispatch_noalloc
+ * (dispatch with library-owned scratch).
  *
  * Conventions
  *   T tokens, E experts, k experts per token, A = T*k assignments (assignment
