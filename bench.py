@@ -495,7 +495,7 @@ def routing_summary(step, c, small_threshold):
         n_groups = int(step.rep_base[-1].item()) if step.replicate else c.E
         rows = np.diff(go[:n_groups + 1])
         mean = hist.mean()
-        return {"of": "last layer call of the last step",
+        return {"of": "the last layer call made (after the timed region)",
                 "load_max_over_mean": round(float(hist.max() / mean), 3),
                 "load_stddev_over_mean": round(float(hist.std() / mean), 3),
                 "replica_groups": n_groups, "extra_replicas": n_groups - c.E,
