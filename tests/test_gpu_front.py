@@ -134,3 +134,86 @@ def test_front_replicates_from_a_prediction(budget):
             share = a["p_next"].clone()
         prev_a, prev_b = a["idx"], b["idx"]
     M.moe_check()
+
+
+def _front_vs_oracle(lg_np, x, st, ost, it, j, k, prev_d, prev_o, oracle_pred):
+    """One fused-front call against the oracle at the same point of the
+    stream: routing, histogram, window ring and sums, prediction, replica
+    table and dispatch (with the row copy)."""
+    E = lg_np.shape[1]
+    lg = torch.from_numpy(lg_np).cuda()
+    b = M.moe_layer_front(lg, x, st, it, j, k, idx_prev=prev_d, predict=True, replicate=True)
+    M.moe_check()
+    oi, ow = O.topk_gate(lg_np, k)
+    assert np.array_equal(b["idx"].cpu().numpy(), oi), (it, j)
+    assert np.abs(b["w"].cpu().numpy() - ow).max() <= 1e-6
+    oh = ost.update(it, j, oi, prev_o)
+    assert np.array_equal(b["hist"].cpu().numpy(), oh), (it, j)
+    ring_h, hsum, ring_c, csum = st.state_arrays()
+    assert np.array_equal(ring_h.astype(np.int64), ost.h), (it, j)
+    assert np.array_equal(ring_c.astype(np.int64), ost.C), (it, j)
+    assert np.array_equal(hsum[j].astype(np.int64), ost.window_hist(j)), (it, j)
+    if j > 0:
+        assert np.array_equal(csum[j - 1].astype(np.int64), ost.window_cosel(j - 1)), (it, j)
+    op, oc, opn = oracle_pred(j)
+    assert np.abs(b["p_seq"].cpu().numpy() - op).max() <= 1e-6, (it, j)
+    if oc is not None:
+        assert np.abs(b["cond"].cpu().numpy() - oc).max() <= 1e-6, (it, j)
+        assert np.abs(b["p_next"].cpu().numpy() - opn).max() <= 1e-6, (it, j)
+    copies, rb, ge = O.replicate(oh, oi.size)
+    assert b["copies"].cpu().numpy().tolist() == copies.tolist(), (it, j)
+    assert b["rep_base"].cpu().numpy().tolist() == rb.tolist(), (it, j)
+    G = int(rb[-1])
+    assert b["group_expert"].cpu().numpy()[:G].tolist() == ge[:G].tolist(), (it, j)
+    go, perm, inv = O.dispatch(oi, E, rb)
+    assert np.array_equal(b["group_offsets"].cpu().numpy(), go), (it, j)
+    assert np.array_equal(b["perm"].cpu().numpy(), perm), (it, j)
+    assert np.array_equal(b["inv_perm"].cpu().numpy(), inv), (it, j)
+    if x is not None:
+        src = b["perm"].long() // k
+        assert torch.equal(b["xp"], x[src]), (it, j)
+    return b, oi, G
+
+
+def test_front_across_ring_wrap_moe_gpt_stream():
+    """The fused front over the full-size moe_gpt_stream workload (12 layers,
+    T = 16384, window s = 10) for 25 iterations -- the ring wraps twice, so
+    every window sum has had slots replaced (new - old) -- and then for
+    iterations 50..55 of the stationary skewed phase, where hot experts get
+    replicas.  Every layer of every iteration is compared with the oracle's
+    window (PopFetcher review, Routing Information Collector, s = 10)."""
+    c = W.config_by_name("moe_gpt_stream")
+    st = M.MoEStats(c.L, c.E, c.window)
+    ost = O.WindowStats(c.L, c.E, c.window)
+    extra = 0
+    its = list(range(25)) + list(range(50, 56))
+    for it in its:
+        lgs = W.make_layer_logits(c, it)
+        prev_d = prev_o = None
+        for j in range(c.L):
+            x = W.make_x(c, it, j, device="cuda") if j in (0, c.L - 1) else None
+            b, oi, G = _front_vs_oracle(lgs[j], x, st, ost, it, j, c.k, prev_d, prev_o, ost.predict)
+            if it >= 50:
+                extra += G - c.E
+            prev_d, prev_o = b["idx"], oi
+    assert extra > 0   # the skewed phase does split hot experts
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 4, 2), (17, 8, 3), (1000, 160, 6), (2049, 256, 8), (5000, 16, 1),
+                                   (333, 64, 4)])
+def test_front_across_ring_wrap_edges(T, E, k):
+    """Window s = 4 over 10 iterations of three layers (the ring wraps twice),
+    tie-heavy logits, edge shapes: every call against the oracle."""
+    rng = np.random.default_rng([T, E, k])
+    L, s = 3, 4
+    st = M.MoEStats(L, E, s)
+    ost = O.WindowStats(L, E, s)
+    for it in range(10):
+        prev_d = prev_o = None
+        for j in range(L):
+            lg_np = rng.standard_normal((T, E)).astype(np.float32)
+            lg_np[:, ::5] = np.round(lg_np[:, ::5])
+            lg_np[:, 0] += 1.5 * (it % 3)     # drifting skew: replica tables change
+            x = torch.randn((T, 64), device="cuda").to(torch.bfloat16)
+            b, oi, _ = _front_vs_oracle(lg_np, x, st, ost, it, j, k, prev_d, prev_o, ost.predict)
+            prev_d, prev_o = b["idx"], oi
