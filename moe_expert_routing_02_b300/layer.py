@@ -17,7 +17,7 @@ from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_EXPERT_FFN_COMBINE, MO
                moe_replicate_weights, moe_expert_ffn_slots, moe_route, moe_route_backward, moe_stats_update,
                workspace_bytes)
 
-__all__ = ["MoELayerStep", "MoESaved", "ChunkedLayerStep", "HostPipeline"]
+__all__ = ["MoELayerStep", "MoESaved", "ChunkedLayerStep", "HostPipeline", "capture_slot_graphs"]
 
 
 def _front_launches(layer: int, predict: bool) -> int:
@@ -443,3 +443,29 @@ class HostPipeline:
             self._fresh[b] = False
         # the caller's stream covers the last copies back
         comp.wait_stream(self.d2h)
+
+
+def capture_slot_graphs(run_iteration, slots: int, make_events=None):
+    """One CUDA graph per window slot of a multi-layer iteration.
+
+    The statistics update uses the iteration only modulo the window s, so a
+    graph captured for slot q replays every iteration i with i mod s = q
+    exactly.  `run_iteration(q, events)` enqueues one whole iteration (every
+    layer) for slot q on the current stream; `make_events()`, if given,
+    returns the per-layer stage events recorded inside that graph (external
+    events, readable after a replay).  Returns (graphs, events), one entry per
+    slot; replay graph i mod s for iteration i."""
+    graphs, evs = [], []
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        for q in range(slots):
+            g = torch.cuda.CUDAGraph()
+            ev = None if make_events is None else make_events()
+            with torch.cuda.graph(g, stream=cap):
+                run_iteration(q, ev)
+            graphs.append(g)
+            evs.append(ev)
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+    return graphs, evs
