@@ -44,7 +44,12 @@
  *   (created with two events at the first call on that device, kept for the
  *   life of the process), forked from `stream` and joined back to it within
  *   the call, so callers see ordinary stream order; calls on different
- *   streams share that side stream (one fork/join at a time).  Under CUDA
+ *   streams share that side stream (one fork/join at a time, under a
+ *   process-wide lock).  The sharing adds an ordering between callers that
+ *   work on independent streams: the side-stream part of a later call waits
+ *   for the side-stream part of every earlier one on that device, and so does
+ *   the caller's stream at the join.  Results are unaffected; only overlap
+ *   between such callers is lost.  Under CUDA
  *   graph capture the side stream joins the capture through the fork event
  *   and stays part of it until the capture ends, so while one thread captures
  *   these calls no other thread may enqueue them on the same device; make the
@@ -518,7 +523,10 @@ moe_status moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* 
  *           requests return MOE_ERR_WORKSPACE and enqueue nothing.
  *   Set-up  the first call on a device (with that device current) looks up
  *           the array's device address once; make that first call before
- *           any stream capture.
+ *           any stream capture.  The address is kept for the life of the
+ *           process: after cudaDeviceReset (or anything else that destroys
+ *           the device's primary context) it is stale, and this call must
+ *           not be used on that device again in the same process.
  *   Sharing every call on a device uses the same array, which keeps the last
  *           call's contents (each call writes every word it reads, so nothing
  *           needs clearing).  Calls whose work overlaps on the GPU (different

@@ -12,7 +12,10 @@
 // loads the library holds it until the process exits.  In host code the
 // array's name is a host-side stand-in, not a device address, so the address
 // handed to the kernels comes from cudaGetSymbolAddress, taken once per device
-// (with that device current) on the first call there.
+// (with that device current) on the first call there and kept for the life of
+// the process.  A cudaDeviceReset destroys the context the address belongs to;
+// the library does not detect that, so the header tells callers not to use
+// this entry point on a device after resetting it.
 //
 // This file is compiled as part of the library's single translation unit (it
 // is included at the end of moe_api.cu), so its kernels report through the

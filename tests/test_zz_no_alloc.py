@@ -51,12 +51,15 @@ def test_noalloc_dispatch_matches_dispatch_on_two_calls(M):
 
 def test_noalloc_dispatch_through_the_c_abi_rejects_oversize(M):
     L = M.lib()
-    # 1.1M assignments over 256 experts need more than the 1 MiB of scratch:
-    # refused on the host, nothing enqueued
+    # 2^17 * 8 = 1,048,576 assignments over 256 experts: just over the limit
+    # (1024-assignment tiles: (1025 + 4) * 256 * 4 bytes > 1 MiB); one
+    # assignment past the exact boundary (130,561 * 8) is refused as well.
+    # Refused on the host, nothing enqueued.
     fake = ctypes.c_void_p(0x10000)
-    st = L.moe_dispatch_noalloc(None, fake, 1 << 17, 8, 64, 256, None, fake, fake, fake, None, None)
-    assert st == M.MOE_ERR_WORKSPACE
-    assert b"scratch" in L.moe_last_error()
+    for T in (1 << 17, 130561):
+        st = L.moe_dispatch_noalloc(None, fake, T, 8, 64, 256, None, fake, fake, fake, None, None)
+        assert st == M.MOE_ERR_WORKSPACE
+        assert b"scratch" in L.moe_last_error()
     # a size that fits goes through the raw C call and matches moe_dispatch
     idx, _ = _inputs(3, 4097, 160, 6, 64)
     T, k = idx.shape
@@ -73,3 +76,18 @@ def test_noalloc_dispatch_through_the_c_abi_rejects_oversize(M):
         want = M.moe_dispatch(None, idx, 160)
         M.moe_check()
         assert torch.equal(go, want[0]) and torch.equal(perm, want[1]) and torch.equal(inv, want[2])
+
+
+def test_noalloc_dispatch_at_the_exact_limit(M):
+    """130,560 tokens x top-8 over 256 experts = 1020 tiles of 1024
+    assignments: (1020 + 4) * 256 * 4 bytes = exactly 1 MiB of scratch, the
+    largest request at E = 256 that is accepted; it must match moe_dispatch."""
+    T, E, k = 130560, 256, 8
+    assert M.workspace_bytes(M.MOE_OP_DISPATCH, T, k, E) == 1 << 20
+    idx, x = _inputs(4, T, E, k, 64)
+    for _ in range(2):
+        want = M.moe_dispatch(x, idx, E, None)
+        got = M.moe_dispatch_noalloc(x, idx, E, None)
+        M.moe_check()
+        for a, b in zip(want, got):
+            assert torch.equal(a, b)
