@@ -464,7 +464,7 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world} (no data exchange)",
                    "l2": "no flush: each step streams ~1.5 GB of weights + activations, >> 126 MB L2",
                    "launch": "eager" if args.eager else f"CUDA graph per step ({c.window} graphs, one per window slot)",
-                   "front": "separate calls" if args.unfused else "moe_layer_front (3 launches, one on the side stream)",
+                   "front": "separate calls" if args.unfused else "moe_layer_front (2 launches)",
                    "ffn_kernel": args.ffn_kernel,
                    "pdl": not args.no_pdl,
                    "small_group_threshold": args.small_threshold,

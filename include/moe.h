@@ -15,7 +15,7 @@
  *   moe_combine       gate-weighted sum of each token's k expert outputs
  *
  * Fused forms of the same work: moe_layer_front (route through dispatch in
- * three launches), moe_expert_ffn_gather (the FFN reading the token rows in
+ * two launches), moe_expert_ffn_gather (the FFN reading the token rows in
  * place, so that dispatch writes only the permutation) and
  * moe_expert_ffn_combine (the combine in the second GEMM's epilogue).
  * Widened calls: moe_predict_decay and moe_replicate_predicted (replicas from
@@ -39,8 +39,7 @@
  *   work on `stream` and returns; none synchronises except moe_check,
  *   moe_stats_export and moe_stats_import.  Calls that share a moe_stats
  *   handle or a workspace must be ordered on one stream.  The expert FFN
- *   (its small-batch kernels) and moe_layer_front (its co-selection fold and
- *   prediction) run part of their work on a library-owned stream per device
+ *   calls run their small-batch kernels on a library-owned stream per device
  *   (created with two events at the first call on that device, kept for the
  *   life of the process), forked from `stream` and joined back to it within
  *   the call, so callers see ordinary stream order; calls on different
@@ -252,7 +251,7 @@ moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int
 
 /* ---------------------------------------------------------------------------
  * moe_layer_front -- route, statistics, prediction, replicas and dispatch of one
- * layer in three launches (one of them on the library's side stream).
+ * layer in two launches.
  * The same results, bit for bit, as
  *   moe_route(logits) -> moe_stats_update(st, iter, layer, idx, idx_prev) ->
  *   moe_predict(st, layer) [when p_seq != NULL] -> moe_replicate(hist, T*k)
@@ -276,13 +275,12 @@ moe_status moe_dispatch(const uint16_t* x, const int32_t* idx, int T, int k, int
  * histogram.  budget bounds the total copies in both cases (-1 = none;
  * hottest experts first).  The tokens are still dispatched by their actual
  * choices, split over the replica groups of their expert.
- * The first launch routes tiles of tokens and counts them; its last block
- * folds the histogram into the window, replicates and lays out the groups;
- * the second scatters the permutation and copies the rows.  When there is a
- * previous layer's choice or a prediction to make, a third launch, one block
- * on the library's side stream (forked after the first launch, joined back
- * into `stream` after the second), folds the co-selection counts and
- * predicts.  E must equal the handle's E.
+ * The first launch routes tiles of tokens and counts them.  In the second,
+ * one block folds the histogram and the co-selection counts into the window
+ * and predicts, while every other block computes the replica table and the
+ * group layout from the histogram (the same integers in each), then
+ * scatters the permutation of its tile and copies its rows.  E must equal
+ * the handle's E.
  * ------------------------------------------------------------------------- */
 moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E, int k, int H, int renorm,
                            moe_stats* st, int64_t iter, int layer, const int32_t* idx_prev, int replicate,

@@ -422,7 +422,7 @@ def moe_layer_front(logits, x, stats: "MoEStats", it: int, layer: int, k: int, i
                     predict: bool = True, replicate: bool = True, thresh=(6, 5), max_copies: int = -1,
                     rep_share=None, budget: int = -1, out=None, workspace=None, stream=None):
     """Route + stats update + predict + replicate + dispatch of one layer in
-    three launches, one of them on the library's side stream (results identical
+    two launches (results identical
     to the separate calls).  Returns a dict of the
     outputs: idx, w, hist, p_seq, cond, p_next, copies, rep_base, group_expert,
     group_offsets, perm, inv_perm, xp (absent ones None).  `out` may hold

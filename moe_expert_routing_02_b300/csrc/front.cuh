@@ -1,5 +1,5 @@
 // Fused front of the layer: top-k gate, token statistics and window, next-layer
-// prediction, replica counts and the dispatch, in three launches.
+// prediction, replica counts and the dispatch, in two launches.
 //
 // Same results as moe_route -> moe_stats_update -> moe_predict ->
 // moe_replicate -> moe_dispatch (PopFetcher review: gate, Routing Information
@@ -12,28 +12,24 @@
 //      within the block, and the block's totals (blk_tot, and added to the
 //      histogram accumulator); the co-selection pairs with the previous
 //      layer's routing (shared atomics, flushed to the window state's
-//      accumulator).  The last block to finish (ticket after a fence) then,
-//      alone:
-//        - takes the histogram from the accumulator,
-//        - folds the histogram into the window ring and sums, and, unless
-//          they are deferred to F3, the co-selection counts (as
-//          stats::update_kernel does) and the prediction of the next layer
-//          (stats::predict_block),
-//        - computes replica counts (replicate::replicate_block) from the
-//          histogram, or from the apportionment of a predicted popularity
-//          (replicate::apportion_block) when one is given,
-//        - lays out the groups (closed form of the round-robin split).
-//   F2 (scatter_copy_kernel), one block per tile: the tile's starting rank
-//      per expert (totals of the route blocks before its own, plus its
-//      prefix within its block), stable in-tile ranks -> slots -> perm /
-//      inv_perm, then the rows of the tile's assignments are copied to their
-//      slots with 16-byte vectors.
-//   F3 (stats_tail_kernel), one block on the side stream, forked after F1
-//      and joined after F2: the co-selection fold and the prediction, which
-//      the dispatch does not read, run beside F2 instead of inside the plan.
-// The plan (last block) thus reads O(E) and O(E^2) values only; the
-// per-tile prefix over the route blocks is spread over the F2 blocks.
-// Counts are integers, so nothing depends on the order of atomics.
+//      accumulator).
+//   F2 (scatter_copy_kernel), one block per tile plus one statistics block.
+//      Every block takes the histogram from the accumulator.  The statistics
+//      block folds it and the co-selection counts into the window ring and
+//      sums (as stats::update_kernel does) and predicts the next layer
+//      (stats::predict_block); the dispatch reads none of that, so it runs
+//      beside the tiles.  Each tile block computes the replica counts
+//      (replicate::replicate_block, or replicate::apportion_block first when
+//      a predicted popularity is given) and the group layout (closed form of
+//      the round-robin split) itself -- O(E) integer work, the same in every
+//      block -- then the tile's starting rank per expert (totals of the route
+//      blocks before its own, plus its prefix within its block), stable
+//      in-tile ranks -> slots -> perm / inv_perm, and the copy of the rows of
+//      the tile's assignments to their slots with 16-byte vectors.
+// No block waits for a single planner: the plan that one block used to run
+// after all the routing (histogram fold, prediction, replica table, layout)
+// is spread over the blocks that need it.  Counts are integers, so nothing
+// depends on the order of atomics.
 #pragma once
 #include "common.cuh"
 #include "dispatch.cuh"
@@ -58,7 +54,8 @@ __host__ inline long long num_tiles(long long T) { return (T + tile_tokens(T) - 
 // Route blocks: at most kMaxRouteBlocks (the F2 prologue reads the totals
 // of the blocks before its own), and at least one pass of every warp.
 constexpr int kMaxRouteBlocks = 128;
-// Workspace: tile prefixes [ntiles][E], block totals [<= ntiles][E], info [4][E].
+// Workspace: tile prefixes [ntiles][E], block totals [<= ntiles][E] (the
+// size keeps room for [4][E] more words).
 __host__ inline size_t workspace_bytes(long long T, int E) {
   const long long nt = num_tiles(T) > 0 ? num_tiles(T) : 1;
   return (size_t)(2 * nt * E + 4LL * E) * sizeof(int32_t);
@@ -75,15 +72,12 @@ struct Args {
   const int32_t* idx_prev;
   uint32_t* acc_h;   // [E] histogram accumulator (zero between calls)
   uint32_t* acc_c;   // [E*E] co-selection accumulator (zero between calls)
-  uint32_t* ticket;
+  uint32_t* ticket;  // F2 blocks that took the histogram (zero between calls)
   uint32_t* ring_h;
   unsigned long long* hsum;
   uint32_t* ring_c;
   unsigned long long* csum;
   int32_t* hist_out;
-  // deferred = 1: the co-selection window fold and the prediction are left
-  // to stats_tail_kernel (launched beside the scatter/copy), not the plan
-  int deferred;
   // prediction (p_seq == null: skipped); pred_csum null for the last layer
   const unsigned long long* pred_csum;
   float* p_seq;
@@ -101,7 +95,6 @@ struct Args {
   long long ntiles;
   int32_t* counts;   // [ntiles][E]: tile's exclusive prefix within its route block
   int32_t* blk_tot;  // [route blocks][E]: block totals
-  int32_t* info;     // [4][E]: expert base, replicas, rows, loads from rep_share
   int32_t* group_offsets;
 };
 
@@ -115,13 +108,20 @@ __device__ __forceinline__ void fold_cosel(const Args& a) {
   }
 }
 
-// The part of the plan that the dispatch does not wait for: the co-selection
-// window fold and the prediction for the next layer (one block, after the
-// route/plan kernel, beside the scatter/copy).
-__global__ void __launch_bounds__(kThreads) stats_tail_kernel(Args a) {
+// The statistics block of F2: the histogram into the window ring and sums,
+// the co-selection counts likewise, then the prediction for the next layer.
+// Nothing in the dispatch reads these, so the block runs beside the copy.
+__device__ __forceinline__ void stats_tail(const Args& a, const int32_t* hist_s) {
+  for (int e = threadIdx.x; e < a.E; e += kThreads) {
+    const int32_t h = hist_s[e];
+    const uint32_t old = a.ring_h[e];
+    a.ring_h[e] = (uint32_t)h;
+    a.hsum[e] = a.hsum[e] + (uint32_t)h - old;
+    if (a.hist_out) a.hist_out[e] = h;
+  }
   if (a.has_prev) fold_cosel(a);
-  __syncthreads();
-  if (a.p_seq) stats::predict_block<unsigned long long>(a.hsum, a.pred_csum, a.E, a.p_seq, a.cond, a.p_next);
+  __syncthreads();  // hsum and csum written above are read by other threads below
+  if (a.p_seq) stats::predict_block<unsigned long long, 16>(a.hsum, a.pred_csum, a.E, a.p_seq, a.cond, a.p_next);
 }
 
 template <int G, bool VEC>
@@ -202,109 +202,117 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
   if (cos_smem)
     for (int i = threadIdx.x; i < E * E; i += kThreads)
       if (cs[i]) atomicAdd(a.acc_c + i, cs[i]);
+}
 
-  // ---- the last block plans the layer
-  __shared__ bool is_last;
-  __shared__ int32_t hist_s[256];
+// Dynamic shared memory of scatter_copy_kernel, in int32 words.
+__host__ __device__ inline int scatter_smem_words(int E, int TT, int k) { return (16 + kWarps) * E + 1 + TT * k; }
+
+// F2.  Block 0 is the statistics block (stats_tail); block b >= 1 serves
+// dispatch tile b - 1.  Every block first takes the layer's histogram from the
+// accumulator the route blocks added their totals to; the last block to take
+// it clears the accumulator (and the ticket) for the next call.  A tile block
+// then computes the replica table and the group layout itself -- O(E) integer
+// work, identical in every block -- so no block waits for a single planner;
+// tile 0's block writes the tables out.  Then: the tile's starting rank per
+// expert (totals of the route blocks before its own, plus its prefix within
+// its block), stable in-tile ranks of its assignments (in f order), slots,
+// perm / inv_perm, and the row copy xp[slot] = x[f / k].
+__global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, const uint16_t* __restrict__ x, int H,
+                                                                uint16_t* __restrict__ xp,
+                                                                int32_t* __restrict__ perm,
+                                                                int32_t* __restrict__ inv_perm) {
+  pdl_wait();
+  extern __shared__ int32_t sm[];
+  const int E = a.E, k = a.k;
+  int32_t* hist_s = sm;                   // [E]
+  int32_t* base_s = hist_s + E;           // [E]   first slot of the expert's rows
+  int32_t* n_s = base_s + E;              // [E]   replica groups of the expert
+  int32_t* rb_s = n_s + E;                // [E+1] first group of the expert
+  int32_t* copies_s = rb_s + E + 1;       // [E]
+  int32_t* ge_s = copies_s + E;           // [2E]
+  int32_t* load_s = ge_s + 2 * E;         // [E]   loads apportioned from the shares
+  int32_t* warp_cnt = load_s + E;         // [kWarps][E]
+  int32_t* run = warp_cnt + kWarps * E;   // [E]
+  int32_t* slot_s = run + E;              // [TT*k]
   __shared__ int32_t wtot[kWarps];
-  __threadfence();
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
+  for (int e = tid; e < E; e += kThreads) hist_s[e] = (int32_t)a.acc_h[e];
   __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  const int e = threadIdx.x;
-  if (e < E) {
-    const int h = (int)atomicExch(a.acc_h + e, 0u);
-    hist_s[e] = h;
-    // window: histogram slot and sums
-    const uint32_t old = a.ring_h[e];
-    a.ring_h[e] = (uint32_t)h;
-    a.hsum[e] = a.hsum[e] + (uint32_t)h - old;
-    if (a.hist_out) a.hist_out[e] = h;
+  if (tid == 0 && atomicAdd(a.ticket, 1u) == gridDim.x - 1) {
+    // every block holds its copy of the histogram now
+    for (int e = 0; e < E; ++e) a.acc_h[e] = 0u;
+    *a.ticket = 0u;
   }
-  if (!a.deferred) {
-    if (cos) fold_cosel(a);
-    __syncthreads();
-    if (a.p_seq) stats::predict_block<unsigned long long>(a.hsum, a.pred_csum, E, a.p_seq, a.cond, a.p_next);
+  if (blockIdx.x == 0) {
+    stats_tail(a, hist_s);
+    return;
   }
-  __syncthreads();
+  const int tile = (int)blockIdx.x - 1;
   const long long A = (long long)a.T * k;
+
+  // ---- replica table and group layout
   if (a.replicate) {
     const int32_t* ld = hist_s;
     if (a.rep_share) {  // replicas from a prediction: loads apportioned by the shares
-      replicate::apportion_block(a.rep_share, E, A, a.info + 3 * E);
+      replicate::apportion_block(a.rep_share, E, A, load_s);
       __syncthreads();
-      ld = a.info + 3 * E;
+      ld = load_s;
     }
-    replicate::replicate_block(ld, E, A, a.num, a.den, a.max_copies, a.copies, a.rep_base, a.group_expert,
-                               a.budget);
+    replicate::replicate_block(ld, E, A, a.num, a.den, a.max_copies, copies_s, rb_s, ge_s, a.budget);
+  } else {
+    for (int e = tid; e <= E; e += kThreads) rb_s[e] = e;
   }
   __syncthreads();
-  // group layout: expert bases (exclusive scan of the histogram), replicas,
-  // group offsets in the closed form of the round-robin split
-  const int lane2 = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  // expert bases: exclusive scan of the histogram (E <= kThreads)
+  const int e = tid;
   int incl = e < E ? hist_s[e] : 0;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane2 >= off) incl += v;
+    if (lane >= off) incl += v;
   }
-  if (lane2 == 31) wtot[wid] = incl;
+  if (lane == 31) wtot[wid] = incl;
   __syncthreads();
   int before = 0;
   for (int ww = 0; ww < wid; ++ww) before += wtot[ww];
-  const int ngroups = a.replicate ? a.rep_base[E] : E;
   if (e < E) {
-    const int hh = hist_s[e];
-    const int base = before + incl - hh;
-    int n = 1, rb = e;
-    if (a.replicate) {
-      rb = a.rep_base[e];
-      n = a.rep_base[e + 1] - rb;
-    }
-    a.info[e] = base;
-    a.info[E + e] = n;
-    a.info[2 * E + e] = hh;
-    const int qs = hh / n, qr = hh % n;
-    for (int q = 0; q < n; ++q) a.group_offsets[rb + q] = base + q * qs + (q < qr ? q : qr);
+    base_s[e] = before + incl - hist_s[e];
+    n_s[e] = rb_s[e + 1] - rb_s[e];
   }
-  for (int g = ngroups + threadIdx.x; g <= 2 * E; g += kThreads) a.group_offsets[g] = (int32_t)A;
-  if (threadIdx.x == 0) *a.ticket = 0;
-}
+  __syncthreads();
+  if (tile == 0) {
+    const int ngroups = rb_s[E];
+    if (e < E) {
+      const int hh = hist_s[e], n = n_s[e], rb = rb_s[e], base = base_s[e];
+      const int qs = hh / n, qr = hh % n;
+      for (int q = 0; q < n; ++q) a.group_offsets[rb + q] = base + q * qs + (q < qr ? q : qr);
+      if (a.replicate) {
+        a.copies[e] = copies_s[e];
+        a.rep_base[e] = rb;
+      }
+    }
+    if (a.replicate) {
+      if (tid == 0) a.rep_base[E] = ngroups;
+      for (int g = tid; g < 2 * E; g += kThreads) a.group_expert[g] = ge_s[g];
+    }
+    for (int g = ngroups + tid; g <= 2 * E; g += kThreads) a.group_offsets[g] = (int32_t)A;
+  }
 
-// One block per tile: the tile's starting ranks, stable ranks of its
-// assignments (in f order), slots, perm / inv_perm, then the row copy
-// xp[slot] = x[f / k].
-__global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const int32_t* __restrict__ idx, long long T, int k,
-                                                                int E, int TT, int tpb,
-                                                                const int32_t* __restrict__ tile_pre,
-                                                                const int32_t* __restrict__ blk_tot,
-                                                                const int32_t* __restrict__ info,
-                                                                int32_t* __restrict__ perm,
-                                                                int32_t* __restrict__ inv_perm,
-                                                                const uint16_t* __restrict__ x, int H,
-                                                                uint16_t* __restrict__ xp) {
-  pdl_wait();
-  extern __shared__ int32_t sm[];
-  int32_t* warp_cnt = sm;                 // [kWarps][E]
-  int32_t* run = sm + kWarps * E;         // [E]
-  int32_t* slot_s = run + E;              // [TT*k]
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const long long A = T * k;
-  const long long f0 = (long long)blockIdx.x * TT * k;
-  long long f1 = f0 + (long long)TT * k;
+  // ---- starting ranks of the tile
+  const long long f0 = (long long)tile * a.TT * k;
+  long long f1 = f0 + (long long)a.TT * k;
   if (f1 > A) f1 = A;
   const int nA = (int)(f1 - f0);
   for (int i = tid; i < kWarps * E; i += kThreads) warp_cnt[i] = 0;
-  for (int i = tid; i < E; i += kThreads) run[i] = tile_pre[(size_t)blockIdx.x * E + i];
+  for (int i = tid; i < E; i += kThreads) run[i] = a.counts[(size_t)tile * E + i];
   __syncthreads();
-  // starting rank of the tile: add the totals of the route blocks before its own
-  const int nprev = (int)(blockIdx.x / tpb) * E;
+  // add the totals of the route blocks before the tile's own
+  const int nprev = (tile / a.tiles_per_block) * E;
   for (int i0 = tid; i0 < nprev; i0 += 8 * kThreads) {
     int v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = i0 + u * kThreads < nprev ? blk_tot[i0 + u * kThreads] : 0;
+    for (int u = 0; u < 8; ++u) v[u] = i0 + u * kThreads < nprev ? a.blk_tot[i0 + u * kThreads] : 0;
 #pragma unroll
     for (int u = 0; u < 8; ++u)
       if (v[u]) atomicAdd(&run[(i0 + u * kThreads) % E], v[u]);
@@ -312,19 +320,19 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const int32_t* _
   __syncthreads();
   for (int r0 = 0; r0 < nA; r0 += kThreads) {
     const int i = r0 + tid;
-    int e = -1;
+    int ex = -1;
     if (i < nA) {
-      e = idx[f0 + i];
-      if ((unsigned)e >= (unsigned)E) e = -1;
+      ex = a.idx[f0 + i];
+      if ((unsigned)ex >= (unsigned)E) ex = -1;
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) warp_cnt[wid * E + e] = __popc(peers);
+    const unsigned peers = __match_any_sync(0xffffffffu, ex);
+    if (ex >= 0 && lane == __ffs(peers) - 1) warp_cnt[wid * E + ex] = __popc(peers);
     __syncthreads();
     int slot = -1;
-    if (e >= 0) {
-      int m = run[e] + __popc(peers & lanemask_lt());
-      for (int w = 0; w < wid; ++w) m += warp_cnt[w * E + e];
-      const int base = info[e], n = info[E + e], h = info[2 * E + e];
+    if (ex >= 0) {
+      int m = run[ex] + __popc(peers & lanemask_lt());
+      for (int w = 0; w < wid; ++w) m += warp_cnt[w * E + ex];
+      const int base = base_s[ex], n = n_s[ex], h = hist_s[ex];
       const int q = m % n, pos = m / n, qs = h / n, qr = h % n;
       slot = base + q * qs + (q < qr ? q : qr) + pos;
       if ((unsigned long long)slot < (unsigned long long)A) {
@@ -379,19 +387,21 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const int32_t* _
 }
 
 // Dynamic shared memory of route_count_kernel stays below 17 KB (tile counts
-// plus, for E <= 64, the E*E co-selection bins); with the block-level static
-// arrays of the plan phase it passes 48 KB, so the limit is raised once per
-// device and kernel instance.
+// plus, for E <= 64, the E*E co-selection bins); that of scatter_copy_kernel
+// below 29 KB (E = 256, 128-token tiles of top-8), which with the static
+// arrays of the replica, apportionment and prediction block functions can pass
+// 48 KB.  The limits are raised once per device and kernel instance.
 constexpr int kRouteDynSmemMax = 20 * 1024;
+constexpr int kScatterDynSmemMax = 32 * 1024;
 
 template <typename K>
-static cudaError_t ensure_smem_attr(K kernel, bool* done_per_device) {
+static cudaError_t ensure_smem_attr(K kernel, bool* done_per_device, int bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (done_per_device[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteDynSmemMax);
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) done_per_device[dev] = true;
   return e;
 }
@@ -418,12 +428,12 @@ static cudaError_t launch_route_g(const Args& a, bool vec, cudaStream_t st) {
   const size_t smem = sizeof(uint32_t) * ((size_t)a.tiles_per_block * a.E + (cos_smem ? (size_t)a.E * a.E : 0));
   if (smem > (size_t)kRouteDynSmemMax) return cudaErrorInvalidValue;
   if (vec) {
-    cudaError_t e = ensure_smem_attr(route_count_kernel<G, true>, done_vec);
+    cudaError_t e = ensure_smem_attr(route_count_kernel<G, true>, done_vec, kRouteDynSmemMax);
     if (e != cudaSuccess) return e;
     e = launch_pdl(route_count_kernel<G, true>, dim3((unsigned)blocks), dim3(kThreads), smem, st, a);
     if (e != cudaSuccess) return e;
   } else {
-    cudaError_t e = ensure_smem_attr(route_count_kernel<G, false>, done_scalar);
+    cudaError_t e = ensure_smem_attr(route_count_kernel<G, false>, done_scalar, kRouteDynSmemMax);
     if (e != cudaSuccess) return e;
     e = launch_pdl(route_count_kernel<G, false>, dim3((unsigned)blocks), dim3(kThreads), smem, st, a);
     if (e != cudaSuccess) return e;
@@ -431,15 +441,9 @@ static cudaError_t launch_route_g(const Args& a, bool vec, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// side != null: the co-selection fold and the prediction run in
-// stats_tail_kernel on `side`, forked after the route/plan kernel through
-// fork_ev and joined back into `st` after the scatter/copy through join_ev.
 static cudaError_t launch(const Args& a0, const uint16_t* x, int H, uint16_t* xp, int32_t* perm, int32_t* inv_perm,
-                          cudaStream_t st, cudaStream_t side = nullptr, cudaEvent_t fork_ev = nullptr,
-                          cudaEvent_t join_ev = nullptr) {
+                          cudaStream_t st) {
   Args a = a0;
-  const bool tail = side != nullptr && (a.has_prev || a.p_seq != nullptr);
-  a.deferred = tail ? 1 : 0;
   a.tiles_per_block = route_tiles_per_block(a.T, a.E);
   const bool vec = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.logits) & 15) == 0);
   cudaError_t e;
@@ -450,21 +454,14 @@ static cudaError_t launch(const Args& a0, const uint16_t* x, int H, uint16_t* xp
   else if (a.E <= 128) e = launch_route_g<16>(a, vec, st);
   else e = launch_route_g<32>(a, vec, st);
   if (e != cudaSuccess) return e;
-  if (tail) {
-    if ((e = cudaEventRecord(fork_ev, st)) != cudaSuccess) return e;
-    if ((e = cudaStreamWaitEvent(side, fork_ev, 0)) != cudaSuccess) return e;
-    stats_tail_kernel<<<1, kThreads, 0, side>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  const size_t smem = sizeof(int32_t) * ((size_t)(kWarps + 1) * a.E + (size_t)a.TT * a.k);
-  e = launch_pdl(scatter_copy_kernel, dim3((unsigned)a.ntiles), dim3(kThreads), smem, st, a.idx, a.T, a.k, a.E,
-                 a.TT, a.tiles_per_block, a.counts, a.blk_tot, a.info, perm, inv_perm, x, H, xp);
-  if (tail) {
-    cudaError_t j = cudaEventRecord(join_ev, side);
-    if (j == cudaSuccess) j = cudaStreamWaitEvent(st, join_ev, 0);
-    if (e == cudaSuccess) e = j;
-  }
-  return e;
+  static bool done_scatter[64] = {};
+  const size_t smem = sizeof(int32_t) * (size_t)scatter_smem_words(a.E, a.TT, a.k);
+  if (smem > (size_t)kScatterDynSmemMax) return cudaErrorInvalidValue;
+  if ((e = ensure_smem_attr(scatter_copy_kernel, done_scatter, kScatterDynSmemMax)) != cudaSuccess) return e;
+  e = launch_pdl(scatter_copy_kernel, dim3((unsigned)(a.ntiles + 1)), dim3(kThreads), smem, st, a, x, H, xp, perm,
+                 inv_perm);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace front

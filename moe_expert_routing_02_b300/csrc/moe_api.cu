@@ -509,16 +509,8 @@ moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E,
   a.ntiles = front::num_tiles(T);
   a.counts = static_cast<int32_t*>(workspace);
   a.blk_tot = a.counts + a.ntiles * E;
-  a.info = a.blk_tot + a.ntiles * E;
   a.group_offsets = group_offsets;
-  // the fold of the co-selection counts and the prediction run beside the
-  // scatter/copy on the device's side stream (one fork/join at a time)
-  DeviceInfo* d = nullptr;
-  moe_status ms = device_info(&d);
-  if (ms != MOE_OK) return ms;
-  std::lock_guard<std::mutex> side_lock(g_side_mu);
-  return cuda_status(front::launch(a, x, H, xp, perm, inv_perm, static_cast<cudaStream_t>(stream), d->side,
-                                   d->fork_ev, d->join_ev),
+  return cuda_status(front::launch(a, x, H, xp, perm, inv_perm, static_cast<cudaStream_t>(stream)),
                      "moe_layer_front launch");
 }
 

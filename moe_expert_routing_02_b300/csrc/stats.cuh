@@ -159,7 +159,10 @@ constexpr int kPredictSmemE = 64;  // Cbar staged in shared memory up to E = 64
 // block reaches it with all threads.  S is the type of the window sums:
 // unsigned long long (plain window) or double (decay-weighted window; integer
 // sums are exact in double, so both give the same result for equal sums).
-template <typename S>
+// Cbar is staged in shared memory for E <= STAGE_E (a kernel that runs this
+// in one of many blocks keeps STAGE_E small, since the staging array is part
+// of every block's static shared memory); the result does not depend on it.
+template <typename S, int STAGE_E = kPredictSmemE>
 __device__ __forceinline__ void predict_block(const S* __restrict__ hsum, const S* __restrict__ csum, int E,
                                               float* __restrict__ p_seq, float* __restrict__ cond,
                                               float* __restrict__ p_next) {
@@ -167,9 +170,9 @@ __device__ __forceinline__ void predict_block(const S* __restrict__ hsum, const 
   __shared__ double rinv[256];   // 1 / row sum, or 0 for an empty row
   __shared__ S rsum[256];
   __shared__ S wsum[kThreads / 32];
-  __shared__ S cs[kPredictSmemE * kPredictSmemE];
+  __shared__ S cs[STAGE_E * STAGE_E];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const bool stage = csum != nullptr && E <= kPredictSmemE;
+  const bool stage = csum != nullptr && E <= STAGE_E;
   S h = tid < E ? hsum[tid] : S(0);
   if (stage)
     for (int i = tid; i < E * E; i += kThreads) cs[i] = csum[i];

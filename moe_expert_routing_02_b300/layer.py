@@ -21,10 +21,9 @@ __all__ = ["MoELayerStep", "MoESaved", "ChunkedLayerStep", "HostPipeline", "capt
 
 
 def _front_launches(layer: int, predict: bool) -> int:
-    """Kernels moe_layer_front launches: route/plan and scatter/copy, plus the
-    co-selection fold and prediction on the side stream when there is a
-    previous layer's choice or a prediction to make."""
-    return 2 + (1 if layer > 0 or predict else 0)
+    """Kernels moe_layer_front launches: route/count, then the statistics
+    block beside the plan, scatter and copy of every tile."""
+    return 2
 
 
 class MoESaved:
@@ -46,9 +45,7 @@ class MoELayerStep:
     unchanged); it needs stats, whose update writes that histogram.  stats
     (MoEStats) is shared by all layers of a model.
     fused=True (needs stats) runs route, statistics, prediction, replicas and
-    dispatch as moe_layer_front (two launches, plus a third on the side stream
-    for the co-selection fold and prediction when layer > 0 or predict=True);
-    fused=False makes the five
+    dispatch as moe_layer_front (two launches); fused=False makes the five
     separate calls.  gather=True leaves the token rows in place: dispatch
     writes only the permutation and the FFN's first GEMM reads the rows of x
     through it (moe_expert_ffn_gather); gather=False copies the rows into
