@@ -41,6 +41,36 @@ struct UpdateArgs {
 
 constexpr int kTokensAhead = 4;
 
+// The last block to finish (ticket after a fence) moves the accumulated
+// totals into ring slot iter % s, updates the window sums by (new - old) and
+// zeroes the accumulator and the ticket for the next call.
+template <int NT>
+__device__ __forceinline__ void fold_last_block(const UpdateArgs& a) {
+  __shared__ bool is_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < a.E; i += NT) {
+    const uint32_t nw = atomicExch(a.acc_h + i, 0u);
+    const uint32_t old = a.ring_h[i];
+    a.ring_h[i] = nw;
+    a.hsum[i] = a.hsum[i] + nw - old;
+    if (a.hist_out) a.hist_out[i] = (int32_t)nw;
+  }
+  if (a.has_prev) {
+    for (int i = threadIdx.x; i < a.E * a.E; i += NT) {
+      const uint32_t nw = atomicExch(a.acc_c + i, 0u);
+      const uint32_t old = a.ring_c[i];
+      a.ring_c[i] = nw;
+      a.csum[i] = a.csum[i] + nw - old;
+    }
+  }
+  if (threadIdx.x == 0) *a.ticket = 0;
+}
+
 __global__ void __launch_bounds__(kThreads) update_kernel(UpdateArgs a) {
   extern __shared__ uint32_t sh[];
   const int E = a.E, k = a.k;
@@ -111,33 +141,129 @@ __global__ void __launch_bounds__(kThreads) update_kernel(UpdateArgs a) {
     for (int i = threadIdx.x; i < E * E; i += kThreads)
       if (sh_c[i]) atomicAdd(a.acc_c + i, sh_c[i]);
 
-  // last block folds the totals into the window
-  __shared__ bool is_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  for (int i = threadIdx.x; i < E; i += kThreads) {
-    const uint32_t nw = atomicExch(a.acc_h + i, 0u);
-    const uint32_t old = a.ring_h[i];
-    a.ring_h[i] = nw;
-    a.hsum[i] = a.hsum[i] + nw - old;
-    if (a.hist_out) a.hist_out[i] = (int32_t)nw;
-  }
-  if (cos) {
-    for (int i = threadIdx.x; i < E * E; i += kThreads) {
-      const uint32_t nw = atomicExch(a.acc_c + i, 0u);
-      const uint32_t old = a.ring_c[i];
-      a.ring_c[i] = nw;
-      a.csum[i] = a.csum[i] + nw - old;
-    }
-  }
-  if (threadIdx.x == 0) *a.ticket = 0;
+  fold_last_block<kThreads>(a);
 }
 
+// E <= 16: the histogram lives in 16 registers per thread (a compare-and-add
+// per bin, no dynamic indexing), so the Zipf-skewed hot bins take no atomics
+// at all; each warp counts its co-selection pairs into its own E*E bins in
+// shared memory (8 KB per block), so shared atomics meet only the other lanes
+// of their warp, not the whole block.  At the end the warps' bins are summed
+// per bin, the histogram per warp by shuffles, each block adds its non-zero
+// bins to the global accumulator, and the last block folds as update_kernel
+// does.
+constexpr int kSmallE = 16;
+constexpr int kSmallThreads = 256;
+constexpr int kSmallWarps = kSmallThreads / 32;
+
+// KM: the largest k the instance handles (2 covers top-1 and top-2 with far
+// fewer registers; 8 the rest).
+template <int KM>
+__global__ void __launch_bounds__(kSmallThreads, 2) update_small_kernel(UpdateArgs a) {
+  __shared__ uint32_t wb[kSmallWarps][kSmallE * kSmallE];  // per-warp co-selection bins p * 16 + c
+  __shared__ uint32_t hs[kSmallE];
+  const int E = a.E, k = a.k;
+  const bool cos = a.has_prev != 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < kSmallE) hs[threadIdx.x] = 0;
+  if (cos)
+    for (int i = threadIdx.x; i < kSmallWarps * kSmallE * kSmallE; i += kSmallThreads) (&wb[0][0])[i] = 0u;
+  __syncthreads();
+  uint32_t* mb = wb[warp];
+  uint32_t h[kSmallE];
+#pragma unroll
+  for (int q = 0; q < kSmallE; ++q) h[q] = 0u;
+
+  constexpr int U = KM <= 2 ? kTokensAhead : 2;  // tokens in flight per thread, within 128 registers
+  const long long stride = (long long)gridDim.x * kSmallThreads * U;
+  bool bad = false;
+  for (long long base = (long long)blockIdx.x * kSmallThreads * U + threadIdx.x; base < a.T; base += stride) {
+    int cur[U][KM], prv[U][KM];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long t = base + (long long)u * kSmallThreads;
+      const bool live = t < a.T;
+#pragma unroll
+      for (int r = 0; r < KM; ++r) {
+        cur[u][r] = -1;
+        prv[u][r] = -1;
+        if (r < k && live) {
+          cur[u][r] = a.idx_cur[t * k + r];
+          if (cos) prv[u][r] = a.idx_prev[t * k + r];
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (base + (long long)u * kSmallThreads >= a.T) continue;
+#pragma unroll
+      for (int r = 0; r < KM; ++r) {
+        if (r < k) {
+          const int e = cur[u][r];
+          if ((unsigned)e >= (unsigned)E) {
+            bad = true;
+            continue;
+          }
+#pragma unroll
+          for (int q = 0; q < kSmallE; ++q) h[q] += (e == q) ? 1u : 0u;
+        }
+      }
+      if (cos) {
+#pragma unroll
+        for (int r1 = 0; r1 < KM; ++r1) {
+          if (r1 < k) {
+            const int pe = prv[u][r1];
+            if ((unsigned)pe >= (unsigned)E) {
+              bad = true;
+              continue;
+            }
+#pragma unroll
+            for (int r2 = 0; r2 < KM; ++r2)
+              if (r2 < k && (unsigned)cur[u][r2] < (unsigned)E) atomicAdd(mb + pe * kSmallE + cur[u][r2], 1u);
+          }
+        }
+      }
+    }
+  }
+  if (bad) moe_flag_error(MOE_DEVERR_DATA);
+  // histogram: warp sums by butterflies, then one shared add per warp and bin
+#pragma unroll
+  for (int q = 0; q < kSmallE; ++q) {
+    uint32_t v = h[q];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    h[q] = v;
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int q = 0; q < kSmallE; ++q)
+      if (h[q]) atomicAdd(&hs[q], h[q]);
+  }
+  __syncthreads();
+  if (cos) {
+    const int b = threadIdx.x;  // kSmallThreads == 16 * 16 bins
+    uint32_t v = 0;
+#pragma unroll
+    for (int w = 0; w < kSmallWarps; ++w) v += wb[w][b];
+    const int p = b / kSmallE, c = b % kSmallE;
+    if (v && p < E && c < E) atomicAdd(a.acc_c + p * E + c, v);
+  }
+  if (threadIdx.x < E && hs[threadIdx.x]) atomicAdd(a.acc_h + threadIdx.x, hs[threadIdx.x]);
+  fold_last_block<kSmallThreads>(a);
+}
+static_assert(kSmallThreads == kSmallE * kSmallE, "one thread per co-selection bin in the block sum");
+
 static cudaError_t launch_update(const UpdateArgs& a, int num_sms, cudaStream_t st) {
+  if (a.E <= kSmallE) {
+    long long blocks = ((long long)a.T + kTokensAhead * kSmallThreads - 1) / (kTokensAhead * kSmallThreads);
+    if (blocks > 2LL * num_sms) blocks = 2LL * num_sms;  // each block flushes up to E + E*E bins
+    if (blocks < 1) blocks = 1;
+    if (a.k <= 2)
+      update_small_kernel<2><<<(int)blocks, kSmallThreads, 0, st>>>(a);
+    else
+      update_small_kernel<8><<<(int)blocks, kSmallThreads, 0, st>>>(a);
+    return cudaGetLastError();
+  }
   const bool cos_smem = a.has_prev != 0 && a.E <= kSmemCoselMaxE;
   const size_t smem = sizeof(uint32_t) * (a.E + (cos_smem ? a.E * a.E : 0));
   long long blocks = ((long long)a.T + kTokensAhead * kThreads - 1) / (kTokensAhead * kThreads);
