@@ -231,7 +231,7 @@ __device__ __forceinline__ void select_k16(const float (&v)[16], unsigned valid,
 template <int G, bool VEC, int K>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict__ logits, int T, int E,
                                                         int renorm, int32_t* __restrict__ idx,
-                                                        float* __restrict__ wout) {
+                                                        float* __restrict__ wout, int vec_store) {
   constexpr int TPW = 32 / G;
   const int lane = threadIdx.x & 31, gl = lane % G;
   const long long t = (((long long)blockIdx.x * kThreads + threadIdx.x) >> 5) * TPW + lane / G;
@@ -242,6 +242,24 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
   load_token16<G, VEC>(logits + (size_t)(live ? t : 0) * E, live, E, v, valid);
   select_k16<G, K>(v, valid, live, E, renorm, sel_i, ex, &denom);
   if (!live) return;
+  if (G == 1 && (K == 2 || K == 4 || K == 8) && vec_store) {
+    // one lane holds the whole token: its K indices and weights as vector
+    // stores (K * 4 bytes at t * K * 4; vec_store says idx and w are
+    // 16-byte aligned)
+#pragma unroll
+    for (int r = 0; r < K; r += (K == 2 ? 2 : 4)) {
+      if (K == 2) {
+        *reinterpret_cast<int2*>(idx + (size_t)t * K + r) = make_int2(sel_i[r], sel_i[r + 1]);
+        *reinterpret_cast<float2*>(wout + (size_t)t * K + r) = make_float2(ex[r] / denom, ex[r + 1] / denom);
+      } else {
+        *reinterpret_cast<int4*>(idx + (size_t)t * K + r) =
+            make_int4(sel_i[r], sel_i[r + 1], sel_i[r + 2], sel_i[r + 3]);
+        *reinterpret_cast<float4*>(wout + (size_t)t * K + r) =
+            make_float4(ex[r] / denom, ex[r + 1] / denom, ex[r + 2] / denom, ex[r + 3] / denom);
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int r = 0; r < K; ++r) {
     if ((r % G) == gl) {
@@ -256,10 +274,11 @@ static cudaError_t launch_gk(const float* logits, int T, int E, int renorm, int3
   constexpr int tokens_per_block = (kThreads / 32) * (32 / G);
   const long long blocks = ((long long)T + tokens_per_block - 1) / tokens_per_block;
   const bool vec = (E % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
+  const int vst = ((reinterpret_cast<uintptr_t>(idx) | reinterpret_cast<uintptr_t>(w)) & 15) == 0 ? 1 : 0;
   if (vec)
-    topk_kernel<G, true, K><<<(unsigned)blocks, kThreads, 0, st>>>(logits, T, E, renorm, idx, w);
+    topk_kernel<G, true, K><<<(unsigned)blocks, kThreads, 0, st>>>(logits, T, E, renorm, idx, w, vst);
   else
-    topk_kernel<G, false, K><<<(unsigned)blocks, kThreads, 0, st>>>(logits, T, E, renorm, idx, w);
+    topk_kernel<G, false, K><<<(unsigned)blocks, kThreads, 0, st>>>(logits, T, E, renorm, idx, w, vst);
   return cudaGetLastError();
 }
 
