@@ -181,12 +181,14 @@ struct Smem {
   uint32_t tmem_base;
   uint32_t abort_flag;
   int32_t total_tiles;
+  int32_t total_a;           // tiles of the weight-streaming class (unit_tile_prefix)
   int32_t u_count;
   int32_t goff[MAX_G + 1];   // staged group offsets
   int32_t us[MAX_G + 1];     // unit first rows (build_units)
-  int32_t tstart[MAX_G + 1];
+  int32_t tstart[MAX_G + 1]; // first tile of the i-th unit in class order
   int32_t mt[MAX_G];
   int32_t ex[MAX_G];         // unit experts
+  int32_t ord[MAX_G];        // units in class order
   alignas(128) uint8_t stg[EPI_WARPS][1024];  // per-warp output staging (store_rows32; 16-byte accesses)
 };
 
@@ -278,9 +280,17 @@ __device__ int build_units(const Params& p, int32_t* goff, int32_t* us, int32_t*
 
 // Tiles of each unit and their prefix (warp 0): tiles_u = ceil(rows_u / tile_rows)
 // * n_tiles for units the caller's filter keeps (keep(rows) -> bool), else 0.
+// Without `ord`, tstart[u] is unit u's first tile (units in row order).  With
+// `ord`, the units are taken in class order -- first those of one row tile
+// (mt == 1: each weight tile serves one row tile, so they stream weights and
+// are bound by HBM), then the others (bound by the tensor pipe) -- ord[i] is
+// the i-th unit of that order, tstart[i] its first tile and *total_a the
+// tiles of the first class; interleave() then spreads the two classes over
+// the schedule.
 template <int NT, typename Keep>
 __device__ void unit_tile_prefix(const Params& p, int U, const int32_t* us, const int32_t* ue, int32_t* mt,
-                                 int32_t* tstart, int32_t* total, int tile_rows, Keep keep) {
+                                 int32_t* tstart, int32_t* total, int tile_rows, Keep keep,
+                                 int32_t* ord = nullptr, int32_t* total_a = nullptr) {
   const int lane = threadIdx.x & 31;
   for (int u = threadIdx.x; u < U; u += NT) {
     const int rows = us[u + 1] - us[u];
@@ -288,18 +298,28 @@ __device__ void unit_tile_prefix(const Params& p, int U, const int32_t* us, cons
   }
   __syncthreads();
   if (threadIdx.x < 32) {
-    int carry = 0;
-    for (int c0 = 0; c0 < U; c0 += 32) {
-      const int u = c0 + lane;
-      const int v = u < U ? mt[u] * p.n_tiles : 0;
-      int incl = v;
+    int carry = 0, pos = 0;
+    for (int cls = 0; cls < (ord ? 2 : 1); ++cls) {
+      for (int c0 = 0; c0 < U; c0 += 32) {
+        const int u = c0 + lane;
+        const bool in = u < U && (!ord || ((mt[u] == 1) == (cls == 0)));
+        const unsigned m = __ballot_sync(0xffffffffu, in);
+        const int v = in ? mt[u] * p.n_tiles : 0;
+        int incl = v;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int w = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += w;
+        for (int off = 1; off < 32; off <<= 1) {
+          const int w = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += w;
+        }
+        const int i = pos + __popc(m & ((1u << lane) - 1u));
+        if (in) {
+          tstart[i] = carry + incl - v;
+          if (ord) ord[i] = u;
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+        pos += __popc(m);
       }
-      if (u < U) tstart[u] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+      if (cls == 0 && total_a && lane == 0) *total_a = carry;
     }
     if (lane == 0) {
       tstart[U] = carry;
@@ -308,24 +328,40 @@ __device__ void unit_tile_prefix(const Params& p, int U, const int32_t* us, cons
   }
 }
 
+// Schedule position -> tile index in class order: the first-class tiles
+// [0, ta) are spread evenly over the positions (position q is one of them iff
+// floor((q + 1) ta / total) > floor(q ta / total)), the rest keep their order,
+// so every round of the persistent grid mixes weight-streaming tiles with
+// tensor-bound ones in the proportion of their totals.  A bijection on
+// [0, total); the identity when ta is 0 or total.
+__device__ __forceinline__ int interleave(int q, int ta, int total) {
+  if (ta <= 0 || ta >= total) return q;
+  const int a0 = (int)((long long)q * ta / total);
+  const int a1 = (int)((long long)(q + 1) * ta / total);
+  return a1 > a0 ? a0 : ta + (q - a0);
+}
+
 struct Tile {
   int g, nt, rows;
   long long row0;
 };
 
-__device__ __forceinline__ Tile decode(const Smem& s, int U, int tile) {
+// Schedule position -> tile (units in class order, see unit_tile_prefix).
+__device__ __forceinline__ Tile decode(const Smem& s, int U, int pos) {
+  const int tile = interleave(pos, s.total_a, s.total_tiles);
   int lo = 0, hi = U;  // tstart[lo] <= tile < tstart[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (s.tstart[mid] <= tile) lo = mid; else hi = mid;
   }
+  const int u = s.ord[lo];
   Tile t;
-  t.g = lo;  // unit
+  t.g = u;  // unit
   const int local = tile - s.tstart[lo];
-  const int m = s.mt[lo];
+  const int m = s.mt[u];
   t.nt = local / m;
-  t.row0 = (long long)s.us[lo] + (long long)(local % m) * BM;
-  const long long left = (long long)s.us[lo + 1] - t.row0;
+  t.row0 = (long long)s.us[u] + (long long)(local % m) * BM;
+  const long long left = (long long)s.us[u + 1] - t.row0;
   t.rows = left < BM ? (int)left : BM;
   return t;
 }
@@ -583,7 +619,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   // below the small-batch threshold are left to the small-batch kernel
   const int U = build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
   unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.mt, s.tstart, &s.total_tiles, BM,
-                            [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; });
+                            [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; },
+                            s.ord, &s.total_a);
   __syncthreads();
   if (s.total_tiles == 0) return;  // no tiles: exit before any barrier or TMEM set-up
   if (threadIdx.x == 0) {

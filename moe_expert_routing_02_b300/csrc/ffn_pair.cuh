@@ -68,12 +68,14 @@ struct Smem {
   uint32_t tmem_base;
   uint32_t abort_flag;
   int32_t total_tiles;
+  int32_t total_a;           // tiles of the weight-streaming class (ffn::unit_tile_prefix)
   int32_t u_count;
   int32_t goff[MAX_G + 1];   // staged group offsets
   int32_t us[MAX_G + 1];     // unit first rows (ffn::build_units)
-  int32_t tstart[MAX_G + 1];
+  int32_t tstart[MAX_G + 1]; // first tile of the i-th unit in class order
   int32_t mt[MAX_G];
   int32_t ex[MAX_G];         // unit experts
+  int32_t ord[MAX_G];        // units in class order
   alignas(128) uint8_t stg[EPI_WARPS][1024];  // per-warp output staging (store_rows32; 16-byte accesses)
 };
 
@@ -108,18 +110,22 @@ struct Tile {
   long long row0;  // first row of the pair tile
 };
 
-__device__ __forceinline__ Tile decode(const Smem& s, int U, int tile) {
+// Schedule position -> pair tile (units in class order, ffn::unit_tile_prefix;
+// positions spread over the classes by ffn::interleave).
+__device__ __forceinline__ Tile decode(const Smem& s, int U, int pos) {
+  const int tile = ffn::interleave(pos, s.total_a, s.total_tiles);
   int lo = 0, hi = U;  // tstart[lo] <= tile < tstart[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (s.tstart[mid] <= tile) lo = mid; else hi = mid;
   }
+  const int u = s.ord[lo];
   Tile t;
-  t.g = lo;
+  t.g = u;
   const int local = tile - s.tstart[lo];
-  const int m = s.mt[lo];
+  const int m = s.mt[u];
   t.nt = local / m;
-  t.row0 = (long long)s.us[lo] + (long long)(local % m) * BMP;
+  t.row0 = (long long)s.us[u] + (long long)(local % m) * BMP;
   return t;
 }
 
@@ -142,7 +148,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // below the small-batch threshold are left to the small-batch kernel
   const int U = ffn::build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
   ffn::unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.mt, s.tstart, &s.total_tiles, BMP,
-                                 [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; });
+                                 [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; },
+                                 s.ord, &s.total_a);
   __syncthreads();
   if (s.total_tiles == 0) return;  // no tiles: exit before any barrier or TMEM set-up
   if (threadIdx.x == 0) {
