@@ -86,6 +86,9 @@ def parse_args(argv=None):
     ap.add_argument("--wgrad-bf16", action="store_true", help="--backward: weight gradients written in bf16")
     ap.add_argument("--backward", action="store_true",
                     help="time the layer's backward (moe_ffn_backward + moe_route_backward) instead; one JSON line")
+    ap.add_argument("--crossover", action="store_true",
+                    help="time the EPS-MoE GEMM crossover shapes on the grouped and small-batch FFN kernels "
+                         "(one JSON line per shape; not the bench line)")
     ap.add_argument("--sweep-min-log2", type=int, default=14)
     ap.add_argument("--sweep-max-log2", type=int, default=20)
     return ap.parse_args(argv)
@@ -648,12 +651,30 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+class L2Flush:
+    """Empties L2 between timed calls: writes a buffer of twice the L2 size
+    (evicting everything the previous call left, including its dirty lines),
+    then reads a second one of the same size, so that the flush's own dirty
+    lines are written back here and not during the next timed call (which
+    would otherwise pay up to an L2's worth of write-backs it did not cause)."""
+
+    def __init__(self, dev, l2_bytes=126 * 2 ** 20):
+        import torch
+        self.w = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(2 * l2_bytes // 8, dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.max()
+
+
 def run_sweep(args):
     """Every stage of the path timed alone over T = 2^14 .. 2^20 tokens with the
     moe_gpt_stream workload's distributions (E=16, top-2, H=1024, Zipf bias,
     correlated second layer).  Each stage: 5 warm-up calls, then 20 calls,
-    each preceded by a write of 2x the L2 size (L2 flushed) and timed alone with
-    CUDA events; median, p10 and p90.  Fraction of HBM = algorithmic bytes /
+    each preceded by an L2 flush (L2Flush: a write, then a read, of 2x the L2
+    size, so the timed call pays no write-back of the flush's dirty lines) and
+    timed alone with CUDA events; median, p10 and p90.  Fraction of HBM = algorithmic bytes /
     median time / the measured copy bandwidth."""
     import dataclasses
     import torch
@@ -663,7 +684,7 @@ def run_sweep(args):
     base = W.config_by_name(args.config)
     peaks = load_peaks()
     dev = torch.device("cuda", 0)
-    flush = torch.empty(2 * 126 * 2 ** 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     for lg2 in range(args.sweep_min_log2, args.sweep_max_log2 + 1):
         T = 2 ** lg2
         c = dataclasses.replace(base, T=T, L=2)
@@ -711,7 +732,7 @@ def run_sweep(args):
             torch.cuda.synchronize()
             ts = []
             for _ in range(20):
-                flush.zero_()
+                flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 fn()
@@ -724,7 +745,7 @@ def run_sweep(args):
             gbs = nbytes / (med * 1e-6) / 1e9
             res[name] = {"us_median": round(med, 2), "us_p10": round(ts[2], 2), "us_p90": round(ts[17], 2),
                          "bytes": int(nbytes), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)}
-        print(json.dumps({"sweep": f"{c.name} distributions, each stage alone, L2 flushed before every call",
+        print(json.dumps({"sweep": f"{c.name} distributions, each stage alone, L2 flushed (written, then read clean) before every call",
                           "T": T, "E": E, "k": k, "H": H, "hbm_peak_gbs": peaks["hbm_gbs"],
                           "peak_source": peaks["source"], "stages": res}), flush=True)
         del lgs, x, st, idx0, w0, idx1, w1, disp, ws, y, out, front_out, stages
@@ -841,6 +862,88 @@ def run_backward(args):
     return res
 
 
+CROSSOVER_SHAPES = [(5120, 1536), (5120, 14336)]   # (H, F): GEMM2 is M x H x F
+
+
+def run_crossover(args):
+    """GroupGemm vs DenseGemm crossover (EPS-MoE review, analysis of the two
+    GEMM forms over the shapes 512x5120x1536, 2048x5120x1536 and
+    512x5120x14336, M x N x K): SwiGLU experts with H = 5120 and F = 1536 or
+    14336 -- an expert's down projection is exactly the M x 5120 x F GEMM of
+    those shapes -- each with M rows, through moe_expert_ffn on the grouped
+    tcgen05 kernels (small_group_threshold 0) and on the small-batch
+    weight-streaming kernel (threshold above M; rows beyond 64 are taken in
+    64-row chunks, each streaming the weights again).  Two layer forms: one
+    expert alone (the pages' single GEMMs; few tiles, so neither kernel fills
+    the GPU at small M) and 32 experts of M rows each (a fine-grained layer's
+    many small groups, the case the threshold decides).  Each timing: 3
+    warm-up calls, then 20 calls, each after an L2 flush (weights and rows
+    start in HBM), CUDA events around the call alone; median.  One JSON line
+    per (H, F, experts) with the times per M and the faster path."""
+    import torch
+    import moe_expert_routing_02_b300 as M
+    M.lib()
+    peaks = load_peaks()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = L2Flush(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    forms = [(1, [16, 32, 48, 64, 96, 128, 192, 256, 512, 1024, 2048]), (32, [16, 32, 48, 64, 96, 128, 256, 512])]
+    for H, F in CROSSOVER_SHAPES:
+        for ne, rows in forms:
+            w1 = (torch.randn((ne, H, F), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            w3 = (torch.randn((ne, H, F), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            w2 = (torch.randn((ne, F, H), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            wbytes = 3 * H * F * 2 * ne
+            res = []
+            for m in rows:
+                A = m * ne
+                xp = torch.randn((A, H), generator=g, device=dev).to(torch.bfloat16)
+                go = torch.arange(0, A + 1, m, dtype=torch.int32, device=dev)
+                y = torch.empty((A, H), dtype=torch.bfloat16, device=dev)
+                ws = torch.empty(max(M.workspace_bytes(M.MOE_OP_EXPERT_FFN, A, 1, ne, H, F), 1024),
+                                 dtype=torch.uint8, device=dev)
+                row = {"M": m}
+                for name, thr in (("grouped", 0), ("small_batch", 1 << 30)):
+                    fn = lambda: M.moe_expert_ffn(xp, go, None, None, w1, w3, w2, "swiglu", thr, y=y, workspace=ws)
+                    for _ in range(3):
+                        fn()
+                    torch.cuda.synchronize()
+                    ts = []
+                    for _ in range(20):
+                        flush()
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record()
+                        fn()
+                        e1.record()
+                        e1.synchronize()
+                        ts.append(e0.elapsed_time(e1) * 1e3)
+                    M.moe_check()
+                    ts.sort()
+                    row[name + "_us"] = round(ts[len(ts) // 2], 1)
+                flops = 6 * A * H * F
+                row["faster"] = "small_batch" if row["small_batch_us"] < row["grouped_us"] else "grouped"
+                row["grouped_tflops"] = round(flops / row["grouped_us"] / 1e6, 1)
+                row["small_batch_weights_gbs"] = round(wbytes / row["small_batch_us"] / 1e3, 1)
+                # lower bound of the call: weights once from HBM, or the flops at the burst bf16 rate
+                row["bound_us"] = round(max(wbytes / (peaks["hbm_gbs"] * 1e3), flops / (peaks["bf16_tflops"] * 1e6)),
+                                       1)
+                res.append(row)
+                del xp, y, ws
+            cross = [r["M"] for r in res if r["faster"] == "grouped"]
+            print(json.dumps({"crossover": f"{ne} expert(s) of M rows each, SwiGLU, H={H}, F={F} "
+                                           f"(down projection M x {H} x {F})",
+                              "experts": ne, "weights_bytes": wbytes, "rows": res,
+                              "smallest_M_where_grouped_is_faster": min(cross) if cross else None,
+                              "library_threshold": 64, "peaks": peaks["source"],
+                              "timing": "median of 20 calls, L2 flushed (written, then read clean) before each, "
+                                        "CUDA events"}), flush=True)
+            del w1, w3, w2
+            torch.cuda.empty_cache()
+    return 0
+
+
 def _top_overlap(p_pred, load, m=5):
     """Share of the m most loaded experts that are among the m most popular
     predicted ones (ties: lower expert first on both sides)."""
@@ -940,6 +1043,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.sweep:
         return run_sweep(args)
+    if args.crossover:
+        return run_crossover(args)
     if args.quality:
         print(json.dumps(run_quality(args)), flush=True)
         return 0
