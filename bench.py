@@ -69,6 +69,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-pdl", action="store_true", help="ordinary launches instead of programmatic dependent launch")
     ap.add_argument("--fuse-combine", action="store_true",
                     help="the combine in the FFN's second GEMM epilogue (moe_expert_ffn_combine)")
+    ap.add_argument("--small-sms", type=int, default=-1,
+                    help="SMs of the FFN's small-batch kernels (MOE_OPT_FFN_SMALL_SMS; -1: the library's split model, "
+                         "0: no small-batch path)")
     ap.add_argument("--small-threshold", type=int, default=64,
                     help="experts with fewer rows take the small-batch FFN kernel (0: none, no side-stream launches)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -317,6 +320,7 @@ def run_ours(args, rank, world, local):
                                             "pair": M.MOE_FFN_KERNEL_PAIR,
                                             "fused": M.MOE_FFN_KERNEL_FUSED}[args.ffn_kernel])
     M.moe_set_option(M.MOE_OPT_PDL, 0 if args.no_pdl else 1)
+    M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, args.small_sms)
 
     def run_step(it, ev=None):
         for j in range(c.L):
@@ -445,7 +449,7 @@ def run_ours(args, rank, world, local):
                     "frac": round(achieved / peaks["hbm_gbs"], 4),
                     "peak_source": f"hbm_gbs of {peaks['source']} peaks",
                     "tflops": round(fl / ffn_t / 1e12, 1)}
-    n_ffn = M.moe_ffn_launches(c.A, c.E, c.H, c.F, c.act, 64, step.gather)
+    n_ffn = M.moe_ffn_launches(c.A, c.E, c.H, c.F, c.act, args.small_threshold, step.gather)
     ffn_desc = ("moe_expert_ffn: fused GEMM1+GEMM2 launch" if n_ffn in (1, 3) else
                 "moe_expert_ffn: GEMM1 and GEMM2 launches") + (" (+2 small-batch launches on the side stream)"
                                                                if n_ffn >= 3 else "")
@@ -471,6 +475,7 @@ def run_ours(args, rank, world, local):
                    "ffn_kernel": args.ffn_kernel,
                    "pdl": not args.no_pdl,
                    "small_group_threshold": args.small_threshold,
+                   "small_path_sms": "split model" if args.small_sms < 0 else args.small_sms,
                    "combine": "in the FFN's second GEMM epilogue" if args.fuse_combine else "separate kernel",
                    "chunks": args.chunks,
                    "replicas": ("physical copies (moe_replicate_weights)" if args.physical_replicas

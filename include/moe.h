@@ -567,12 +567,35 @@ moe_status moe_dispatch_noalloc(const uint16_t* x, const int32_t* idx, int T, in
  *     has exited, and each waits for that kernel's completion (griddepcontrol
  *     .wait) before touching memory; no kernel releases its dependents early.
  *     0: ordinary launches.  Results are identical either way.
+ *   MOE_OPT_FFN_SMALL_SMS  how the SMs are shared between the small-batch
+ *     kernels and the grouped kernels of an expert-FFN call whose
+ *     small_group_threshold is > 0 (EPS-MoE review, "GroupGemm vs
+ *     DenseGemm": experts with few tokens on a separate path):
+ *       -1 (default)  each call's kernels choose from the group table, all
+ *                     the same way: the small-batch kernels (a weight
+ *                     stream, bound by HBM) get the SMs that balance their
+ *                     time against the grouped kernels' (bound by the
+ *                     tensor pipe) on the rest, and both run at once; when
+ *                     running the small experts as padded grouped tiles on
+ *                     every SM is expected to be faster, they do that
+ *                     instead and the small-batch kernels do nothing;
+ *       0             no small-batch path: the grouped kernels take every
+ *                     expert;
+ *       n > 0         the small-batch kernels use n SMs (even n with the
+ *                     CTA-pair kernels), the grouped kernels the rest.
+ *     The outputs are the same within the FFN tolerance whichever path an
+ *     expert takes (bit-identical for the experts on the grouped kernels).
  * Unknown options or values return MOE_ERR_INVALID.  Options are process-wide
  * and stored atomically; a call reads each one once when it is made, so a
  * set from another thread applies to the calls that start after it returns
  * (a call made at the same time sees the old or the new value).
  * ------------------------------------------------------------------------- */
-typedef enum { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_FFN_TIMEOUT_SELFTEST = 2, MOE_OPT_PDL = 3 } moe_option;
+typedef enum {
+    MOE_OPT_FFN_KERNEL = 1,
+    MOE_OPT_FFN_TIMEOUT_SELFTEST = 2,
+    MOE_OPT_PDL = 3,
+    MOE_OPT_FFN_SMALL_SMS = 4
+} moe_option;
 typedef enum {
     MOE_FFN_KERNEL_AUTO = 0,
     MOE_FFN_KERNEL_SINGLE = 1,

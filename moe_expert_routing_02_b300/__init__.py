@@ -34,6 +34,7 @@ __all__ = [
     "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_OP_LAYER_FRONT", "MOE_OP_EXPERT_FFN_COMBINE",
     "MOE_ACT_GELU", "MOE_ACT_SWIGLU", "MOE_OPT_FFN_KERNEL", "MOE_FFN_KERNEL_AUTO", "MOE_FFN_KERNEL_SINGLE",
     "MOE_FFN_KERNEL_PAIR", "MOE_FFN_KERNEL_FUSED", "MOE_OPT_FFN_TIMEOUT_SELFTEST", "MOE_OPT_PDL",
+    "MOE_OPT_FFN_SMALL_SMS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +43,7 @@ library_path = os.path.join(_HERE, "libmoe.so")
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_WORKSPACE, MOE_ERR_DEVICE = range(7)
 MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
 MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT, MOE_OP_EXPERT_FFN_COMBINE = 1, 2, 3, 4
-MOE_OPT_FFN_KERNEL, MOE_OPT_FFN_TIMEOUT_SELFTEST, MOE_OPT_PDL = 1, 2, 3
+MOE_OPT_FFN_KERNEL, MOE_OPT_FFN_TIMEOUT_SELFTEST, MOE_OPT_PDL, MOE_OPT_FFN_SMALL_SMS = 1, 2, 3, 4
 MOE_FFN_KERNEL_AUTO, MOE_FFN_KERNEL_SINGLE, MOE_FFN_KERNEL_PAIR, MOE_FFN_KERNEL_FUSED = 0, 1, 2, 3
 
 _P = ctypes.c_void_p

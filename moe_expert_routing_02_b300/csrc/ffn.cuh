@@ -140,7 +140,154 @@ struct Params {
   const float* comb_w;
   int comb_k;
   float* comb_acc;
+  // SM split between the small-batch kernels and the grouped kernels of one
+  // forward FFN call (small_sms below).  split_ctas = 0: no split -- the
+  // grouped kernels skip the experts below small_threshold and the
+  // small-batch kernels take them with their whole grid.  Otherwise every
+  // kernel of the call gets the same values: split_ctas = the SMs they share,
+  // split_force = -1 (the model decides) or the small-batch kernels' SMs
+  // (0 = no small-batch path), split_pair = the grouped kernel runs CTA
+  // pairs, split_rows = rows per grouped tile, ffn_H / ffn_F / ffn_mats = the
+  // whole FFN's shape and weight matrices per expert (2 GeLU, 3 SwiGLU).
+  int split_ctas;
+  int split_force;
+  int split_pair;
+  int split_rows;
+  int ffn_H, ffn_F, ffn_mats;
 };
+
+// Rates of the split model (per SM unless stated): the small-batch kernel
+// streams about kSplitSmallBytesPerNs bytes of weights per ns on one SM
+// (measured on B300: 59-63 GB/s per SM with 8 to 48 SMs given to it on the
+// DeepSeekV2-shaped layer; about 200 KB of stages in flight against the HBM
+// latency under load); the grouped kernel executes about kSplitGroupFlopPerNs
+// padded-tile flops per ns on one SM; HBM moves about kSplitHbmBytesPerNs
+// bytes per ns in all.
+#ifndef MOE_SPLIT_SMALL_BPNS
+#define MOE_SPLIT_SMALL_BPNS 60
+#endif
+#ifndef MOE_SPLIT_GROUP_FPNS
+#define MOE_SPLIT_GROUP_FPNS 8000
+#endif
+constexpr long long kSplitSmallBytesPerNs = MOE_SPLIT_SMALL_BPNS;
+constexpr long long kSplitGroupFlopPerNs = MOE_SPLIT_GROUP_FPNS;
+constexpr long long kSplitHbmBytesPerNs = 6000;
+
+// The SMs that the small-batch kernels of this FFN call take (0: no
+// small-batch path this call; the grouped kernels then take every expert).
+// A two-resource model (the small-batch kernel is a weight stream, bound by
+// HBM; the grouped kernel's large experts are bound by the tensor pipe):
+// with S SMs for the small-batch experts and the rest for the grouped ones,
+//   t(S) = max(small weights / min(S rate, HBM), grouped flops / ((N-S) rate),
+//              all weights / HBM),
+// against t(0) = the grouped kernels alone on every SM, the small experts as
+// padded tiles, which a split must beat by 1/8.  The first term falls and the
+// second rises with S, so the
+// best S sits where they cross, S* = N Ws Rt / (Ws Rt + Fg Rs), capped where
+// the small-batch kernel alone would saturate HBM; the lanes of warp 0 score
+// the split sizes next to it and t(0), and the smallest t wins (the smaller
+// S on ties).  Only from the unit table and the call's parameters, with
+// integer sums and explicitly rounded fp32 operations, so every kernel of the
+// call computes the same S.  Call from all NT threads
+// after build_units; `red` is shared scratch of 8 long longs.
+template <int NT>
+__device__ int small_sms(const Params& p, int U, const int32_t* us, const int32_t* ue, long long* red) {
+  if (p.split_ctas <= 0 || p.small_threshold <= 0) {
+    __syncthreads();
+    return -1;  // no split: legacy behaviour
+  }
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    long long small_chunks = 0, small_units = 0, small_pad = 0, grp_pad = 0, grp_units = 0;
+    const long long gr = p.split_rows;
+    for (int c0 = 0; c0 < U; c0 += 32) {
+      const int u = c0 + lane;
+      long long sc = 0, su = 0, sp = 0, gp = 0, gu = 0;
+      if (u < U) {
+        const long long rows = us[u + 1] - us[u];
+        if (rows > 0 && ue[u] >= 0) {
+          if (rows < p.small_threshold) {
+            sc = (rows + 63) / 64;
+            su = 1;
+            sp = (rows + gr - 1) / gr * gr;
+          } else {
+            gp = (rows + gr - 1) / gr * gr;
+            gu = 1;
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        sc += __shfl_xor_sync(0xffffffffu, sc, off);
+        su += __shfl_xor_sync(0xffffffffu, su, off);
+        sp += __shfl_xor_sync(0xffffffffu, sp, off);
+        gp += __shfl_xor_sync(0xffffffffu, gp, off);
+        gu += __shfl_xor_sync(0xffffffffu, gu, off);
+      }
+      small_chunks += sc;
+      small_units += su;
+      small_pad += sp;
+      grp_pad += gp;
+      grp_units += gu;
+    }
+    const long long N = p.split_ctas, step = p.split_pair ? 2 : 1;
+    long long S = 0;
+    if (small_units > 0 && p.split_force > 0) {
+      S = p.split_force;
+    } else if (small_units > 0 && p.split_force < 0) {
+      // times in ns as fp32 with explicitly rounded operations (never
+      // contracted), so every kernel reaches the same S; a wrong S only costs
+      // time, never a result
+      const float wb = __fmul_rn(__fmul_rn((float)p.ffn_mats, (float)p.ffn_H), __fmul_rn((float)p.ffn_F, 2.f));
+      const float fl = wb;  // flops per row = 2 * mats * H * F = the weight bytes of an expert
+      const float Ws = __fmul_rn((float)small_chunks, wb), Bs = __fmul_rn((float)small_units, wb);
+      const float Bg = __fmul_rn((float)grp_units, wb);
+      const float Fg = __fmul_rn((float)grp_pad, fl), F0 = __fmul_rn((float)(grp_pad + small_pad), fl);
+      const float rs1 = (float)kSplitSmallBytesPerNs, rt1 = (float)kSplitGroupFlopPerNs;
+      const float bw = (float)kSplitHbmBytesPerNs, Nf = (float)N;
+      const long long hi = N - step;
+      long long cap = kSplitHbmBytesPerNs / kSplitSmallBytesPerNs;
+      if (cap > hi) cap = hi;
+      // crossing of the small-batch and grouped times: S* = N Ws Rt / (Ws Rt + Fg Rs)
+      const float a = __fmul_rn(Ws, rt1);
+      const float xf = __fdiv_rn(__fmul_rn(Nf, a), __fadd_rn(a, __fmul_rn(Fg, rs1)));
+      long long xs = (long long)xf;  // truncation toward zero of a non-negative value
+      if (xs > cap) xs = cap;
+      long long cand = (xs / step + (lane - 4)) * step;  // lanes 1..8: -3 .. +4 steps around it
+      float t = __int_as_float(0x7f800000);            // +inf
+      if (lane == 0) {
+        // a split must beat the grouped-only time by 1/8: giving SMs away
+        // also costs what the model leaves out (measured: 2 SMs taken from
+        // the fused CTA-pair kernel on the moe_gpt_stream layer cost 8%, as the
+        // small-batch CTAs break up SM pairs the clusters need)
+        cand = 0;
+        t = __fmul_rn(fmaxf(__fdiv_rn(F0, __fmul_rn(Nf, rt1)), __fdiv_rn(__fadd_rn(Bs, Bg), bw)), 0.875f);
+      } else if (lane <= 8 && cand >= step && cand <= hi) {
+        const float rs = fminf(__fmul_rn((float)cand, rs1), bw);
+        t = __fdiv_rn(Ws, rs);
+        if (grp_units) t = fmaxf(t, __fdiv_rn(Fg, __fmul_rn((float)(N - cand), rt1)));
+        t = fmaxf(t, __fdiv_rn(__fadd_rn(Ws, Bg), bw));
+      }
+      // the smallest (t, S) over the warp
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const float ot = __shfl_xor_sync(0xffffffffu, t, off);
+        const long long oc = __shfl_xor_sync(0xffffffffu, cand, off);
+        if (ot < t || (ot == t && oc < cand)) {
+          t = ot;
+          cand = oc;
+        }
+      }
+      S = cand;
+    }
+    if (S > N - step) S = N - step;
+    if (S < 0) S = 0;
+    if (step == 2) S &= ~1LL;
+    if (lane == 0) red[0] = S;
+  }
+  __syncthreads();
+  return (int)red[0];
+}
 
 // acc[t, c .. c+31] += wt * v[0 .. 31] with vector fp32 reductions (8 per
 // row segment).  For k = 2 every accumulator element receives exactly two
@@ -189,6 +336,7 @@ struct Smem {
   int32_t mt[MAX_G];
   int32_t ex[MAX_G];         // unit experts
   int32_t ord[MAX_G];        // units in class order
+  long long red[8];          // small_sms scratch
   alignas(128) uint8_t stg[EPI_WARPS][1024];  // per-warp output staging (store_rows32; 16-byte accesses)
 };
 
@@ -618,11 +766,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- units (an expert's adjacent groups), their tiles and prefix; experts
   // below the small-batch threshold are left to the small-batch kernel
   const int U = build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
+  // with an SM split (small_sms) the small-batch experts are left to the
+  // small-batch kernels only when they get SMs (S > 0), and this kernel runs
+  // on the other split_ctas - S SMs
+  const int S = small_sms<THREADS>(p, U, s.us, s.ex, s.red);
+  const bool skip_small = p.small_threshold > 0 && S != 0;
   unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.mt, s.tstart, &s.total_tiles, BM,
-                            [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; },
+                            [&](int rows) { return !skip_small || rows >= p.small_threshold; },
                             s.ord, &s.total_a);
   __syncthreads();
-  if (s.total_tiles == 0) return;  // no tiles: exit before any barrier or TMEM set-up
+  const int nctas = (S > 0 && p.split_ctas - S < (int)gridDim.x) ? p.split_ctas - S : (int)gridDim.x;
+  // no tiles, or a CTA beyond this kernel's share: exit before any barrier or TMEM set-up
+  if (s.total_tiles == 0 || (int)blockIdx.x >= nctas) return;
+  s.red[1] = nctas;  // read back per tile: the loops below keep no register for it
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&s.full[i], 1);
@@ -667,7 +823,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool gather = p.a_src != nullptr;
     uint32_t stage = 0, phase = 0, issued = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < total && ok; tile += (int)*(volatile long long*)&s.red[1]) {
       const Tile t = decode(s, U, tile);
       const int brow = epi_kmajor_b(EPI) ? s.ex[t.g] * p.N_out + t.nt * BN : s.ex[t.g] * p.K;
       const int arow = (int)t.row0;
@@ -736,7 +892,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t bdesc0 = smem_desc_sw128(smem_u32(s.b[0]), kmb ? 16u : (uint32_t)B_BOX_BYTES, 1024);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true, withheld = false, any_mma = false;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = blockIdx.x; tile < total && ok; tile += (int)*(volatile long long*)&s.red[1]) {
         if (!wait_phase(&s.tempty[acc], acc_phase ^ 1, &s.abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
@@ -788,7 +944,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                        s.a[STAGES - 1] + (warp - 2) * 1024};
     uint32_t fph[3] = {0u, 0u, 0u};
     bool fpend[3] = {false, false, false};
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < total; tile += (int)*(volatile long long*)&s.red[1]) {
       const Tile t = decode(s, U, tile);
       // Multiply epilogues: the factor rows of the warp's 64 columns are
       // requested before the accumulator wait.  kStoreKMMul: two 32x16 TMA

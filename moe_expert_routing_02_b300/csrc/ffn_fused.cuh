@@ -159,7 +159,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1;
-  const int npairs = gridDim.x >> 1;
   const Params& p1 = fp.p1;
   const Params& p2 = fp.p2;
 
@@ -167,11 +166,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   Params pb = p1;
   pb.n_tiles = 1;
   const int U = ffn::build_units<THREADS>(pb, s.goff, s.us, s.ex, &s.u_count);
+  // with an SM split (ffn::small_sms) the small-batch experts are left to the
+  // small-batch kernels only when they get SMs (S > 0), and the pairs beyond
+  // this kernel's (split_ctas - S) / 2 exit.  The pairs that stay are
+  // co-resident once the exiting CTAs and the small-batch kernels' CTAs
+  // beyond their own share have left, which they do without waiting on
+  // anything, so the dependency waits below still always progress.
+  const int S = ffn::small_sms<THREADS>(pb, U, s.us, s.ex, s.red);
+  const bool skip_small = pb.small_threshold > 0 && S != 0;
   ffn::unit_tile_prefix<THREADS>(pb, U, s.us, s.ex, s.mt, s.tstart, &s.total_tiles, BMP,
-                                 [&](int rows) { return pb.small_threshold <= 0 || rows >= pb.small_threshold; });
+                                 [&](int rows) { return !skip_small || rows >= pb.small_threshold; });
   __syncthreads();
   const int B = s.total_tiles;
-  if (B == 0) return;  // no tiles: exit before any barrier or TMEM set-up
+  const int npairs = (S > 0 && (pb.split_ctas - S) / 2 < (int)(gridDim.x >> 1)) ? (pb.split_ctas - S) / 2
+                                                                                   : (int)(gridDim.x >> 1);
+  // no tiles, or a pair beyond this kernel's share: exit before any barrier or TMEM set-up
+  if (B == 0 || pair >= npairs) return;
+  s.red[1] = npairs;  // read back per tile: the loops below keep no register for it
   const int N1 = p1.n_tiles, N2 = p2.n_tiles;
   const int D = fp.lag < B ? fp.lag : B;
   const int total = B * (N1 + N2);
@@ -212,7 +223,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
       const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);  // leader's barriers
-      for (int pos = pair; pos < total && ok; pos += npairs) {
+      for (int pos = pair; pos < total && ok; pos += (int)*(volatile long long*)&s.red[1]) {
         const FTile t = decode(s, U, B, N1, N2, D, pos);
         const bool g1 = t.phase == 1;
         const Params& p = g1 ? p1 : p2;
@@ -263,7 +274,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint64_t bdesc0 = smem_desc_sw128(smem_u32(s.b[0]), B_BOX_BYTES, 1024);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true, withheld = false, any_mma = false;
-      for (int pos = pair; pos < total && ok; pos += npairs) {
+      for (int pos = pair; pos < total && ok; pos += (int)*(volatile long long*)&s.red[1]) {
         const FTile t = decode(s, U, B, N1, N2, D, pos);
         const int kblocks = (t.phase == 1 ? p1.K : p2.K) / BK;
         if (!wait_phase<true>(&s.tempty[acc], acc_phase ^ 1, &s.abort_flag)) break;
@@ -308,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int slice = (warp - 2) >> 2;
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&s.tempty[0]), 0);
     uint32_t acc = 0, acc_phase = 0;
-    for (int pos = pair; pos < total; pos += npairs) {
+    for (int pos = pair; pos < total; pos += (int)*(volatile long long*)&s.red[1]) {
       const FTile t = decode(s, U, B, N1, N2, D, pos);
       if (!__all_sync(0xffffffffu, wait_phase<true>(&s.tfull[acc], acc_phase, &s.abort_flag))) break;
       tc_fence_after();

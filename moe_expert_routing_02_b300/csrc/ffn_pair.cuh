@@ -76,6 +76,7 @@ struct Smem {
   int32_t mt[MAX_G];
   int32_t ex[MAX_G];         // unit experts
   int32_t ord[MAX_G];        // units in class order
+  long long red[8];          // ffn::small_sms scratch
   alignas(128) uint8_t stg[EPI_WARPS][1024];  // per-warp output staging (store_rows32; 16-byte accesses)
 };
 
@@ -142,16 +143,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const int pair = blockIdx.x >> 1;
-  const int npairs = gridDim.x >> 1;
 
   // ---- units and their tiles (identical in both CTAs of the pair); experts
   // below the small-batch threshold are left to the small-batch kernel
   const int U = ffn::build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
+  // with an SM split (ffn::small_sms) the small-batch experts are left to the
+  // small-batch kernels only when they get SMs (S > 0), and the pairs beyond
+  // this kernel's (split_ctas - S) / 2 exit
+  const int S = ffn::small_sms<THREADS>(p, U, s.us, s.ex, s.red);
+  const bool skip_small = p.small_threshold > 0 && S != 0;
   ffn::unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.mt, s.tstart, &s.total_tiles, BMP,
-                                 [&](int rows) { return p.small_threshold <= 0 || rows >= p.small_threshold; },
+                                 [&](int rows) { return !skip_small || rows >= p.small_threshold; },
                                  s.ord, &s.total_a);
   __syncthreads();
-  if (s.total_tiles == 0) return;  // no tiles: exit before any barrier or TMEM set-up
+  const int npairs = (S > 0 && (p.split_ctas - S) / 2 < (int)(gridDim.x >> 1)) ? (p.split_ctas - S) / 2
+                                                                                 : (int)(gridDim.x >> 1);
+  // no tiles, or a pair beyond this kernel's share (both CTAs of a pair agree):
+  // exit before any barrier or TMEM set-up
+  if (s.total_tiles == 0 || pair >= npairs) return;
+  s.red[1] = npairs;  // read back per tile: the loops below keep no register for it
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&s.full[i], 1);
@@ -191,7 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     bool ok = true;
     const CUtensorMap* mB = (EPI == kSwiglu && !leader) ? &tmB1 : &tmB0;
     const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);  // leader's barriers
-    for (int tile = pair; tile < total && ok; tile += npairs) {
+    for (int tile = pair; tile < total && ok; tile += (int)*(volatile long long*)&s.red[1]) {
       const Tile t = decode(s, U, tile);
       const int brow = s.ex[t.g] * p.K;
       const int arow = (int)(t.row0 + BM * rank);
@@ -240,7 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint64_t bdesc0 = smem_desc_sw128(smem_u32(s.b[0]), B_BOX_BYTES, 1024);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true, withheld = false, any_mma = false;
-      for (int tile = pair; tile < total && ok; tile += npairs) {
+      for (int tile = pair; tile < total && ok; tile += (int)*(volatile long long*)&s.red[1]) {
         if (!wait_phase<true>(&s.tempty[acc], acc_phase ^ 1, &s.abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
@@ -283,7 +293,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int slice = (warp - 2) >> 2;
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&s.tempty[0]), 0);
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = pair; tile < total; tile += npairs) {
+    for (int tile = pair; tile < total; tile += (int)*(volatile long long*)&s.red[1]) {
       const Tile t = decode(s, U, tile);
       if (!__all_sync(0xffffffffu, wait_phase<true>(&s.tfull[acc], acc_phase, &s.abort_flag))) break;
       tc_fence_after();

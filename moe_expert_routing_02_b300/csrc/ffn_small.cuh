@@ -70,6 +70,7 @@ struct Smem {
   int32_t tstart[MAX_G + 1];
   int32_t nchunk[MAX_G];     // 64-token chunks of each small unit (0 = not handled here)
   int32_t ex[MAX_G];         // unit experts
+  long long red[8];          // ffn::small_sms scratch
 };
 
 template <int EPI>
@@ -129,10 +130,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- units (an expert's adjacent groups) with fewer than small_threshold
   // rows, in 64-token chunks
   const int U = ffn::build_units<THREADS>(p, s.goff, s.us, s.ex, &s.u_count);
+  // with an SM split (ffn::small_sms) this kernel runs on S SMs, or not at
+  // all when S = 0 (the grouped kernels then take the small experts too)
+  const int S = ffn::small_sms<THREADS>(p, U, s.us, s.ex, s.red);
   ffn::unit_tile_prefix<THREADS>(p, U, s.us, s.ex, s.nchunk, s.tstart, &s.total_tiles, BT,
-                                 [&](int rows) { return rows < p.small_threshold; });
+                                 [&](int rows) { return S != 0 && rows < p.small_threshold; });
   __syncthreads();
-  if (s.total_tiles == 0) return;  // no tiles: exit before any barrier or TMEM set-up
+  const int nctas = (S > 0 && S < (int)gridDim.x) ? S : (int)gridDim.x;
+  // no tiles, or a CTA beyond this kernel's share: exit before any barrier or TMEM set-up
+  if (s.total_tiles == 0 || (int)blockIdx.x >= nctas) return;
+  s.red[1] = nctas;  // read back per tile: the loops below keep no register for it
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(&s.full[i], 1);
@@ -169,7 +176,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool gather = p.a_src != nullptr;
     uint32_t stage = 0, phase = 0, issued = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < total && ok; tile += (int)*(volatile long long*)&s.red[1]) {
       const Tile t = decode(s, U, tile);
       const int wrow = s.ex[t.g] * p.K;
       const int f0 = t.ft * BMF;
@@ -219,7 +226,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // (128-byte rows, 8-row groups 1024 B apart, K step of 16 = +2)
       const uint64_t wdesc0 = smem_desc_sw128(smem_u32(s.stage[0]), W_BOX_BYTES, 1024);
       const uint64_t xdesc0 = smem_desc_sw128(smem_u32(s.stage[0]) + C::NW * W_BYTES, 16, 1024);
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = blockIdx.x; tile < total && ok; tile += (int)*(volatile long long*)&s.red[1]) {
         const Tile t = decode(s, U, tile);
         const int npad = (t.rows + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(BMF, npad, true, false);
@@ -264,7 +271,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes (features) 32*quarter .. +31
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < total; tile += (int)*(volatile long long*)&s.red[1]) {
       const Tile t = decode(s, U, tile);
       if (!__all_sync(0xffffffffu, wait_phase(&s.tfull[acc], acc_phase, &s.abort_flag))) break;
       tc_fence_after();

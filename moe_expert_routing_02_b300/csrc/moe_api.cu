@@ -78,6 +78,7 @@ struct DeviceInfo {
 // Process-wide and atomic: a call reads each option once when it is made.
 std::atomic<int> g_opt_ffn_kernel{MOE_FFN_KERNEL_AUTO};
 std::atomic<int> g_opt_ffn_selftest{0};  // one-shot: next GEMM1 withholds an accumulator signal
+std::atomic<int> g_opt_ffn_small_sms{-1};  // SM split of the FFN's small-batch path (-1: model)
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 std::mutex g_side_mu;  // one fork/join sequence at a time per process
@@ -619,6 +620,17 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   p1.flags = g_opt_ffn_selftest.exchange(0) ? 1 : 0;
   p1.rep_base = rep_base;
   p1.small_threshold = small_group_threshold;
+  // SM split between the small-batch and the grouped kernels (every kernel
+  // of the call gets the same split fields, so they agree on it)
+  if (small_group_threshold > 0) {
+    p1.split_ctas = d->num_sms;
+    p1.split_force = g_opt_ffn_small_sms.load(std::memory_order_relaxed);
+    p1.split_pair = use_pair ? 1 : 0;
+    p1.split_rows = use_pair ? ffn2::BMP : ffn::BM;
+    p1.ffn_H = H;
+    p1.ffn_F = F;
+    p1.ffn_mats = act == MOE_ACT_SWIGLU ? 3 : 2;
+  }
   p1.a_src = a_src;
   p1.a_src_div = gather ? k : 1;
   p1.a_src_rows = gather ? T : 0;
@@ -963,6 +975,11 @@ moe_status moe_set_option(int option, int value) {
     g_opt_ffn_selftest.store(value);
     return MOE_OK;
   }
+  if (option == MOE_OPT_FFN_SMALL_SMS) {
+    if (value < -1 || value > 4096) return fail(MOE_ERR_INVALID, "moe_set_option: small-path SMs must be -1..4096");
+    g_opt_ffn_small_sms.store(value);
+    return MOE_OK;
+  }
   return fail(MOE_ERR_INVALID, "moe_set_option: unknown option %d", option);
 }
 
@@ -978,6 +995,10 @@ moe_status moe_get_option(int option, int* value) {
   }
   if (option == MOE_OPT_FFN_TIMEOUT_SELFTEST) {
     *value = g_opt_ffn_selftest.load();
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_FFN_SMALL_SMS) {
+    *value = g_opt_ffn_small_sms.load();
     return MOE_OK;
   }
   return fail(MOE_ERR_INVALID, "moe_get_option: unknown option %d", option);

@@ -139,6 +139,13 @@ def test_stats_and_replicate_reject_bad_arguments(L):
     assert L.moe_set_option(M.MOE_OPT_FFN_TIMEOUT_SELFTEST, 2) == inv
     v = ctypes.c_int(-1)
     assert L.moe_get_option(M.MOE_OPT_FFN_KERNEL, ctypes.byref(v)) == M.MOE_OK and v.value == 0
+    # the small-path SM split: -1 (model) by default, -1..4096 accepted
+    assert L.moe_get_option(M.MOE_OPT_FFN_SMALL_SMS, ctypes.byref(v)) == M.MOE_OK and v.value == -1
+    assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, -2) == inv
+    assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 5000) == inv
+    assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 24) == M.MOE_OK
+    assert L.moe_get_option(M.MOE_OPT_FFN_SMALL_SMS, ctypes.byref(v)) == M.MOE_OK and v.value == 24
+    assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, -1) == M.MOE_OK
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

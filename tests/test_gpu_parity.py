@@ -376,8 +376,14 @@ def test_ffn_small_batch_path_thresholds(thresh, act, ffn_kernel):
     x = W.make_x(c, 0, 0, device="cuda", T=idx.shape[0])
     w1, w3, w2 = _weights(c)
     go, perm, inv, xp = M.moe_dispatch(x, dev(idx), c.E)
-    y = M.moe_expert_ffn(xp, go, None, None, w1, w3, w2, act, small_group_threshold=thresh)
-    ok_check()
+    # give the small-batch kernel SMs of its own (the split model may
+    # otherwise leave such a small layer to the grouped kernel alone)
+    M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 8)
+    try:
+        y = M.moe_expert_ffn(xp, go, None, None, w1, w3, w2, act, small_group_threshold=thresh)
+        ok_check()
+    finally:
+        M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, -1)
     ref = O.expert_ffn(W.bf16_bits(xp), host(go)[:c.E + 1], None, W.bf16_bits(w1),
                        None if w3 is None else W.bf16_bits(w3), W.bf16_bits(w2), act)
     got = O.bf16_to_f64(W.bf16_bits(y))
