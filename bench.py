@@ -834,7 +834,9 @@ def run_backward(args):
     t_fwd = timed(fwd, steps, warmup)
     fl_b = backward_flops(c)
     fl_f = (6 if c.act == "swiglu" else 4) * c.A * H * F
-    peak = peaks["bf16_tflops_sustained"]
+    # the burst bf16 rate bounds a timed region of well under a second at the
+    # maximum clock; the sustained rate (measured under the power cap) is given beside it
+    peak = peaks["bf16_tflops"]
     # bytes the backward must move at least: the weights read by the GEMM1
     # recompute, the dA and the dxp GEMMs (W1, W3 twice; W2 once), the fp32
     # weight gradients written, and its inputs and outputs (x, dout, y, dx)
@@ -850,17 +852,20 @@ def run_backward(args):
         "us_per_backward": round(t_bwd * 1e6, 1),
         "tokens_per_s": round(T / t_bwd, 1),
         "backward_tflops": round(fl_b / t_bwd / 1e12, 1),
-        "backward_frac_of_sustained_bf16": round(fl_b / t_bwd / 1e12 / peak, 3),
+        "backward_frac_of_burst_bf16": round(fl_b / t_bwd / 1e12 / peak, 3),
+        "backward_frac_of_sustained_bf16": round(fl_b / t_bwd / 1e12 / peaks["bf16_tflops_sustained"], 3),
+        "timed_region_s": round(t_bwd * steps, 3),
         "roofline": {"bound": bound, "flops": fl_b, "bytes": by_b,
                      "time_lower_bound_us": round(max(t_tensor, t_hbm) * 1e6, 1),
                      "frac": round(max(t_tensor, t_hbm) / t_bwd, 3),
-                     "peaks": "sustained bf16 and measured copy rate of MEASURED_PEAKS.json"},
+                     "peaks": "burst bf16 and measured copy rate of MEASURED_PEAKS.json"},
         "us_forward_ffn": round(t_fwd * 1e6, 1),
         "forward_ffn_tflops": round(fl_f / t_fwd / 1e12, 1),
         "backward_over_forward_ffn": round(t_bwd / t_fwd, 2),
         "gpu_launches_per_backward": 8,
         "weight_gradients": "bf16" if args.wgrad_bf16 else "fp32",
-        "peak": {"bf16_tflops_sustained": peak, "source": peaks["source"]},
+        "peak": {"bf16_tflops": peak, "bf16_tflops_sustained": peaks["bf16_tflops_sustained"],
+                 "source": peaks["source"]},
         "clocks": clocks,
         "data": "synthetic: the config's logits, x and weights; dout ~ N(0,1) bf16",
     }
