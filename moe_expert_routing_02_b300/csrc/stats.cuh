@@ -174,7 +174,12 @@ __global__ void __launch_bounds__(kSmallThreads, 2) update_small_kernel(UpdateAr
 #pragma unroll
   for (int q = 0; q < kSmallE; ++q) h[q] = 0u;
 
-  constexpr int U = KM <= 2 ? kTokensAhead : 2;  // tokens in flight per thread, within 128 registers
+  // tokens in flight per thread (the loop is bound by the latency of its
+  // loads), within 128 registers; top-2 rows are read as one 8-byte load when
+  // both index arrays are 8-byte aligned
+  constexpr int U = KM <= 2 ? 6 : 2;
+  const bool pair_loads = KM == 2 && k == 2 &&
+                          ((reinterpret_cast<uintptr_t>(a.idx_cur) | reinterpret_cast<uintptr_t>(a.idx_prev)) & 7) == 0;
   const long long stride = (long long)gridDim.x * kSmallThreads * U;
   bool bad = false;
   for (long long base = (long long)blockIdx.x * kSmallThreads * U + threadIdx.x; base < a.T; base += stride) {
@@ -187,9 +192,25 @@ __global__ void __launch_bounds__(kSmallThreads, 2) update_small_kernel(UpdateAr
       for (int r = 0; r < KM; ++r) {
         cur[u][r] = -1;
         prv[u][r] = -1;
-        if (r < k && live) {
-          cur[u][r] = a.idx_cur[t * k + r];
-          if (cos) prv[u][r] = a.idx_prev[t * k + r];
+      }
+      if (pair_loads) {
+        if (live) {
+          const int2 c2 = *reinterpret_cast<const int2*>(a.idx_cur + t * 2);
+          cur[u][0] = c2.x;
+          cur[u][KM - 1] = c2.y;
+          if (cos) {
+            const int2 p2 = *reinterpret_cast<const int2*>(a.idx_prev + t * 2);
+            prv[u][0] = p2.x;
+            prv[u][KM - 1] = p2.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < KM; ++r) {
+          if (r < k && live) {
+            cur[u][r] = a.idx_cur[t * k + r];
+            if (cos) prv[u][r] = a.idx_prev[t * k + r];
+          }
         }
       }
     }
