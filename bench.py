@@ -245,7 +245,9 @@ def load_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
-FFN_SOURCES = ("ffn.cuh", "ffn_pair.cuh", "ffn_fused.cuh", "ffn_small.cuh", "sm100_ptx.cuh")
+# the FFN kernels and the host code that sets their launch parameters (the
+# fused kernel's lag between a block's GEMM1 and GEMM2 tiles changes its traffic)
+FFN_SOURCES = ("ffn.cuh", "ffn_pair.cuh", "ffn_fused.cuh", "ffn_small.cuh", "sm100_ptx.cuh", "moe_api.cu")
 
 
 def ffn_source_hash():

@@ -14,7 +14,7 @@
 //   GEMM2 tiles of blocks B-D..B-1.
 // Pair c takes positions c, c + pairs, ...  so every pair alternates short
 // GEMM1 tiles (heavy epilogue) with long GEMM2 tiles, and the epilogue of one
-// overlaps the main loop of the next; the lag D (about two rounds of tiles)
+// overlaps the main loop of the next; the lag D (about three rounds of tiles)
 // lets a block's GEMM1 tiles finish before its GEMM2 tiles come up.
 //
 // Dependency: a GEMM2 tile reads the bf16 intermediate rows of its block,
