@@ -3,8 +3,8 @@
 // EPS-MoE review, compute/communication overlap: the LocalReduce of expert
 // outputs is a memory-bound step; PopFetcher review: result collect.
 //   out[t] = sum_{r<k} w[t,r] * y[inv_perm[t*k+r]]
-// One warp per token row; each lane owns 16-byte chunks (8 bf16) and, for
-// each chunk, issues the k gathered row loads before accumulating them in
+// One warp per token row; each lane owns 16-byte chunks (8 bf16), issues the
+// k gathered row loads of several chunks before accumulating each chunk in
 // fp32 in rank order r = 0..k-1, rounding once to bf16.  Bound by HBM
 // bandwidth: A*H*2 bytes read, T*H*2 written, plus the small index/weight reads.
 #pragma once
@@ -15,32 +15,46 @@ namespace combine {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
+// The row's chunks are taken NC at a time (NC * K <= 8 loads of 16 bytes in
+// flight per lane, all issued before any is used), so a warp keeps a whole
+// 1024-wide row of top-2 outputs in flight instead of one chunk per lane.
 template <int K>
 __device__ __forceinline__ void combine_row(const uint16_t* __restrict__ y, const long long* slot, const float* wr,
                                             int H, uint16_t* __restrict__ dst, int lane) {
+  constexpr int NC = K <= 2 ? 4 : (K <= 4 ? 2 : 1);
   const int chunks = H / 8;
-  for (int c = lane; c < chunks; c += 32) {
-    uint4 v[K];
+  for (int c0 = lane; c0 < chunks; c0 += 32 * NC) {
+    uint4 v[NC][K];
 #pragma unroll
-    for (int r = 0; r < K; ++r) v[r] = ld_nc_v4(y + slot[r] * H + (size_t)c * 8);
-    float acc[8];
+    for (int j = 0; j < NC; ++j) {
+      const int c = c0 + 32 * j;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-    for (int r = 0; r < K; ++r) {
-      const uint32_t u[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(wr[r], bf16lo(u[i]), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(wr[r], bf16hi(u[i]), acc[2 * i + 1]);
-      }
+      for (int r = 0; r < K; ++r)
+        if (c < chunks) v[j][r] = ld_nc_v4(y + slot[r] * H + (size_t)c * 8);
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    st_v4(dst + (size_t)c * 8, o);
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      const int c = c0 + 32 * j;
+      if (c >= chunks) break;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+      for (int r = 0; r < K; ++r) {
+        const uint32_t u[4] = {v[j][r].x, v[j][r].y, v[j][r].z, v[j][r].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(wr[r], bf16lo(u[i]), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wr[r], bf16hi(u[i]), acc[2 * i + 1]);
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      st_v4(dst + (size_t)c * 8, o);
+    }
   }
 }
 
