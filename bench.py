@@ -69,9 +69,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-pdl", action="store_true", help="ordinary launches instead of programmatic dependent launch")
     ap.add_argument("--fuse-combine", action="store_true",
                     help="the combine in the FFN's second GEMM epilogue (moe_expert_ffn_combine)")
-    ap.add_argument("--small-sms", type=int, default=-1,
-                    help="SMs of the FFN's small-batch kernels (MOE_OPT_FFN_SMALL_SMS; -1: the library's split model, "
-                         "0: no small-batch path)")
+    ap.add_argument("--small-sms", type=int, default=0,
+                    help="SMs of the FFN's small-batch kernels (MOE_OPT_FFN_SMALL_SMS; 0, the library's default: no "
+                         "small-batch path; -1: the split model chooses)")
     ap.add_argument("--small-threshold", type=int, default=64,
                     help="experts with fewer rows take the small-batch FFN kernel (0: none, no side-stream launches)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -477,7 +477,8 @@ def run_ours(args, rank, world, local):
                    "ffn_kernel": args.ffn_kernel,
                    "pdl": not args.no_pdl,
                    "small_group_threshold": args.small_threshold,
-                   "small_path_sms": "split model" if args.small_sms < 0 else args.small_sms,
+                   "small_path_sms": "split model" if args.small_sms < 0 else (
+                       "none (the grouped kernel takes every expert)" if args.small_sms == 0 else args.small_sms),
                    "combine": "in the FFN's second GEMM epilogue" if args.fuse_combine else "separate kernel",
                    "chunks": args.chunks,
                    "replicas": ("physical copies (moe_replicate_weights)" if args.physical_replicas

@@ -571,16 +571,21 @@ moe_status moe_dispatch_noalloc(const uint16_t* x, const int32_t* idx, int T, in
  *     kernels and the grouped kernels of an expert-FFN call whose
  *     small_group_threshold is > 0 (EPS-MoE review, "GroupGemm vs
  *     DenseGemm": experts with few tokens on a separate path):
- *       -1 (default)  each call's kernels choose from the group table, all
+ *       0 (default)   no small-batch path: the grouped kernels take every
+ *                     expert (their schedule mixes the tiles of experts with
+ *                     one row tile, which stream weights, with the others)
+ *                     and the small-batch kernels are not launched.  On
+ *                     B300 no split measured faster on the workloads this
+ *                     library was tuned on, and the model below chose none,
+ *                     so by default the two launches are left out;
+ *       -1            each call's kernels choose from the group table, all
  *                     the same way: the small-batch kernels (a weight
  *                     stream, bound by HBM) get the SMs that balance their
  *                     time against the grouped kernels' (bound by the
  *                     tensor pipe) on the rest, and both run at once; when
  *                     running the small experts as padded grouped tiles on
  *                     every SM is expected to be faster, they do that
- *                     instead and the small-batch kernels do nothing;
- *       0             no small-batch path: the grouped kernels take every
- *                     expert;
+ *                     instead and the small-batch kernels exit at once;
  *       n > 0         the small-batch kernels use n SMs (even n with the
  *                     CTA-pair kernels), the grouped kernels the rest.
  *     The outputs are the same within the FFN tolerance whichever path an
@@ -607,7 +612,8 @@ moe_status moe_get_option(int option, int* value /* host */);
 
 /* Kernel launches one moe_expert_ffn (gather = 0) or moe_expert_ffn_gather
  * (gather = 1) call makes under the current options: 1 (fused) or 2 grouped
- * launches, plus 2 small-batch launches when small_group_threshold > 0.
+ * launches, plus 2 small-batch launches when small_group_threshold > 0 and
+ * MOE_OPT_FFN_SMALL_SMS is not 0.
  * 0 for sizes, activations or thresholds the FFN refuses.  Host only. */
 int moe_ffn_launches(int A, int E, int H, int F, int act, int small_group_threshold, int gather);
 

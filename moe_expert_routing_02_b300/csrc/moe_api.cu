@@ -78,7 +78,7 @@ struct DeviceInfo {
 // Process-wide and atomic: a call reads each option once when it is made.
 std::atomic<int> g_opt_ffn_kernel{MOE_FFN_KERNEL_AUTO};
 std::atomic<int> g_opt_ffn_selftest{0};  // one-shot: next GEMM1 withholds an accumulator signal
-std::atomic<int> g_opt_ffn_small_sms{-1};  // SM split of the FFN's small-batch path (-1: model)
+std::atomic<int> g_opt_ffn_small_sms{0};  // SM split of the FFN's small-batch path (0: none, -1: model)
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 std::mutex g_side_mu;  // one fork/join sequence at a time per process
@@ -621,10 +621,13 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   p1.rep_base = rep_base;
   p1.small_threshold = small_group_threshold;
   // SM split between the small-batch and the grouped kernels (every kernel
-  // of the call gets the same split fields, so they agree on it)
+  // of the call gets the same split fields, so they agree on it); with the
+  // option at 0 the grouped kernels take every expert and the small-batch
+  // kernels are not launched
+  const int small_sms_opt = g_opt_ffn_small_sms.load(std::memory_order_relaxed);
   if (small_group_threshold > 0) {
     p1.split_ctas = d->num_sms;
-    p1.split_force = g_opt_ffn_small_sms.load(std::memory_order_relaxed);
+    p1.split_force = small_sms_opt;
     p1.split_pair = use_pair ? 1 : 0;
     p1.split_rows = use_pair ? ffn2::BMP : ffn::BM;
     p1.ffn_H = H;
@@ -656,7 +659,7 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   ps1.flags = 0;
   ps1.n_tiles = (F + ffn_small::BMF - 1) / ffn_small::BMF;
   ps2.n_tiles = (H + ffn_small::BMF - 1) / ffn_small::BMF;
-  const bool small_path = small_group_threshold > 0;
+  const bool small_path = small_group_threshold > 0 && small_sms_opt != 0;
   if (small_path) {
     if (gather)
       mS1 = mA1;
@@ -957,7 +960,8 @@ int moe_ffn_launches(int A, int E, int H, int F, int act, int small_group_thresh
   if ((act != MOE_ACT_GELU && act != MOE_ACT_SWIGLU) || small_group_threshold < 0) return 0;
   bool use_pair = false, use_fused = false;
   ffn_choice(A, E, H, F, act, gather != 0, &use_pair, &use_fused);
-  return (use_fused ? 1 : 2) + (small_group_threshold > 0 ? 2 : 0);
+  const bool small_path = small_group_threshold > 0 && g_opt_ffn_small_sms.load(std::memory_order_relaxed) != 0;
+  return (use_fused ? 1 : 2) + (small_path ? 2 : 0);
 }
 
 // ------------------------------------------------------------------ options

@@ -139,13 +139,13 @@ def test_stats_and_replicate_reject_bad_arguments(L):
     assert L.moe_set_option(M.MOE_OPT_FFN_TIMEOUT_SELFTEST, 2) == inv
     v = ctypes.c_int(-1)
     assert L.moe_get_option(M.MOE_OPT_FFN_KERNEL, ctypes.byref(v)) == M.MOE_OK and v.value == 0
-    # the small-path SM split: -1 (model) by default, -1..4096 accepted
-    assert L.moe_get_option(M.MOE_OPT_FFN_SMALL_SMS, ctypes.byref(v)) == M.MOE_OK and v.value == -1
+    # the small-path SM split: 0 (no small-batch path) by default, -1..4096 accepted
+    assert L.moe_get_option(M.MOE_OPT_FFN_SMALL_SMS, ctypes.byref(v)) == M.MOE_OK and v.value == 0
     assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, -2) == inv
     assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 5000) == inv
     assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 24) == M.MOE_OK
     assert L.moe_get_option(M.MOE_OPT_FFN_SMALL_SMS, ctypes.byref(v)) == M.MOE_OK and v.value == 24
-    assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, -1) == M.MOE_OK
+    assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 0) == M.MOE_OK
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
@@ -256,19 +256,23 @@ def test_backward_calls_reject_bad_arguments(L):
 
 
 def test_ffn_launch_count_rule(L):
-    """The FFN's launch count under the default options: the fused kernel
-    (one launch) for CTA-pair-sized batches of experts of at most 16 MB, two
-    GEMM launches otherwise (the gather path, larger experts, small batches),
-    plus the two small-batch launches when the threshold is positive."""
+    """The FFN's launch count: the fused kernel (one launch) for
+    CTA-pair-sized batches of experts of at most 16 MB, two GEMM launches
+    otherwise (the gather path, larger experts, small batches), plus the two
+    small-batch launches when the threshold is positive and the small-batch
+    path is on (MOE_OPT_FFN_SMALL_SMS not 0; off by default)."""
     n = L.moe_ffn_launches
     gel, swi = M.MOE_ACT_GELU, M.MOE_ACT_SWIGLU
-    assert n(32768, 16, 1024, 2048, gel, 64, 0) == 3        # 8 MB experts: fused
-    assert n(32768, 16, 1024, 2048, gel, 0, 0) == 1
-    assert n(32768, 16, 1024, 2048, gel, 64, 1) == 4        # gather: two GEMM launches
-    assert n(32768, 16, 1024, 8192, gel, 64, 0) == 4        # 32 MB experts
-    assert n(32768, 16, 1024, 2048, swi, 64, 0) == 3        # 12 MB
-    assert n(32768, 16, 1024, 4096, swi, 64, 0) == 4        # 24 MB
-    assert n(1000, 16, 1024, 2048, gel, 64, 0) == 4         # A < 256 E: single-CTA GEMMs
+    for opt, small in ((0, 0), (-1, 2), (8, 2)):
+        assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, opt) == M.MOE_OK
+        assert n(32768, 16, 1024, 2048, gel, 64, 0) == 1 + small    # 8 MB experts: fused
+        assert n(32768, 16, 1024, 2048, gel, 0, 0) == 1
+        assert n(32768, 16, 1024, 2048, gel, 64, 1) == 2 + small    # gather: two GEMM launches
+        assert n(32768, 16, 1024, 8192, gel, 64, 0) == 2 + small    # 32 MB experts
+        assert n(32768, 16, 1024, 2048, swi, 64, 0) == 1 + small    # 12 MB
+        assert n(32768, 16, 1024, 4096, swi, 64, 0) == 2 + small    # 24 MB
+        assert n(1000, 16, 1024, 2048, gel, 64, 0) == 2 + small     # A < 256 E: single-CTA GEMMs
+    assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 0) == M.MOE_OK
     assert n(0, 16, 1024, 2048, gel, 64, 0) == 0
     assert n(32768, 16, 96, 2048, gel, 64, 0) == 0
     assert n(32768, 16, 1024, 2000, gel, 64, 0) == 0
@@ -310,7 +314,7 @@ int main(void) {
     assert out.returncode == 0, out.stderr
     ver, ws, bad, msg, n = out.stdout.strip().split("|")
     assert ver == "sm_103a" and int(ws) == (32 * 16 + 64) * 4
-    assert int(bad) == M.MOE_ERR_INVALID and msg and int(n) == 3
+    assert int(bad) == M.MOE_ERR_INVALID and msg and int(n) == 1   # fused; no small-batch path by default
 
 
 def test_every_entry_point_names_its_passage():

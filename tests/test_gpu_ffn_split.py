@@ -28,7 +28,7 @@ def _lib():
     _build.build()
     M.lib()
     yield
-    M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, -1)
+    M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 0)
     M.moe_set_option(M.MOE_OPT_FFN_KERNEL, M.MOE_FFN_KERNEL_AUTO)
 
 
@@ -55,7 +55,7 @@ def test_split_matches_oracle_and_grouped_rows_are_stable(kernel, act):
         M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, sms)
         ys[sms] = M.moe_expert_ffn(xp, go, None, None, w1, w3, w2, act, small_group_threshold=64)
         M.moe_check()
-    M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, -1)
+    M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 0)
     gof = go.cpu().numpy()
     ref = O.expert_ffn(W.bf16_bits(xp), gof[:E + 1], None, W.bf16_bits(w1),
                        None if w3 is None else W.bf16_bits(w3), W.bf16_bits(w2), act)

@@ -383,7 +383,7 @@ def test_ffn_small_batch_path_thresholds(thresh, act, ffn_kernel):
         y = M.moe_expert_ffn(xp, go, None, None, w1, w3, w2, act, small_group_threshold=thresh)
         ok_check()
     finally:
-        M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, -1)
+        M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 0)
     ref = O.expert_ffn(W.bf16_bits(xp), host(go)[:c.E + 1], None, W.bf16_bits(w1),
                        None if w3 is None else W.bf16_bits(w3), W.bf16_bits(w2), act)
     got = O.bf16_to_f64(W.bf16_bits(y))
