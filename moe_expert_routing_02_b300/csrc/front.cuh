@@ -10,22 +10,30 @@
 //      top-k of each token (route::topk_token), idx / w written; per tile the
 //      expert counts (shared atomics), written as the tile's exclusive prefix
 //      within the block, and the block's totals (blk_tot, and added to the
-//      histogram accumulator); the co-selection pairs with the previous
+//      histogram accumulator and to the totals of the block's segment of
+//      kSegBlocks route blocks); the co-selection pairs with the previous
 //      layer's routing (shared atomics, flushed to the window state's
 //      accumulator).
 //   F2 (scatter_copy_kernel), one block per tile plus one statistics block.
-//      Every block takes the histogram from the accumulator.  The statistics
-//      block folds it and the co-selection counts into the window ring and
-//      sums (as stats::update_kernel does) and predicts the next layer
+//      Every block first issues all its independent loads at once (the
+//      histogram; for a tile, its prefix, the segment and block totals before
+//      it, its first expert ids).  The statistics block folds the histogram
+//      and the co-selection counts into the window ring and sums (as
+//      stats::update_kernel does) and predicts the next layer
 //      (stats::predict_block); the dispatch reads none of that, so it runs
-//      beside the tiles.  Each tile block computes the replica counts
-//      (replicate::replicate_block, or replicate::apportion_block first when
-//      a predicted popularity is given) and the group layout (closed form of
-//      the round-robin split) itself -- O(E) integer work, the same in every
-//      block -- then the tile's starting rank per expert (totals of the route
-//      blocks before its own, plus its prefix within its block), stable
-//      in-tile ranks -> slots -> perm / inv_perm, and the copy of the rows of
-//      the tile's assignments to their slots with 16-byte vectors.
+//      beside the tiles.  Each tile block computes the replica counts and the
+//      group layout itself -- O(E) integer work, the same in every block: one
+//      scan for replicas from the histogram, the block forms
+//      (replicate::replicate_block, after replicate::apportion_block for a
+//      predicted popularity) with a copies budget -- then the tile's starting
+//      rank per expert, stable in-tile ranks -> slots -> perm / inv_perm, and
+//      the copy of the rows of the tile's assignments to their slots with
+//      16-byte vectors.  For short rows the route blocks let this kernel
+//      start as soon as they passed their own wait, and each tile block first
+//      asks L2 for its token rows, so that read overlaps the routing and the
+//      plan.  The paths few blocks take (statistics, budget or shares, table
+//      writes) are out of line: the code every tile block runs stays compact,
+//      which measured ~3 us shorter than with everything inlined.
 // No block waits for a single planner: the plan that one block used to run
 // after all the routing (histogram fold, prediction, replica table, layout)
 // is spread over the blocks that need it.  Counts are integers, so nothing
@@ -35,6 +43,7 @@
 #include "dispatch.cuh"
 #include "replicate.cuh"
 #include "route.cuh"
+#include "sm100_ptx.cuh"
 #include "stats.cuh"
 
 namespace front {
@@ -54,6 +63,13 @@ __host__ inline long long num_tiles(long long T) { return (T + tile_tokens(T) - 
 // Route blocks: at most kMaxRouteBlocks (the F2 prologue reads the totals
 // of the blocks before its own), and at least one pass of every warp.
 constexpr int kMaxRouteBlocks = 128;
+// Route blocks are grouped in segments of kSegBlocks; each route block also
+// adds its totals to its segment's, so a tile's starting ranks need at most
+// kSegments - 1 segment totals and kSegBlocks - 1 block totals.
+constexpr int kSegBlocks = 8;
+constexpr int kSegments = kMaxRouteBlocks / kSegBlocks;
+// Those totals are loaded kPreLoads per thread at once (more in a loop).
+constexpr int kPreLoads = 8;
 // Workspace: tile prefixes [ntiles][E], block totals [<= ntiles][E] (the
 // size keeps room for [4][E] more words).
 __host__ inline size_t workspace_bytes(long long T, int E) {
@@ -72,7 +88,8 @@ struct Args {
   const int32_t* idx_prev;
   uint32_t* acc_h;   // [E] histogram accumulator (zero between calls)
   uint32_t* acc_c;   // [E*E] co-selection accumulator (zero between calls)
-  uint32_t* ticket;  // F2 blocks that took the histogram (zero between calls)
+  uint32_t* seg_tot; // [kSegments][E] route-block totals per segment (zero between calls)
+  uint32_t* ticket;  // F2 blocks that left (zero between calls)
   uint32_t* ring_h;
   unsigned long long* hsum;
   uint32_t* ring_c;
@@ -96,6 +113,7 @@ struct Args {
   int32_t* counts;   // [ntiles][E]: tile's exclusive prefix within its route block
   int32_t* blk_tot;  // [route blocks][E]: block totals
   int32_t* group_offsets;
+  int release_early;  // route blocks let the scatter/copy kernel start once they passed their wait
 };
 
 // The layer's co-selection counts into window ring slot and sums (pair j-1, j).
@@ -111,7 +129,7 @@ __device__ __forceinline__ void fold_cosel(const Args& a) {
 // The statistics block of F2: the histogram into the window ring and sums,
 // the co-selection counts likewise, then the prediction for the next layer.
 // Nothing in the dispatch reads these, so the block runs beside the copy.
-__device__ __forceinline__ void stats_tail(const Args& a, const int32_t* hist_s) {
+__device__ __noinline__ void stats_tail(const Args& a, const int32_t* hist_s) {
   for (int e = threadIdx.x; e < a.E; e += kThreads) {
     const int32_t h = hist_s[e];
     const uint32_t old = a.ring_h[e];
@@ -127,6 +145,9 @@ __device__ __forceinline__ void stats_tail(const Args& a, const int32_t* hist_s)
 template <int G, bool VEC>
 __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
   pdl_wait();
+  // The scatter/copy kernel may start now: before its own wait it only reads
+  // x, which the wait above has seen completed.
+  if (a.release_early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint32_t dsm[];  // cnt[tiles_per_block][E], then cosel[E*E] (small E)
   constexpr int TPW = 32 / G;
   const int E = a.E, k = a.k;
@@ -197,7 +218,10 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
       run += cnt[i * E + e];
     }
     a.blk_tot[(size_t)blockIdx.x * E + e] = (int32_t)run;
-    if (run) atomicAdd(a.acc_h + e, run);
+    if (run) {
+      atomicAdd(a.acc_h + e, run);
+      atomicAdd(a.seg_tot + (size_t)(blockIdx.x / kSegBlocks) * E + e, run);
+    }
   }
   if (cos_smem)
     for (int i = threadIdx.x; i < E * E; i += kThreads)
@@ -205,67 +229,94 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
 }
 
 // Dynamic shared memory of scatter_copy_kernel, in int32 words.
-__host__ __device__ inline int scatter_smem_words(int E, int TT, int k) { return (16 + kWarps) * E + 1 + TT * k; }
+__host__ __device__ inline int scatter_smem_words(int E, int TT, int k) {
+  return (16 + kWarps) * E + 1 + TT * k + kThreads;
+}
+// A tile's token rows are prefetched into L2 when they take at most this many
+// bytes (measured: on 160 KB tiles of 10 KB rows the prefetch slowed the copy).
+constexpr long long kPrefetchMaxBytes = 64 * 1024;
 
-// F2.  Block 0 is the statistics block (stats_tail); block b >= 1 serves
-// dispatch tile b - 1.  Every block first takes the layer's histogram from the
-// accumulator the route blocks added their totals to; the last block to take
-// it clears the accumulator (and the ticket) for the next call.  A tile block
-// then computes the replica table and the group layout itself -- O(E) integer
-// work, identical in every block -- so no block waits for a single planner;
-// tile 0's block writes the tables out.  Then: the tile's starting rank per
-// expert (totals of the route blocks before its own, plus its prefix within
-// its block), stable in-tile ranks of its assignments (in f order), slots,
-// perm / inv_perm, and the row copy xp[slot] = x[f / k].
-__global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, const uint16_t* __restrict__ x, int H,
-                                                                uint16_t* __restrict__ xp,
-                                                                int32_t* __restrict__ perm,
-                                                                int32_t* __restrict__ inv_perm) {
-  pdl_wait();
-  extern __shared__ int32_t sm[];
-  const int E = a.E, k = a.k;
-  int32_t* hist_s = sm;                   // [E]
-  int32_t* base_s = hist_s + E;           // [E]   first slot of the expert's rows
-  int32_t* n_s = base_s + E;              // [E]   replica groups of the expert
-  int32_t* rb_s = n_s + E;                // [E+1] first group of the expert
-  int32_t* copies_s = rb_s + E + 1;       // [E]
-  int32_t* ge_s = copies_s + E;           // [2E]
-  int32_t* load_s = ge_s + 2 * E;         // [E]   loads apportioned from the shares
-  int32_t* warp_cnt = load_s + E;         // [kWarps][E]
-  int32_t* run = warp_cnt + kWarps * E;   // [E]
-  int32_t* slot_s = run + E;              // [TT*k]
-  __shared__ int32_t wtot[kWarps];
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-
-  for (int e = tid; e < E; e += kThreads) hist_s[e] = (int32_t)a.acc_h[e];
-  __syncthreads();
-  if (tid == 0 && atomicAdd(a.ticket, 1u) == gridDim.x - 1) {
-    // every block holds its copy of the histogram now
-    for (int e = 0; e < E; ++e) a.acc_h[e] = 0u;
-    *a.ticket = 0u;
-  }
-  if (blockIdx.x == 0) {
-    stats_tail(a, hist_s);
-    return;
-  }
-  const int tile = (int)blockIdx.x - 1;
-  const long long A = (long long)a.T * k;
-
-  // ---- replica table and group layout
-  if (a.replicate) {
-    const int32_t* ld = hist_s;
-    if (a.rep_share) {  // replicas from a prediction: loads apportioned by the shares
-      replicate::apportion_block(a.rep_share, E, A, load_s);
-      __syncthreads();
-      ld = load_s;
+// The row copy of a tile: one warp per two assignments (8
+// loads of 16 bytes in flight per lane), 16-byte chunks.
+__device__ __forceinline__ void copy_rows(const uint16_t* __restrict__ x, int H, uint16_t* __restrict__ xp, int k,
+                                          long long f0, int nA, const int32_t* slot_s) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int chunks = H / 8;
+  for (int i = 2 * wid; i < nA; i += 2 * kWarps) {
+    const int s0 = slot_s[i], s1 = i + 1 < nA ? slot_s[i + 1] : -1;
+    const uint16_t* src0 = x + ((f0 + i) / k) * H;
+    const uint16_t* src1 = x + ((f0 + i + 1) / k) * H;
+    uint16_t* dst0 = xp + (size_t)(s0 < 0 ? 0 : s0) * H;
+    uint16_t* dst1 = xp + (size_t)(s1 < 0 ? 0 : s1) * H;
+    for (int c = lane; c < chunks; c += 128) {
+      uint4 v0[4], v1[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int cu = c + 32 * u;
+        if (cu < chunks) {
+          if (s0 >= 0) v0[u] = ld_nc_v4(src0 + (size_t)cu * 8);
+          if (s1 >= 0) v1[u] = ld_nc_v4(src1 + (size_t)cu * 8);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int cu = c + 32 * u;
+        if (cu < chunks) {
+          if (s0 >= 0) st_v4(dst0 + (size_t)cu * 8, v0[u]);
+          if (s1 >= 0) st_v4(dst1 + (size_t)cu * 8, v1[u]);
+        }
+      }
     }
-    replicate::replicate_block(ld, E, A, a.num, a.den, a.max_copies, copies_s, rb_s, ge_s, a.budget);
-  } else {
-    for (int e = tid; e <= E; e += kThreads) rb_s[e] = e;
   }
+}
+
+// Every block takes a ticket (thread 0) once it has read the histogram and
+// segment accumulators; the ticket's value is first needed at the block's
+// exit, where the last block to have taken one clears those accumulators and
+// the ticket for the next call.
+__device__ __forceinline__ unsigned take_ticket(const Args& a) {
+  return threadIdx.x == 0 ? atomicAdd(a.ticket, 1u) : 0u;
+}
+__device__ __forceinline__ void leave_block(const Args& a, unsigned ticket) {
+  __shared__ int last_s;
+  if (threadIdx.x == 0) last_s = ticket == gridDim.x - 1;
+  __syncthreads();
+  if (last_s) {
+    for (int i = threadIdx.x; i < a.E; i += kThreads) a.acc_h[i] = 0u;
+    for (int i = threadIdx.x; i < kSegments * a.E; i += kThreads) a.seg_tot[i] = 0u;
+    if (threadIdx.x == 0) *a.ticket = 0u;
+  }
+}
+
+// Shared-memory arrays of the plan in scatter_copy_kernel.
+struct Plan {
+  int32_t* hist;    // [E]   histogram
+  int32_t* base;    // [E]   first slot of the expert's rows
+  int32_t* n;       // [E]   replica groups of the expert
+  int32_t* rb;      // [E+1] first group of the expert
+  int32_t* copies;  // [E]
+  int32_t* ge;      // [2E]  expert of each group
+  int32_t* load;    // [E]   loads apportioned from the shares
+};
+
+// The plan with a copies budget or from predicted shares (the block forms of
+// the replica rule), then the expert bases.  Kept out of line, like the other
+// paths few blocks take, so the instructions every tile block runs stay
+// together.
+__device__ __noinline__ void plan_general(const Args& a, const Plan& pl, long long A) {
+  __shared__ int32_t wtot[kWarps];
+  const int E = a.E, e = threadIdx.x, lane = e & 31, wid = e >> 5;
+  int32_t *hist_s = pl.hist, *base_s = pl.base, *n_s = pl.n, *rb_s = pl.rb, *copies_s = pl.copies, *ge_s = pl.ge,
+          *load_s = pl.load;
+  const int32_t* ld = hist_s;
+  if (a.rep_share) {  // replicas from a prediction: loads apportioned by the shares
+    replicate::apportion_block(a.rep_share, E, A, load_s);
+    __syncthreads();
+    ld = load_s;
+  }
+  replicate::replicate_block(ld, E, A, a.num, a.den, a.max_copies, copies_s, rb_s, ge_s, a.budget);
   __syncthreads();
   // expert bases: exclusive scan of the histogram (E <= kThreads)
-  const int e = tid;
   int incl = e < E ? hist_s[e] : 0;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -280,49 +331,232 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, co
     base_s[e] = before + incl - hist_s[e];
     n_s[e] = rb_s[e + 1] - rb_s[e];
   }
-  __syncthreads();
-  if (tile == 0) {
-    const int ngroups = rb_s[E];
-    if (e < E) {
-      const int hh = hist_s[e], n = n_s[e], rb = rb_s[e], base = base_s[e];
-      const int qs = hh / n, qr = hh % n;
-      for (int q = 0; q < n; ++q) a.group_offsets[rb + q] = base + q * qs + (q < qr ? q : qr);
-      if (a.replicate) {
-        a.copies[e] = copies_s[e];
-        a.rep_base[e] = rb;
-      }
-    }
-    if (a.replicate) {
-      if (tid == 0) a.rep_base[E] = ngroups;
-      for (int g = tid; g < 2 * E; g += kThreads) a.group_expert[g] = ge_s[g];
-    }
-    for (int g = ngroups + tid; g <= 2 * E; g += kThreads) a.group_offsets[g] = (int32_t)A;
-  }
+}
 
-  // ---- starting ranks of the tile
-  const long long f0 = (long long)tile * a.TT * k;
-  long long f1 = f0 + (long long)a.TT * k;
+// Tile 0's block writes the replica table and the group offsets.
+__device__ __noinline__ void write_tables(const Args& a, const Plan& pl, long long A) {
+  const int E = a.E, e = threadIdx.x, tid = threadIdx.x;
+  const int32_t *hist_s = pl.hist, *base_s = pl.base, *n_s = pl.n, *rb_s = pl.rb, *copies_s = pl.copies,
+                *ge_s = pl.ge;
+  const int ngroups = rb_s[E];
+  if (e < E) {
+    const int hh = hist_s[e], n = n_s[e], rb = rb_s[e], base = base_s[e];
+    const int qs = hh / n, qr = hh % n;
+    for (int q = 0; q < n; ++q) a.group_offsets[rb + q] = base + q * qs + (q < qr ? q : qr);
+    if (a.replicate) {
+      a.copies[e] = copies_s[e];
+      a.rep_base[e] = rb;
+    }
+  }
+  if (a.replicate) {
+    if (tid == 0) a.rep_base[E] = ngroups;
+    for (int g = tid; g < 2 * E; g += kThreads) a.group_expert[g] = ge_s[g];
+  }
+  for (int g = ngroups + tid; g <= 2 * E; g += kThreads) a.group_offsets[g] = (int32_t)A;
+}
+
+// F2.  Block 0 is the statistics block (stats_tail); block b >= 1 serves
+// dispatch tile b - 1.  Every block first takes the layer's histogram from the
+// accumulator the route blocks added their totals to; the last block to take
+// it clears the accumulator (and the ticket) for the next call.  A tile block
+// then computes the replica table and the group layout itself -- O(E) integer
+// work, identical in every block -- so no block waits for a single planner;
+// tile 0's block writes the tables out.  Then: the tile's starting rank per
+// expert (totals of the route blocks before its own, plus its prefix within
+// its block), stable in-tile ranks of its assignments (in f order), slots,
+// perm / inv_perm, and the row copy xp[slot] = x[f / k].  With `prefetch`,
+// each tile block asks L2 for its token rows before the wait on the previous
+// kernel: x is the layer's input, complete before the route kernel of this
+// call passed its own wait (and this kernel starts only after every route
+// block has passed it), so the read may overlap everything that follows.
+__global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, const uint16_t* __restrict__ x, int H,
+                                                                uint16_t* __restrict__ xp,
+                                                                int32_t* __restrict__ perm,
+                                                                int32_t* __restrict__ inv_perm, int prefetch) {
+  extern __shared__ int32_t sm[];
+  if (prefetch && blockIdx.x > 0 && threadIdx.x == 0) {
+    const long long t0 = (long long)(blockIdx.x - 1) * a.TT;
+    const long long nt = a.T - t0 < a.TT ? a.T - t0 : a.TT;
+    sm100::bulk_prefetch_l2(x + t0 * H, (uint32_t)(nt * H * 2));
+  }
+  pdl_wait();
+  const int E = a.E, k = a.k;
+  int32_t* hist_s = sm;                   // [E]
+  int32_t* base_s = hist_s + E;           // [E]   first slot of the expert's rows
+  int32_t* n_s = base_s + E;              // [E]   replica groups of the expert
+  int32_t* rb_s = n_s + E;                // [E+1] first group of the expert
+  int32_t* copies_s = rb_s + E + 1;       // [E]
+  int32_t* ge_s = copies_s + E;           // [2E]
+  int32_t* load_s = ge_s + 2 * E;         // [E]   loads apportioned from the shares
+  int32_t* warp_cnt = load_s + E;         // [kWarps][E]
+  int32_t* run = warp_cnt + kWarps * E;   // [E]
+  int32_t* slot_s = run + E;              // [TT*k]
+  int32_t* part_s = slot_s + a.TT * k;    // [kThreads] partial sums
+  const Plan pl{hist_s, base_s, n_s, rb_s, copies_s, ge_s, load_s};
+  __shared__ int32_t wtot[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int tile = (int)blockIdx.x - 1;
+  const long long A = (long long)a.T * k;
+  const long long f0 = tile >= 0 ? (long long)tile * a.TT * k : 0;
+  long long f1 = tile >= 0 ? f0 + (long long)a.TT * k : 0;
   if (f1 > A) f1 = A;
   const int nA = (int)(f1 - f0);
+
+  // Every load that does not depend on another is issued here at once: the
+  // histogram, the tile's prefix within its route block, the totals of the
+  // segments and route blocks before it, and the tile's first expert ids.
+  const int rblk = tile >= 0 ? tile / a.tiles_per_block : 0;
+  const int sg = rblk / kSegBlocks;
+  const int nseg = sg * E;                        // segment totals before the tile's segment
+  const int npre = nseg + (rblk - sg * kSegBlocks) * E;  // ... plus its route blocks before the tile's
+  const int32_t* blk_seg = a.blk_tot + (size_t)sg * kSegBlocks * E;
+  int hv = 0, cv = 0, ex0 = -1;
+  int pv[kPreLoads];
+  if (tid < E) hv = (int32_t)a.acc_h[tid];
+  if (tile >= 0) {
+    if (tid < E) cv = a.counts[(size_t)tile * E + tid];
+#pragma unroll
+    for (int u = 0; u < kPreLoads; ++u) {
+      const int i = tid + u * kThreads;
+      pv[u] = i < nseg ? (int32_t)a.seg_tot[i] : i < npre ? blk_seg[i - nseg] : 0;
+    }
+    if (tid < nA) ex0 = a.idx[f0 + tid];
+  }
+  if (tid < E) {
+    hist_s[tid] = hv;
+    run[tid] = cv;
+  }
   for (int i = tid; i < kWarps * E; i += kThreads) warp_cnt[i] = 0;
-  for (int i = tid; i < E; i += kThreads) run[i] = a.counts[(size_t)tile * E + i];
   __syncthreads();
-  // add the totals of the route blocks before the tile's own
-  const int nprev = (tile / a.tiles_per_block) * E;
-  for (int i0 = tid; i0 < nprev; i0 += 8 * kThreads) {
-    int v[8];
+  if (tile < 0) {
+    const unsigned ticket = take_ticket(a);
+    stats_tail(a, hist_s);
+    leave_block(a, ticket);
+    return;
+  }
+  // starting rank of the tile per expert: its prefix within its route block
+  // plus the totals before that block (integers: any order of the adds)
+  if (kThreads % E == 0) {
+    // every total this thread loads belongs to expert tid % E: add them here,
+    // then across that expert's threads (shuffles, then shared memory), with
+    // no atomics on the few hot bins
+    int acc = 0;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = i0 + u * kThreads < nprev ? a.blk_tot[i0 + u * kThreads] : 0;
+    for (int u = 0; u < kPreLoads; ++u) acc += pv[u];
+    for (int i0 = tid + kPreLoads * kThreads; i0 < npre; i0 += kPreLoads * kThreads) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (v[u]) atomicAdd(&run[(i0 + u * kThreads) % E], v[u]);
+      for (int u = 0; u < kPreLoads; ++u) {
+        const int i = i0 + u * kThreads;
+        acc += i < nseg ? (int32_t)a.seg_tot[i] : i < npre ? blk_seg[i - nseg] : 0;
+      }
+    }
+    if (E < 32) {
+      for (int off = E; off < 32; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane < E) part_s[wid * E + lane] = acc;
+    } else {
+      part_s[tid] = acc;
+    }
+    __syncthreads();
+    if (tid < E) {
+      const int nparts = E < 32 ? kWarps : kThreads / E;
+      int s2 = 0;
+      for (int j = 0; j < nparts; ++j) s2 += part_s[j * E + tid];
+      run[tid] += s2;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kPreLoads; ++u)
+      if (pv[u]) atomicAdd(&run[(tid + u * kThreads) % E], pv[u]);
+    for (int i0 = tid + kPreLoads * kThreads; i0 < npre; i0 += kPreLoads * kThreads) {
+#pragma unroll
+      for (int u = 0; u < kPreLoads; ++u) {
+        const int i = i0 + u * kThreads;
+        pv[u] = i < nseg ? (int32_t)a.seg_tot[i] : i < npre ? blk_seg[i - nseg] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kPreLoads; ++u)
+        if (pv[u]) atomicAdd(&run[(i0 + u * kThreads) % E], pv[u]);
+    }
+    __syncthreads();
+  }
+  // every thread's reads of the accumulators are done (both branches end in a barrier)
+  const unsigned ticket = take_ticket(a);
+
+  // ---- replica table and group layout
+  const int e = tid;
+  if (a.replicate && (a.rep_share || a.budget >= 0)) {
+    plan_general(a, pl, A);
+  } else {
+    // Replicas from the histogram with no copies budget (or none at all): the
+    // replica rule is a closed form per expert (replicate::replicate_block
+    // states it), so the copies, the expert bases and the group bases come
+    // from one scan of (load, groups) over the experts.
+    __shared__ int32_t wtot_n[kWarps];
+    const int h = e < E ? hist_s[e] : 0;
+    int c = 0;
+    if (a.replicate && e < E && A > 0 && (long long)h * E * a.den > (long long)a.num * A) {
+      const long long q = (long long)h * E + A - 1;  // ceil(h * E / A) by a 32-bit division when it fits
+      c = (q >> 31) == 0 ? (int)((unsigned)q / (unsigned)A) - 1 : (int)(q / A - 1);
+      if (a.max_copies >= 0 && c > a.max_copies) c = a.max_copies;
+    }
+    const int n = e < E ? c + 1 : 0;
+    int ih = h, in = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int vh = __shfl_up_sync(0xffffffffu, ih, off);
+      const int vn = __shfl_up_sync(0xffffffffu, in, off);
+      if (lane >= off) {
+        ih += vh;
+        in += vn;
+      }
+    }
+    if (lane == 31) {
+      wtot[wid] = ih;
+      wtot_n[wid] = in;
+    }
+    const int any_negative = __syncthreads_or(e < E && h < 0);
+    int bh = 0, bn = 0;
+    long long all_h = 0;
+    int all_n = 0;
+    for (int ww = 0; ww < kWarps; ++ww) {
+      if (ww < wid) {
+        bh += wtot[ww];
+        bn += wtot_n[ww];
+      }
+      all_h += wtot[ww];
+      all_n += wtot_n[ww];
+    }
+    // the block form's precondition: loads non-negative and summing to at
+    // most the total (then fewer than 2E groups); broken -> no replication
+    const bool bad = a.replicate && (any_negative || (A > 0 && all_h > A) || all_n > 2 * E);
+    if (bad && tid == 0) moe_flag_error(MOE_DEVERR_DATA);
+    if (e < E) {
+      base_s[e] = bh + ih - h;
+      const int rb = bad ? e : bn + in - n;
+      n_s[e] = bad ? 1 : n;
+      rb_s[e] = rb;
+      copies_s[e] = bad ? 0 : c;
+      if (a.replicate && tile == 0) {
+        ge_s[rb] = e;
+        if (bad) ge_s[E + e] = -1;
+        else
+          for (int q = 1; q < n; ++q) ge_s[rb + q] = e;
+      }
+    }
+    const int ngroups = bad ? E : all_n;
+    if (tid == 0) rb_s[E] = ngroups;
+    if (a.replicate && tile == 0)
+      for (int g = ngroups + tid; g < 2 * E; g += kThreads) ge_s[g] = -1;
   }
   __syncthreads();
+  if (tile == 0) write_tables(a, pl, A);
+
+  // ---- stable in-tile ranks, slots, perm / inv_perm
   for (int r0 = 0; r0 < nA; r0 += kThreads) {
     const int i = r0 + tid;
     int ex = -1;
     if (i < nA) {
-      ex = a.idx[f0 + i];
+      ex = r0 == 0 ? ex0 : a.idx[f0 + i];
       if ((unsigned)ex >= (unsigned)E) ex = -1;
     }
     const unsigned peers = __match_any_sync(0xffffffffu, ex);
@@ -354,36 +588,8 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, co
     }
     __syncthreads();
   }
-  if (x == nullptr) return;
-  // rows: one warp per two assignments (8 loads of 16 bytes in flight per
-  // lane), 16-byte chunks
-  const int chunks = H / 8;
-  for (int i = 2 * wid; i < nA; i += 2 * kWarps) {
-    const int s0 = slot_s[i], s1 = i + 1 < nA ? slot_s[i + 1] : -1;
-    const uint16_t* src0 = x + ((f0 + i) / k) * H;
-    const uint16_t* src1 = x + ((f0 + i + 1) / k) * H;
-    uint16_t* dst0 = xp + (size_t)(s0 < 0 ? 0 : s0) * H;
-    uint16_t* dst1 = xp + (size_t)(s1 < 0 ? 0 : s1) * H;
-    for (int c = lane; c < chunks; c += 128) {
-      uint4 v0[4], v1[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int cu = c + 32 * u;
-        if (cu < chunks) {
-          if (s0 >= 0) v0[u] = ld_nc_v4(src0 + (size_t)cu * 8);
-          if (s1 >= 0) v1[u] = ld_nc_v4(src1 + (size_t)cu * 8);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int cu = c + 32 * u;
-        if (cu < chunks) {
-          if (s0 >= 0) st_v4(dst0 + (size_t)cu * 8, v0[u]);
-          if (s1 >= 0) st_v4(dst1 + (size_t)cu * 8, v1[u]);
-        }
-      }
-    }
-  }
+  if (x != nullptr) copy_rows(x, H, xp, k, f0, nA, slot_s);
+  leave_block(a, ticket);
 }
 
 // Dynamic shared memory of route_count_kernel stays below 17 KB (tile counts
@@ -445,6 +651,11 @@ static cudaError_t launch(const Args& a0, const uint16_t* x, int H, uint16_t* xp
                           cudaStream_t st) {
   Args a = a0;
   a.tiles_per_block = route_tiles_per_block(a.T, a.E);
+  // Short token rows: the scatter/copy blocks start while the route blocks
+  // run and ask L2 for their rows first (measured better than the route
+  // blocks prefetching them, which slowed the routing itself).
+  const int prefetch = (x != nullptr && a.ntiles > 0 && (long long)a.TT * H * 2 <= kPrefetchMaxBytes) ? 1 : 0;
+  a.release_early = prefetch;
   const bool vec = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.logits) & 15) == 0);
   cudaError_t e;
   if (a.E <= 8) e = launch_route_g<1>(a, vec, st);
@@ -459,7 +670,7 @@ static cudaError_t launch(const Args& a0, const uint16_t* x, int H, uint16_t* xp
   if (smem > (size_t)kScatterDynSmemMax) return cudaErrorInvalidValue;
   if ((e = ensure_smem_attr(scatter_copy_kernel, done_scatter, kScatterDynSmemMax)) != cudaSuccess) return e;
   e = launch_pdl(scatter_copy_kernel, dim3((unsigned)(a.ntiles + 1)), dim3(kThreads), smem, st, a, x, H, xp, perm,
-                 inv_perm);
+                 inv_perm, prefetch);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -160,6 +160,7 @@ struct moe_stats {
   uint32_t* ring_c;                  // [L-1][s][E][E]
   unsigned long long* csum;          // [L-1][E][E]
   uint32_t* acc;                     // [E + E*E] (zero between calls)
+  uint32_t* seg;                     // [front::kSegments][E] (zero between calls)
   uint32_t* ticket;                  // [1]
   double* dscratch;                  // [E + E*E] decay-weighted sums (moe_predict_decay), not exported
   size_t state_bytes;                // exported bytes (rings + sums), without header
@@ -226,8 +227,9 @@ moe_status moe_stats_create(moe_stats** out, int L, int E, int window, void* str
   const size_t nc = (size_t)(L - 1) * window * E * E;
   const size_t ncs = (size_t)(L - 1) * E * E;
   const size_t nacc = (size_t)E + (size_t)E * E;
+  const size_t nseg = (size_t)front::kSegments * E;
   // layout: 8-byte sums first, then 4-byte arrays, then the fp64 scratch
-  const size_t four = ((nh + nc + nacc + 1) * 4 + 7) / 8 * 8;
+  const size_t four = ((nh + nc + nacc + nseg + 1) * 4 + 7) / 8 * 8;
   const size_t bytes = (nhs + ncs) * 8 + four + nacc * 8;
   cudaError_t e = cudaMalloc(&st->block, bytes);
   if (e != cudaSuccess) {
@@ -246,6 +248,8 @@ moe_status moe_stats_create(moe_stats** out, int L, int E, int window, void* str
   p += nc * 4;
   st->acc = reinterpret_cast<uint32_t*>(p);
   p += nacc * 4;
+  st->seg = reinterpret_cast<uint32_t*>(p);
+  p += nseg * 4;
   st->ticket = reinterpret_cast<uint32_t*>(p);
   st->dscratch = reinterpret_cast<double*>(static_cast<char*>(st->block) + (nhs + ncs) * 8 + four);
   st->state_bytes = (nhs + ncs) * 8 + (nh + nc) * 4;
@@ -328,7 +332,6 @@ moe_status moe_stats_update(moe_stats* st, int64_t iter, int layer, const int32_
   a.T = T;
   a.k = k;
   a.E = E;
-  a.acc_h = st->acc;
   a.acc_h = st->acc;
   a.acc_c = st->acc + E;
   a.ticket = st->ticket;
@@ -487,6 +490,7 @@ moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E,
   a.idx_prev = idx_prev;
   a.acc_h = st->acc;
   a.acc_c = st->acc + E;
+  a.seg_tot = st->seg;
   a.ticket = st->ticket;
   a.ring_h = st->ring_h + ((size_t)layer * s + slot) * E;
   a.hsum = st->hsum + (size_t)layer * E;
