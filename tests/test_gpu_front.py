@@ -217,3 +217,37 @@ def test_front_across_ring_wrap_edges(T, E, k):
             x = torch.randn((T, 64), device="cuda").to(torch.bfloat16)
             b, oi, _ = _front_vs_oracle(lg_np, x, st, ost, it, j, k, prev_d, prev_o, ost.predict)
             prev_d, prev_o = b["idx"], oi
+
+
+@pytest.mark.parametrize("T,E,k,H", [(131149, 16, 2, 64), (200003, 160, 6, 8), (150001, 256, 8, 8),
+                                     (70001, 63, 3, 16)])
+def test_front_many_tiles(T, E, k, H):
+    """Past 512 dispatch tiles (T > 65,536: 128-token tiles, many tiles per
+    route block, every segment of route blocks in use; E dividing the block or
+    not, so both ways of summing the earlier totals run), two layers: bit-identical
+    to the separate calls, and routing, histogram and dispatch against the
+    oracle."""
+    rng = np.random.default_rng([11, T, E])
+    st_a = M.MoEStats(2, E, 3)
+    st_b = M.MoEStats(2, E, 3)
+    prev_a = prev_b = None
+    bias = -1.1 * np.log(np.arange(1, E + 1, dtype=np.float64))
+    for j in range(2):
+        lg_np = (rng.standard_normal((T, E)) + bias[None, :]).astype(np.float32)
+        lg_np[:, ::7] = np.round(lg_np[:, ::7])
+        lg = torch.from_numpy(lg_np).cuda()
+        x = torch.randn((T, H), device="cuda").to(torch.bfloat16)
+        a = _separate(lg, x, st_a, 2, j, k, prev_a, True, True)
+        b = M.moe_layer_front(lg, x, st_b, 2, j, k, idx_prev=prev_b, predict=True, replicate=True)
+        M.moe_check()
+        _compare(a, b, list(a))
+        oi, _ = O.topk_gate(lg_np, k)
+        assert np.array_equal(b["idx"].cpu().numpy(), oi)
+        oh = np.bincount(oi.ravel(), minlength=E)
+        assert np.array_equal(b["hist"].cpu().numpy(), oh)
+        go, perm, inv = O.dispatch(oi, E, b["rep_base"].cpu().numpy())
+        assert np.array_equal(b["group_offsets"].cpu().numpy(), go)
+        assert np.array_equal(b["perm"].cpu().numpy(), perm)
+        assert np.array_equal(b["inv_perm"].cpu().numpy(), inv)
+        prev_a, prev_b = a["idx"], b["idx"]
+    assert st_a.export_state() == st_b.export_state()
