@@ -118,6 +118,7 @@ struct Params {
   int flags;         // bit 0: CTA 0 withholds its first accumulator signal (timeout self-test)
   const int32_t* rep_base;  // [E+1] or null: groups of expert e are rep_base[e]..rep_base[e+1]-1
   int small_threshold;      // experts with fewer rows take the small-batch kernel (0 = none)
+  int b3d;                  // the MN-major weight maps are 3-D (64, rows, N/64): one load per stage and matrix
   // Gathered A operand (GEMM1 only): row i of A is row a_src[i] / a_src_div
   // of the tensor behind tmA (a token of x, a_src = the dispatch permutation,
   // a_src_div = k); null = A is stored in row order.
@@ -847,17 +848,27 @@ __global__ void __launch_bounds__(THREADS, 1)
           } else if (epi_pair_b(EPI)) {
             // first half of the B tile: W1 (gate) columns, second half: the same W3 (up) columns
             const int n0 = t.nt * (BN / 2);
+            if (p.b3d) {
+              tma_load_3d(s.b[stage], &tmB0, &s.full[stage], 0, brow + kb * BK, n0 / 64);
+              tma_load_3d(s.b[stage] + (B_BOXES / 2) * B_BOX_BYTES, &tmB1, &s.full[stage], 0, brow + kb * BK,
+                          n0 / 64);
+            } else {
 #pragma unroll
-            for (int c = 0; c < B_BOXES / 2; ++c) {
-              tma_load_2d(s.b[stage] + c * B_BOX_BYTES, &tmB0, &s.full[stage], n0 + 64 * c, brow + kb * BK);
-              tma_load_2d(s.b[stage] + (c + B_BOXES / 2) * B_BOX_BYTES, &tmB1, &s.full[stage], n0 + 64 * c,
-                          brow + kb * BK);
+              for (int c = 0; c < B_BOXES / 2; ++c) {
+                tma_load_2d(s.b[stage] + c * B_BOX_BYTES, &tmB0, &s.full[stage], n0 + 64 * c, brow + kb * BK);
+                tma_load_2d(s.b[stage] + (c + B_BOXES / 2) * B_BOX_BYTES, &tmB1, &s.full[stage], n0 + 64 * c,
+                            brow + kb * BK);
+              }
             }
           } else {
             const int n0 = t.nt * BN;
+            if (p.b3d) {
+              tma_load_3d(s.b[stage], &tmB0, &s.full[stage], 0, brow + kb * BK, n0 / 64);
+            } else {
 #pragma unroll
-            for (int c = 0; c < B_BOXES; ++c)
-              tma_load_2d(s.b[stage] + c * B_BOX_BYTES, &tmB0, &s.full[stage], n0 + 64 * c, brow + kb * BK);
+              for (int c = 0; c < B_BOXES; ++c)
+                tma_load_2d(s.b[stage] + c * B_BOX_BYTES, &tmB0, &s.full[stage], n0 + 64 * c, brow + kb * BK);
+            }
           }
         }
         __syncwarp();

@@ -248,8 +248,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t fb = full0 + stage * (uint32_t)sizeof(uint64_t);
           if (leader) mbar_arrive_expect_tx(&s.full[stage], 2 * (A_BYTES + B_HALF_BYTES));
           tma_load_2d_pair(s.a[stage], mA, fb, kb * BK, arow);
-          tma_load_2d_pair(s.b[stage], mB, fb, n0, brow + kb * BK);
-          tma_load_2d_pair(s.b[stage] + B_BOX_BYTES, mB, fb, n0 + 64, brow + kb * BK);
+          if (p.b3d) {
+            tma_load_3d_pair(s.b[stage], mB, fb, 0, brow + kb * BK, n0 / 64);
+          } else {
+            tma_load_2d_pair(s.b[stage], mB, fb, n0, brow + kb * BK);
+            tma_load_2d_pair(s.b[stage] + B_BOX_BYTES, mB, fb, n0 + 64, brow + kb * BK);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;

@@ -134,6 +134,24 @@ moe_status encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t o
   return MOE_OK;
 }
 
+// 3-D view of a weight matrix [rows][n] bf16 (n a multiple of 64) for the
+// grouped kernels: dims (64, rows, n/64), strides (n*2, 128) bytes, box
+// (64, 64, chunks), 128-byte swizzle.  One box brings `chunks` adjacent
+// 64-column chunks of 64 rows, laid out in shared memory as `chunks` 2-D
+// boxes of 64 x 64 one after another -- the layout the kernels' descriptors
+// expect -- with one TMA request instead of `chunks`.
+moe_status encode_w3d(CUtensorMap* m, const void* ptr, uint64_t n, uint64_t rows, uint32_t chunks) {
+  cuuint64_t dims[3] = {64, rows, n / 64};
+  cuuint64_t strides[2] = {n * 2, 128};
+  cuuint32_t box[3] = {64, 64, chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", (int)r);
+  return MOE_OK;
+}
+
 // Upper bound on the 256-row blocks of the fused FFN kernel: each unit (at
 // most 2E of them) adds at most one partial block.
 long long ffn_blocks_bound(long long A, int G) { return (A + 255) / 256 + (long long)G + 1; }
@@ -776,9 +794,19 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
         d->fused_attr[fi] = true;
       }
     }
+    // weight tiles: one 3-D box of both 64-column chunks of a CTA's half
+    CUtensorMap mW1q, mW3q, mW2q;
+    if ((ms = encode_w3d(&mW1q, w1, F, (uint64_t)E * H, 2)) != MOE_OK) return ms;
+    if (act == MOE_ACT_SWIGLU) {
+      if ((ms = encode_w3d(&mW3q, w3, F, (uint64_t)E * H, 2)) != MOE_OK) return ms;
+    } else {
+      mW3q = mW1q;
+    }
+    if ((ms = encode_w3d(&mW2q, w2, H, (uint64_t)E * F, 2)) != MOE_OK) return ms;
     ffn3::FusedParams fp;
     fp.p1 = p1;
     fp.p2 = p2;
+    fp.p1.b3d = fp.p2.b3d = 1;
     fp.p1.n_tiles = act == MOE_ACT_SWIGLU ? (F + ffn2::BN / 2 - 1) / (ffn2::BN / 2) : (F + ffn2::BN - 1) / ffn2::BN;
     fp.p2.n_tiles = (H + ffn2::BN - 1) / ffn2::BN;
     const long long blocks = ffn_blocks_bound(A, G);
@@ -795,8 +823,8 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
     if (e != cudaSuccess) return cuda_at(who, e, "cudaMemsetAsync (block counters)");
     if (cudaError_t fe = fork(); fe != cudaSuccess) return cuda_at(who, fe, "fork of the small-batch chain");
     cudaError_t le = launch_pdl(fi ? ffn3::ffn_fused_kernel<ffn::kSwiglu> : ffn3::ffn_fused_kernel<ffn::kGelu>,
-                                dim3((unsigned)(2 * pairs)), dim3(ffn2::THREADS), ffn2::kSmemBytes, st, mA1, mW1, mW3,
-                                mA2, mW2, fp);
+                                dim3((unsigned)(2 * pairs)), dim3(ffn2::THREADS), ffn2::kSmemBytes, st, mA1, mW1q, mW3q,
+                                mA2, mW2q, fp);
     return finish(le, "fused FFN launch");
   }
 
@@ -832,6 +860,15 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
     }
     p1.n_tiles = act == MOE_ACT_SWIGLU ? (F + ffn2::BN / 2 - 1) / (ffn2::BN / 2) : (F + ffn2::BN - 1) / ffn2::BN;
     p2.n_tiles = (H + ffn2::BN - 1) / ffn2::BN;
+    CUtensorMap mW1q, mW3q, mW2q;
+    if ((ms = encode_w3d(&mW1q, w1, F, (uint64_t)E * H, 2)) != MOE_OK) return ms;
+    if (act == MOE_ACT_SWIGLU) {
+      if ((ms = encode_w3d(&mW3q, w3, F, (uint64_t)E * H, 2)) != MOE_OK) return ms;
+    } else {
+      mW3q = mW1q;
+    }
+    if ((ms = encode_w3d(&mW2q, w2, H, (uint64_t)E * F, 2)) != MOE_OK) return ms;
+    p1.b3d = p2.b3d = 1;
     const long long pt_bound = (long long)(A + ffn2::BMP - 1) / ffn2::BMP + G;
     auto grid_for = [&](const ffn::Params& p, int inst) {
       long long pairs = pt_bound * p.n_tiles;
@@ -842,10 +879,10 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
     cudaError_t e = launch_pdl(epi1 == ffn::kSwiglu ? ffn2::gemm_pair_kernel<ffn::kSwiglu>
                                                     : ffn2::gemm_pair_kernel<ffn::kGelu>,
                                dim3(grid_for(p1, epi1 == ffn::kSwiglu ? 1 : 0)), dim3(ffn2::THREADS),
-                               ffn2::kSmemBytes, st, mA1, mW1, mW3, p1);
+                               ffn2::kSmemBytes, st, mA1, mW1q, mW3q, p1);
     if (e != cudaSuccess) return finish(e, "GEMM1 (pair) launch");
     e = launch_pdl(comb ? ffn2::gemm_pair_kernel<ffn::kCombine> : ffn2::gemm_pair_kernel<ffn::kStore>,
-                   dim3(grid_for(p2, comb ? 3 : 2)), dim3(ffn2::THREADS), ffn2::kSmemBytes, st, mA2, mW2, mW2, p2);
+                   dim3(grid_for(p2, comb ? 3 : 2)), dim3(ffn2::THREADS), ffn2::kSmemBytes, st, mA2, mW2q, mW2q, p2);
     return finish(e, "GEMM2 (pair) launch");
   }
 
@@ -864,6 +901,17 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   }
   p1.n_tiles = act == MOE_ACT_SWIGLU ? (F + ffn::BN / 2 - 1) / (ffn::BN / 2) : (F + ffn::BN - 1) / ffn::BN;
   p2.n_tiles = (H + ffn::BN - 1) / ffn::BN;
+  // weight tiles: one 3-D box per matrix and stage (four chunks, or two of
+  // each of W1 and W3)
+  CUtensorMap mW1q, mW3q, mW2q;
+  if ((ms = encode_w3d(&mW1q, w1, F, (uint64_t)E * H, act == MOE_ACT_SWIGLU ? 2 : 4)) != MOE_OK) return ms;
+  if (act == MOE_ACT_SWIGLU) {
+    if ((ms = encode_w3d(&mW3q, w3, F, (uint64_t)E * H, 2)) != MOE_OK) return ms;
+  } else {
+    mW3q = mW1q;
+  }
+  if ((ms = encode_w3d(&mW2q, w2, H, (uint64_t)E * F, 4)) != MOE_OK) return ms;
+  p1.b3d = p2.b3d = 1;
   const long long mt_bound = (long long)(A + ffn::BM - 1) / ffn::BM + G;
   auto grid_for = [&](const ffn::Params& p) {
     long long g = mt_bound * p.n_tiles;
@@ -872,15 +920,15 @@ moe_status expert_ffn(const char* who, const uint16_t* a, const int32_t* a_src, 
   };
   if (cudaError_t fe = fork(); fe != cudaSuccess) return cuda_at(who, fe, "fork of the small-batch chain");
   if (epi1 == ffn::kSwiglu)
-    ffn::gemm_kernel<ffn::kSwiglu><<<grid_for(p1), ffn::THREADS, ffn::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
+    ffn::gemm_kernel<ffn::kSwiglu><<<grid_for(p1), ffn::THREADS, ffn::kSmemBytes, st>>>(mA1, mW1q, mW3q, p1);
   else
-    ffn::gemm_kernel<ffn::kGelu><<<grid_for(p1), ffn::THREADS, ffn::kSmemBytes, st>>>(mA1, mW1, mW3, p1);
+    ffn::gemm_kernel<ffn::kGelu><<<grid_for(p1), ffn::THREADS, ffn::kSmemBytes, st>>>(mA1, mW1q, mW3q, p1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return finish(e, "GEMM1 launch");
   if (comb)
-    ffn::gemm_kernel<ffn::kCombine><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
+    ffn::gemm_kernel<ffn::kCombine><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2q, mW2q, p2);
   else
-    ffn::gemm_kernel<ffn::kStore><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2, mW2, p2);
+    ffn::gemm_kernel<ffn::kStore><<<grid_for(p2), ffn::THREADS, ffn::kSmemBytes, st>>>(mA2, mW2q, mW2q, p2);
   return finish(cudaGetLastError(), "GEMM2 launch");
 }
 
