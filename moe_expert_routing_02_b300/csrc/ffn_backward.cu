@@ -142,12 +142,10 @@ moe_status moe_ffn_backward(const uint16_t* x, const uint16_t* dout, const float
   const long long P = L.P;
 
   // ---- tensor maps
-  CUtensorMap mDy, mW2k, mXp, mW1, mW3, mDz, mW1k, mW3k;
+  CUtensorMap mDy, mW2k, mXp, mDz, mW1k, mW3k;
   if ((ms = encode_2d(&mDy, dy, H, P, 64, ffn::BM)) != MOE_OK) return ms;
   if ((ms = encode_2d(&mW2k, w2, H, (uint64_t)E * F, 64, ffn::BN)) != MOE_OK) return ms;
   if ((ms = encode_2d(&mXp, xp, H, P, 64, ffn::BM)) != MOE_OK) return ms;
-  if ((ms = encode_2d(&mW1, w1, F, (uint64_t)E * H, 64, 64)) != MOE_OK) return ms;
-  if ((ms = encode_2d(&mW3, swiglu ? w3 : w1, F, (uint64_t)E * H, 64, 64)) != MOE_OK) return ms;
   if ((ms = encode_2d(&mDz, dz, KZ, P, 64, ffn::BM)) != MOE_OK) return ms;
   if ((ms = encode_2d(&mW1k, w1, F, (uint64_t)E * H, 64, ffn::BN)) != MOE_OK) return ms;
   if ((ms = encode_2d(&mW3k, swiglu ? w3 : w1, F, (uint64_t)E * H, 64, ffn::BN)) != MOE_OK) return ms;
@@ -192,10 +190,15 @@ moe_status moe_ffn_backward(const uint16_t* x, const uint16_t* dout, const float
   p4.n_tiles = swiglu ? (F + ffn::BN / 2 - 1) / (ffn::BN / 2) : (F + ffn::BN - 1) / ffn::BN;
   p4.out = av;
   p4.out2 = dz;
+  // the weight tiles as one 3-D box per matrix and stage, as in the forward
+  CUtensorMap mW1q, mW3q;
+  if ((ms = encode_w3d(&mW1q, w1, F, (uint64_t)E * H, swiglu ? 2 : 4)) != MOE_OK) return ms;
+  if ((ms = encode_w3d(&mW3q, swiglu ? w3 : w1, F, (uint64_t)E * H, swiglu ? 2 : 4)) != MOE_OK) return ms;
+  p4.b3d = 1;
   if (swiglu)
-    ffn::gemm_kernel<ffn::kBwdSwiglu><<<grid_for(p4), ffn::THREADS, ffn::kSmemBytes, st>>>(mXp, mW1, mW3, p4);
+    ffn::gemm_kernel<ffn::kBwdSwiglu><<<grid_for(p4), ffn::THREADS, ffn::kSmemBytes, st>>>(mXp, mW1q, mW3q, p4);
   else
-    ffn::gemm_kernel<ffn::kBwdGelu><<<grid_for(p4), ffn::THREADS, ffn::kSmemBytes, st>>>(mXp, mW1, mW3, p4);
+    ffn::gemm_kernel<ffn::kBwdGelu><<<grid_for(p4), ffn::THREADS, ffn::kSmemBytes, st>>>(mXp, mW1q, mW3q, p4);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_at(who, e, "recompute launch");
 
   ffn::Params p3 = pb;  // dA = dY W2^T (K = H, N = F) times the factors, in place
