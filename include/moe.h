@@ -590,6 +590,16 @@ moe_status moe_dispatch_noalloc(const uint16_t* x, const int32_t* idx, int T, in
  *                     CTA-pair kernels), the grouped kernels the rest.
  *     The outputs are the same within the FFN tolerance whichever path an
  *     expert takes (bit-identical for the experts on the grouped kernels).
+ *   MOE_OPT_FRONT_ONE_LAUNCH  0 (default): moe_layer_front makes two
+ *     launches (route/count, then plan, statistics, ranks and copy).  1: it
+ *     runs as one cooperative launch when all of its blocks (one per
+ *     dispatch tile, plus one) can be resident on the device at once: each
+ *     block routes its own tile, the blocks meet at a grid-wide barrier (a
+ *     bounded wait: after ~2 s moe_check reports MOE_ERR_TIMEOUT and the
+ *     call's outputs are not to be used), then the dispatch runs as in the
+ *     two-launch form; other sizes take the two launches.  The outputs are
+ *     bit-identical either way; on B300 the one launch measured slower on
+ *     the 16K-token layer and no faster on the others.
  * Unknown options or values return MOE_ERR_INVALID.  Options are process-wide
  * and stored atomically; a call reads each one once when it is made, so a
  * set from another thread applies to the calls that start after it returns
@@ -599,7 +609,8 @@ typedef enum {
     MOE_OPT_FFN_KERNEL = 1,
     MOE_OPT_FFN_TIMEOUT_SELFTEST = 2,
     MOE_OPT_PDL = 3,
-    MOE_OPT_FFN_SMALL_SMS = 4
+    MOE_OPT_FFN_SMALL_SMS = 4,
+    MOE_OPT_FRONT_ONE_LAUNCH = 5
 } moe_option;
 typedef enum {
     MOE_FFN_KERNEL_AUTO = 0,
@@ -616,6 +627,14 @@ moe_status moe_get_option(int option, int* value /* host */);
  * MOE_OPT_FFN_SMALL_SMS is not 0.
  * 0 for sizes, activations or thresholds the FFN refuses.  Host only. */
 int moe_ffn_launches(int A, int E, int H, int F, int act, int small_group_threshold, int gather);
+
+/* Kernel launches one moe_layer_front call with T > 0 tokens makes on the
+ * current device under the current options: 1 when it runs as one
+ * cooperative launch (MOE_OPT_FRONT_ONE_LAUNCH on, and all of its blocks can
+ * be resident at once), else 2.  has_prev: the call passes the previous
+ * layer's choices (co-selection counts kept).  0 for refused sizes or when no
+ * device can be queried.  Host only (queries the device's occupancy). */
+int moe_layer_front_launches(int T, int E, int k, int has_prev);
 
 /* Workspace bytes for op (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT or
  * MOE_OP_EXPERT_FFN_COMBINE); 0 for bad sizes. */

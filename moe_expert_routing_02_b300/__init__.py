@@ -30,11 +30,11 @@ __all__ = [
     "moe_ffn_backward", "moe_ffn_backward_workspace_bytes", "moe_route_backward",
     "MOE_BWD_ACCUMULATE_WGRAD", "MOE_BWD_WGRAD_BF16",
     # sizes, options, constants
-    "workspace_bytes", "moe_ffn_launches", "moe_set_option", "moe_get_option",
+    "workspace_bytes", "moe_ffn_launches", "moe_layer_front_launches", "moe_set_option", "moe_get_option",
     "MOE_OP_DISPATCH", "MOE_OP_EXPERT_FFN", "MOE_OP_LAYER_FRONT", "MOE_OP_EXPERT_FFN_COMBINE",
     "MOE_ACT_GELU", "MOE_ACT_SWIGLU", "MOE_OPT_FFN_KERNEL", "MOE_FFN_KERNEL_AUTO", "MOE_FFN_KERNEL_SINGLE",
     "MOE_FFN_KERNEL_PAIR", "MOE_FFN_KERNEL_FUSED", "MOE_OPT_FFN_TIMEOUT_SELFTEST", "MOE_OPT_PDL",
-    "MOE_OPT_FFN_SMALL_SMS",
+    "MOE_OPT_FFN_SMALL_SMS", "MOE_OPT_FRONT_ONE_LAUNCH",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -44,6 +44,7 @@ MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE
 MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
 MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT, MOE_OP_EXPERT_FFN_COMBINE = 1, 2, 3, 4
 MOE_OPT_FFN_KERNEL, MOE_OPT_FFN_TIMEOUT_SELFTEST, MOE_OPT_PDL, MOE_OPT_FFN_SMALL_SMS = 1, 2, 3, 4
+MOE_OPT_FRONT_ONE_LAUNCH = 5
 MOE_FFN_KERNEL_AUTO, MOE_FFN_KERNEL_SINGLE, MOE_FFN_KERNEL_PAIR, MOE_FFN_KERNEL_FUSED = 0, 1, 2, 3
 
 _P = ctypes.c_void_p
@@ -65,6 +66,7 @@ _SIGS = {
     "moe_replicate_weights": (_I, [_P, _I, _P, _I, _I, _P, _P]),
     "moe_expert_ffn_slots": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_ffn_launches": (_I, [_I, _I, _I, _I, _I, _I, _I]),
+    "moe_layer_front_launches": (_I, [_I, _I, _I, _I]),
     "moe_predict_decay": (_I, [_P, _I, ctypes.c_int64, ctypes.c_double, _P, _P, _P, _P]),
     "moe_replicate_predicted": (_I, [_P, _I, ctypes.c_int64, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_expert_ffn_gather": (_I, [_P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
@@ -648,6 +650,12 @@ def moe_ffn_launches(A: int, E: int, H: int, F: int, act: str = "gelu", small_gr
     act_id = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU}[act]
     return int(lib().moe_ffn_launches(int(A), int(E), int(H), int(F), act_id, int(small_group_threshold),
                                       int(bool(gather))))
+
+
+def moe_layer_front_launches(T: int, E: int, k: int, has_prev: bool = True) -> int:
+    """Kernel launches of one moe_layer_front call (T > 0) on the current
+    device under the current options: 1 (one cooperative launch) or 2."""
+    return int(lib().moe_layer_front_launches(int(T), int(E), int(k), int(bool(has_prev))))
 
 
 MOE_BWD_ACCUMULATE_WGRAD = 1

@@ -70,6 +70,12 @@ constexpr int kSegBlocks = 8;
 constexpr int kSegments = kMaxRouteBlocks / kSegBlocks;
 // Those totals are loaded kPreLoads per thread at once (more in a loop).
 constexpr int kPreLoads = 8;
+// The one-launch front (front_coop_kernel) groups tiles in segments of
+// kSegTiles; the statistics handle keeps kSegSlots segment rows, enough for
+// both forms (the one-launch front runs at most kSegTiles * kSegSlots tiles).
+constexpr int kSegTiles = 32;
+constexpr int kSegSlots = 32;
+static_assert(kSegSlots >= kSegments, "segment rows of the two-launch front");
 // Workspace: tile prefixes [ntiles][E], block totals [<= ntiles][E] (the
 // size keeps room for [4][E] more words).
 __host__ inline size_t workspace_bytes(long long T, int E) {
@@ -88,8 +94,9 @@ struct Args {
   const int32_t* idx_prev;
   uint32_t* acc_h;   // [E] histogram accumulator (zero between calls)
   uint32_t* acc_c;   // [E*E] co-selection accumulator (zero between calls)
-  uint32_t* seg_tot; // [kSegments][E] route-block totals per segment (zero between calls)
+  uint32_t* seg_tot; // [kSegSlots][E] totals per segment of route blocks or tiles (zero between calls)
   uint32_t* ticket;  // F2 blocks that left (zero between calls)
+  uint32_t* arrive;  // blocks past the routing of the one-launch front (zero between calls)
   uint32_t* ring_h;
   unsigned long long* hsum;
   uint32_t* ring_c;
@@ -228,6 +235,11 @@ __global__ void __launch_bounds__(kThreads) route_count_kernel(Args a) {
       if (cs[i]) atomicAdd(a.acc_c + i, cs[i]);
 }
 
+// Offset of scatter_body's slot_s in its dynamic shared memory, in int32
+// words (histogram, bases, groups, group bases, copies, group experts, loads,
+// per-warp counts, running counts before it).
+__host__ __device__ inline int scatter_slot_offset(int E) { return 9 * E + 1 + kWarps * E; }
+
 // Dynamic shared memory of scatter_copy_kernel, in int32 words.
 __host__ __device__ inline int scatter_smem_words(int E, int TT, int k) {
   return (16 + kWarps) * E + 1 + TT * k + kThreads;
@@ -283,9 +295,19 @@ __device__ __forceinline__ void leave_block(const Args& a, unsigned ticket) {
   __syncthreads();
   if (last_s) {
     for (int i = threadIdx.x; i < a.E; i += kThreads) a.acc_h[i] = 0u;
-    for (int i = threadIdx.x; i < kSegments * a.E; i += kThreads) a.seg_tot[i] = 0u;
-    if (threadIdx.x == 0) *a.ticket = 0u;
+    for (int i = threadIdx.x; i < kSegSlots * a.E; i += kThreads) a.seg_tot[i] = 0u;
+    if (threadIdx.x == 0) {
+      *a.ticket = 0u;
+      *a.arrive = 0u;
+    }
   }
+}
+
+// A load of a word another block may have written: through L2 (ld.cg) in the
+// one-launch front, where the writer ran in the same launch.
+template <bool THROUGH_L2>
+__device__ __forceinline__ uint32_t ld_front(const uint32_t* p) {
+  return THROUGH_L2 ? __ldcg(p) : *p;
 }
 
 // Shared-memory arrays of the plan in scatter_copy_kernel.
@@ -369,17 +391,16 @@ __device__ __noinline__ void write_tables(const Args& a, const Plan& pl, long lo
 // kernel: x is the layer's input, complete before the route kernel of this
 // call passed its own wait (and this kernel starts only after every route
 // block has passed it), so the read may overlap everything that follows.
-__global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, const uint16_t* __restrict__ x, int H,
-                                                                uint16_t* __restrict__ xp,
-                                                                int32_t* __restrict__ perm,
-                                                                int32_t* __restrict__ inv_perm, int prefetch) {
-  extern __shared__ int32_t sm[];
-  if (prefetch && blockIdx.x > 0 && threadIdx.x == 0) {
-    const long long t0 = (long long)(blockIdx.x - 1) * a.TT;
-    const long long nt = a.T - t0 < a.TT ? a.T - t0 : a.TT;
-    sm100::bulk_prefetch_l2(x + t0 * H, (uint32_t)(nt * H * 2));
-  }
-  pdl_wait();
+// The part of F2 after its wait (see scatter_copy_kernel), shared with the
+// one-launch front (front_coop_kernel).  COOP: the tile's assignments were
+// routed by this block (their experts are in slot_s), the starting ranks come
+// from the totals of the tile segments before the tile's and of the tiles
+// before it in its segment, and everything other blocks wrote in this launch
+// is read through L2.
+template <bool COOP>
+__device__ __forceinline__ void scatter_body(const Args& a, const uint16_t* __restrict__ x, int H,
+                                             uint16_t* __restrict__ xp, int32_t* __restrict__ perm,
+                                             int32_t* __restrict__ inv_perm, int32_t* sm) {
   const int E = a.E, k = a.k;
   int32_t* hist_s = sm;                   // [E]
   int32_t* base_s = hist_s + E;           // [E]   first slot of the expert's rows
@@ -390,7 +411,7 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, co
   int32_t* load_s = ge_s + 2 * E;         // [E]   loads apportioned from the shares
   int32_t* warp_cnt = load_s + E;         // [kWarps][E]
   int32_t* run = warp_cnt + kWarps * E;   // [E]
-  int32_t* slot_s = run + E;              // [TT*k]
+  int32_t* slot_s = sm + scatter_slot_offset(E);  // [TT*k], right after run
   int32_t* part_s = slot_s + a.TT * k;    // [kThreads] partial sums
   const Plan pl{hist_s, base_s, n_s, rb_s, copies_s, ge_s, load_s};
   __shared__ int32_t wtot[kWarps];
@@ -405,22 +426,36 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, co
   // Every load that does not depend on another is issued here at once: the
   // histogram, the tile's prefix within its route block, the totals of the
   // segments and route blocks before it, and the tile's first expert ids.
-  const int rblk = tile >= 0 ? tile / a.tiles_per_block : 0;
-  const int sg = rblk / kSegBlocks;
-  const int nseg = sg * E;                        // segment totals before the tile's segment
-  const int npre = nseg + (rblk - sg * kSegBlocks) * E;  // ... plus its route blocks before the tile's
-  const int32_t* blk_seg = a.blk_tot + (size_t)sg * kSegBlocks * E;
+  // (COOP: segments of kSegTiles tiles, then the tiles before this one in
+  // its segment, whose counts are in `counts`; otherwise segments of route
+  // blocks, then the route blocks before the tile's, plus the tile's prefix
+  // within its route block)
+  int nseg, npre;
+  const int32_t* blk_seg;
+  if (COOP) {
+    const int sg = tile >= 0 ? tile / kSegTiles : 0;
+    nseg = sg * E;
+    npre = nseg + (tile >= 0 ? tile - sg * kSegTiles : 0) * E;
+    blk_seg = a.counts + (size_t)sg * kSegTiles * E;
+  } else {
+    const int rblk = tile >= 0 ? tile / a.tiles_per_block : 0;
+    const int sg = rblk / kSegBlocks;
+    nseg = sg * E;
+    npre = nseg + (rblk - sg * kSegBlocks) * E;
+    blk_seg = a.blk_tot + (size_t)sg * kSegBlocks * E;
+  }
   int hv = 0, cv = 0, ex0 = -1;
   int pv[kPreLoads];
-  if (tid < E) hv = (int32_t)a.acc_h[tid];
+  if (tid < E) hv = (int32_t)ld_front<COOP>(a.acc_h + tid);
   if (tile >= 0) {
-    if (tid < E) cv = a.counts[(size_t)tile * E + tid];
+    if (!COOP && tid < E) cv = a.counts[(size_t)tile * E + tid];
 #pragma unroll
     for (int u = 0; u < kPreLoads; ++u) {
       const int i = tid + u * kThreads;
-      pv[u] = i < nseg ? (int32_t)a.seg_tot[i] : i < npre ? blk_seg[i - nseg] : 0;
+      pv[u] = i < nseg ? (int32_t)ld_front<COOP>(a.seg_tot + i)
+                       : i < npre ? (int32_t)ld_front<COOP>(reinterpret_cast<const uint32_t*>(blk_seg) + i - nseg) : 0;
     }
-    if (tid < nA) ex0 = a.idx[f0 + tid];
+    if (tid < nA) ex0 = COOP ? slot_s[tid] : a.idx[f0 + tid];
   }
   if (tid < E) {
     hist_s[tid] = hv;
@@ -447,7 +482,9 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, co
 #pragma unroll
       for (int u = 0; u < kPreLoads; ++u) {
         const int i = i0 + u * kThreads;
-        acc += i < nseg ? (int32_t)a.seg_tot[i] : i < npre ? blk_seg[i - nseg] : 0;
+        acc += i < nseg ? (int32_t)ld_front<COOP>(a.seg_tot + i)
+                        : i < npre ? (int32_t)ld_front<COOP>(reinterpret_cast<const uint32_t*>(blk_seg) + i - nseg)
+                                   : 0;
       }
     }
     if (E < 32) {
@@ -471,7 +508,9 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, co
 #pragma unroll
       for (int u = 0; u < kPreLoads; ++u) {
         const int i = i0 + u * kThreads;
-        pv[u] = i < nseg ? (int32_t)a.seg_tot[i] : i < npre ? blk_seg[i - nseg] : 0;
+        pv[u] = i < nseg ? (int32_t)ld_front<COOP>(a.seg_tot + i)
+                         : i < npre ? (int32_t)ld_front<COOP>(reinterpret_cast<const uint32_t*>(blk_seg) + i - nseg)
+                                    : 0;
       }
 #pragma unroll
       for (int u = 0; u < kPreLoads; ++u)
@@ -556,7 +595,7 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, co
     const int i = r0 + tid;
     int ex = -1;
     if (i < nA) {
-      ex = r0 == 0 ? ex0 : a.idx[f0 + i];
+      ex = r0 == 0 ? ex0 : COOP ? slot_s[i] : a.idx[f0 + i];
       if ((unsigned)ex >= (unsigned)E) ex = -1;
     }
     const unsigned peers = __match_any_sync(0xffffffffu, ex);
@@ -592,6 +631,20 @@ __global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, co
   leave_block(a, ticket);
 }
 
+__global__ void __launch_bounds__(kThreads) scatter_copy_kernel(const Args a, const uint16_t* __restrict__ x, int H,
+                                                                uint16_t* __restrict__ xp,
+                                                                int32_t* __restrict__ perm,
+                                                                int32_t* __restrict__ inv_perm, int prefetch) {
+  extern __shared__ int32_t sm[];
+  if (prefetch && blockIdx.x > 0 && threadIdx.x == 0) {
+    const long long t0 = (long long)(blockIdx.x - 1) * a.TT;
+    const long long nt = a.T - t0 < a.TT ? a.T - t0 : a.TT;
+    sm100::bulk_prefetch_l2(x + t0 * H, (uint32_t)(nt * H * 2));
+  }
+  pdl_wait();
+  scatter_body<false>(a, x, H, xp, perm, inv_perm, sm);
+}
+
 // Dynamic shared memory of route_count_kernel stays below 17 KB (tile counts
 // plus, for E <= 64, the E*E co-selection bins); that of scatter_copy_kernel
 // below 29 KB (E = 256, 128-token tiles of top-8), which with the static
@@ -610,6 +663,176 @@ static cudaError_t ensure_smem_attr(K kernel, bool* done_per_device, int bytes) 
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) done_per_device[dev] = true;
   return e;
+}
+
+// ---------------------------------------------------------------- one launch
+// The front in one cooperative launch (every block resident): each tile block
+// routes its own TT tokens (the same per-token work as route_count_kernel),
+// keeps their experts in shared memory, publishes its tile counts (to
+// `counts`, the histogram accumulator and its tile segment's totals) and its
+// co-selection pairs, then all blocks meet at a grid-wide barrier; after it,
+// scatter_body<true> runs the dispatch as scatter_copy_kernel does, without a
+// second launch and without reloading the tile's experts.
+
+// Route the tile's tokens [t0, t0 + nt); counts into cnt_s, the experts of
+// assignment f = (t - t0) * k + r into ex_s[f], co-selection pairs into cs_s
+// (cos_smem) or the accumulator.
+template <int G, bool VEC>
+__device__ __forceinline__ void route_tile(const Args& a, long long t0, int nt, int32_t* cnt_s, uint32_t* cs_s,
+                                           bool cos_smem, int32_t* ex_s) {
+  constexpr int TPW = 32 / G;
+  const int E = a.E, k = a.k;
+  const bool cos = a.has_prev != 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gl = lane % G;
+  bool bad = false;
+  for (int tt0 = warp * TPW; tt0 < nt; tt0 += kWarps * TPW) {
+    const int tt = tt0 + lane / G;
+    const bool live = tt < nt;
+    const long long t = t0 + tt;
+    int pe[8];
+#pragma unroll
+    for (int r1 = 0; r1 < 8; ++r1) pe[r1] = (cos && live && gl == 0 && r1 < k) ? a.idx_prev[t * k + r1] : 0;
+    float sel_v[8], denom;
+    int sel_i[8];
+    route::topk_token<G, VEC>(a.logits + (size_t)(live ? t : 0) * E, live, E, k, a.renorm, sel_v, sel_i, &denom);
+    if (live) {
+      route::write_token<G>(t, k, sel_v, sel_i, denom, a.idx, a.w);
+      if (gl == 0) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (r < k) {
+            atomicAdd(cnt_s + sel_i[r], 1);
+            ex_s[tt * k + r] = sel_i[r];
+          }
+        }
+        if (cos) {
+#pragma unroll
+          for (int r1 = 0; r1 < 8; ++r1) {
+            if (r1 < k) {
+              if ((unsigned)pe[r1] >= (unsigned)E) {
+                bad = true;
+                continue;
+              }
+#pragma unroll
+              for (int r2 = 0; r2 < 8; ++r2) {
+                if (r2 < k) {
+                  const int bin = pe[r1] * E + sel_i[r2];
+                  if (cos_smem)
+                    atomicAdd(cs_s + bin, 1u);
+                  else
+                    atomicAdd(a.acc_c + bin, 1u);
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  if (bad) moe_flag_error(MOE_DEVERR_DATA);
+}
+
+// Grid-wide barrier of the one-launch front: thread 0 of each block makes the
+// block's writes visible, arrives, and polls the count with a bounded wait
+// (~2 s, then the device timeout bit; the block goes on and the call's
+// results are not to be used).
+__device__ __forceinline__ void grid_barrier(const Args& a) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(a.arrive, 1u);
+    const uint64_t start = sm100::globaltimer_ns();
+    for (uint32_t i = 0; i < (1u << 28); ++i) {
+      uint32_t v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.arrive) : "memory");
+      if (v >= gridDim.x) break;
+      if ((i & 63) == 63 && sm100::globaltimer_ns() - start > 2000000000ull) {
+        moe_flag_error(MOE_DEVERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+// Dynamic shared memory of front_coop_kernel, in int32 words: scatter_body's,
+// then the tile counts [E] and, for E <= kSmemCoselMaxE, the co-selection
+// bins [E*E].
+__host__ __device__ inline int coop_smem_words(int E, int TT, int k, bool cos_smem) {
+  return scatter_smem_words(E, TT, k) + E + (cos_smem ? E * E : 0);
+}
+
+template <int G, bool VEC>
+__global__ void __launch_bounds__(kThreads, 4) front_coop_kernel(const Args a, const uint16_t* __restrict__ x, int H,
+                                                                 uint16_t* __restrict__ xp,
+                                                                 int32_t* __restrict__ perm,
+                                                                 int32_t* __restrict__ inv_perm, int prefetch) {
+  extern __shared__ int32_t sm[];
+  pdl_wait();
+  const int E = a.E, k = a.k, tid = threadIdx.x;
+  const int tile = (int)blockIdx.x - 1;
+  const bool cos_smem = a.has_prev != 0 && E <= kSmemCoselMaxE;
+  int32_t* ex_s = sm + scatter_slot_offset(E);  // scatter_body's slot_s: the tile's experts until its ranks
+  int32_t* cnt_s = sm + scatter_smem_words(E, a.TT, k);
+  uint32_t* cs_s = reinterpret_cast<uint32_t*>(cnt_s + E);
+  if (tile >= 0) {
+    const long long t0 = (long long)tile * a.TT;
+    const int nt = (int)(a.T - t0 < a.TT ? a.T - t0 : a.TT);
+    if (prefetch && tid == 0) sm100::bulk_prefetch_l2(x + t0 * H, (uint32_t)((long long)nt * H * 2));
+    for (int i = tid; i < E + (cos_smem ? E * E : 0); i += kThreads) cnt_s[i] = 0;
+    __syncthreads();
+    route_tile<G, VEC>(a, t0, nt, cnt_s, cs_s, cos_smem, ex_s);
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) {
+      const int c = cnt_s[e];
+      a.counts[(size_t)tile * E + e] = c;
+      if (c) {
+        atomicAdd(a.acc_h + e, (uint32_t)c);
+        atomicAdd(a.seg_tot + (size_t)(tile / kSegTiles) * E + e, (uint32_t)c);
+      }
+    }
+    if (cos_smem)
+      for (int i = tid; i < E * E; i += kThreads)
+        if (cs_s[i]) atomicAdd(a.acc_c + i, cs_s[i]);
+  }
+  grid_barrier(a);
+  scatter_body<true>(a, x, H, xp, perm, inv_perm, sm);
+}
+
+// Host side of the one-launch front: blocks per SM of the instance at this
+// shared-memory size (0 if it cannot be resident), cached per device.
+template <int G, bool VEC>
+static cudaError_t launch_coop_g(const Args& a, const uint16_t* x, int H, uint16_t* xp, int32_t* perm,
+                                 int32_t* inv_perm, int prefetch, int num_sms, bool* launched, cudaStream_t st) {
+  *launched = false;
+  static bool done[64] = {};
+  const bool cos_smem = a.has_prev != 0 && a.E <= kSmemCoselMaxE;
+  const size_t smem = sizeof(int32_t) * (size_t)coop_smem_words(a.E, a.TT, a.k, cos_smem);
+  if (smem > (size_t)kScatterDynSmemMax) return cudaSuccess;
+  cudaError_t e = ensure_smem_attr(front_coop_kernel<G, VEC>, done, kScatterDynSmemMax);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, front_coop_kernel<G, VEC>, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if ((long long)per_sm * num_sms < a.ntiles + 1) return cudaSuccess;  // not all resident: two launches
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.ntiles + 1));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = g_moe_pdl.load(std::memory_order_relaxed) ? 2 : 1;
+  e = cudaLaunchKernelEx(&cfg, front_coop_kernel<G, VEC>, a, x, H, xp, perm, inv_perm, prefetch);
+  if (e != cudaSuccess) return e;
+  *launched = true;
+  return cudaGetLastError();
 }
 
 // Tiles per route block: every warp gets at least one pass of tokens, and
@@ -647,17 +870,45 @@ static cudaError_t launch_route_g(const Args& a, bool vec, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Process-wide choice of the front's form (moe_set_option(MOE_OPT_FRONT_ONE_LAUNCH)).
+// Off by default: on the moe_gpt_stream layer the one launch measured slower
+// (per-block stamps: routing in 513 blocks done at 6.1-7.4 us against 4.2 us
+// in 128 route blocks -- 4x the co-selection flushes onto the same bins --
+// and 2.5-3 us in the grid-wide barrier; last copy done at 29.7 against
+// 23.8 us), and no faster on the single-layer workloads.
+inline std::atomic<int> g_front_one_launch{0};
+
 static cudaError_t launch(const Args& a0, const uint16_t* x, int H, uint16_t* xp, int32_t* perm, int32_t* inv_perm,
-                          cudaStream_t st) {
+                          int num_sms, cudaStream_t st) {
   Args a = a0;
   a.tiles_per_block = route_tiles_per_block(a.T, a.E);
   // Short token rows: the scatter/copy blocks start while the route blocks
   // run and ask L2 for their rows first (measured better than the route
   // blocks prefetching them, which slowed the routing itself).
   const int prefetch = (x != nullptr && a.ntiles > 0 && (long long)a.TT * H * 2 <= kPrefetchMaxBytes) ? 1 : 0;
-  a.release_early = prefetch;
   const bool vec = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.logits) & 15) == 0);
   cudaError_t e;
+  if (g_front_one_launch.load(std::memory_order_relaxed) && a.ntiles > 0 &&
+      a.ntiles <= (long long)kSegTiles * kSegSlots) {
+    a.release_early = 0;
+    bool launched = false;
+    if (a.E <= 8) e = vec ? launch_coop_g<1, true>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st)
+                          : launch_coop_g<1, false>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st);
+    else if (a.E <= 16) e = vec ? launch_coop_g<2, true>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st)
+                                : launch_coop_g<2, false>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st);
+    else if (a.E <= 32) e = vec ? launch_coop_g<4, true>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st)
+                                : launch_coop_g<4, false>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st);
+    else if (a.E <= 64) e = vec ? launch_coop_g<8, true>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st)
+                                : launch_coop_g<8, false>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st);
+    else if (a.E <= 128)
+      e = vec ? launch_coop_g<16, true>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st)
+              : launch_coop_g<16, false>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st);
+    else
+      e = vec ? launch_coop_g<32, true>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st)
+              : launch_coop_g<32, false>(a, x, H, xp, perm, inv_perm, prefetch, num_sms, &launched, st);
+    if (e != cudaSuccess || launched) return e;
+  }
+  a.release_early = prefetch;
   if (a.E <= 8) e = launch_route_g<1>(a, vec, st);
   else if (a.E <= 16) e = launch_route_g<2>(a, vec, st);
   else if (a.E <= 32) e = launch_route_g<4>(a, vec, st);
@@ -673,6 +924,29 @@ static cudaError_t launch(const Args& a0, const uint16_t* x, int H, uint16_t* xp
                  inv_perm, prefetch);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Kernels one call of launch() makes for these sizes on the current device
+// (T > 0): 1 when the one-launch form applies, else 2.  Host only.
+static int launches(long long T, int E, int k, bool has_prev, int num_sms) {
+  const long long nt = num_tiles(T);
+  if (!g_front_one_launch.load(std::memory_order_relaxed) || nt <= 0 || nt > (long long)kSegTiles * kSegSlots)
+    return 2;
+  const bool cos_smem = has_prev && E <= kSmemCoselMaxE;
+  const size_t smem = sizeof(int32_t) * (size_t)coop_smem_words(E, tile_tokens(T), k, cos_smem);
+  if (smem > (size_t)kScatterDynSmemMax) return 2;
+  int per_sm = 0;
+  cudaError_t e;
+  if (E <= 8) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, front_coop_kernel<1, true>, kThreads, smem);
+  else if (E <= 16) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, front_coop_kernel<2, true>, kThreads, smem);
+  else if (E <= 32) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, front_coop_kernel<4, true>, kThreads, smem);
+  else if (E <= 64) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, front_coop_kernel<8, true>, kThreads, smem);
+  else if (E <= 128)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, front_coop_kernel<16, true>, kThreads, smem);
+  else
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, front_coop_kernel<32, true>, kThreads, smem);
+  if (e != cudaSuccess) return 2;
+  return (long long)per_sm * num_sms >= nt + 1 ? 1 : 2;
 }
 
 }  // namespace front

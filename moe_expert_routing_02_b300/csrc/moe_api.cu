@@ -178,8 +178,8 @@ struct moe_stats {
   uint32_t* ring_c;                  // [L-1][s][E][E]
   unsigned long long* csum;          // [L-1][E][E]
   uint32_t* acc;                     // [E + E*E] (zero between calls)
-  uint32_t* seg;                     // [front::kSegments][E] (zero between calls)
-  uint32_t* ticket;                  // [1]
+  uint32_t* seg;                     // [front::kSegSlots][E] (zero between calls)
+  uint32_t* ticket;                  // [2]: the ticket, then the one-launch front's arrival count
   double* dscratch;                  // [E + E*E] decay-weighted sums (moe_predict_decay), not exported
   size_t state_bytes;                // exported bytes (rings + sums), without header
 };
@@ -245,9 +245,9 @@ moe_status moe_stats_create(moe_stats** out, int L, int E, int window, void* str
   const size_t nc = (size_t)(L - 1) * window * E * E;
   const size_t ncs = (size_t)(L - 1) * E * E;
   const size_t nacc = (size_t)E + (size_t)E * E;
-  const size_t nseg = (size_t)front::kSegments * E;
+  const size_t nseg = (size_t)front::kSegSlots * E;
   // layout: 8-byte sums first, then 4-byte arrays, then the fp64 scratch
-  const size_t four = ((nh + nc + nacc + nseg + 1) * 4 + 7) / 8 * 8;
+  const size_t four = ((nh + nc + nacc + nseg + 2) * 4 + 7) / 8 * 8;
   const size_t bytes = (nhs + ncs) * 8 + four + nacc * 8;
   cudaError_t e = cudaMalloc(&st->block, bytes);
   if (e != cudaSuccess) {
@@ -510,6 +510,7 @@ moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E,
   a.acc_c = st->acc + E;
   a.seg_tot = st->seg;
   a.ticket = st->ticket;
+  a.arrive = st->ticket + 1;
   a.ring_h = st->ring_h + ((size_t)layer * s + slot) * E;
   a.hsum = st->hsum + (size_t)layer * E;
   a.ring_c = layer > 0 ? st->ring_c + ((size_t)(layer - 1) * s + slot) * E * E : nullptr;
@@ -533,7 +534,9 @@ moe_status moe_layer_front(const float* logits, const uint16_t* x, int T, int E,
   a.counts = static_cast<int32_t*>(workspace);
   a.blk_tot = a.counts + a.ntiles * E;
   a.group_offsets = group_offsets;
-  return cuda_status(front::launch(a, x, H, xp, perm, inv_perm, static_cast<cudaStream_t>(stream)),
+  DeviceInfo* dinfo = nullptr;
+  if (moe_status ds = device_info(&dinfo); ds != MOE_OK) return ds;
+  return cuda_status(front::launch(a, x, H, xp, perm, inv_perm, dinfo->num_sms, static_cast<cudaStream_t>(stream)),
                      "moe_layer_front launch");
 }
 
@@ -1039,6 +1042,11 @@ moe_status moe_set_option(int option, int value) {
     g_opt_ffn_small_sms.store(value);
     return MOE_OK;
   }
+  if (option == MOE_OPT_FRONT_ONE_LAUNCH) {
+    if (value != 0 && value != 1) return fail(MOE_ERR_INVALID, "moe_set_option: one-launch front value must be 0 or 1");
+    front::g_front_one_launch.store(value);
+    return MOE_OK;
+  }
   return fail(MOE_ERR_INVALID, "moe_set_option: unknown option %d", option);
 }
 
@@ -1060,7 +1068,18 @@ moe_status moe_get_option(int option, int* value) {
     *value = g_opt_ffn_small_sms.load();
     return MOE_OK;
   }
+  if (option == MOE_OPT_FRONT_ONE_LAUNCH) {
+    *value = front::g_front_one_launch.load();
+    return MOE_OK;
+  }
   return fail(MOE_ERR_INVALID, "moe_get_option: unknown option %d", option);
+}
+
+int moe_layer_front_launches(int T, int E, int k, int has_prev) {
+  if (T <= 0 || E < 1 || E > 256 || k < 1 || k > 8 || k > E) return 0;
+  DeviceInfo* d = nullptr;
+  if (device_info(&d) != MOE_OK) return 0;
+  return front::launches(T, E, k, has_prev != 0, d->num_sms);
 }
 
 // ------------------------------------------------------------------ combine

@@ -20,10 +20,13 @@ from . import (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_EXPERT_FFN_COMBINE, MO
 __all__ = ["MoELayerStep", "MoESaved", "ChunkedLayerStep", "HostPipeline", "capture_slot_graphs"]
 
 
-def _front_launches(layer: int, predict: bool) -> int:
-    """Kernels moe_layer_front launches: route/count, then the statistics
-    block beside the plan, scatter and copy of every tile."""
-    return 2
+def _front_launches(T: int, E: int, k: int, layer: int) -> int:
+    """Kernels moe_layer_front launches on this device: one cooperative launch
+    (routing, a grid-wide barrier, then the dispatch) when all its blocks fit,
+    else route/count, then the statistics block beside the plan, scatter and
+    copy of every tile."""
+    from . import moe_layer_front_launches
+    return moe_layer_front_launches(T, E, k, layer > 0)
 
 
 class MoESaved:
@@ -255,7 +258,7 @@ class MoELayerStep:
         return dx, dl, (dw1, dw3, dw2)
 
     def launches(self, layer: int, L: int, predict: bool = True) -> int:
-        front = _front_launches(layer, predict)
+        front = _front_launches(self.T, self.E, self.k, layer)
         if self.physical:   # slot map + copy kernel per weight matrix, FFN over 2E-1 slots
             ffn = (moe_ffn_launches(self.A, 2 * self.E - 1, self.H, self.F, self.act, self.small, False)
                    + 2 * (3 if self.act == "swiglu" else 2))
@@ -385,7 +388,7 @@ class ChunkedLayerStep:
 
     def launches(self, layer: int, L: int, predict: bool = True) -> int:
         ffn = moe_ffn_launches(self.Tc * self.k, self.E, self.H, self.F, self.act, self.small, False)
-        return _front_launches(layer, predict) + self.chunks * (4 + ffn + 1)
+        return _front_launches(self.T, self.E, self.k, layer) + self.chunks * (4 + ffn + 1)
 
 
 class HostPipeline:

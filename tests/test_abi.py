@@ -146,6 +146,12 @@ def test_stats_and_replicate_reject_bad_arguments(L):
     assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 24) == M.MOE_OK
     assert L.moe_get_option(M.MOE_OPT_FFN_SMALL_SMS, ctypes.byref(v)) == M.MOE_OK and v.value == 24
     assert L.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 0) == M.MOE_OK
+    # the one-launch front: off by default, 0 or 1
+    assert L.moe_get_option(M.MOE_OPT_FRONT_ONE_LAUNCH, ctypes.byref(v)) == M.MOE_OK and v.value == 0
+    assert L.moe_set_option(M.MOE_OPT_FRONT_ONE_LAUNCH, 2) == inv
+    assert L.moe_set_option(M.MOE_OPT_FRONT_ONE_LAUNCH, 1) == M.MOE_OK
+    assert L.moe_get_option(M.MOE_OPT_FRONT_ONE_LAUNCH, ctypes.byref(v)) == M.MOE_OK and v.value == 1
+    assert L.moe_set_option(M.MOE_OPT_FRONT_ONE_LAUNCH, 0) == M.MOE_OK
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

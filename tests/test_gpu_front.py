@@ -251,3 +251,33 @@ def test_front_many_tiles(T, E, k, H):
         assert np.array_equal(b["inv_perm"].cpu().numpy(), inv)
         prev_a, prev_b = a["idx"], b["idx"]
     assert st_a.export_state() == st_b.export_state()
+
+
+@pytest.mark.parametrize("name", [c.name for c in W.CONFIGS])
+def test_front_one_launch_matches_two_launches(name):
+    """The one-launch front (cooperative, grid-wide barrier) against the two
+    launches: every output and the window state bit-identical, over iterations
+    that wrap the window ring, with replicas and the prediction on."""
+    c = W.config_by_name(name)
+    L = min(c.L, 3)
+    st = {f: M.MoEStats(c.L, c.E, c.window) for f in (0, 1)}
+    keys = ["idx", "w", "hist", "p_seq", "cond", "p_next", "copies", "rep_base", "group_expert",
+            "group_offsets", "perm", "inv_perm", "xp"]
+    try:
+        for it in range(c.window + 2):
+            lgs = W.make_layer_logits(c, it, layers=L)
+            prev = {0: None, 1: None}
+            for j in range(L):
+                lg = torch.from_numpy(lgs[j]).cuda()
+                x = W.make_x(c, it, j, device="cuda") if j == 0 or c.H <= 1024 else None
+                out = {}
+                for f in (0, 1):
+                    M.moe_set_option(M.MOE_OPT_FRONT_ONE_LAUNCH, f)
+                    out[f] = M.moe_layer_front(lg, x, st[f], it, j, c.k, idx_prev=prev[f], predict=True,
+                                               replicate=True)
+                    M.moe_check()
+                    prev[f] = out[f]["idx"]
+                _compare(out[0], out[1], keys)
+    finally:
+        M.moe_set_option(M.MOE_OPT_FRONT_ONE_LAUNCH, 0)
+    assert st[0].export_state() == st[1].export_state()

@@ -54,8 +54,17 @@ def _expected_table(load, total, c, E):
     return copies, rb, ge
 
 
+@pytest.fixture(params=[1, 0], ids=["one_launch", "two_launches"])
+def front_form(request):
+    """Both forms of the front: one cooperative launch (where all its blocks
+    fit on the device) and the two launches (the default)."""
+    M.moe_set_option(M.MOE_OPT_FRONT_ONE_LAUNCH, request.param)
+    yield request.param
+    M.moe_set_option(M.MOE_OPT_FRONT_ONE_LAUNCH, 0)
+
+
 @pytest.mark.parametrize("seed", range(40))
-def test_front_random_shapes_against_oracle(seed):
+def test_front_random_shapes_against_oracle(seed, front_form):
     rng, c = _case(seed)
     E, k, T, H, s = c["E"], c["k"], c["T"], c["H"], c["s"]
     L = 2

@@ -127,3 +127,31 @@ def test_chunked_step_launch_count():
     M.moe_check()
     want = sum(step.launches(j, c.L) for j in range(c.L))
     assert got == want, (want, names)
+
+
+@pytest.mark.parametrize("T", [2048, 16384, 200000])
+def test_front_launch_count_one_launch_option(T):
+    """With MOE_OPT_FRONT_ONE_LAUNCH on, the front is one kernel where all its
+    blocks fit on the device (two past that); the count the layer step reports
+    follows the library's own answer, checked against the profiler."""
+    c = dataclasses.replace(W.config_by_name("moe_gpt_stream"), T=T, L=2, H=64, F=128)
+    M.moe_set_option(M.MOE_OPT_FRONT_ONE_LAUNCH, 1)
+    try:
+        st = M.MoEStats(c.L, c.E, c.window)
+        step = MoELayerStep(c.T, c.E, c.k, c.H, c.F, c.act, st)
+        lgs, xs, ws, outs = _layer_inputs(c)
+
+        def body():
+            for j in range(c.L):
+                step.run(0, j, lgs[j], xs[j], ws[j], outs[j])
+
+        body()
+        torch.cuda.synchronize()
+        M.moe_check()
+        got, names = _count_kernels(body)
+        M.moe_check()
+        want = sum(step.launches(j, c.L) for j in range(c.L))
+        assert got == want, (want, names)
+        assert M.moe_layer_front_launches(T, c.E, c.k) == (1 if T <= 16384 else 2)
+    finally:
+        M.moe_set_option(M.MOE_OPT_FRONT_ONE_LAUNCH, 0)
