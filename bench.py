@@ -899,6 +899,7 @@ def run_crossover(args):
     peaks = load_peaks()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     flush = L2Flush(dev)
     g = torch.Generator(device=dev)
     g.manual_seed(7)
@@ -919,6 +920,9 @@ def run_crossover(args):
                                  dtype=torch.uint8, device=dev)
                 row = {"M": m}
                 for name, thr in (("grouped", 0), ("small_batch", 1 << 30)):
+                    # the small-batch arm gives the small-batch kernels every SM (the
+                    # library's default leaves that path off)
+                    M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, nsm if name == "small_batch" else 0)
                     fn = lambda: M.moe_expert_ffn(xp, go, None, None, w1, w3, w2, "swiglu", thr, y=y, workspace=ws)
                     for _ in range(3):
                         fn()
@@ -933,6 +937,7 @@ def run_crossover(args):
                         e1.synchronize()
                         ts.append(e0.elapsed_time(e1) * 1e3)
                     M.moe_check()
+                    M.moe_set_option(M.MOE_OPT_FFN_SMALL_SMS, 0)
                     ts.sort()
                     row[name + "_us"] = round(ts[len(ts) // 2], 1)
                 flops = 6 * A * H * F
