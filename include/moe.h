@@ -565,7 +565,10 @@ moe_status moe_dispatch_noalloc(const uint16_t* x, const int32_t* idx, int T, in
  *     previous kernel in their stream (CUDA programmatic dependent launch):
  *     the hardware may start one once every block of the kernel before it
  *     has exited, and each waits for that kernel's completion (griddepcontrol
- *     .wait) before touching memory; no kernel releases its dependents early.
+ *     .wait) before touching memory.  Only the front's route kernel releases
+ *     its dependent early (for rows of at most 64 KB per dispatch tile: the
+ *     scatter/copy blocks start while it runs and prefetch their token rows
+ *     into L2, reading nothing the route kernel writes before their own wait).
  *     0: ordinary launches.  Results are identical either way.
  *   MOE_OPT_FFN_SMALL_SMS  how the SMs are shared between the small-batch
  *     kernels and the grouped kernels of an expert-FFN call whose

@@ -23,10 +23,12 @@ __device__ __forceinline__ void moe_flag_error(unsigned int bits) { atomicOr(&g_
 // has exited, before that kernel's completion is processed; it calls
 // pdl_wait() before its first access to memory that earlier work writes or
 // reads, which waits for that completion and its memory operations.  Without
-// a programmatic predecessor pdl_wait() returns at once.  No kernel here
-// releases its dependents early (measured: blocks of the next kernel parked
-// beside the running one cost more than the launch latency they hide), so a
-// dependent never shares the GPU with its predecessor's blocks.
+// a programmatic predecessor pdl_wait() returns at once.  One kernel releases
+// its dependent early: the front's route kernel, for short token rows, lets
+// the scatter/copy blocks start and ask L2 for their rows while it routes
+// (parked blocks with nothing to do measured slower than the launch latency
+// they hide); every other dependent starts only after its predecessor's
+// blocks have exited, so it never shares the GPU with them.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // host option (moe_set_option(MOE_OPT_PDL, ...)); read once per launch
