@@ -635,8 +635,9 @@ int moe_ffn_launches(int A, int E, int H, int F, int act, int small_group_thresh
  * current device under the current options: 1 when it runs as one
  * cooperative launch (MOE_OPT_FRONT_ONE_LAUNCH on, and all of its blocks can
  * be resident at once), else 2.  has_prev: the call passes the previous
- * layer's choices (co-selection counts kept).  0 for refused sizes or when no
- * device can be queried.  Host only (queries the device's occupancy). */
+ * layer's choices (co-selection counts kept).  0 for T <= 0 (an empty batch
+ * runs the separate calls instead), for sizes moe_layer_front refuses, or
+ * when no device can be queried.  Host only (queries the device's occupancy). */
 int moe_layer_front_launches(int T, int E, int k, int has_prev);
 
 /* Workspace bytes for op (MOE_OP_DISPATCH, MOE_OP_EXPERT_FFN, MOE_OP_LAYER_FRONT or
