@@ -333,3 +333,15 @@ def test_every_entry_point_names_its_passage():
         decls = re.findall(r"\b(moe_\w+)\s*\(", re.sub(r"/\*.*?\*/", "", block, flags=re.S))
         if decls:
             assert any(m in block for m in marks), decls
+
+
+def test_front_launch_count_refusals(L):
+    """moe_layer_front_launches answers 0 for an empty batch and for sizes the
+    front refuses, before it queries any device."""
+    f = L.moe_layer_front_launches
+    assert f(0, 16, 2, 1) == 0          # empty batch: the separate calls run instead
+    assert f(-1, 16, 2, 1) == 0
+    assert f(1024, 0, 2, 1) == 0        # E out of range
+    assert f(1024, 257, 2, 1) == 0
+    assert f(1024, 16, 0, 1) == 0       # k out of range
+    assert f(1024, 4, 8, 1) == 0        # k > E
