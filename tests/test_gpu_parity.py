@@ -177,6 +177,50 @@ def test_stats_checkpoint_resume():
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("E,k", [(1, 1), (2, 1), (2, 2), (5, 2), (8, 1), (8, 2), (13, 2), (16, 1), (16, 2),
+                                 (16, 3), (16, 4)])
+def test_stats_small_e_coselection_shapes(E, k):
+    """Up to 16 experts (the register-histogram kernel; for k <= 2 its
+    co-selection counts come from bf16 MMAs over one-hot choice counts):
+    ragged token counts that leave partial warps and blocks, repeated experts
+    within a token's choices (each pair counts), k = 1, out-of-range ids
+    (flagged; only their own pairs are dropped).  Ring slots and window sums
+    against the oracle, bit for bit."""
+    rng = np.random.default_rng([5, E, k])
+    for T in (1, 31, 33, 1000, 4097, 100003):
+        st = M.MoEStats(2, E, 3)
+        prev = rng.integers(0, E, (T, k)).astype(np.int32)
+        cur = rng.integers(0, E, (T, k)).astype(np.int32)
+        M.moe_stats_update(st, 0, 0, dev(prev))
+        M.moe_stats_update(st, 0, 1, dev(cur), dev(prev))
+        ok_check()
+        ring_h, hsum, ring_c, csum = st.state_arrays()
+        assert np.array_equal(ring_h[0, 0].astype(np.int64), O.histogram(prev, E)), T
+        assert np.array_equal(ring_h[1, 0].astype(np.int64), O.histogram(cur, E)), T
+        assert np.array_equal(ring_c[0, 0].astype(np.int64), O.coselection(prev, cur, E)), T
+        assert np.array_equal(csum[0].astype(np.int64), O.coselection(prev, cur, E)), T
+    # an out-of-range id in either layer: flagged, and only its own pairs are left out
+    st = M.MoEStats(2, E, 3)
+    prev = rng.integers(0, E, (300, k)).astype(np.int32)
+    cur = rng.integers(0, E, (300, k)).astype(np.int32)
+    prev[7, 0] = E + 3
+    cur[11, k - 1] = -1
+    M.moe_stats_update(st, 1, 1, dev(cur), dev(prev))
+    with pytest.raises(M.MoEError):
+        M.moe_check()
+    M.moe_check()
+    keep_p = (prev >= 0) & (prev < E)
+    keep_c = (cur >= 0) & (cur < E)
+    want = np.zeros((E, E), np.int64)
+    for t in range(300):
+        for r1 in range(k):
+            for r2 in range(k):
+                if keep_p[t, r1] and keep_c[t, r2]:
+                    want[prev[t, r1], cur[t, r2]] += 1
+    _, _, ring_c, _ = st.state_arrays()
+    assert np.array_equal(ring_c[0, 1].astype(np.int64), want)
+
+
 def test_stats_empty_batch_and_invalid_ids():
     st = M.MoEStats(2, 8, 4)
     e = torch.empty((0, 2), dtype=torch.int32, device="cuda")
