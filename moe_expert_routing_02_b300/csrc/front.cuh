@@ -248,34 +248,43 @@ __host__ __device__ inline int scatter_smem_words(int E, int TT, int k) {
 // bytes (measured: on 160 KB tiles of 10 KB rows the prefetch slowed the copy).
 constexpr long long kPrefetchMaxBytes = 64 * 1024;
 
-// The row copy of a tile: one warp per two assignments (8
-// loads of 16 bytes in flight per lane), 16-byte chunks.
+// The row copy of a tile, by token: one warp per two tokens (8 loads of 16
+// bytes in flight per lane), each token row read once and stored to the
+// slots of all k of its assignments (16-byte chunks).
 __device__ __forceinline__ void copy_rows(const uint16_t* __restrict__ x, int H, uint16_t* __restrict__ xp, int k,
                                           long long f0, int nA, const int32_t* slot_s) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int chunks = H / 8;
-  for (int i = 2 * wid; i < nA; i += 2 * kWarps) {
-    const int s0 = slot_s[i], s1 = i + 1 < nA ? slot_s[i + 1] : -1;
-    const uint16_t* src0 = x + ((f0 + i) / k) * H;
-    const uint16_t* src1 = x + ((f0 + i + 1) / k) * H;
-    uint16_t* dst0 = xp + (size_t)(s0 < 0 ? 0 : s0) * H;
-    uint16_t* dst1 = xp + (size_t)(s1 < 0 ? 0 : s1) * H;
+  const long long t0 = f0 / k;
+  const int nt = nA / k;
+  for (int tt = 2 * wid; tt < nt; tt += 2 * kWarps) {
+    const bool has1 = tt + 1 < nt;
+    const uint16_t* src0 = x + (t0 + tt) * H;
+    const uint16_t* src1 = src0 + H;
     for (int c = lane; c < chunks; c += 128) {
       uint4 v0[4], v1[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int cu = c + 32 * u;
         if (cu < chunks) {
-          if (s0 >= 0) v0[u] = ld_nc_v4(src0 + (size_t)cu * 8);
-          if (s1 >= 0) v1[u] = ld_nc_v4(src1 + (size_t)cu * 8);
+          v0[u] = ld_nc_v4(src0 + (size_t)cu * 8);
+          if (has1) v1[u] = ld_nc_v4(src1 + (size_t)cu * 8);
         }
       }
+      for (int r = 0; r < k; ++r) {
+        const int s0 = slot_s[tt * k + r];
+        if (s0 >= 0) {
+          uint16_t* dst = xp + (size_t)s0 * H;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int cu = c + 32 * u;
-        if (cu < chunks) {
-          if (s0 >= 0) st_v4(dst0 + (size_t)cu * 8, v0[u]);
-          if (s1 >= 0) st_v4(dst1 + (size_t)cu * 8, v1[u]);
+          for (int u = 0; u < 4; ++u)
+            if (c + 32 * u < chunks) st_v4(dst + (size_t)(c + 32 * u) * 8, v0[u]);
+        }
+        const int s1 = has1 ? slot_s[(tt + 1) * k + r] : -1;
+        if (s1 >= 0) {
+          uint16_t* dst = xp + (size_t)s1 * H;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (c + 32 * u < chunks) st_v4(dst + (size_t)(c + 32 * u) * 8, v1[u]);
         }
       }
     }
