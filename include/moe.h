@@ -238,7 +238,8 @@ moe_status moe_replicate_predicted(const float* p_next, int E, int64_t total, in
  *   group_offsets  [2E+1] int32 out: row offset of each group in xp;
  *                  entries past the last group equal A
  *   perm           [A] int32 out: slot -> assignment f
- *   inv_perm       [A] int32 out: assignment f -> slot
+ *   inv_perm       [A] int32 out: assignment f -> slot (-1 for an assignment
+ *                  whose expert is out of range; the call flags that)
  *   xp             [A,H] bf16 out: xp[slot] = x[perm[slot] / k] (bit copy)
  *   workspace      ws_bytes >= moe_workspace_bytes(MOE_OP_DISPATCH, T, k, E, H, 0),
  *                  16-byte aligned

@@ -167,7 +167,11 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
       if ((unsigned long long)slot < (unsigned long long)A) {
         perm[slot] = (int32_t)f;
         inv_perm[f] = slot;
+      } else {
+        inv_perm[f] = -1;
       }
+    } else if (f < A) {
+      inv_perm[f] = -1;  // expert out of range (flagged by count_kernel): no slot
     }
     __syncthreads();
     for (int i = tid; i < E; i += kThreads) {
@@ -182,31 +186,48 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const int32_t* __rest
   }
 }
 
-// xp[slot, :] = x[perm[slot] / k, :], one warp per row, 16-byte vectors.
+// xp[inv_perm[t k + r], :] = x[t, :] for every assignment with a slot: two tokens per
+// warp, each token row read once, 16-byte vectors.
 __global__ void __launch_bounds__(kThreads) gather_kernel(const uint16_t* __restrict__ x,
-                                                          const int32_t* __restrict__ perm, long long A, int k,
+                                                          const int32_t* __restrict__ inv_perm, long long T, int k,
                                                           int H, uint16_t* __restrict__ xp) {
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * kWarps;
+  const long long A = T * k;
   const int chunks = H / 8;
-  for (long long row = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5; row < A; row += warps) {
-    const int32_t p = perm[row];
-    if ((unsigned long long)p >= (unsigned long long)A) continue;  // hole left by invalid routing
-    const long long t = p / k;
-    const uint16_t* src = x + t * H;
-    uint16_t* dst = xp + row * H;
-    int c = lane;
-    for (; c + 96 < chunks; c += 128) {
-      const uint4 v0 = ld_nc_v4(src + (size_t)c * 8);
-      const uint4 v1 = ld_nc_v4(src + (size_t)(c + 32) * 8);
-      const uint4 v2 = ld_nc_v4(src + (size_t)(c + 64) * 8);
-      const uint4 v3 = ld_nc_v4(src + (size_t)(c + 96) * 8);
-      st_v4(dst + (size_t)c * 8, v0);
-      st_v4(dst + (size_t)(c + 32) * 8, v1);
-      st_v4(dst + (size_t)(c + 64) * 8, v2);
-      st_v4(dst + (size_t)(c + 96) * 8, v3);
+  // two tokens per warp (eight 16-byte loads in flight per lane); each token
+  // row is read once and stored to the slots of all k of its assignments
+  for (long long t = (((long long)blockIdx.x * kThreads + threadIdx.x) >> 5) * 2; t < T; t += 2 * warps) {
+    const bool has1 = t + 1 < T;
+    const uint16_t* src0 = x + t * H;
+    const uint16_t* src1 = src0 + H;
+    for (int c = lane; c < chunks; c += 128) {
+      uint4 v0[4], v1[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int cu = c + 32 * u;
+        if (cu < chunks) {
+          v0[u] = ld_nc_v4(src0 + (size_t)cu * 8);
+          if (has1) v1[u] = ld_nc_v4(src1 + (size_t)cu * 8);
+        }
+      }
+      for (int r = 0; r < k; ++r) {
+        const int32_t s0 = inv_perm[t * k + r];
+        if ((unsigned long long)s0 < (unsigned long long)A) {  // -1: no slot (invalid routing)
+          uint16_t* dst = xp + (size_t)s0 * H;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (c + 32 * u < chunks) st_v4(dst + (size_t)(c + 32 * u) * 8, v0[u]);
+        }
+        const int32_t s1 = has1 ? inv_perm[(t + 1) * k + r] : -1;
+        if ((unsigned long long)s1 < (unsigned long long)A) {
+          uint16_t* dst = xp + (size_t)s1 * H;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (c + 32 * u < chunks) st_v4(dst + (size_t)(c + 32 * u) * 8, v1[u]);
+        }
+      }
     }
-    for (; c < chunks; c += 32) st_v4(dst + (size_t)c * 8, ld_nc_v4(src + (size_t)c * 8));
   }
 }
 
@@ -238,10 +259,10 @@ static cudaError_t launch(const Args& a, int num_sms, cudaStream_t st) {
   scatter_kernel<<<(unsigned)nt, kThreads, sizeof(int32_t) * (kWarps + 1) * E, st>>>(a.idx, A, E, counts, info,
                                                                                       a.perm, a.inv_perm);
   if (a.x != nullptr) {
-    long long blocks = (A + kWarps - 1) / kWarps;
+    long long blocks = (a.T + 2 * kWarps - 1) / (2 * kWarps);
     const long long cap = (long long)num_sms * 16;
     if (blocks > cap) blocks = cap;
-    gather_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(a.x, a.perm, A, a.k, a.H, a.xp);
+    gather_kernel<<<(unsigned)blocks, kThreads, 0, st>>>(a.x, a.inv_perm, a.T, a.k, a.H, a.xp);
   }
   return cudaGetLastError();
 }

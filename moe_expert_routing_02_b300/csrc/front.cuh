@@ -622,7 +622,10 @@ __device__ __forceinline__ void scatter_body(const Args& a, const uint16_t* __re
         inv_perm[f0 + i] = slot;
       } else {
         slot = -1;
+        inv_perm[f0 + i] = -1;
       }
+    } else if (i < nA) {
+      inv_perm[f0 + i] = -1;  // expert out of range (flagged): no slot
     }
     if (i < nA) slot_s[i] = slot;
     __syncthreads();

@@ -319,6 +319,33 @@ def test_dispatch_edges():
     ok_check()
 
 
+def test_dispatch_invalid_expert_has_no_slot():
+    """An assignment whose expert is out of range is flagged and gets no slot
+    (inv_perm -1); every other assignment's slot holds its token's row, and
+    perm inverts inv_perm on them."""
+    rng = np.random.default_rng(13)
+    T, k, E, H = 700, 2, 6, 64
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    bad = [(5, 0), (333, 1), (699, 1)]
+    for t, r in bad:
+        idx[t, r] = E + 2 if r == 0 else -3
+    x = torch.randn((T, H), device="cuda").to(torch.bfloat16)
+    go, perm, inv, xp = M.moe_dispatch(x, dev(idx), E)
+    with pytest.raises(M.MoEError):
+        M.moe_check()
+    M.moe_check()
+    inv_h, perm_h = host(inv), host(perm)
+    xh, xph = x.cpu(), xp.cpu()
+    for f in range(T * k):
+        t, r = divmod(f, k)
+        if (t, r) in bad:
+            assert inv_h[f] == -1, f
+        else:
+            s_ = int(inv_h[f])
+            assert 0 <= s_ < T * k and perm_h[s_] == f, f
+            assert torch.equal(xph[s_], xh[t]), f
+
+
 # ----------------------------------------------------------------------------
 # K6 expert FFN
 # ----------------------------------------------------------------------------
